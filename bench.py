@@ -1,0 +1,489 @@
+#!/usr/bin/env python
+"""Benchmark of the triangle-attention forward on GB300: one JSON line.
+
+A step is one forward pass of the whole path (mask resolution, tile loads,
+QK^T, online softmax with -1e9 masking, PV, epilogue with lse/max) over one
+batch of the workload.  The default workload is "bf16_long"
+(B=1,N=768,H=4,Q=K=768,D=64 bf16, bias bf16, kv_lengths uniform in [0,768]
+with all-masked rows); its q/k/v/O (1.2 GB) exceed the 129 MB L2, so no L2
+flush is needed between steps.  The other workloads are reported under
+"per_config" with an L2 flush before every timed launch.
+
+Metric: effective TFLOP/s = 4*B*N*H*Q*D*sum(K_valid) / time (varlen: 4*H*D
+* valid (q,k) pairs / time).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N>1) every rank runs the full workload (weak scaling, no
+data-path collective); rank 0 prints the line with the max time over ranks.
+--impl reference times the fp64 CPU oracle on a bounded sample of the
+workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "fwd effective TFLOP/s and % of GB300 dense-bf16 peak, per config, 1 GPU"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 1024 * 1024
+ESIZE = {"f32": 4, "f16": 2, "bf16": 2}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------------------
+# Work accounting (effective FLOPs and algorithmic bytes)
+# ---------------------------------------------------------------------------
+
+def kv_valid(c) -> torch.Tensor:
+    """Per (b,n) count of valid keys: clamp(kv_len,0,K), popcount of the mask, or K."""
+    if c.kv_lengths is not None:
+        return c.kv_lengths.clamp(0, c.K).to(torch.int64)
+    if c.mask is not None:
+        return (c.mask.reshape(c.B, c.N, c.K) != 0).sum(-1).to(torch.int64)
+    return torch.full((c.B, c.N), c.K, dtype=torch.int64)
+
+
+def triangle_work(c, slabs=None):
+    """(effective flops, algorithmic bytes) of the triangle workload, or of the (b,n) slabs listed."""
+    kv = kv_valid(c).reshape(-1)
+    if slabs is not None:
+        kv = kv[torch.as_tensor(slabs)]
+    nslab = kv.numel()
+    e, eb = ESIZE[c.dtype], ESIZE[c.bias_dtype]
+    flops = 4.0 * c.H * c.Q * c.D * float(kv.sum())
+    byts = 2.0 * nslab * c.H * c.Q * c.D * e                      # Q and O
+    byts += 2.0 * c.H * c.D * e * float(kv.sum())                 # K and V of valid keys
+    byts += float((kv == 0).sum()) * c.H * c.K * c.D * e          # V of all-masked slabs (mean of V)
+    byts += c.B * c.H * c.Q * c.K * eb                            # bias, once
+    byts += (nslab * c.K) if c.mask is not None else (4 * nslab if c.kv_lengths is not None else 0)
+    byts += 8.0 * nslab * c.H * c.Q                               # lse and max
+    return flops, byts
+
+
+def varlen_work(c):
+    L = c.lengths.to(torch.int64)
+    pairs = float((L * (L + 1) // 2).sum()) if c.mask_mod == "causal" else float((L * L).sum())
+    e = ESIZE[c.dtype]
+    total = float(L.sum())
+    flops = 4.0 * c.H * c.D * pairs
+    byts = 4.0 * total * c.H * c.D * e + 8.0 * c.H * total        # Q, K, V, O once; lse, max
+    return flops, byts
+
+
+# ---------------------------------------------------------------------------
+# Clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.idx), "-lms", "50"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.15)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r.split(",") for r in out.strip().splitlines() if r.count(",") >= 8]
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------
+
+def gpu_triangle_inputs(c, dev):
+    g = lambda t: None if t is None else t.to(dev)  # noqa: E731
+    return dict(q=g(c.q), k=g(c.k), v=g(c.v), bias=g(c.bias), mask=g(c.mask), kv_lengths=g(c.kv_lengths))
+
+
+def make_l2_flusher(dev):
+    buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def flush():
+        buf.fill_(1.0)
+    return flush
+
+
+def time_triangle(ta, c, dev, steps, warmup, flush=None):
+    """Device time (ms) per launch over `steps` launches, CUDA events on the launching stream."""
+    x = gpu_triangle_inputs(c, dev)
+    out = torch.empty_like(x["q"])
+    lse = torch.empty(c.B, c.N, c.H, c.Q, 1, device=dev, dtype=torch.float32)
+    mx = torch.empty_like(lse)
+
+    # The C-ABI call with the pointers resolved once, so host overhead per launch stays small.
+    from masked_attention_tri_gb300 import abi
+    from masked_attention_tri_gb300.api import _DT, _ptr
+    argv = (_ptr(x["q"]), _ptr(x["k"]), _ptr(x["v"]), _DT[x["q"].dtype], _ptr(x["bias"]), _DT[x["bias"].dtype],
+            _ptr(None if x["mask"] is None else x["mask"].view(torch.uint8)), _ptr(x["kv_lengths"]),
+            c.B, c.N, c.H, c.Q, c.K, c.D, c.scale, _ptr(out), _ptr(lse), _ptr(mx),
+            torch.cuda.current_stream(dev).cuda_stream)
+
+    def launch():
+        abi.tri_attn_fwd(*argv)
+
+    for _ in range(warmup):
+        launch()
+    torch.cuda.synchronize(dev)
+    stream = torch.cuda.current_stream(dev)
+    if flush is None:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            launch()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / steps
+    tot = 0.0
+    for _ in range(steps):
+        flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        launch()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        tot += e0.elapsed_time(e1)
+    return tot / steps
+
+
+def time_varlen(ta, c, dev, steps, warmup, flush):
+    q, k, v = c.q.to(dev), c.k.to(dev), c.v.to(dev)
+    cu = c.cu_seqlens.to(dev)
+    bm = ta.BlockMask.from_kv_blocks(c.kv_num_blocks.to(dev), c.kv_indices.to(dev), c.full_kv_num_blocks.to(dev),
+                                     c.full_kv_indices.to(dev), BLOCK_SIZE=c.block, mask_mod=c.mask_mod)
+    out = torch.empty_like(q)
+
+    def launch():
+        ta.varlen_attention(q, k, v, cu, cu, c.max_seqlen, c.max_seqlen, block_mask=bm, scale=c.scale, out=out,
+                            return_aux=True)
+
+    for _ in range(warmup):
+        launch()
+    torch.cuda.synchronize(dev)
+    stream = torch.cuda.current_stream(dev)
+    tot = 0.0
+    for _ in range(steps):
+        flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        launch()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        tot += e0.elapsed_time(e1)
+    return tot / steps
+
+
+def e2e_triangle(ta, c, dev, steps, warmup):
+    """Same metric through the public API with pinned host buffers; copies inside the timed region."""
+    hq, hk, hv, hb = (t.pin_memory() for t in (c.q, c.k, c.v, c.bias))
+    hkl = c.kv_lengths.pin_memory() if c.kv_lengths is not None else None
+    hm = c.mask.pin_memory() if c.mask is not None else None
+    dq, dk, dv, db = (torch.empty_like(t, device=dev) for t in (hq, hk, hv, hb))
+    dkl = torch.empty_like(hkl, device=dev) if hkl is not None else None
+    dm = torch.empty_like(hm, device=dev) if hm is not None else None
+    dout = torch.empty_like(dq)
+    ho = torch.empty_like(hq).pin_memory()
+    hl = torch.empty(c.B, c.N, c.H, c.Q, 1, dtype=torch.float32).pin_memory()
+    hmx = torch.empty_like(hl).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hb) + ((hkl,) if hkl is not None else ())
+              + ((hm,) if hm is not None else ()))
+    d2h = ho.numel() * ho.element_size() + 2 * hl.numel() * 4
+
+    def step():
+        for d, h in ((dq, hq), (dk, hk), (dv, hv), (db, hb)):
+            d.copy_(h, non_blocking=True)
+        if dkl is not None:
+            dkl.copy_(hkl, non_blocking=True)
+        if dm is not None:
+            dm.copy_(hm, non_blocking=True)
+        o, lse, mx = ta.triangle_attention(dq, dk, dv, db, mask=dm, scale=c.scale, return_aux=True, kv_lengths=dkl,
+                                           out=dout)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+        hmx.copy_(mx, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    stream = torch.cuda.current_stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) / steps, h2d, d2h
+
+
+def cpu_oracle_sample(c, budget_s: float, max_slabs=None):
+    """Time the oracle (as it stands) on whole (b,n) slabs of the workload; returns
+    (effective TFLOP/s, seconds, slabs, threads)."""
+    import numpy as np
+    import oracle
+    threads = oracle.default_threads()
+    nslab_total = c.B * c.N
+    per = c.H * c.Q
+
+    def rows_of(slabs):
+        return np.concatenate([np.arange(s * per, (s + 1) * per, dtype=np.int64) for s in slabs])
+
+    # calibrate on one slab that is not all-masked
+    kv = kv_valid(c).reshape(-1)
+    order = [int(i) for i in torch.argsort(kv, descending=True)[: max(1, nslab_total)]]
+    probe = [order[len(order) // 2]]
+    t0 = time.perf_counter()
+    oracle.tri_fwd(c.q, c.k, c.v, c.bias, mask=c.mask, kv_lengths=c.kv_lengths, scale=c.scale, rows=rows_of(probe),
+                   threads=threads)
+    t1 = time.perf_counter() - t0
+    n = max(1, min(nslab_total, int(budget_s / max(t1, 1e-6))))
+    if max_slabs:
+        n = min(n, max_slabs)
+    slabs = [int(s) for s in np.linspace(0, nslab_total - 1, n).round().astype(int)]
+    slabs = sorted(set(slabs))
+    t0 = time.perf_counter()
+    oracle.tri_fwd(c.q, c.k, c.v, c.bias, mask=c.mask, kv_lengths=c.kv_lengths, scale=c.scale, rows=rows_of(slabs),
+                   threads=threads)
+    dt = time.perf_counter() - t0
+    flops, _ = triangle_work(c, slabs)
+    return flops / dt / 1e12, dt, slabs, threads
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, dev) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=dev if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(args, world, rank):
+    """The oracle arm: the fp64 CPU oracle, as it stands, on bounded samples of the workload."""
+    if rank != 0:
+        return
+    c = synth.TRIANGLE_WORKLOADS[args.workload]()
+    budget = max(1.0, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    vals = []
+    times = []
+    info = None
+    for i in range(args.warmup + args.steps):
+        v, dt, slabs, threads = cpu_oracle_sample(c, budget)
+        if i >= args.warmup:
+            vals.append(v)
+            times.append(dt)
+            info = (slabs, threads)
+    slabs, threads = info
+    value = statistics.mean(vals)
+    flops, _ = triangle_work(c, slabs)
+    sample = f"{len(slabs)} of {c.B * c.N} (b,n) slabs of {args.workload} (all H*Q rows each), {flops:.3e} effective FLOP"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(c),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(c):
+    desc = {
+        "bf16_long": "bf16 long: B=1,N=768,H=4,Q=K=768,D=64; q,k,v,bias ~N(0,1) bf16; kv_lengths U[0,768] incl. 0",
+        "bf16_pairstack": "bf16 pair-stack: B=1,N=384,H=4,Q=K=384,D=32; bias ~N(0,4) bf16; kv_lengths U[192,384]",
+        "fp16_kvlen": "fp16: B=1,N=128,H=2,Q=K=128,D=32; bias fp32; kv_lengths=96",
+        "fp16_dense": "fp16: B=1,N=128,H=2,Q=K=128,D=32; bias fp32; dense Bernoulli(0.5) key mask",
+        "tiny_fp32": "tiny fp32: B=1,N=32,H=2,Q=K=32,D=32; no mask",
+    }.get(c.name, c.name)
+    return {"workload": desc, "B": c.B, "N": c.N, "H": c.H, "Q": c.Q, "K": c.K, "D": c.D,
+            "qkv_dtype": c.dtype, "bias_dtype": c.bias_dtype,
+            "mask": "kv_lengths" if c.kv_lengths is not None else ("dense" if c.mask is not None else "none")}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="bf16_long", choices=sorted(synth.TRIANGLE_WORKLOADS))
+    ap.add_argument("--no-per-config", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+
+    import masked_attention_tri_gb300 as ta
+    from masked_attention_tri_gb300 import build
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    build.build()
+    peaks, peak_kind = load_peaks()
+    c = synth.TRIANGLE_WORKLOADS[args.workload]()
+    flops, byts = triangle_work(c)
+
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else
+                           int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
+    sampler.start()
+    ms = time_triangle(ta, c, dev, args.steps, args.warmup)
+    clocks = sampler.stop()
+    status = ta.get_status()
+    barrier(world)
+    ms_max = max_over_ranks(ms, world, dev)
+    assert status == 0, f"device status {status}"
+
+    value = world * flops / (ms_max * 1e-3) / 1e12
+    t_mma = flops / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = byts / (peaks["hbm_gbs"] * 1e9)
+    bound = "hbm" if t_hbm >= t_mma else "tensor"
+    if bound == "hbm":
+        achieved = byts / (ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": None}
+    else:
+        achieved = flops / (ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"], "traffic": None}
+    roof["peak_source"] = f"{peak_kind} (MEASURED_PEAKS.json burst)" if peak_kind == "measured" else "fallback"
+    roof["algorithmic_bytes"] = byts
+    roof["effective_flops"] = flops
+    roof["two_term_roofline_frac"] = max(t_mma, t_hbm) / (ms * 1e-3)
+
+    e2e_ms, h2d, d2h = e2e_triangle(ta, c, dev, max(3, min(args.steps, 50)), 3)
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
+
+    per_config = {}
+    if not args.no_per_config and rank == 0:
+        flush = make_l2_flusher(dev)
+        for name in ("tiny_fp32", "fp16_kvlen", "fp16_dense", "bf16_pairstack"):
+            cc = synth.TRIANGLE_WORKLOADS[name]()
+            f, b = triangle_work(cc)
+            t = time_triangle(ta, cc, dev, 50, 5, flush=flush)
+            per_config[name] = {"us": 1e3 * t, "tflops": f / (t * 1e-3) / 1e12,
+                                "pct_bf16_peak": 100 * f / (t * 1e-3) / (peaks["bf16_tflops"] * 1e12),
+                                "two_term_roofline_frac": max(f / (peaks["bf16_tflops"] * 1e12),
+                                                              b / (peaks["hbm_gbs"] * 1e9)) / (t * 1e-3),
+                                "l2": "flushed before each launch"}
+        vc = synth.bf16_varlen()
+        f, b = varlen_work(vc)
+        t = time_varlen(ta, vc, dev, 50, 5, flush)
+        per_config["bf16_varlen"] = {"us": 1e3 * t, "tflops": f / (t * 1e-3) / 1e12,
+                                     "pct_bf16_peak": 100 * f / (t * 1e-3) / (peaks["bf16_tflops"] * 1e12),
+                                     "two_term_roofline_frac": max(f / (peaks["bf16_tflops"] * 1e12),
+                                                                   b / (peaks["hbm_gbs"] * 1e9)) / (t * 1e-3),
+                                     "lengths": vc.lengths.tolist(), "l2": "flushed before each launch"}
+        per_config["bf16_long"] = {"us": 1e3 * ms, "tflops": flops / (ms * 1e-3) / 1e12,
+                                   "pct_bf16_peak": 100 * flops / (ms * 1e-3) / (peaks["bf16_tflops"] * 1e12),
+                                   "two_term_roofline_frac": roof["two_term_roofline_frac"],
+                                   "l2": "inputs larger than L2"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, dt, slabs, threads = cpu_oracle_sample(c, args.cpu_budget)
+        fl, _ = triangle_work(c, slabs)
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": f"{len(slabs)} of {c.B * c.N} (b,n) slabs of {args.workload} (all H*Q rows each), "
+                         f"{fl:.3e} effective FLOP in {dt:.1f} s"}
+
+    if rank == 0:
+        cfg = workload_config(c)
+        cfg.update({"global_batch": c.B * world, "parallelism": f"replicas{world}" if world > 1 else "single",
+                    "l2": "inputs larger than L2 (q,k,v,O 1.2 GB vs 129 MB)" if args.workload == "bf16_long"
+                    else "not flushed"})
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": c.dtype, "data": "synthetic", "config": cfg,
+            "pct_bf16_peak": 100 * flops / (ms_max * 1e-3) / (peaks["bf16_tflops"] * 1e12),
+            "roofline": roof, "cpu_baseline": cpu,
+            "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": args.steps, "clocks": clocks, "per_config": per_config,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

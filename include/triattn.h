@@ -1,0 +1,163 @@
+/*
+ * triattn.h -- C ABI of the GB300 (sm_103a) triangle-attention forward.
+ *
+ * Operation (cuEquivariance "triangle_attention" API page, formula):
+ *
+ *   O[b,n,h,q,:] = sum_k softmax_k(x) V[b,n,h,k,:]
+ *   x_k = s * (Q[b,n,h,q,:] . K[b,n,h,k,:]) + bias[b,0,h,q,k]   if key k is valid
+ *   x_k = -1e9                                                   otherwise
+ *   lse[b,n,h,q] = log sum_k exp(x_k),   max[b,n,h,q] = max_k x_k
+ *
+ * A masked key's logit is REPLACED by -1e9, so a row with no valid key gets a
+ * uniform softmax over all K keys: O is the mean of V, max = -1e9 and
+ * lse = -1e9 + ln K, which is -1e9 after rounding to fp32.
+ *
+ * Conventions shared by every entry point:
+ *   - All tensors are dense, contiguous, row-major device buffers owned by the
+ *     caller; every pointer must be 16-byte aligned.  The library allocates
+ *     no device memory per call and keeps no state between calls besides one
+ *     device-side status word (see tri_attn_get_status).
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
+ *     enqueued asynchronously on it; results are ready when the stream is.
+ *   - Argument checks are made on the host before anything is enqueued, read
+ *     no device memory, and return TA_ERR_INVALID_ARG (malformed call) or
+ *     TA_ERR_UNSUPPORTED (well-formed but outside what the kernels cover).
+ *     A CUDA launch error returns TA_ERR_CUDA.  Nothing throws across the ABI.
+ *   - Faults detected inside a kernel (a bounded wait that ran out, a device
+ *     value outside its contract) do not trap: the kernel records a code in
+ *     the status word and returns.  tri_attn_get_status() reports it.
+ *   - Entry points are thread-safe; calls on different streams may overlap.
+ */
+#ifndef TRIATTN_H
+#define TRIATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TA_OK = 0,
+    TA_ERR_INVALID_ARG = 1, /* malformed call: NULL required pointer, size <= 0, misaligned pointer, both mask kinds */
+    TA_ERR_UNSUPPORTED = 2, /* well-formed but outside the kernels: dtype pair, D, K alignment, block size */
+    TA_ERR_CUDA = 3,        /* a CUDA runtime / driver call failed (no device, launch failure, ...) */
+    TA_ERR_TIMEOUT = 4,     /* a kernel's bounded pipeline wait ran out (reported by tri_attn_get_status) */
+    TA_ERR_DEVICE = 5       /* a kernel saw a device-side value outside its contract (e.g. seqlen > max_seqlen) */
+} ta_status;
+
+/* Element types.  Precision follows the input dtype (triangle_attention page, Notes 2). */
+typedef enum { TA_F32 = 0, TA_F16 = 1, TA_BF16 = 2 } ta_dtype;
+
+/* Element predicate applied on partial blocks of a BlockMask (tensorplay
+ * "BlockMask", Details 2: mask_mod is skipped on full blocks).  CAUSAL keeps
+ * key k for query q when k <= q, both indices local to their sequence. */
+typedef enum { TA_MASK_NONE = 0, TA_MASK_CAUSAL = 1 } ta_mask_mod;
+
+/*
+ * tri_attn_fwd -- triangle-attention forward.
+ * (cuEquivariance triangle_attention page: formula; Parameters q, k, v, bias,
+ *  mask, scale, kv_lengths; Returns.)
+ *
+ *   q, out      (B, N, H, Q, D) of `qkv_dtype`
+ *   k, v        (B, N, H, K, D) of `qkv_dtype`
+ *   bias        (B, 1, H, Q, K) of `bias_dtype`; required; shared over N.
+ *               bias_dtype is TA_F32 or equal to qkv_dtype; it is read in
+ *               its stored type, never cast.
+ *   mask        optional (B, N, 1, 1, K) uint8, nonzero = valid key
+ *   kv_lengths  optional (B, N) int32 (same memory as (B, N, 1, 1, 1)): keys
+ *               j < kv_lengths[b,n] are valid.  Values above K are clamped to
+ *               K (the page); negative values are read as 0 (all masked).
+ *               At most one of mask / kv_lengths may be given (the page:
+ *               "Pass either mask or kv_lengths, not both"); neither = no mask.
+ *   scale       s in the formula, used as given (the Python binding applies
+ *               the page's default 1/sqrt(D) when scale is None).
+ *   lse, max    optional (B, N, H, Q) fp32 outputs (return_aux); NULL skips.
+ *
+ * Supported: fp16/bf16 q/k/v with D % 8 == 0, D <= 128 and K % 8 == 0 (the
+ * page's Notes 3-4 bounds for the half-precision kernels), on tcgen05 tensor
+ * cores; fp32 q/k/v with D % 4 == 0, D <= 128 on exact-fp32 CUDA-core
+ * arithmetic (no TF32).  fp32 bias with 16-bit q/k/v additionally needs
+ * K % 4 == 0 (met by K % 8).  Anything else -> TA_ERR_UNSUPPORTED; there is
+ * no fallback path.
+ */
+ta_status tri_attn_fwd(const void* q, const void* k, const void* v, ta_dtype qkv_dtype,
+                       const void* bias, ta_dtype bias_dtype,
+                       const uint8_t* mask, const int32_t* kv_lengths,
+                       int B, int N, int H, int Q, int K, int D, float scale,
+                       void* out, float* lse, float* max, void* stream);
+
+/*
+ * tri_attn_varlen_fwd -- packed-sequence forward with a block-sparse mask.
+ * (Transformer Engine 0.9 fused_attn.h: NVTE_NOT_INTERLEAVED layout,
+ *  cu_seqlens_q / cu_seqlens_kv, max_seqlen_q / max_seqlen_kv; tensorplay
+ *  nn.attention "BlockMask": kv_num_blocks / kv_indices, full_kv_* lists,
+ *  BLOCK_SIZE, mask_mod.)
+ *
+ *   q, out        (total_q, H, D) of `dtype`;  k, v (total_k, H, D)
+ *   cu_seqlens_q  (num_seqs + 1) int32, cu_seqlens_q[0] = 0, non-decreasing;
+ *   cu_seqlens_k  likewise for keys.  Sequence i holds rows
+ *                 [cu[i], cu[i+1]).  Every length must be <= the matching
+ *                 max_seqlen (else TA_ERR_DEVICE is recorded and that
+ *                 sequence is skipped).
+ *   kv_num_blocks (num_seqs, mask_heads, max_q_blocks) int32 and
+ *   kv_indices    (num_seqs, mask_heads, max_q_blocks, max_kv_blocks) int32:
+ *                 partial kv blocks of each 128-row q block, sequence-local
+ *                 block indices; entries past the count are never read and
+ *                 out-of-range indices are skipped.  NULL (both) = every
+ *                 block of the sequence is partial.
+ *   full_kv_num_blocks / full_kv_indices: same shapes, optional, both or
+ *                 neither (else TA_ERR_INVALID_ARG): blocks where every key
+ *                 is valid, visited without mask_mod.  The two lists must be
+ *                 disjoint.  Keys outside every listed block have logit -1e9.
+ *   mask_heads    1 (one mask for all heads) or H.
+ *   block_q, block_k  must both be 128 (else TA_ERR_UNSUPPORTED).
+ *   lse, max      optional (H, total_q) fp32.
+ *   No bias.  A key row past the end of its sequence takes no part.  A
+ *   sequence with no keys gets O = 0 and lse = max = -inf.
+ *
+ * Supported: fp16/bf16 with D % 8 == 0, D <= 128 (tcgen05), fp32 with
+ * D % 4 == 0, D <= 128 (CUDA cores).
+ */
+ta_status tri_attn_varlen_fwd(const void* q, const void* k, const void* v, ta_dtype dtype,
+                              const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                              int num_seqs, int max_seqlen_q, int max_seqlen_k, int H, int D,
+                              float scale,
+                              const int32_t* kv_num_blocks, const int32_t* kv_indices,
+                              const int32_t* full_kv_num_blocks, const int32_t* full_kv_indices,
+                              int mask_heads, int max_q_blocks, int max_kv_blocks,
+                              int block_q, int block_k, ta_mask_mod mask_mod,
+                              void* out, float* lse, float* max, void* stream);
+
+/*
+ * tri_attn_mask_to_kv_lengths -- dense key mask -> prefix lengths.
+ * (triangle_attention page, Example: mask_to_kv_lengths(mask).)
+ *
+ *   mask            (B, N, 1, 1, K) uint8, nonzero = valid
+ *   kv_lengths      (B, N) int32 output: count of leading valid keys per row
+ *   nonprefix_count optional single int32 on the device; the number of rows
+ *                   that have a valid key after their first masked key (rows
+ *                   a prefix length cannot represent) is ADDED to it.
+ */
+ta_status tri_attn_mask_to_kv_lengths(const uint8_t* mask, int B, int N, int K, int32_t* kv_lengths,
+                                      int32_t* nonprefix_count, void* stream);
+
+/*
+ * tri_attn_get_status -- synchronize `stream`, then read and clear the
+ * device-side status word of the current device.  Returns TA_OK, or the first
+ * TA_ERR_TIMEOUT / TA_ERR_DEVICE recorded by a kernel since the last call, or
+ * TA_ERR_CUDA if the synchronization itself failed.
+ */
+ta_status tri_attn_get_status(void* stream);
+
+/* Static, human-readable name of a status code (never NULL). */
+const char* tri_attn_error_string(ta_status status);
+
+/* Library ABI version, (major << 16) | minor. */
+int tri_attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TRIATTN_H */

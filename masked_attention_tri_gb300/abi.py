@@ -1,0 +1,108 @@
+"""ctypes binding of libtriattn.so: one Python function per C entry point, same names.
+
+Argument marshalling only (pointers and sizes in, status code out); every step
+of the computation runs in the library's CUDA kernels.  A non-OK status is
+raised: TA_ERR_INVALID_ARG as ValueError, TA_ERR_UNSUPPORTED as
+NotImplementedError, anything else as RuntimeError.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libtriattn.so")
+
+TA_OK, TA_ERR_INVALID_ARG, TA_ERR_UNSUPPORTED, TA_ERR_CUDA, TA_ERR_TIMEOUT, TA_ERR_DEVICE = range(6)
+TA_F32, TA_F16, TA_BF16 = 0, 1, 2
+TA_MASK_NONE, TA_MASK_CAUSAL = 0, 1
+
+# Every symbol include/triattn.h declares.
+EXPORTS = ("tri_attn_fwd", "tri_attn_varlen_fwd", "tri_attn_mask_to_kv_lengths", "tri_attn_get_status",
+           "tri_attn_error_string", "tri_attn_version")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class TriAttnError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(msg)
+        self.status = status
+
+
+def load() -> ctypes.CDLL:
+    """Load the built library; raise loudly if it is missing (there is no fallback)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is not built; run masked_attention_tri_gb300.build.build() "
+                              "(nvcc, sm_103a) first")
+        lib = ctypes.CDLL(LIB_PATH)
+        P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        lib.tri_attn_fwd.argtypes = [P, P, P, I, P, I, P, P, I, I, I, I, I, I, F, P, P, P, P]
+        lib.tri_attn_fwd.restype = I
+        lib.tri_attn_varlen_fwd.argtypes = [P, P, P, I, P, P, I, I, I, I, I, F, P, P, P, P, I, I, I, I, I, I,
+                                            P, P, P, P]
+        lib.tri_attn_varlen_fwd.restype = I
+        lib.tri_attn_mask_to_kv_lengths.argtypes = [P, I, I, I, P, P, P]
+        lib.tri_attn_mask_to_kv_lengths.restype = I
+        lib.tri_attn_get_status.argtypes = [P]
+        lib.tri_attn_get_status.restype = I
+        lib.tri_attn_error_string.argtypes = [I]
+        lib.tri_attn_error_string.restype = ctypes.c_char_p
+        lib.tri_attn_version.argtypes = []
+        lib.tri_attn_version.restype = I
+        _lib = lib
+        return lib
+
+
+def tri_attn_error_string(status: int) -> str:
+    return load().tri_attn_error_string(int(status)).decode()
+
+
+def _check(status: int, fn: str) -> None:
+    if status == TA_OK:
+        return
+    msg = f"{fn}: {tri_attn_error_string(status)} (status {status})"
+    if status == TA_ERR_INVALID_ARG:
+        raise ValueError(msg)
+    if status == TA_ERR_UNSUPPORTED:
+        raise NotImplementedError(msg)
+    raise TriAttnError(status, msg)
+
+
+def tri_attn_fwd(q, k, v, qkv_dtype, bias, bias_dtype, mask, kv_lengths, B, N, H, Q, K, D, scale, out, lse, max_,
+                 stream) -> None:
+    """Pointers are ints (0 = NULL); stream is a cudaStream_t handle as int."""
+    st = load().tri_attn_fwd(q, k, v, qkv_dtype, bias, bias_dtype, mask or None, kv_lengths or None, B, N, H, Q, K,
+                             D, float(scale), out, lse or None, max_ or None, stream or None)
+    _check(st, "tri_attn_fwd")
+
+
+def tri_attn_varlen_fwd(q, k, v, dtype, cu_seqlens_q, cu_seqlens_k, num_seqs, max_seqlen_q, max_seqlen_k, H, D,
+                        scale, kv_num_blocks, kv_indices, full_kv_num_blocks, full_kv_indices, mask_heads,
+                        max_q_blocks, max_kv_blocks, block_q, block_k, mask_mod, out, lse, max_, stream) -> None:
+    st = load().tri_attn_varlen_fwd(q, k, v, dtype, cu_seqlens_q, cu_seqlens_k, num_seqs, max_seqlen_q,
+                                    max_seqlen_k, H, D, float(scale), kv_num_blocks or None, kv_indices or None,
+                                    full_kv_num_blocks or None, full_kv_indices or None, mask_heads, max_q_blocks,
+                                    max_kv_blocks, block_q, block_k, mask_mod, out, lse or None, max_ or None,
+                                    stream or None)
+    _check(st, "tri_attn_varlen_fwd")
+
+
+def tri_attn_mask_to_kv_lengths(mask, B, N, K, kv_lengths, nonprefix_count, stream) -> None:
+    st = load().tri_attn_mask_to_kv_lengths(mask, B, N, K, kv_lengths, nonprefix_count or None, stream or None)
+    _check(st, "tri_attn_mask_to_kv_lengths")
+
+
+def tri_attn_get_status(stream) -> int:
+    """Synchronize the stream and return (and clear) the device status word."""
+    return int(load().tri_attn_get_status(stream or None))
+
+
+def tri_attn_version() -> int:
+    return int(load().tri_attn_version())

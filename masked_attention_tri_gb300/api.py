@@ -1,0 +1,260 @@
+"""PyTorch-facing API over the C ABI.
+
+Mirrors the cuEquivariance ``triangle_attention`` signature (forward only)
+and adds the packed-sequence entry with a tensorplay-style ``BlockMask``.
+PyTorch provides device memory and the current stream; the work is done by
+libtriattn.so's kernels.  Inputs are used in place (no casts or copies): they
+must be contiguous CUDA tensors of the documented dtypes.
+"""
+from __future__ import annotations
+
+import math
+from typing import Optional
+
+import torch
+
+from . import abi
+
+_DT = {torch.float32: abi.TA_F32, torch.float16: abi.TA_F16, torch.bfloat16: abi.TA_BF16}
+
+
+def _ptr(t: Optional[torch.Tensor]) -> int:
+    return 0 if t is None else t.data_ptr()
+
+
+def _need(t: torch.Tensor, name: str, device: torch.device) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _stream(device: torch.device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def triangle_attention(q, k, v, bias, mask=None, scale=None, return_aux=False, *, kv_lengths=None, out=None):
+    """Triangle-attention forward (cuEquivariance triangle_attention page: formula, Parameters).
+
+    q (B,N,H,Q,D), k/v (B,N,H,K,D), bias (B,1,H,Q,K); for B=1 the 4-D forms
+    (N,H,Q,D) / (1,H,Q,K) / (N,1,1,K) are accepted.  mask: bool/uint8
+    (B,N,1,1,K); kv_lengths: int32 (B,N,1,1,1) or (B,N); at most one of them.
+    scale defaults to 1/sqrt(D).  Returns O, or (O, lse, max) with
+    return_aux (lse / max fp32 shaped (B,N,H,Q,1)).
+    """
+    if mask is not None and kv_lengths is not None:
+        raise ValueError("pass either mask or kv_lengths, not both")
+    four_d = q.dim() == 4
+    if four_d:
+        q, k, v = q.unsqueeze(0), k.unsqueeze(0), v.unsqueeze(0)
+        if bias.dim() == 4:
+            bias = bias.unsqueeze(0)
+        if mask is not None and mask.dim() == 4:
+            mask = mask.unsqueeze(0)
+    if q.dim() != 5 or k.dim() != 5 or v.dim() != 5 or bias.dim() != 5:
+        raise ValueError("expected q/k/v (B,N,H,Q|K,D) and bias (B,1,H,Q,K)")
+    B, N, H, Q, D = q.shape
+    K = k.shape[3]
+    if tuple(k.shape) != (B, N, H, K, D) or tuple(v.shape) != (B, N, H, K, D):
+        raise ValueError(f"k/v must be {(B, N, H, K, D)}, got {tuple(k.shape)} / {tuple(v.shape)}")
+    if tuple(bias.shape) != (B, 1, H, Q, K):
+        raise ValueError(f"bias must be {(B, 1, H, Q, K)}, got {tuple(bias.shape)}")
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("triangle_attention runs on CUDA tensors only")
+    for t, nm in ((q, "q"), (k, "k"), (v, "v"), (bias, "bias")):
+        _need(t, nm, dev)
+    if q.dtype not in _DT or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share one dtype among float32 / float16 / bfloat16")
+    if bias.dtype not in (torch.float32, q.dtype):
+        raise TypeError("bias must be float32 or q's dtype")
+    m8 = None
+    if mask is not None:
+        if tuple(mask.shape) != (B, N, 1, 1, K):
+            raise ValueError(f"mask must be {(B, N, 1, 1, K)}, got {tuple(mask.shape)}")
+        if mask.dtype not in (torch.bool, torch.uint8, torch.int8):
+            raise TypeError("mask must be bool, uint8 or int8 (nonzero = valid)")
+        _need(mask, "mask", dev)
+        m8 = mask.view(torch.uint8)
+    kl = None
+    if kv_lengths is not None:
+        if kv_lengths.dtype != torch.int32 or kv_lengths.numel() != B * N:
+            raise ValueError("kv_lengths must be int32 with B*N elements ((B,N,1,1,1) or (B,N))")
+        _need(kv_lengths, "kv_lengths", dev)
+        kl = kv_lengths
+    s = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need(out, "out", dev)
+    lse = mx = None
+    if return_aux:
+        lse = torch.empty(B, N, H, Q, 1, device=dev, dtype=torch.float32)
+        mx = torch.empty(B, N, H, Q, 1, device=dev, dtype=torch.float32)
+    with torch.cuda.device(dev):
+        abi.tri_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _DT[q.dtype], _ptr(bias), _DT[bias.dtype], _ptr(m8), _ptr(kl),
+                         B, N, H, Q, K, D, s, _ptr(out), _ptr(lse), _ptr(mx), _stream(dev))
+    if four_d:
+        out = out.squeeze(0)
+        if return_aux:
+            lse, mx = lse.squeeze(0), mx.squeeze(0)
+    return (out, lse, mx) if return_aux else out
+
+
+def mask_to_kv_lengths(mask: torch.Tensor, return_nonprefix: bool = False):
+    """(B,N,1,1,K) key mask -> int32 (B,N,1,1,1) counts of leading valid keys.
+
+    The triangle_attention page's Example uses this to turn a right-padded
+    mask into kv_lengths.  With return_nonprefix, also returns a 1-element
+    int32 tensor counting rows that are not a prefix mask.
+    """
+    if mask.dim() == 4:
+        mask = mask.unsqueeze(0)
+    B, N, K = mask.shape[0], mask.shape[1], mask.shape[-1]
+    if mask.numel() != B * N * K:
+        raise ValueError("mask must be (B,N,1,1,K)")
+    if mask.dtype not in (torch.bool, torch.uint8, torch.int8):
+        raise TypeError("mask must be bool, uint8 or int8")
+    dev = mask.device
+    _need(mask, "mask", dev)
+    kl = torch.empty(B, N, 1, 1, 1, device=dev, dtype=torch.int32)
+    cnt = torch.zeros(1, device=dev, dtype=torch.int32) if return_nonprefix else None
+    with torch.cuda.device(dev):
+        abi.tri_attn_mask_to_kv_lengths(_ptr(mask.view(torch.uint8)), B, N, K, _ptr(kl), _ptr(cnt), _stream(dev))
+    return (kl, cnt) if return_nonprefix else kl
+
+
+class BlockMask:
+    """Block-sparse mask in the tensorplay BlockMask format (kv side, forward only).
+
+    kv_num_blocks (S, Hm, MQ) and kv_indices (S, Hm, MQ, MK): partial blocks
+    of each q block, where mask_mod applies; full_kv_* (optional, same shapes):
+    blocks where every key is valid.  Indices are sequence-local 128-row
+    blocks.  mask_mod is None or "causal" (a C ABI cannot take a callable).
+    """
+
+    def __init__(self, kv_num_blocks, kv_indices, full_kv_num_blocks=None, full_kv_indices=None, BLOCK_SIZE=128,
+                 mask_mod=None):
+        self.kv_num_blocks = kv_num_blocks
+        self.kv_indices = kv_indices
+        self.full_kv_num_blocks = full_kv_num_blocks
+        self.full_kv_indices = full_kv_indices
+        self.BLOCK_SIZE = (BLOCK_SIZE, BLOCK_SIZE) if isinstance(BLOCK_SIZE, int) else tuple(BLOCK_SIZE)
+        self.mask_mod = mask_mod
+
+    @classmethod
+    def from_kv_blocks(cls, kv_num_blocks, kv_indices, full_kv_num_blocks=None, full_kv_indices=None,
+                       BLOCK_SIZE=128, mask_mod=None):
+        """Same error rules as the BlockMask page's from_kv_blocks (Raises)."""
+        if kv_indices.dim() < 2:
+            raise RuntimeError("BlockMask must have at least 2 dimensions")
+        assert (full_kv_num_blocks is None) == (full_kv_indices is None), \
+            "full_kv_num_blocks and full_kv_indices must be both provided or omitted"
+        if mask_mod not in (None, "causal", "none"):
+            raise ValueError("mask_mod must be None or 'causal'")
+        return cls(kv_num_blocks, kv_indices, full_kv_num_blocks, full_kv_indices, BLOCK_SIZE, mask_mod)
+
+    @property
+    def mask_mod_code(self) -> int:
+        return abi.TA_MASK_CAUSAL if self.mask_mod == "causal" else abi.TA_MASK_NONE
+
+    def numel(self) -> int:
+        """Blocks in the mask, not accounting for sparsity (q blocks x kv blocks x leading dims)."""
+        *lead, mq = self.kv_num_blocks.shape
+        n = 1
+        for x in lead:
+            n *= int(x)
+        return n * int(mq) * int(self.kv_indices.shape[-1])
+
+    def to_dense(self) -> torch.Tensor:
+        """Dense (…, MQ, MK) block mask: 1 where a block is listed (partial or full)."""
+        num = self.kv_num_blocks.cpu()
+        idx = self.kv_indices.cpu()
+        MK = idx.shape[-1]
+        dense = torch.zeros(*num.shape, MK, dtype=torch.int32)
+        pairs = [(num, idx)]
+        if self.full_kv_num_blocks is not None:
+            pairs.append((self.full_kv_num_blocks.cpu(), self.full_kv_indices.cpu()))
+        for nb, ix in pairs:
+            flat_n = nb.reshape(-1)
+            flat_i = ix.reshape(-1, MK)
+            flat_d = dense.view(-1, MK)
+            for r in range(flat_n.numel()):
+                for t in range(int(flat_n[r])):
+                    c = int(flat_i[r, t])
+                    if 0 <= c < MK:
+                        flat_d[r, c] = 1
+        return dense
+
+    def sparsity(self) -> float:
+        """Percentage of blocks that are not computed."""
+        dense = self.to_dense()
+        return 100.0 * (1.0 - float(dense.sum()) / max(1, dense.numel()))
+
+
+def varlen_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, block_mask=None, scale=None,
+                     return_aux=False, *, mask_mod=None, out=None):
+    """Packed-sequence forward (NVTE_NOT_INTERLEAVED layout) with an optional BlockMask.
+
+    q (total_q,H,D), k/v (total_k,H,D), cu_seqlens int32 (S+1,).  Without a
+    block_mask every block is visited and ``mask_mod`` (None / "causal")
+    applies everywhere.  Returns O, or (O, lse, max) with lse/max (H, total_q).
+    """
+    if q.dim() != 3 or k.dim() != 3 or v.dim() != 3:
+        raise ValueError("expected q (total_q,H,D), k/v (total_k,H,D)")
+    total_q, H, D = q.shape
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("varlen_attention runs on CUDA tensors only")
+    for t, nm in ((q, "q"), (k, "k"), (v, "v"), (cu_seqlens_q, "cu_seqlens_q"), (cu_seqlens_k, "cu_seqlens_k")):
+        _need(t, nm, dev)
+    if q.dtype not in _DT or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share one dtype among float32 / float16 / bfloat16")
+    if cu_seqlens_q.dtype != torch.int32 or cu_seqlens_k.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
+    S = cu_seqlens_q.numel() - 1
+    if cu_seqlens_k.numel() != S + 1 or S <= 0:
+        raise ValueError("cu_seqlens_q / cu_seqlens_k must both have num_seqs + 1 entries")
+    s = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    kn = ki = fn = fi = None
+    mask_heads = MQ = MK = 0
+    bq = bk = 128
+    mm = abi.TA_MASK_CAUSAL if mask_mod == "causal" else abi.TA_MASK_NONE
+    if block_mask is not None:
+        kn, ki = block_mask.kv_num_blocks, block_mask.kv_indices
+        fn, fi = block_mask.full_kv_num_blocks, block_mask.full_kv_indices
+        for t, nm in ((kn, "kv_num_blocks"), (ki, "kv_indices"), (fn, "full_kv_num_blocks"),
+                      (fi, "full_kv_indices")):
+            if t is not None:
+                _need(t, nm, dev)
+                if t.dtype != torch.int32:
+                    raise TypeError(f"{nm} must be int32")
+        if kn.dim() != 3 or ki.dim() != 4:
+            raise ValueError("kv_num_blocks must be (S, Hm, MQ) and kv_indices (S, Hm, MQ, MK)")
+        mask_heads, MQ, MK = kn.shape[1], kn.shape[2], ki.shape[3]
+        if fn is not None and (tuple(fn.shape) != tuple(kn.shape) or tuple(fi.shape) != tuple(ki.shape)):
+            raise ValueError("full_kv_* must have the shapes of kv_*")
+        bq, bk = block_mask.BLOCK_SIZE
+        mm = block_mask.mask_mod_code
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need(out, "out", dev)
+    lse = mx = None
+    if return_aux:
+        lse = torch.empty(H, total_q, device=dev, dtype=torch.float32)
+        mx = torch.empty(H, total_q, device=dev, dtype=torch.float32)
+    with torch.cuda.device(dev):
+        abi.tri_attn_varlen_fwd(_ptr(q), _ptr(k), _ptr(v), _DT[q.dtype], _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), S,
+                                int(max_seqlen_q), int(max_seqlen_k), H, D, s, _ptr(kn), _ptr(ki), _ptr(fn), _ptr(fi),
+                                mask_heads, MQ, MK, bq, bk, mm, _ptr(out), _ptr(lse), _ptr(mx), _stream(dev))
+    return (out, lse, mx) if return_aux else out
+
+
+def get_status(device=None) -> int:
+    """Synchronize the current stream and return/clear the device status word (0 = OK)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        return abi.tri_attn_get_status(_stream(dev))

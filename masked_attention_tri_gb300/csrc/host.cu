@@ -1,0 +1,202 @@
+// host.cu -- the C ABI (include/triattn.h): argument checks, dispatch by
+// dtype, and the device status word.
+//
+// Checks follow the cuEquivariance triangle_attention page (Parameters:
+// "Pass either mask or kv_lengths, not both"; Notes 3-4 for the supported
+// head dimensions and the K % 8 rule of the Blackwell kernels), the
+// Transformer Engine fused_attn.h page (cu_seqlens, max_seqlen) and the
+// tensorplay BlockMask page (full_kv_* lists given together, BLOCK_SIZE).
+
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "internal.h"
+
+#define TA_EXPORT extern "C" __attribute__((visibility("default")))
+
+namespace triattn {
+
+// One status word per device, written by kernels that give up.
+__device__ int g_status_word = 0;
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_status_mu;
+int* g_status_ptr[kMaxDevices] = {};
+}  // namespace
+
+int* status_word() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_status_mu);
+    if (!g_status_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+        g_status_ptr[dev] = static_cast<int*>(p);
+    }
+    return g_status_ptr[dev];
+}
+
+}  // namespace triattn
+
+using triattn::AttnParams;
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool valid_dtype(int d) { return d == TA_F32 || d == TA_F16 || d == TA_BF16; }
+
+// Head-dimension rules: 16-bit inputs D % 8 == 0 and D <= 128; fp32 D % 4 == 0 and D <= 128.
+bool supported_d(int dtype, int D) {
+    if (D > 128) return false;
+    return dtype == TA_F32 ? (D % 4 == 0) : (D % 8 == 0);
+}
+
+ta_status run(const AttnParams& p, cudaStream_t stream) {
+    cudaError_t e = triattn::launch_simt_fwd(p, stream);
+    return e == cudaSuccess ? TA_OK : TA_ERR_CUDA;
+}
+
+}  // namespace
+
+TA_EXPORT ta_status tri_attn_fwd(const void* q, const void* k, const void* v, ta_dtype qkv_dtype, const void* bias,
+                                 ta_dtype bias_dtype, const uint8_t* mask, const int32_t* kv_lengths, int B, int N,
+                                 int H, int Q, int K, int D, float scale, void* out, float* lse, float* max,
+                                 void* stream) {
+    if (!q || !k || !v || !bias || !out) return TA_ERR_INVALID_ARG;
+    if (B <= 0 || N <= 0 || H <= 0 || Q <= 0 || K <= 0 || D <= 0) return TA_ERR_INVALID_ARG;
+    if (mask && kv_lengths) return TA_ERR_INVALID_ARG;
+    if (!valid_dtype(qkv_dtype) || !valid_dtype(bias_dtype)) return TA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(bias, 16) || !aligned(out, 16))
+        return TA_ERR_INVALID_ARG;
+    if ((lse && !aligned(lse, 4)) || (max && !aligned(max, 4)) || (kv_lengths && !aligned(kv_lengths, 4)))
+        return TA_ERR_INVALID_ARG;
+    if (bias_dtype != TA_F32 && bias_dtype != qkv_dtype) return TA_ERR_UNSUPPORTED;
+    if (!supported_d(qkv_dtype, D)) return TA_ERR_UNSUPPORTED;
+    if (qkv_dtype != TA_F32 && K % 8 != 0) return TA_ERR_UNSUPPORTED;
+    // Sizes: every flat element index must fit in 63 bits and the grid in 31.
+    const long long units = (long long)B * N * H;
+    if (units > (1LL << 40) || (long long)Q * K > (1LL << 40) || units * ((Q + 31) / 32) > 0x7fffffffLL)
+        return TA_ERR_UNSUPPORTED;
+
+    int* status = triattn::status_word();
+    if (!status) return TA_ERR_CUDA;
+    AttnParams p{};
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.bias = bias;
+    p.mask = mask;
+    p.kv_len = kv_lengths;
+    p.out = out;
+    p.lse = lse;
+    p.mx = max;
+    p.status = status;
+    p.dtype = qkv_dtype;
+    p.bias_f32 = bias_dtype == TA_F32;
+    p.scale = scale;
+    p.B = B;
+    p.N = N;
+    p.H = H;
+    p.Q = Q;
+    p.K = K;
+    p.D = D;
+    p.varlen = 0;
+    return run(p, static_cast<cudaStream_t>(stream));
+}
+
+TA_EXPORT ta_status tri_attn_varlen_fwd(const void* q, const void* k, const void* v, ta_dtype dtype,
+                                        const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int num_seqs,
+                                        int max_seqlen_q, int max_seqlen_k, int H, int D, float scale,
+                                        const int32_t* kv_num_blocks, const int32_t* kv_indices,
+                                        const int32_t* full_kv_num_blocks, const int32_t* full_kv_indices,
+                                        int mask_heads, int max_q_blocks, int max_kv_blocks, int block_q,
+                                        int block_k, ta_mask_mod mask_mod, void* out, float* lse, float* max,
+                                        void* stream) {
+    if (!q || !k || !v || !out || !cu_seqlens_q || !cu_seqlens_k) return TA_ERR_INVALID_ARG;
+    if (num_seqs <= 0 || H <= 0 || D <= 0 || max_seqlen_q < 0 || max_seqlen_k < 0) return TA_ERR_INVALID_ARG;
+    if (!valid_dtype(dtype)) return TA_ERR_INVALID_ARG;
+    if (mask_mod != TA_MASK_NONE && mask_mod != TA_MASK_CAUSAL) return TA_ERR_INVALID_ARG;
+    if ((kv_num_blocks == nullptr) != (kv_indices == nullptr)) return TA_ERR_INVALID_ARG;
+    if ((full_kv_num_blocks == nullptr) != (full_kv_indices == nullptr)) return TA_ERR_INVALID_ARG;
+    if (full_kv_num_blocks && !kv_num_blocks) return TA_ERR_INVALID_ARG;
+    if (kv_num_blocks) {
+        if (mask_heads != 1 && mask_heads != H) return TA_ERR_INVALID_ARG;
+        if (max_q_blocks <= 0 || max_kv_blocks <= 0) return TA_ERR_INVALID_ARG;
+    }
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16)) return TA_ERR_INVALID_ARG;
+    if ((lse && !aligned(lse, 4)) || (max && !aligned(max, 4))) return TA_ERR_INVALID_ARG;
+    if (block_q != 128 || block_k != 128) return TA_ERR_UNSUPPORTED;
+    if (!supported_d(dtype, D)) return TA_ERR_UNSUPPORTED;
+    if ((long long)num_seqs * H * ((max_seqlen_q + 31) / 32) > 0x7fffffffLL) return TA_ERR_UNSUPPORTED;
+    if (max_seqlen_q == 0) return TA_OK;
+
+    int* status = triattn::status_word();
+    if (!status) return TA_ERR_CUDA;
+    // total_q (the lse/max row stride) is cu_seqlens_q[num_seqs]; the host does
+    // not read device memory, so the kernels take it from the device array.
+    AttnParams p{};
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.out = out;
+    p.lse = lse;
+    p.mx = max;
+    p.status = status;
+    p.dtype = dtype;
+    p.scale = scale;
+    p.H = H;
+    p.D = D;
+    p.varlen = 1;
+    p.cu_q = cu_seqlens_q;
+    p.cu_k = cu_seqlens_k;
+    p.num_seqs = num_seqs;
+    p.max_q = max_seqlen_q;
+    p.max_k = max_seqlen_k;
+    p.kv_num = kv_num_blocks;
+    p.kv_idx = kv_indices;
+    p.full_num = full_kv_num_blocks;
+    p.full_idx = full_kv_indices;
+    p.mask_heads = kv_num_blocks ? mask_heads : 1;
+    p.MQ = kv_num_blocks ? max_q_blocks : 0;
+    p.MK = kv_num_blocks ? max_kv_blocks : 0;
+    p.mask_mod = mask_mod;
+    p.total_q = -1;
+    return run(p, static_cast<cudaStream_t>(stream));
+}
+
+TA_EXPORT ta_status tri_attn_mask_to_kv_lengths(const uint8_t* mask, int B, int N, int K, int32_t* kv_lengths,
+                                                int32_t* nonprefix_count, void* stream) {
+    if (!mask || !kv_lengths) return TA_ERR_INVALID_ARG;
+    if (B <= 0 || N <= 0 || K <= 0) return TA_ERR_INVALID_ARG;
+    if (!aligned(kv_lengths, 4) || (nonprefix_count && !aligned(nonprefix_count, 4))) return TA_ERR_INVALID_ARG;
+    cudaError_t e = triattn::launch_mask_to_kv_lengths(mask, (long long)B * N, K, kv_lengths, nonprefix_count,
+                                                       static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TA_OK : TA_ERR_CUDA;
+}
+
+TA_EXPORT ta_status tri_attn_get_status(void* stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return TA_ERR_CUDA;
+    int* w = triattn::status_word();
+    if (!w) return TA_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, w, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return TA_ERR_CUDA;
+    if (v != 0 && cudaMemset(w, 0, sizeof(int)) != cudaSuccess) return TA_ERR_CUDA;
+    return static_cast<ta_status>(v);
+}
+
+TA_EXPORT const char* tri_attn_error_string(ta_status s) {
+    switch (s) {
+    case TA_OK: return "ok";
+    case TA_ERR_INVALID_ARG: return "invalid argument";
+    case TA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case TA_ERR_CUDA: return "CUDA error";
+    case TA_ERR_TIMEOUT: return "kernel pipeline wait timed out";
+    case TA_ERR_DEVICE: return "device-side value outside its contract";
+    default: return "unknown status";
+    }
+}
+
+TA_EXPORT int tri_attn_version(void) { return (1 << 16) | 0; }

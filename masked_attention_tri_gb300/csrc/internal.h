@@ -1,0 +1,64 @@
+// internal.h -- parameter blocks and launchers shared by the host entry points
+// and the kernels of the triangle-attention library.  Not part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/triattn.h"
+
+namespace triattn {
+
+// Device-side status codes (match ta_status).  A kernel that gives up writes
+// one with atomicCAS(status, 0, code) so the first fault is kept.
+enum : int { kStatusOk = 0, kStatusTimeout = TA_ERR_TIMEOUT, kStatusDevice = TA_ERR_DEVICE };
+
+// One attention problem as the kernels see it.  Triangle form: units are
+// (b, n, h) slabs with Q query rows and K keys.  Varlen form: units are
+// (sequence, h) with lengths read from cu_seqlens.
+struct AttnParams {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* bias;       // triangle only, may be NULL in varlen
+    const uint8_t* mask;    // triangle dense key mask (B,N,K) or NULL
+    const int32_t* kv_len;  // triangle kv_lengths (B,N) or NULL
+    void* out;
+    float* lse;
+    float* mx;
+    int* status;            // device status word
+
+    int dtype;              // ta_dtype of q/k/v/out
+    int bias_f32;           // 1: bias is fp32, 0: bias has the q/k/v dtype
+    float scale;
+
+    // triangle sizes
+    int B, N, H, Q, K, D;
+
+    // varlen
+    int varlen;
+    const int32_t* cu_q;
+    const int32_t* cu_k;
+    int num_seqs, max_q, max_k;
+    const int32_t* kv_num;
+    const int32_t* kv_idx;
+    const int32_t* full_num;
+    const int32_t* full_idx;
+    int mask_heads, MQ, MK, mask_mod;
+    long long total_q;      // rows of q/out (lse/max stride in varlen)
+};
+
+// CUDA-core path: exact fp32 arithmetic, any dtype, both forms.
+cudaError_t launch_simt_fwd(const AttnParams& p, cudaStream_t stream);
+
+// tcgen05 / TMA path for fp16 / bf16 (both forms).
+cudaError_t launch_tc_fwd(const AttnParams& p, cudaStream_t stream);
+
+// mask -> prefix lengths.
+cudaError_t launch_mask_to_kv_lengths(const uint8_t* mask, long long rows, int K, int32_t* kv_len,
+                                      int32_t* nonprefix, cudaStream_t stream);
+
+// Device address of the status word on the current device (set up once per device).
+int* status_word();
+
+}  // namespace triattn

@@ -1,0 +1,110 @@
+"""CPU-only checks of the C ABI: the library builds, loads, exports every
+declared symbol, and its host-side argument checks return the documented
+status codes without touching a GPU (none of these calls reaches CUDA)."""
+import os
+import re
+
+import pytest
+
+from masked_attention_tri_gb300 import abi, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return abi.load()
+
+
+def _declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s*(tri_attn_[a-z0-9_]+)\s*\(", src,
+                                flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = _declared_functions()
+    assert len(declared) >= 6
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert set(declared) == set(abi.EXPORTS)
+
+
+def test_version_and_error_strings(lib):
+    assert abi.tri_attn_version() >> 16 == 1
+    for code, text in [(0, "ok"), (1, "invalid argument"), (2, "unsupported configuration"), (4, "timed out")]:
+        assert text in abi.tri_attn_error_string(code)
+    assert abi.tri_attn_error_string(99) == "unknown status"
+
+
+# Fake, 16-byte aligned addresses: host checks never dereference them.
+A = 0x10000
+MIS = 0x10008
+
+
+def _fwd(**kw):
+    args = dict(q=A, k=A, v=A, qkv_dtype=abi.TA_BF16, bias=A, bias_dtype=abi.TA_BF16, mask=0, kv_lengths=0, B=1, N=2,
+                H=2, Q=64, K=64, D=64, scale=0.125, out=A, lse=0, max_=0, stream=0)
+    args.update(kw)
+    return lambda: abi.tri_attn_fwd(**args)
+
+
+@pytest.mark.parametrize("kw,exc", [
+    (dict(q=0), ValueError),
+    (dict(bias=0), ValueError),
+    (dict(B=0), ValueError),
+    (dict(K=-1), ValueError),
+    (dict(mask=A, kv_lengths=A), ValueError),  # "pass either mask or kv_lengths, not both"
+    (dict(q=MIS), ValueError),
+    (dict(qkv_dtype=7), ValueError),
+    (dict(bias_dtype=abi.TA_F16), NotImplementedError),  # bias must be fp32 or the q dtype
+    (dict(D=136), NotImplementedError),
+    (dict(D=12), NotImplementedError),  # 16-bit needs D % 8
+    (dict(K=60), NotImplementedError),  # 16-bit needs K % 8
+    (dict(qkv_dtype=abi.TA_F32, bias_dtype=abi.TA_F32, D=6), NotImplementedError),
+])
+def test_triangle_host_checks(lib, kw, exc):
+    with pytest.raises(exc):
+        _fwd(**kw)()
+
+
+def _varlen(**kw):
+    args = dict(q=A, k=A, v=A, dtype=abi.TA_BF16, cu_seqlens_q=A, cu_seqlens_k=A, num_seqs=2, max_seqlen_q=256,
+                max_seqlen_k=256, H=2, D=64, scale=0.125, kv_num_blocks=A, kv_indices=A, full_kv_num_blocks=A,
+                full_kv_indices=A, mask_heads=1, max_q_blocks=2, max_kv_blocks=2, block_q=128, block_k=128,
+                mask_mod=abi.TA_MASK_CAUSAL, out=A, lse=0, max_=0, stream=0)
+    args.update(kw)
+    return lambda: abi.tri_attn_varlen_fwd(**args)
+
+
+@pytest.mark.parametrize("kw,exc", [
+    (dict(cu_seqlens_q=0), ValueError),
+    (dict(num_seqs=0), ValueError),
+    (dict(full_kv_indices=0), ValueError),  # only one of the full_kv_* pair
+    (dict(kv_indices=0), ValueError),
+    (dict(kv_num_blocks=0, kv_indices=0), ValueError),  # full lists without partial lists
+    (dict(mask_heads=3), ValueError),
+    (dict(mask_mod=5), ValueError),
+    (dict(block_q=64), NotImplementedError),
+    (dict(D=256), NotImplementedError),
+])
+def test_varlen_host_checks(lib, kw, exc):
+    with pytest.raises(exc):
+        _varlen(**kw)()
+
+
+def test_varlen_empty_is_noop(lib):
+    _varlen(max_seqlen_q=0)()
+
+
+def test_mask_to_kv_lengths_host_checks(lib):
+    with pytest.raises(ValueError):
+        abi.tri_attn_mask_to_kv_lengths(0, 1, 1, 8, A, 0, 0)
+    with pytest.raises(ValueError):
+        abi.tri_attn_mask_to_kv_lengths(A, 1, 0, 8, A, 0, 0)

@@ -1,0 +1,242 @@
+"""GPU parity: the library against the fp64 oracle on the same seeded inputs.
+
+Tolerances (max-abs): fp32 inputs O 1e-4, lse/max 1e-5; fp16/bf16 inputs
+O 2e-2, lse/max 5e-3.  The named workloads run at full size (the largest one
+is checked on a sample of rows the oracle computes one by one, in the same
+launch configuration the benchmark times); edge cases cover ragged tails,
+every supported head dimension, all-masked rows and kv_lengths extremes.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from parity_helpers import check_triangle, check_varlen, compare, run_triangle, run_varlen
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from masked_attention_tri_gb300 import build
+    build.build()
+
+
+# ---------------------------------------------------------------------------
+# The named workloads
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["tiny_fp32", "fp16_kvlen", "fp16_dense", "fp16_page_example", "bf16_pairstack"])
+def test_workload_full(name):
+    check_triangle(synth.TRIANGLE_WORKLOADS[name]())
+
+
+def test_bf16_long_sampled_rows():
+    c = synth.bf16_long()
+    rng = np.random.default_rng(0)
+    total = c.B * c.N * c.H * c.Q
+    per_n = c.H * c.Q
+    rows = set(rng.choice(total, 3000, replace=False).tolist())
+    # every row of the all-masked slab n=0 and the full-length slab n=1 (first head)
+    rows |= set(range(0, c.Q)) | set(range(per_n, per_n + c.Q))
+    # tile edges of a few other slabs
+    for n in (2, 100, 767):
+        for qi in (0, 127, 128, 255, 256, 511, 512, 767):
+            rows.add(n * per_n + 3 * c.Q + qi)
+    rows = np.array(sorted(rows), dtype=np.int64)
+    check_triangle(c, rows=rows)
+
+
+def test_bf16_varlen_full():
+    check_varlen(synth.bf16_varlen())
+
+
+# ---------------------------------------------------------------------------
+# Edge cases: ragged tiles, head dimensions, kv_lengths extremes
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("D", [8, 16, 24, 32, 48, 64, 96, 128])
+def test_bf16_head_dims_ragged(D):
+    c = synth.make_triangle(f"bf16_D{D}", 1, 3, 2, 200, 136, D, "bf16", "bf16", seed=100 + D, mask="kvlen",
+                            kv_range=(0, 136))
+    c.kv_lengths.view(-1)[:3] = torch.tensor([0, 136, 1000], dtype=torch.int32)
+    check_triangle(c)
+
+
+@pytest.mark.parametrize("D", [8, 32, 64, 128])
+def test_fp16_fp32_bias_no_mask(D):
+    c = synth.make_triangle(f"f16_D{D}", 2, 2, 3, 130, 264, D, "f16", "f32", seed=200 + D)
+    check_triangle(c)
+
+
+@pytest.mark.parametrize("L", [0, 1, 7, 127, 128, 129, 255, 256, 300, 1000, -4])
+def test_kv_length_values(L):
+    c = synth.make_triangle(f"kvlen_{L}", 1, 2, 2, 160, 256, 64, "bf16", "bf16", seed=300, mask="kvlen", kv_const=L)
+    check_triangle(c)
+
+
+def test_dense_mask_special_rows():
+    c = synth.make_triangle("dense_rows", 1, 6, 2, 150, 200, 32, "f16", "f16", seed=301, mask="dense", mask_p=0.3)
+    c.mask[0, 0] = 0                 # all masked -> mean of V
+    c.mask[0, 1] = 0
+    c.mask[0, 1, ..., 199] = 1       # one valid key, in the ragged last tile
+    c.mask[0, 2] = 1                 # all valid
+    c.mask[0, 3, ..., 128:] = 0      # second tile fully masked
+    check_triangle(c)
+
+
+@pytest.mark.parametrize("D", [4, 12, 32, 100, 128])
+def test_fp32_head_dims(D):
+    c = synth.make_triangle(f"f32_D{D}", 1, 2, 2, 45, 70, D, "f32", "f32", seed=400 + D, mask="kvlen",
+                            kv_range=(0, 70))
+    c.kv_lengths.view(-1)[0] = 0
+    check_triangle(c)
+
+
+def test_fp32_dense_mask():
+    c = synth.make_triangle("f32_dense", 2, 3, 2, 33, 65, 16, "f32", "f32", seed=450, mask="dense")
+    c.mask[1, 2] = 0
+    check_triangle(c)
+
+
+def test_single_query_single_key():
+    c = synth.make_triangle("1x8", 1, 1, 1, 1, 8, 8, "bf16", "f32", seed=451)
+    check_triangle(c)
+
+
+def test_large_logits_bias_and_scale():
+    c = synth.make_triangle("large", 1, 2, 2, 128, 128, 64, "bf16", "bf16", seed=452, bias_std=30.0, scale=0.5,
+                            mask="kvlen", kv_range=(1, 128))
+    check_triangle(c)
+
+
+# ---------------------------------------------------------------------------
+# Packed sequences
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("D", [32, 64, 128])
+def test_varlen_causal_ragged(D):
+    c = synth.make_varlen(f"vl_causal_D{D}", 4, 0, 0, 2, D, "bf16", seed=500 + D, lengths=[1, 129, 300, 128])
+    check_varlen(c)
+
+
+def test_varlen_no_lists_full_and_causal():
+    c = synth.make_varlen("vl_none", 3, 0, 0, 2, 64, "f16", seed=510, lengths=[77, 256, 5], block_lists="none",
+                          mask_mod="none")
+    check_varlen(c)
+    c.mask_mod = "causal"
+    check_varlen(c)
+
+
+def test_varlen_fp32():
+    c = synth.make_varlen("vl_f32", 3, 0, 0, 2, 32, "f32", seed=520, lengths=[40, 200, 131])
+    check_varlen(c)
+
+
+def test_varlen_random_lists_and_unlisted_blocks():
+    c = synth.make_varlen("vl_rand", 2, 0, 0, 2, 64, "bf16", seed=530, lengths=[400, 260])
+    g = np.random.default_rng(1)
+    S, MQ = 2, 4
+    kn = torch.zeros(S, 1, MQ, dtype=torch.int32)
+    ki = torch.full((S, 1, MQ, MQ), 77, dtype=torch.int32)
+    fn = torch.zeros(S, 1, MQ, dtype=torch.int32)
+    fi = torch.full((S, 1, MQ, MQ), 77, dtype=torch.int32)
+    for s, L in enumerate([400, 260]):
+        nb = (L + 127) // 128
+        for qb in range(nb):
+            if qb == 1:
+                continue  # q block with no listed kv block: every logit -1e9 -> mean of V
+            perm = g.permutation(nb).tolist()
+            nf = int(g.integers(0, nb + 1))
+            fn[s, 0, qb] = nf
+            fi[s, 0, qb, :nf] = torch.tensor(perm[:nf], dtype=torch.int32)
+            kn[s, 0, qb] = nb - nf
+            ki[s, 0, qb, :nb - nf] = torch.tensor(perm[nf:], dtype=torch.int32)
+    c.kv_num_blocks, c.kv_indices, c.full_kv_num_blocks, c.full_kv_indices = kn, ki, fn, fi
+    check_varlen(c)
+
+
+def test_varlen_per_head_masks():
+    c = synth.make_varlen("vl_heads", 2, 0, 0, 2, 64, "bf16", seed=540, lengths=[256, 200])
+    kn, ki, fn, fi = synth.causal_block_lists([256, 200], mask_heads=2)
+    # head 1: only the diagonal blocks, no full blocks
+    fn[:, 1] = 0
+    c.kv_num_blocks, c.kv_indices, c.full_kv_num_blocks, c.full_kv_indices = kn, ki, fn, fi
+    check_varlen(c)
+
+
+def test_varlen_length_over_max_is_reported():
+    import masked_attention_tri_gb300 as ta
+    c = synth.make_varlen("vl_bad", 2, 0, 0, 1, 32, "bf16", seed=550, lengths=[64, 100], block_lists="none")
+    cu = c.cu_seqlens.cuda()
+    out = ta.varlen_attention(c.q.cuda(), c.k.cuda(), c.v.cuda(), cu, cu, 80, 80, mask_mod="causal")
+    assert ta.get_status() == 5  # TA_ERR_DEVICE: a sequence longer than max_seqlen
+    assert ta.get_status() == 0  # read-and-clear
+    assert torch.isfinite(out[:64].float()).all()
+
+
+# ---------------------------------------------------------------------------
+# mask_to_kv_lengths, the page example flow, robustness
+# ---------------------------------------------------------------------------
+
+def test_mask_to_kv_lengths_matches_oracle():
+    import masked_attention_tri_gb300 as ta
+    g = torch.Generator().manual_seed(9)
+    B, N, K = 2, 50, 200
+    lens = torch.randint(0, K + 1, (B, N), generator=g)
+    m = (torch.arange(K).view(1, 1, K) < lens.view(B, N, 1)).view(B, N, 1, 1, K)
+    m[0, 3, 0, 0, 150] = True   # holey rows
+    m[1, 7, 0, 0, K - 1] = True
+    m[1, 8] = False
+    m[1, 8, 0, 0, 40] = True
+    kl, cnt = ta.mask_to_kv_lengths(m.cuda(), return_nonprefix=True)
+    ref, prefix = oracle.mask_to_kv_lengths(m)
+    assert torch.equal(kl.view(B, N).cpu(), ref)
+    assert int(cnt.item()) == int((~prefix).sum())
+
+
+def test_page_example_flow():
+    """The triangle_attention page's Example: mask -> kv_lengths -> forward, and the dense-mask call."""
+    import masked_attention_tri_gb300 as ta
+    c = synth.fp16_page_example()
+    mask = synth.page_example_kv_lengths(128, 96).cuda()
+    kl = ta.mask_to_kv_lengths(mask)
+    assert kl.shape == (1, 128, 1, 1, 1)
+    assert kl.view(-1).tolist() == [96] * 96 + [0] * 32
+    q, k, v, bias = (x.cuda() for x in (c.q, c.k, c.v, c.bias))
+    out, lse, mx = ta.triangle_attention(q=q, k=k, v=v, bias=bias, scale=c.scale, return_aux=True, kv_lengths=kl)
+    assert out.shape == (1, 128, 2, 128, 32) and out.dtype == torch.float16
+    assert lse.dtype == torch.float32 and mx.dtype == torch.float32
+    dense = (torch.rand(1, 128, 1, 1, 128, generator=torch.Generator().manual_seed(0)) < 0.5).cuda()
+    o2 = ta.triangle_attention(q=q, k=k, v=v, bias=bias, mask=dense, scale=c.scale)
+    rO, _, _ = oracle.tri_fwd(c.q, c.k, c.v, c.bias, mask=dense.cpu(), scale=c.scale)
+    assert np.abs(o2.double().cpu().numpy() - rO).max() <= 2e-2
+    # B=1 four-dimensional forms
+    o4 = ta.triangle_attention(q[0], k[0], v[0], bias[0], scale=c.scale, kv_lengths=kl)
+    assert torch.equal(o4, out[0])
+
+
+def test_deterministic_and_guard_bands():
+    import masked_attention_tri_gb300 as ta
+    c = synth.make_triangle("guard", 1, 4, 2, 200, 264, 64, "bf16", "bf16", seed=600, mask="kvlen", kv_range=(0, 264))
+    q, k, v, bias, kl = (x.cuda() for x in (c.q, c.k, c.v, c.bias, c.kv_lengths))
+    n = q.numel()
+    pad = 4096
+    buf = torch.full((n + 2 * pad,), 12345.0, device="cuda", dtype=torch.bfloat16)
+    out = buf[pad:pad + n].view(q.shape)
+    ta.triangle_attention(q, k, v, bias, scale=c.scale, kv_lengths=kl, out=out)
+    o1 = out.clone()
+    ta.triangle_attention(q, k, v, bias, scale=c.scale, kv_lengths=kl, out=out)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, out)
+    assert (buf[:pad] == 12345.0).all() and (buf[pad + n:] == 12345.0).all()
+
+
+def test_lse_only_outputs_optional():
+    c = synth.make_triangle("noaux", 1, 2, 2, 64, 64, 32, "bf16", "bf16", seed=601)
+    o = run_triangle(c, return_aux=False)
+    O, L, M = run_triangle(c, return_aux=True)
+    assert torch.equal(o, O)
