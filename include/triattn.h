@@ -94,12 +94,14 @@ ta_status tri_attn_fwd(const void* q, const void* k, const void* v, ta_dtype qkv
  *  nn.attention "BlockMask": kv_num_blocks / kv_indices, full_kv_* lists,
  *  BLOCK_SIZE, mask_mod.)
  *
- *   q, out        (total_q, H, D) of `dtype`;  k, v (total_k, H, D)
+ *   q, out        (total_q, H, D) of `dtype`;  k, v (total_k, H, D); total_q and
+ *                 total_k are the row counts of those buffers (the packed
+ *                 "total_seqs" dimension), so no kernel touches a row past them
  *   cu_seqlens_q  (num_seqs + 1) int32, cu_seqlens_q[0] = 0, non-decreasing;
  *   cu_seqlens_k  likewise for keys.  Sequence i holds rows
  *                 [cu[i], cu[i+1]).  Every length must be <= the matching
- *                 max_seqlen (else TA_ERR_DEVICE is recorded and that
- *                 sequence is skipped).
+ *                 max_seqlen and cu[num_seqs] <= the matching total (else
+ *                 TA_ERR_DEVICE is recorded and that sequence is skipped).
  *   kv_num_blocks (num_seqs, mask_heads, max_q_blocks) int32 and
  *   kv_indices    (num_seqs, mask_heads, max_q_blocks, max_kv_blocks) int32:
  *                 partial kv blocks of each 128-row q block, sequence-local
@@ -121,7 +123,8 @@ ta_status tri_attn_fwd(const void* q, const void* k, const void* v, ta_dtype qkv
  */
 ta_status tri_attn_varlen_fwd(const void* q, const void* k, const void* v, ta_dtype dtype,
                               const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
-                              int num_seqs, int max_seqlen_q, int max_seqlen_k, int H, int D,
+                              int num_seqs, int total_q, int total_k,
+                              int max_seqlen_q, int max_seqlen_k, int H, int D,
                               float scale,
                               const int32_t* kv_num_blocks, const int32_t* kv_indices,
                               const int32_t* full_kv_num_blocks, const int32_t* full_kv_indices,

@@ -45,7 +45,7 @@ def load() -> ctypes.CDLL:
         P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
         lib.tri_attn_fwd.argtypes = [P, P, P, I, P, I, P, P, I, I, I, I, I, I, F, P, P, P, P]
         lib.tri_attn_fwd.restype = I
-        lib.tri_attn_varlen_fwd.argtypes = [P, P, P, I, P, P, I, I, I, I, I, F, P, P, P, P, I, I, I, I, I, I,
+        lib.tri_attn_varlen_fwd.argtypes = [P, P, P, I, P, P, I, I, I, I, I, I, I, F, P, P, P, P, I, I, I, I, I, I,
                                             P, P, P, P]
         lib.tri_attn_varlen_fwd.restype = I
         lib.tri_attn_mask_to_kv_lengths.argtypes = [P, I, I, I, P, P, P]
@@ -83,11 +83,11 @@ def tri_attn_fwd(q, k, v, qkv_dtype, bias, bias_dtype, mask, kv_lengths, B, N, H
     _check(st, "tri_attn_fwd")
 
 
-def tri_attn_varlen_fwd(q, k, v, dtype, cu_seqlens_q, cu_seqlens_k, num_seqs, max_seqlen_q, max_seqlen_k, H, D,
-                        scale, kv_num_blocks, kv_indices, full_kv_num_blocks, full_kv_indices, mask_heads,
+def tri_attn_varlen_fwd(q, k, v, dtype, cu_seqlens_q, cu_seqlens_k, num_seqs, total_q, total_k, max_seqlen_q,
+                        max_seqlen_k, H, D, scale, kv_num_blocks, kv_indices, full_kv_num_blocks, full_kv_indices, mask_heads,
                         max_q_blocks, max_kv_blocks, block_q, block_k, mask_mod, out, lse, max_, stream) -> None:
-    st = load().tri_attn_varlen_fwd(q, k, v, dtype, cu_seqlens_q, cu_seqlens_k, num_seqs, max_seqlen_q,
-                                    max_seqlen_k, H, D, float(scale), kv_num_blocks or None, kv_indices or None,
+    st = load().tri_attn_varlen_fwd(q, k, v, dtype, cu_seqlens_q, cu_seqlens_k, num_seqs, total_q, total_k,
+                                    max_seqlen_q, max_seqlen_k, H, D, float(scale), kv_num_blocks or None, kv_indices or None,
                                     full_kv_num_blocks or None, full_kv_indices or None, mask_heads, max_q_blocks,
                                     max_kv_blocks, block_q, block_k, mask_mod, out, lse or None, max_ or None,
                                     stream or None)

@@ -205,6 +205,8 @@ def varlen_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seql
     if q.dim() != 3 or k.dim() != 3 or v.dim() != 3:
         raise ValueError("expected q (total_q,H,D), k/v (total_k,H,D)")
     total_q, H, D = q.shape
+    if tuple(k.shape[1:]) != (H, D) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("k and v must be (total_k, H, D) with q's H and D")
     dev = q.device
     if dev.type != "cuda":
         raise ValueError("varlen_attention runs on CUDA tensors only")
@@ -248,7 +250,7 @@ def varlen_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seql
         mx = torch.empty(H, total_q, device=dev, dtype=torch.float32)
     with torch.cuda.device(dev):
         abi.tri_attn_varlen_fwd(_ptr(q), _ptr(k), _ptr(v), _DT[q.dtype], _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), S,
-                                int(max_seqlen_q), int(max_seqlen_k), H, D, s, _ptr(kn), _ptr(ki), _ptr(fn), _ptr(fi),
+                                total_q, k.shape[0], int(max_seqlen_q), int(max_seqlen_k), H, D, s, _ptr(kn), _ptr(ki), _ptr(fn), _ptr(fi),
                                 mask_heads, MQ, MK, bq, bk, mm, _ptr(out), _ptr(lse), _ptr(mx), _stream(dev))
     return (out, lse, mx) if return_aux else out
 

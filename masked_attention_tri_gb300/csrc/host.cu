@@ -109,7 +109,8 @@ TA_EXPORT ta_status tri_attn_fwd(const void* q, const void* k, const void* v, ta
 
 TA_EXPORT ta_status tri_attn_varlen_fwd(const void* q, const void* k, const void* v, ta_dtype dtype,
                                         const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int num_seqs,
-                                        int max_seqlen_q, int max_seqlen_k, int H, int D, float scale,
+                                        int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int H, int D,
+                                        float scale,
                                         const int32_t* kv_num_blocks, const int32_t* kv_indices,
                                         const int32_t* full_kv_num_blocks, const int32_t* full_kv_indices,
                                         int mask_heads, int max_q_blocks, int max_kv_blocks, int block_q,
@@ -117,6 +118,7 @@ TA_EXPORT ta_status tri_attn_varlen_fwd(const void* q, const void* k, const void
                                         void* stream) {
     if (!q || !k || !v || !out || !cu_seqlens_q || !cu_seqlens_k) return TA_ERR_INVALID_ARG;
     if (num_seqs <= 0 || H <= 0 || D <= 0 || max_seqlen_q < 0 || max_seqlen_k < 0) return TA_ERR_INVALID_ARG;
+    if (total_q < 0 || total_k < 0) return TA_ERR_INVALID_ARG;
     if (!valid_dtype(dtype)) return TA_ERR_INVALID_ARG;
     if (mask_mod != TA_MASK_NONE && mask_mod != TA_MASK_CAUSAL) return TA_ERR_INVALID_ARG;
     if ((kv_num_blocks == nullptr) != (kv_indices == nullptr)) return TA_ERR_INVALID_ARG;
@@ -131,12 +133,10 @@ TA_EXPORT ta_status tri_attn_varlen_fwd(const void* q, const void* k, const void
     if (block_q != 128 || block_k != 128) return TA_ERR_UNSUPPORTED;
     if (!supported_d(dtype, D)) return TA_ERR_UNSUPPORTED;
     if ((long long)num_seqs * H * ((max_seqlen_q + 31) / 32) > 0x7fffffffLL) return TA_ERR_UNSUPPORTED;
-    if (max_seqlen_q == 0) return TA_OK;
+    if (max_seqlen_q == 0 || total_q == 0) return TA_OK;
 
     int* status = triattn::status_word();
     if (!status) return TA_ERR_CUDA;
-    // total_q (the lse/max row stride) is cu_seqlens_q[num_seqs]; the host does
-    // not read device memory, so the kernels take it from the device array.
     AttnParams p{};
     p.q = q;
     p.k = k;
@@ -163,7 +163,8 @@ TA_EXPORT ta_status tri_attn_varlen_fwd(const void* q, const void* k, const void
     p.MQ = kv_num_blocks ? max_q_blocks : 0;
     p.MK = kv_num_blocks ? max_kv_blocks : 0;
     p.mask_mod = mask_mod;
-    p.total_q = -1;
+    p.total_q = total_q;
+    p.total_k = total_k;
     return run(p, static_cast<cudaStream_t>(stream));
 }
 

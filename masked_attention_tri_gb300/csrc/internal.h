@@ -45,7 +45,8 @@ struct AttnParams {
     const int32_t* full_num;
     const int32_t* full_idx;
     int mask_heads, MQ, MK, mask_mod;
-    long long total_q;      // rows of q/out (lse/max stride in varlen)
+    int total_q;            // rows of q/out (lse/max stride in varlen)
+    int total_k;            // rows of k/v
 };
 
 // CUDA-core path: exact fp32 arithmetic, any dtype, both forms.

@@ -210,7 +210,8 @@ __global__ void __launch_bounds__(kWarps * 32) simt_fwd_kernel(const AttnParams 
         const int ck0 = p.cu_k[seq], ck1 = p.cu_k[seq + 1];
         Lq = cq1 - cq0;
         st.Lk = ck1 - ck0;
-        if (Lq > p.max_q || st.Lk > p.max_k || Lq < 0 || st.Lk < 0) {
+        if (Lq > p.max_q || st.Lk > p.max_k || Lq < 0 || st.Lk < 0 || cq0 < 0 || ck0 < 0 || cq1 > p.total_q ||
+            ck1 > p.total_k) {
             if (threadIdx.x == 0 && qt == 0 && h == 0) atomicCAS(p.status, 0, kStatusDevice);
             return;
         }
@@ -218,7 +219,7 @@ __global__ void __launch_bounds__(kWarps * 32) simt_fwd_kernel(const AttnParams 
         q_rs = (long long)p.H * D;
         st.kv_off = (long long)ck0 * p.H * D + (long long)h * D;
         st.kv_rs = (long long)p.H * D;
-        lse_off = (long long)h * p.cu_q[p.num_seqs] + cq0;  // (H, total_q)
+        lse_off = (long long)h * p.total_q + cq0;  // (H, total_q)
     }
     st.q0 = qt * kQT;
     if (st.q0 >= Lq) return;

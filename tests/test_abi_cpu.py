@@ -75,7 +75,7 @@ def test_triangle_host_checks(lib, kw, exc):
 
 
 def _varlen(**kw):
-    args = dict(q=A, k=A, v=A, dtype=abi.TA_BF16, cu_seqlens_q=A, cu_seqlens_k=A, num_seqs=2, max_seqlen_q=256,
+    args = dict(q=A, k=A, v=A, dtype=abi.TA_BF16, cu_seqlens_q=A, cu_seqlens_k=A, num_seqs=2, total_q=400, total_k=400, max_seqlen_q=256,
                 max_seqlen_k=256, H=2, D=64, scale=0.125, kv_num_blocks=A, kv_indices=A, full_kv_num_blocks=A,
                 full_kv_indices=A, mask_heads=1, max_q_blocks=2, max_kv_blocks=2, block_q=128, block_k=128,
                 mask_mod=abi.TA_MASK_CAUSAL, out=A, lse=0, max_=0, stream=0)
@@ -86,6 +86,7 @@ def _varlen(**kw):
 @pytest.mark.parametrize("kw,exc", [
     (dict(cu_seqlens_q=0), ValueError),
     (dict(num_seqs=0), ValueError),
+    (dict(total_k=-1), ValueError),
     (dict(full_kv_indices=0), ValueError),  # only one of the full_kv_* pair
     (dict(kv_indices=0), ValueError),
     (dict(kv_num_blocks=0, kv_indices=0), ValueError),  # full lists without partial lists
