@@ -55,7 +55,7 @@ bool supported_d(int dtype, int D) {
 }
 
 ta_status run(const AttnParams& p, cudaStream_t stream) {
-    cudaError_t e = triattn::launch_simt_fwd(p, stream);
+    cudaError_t e = p.dtype == TA_F32 ? triattn::launch_simt_fwd(p, stream) : triattn::launch_tc_fwd(p, stream);
     return e == cudaSuccess ? TA_OK : TA_ERR_CUDA;
 }
 
