@@ -84,7 +84,7 @@ struct TcParams {
 // ---------------------------------------------------------------------------
 
 struct Layout {
-    uint32_t q, kv, bias, maskw, meanv, bars, tmem_slot, abort_flag, total;
+    uint32_t q, kv, bias, maskw, bars, tmem_slot, abort_flag, total;
     int nbars;
 };
 
@@ -94,8 +94,7 @@ __host__ __device__ inline Layout make_layout(int NQ, const TcParams& P) {
     L.kv = L.q + NQ * P.tile_bytes;
     L.bias = L.kv + P.kv_stages * 2 * P.tile_bytes;
     L.maskw = L.bias + NQ * P.bias_stages * P.bias_bytes;
-    L.meanv = L.maskw + NQ * (P.bias_stages > 0 ? P.bias_stages : 1) * 16;
-    L.bars = L.meanv + NQ * 4 * 128 * 4;  // one D-vector per softmax warp
+    L.bars = L.maskw + NQ * (P.bias_stages > 0 ? P.bias_stages : 1) * 16;
     L.nbars = NQ + 1 + 2 * P.kv_stages + 2 * NQ * P.bias_stages + 3 * NQ + 1;
     L.tmem_slot = L.bars + 8 * L.nbars;
     L.abort_flag = L.tmem_slot + 4;
@@ -594,7 +593,6 @@ __global__ void __launch_bounds__(NQ * 128 + 64, 1) tc_fwd_kernel(const __grid_c
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const uint32_t s_taddr = tmem + lane_off + slot * 128;
         const uint32_t o_taddr = tmem + lane_off + P.o_col0 + slot * P.o_cols;
-        float* wmean = reinterpret_cast<float*>(gbase + L.meanv) + (slot * 4 + wq) * 128;
         uint32_t s_it = 0, bias_it = 0, o_it = 0;
         const float scale = a.scale;
         bool ok = true;
@@ -768,12 +766,17 @@ __global__ void __launch_bounds__(NQ * 128 + 64, 1) tc_fwd_kernel(const __grid_c
             }
             // Rows with no valid key: uniform weights over all keys -> mean of V.
             // Each warp builds the mean once for its rows (lanes split the columns).
+            // Lane l holds the means of columns l, l+32, l+64, l+96.
             const bool any_unseen = __any_sync(0xffffffffu, !seen);
+            float mv[4] = {0.f, 0.f, 0.f, 0.f};
             if (any_unseen && it.Lk > 0) {
                 const long long vrow0 = !a.varlen ? it.unit * a.K : (long long)it.k_row0;
                 const long long vstride = !a.varlen ? a.D : (long long)a.H * a.D;
                 const long long vcol0 = !a.varlen ? 0 : (long long)it.h * a.D;
-                for (int d = lane; d < a.D; d += 32) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int d = lane + 32 * j;
+                    if (d >= a.D) continue;
                     float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
                     int key = 0;
                     for (; key + 4 <= it.Lk; key += 4) {
@@ -783,32 +786,34 @@ __global__ void __launch_bounds__(NQ * 128 + 64, 1) tc_fwd_kernel(const __grid_c
                         s3 += load16<BF16>(a.v, (vrow0 + key + 3) * vstride + vcol0 + d);
                     }
                     for (; key < it.Lk; ++key) s0 += load16<BF16>(a.v, (vrow0 + key) * vstride + vcol0 + d);
-                    wmean[d] = ((s0 + s1) + (s2 + s3)) / (float)it.Lk;
+                    mv[j] = ((s0 + s1) + (s2 + s3)) / (float)it.Lk;
                 }
-                __syncwarp();
             }
             const bool row_ok = qrow < it.Lq;
             const long long orow = !a.varlen ? it.unit * a.Q + qrow : (long long)(it.q_row0 + qrow);
             uint16_t* op = static_cast<uint16_t*>(a.out);
             const long long obase = !a.varlen ? orow * a.D : (orow * a.H + it.h) * a.D;
             const float inv = (seen && l > 0.f) ? 1.f / l : 0.f;
-            for (uint32_t c0 = 0; c0 < P.o_cols; c0 += 16) {
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc) {
+                const uint32_t c0 = cc * 16;
+                if (c0 >= P.o_cols) break;
                 uint32_t o[16];
                 if (jv > 0) tmem_ld_x16(o_taddr + c0, o);
+                float vals[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) vals[e] = __uint_as_float(o[e]) * inv;
+                if (any_unseen) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float m = __shfl_sync(0xffffffffu, mv[(cc * 16 + e) >> 5], (cc * 16 + e) & 31);
+                        if (!seen) vals[e] = m;
+                    }
+                }
                 if (row_ok && (int)c0 < a.D) {
                     uint32_t w[8];
 #pragma unroll
-                    for (int e = 0; e < 16; e += 2) {
-                        float v0, v1;
-                        if (seen) {
-                            v0 = __uint_as_float(o[e]) * inv;
-                            v1 = __uint_as_float(o[e + 1]) * inv;
-                        } else {
-                            v0 = it.Lk > 0 ? wmean[c0 + e] : 0.f;
-                            v1 = it.Lk > 0 ? wmean[c0 + e + 1] : 0.f;
-                        }
-                        w[e / 2] = pack2<BF16>(v0, v1);
-                    }
+                    for (int e = 0; e < 16; e += 2) w[e / 2] = pack2<BF16>(vals[e], vals[e + 1]);
                     uint4* dst = reinterpret_cast<uint4*>(op + obase + c0);
                     dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
                     if ((int)c0 + 8 < a.D) dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
@@ -830,7 +835,6 @@ __global__ void __launch_bounds__(NQ * 128 + 64, 1) tc_fwd_kernel(const __grid_c
                 if (a.lse) a.lse[li] = lse;
                 if (a.mx) a.mx[li] = mx;
             }
-            __syncwarp();  // wmean is rewritten by the next item
         }
         if (!ok) *abort_flag = 1;
     }
@@ -908,7 +912,7 @@ cudaError_t launch_kernel(TcParams& P, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-constexpr size_t kSmemBudget = 232448 - 1024 - 2048;  // 227 KB opt-in, minus alignment slack and barriers
+constexpr size_t kSmemLimit = 232448;  // 227 KB: the per-block opt-in maximum
 
 }  // namespace
 
@@ -963,20 +967,18 @@ cudaError_t launch_tc_fwd(const AttnParams& a, cudaStream_t stream) {
         P.bias_bytes = 0;
         P.bias_boxes = 0;
     }
-    // Pipeline depth: as many stages as fit in shared memory.
-    const size_t fixed = (size_t)NQ * P.tile_bytes + (size_t)NQ * 4 * 128 * 4 + 512;
-    const int prefs[][2] = {{3, 3}, {3, 2}, {2, 2}, {2, 1}, {1, 1}};
+    // Pipeline depth: as many stages as fit in shared memory.  The MMA issues
+    // PV of tile j-1 after waiting for tile j's K/V, so at least two K/V
+    // stages are required.
+    const int prefs[][2] = {{3, 3}, {3, 2}, {2, 2}, {2, 1}};
     P.kv_stages = 0;
     for (auto& pr : prefs) {
-        const int bs = a.varlen ? 0 : pr[1];
-        const size_t need = fixed + (size_t)pr[0] * 2 * P.tile_bytes + (size_t)NQ * bs * (P.bias_bytes + 16);
-        if (need <= kSmemBudget) {
-            P.kv_stages = pr[0];
-            P.bias_stages = bs;
-            break;
-        }
+        P.kv_stages = pr[0];
+        P.bias_stages = a.varlen ? 0 : pr[1];
+        if (make_layout(NQ, P).total + 1024 <= kSmemLimit) break;
+        P.kv_stages = 0;
     }
-    if (P.kv_stages == 0) return cudaErrorInvalidConfiguration;
+    if (P.kv_stages < 2) return cudaErrorInvalidConfiguration;
     P.o_col0 = NQ * 128;
     uint32_t cols = NQ * 128 + NQ * P.o_cols;
     P.tmem_cols = 32;
