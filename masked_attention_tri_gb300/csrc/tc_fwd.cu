@@ -251,6 +251,7 @@ struct Item {
     const int32_t* full_list;
     const int32_t* part_list;
     bool all_blocks;    // varlen without lists
+    bool bad;           // varlen: the sequence breaks the max_seqlen / total contract
     int n_valid;        // entries that name an in-range tile
 };
 
@@ -281,6 +282,7 @@ template <int NQ>
 __device__ Item<NQ> decode(const TcParams& P, int item) {
     Item<NQ> it;
     const AttnParams& a = P.a;
+    it.bad = false;
     it.full_list = nullptr;
     it.part_list = nullptr;
     it.all_blocks = false;
@@ -332,6 +334,7 @@ __device__ Item<NQ> decode(const TcParams& P, int item) {
     it.qt[0] = qt;
     bool ok = it.Lq >= 0 && it.Lk >= 0 && it.Lq <= a.max_q && it.Lk <= a.max_k && cq0 >= 0 && ck0 >= 0 &&
               cq1 <= a.total_q && ck1 <= a.total_k;
+    it.bad = !ok;
     it.slot_on[0] = ok && qt * kBM < it.Lq;
     for (int i = 1; i < NQ; ++i) it.slot_on[i] = false;
     it.n_raw = 0;
@@ -599,6 +602,7 @@ __global__ void __launch_bounds__(NQ * 128 + 64, 1) tc_fwd_kernel(const __grid_c
 
         for (int item = blockIdx.x; item < P.items && ok; item += gridDim.x) {
             const Item<NQ> it = decode<NQ>(P, item);
+            if (it.bad && threadIdx.x == 0) atomicCAS(a.status, 0, kStatusDevice);
             if (!it.slot_on[slot]) continue;
             const int qrow = it.qt[slot] * kBM + r;  // local query row
             float m_true = -INFINITY, m_ref = 0.f, l = 0.f;
