@@ -6,18 +6,22 @@
 // sequences under a tensorplay BlockMask (full_kv_* blocks skip mask_mod).
 //
 // One persistent CTA per SM walks a static list of work items.  A work item
-// is NQ query tiles of 128 rows that share their key/value tiles (triangle
-// form: adjacent q tiles of one (b,n,h) slab).  Warp roles:
+// holds NQ (1 or 2) query tiles of 128 rows that share one stream of key /
+// value tiles: adjacent q tiles of one (b,n,h) slab (triangle form), or
+// adjacent 128-row q blocks of one (sequence, head) (packed form, where each
+// q block visits only the kv blocks its lists name).  Warp roles:
 //   warps 0 .. 4*NQ-1  softmax: warpgroup i owns query tile i, one thread per
-//                      row (= TMEM lane); online softmax in fp32, P written
-//                      back to TMEM as 16-bit, epilogue O / l and lse, max;
+//                      row (= TMEM lane); online softmax in fp32 (packed
+//                      f32x2 arithmetic), P written back to TMEM as 16-bit,
+//                      epilogue O / l, lse, max;
 //   warp 4*NQ          producer: TMA loads of Q, K, V and bias tiles into a
 //                      128B-swizzled shared-memory ring (+ dense-mask bits);
 //   warp 4*NQ+1        MMA: one thread issues tcgen05.mma
-//                      S_i = Q_i K^T (SS, fp32 in TMEM) and O_i += P_i V
-//                      (A = P from TMEM, B = V from shared memory).
+//                      S_i = Q_i K^T (both operands in shared memory, fp32 in
+//                      TMEM) and O_i += P_i V (P from TMEM, V from shared).
 // Tensor memory: S_i at columns [128 i, 128 i + 128), O_i after all S tiles.
-// With NQ = 2 the MMAs of one tile overlap the softmax of the other.
+// With NQ = 2 the MMAs of one tile run while the other tile's softmax does:
+// the tensor core alternates between the two query tiles.
 //
 // Masking: a masked key's logit is replaced by -1e9; a key past the end of
 // its sequence (ragged tail) gets -inf and takes no part.  With kv_lengths,
@@ -37,6 +41,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "internal.h"
@@ -64,9 +69,9 @@ struct TcParams {
     int npv;            // N of the PV MMA (multiple of 16)
     int nqt;            // q tiles per unit (triangle) or per longest sequence (varlen)
     int items;          // work items
-    int items_per_unit; // triangle: ceil(nqt / NQ)
+    int items_per_unit; // ceil(nqt / NQ)
     int kv_stages;
-    int bias_stages;    // 0 for varlen
+    int bias_stages;    // per query tile; 0 for varlen
     int bias_boxes;     // TMA boxes per bias tile
     int bias_box_cols;  // keys per bias box
     uint32_t tile_bytes;
@@ -213,6 +218,20 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+__device__ __forceinline__ uint4 lds128(uint32_t saddr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(saddr));
+    return v;
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     if constexpr (BF16) {
@@ -224,6 +243,16 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     }
 }
 
+// Two 16-bit values of one 32-bit word (low half first) widened to fp32.
+template <bool BF16>
+__device__ __forceinline__ float2 unpack2(uint32_t w) {
+    if constexpr (BF16) {
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    } else {
+        return __half22float2(*reinterpret_cast<const __half2*>(&w));
+    }
+}
+
 template <bool BF16>
 __device__ __forceinline__ float load16(const void* base, long long i) {
     const unsigned short u = static_cast<const unsigned short*>(base)[i];
@@ -232,146 +261,176 @@ __device__ __forceinline__ float load16(const void* base, long long i) {
 }
 
 // ---------------------------------------------------------------------------
-// Work items
+// Work items and their key-tile streams
 // ---------------------------------------------------------------------------
 
 template <int NQ>
 struct Item {
-    bool slot_on[NQ];
-    int qt[NQ];         // q tile per slot
-    long long unit;     // triangle (b*N+n)*H+h
-    int b, n, h, seq;
-    int Lq, Lk;         // query rows / keys of the unit (local)
+    bool on[NQ];        // the query tile has rows
+    int qt[NQ];         // q tile (triangle) / q block (varlen) index per slot
+    long long unit;     // triangle: (b*N+n)*H+h
+    long long bn;       // triangle: b*N+n
+    int b, h, seq;
+    int Lq, Lk;         // query rows / keys of the unit
     int q_row0, k_row0; // varlen: first packed row of the sequence
     int prefix;         // triangle kv_lengths (clamped)
-    long long bn;       // triangle b*N+n
-    // key-tile enumeration: raw entries [0, n_raw)
-    int n_raw;
-    int n_full;         // varlen: leading entries taken from the full list
-    const int32_t* full_list;
-    const int32_t* part_list;
-    bool all_blocks;    // varlen without lists
+    int nkb;            // key blocks that may be visited
     bool bad;           // varlen: the sequence breaks the max_seqlen / total contract
-    int n_valid;        // entries that name an in-range tile
+    bool lists;         // varlen: BlockMask lists given
+    bool any;           // something for the producer / MMA to do
+    const int32_t* full_l[NQ];
+    const int32_t* part_l[NQ];
+    int n_full[NQ];
+    int n_part[NQ];
 };
 
-template <int NQ>
-__device__ bool tile_at(const Item<NQ>& it, const TcParams& P, int t, int& kb, bool& full) {
-    if (!P.a.varlen) {
-        kb = t;
-        full = false;
-        return true;
-    }
-    const int nbk = (it.Lk + kBN - 1) / kBN;
-    if (it.all_blocks) {
-        kb = t;
-        full = false;
-        return t < nbk;
-    }
-    if (t < it.n_full) {
-        kb = it.full_list[t];
-        full = true;
-    } else {
-        kb = it.part_list[t - it.n_full];
-        full = false;
-    }
-    return kb >= 0 && kb < nbk;
-}
-
-template <int NQ>
+template <int NQ, bool VARLEN>
 __device__ Item<NQ> decode(const TcParams& P, int item) {
     Item<NQ> it;
     const AttnParams& a = P.a;
     it.bad = false;
-    it.full_list = nullptr;
-    it.part_list = nullptr;
-    it.all_blocks = false;
-    it.n_full = 0;
+    it.lists = false;
     it.prefix = 0;
     it.seq = 0;
     it.q_row0 = 0;
     it.k_row0 = 0;
-    if (!a.varlen) {
+    for (int i = 0; i < NQ; ++i) {
+        it.full_l[i] = nullptr;
+        it.part_l[i] = nullptr;
+        it.n_full[i] = 0;
+        it.n_part[i] = 0;
+    }
+    if constexpr (!VARLEN) {
         const int qp = item % P.items_per_unit;
-        const int u2 = item / P.items_per_unit;  // ((b*H + h)*N + n): n fastest so bias tiles are reused from L2
-        it.n = u2 % a.N;
+        const int u2 = item / P.items_per_unit;  // ((b*H + h)*N + n): n fastest, so bias tiles are reused from L2
+        const int n = u2 % a.N;
         it.h = (u2 / a.N) % a.H;
         it.b = u2 / (a.N * a.H);
-        it.bn = (long long)it.b * a.N + it.n;
+        it.bn = (long long)it.b * a.N + n;
         it.unit = it.bn * a.H + it.h;
         it.Lq = a.Q;
         it.Lk = a.K;
+        bool any_on = false;
         for (int i = 0; i < NQ; ++i) {
             it.qt[i] = qp * NQ + i;
-            it.slot_on[i] = it.qt[i] < P.nqt;
+            it.on[i] = it.qt[i] < P.nqt;
+            any_on = any_on || it.on[i];
         }
-        int nkt = (a.K + kBN - 1) / kBN;
+        it.nkb = (a.K + kBN - 1) / kBN;
         if (P.mask_kind == 1) {
-            int L = a.kv_len[it.bn];
+            const int L = a.kv_len[it.bn];
             it.prefix = L < 0 ? 0 : (L > a.K ? a.K : L);
-            nkt = (it.prefix + kBN - 1) / kBN;  // 0 when every key is masked
+            it.nkb = (it.prefix + kBN - 1) / kBN;  // 0 when every key is masked
         }
-        it.n_raw = nkt;
-        it.n_valid = nkt;
+        it.any = any_on && it.nkb > 0;
+        return it;
+    } else {
+        // Heaviest q blocks first (a later q block sees more causal kv blocks).
+        const int per = a.num_seqs * a.H;
+        const int qp = P.items_per_unit - 1 - item / per;
+        const int sh = item % per;
+        it.seq = sh / a.H;
+        it.h = sh % a.H;
+        it.b = 0;
+        it.bn = 0;
+        it.unit = 0;
+        const int cq0 = a.cu_q[it.seq], cq1 = a.cu_q[it.seq + 1];
+        const int ck0 = a.cu_k[it.seq], ck1 = a.cu_k[it.seq + 1];
+        it.q_row0 = cq0;
+        it.k_row0 = ck0;
+        it.Lq = cq1 - cq0;
+        it.Lk = ck1 - ck0;
+        const bool ok = it.Lq >= 0 && it.Lk >= 0 && it.Lq <= a.max_q && it.Lk <= a.max_k && cq0 >= 0 && ck0 >= 0 &&
+                        cq1 <= a.total_q && ck1 <= a.total_k;
+        it.bad = !ok;
+        it.nkb = ok ? (it.Lk + kBN - 1) / kBN : 0;
+        it.lists = a.kv_num != nullptr;
+        bool any_on = false;
+        const int hm = a.mask_heads == 1 ? 0 : it.h;
+        for (int i = 0; i < NQ; ++i) {
+            it.qt[i] = qp * NQ + i;
+            it.on[i] = ok && it.qt[i] * kBM < it.Lq;
+            any_on = any_on || it.on[i];
+            if (it.on[i] && it.lists && it.qt[i] < a.MQ) {
+                const long long row = ((long long)it.seq * a.mask_heads + hm) * a.MQ + it.qt[i];
+                it.part_l[i] = a.kv_idx + row * a.MK;
+                it.n_part[i] = min(max(a.kv_num[row], 0), a.MK);
+                if (a.full_num) {
+                    it.full_l[i] = a.full_idx + row * a.MK;
+                    it.n_full[i] = min(max(a.full_num[row], 0), a.MK);
+                }
+            }
+        }
+        it.any = any_on && it.nkb > 0;
         return it;
     }
-    // varlen: heaviest q tiles first (larger q tile index -> more causal blocks)
-    const int per = a.num_seqs * a.H;
-    const int qt = P.nqt - 1 - item / per;
-    const int sh = item % per;
-    it.seq = sh / a.H;
-    it.h = sh % a.H;
-    it.b = 0;
-    it.n = 0;
-    it.bn = 0;
-    it.unit = 0;
-    const int cq0 = a.cu_q[it.seq], cq1 = a.cu_q[it.seq + 1];
-    const int ck0 = a.cu_k[it.seq], ck1 = a.cu_k[it.seq + 1];
-    it.q_row0 = cq0;
-    it.k_row0 = ck0;
-    it.Lq = cq1 - cq0;
-    it.Lk = ck1 - ck0;
-    it.qt[0] = qt;
-    bool ok = it.Lq >= 0 && it.Lk >= 0 && it.Lq <= a.max_q && it.Lk <= a.max_k && cq0 >= 0 && ck0 >= 0 &&
-              cq1 <= a.total_q && ck1 <= a.total_k;
-    it.bad = !ok;
-    it.slot_on[0] = ok && qt * kBM < it.Lq;
-    for (int i = 1; i < NQ; ++i) it.slot_on[i] = false;
-    it.n_raw = 0;
-    it.n_valid = 0;
-    if (!it.slot_on[0]) return it;
-    const int nbk = (it.Lk + kBN - 1) / kBN;
-    if (!a.kv_num) {
-        it.all_blocks = true;
-        it.n_raw = nbk;
-        it.n_valid = nbk;
-        return it;
+}
+
+// Which slots visit key blocks [64w, 64w + 64): `full` blocks skip mask_mod,
+// `part` blocks apply it (triangle: every block of the prefix is `part`; the
+// softmax applies the triangle mask).  Rebuilt from the lists on every window,
+// identically in every role.
+template <int NQ, bool VARLEN>
+__device__ __forceinline__ void window_masks(const Item<NQ>& it, int w, uint64_t (&full)[NQ], uint64_t (&part)[NQ]) {
+    const int lo = 64 * w;
+    const int n = min(64, it.nkb - lo);
+    const uint64_t range = n >= 64 ? ~0ull : ((1ull << n) - 1ull);
+    for (int i = 0; i < NQ; ++i) {
+        full[i] = 0;
+        part[i] = 0;
+        if (!it.on[i]) continue;
+        if (!VARLEN || !it.lists) {
+            part[i] = range;
+            continue;
+        }
+        for (int t = 0; t < it.n_part[i]; ++t) {
+            const int kb = it.part_l[i][t] - lo;
+            if (kb >= 0 && kb < n) part[i] |= 1ull << kb;
+        }
+        for (int t = 0; t < it.n_full[i]; ++t) {
+            const int kb = it.full_l[i][t] - lo;
+            if (kb >= 0 && kb < n) full[i] |= 1ull << kb;
+        }
+        part[i] &= ~full[i];
     }
-    if (qt >= a.MQ) return it;  // q block outside the lists: nothing listed
-    const int hm = a.mask_heads == 1 ? 0 : it.h;
-    const long long row = ((long long)it.seq * a.mask_heads + hm) * a.MQ + qt;
-    if (a.full_num) {
-        it.n_full = min(max(a.full_num[row], 0), a.MK);
-        it.full_list = a.full_idx + row * a.MK;
+}
+
+// Calls f(kb, part_slots, full_slots) for every key block the item visits, in
+// ascending order; bit i of part_slots says query tile i takes part in it,
+// bit i of full_slots that it does so without mask_mod.  Stops when f
+// returns false.  Every role walks the same sequence.
+template <int NQ, bool VARLEN, typename F>
+__device__ __forceinline__ void for_each_tile(const Item<NQ>& it, F&& f) {
+    if constexpr (!VARLEN) {
+        uint32_t on = 0;
+        for (int i = 0; i < NQ; ++i) on |= it.on[i] ? (1u << i) : 0u;
+        for (int kb = 0; kb < it.nkb; ++kb)
+            if (!f(kb, on, 0u)) return;
+    } else {
+        for (int w = 0; w * 64 < it.nkb; ++w) {
+            uint64_t fm[NQ], pm[NQ];
+            window_masks<NQ, VARLEN>(it, w, fm, pm);
+            uint64_t uni = 0;
+            for (int i = 0; i < NQ; ++i) uni |= fm[i] | pm[i];
+            while (uni) {
+                const int bit = __ffsll((long long)uni) - 1;
+                uni &= uni - 1;
+                uint32_t ps = 0, fs = 0;
+                for (int i = 0; i < NQ; ++i) {
+                    ps |= (uint32_t)(((fm[i] | pm[i]) >> bit) & 1ull) << i;
+                    fs |= (uint32_t)((fm[i] >> bit) & 1ull) << i;
+                }
+                if (!f(64 * w + bit, ps, fs)) return;
+            }
+        }
     }
-    const int np = min(max(a.kv_num[row], 0), a.MK);
-    it.part_list = a.kv_idx + row * a.MK;
-    it.n_raw = it.n_full + np;
-    int nv = 0;
-    for (int t = 0; t < it.n_raw; ++t) {
-        int kb;
-        bool full;
-        nv += tile_at(it, P, t, kb, full) ? 1 : 0;
-    }
-    it.n_valid = nv;
-    return it;
 }
 
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
 
-template <int NQ, bool BF16, bool BIAS_F32>
+template <int NQ, bool VARLEN, bool BF16, bool BIAS_F32>
 __global__ void __launch_bounds__(NQ * 128 + 64, 1) tc_fwd_kernel(const __grid_constant__ TcParams P) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -444,21 +503,18 @@ __global__ void __launch_bounds__(NQ * 128 + 64, 1) tc_fwd_kernel(const __grid_c
         uint32_t b_it[NQ];
         for (int i = 0; i < NQ; ++i) b_it[i] = 0;
         bool ok = true;
-        // q_empty completes once per item with work; q_full(i) once per item in which slot i is active.
         for (int item = blockIdx.x; item < P.items && ok; item += gridDim.x) {
-            const Item<NQ> it = decode<NQ>(P, item);
-            bool any = false;
-            for (int i = 0; i < NQ; ++i) any = any || it.slot_on[i];
-            if (!any || it.n_valid == 0) continue;
+            const Item<NQ> it = decode<NQ, VARLEN>(P, item);
+            if (!it.any) continue;
             if (lane == 0 && q_it > 0) ok = wait_bar(q_empty, (q_it - 1) & 1, abort_flag, a.status);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             if (lane == 0) {
                 for (int i = 0; i < NQ; ++i) {
-                    if (!it.slot_on[i]) continue;
+                    if (!it.on[i]) continue;
                     mbar_expect_tx(q_full(i), P.tile_bytes);
                     for (int sb = 0; sb < P.nsub; ++sb) {
-                        if (!a.varlen)
+                        if constexpr (!VARLEN)
                             tma_load_3d(q_smem(i) + sb * kBox, &P.tm_q, sb * 64, it.qt[i] * kBM, (int)it.unit, q_full(i));
                         else
                             tma_load_3d(q_smem(i) + sb * kBox, &P.tm_q, sb * 64, it.h, it.q_row0 + it.qt[i] * kBM,
@@ -467,55 +523,57 @@ __global__ void __launch_bounds__(NQ * 128 + 64, 1) tc_fwd_kernel(const __grid_c
                 }
             }
             ++q_it;
-            for (int t = 0; t < it.n_raw && ok; ++t) {
-                int kb;
-                bool full;
-                if (!tile_at(it, P, t, kb, full)) continue;
+            for_each_tile<NQ, VARLEN>(it, [&](int kb, uint32_t ps, uint32_t) -> bool {
                 const int st = kv_it % S;
-                if (lane == 0 && kv_it >= (uint32_t)S) ok = wait_bar(kv_empty(st), ((kv_it / S) - 1) & 1, abort_flag, a.status);
+                if (lane == 0 && kv_it >= (uint32_t)S)
+                    ok = wait_bar(kv_empty(st), ((kv_it / S) - 1) & 1, abort_flag, a.status);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) break;
+                if (!ok) return false;
                 if (lane == 0) {
                     mbar_expect_tx(kv_full(st), 2 * P.tile_bytes);
                     for (int sb = 0; sb < P.nsub; ++sb) {
-                        if (!a.varlen) {
+                        if constexpr (!VARLEN) {
                             tma_load_3d(k_smem(st) + sb * kBox, &P.tm_k, sb * 64, kb * kBN, (int)it.unit, kv_full(st));
                             tma_load_3d(v_smem(st) + sb * kBox, &P.tm_v, sb * 64, kb * kBN, (int)it.unit, kv_full(st));
                         } else {
-                            tma_load_3d(k_smem(st) + sb * kBox, &P.tm_k, sb * 64, it.h, it.k_row0 + kb * kBN, kv_full(st));
-                            tma_load_3d(v_smem(st) + sb * kBox, &P.tm_v, sb * 64, it.h, it.k_row0 + kb * kBN, kv_full(st));
+                            tma_load_3d(k_smem(st) + sb * kBox, &P.tm_k, sb * 64, it.h, it.k_row0 + kb * kBN,
+                                        kv_full(st));
+                            tma_load_3d(v_smem(st) + sb * kBox, &P.tm_v, sb * 64, it.h, it.k_row0 + kb * kBN,
+                                        kv_full(st));
                         }
                     }
                 }
                 ++kv_it;
-                if (a.varlen) continue;
-                for (int i = 0; i < NQ && ok; ++i) {
-                    if (!it.slot_on[i]) continue;
-                    const int bs = b_it[i] % BS;
-                    if (lane == 0 && b_it[i] >= (uint32_t)BS)
-                        ok = wait_bar(bias_empty(i, bs), ((b_it[i] / BS) - 1) & 1, abort_flag, a.status);
-                    ok = __shfl_sync(0xffffffffu, ok, 0);
-                    if (!ok) break;
-                    if (P.mask_kind == 2) {
-                        // 128 key-validity bits of this tile: word w, bit l <-> key kb*128 + 32w + l
-                        uint32_t* mw = reinterpret_cast<uint32_t*>(gbase + L.maskw + (uint32_t)(i * BS + bs) * 16u);
-                        for (int w = 0; w < 4; ++w) {
-                            const int key = kb * kBN + 32 * w + lane;
-                            const bool v = key < a.K && a.mask[it.bn * a.K + key] != 0;
-                            const uint32_t word = __ballot_sync(0xffffffffu, v);
-                            if (lane == w) mw[w] = word;
+                if constexpr (!VARLEN) {
+                    for (int i = 0; i < NQ; ++i) {
+                        if (!((ps >> i) & 1u)) continue;
+                        const int bs = b_it[i] % BS;
+                        if (lane == 0 && b_it[i] >= (uint32_t)BS)
+                            ok = wait_bar(bias_empty(i, bs), ((b_it[i] / BS) - 1) & 1, abort_flag, a.status);
+                        ok = __shfl_sync(0xffffffffu, ok, 0);
+                        if (!ok) return false;
+                        if (P.mask_kind == 2) {
+                            // 128 key-validity bits: word w, bit l <-> key kb*128 + 32w + l
+                            uint32_t* mw = reinterpret_cast<uint32_t*>(gbase + L.maskw + (uint32_t)(i * BS + bs) * 16u);
+                            for (int ww = 0; ww < 4; ++ww) {
+                                const int key = kb * kBN + 32 * ww + lane;
+                                const bool v = key < a.K && a.mask[it.bn * a.K + key] != 0;
+                                const uint32_t word = __ballot_sync(0xffffffffu, v);
+                                if (lane == ww) mw[ww] = word;
+                            }
+                            __syncwarp();
                         }
-                        __syncwarp();
+                        if (lane == 0) {
+                            mbar_expect_tx(bias_full(i, bs), P.bias_bytes);
+                            for (int bx = 0; bx < P.bias_boxes; ++bx)
+                                tma_load_3d(bias_smem(i, bs) + bx * kBox, &P.tm_bias, kb * kBN + bx * P.bias_box_cols,
+                                            it.qt[i] * kBM, it.b * a.H + it.h, bias_full(i, bs));
+                        }
+                        ++b_it[i];
                     }
-                    if (lane == 0) {
-                        mbar_expect_tx(bias_full(i, bs), P.bias_bytes);
-                        for (int bx = 0; bx < P.bias_boxes; ++bx)
-                            tma_load_3d(bias_smem(i, bs) + bx * kBox, &P.tm_bias, kb * kBN + bx * P.bias_box_cols,
-                                        it.qt[i] * kBM, it.b * a.H + it.h, bias_full(i, bs));
-                    }
-                    ++b_it[i];
                 }
-            }
+                return true;
+            });
         }
         if (!ok) *abort_flag = 1;
     } else if (warp == kMmaWarp) {
@@ -526,61 +584,69 @@ __global__ void __launch_bounds__(NQ * 128 + 64, 1) tc_fwd_kernel(const __grid_c
             for (int i = 0; i < NQ; ++i) p_it[i] = q_it[i] = 0;
             bool ok = true;
             for (int item = blockIdx.x; item < P.items && ok; item += gridDim.x) {
-                const Item<NQ> it = decode<NQ>(P, item);
-                bool any = false;
-                for (int i = 0; i < NQ; ++i) any = any || it.slot_on[i];
-                if (!any || it.n_valid == 0) continue;
+                const Item<NQ> it = decode<NQ, VARLEN>(P, item);
+                if (!it.any) continue;
                 for (int i = 0; i < NQ && ok; ++i)
-                    if (it.slot_on[i]) ok = wait_bar(q_full(i), q_it[i]++ & 1, abort_flag, a.status);
-                int jv = 0, prev = 0;
-                for (int t = 0; t < it.n_raw && ok; ++t) {
-                    int kb;
-                    bool full;
-                    if (!tile_at(it, P, t, kb, full)) continue;
-                    const int st = kv_it % S;
-                    ok = wait_bar(kv_full(st), (kv_it / S) & 1, abort_flag, a.status);
-                    if (!ok) break;
-                    ++kv_it;
-                    tc_fence_after();
-                    for (int i = 0; i < NQ && ok; ++i) {
-                        if (!it.slot_on[i]) continue;
-                        if (jv > 0) {
-                            ok = wait_bar(p_full(i), p_it[i] & 1, abort_flag, a.status);
-                            if (!ok) break;
-                            ++p_it[i];
-                            tc_fence_after();
-                            for (int kk = 0; kk < kBN / 16; ++kk)
-                                mma_ts(tmem + P.o_col0 + i * P.o_cols, tmem + i * 128 + kk * 8,
-                                       sw128_desc(v_smem(prev) + kk * 16 * 128, kBox, 1024), P.idesc_pv,
-                                       (jv > 1 || kk > 0) ? 1u : 0u);
-                        }
-                        for (int kk = 0; kk < P.ksteps; ++kk) {
-                            const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-                            mma_ss(tmem + i * 128, sw128_desc(q_smem(i) + off, 16, 1024),
-                                   sw128_desc(k_smem(st) + off, 16, 1024), P.idesc_qk, kk > 0 ? 1u : 0u);
-                        }
-                        mma_commit(s_full(i));
-                    }
-                    if (!ok) break;
-                    if (jv > 0) mma_commit(kv_empty(prev));
-                    prev = st;
-                    ++jv;
+                    if (it.on[i]) ok = wait_bar(q_full(i), q_it[i]++ & 1, abort_flag, a.status);
+                if (!ok) break;
+                uint32_t pend = 0;  // bit i: P_i of slot i's last tile is still to be multiplied by V
+                int pst[NQ];
+                uint32_t npv[NQ];
+                for (int i = 0; i < NQ; ++i) {
+                    pst[i] = 0;
+                    npv[i] = 0;
                 }
-                for (int i = 0; i < NQ && ok; ++i) {
-                    if (!it.slot_on[i]) continue;
-                    ok = wait_bar(p_full(i), p_it[i] & 1, abort_flag, a.status);
-                    if (!ok) break;
-                    ++p_it[i];
-                    tc_fence_after();
+                int prev = -1;
+                // O_i += P_i V, with V from stage `st` and P_i in S_i's columns.
+                auto issue_pv = [&](int i, int st) {
                     for (int kk = 0; kk < kBN / 16; ++kk)
                         mma_ts(tmem + P.o_col0 + i * P.o_cols, tmem + i * 128 + kk * 8,
-                               sw128_desc(v_smem(prev) + kk * 16 * 128, kBox, 1024), P.idesc_pv,
-                               (jv > 1 || kk > 0) ? 1u : 0u);
-                    mma_commit(o_full(i));
+                               sw128_desc(v_smem(st) + kk * 16 * 128, kBox, 1024), P.idesc_pv,
+                               (npv[i] > 0 || kk > 0) ? 1u : 0u);
+                    ++npv[i];
+                };
+                for_each_tile<NQ, VARLEN>(it, [&](int, uint32_t ps, uint32_t) -> bool {
+                    const int st = kv_it % S;
+                    ok = wait_bar(kv_full(st), (kv_it / S) & 1, abort_flag, a.status);
+                    if (!ok) return false;
+                    ++kv_it;
+                    tc_fence_after();
+                    for (int i = 0; i < NQ; ++i) {
+                        if ((pend >> i) & 1u) {  // PV of this slot's previous tile frees S_i
+                            ok = wait_bar(p_full(i), p_it[i]++ & 1, abort_flag, a.status);
+                            if (!ok) return false;
+                            tc_fence_after();
+                            issue_pv(i, pst[i]);
+                            pend &= ~(1u << i);
+                        }
+                        if ((ps >> i) & 1u) {
+                            for (int kk = 0; kk < P.ksteps; ++kk) {
+                                const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+                                mma_ss(tmem + i * 128, sw128_desc(q_smem(i) + off, 16, 1024),
+                                       sw128_desc(k_smem(st) + off, 16, 1024), P.idesc_qk, kk > 0 ? 1u : 0u);
+                            }
+                            mma_commit(s_full(i));
+                            pend |= 1u << i;
+                            pst[i] = st;
+                        }
+                    }
+                    if (prev >= 0) mma_commit(kv_empty(prev));  // no pending PV reads stage `prev` any more
+                    prev = st;
+                    return true;
+                });
+                if (!ok) break;
+                mma_commit(q_empty);  // every QK of the item is issued: Q tiles may be refilled
+                for (int i = 0; i < NQ && ok; ++i) {
+                    if ((pend >> i) & 1u) {
+                        ok = wait_bar(p_full(i), p_it[i]++ & 1, abort_flag, a.status);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_pv(i, pst[i]);
+                    }
+                    if (npv[i] > 0) mma_commit(o_full(i));
                 }
                 if (!ok) break;
-                mma_commit(kv_empty(prev));
-                mma_commit(q_empty);
+                if (prev >= 0) mma_commit(kv_empty(prev));
             }
             if (!ok) *abort_flag = 1;
             // Let every MMA issued so far finish before TMEM is released.
@@ -588,7 +654,7 @@ __global__ void __launch_bounds__(NQ * 128 + 64, 1) tc_fwd_kernel(const __grid_c
             wait_bar_drain(drain, 0);
         }
         __syncwarp();
-    } else {
+    } else if (warp < 4 * NQ) {
         // -------------------------------------------------------------- softmax
         const int slot = warp / 4;
         const int wq = warp % 4;               // TMEM lane quarter
@@ -596,116 +662,137 @@ __global__ void __launch_bounds__(NQ * 128 + 64, 1) tc_fwd_kernel(const __grid_c
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const uint32_t s_taddr = tmem + lane_off + slot * 128;
         const uint32_t o_taddr = tmem + lane_off + P.o_col0 + slot * P.o_cols;
+        const uint32_t rsw = (uint32_t)(r & 7);  // 128B swizzle: chunk c of row r sits at chunk c ^ (r % 8)
+        const uint32_t rrow = (uint32_t)r * 128u;
         uint32_t s_it = 0, bias_it = 0, o_it = 0;
-        const float scale = a.scale;
+        const float2 scale2 = make_float2(a.scale, a.scale);
+        const float2 log2e2 = make_float2(kLog2e, kLog2e);
         bool ok = true;
 
         for (int item = blockIdx.x; item < P.items && ok; item += gridDim.x) {
-            const Item<NQ> it = decode<NQ>(P, item);
-            if (it.bad && threadIdx.x == 0) atomicCAS(a.status, 0, kStatusDevice);
-            if (!it.slot_on[slot]) continue;
+            const Item<NQ> it = decode<NQ, VARLEN>(P, item);
+            if (VARLEN && it.bad && threadIdx.x == 0) atomicCAS(a.status, 0, kStatusDevice);
+            if (!it.on[slot]) continue;
             const int qrow = it.qt[slot] * kBM + r;  // local query row
             float m_true = -INFINITY, m_ref = 0.f, l = 0.f;
             int jv = 0;
-            for (int t = 0; t < it.n_raw && ok; ++t) {
-                int kb;
-                bool full;
-                if (!tile_at(it, P, t, kb, full)) continue;
+            for_each_tile<NQ, VARLEN>(it, [&](int kb, uint32_t ps, uint32_t fs) -> bool {
+                if (!((ps >> slot) & 1u)) return true;
+                const bool full = (fs >> slot) & 1u;
+                const int key0 = kb * kBN;
                 ok = __all_sync(0xffffffffu, wait_bar(s_full(slot), s_it & 1, abort_flag, a.status));
-                if (!ok) break;
+                if (!ok) return false;
                 ++s_it;
                 tc_fence_after();
-                uint32_t sr[128];
-                tmem_ld_x128(s_taddr, sr);
-                float x[128];
-                const int key0 = kb * kBN;
-                // Which keys exist / are valid in this tile.
-                bool all_valid;
-                int vlim;  // keys < vlim are valid in the prefix / no-mask / full cases
-                if (!a.varlen) {
+
+                // ---- pass 1: logits x = s * S + bias (triangle) or s * S (varlen), masking,
+                // row max; x goes back into S's TMEM columns (fp32), 32 keys at a time.
+                // Per 32-key chunk: vm bit j = key key0+32c+j is valid, em bit j = it exists.
+                int vlim;
+                bool causal = false;
+                if constexpr (!VARLEN) {
                     vlim = P.mask_kind == 1 ? it.prefix : a.K;
-                    all_valid = P.mask_kind != 2 && key0 + kBN <= vlim;
                 } else {
                     vlim = it.Lk;
-                    const bool causal = !full && a.mask_mod == TA_MASK_CAUSAL;
-                    all_valid = key0 + kBN <= it.Lk && (!causal || key0 + kBN - 1 <= it.qt[0] * kBM);
+                    causal = !full && a.mask_mod == TA_MASK_CAUSAL;
                 }
-                if (!a.varlen) {
-                    const int bs = bias_it % BS;
+                const bool all_valid = (VARLEN || P.mask_kind != 2) && key0 + kBN <= vlim &&
+                                       (!causal || key0 + kBN - 1 <= it.qt[slot] * kBM);
+                const int nexist = (VARLEN ? it.Lk : a.K) - key0;
+                uint32_t brow = 0, mwbase = 0;
+                int bs = 0;
+                if constexpr (!VARLEN) {
+                    bs = bias_it % BS;
                     ok = __all_sync(0xffffffffu, wait_bar(bias_full(slot, bs), (bias_it / BS) & 1, abort_flag, a.status));
-                    if (!ok) break;
-                    const uint8_t* bt = gbase + (bias_smem(slot, bs) - base);
-                    const uint32_t sw = (uint32_t)(r & 7);
-                    uint32_t mwords[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
-                    if (P.mask_kind == 2) {
-                        const uint4 mw = *reinterpret_cast<const uint4*>(gbase + L.maskw + (uint32_t)(slot * BS + bs) * 16u);
-                        mwords[0] = mw.x;
-                        mwords[1] = mw.y;
-                        mwords[2] = mw.z;
-                        mwords[3] = mw.w;
-                    }
-                    if constexpr (!BIAS_F32) {
+                    if (!ok) return false;
+                    brow = bias_smem(slot, bs) + rrow;
+                    mwbase = base + L.maskw + (uint32_t)(slot * BS + bs) * 16u;
+                }
+                float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t sr[32];
+                    tmem_ld_x32(s_taddr + 32 * c, sr);
+                    float x[32];
+                    if constexpr (VARLEN) {
 #pragma unroll
-                        for (int g = 0; g < 16; ++g) {  // 8 keys per 16-byte chunk
-                            const uint32_t sub = g >> 3, ch = g & 7;
-                            const uint4 w = *reinterpret_cast<const uint4*>(bt + sub * kBox + r * 128 + ((ch ^ sw) << 4));
-                            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+                        for (int j = 0; j < 32; j += 2) {
+                            const float2 r2 =
+                                __fmul2_rn(make_float2(__uint_as_float(sr[j]), __uint_as_float(sr[j + 1])), scale2);
+                            x[j] = r2.x;
+                            x[j + 1] = r2.y;
+                        }
+                    } else if constexpr (!BIAS_F32) {
+#pragma unroll
+                        for (int g = 0; g < 4; ++g) {  // 8 keys per 16-byte chunk
+                            const uint32_t col8 = 4 * c + g;
+                            const uint4 wv = lds128(brow + (col8 >> 3) * kBox + (((col8 & 7) ^ rsw) << 4));
+                            const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
-                                float b0, b1;
-                                if constexpr (BF16) {
-                                    b0 = __uint_as_float(ww[e] << 16);
-                                    b1 = __uint_as_float(ww[e] & 0xffff0000u);
-                                } else {
-                                    b0 = __half2float(__ushort_as_half((unsigned short)(ww[e] & 0xffffu)));
-                                    b1 = __half2float(__ushort_as_half((unsigned short)(ww[e] >> 16)));
-                                }
-                                x[g * 8 + 2 * e] = fmaf(__uint_as_float(sr[g * 8 + 2 * e]), scale, b0);
-                                x[g * 8 + 2 * e + 1] = fmaf(__uint_as_float(sr[g * 8 + 2 * e + 1]), scale, b1);
+                                const float2 b2 = unpack2<BF16>(ww[e]);
+                                const int j = 8 * g + 2 * e;
+                                const float2 r2 = __ffma2_rn(
+                                    make_float2(__uint_as_float(sr[j]), __uint_as_float(sr[j + 1])), scale2, b2);
+                                x[j] = r2.x;
+                                x[j + 1] = r2.y;
                             }
                         }
                     } else {
 #pragma unroll
-                        for (int g = 0; g < 32; ++g) {  // 4 keys per 16-byte chunk
-                            const uint32_t sub = g >> 3, ch = g & 7;
-                            const float4 w = *reinterpret_cast<const float4*>(bt + sub * kBox + r * 128 + ((ch ^ sw) << 4));
-                            x[g * 4 + 0] = fmaf(__uint_as_float(sr[g * 4 + 0]), scale, w.x);
-                            x[g * 4 + 1] = fmaf(__uint_as_float(sr[g * 4 + 1]), scale, w.y);
-                            x[g * 4 + 2] = fmaf(__uint_as_float(sr[g * 4 + 2]), scale, w.z);
-                            x[g * 4 + 3] = fmaf(__uint_as_float(sr[g * 4 + 3]), scale, w.w);
+                        for (int g = 0; g < 8; ++g) {  // 4 keys per 16-byte chunk
+                            const uint32_t col4 = 8 * c + g;
+                            const uint4 wv = lds128(brow + (col4 >> 3) * kBox + (((col4 & 7) ^ rsw) << 4));
+                            const int j = 4 * g;
+                            const float2 r0 = __ffma2_rn(make_float2(__uint_as_float(sr[j]), __uint_as_float(sr[j + 1])),
+                                                         scale2, make_float2(__uint_as_float(wv.x), __uint_as_float(wv.y)));
+                            const float2 r1 =
+                                __ffma2_rn(make_float2(__uint_as_float(sr[j + 2]), __uint_as_float(sr[j + 3])), scale2,
+                                           make_float2(__uint_as_float(wv.z), __uint_as_float(wv.w)));
+                            x[j] = r0.x;
+                            x[j + 1] = r0.y;
+                            x[j + 2] = r1.x;
+                            x[j + 3] = r1.y;
                         }
                     }
+                    if (!all_valid) {
+                        auto low_bits = [](int n) -> uint32_t {
+                            return n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : ((1u << n) - 1u));
+                        };
+                        const int k0 = 32 * c;
+                        const uint32_t em = low_bits(nexist - k0);
+                        uint32_t vm = em & low_bits(vlim - key0 - k0);
+                        if constexpr (!VARLEN) {
+                            if (P.mask_kind == 2) {
+                                uint32_t word;
+                                asm volatile("ld.shared.u32 %0, [%1];" : "=r"(word) : "r"(mwbase + (uint32_t)c * 4u));
+                                vm &= word;
+                            }
+                        } else {
+                            if (causal) vm &= low_bits(qrow - key0 - k0 + 1);
+                        }
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            x[j] = ((vm >> j) & 1u) ? x[j] : (((em >> j) & 1u) ? kMasked : -INFINITY);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 32; j += 8) {
+                        m0 = max3(m0, x[j], x[j + 1]);
+                        m1 = max3(m1, x[j + 2], x[j + 3]);
+                        m2 = max3(m2, x[j + 4], x[j + 5]);
+                        m3 = max3(m3, x[j + 6], x[j + 7]);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) sr[j] = __float_as_uint(x[j]);
+                    tmem_st_x32(s_taddr + 32 * c, sr);
+                }
+                if constexpr (!VARLEN) {
                     mbar_arrive(bias_empty(slot, bs));
                     ++bias_it;
-                    if (!all_valid) {
-#pragma unroll
-                        for (int c = 0; c < 128; ++c) {
-                            const int key = key0 + c;
-                            const bool exists = key < a.K;
-                            const bool valid = exists && key < vlim && ((mwords[c >> 5] >> (c & 31)) & 1u);
-                            x[c] = valid ? x[c] : (exists ? kMasked : -INFINITY);
-                        }
-                    }
-                } else {
-                    const bool causal = !full && a.mask_mod == TA_MASK_CAUSAL;
-#pragma unroll
-                    for (int c = 0; c < 128; ++c) {
-                        const float v = __uint_as_float(sr[c]) * scale;
-                        if (all_valid) {
-                            x[c] = v;
-                        } else {
-                            const int key = key0 + c;
-                            const bool exists = key < it.Lk;
-                            const bool valid = exists && (!causal || key <= qrow);
-                            x[c] = valid ? v : (exists ? kMasked : -INFINITY);
-                        }
-                    }
                 }
-                // Row max of this tile.
-                float mt = x[0];
-#pragma unroll
-                for (int c = 1; c < 128; ++c) mt = fmaxf(mt, x[c]);
-                const float m_new = fmaxf(m_true, mt);
+                tmem_st_wait();  // the logits must be in TMEM before pass 2 reads them back
+
+                const float m_new = fmaxf(m_true, fmaxf(max3(m0, m1, m2), m3));
                 m_true = m_new;
                 if (jv == 0) {
                     m_ref = m_new;
@@ -713,8 +800,8 @@ __global__ void __launch_bounds__(NQ * 128 + 64, 1) tc_fwd_kernel(const __grid_c
                 } else {
                     const bool need = (m_new - m_ref) * kLog2e > kRescaleLog2;
                     if (__any_sync(0xffffffffu, need)) {
-                        // Raise the reference max to the current max; O (complete
-                        // through the previous tile) and l scale by 2^((m_ref-m_new) log2 e).
+                        // Raise the reference max to the current one; O (complete
+                        // through this slot's previous tile) and l scale by 2^((m_ref-m_new) log2 e).
                         const float alpha = ex2((m_ref - m_new) * kLog2e);
                         l *= alpha;
                         m_ref = m_new;
@@ -727,35 +814,47 @@ __global__ void __launch_bounds__(NQ * 128 + 64, 1) tc_fwd_kernel(const __grid_c
                         }
                     }
                 }
-                uint32_t pk[64];
-                float lsum = 0.f;
-                if (m_ref > kMasked) {
-                    const float nb = -m_ref * kLog2e;
+
+                // ---- pass 2: P = 2^((x - m_ref) log2 e), row sum, P -> TMEM as 16-bit
+                // pairs (P chunk c lands in columns [16c, 16c+16), below unread logits).
+                float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+                const bool live = m_ref > kMasked;
+                const float2 nb2 = make_float2(-m_ref * kLog2e, -m_ref * kLog2e);
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t xr[32];
+                    tmem_ld_x32(s_taddr + 32 * c, xr);
+                    uint32_t pk[16];
+                    if (live) {
 #pragma unroll
-                    for (int c = 0; c < 128; c += 2) {
-                        const float p0 = ex2(fmaf(x[c], kLog2e, nb));
-                        const float p1 = ex2(fmaf(x[c + 1], kLog2e, nb));
-                        lsum += p0 + p1;
-                        pk[c / 2] = pack2<BF16>(p0, p1);
-                    }
-                } else {
-                    // No valid key seen yet (every logit so far is -1e9): the
-                    // weights are exactly 1 for masked keys and 0 for absent ones.
+                        for (int j = 0; j < 16; ++j) {
+                            const float2 y = __ffma2_rn(
+                                make_float2(__uint_as_float(xr[2 * j]), __uint_as_float(xr[2 * j + 1])), log2e2, nb2);
+                            const float2 p = make_float2(ex2(y.x), ex2(y.y));
+                            if (j & 1) acc1 = __fadd2_rn(acc1, p);
+                            else acc0 = __fadd2_rn(acc0, p);
+                            pk[j] = pack2<BF16>(p.x, p.y);
+                        }
+                    } else {
+                        // No valid key seen yet (every logit so far is -1e9): the
+                        // weights are exactly 1 for masked keys and 0 for absent ones.
 #pragma unroll
-                    for (int c = 0; c < 128; c += 2) {
-                        const float p0 = x[c] == kMasked ? 1.f : 0.f;
-                        const float p1 = x[c + 1] == kMasked ? 1.f : 0.f;
-                        lsum += p0 + p1;
-                        pk[c / 2] = pack2<BF16>(p0, p1);
+                        for (int j = 0; j < 16; ++j) {
+                            const float2 p = make_float2(__uint_as_float(xr[2 * j]) == kMasked ? 1.f : 0.f,
+                                                         __uint_as_float(xr[2 * j + 1]) == kMasked ? 1.f : 0.f);
+                            acc0 = __fadd2_rn(acc0, p);
+                            pk[j] = pack2<BF16>(p.x, p.y);
+                        }
                     }
+                    tmem_st_x16(s_taddr + 16 * c, pk);
                 }
-                l += lsum;
-                tmem_st_x64(s_taddr, pk);
+                l += (acc0.x + acc0.y) + (acc1.x + acc1.y);
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(p_full(slot));
                 ++jv;
-            }
+                return true;
+            });
             if (!ok) break;
 
             // ------------------------------------------------------- epilogue
@@ -769,14 +868,13 @@ __global__ void __launch_bounds__(NQ * 128 + 64, 1) tc_fwd_kernel(const __grid_c
                 seen = false;
             }
             // Rows with no valid key: uniform weights over all keys -> mean of V.
-            // Each warp builds the mean once for its rows (lanes split the columns).
             // Lane l holds the means of columns l, l+32, l+64, l+96.
             const bool any_unseen = __any_sync(0xffffffffu, !seen);
             float mv[4] = {0.f, 0.f, 0.f, 0.f};
             if (any_unseen && it.Lk > 0) {
-                const long long vrow0 = !a.varlen ? it.unit * a.K : (long long)it.k_row0;
-                const long long vstride = !a.varlen ? a.D : (long long)a.H * a.D;
-                const long long vcol0 = !a.varlen ? 0 : (long long)it.h * a.D;
+                const long long vrow0 = !VARLEN ? it.unit * a.K : (long long)it.k_row0;
+                const long long vstride = !VARLEN ? a.D : (long long)a.H * a.D;
+                const long long vcol0 = !VARLEN ? 0 : (long long)it.h * a.D;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int d = lane + 32 * j;
@@ -794,9 +892,9 @@ __global__ void __launch_bounds__(NQ * 128 + 64, 1) tc_fwd_kernel(const __grid_c
                 }
             }
             const bool row_ok = qrow < it.Lq;
-            const long long orow = !a.varlen ? it.unit * a.Q + qrow : (long long)(it.q_row0 + qrow);
+            const long long orow = !VARLEN ? it.unit * a.Q + qrow : (long long)(it.q_row0 + qrow);
             uint16_t* op = static_cast<uint16_t*>(a.out);
-            const long long obase = !a.varlen ? orow * a.D : (orow * a.H + it.h) * a.D;
+            const long long obase = !VARLEN ? orow * a.D : (orow * a.H + it.h) * a.D;
             const float inv = (seen && l > 0.f) ? 1.f / l : 0.f;
 #pragma unroll
             for (int cc = 0; cc < 8; ++cc) {
@@ -815,12 +913,12 @@ __global__ void __launch_bounds__(NQ * 128 + 64, 1) tc_fwd_kernel(const __grid_c
                     }
                 }
                 if (row_ok && (int)c0 < a.D) {
-                    uint32_t w[8];
+                    uint32_t wv[8];
 #pragma unroll
-                    for (int e = 0; e < 16; e += 2) w[e / 2] = pack2<BF16>(vals[e], vals[e + 1]);
+                    for (int e = 0; e < 16; e += 2) wv[e / 2] = pack2<BF16>(vals[e], vals[e + 1]);
                     uint4* dst = reinterpret_cast<uint4*>(op + obase + c0);
-                    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                    if ((int)c0 + 8 < a.D) dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    dst[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                    if ((int)c0 + 8 < a.D) dst[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
                 }
             }
             if (row_ok) {
@@ -835,7 +933,7 @@ __global__ void __launch_bounds__(NQ * 128 + 64, 1) tc_fwd_kernel(const __grid_c
                     lse = m_ref + logf(l);
                     mx = m_true;
                 }
-                const long long li = !a.varlen ? orow : (long long)it.h * a.total_q + orow;
+                const long long li = !VARLEN ? orow : (long long)it.h * a.total_q + orow;
                 if (a.lse) a.lse[li] = lse;
                 if (a.mx) a.mx[li] = mx;
             }
@@ -899,11 +997,11 @@ uint32_t make_idesc(bool bf16, int M, int N, bool b_mn_major) {
            ((uint32_t)(M >> 4) << 24);
 }
 
-template <int NQ, bool BF16, bool BIAS_F32>
+template <int NQ, bool VARLEN, bool BF16, bool BIAS_F32>
 cudaError_t launch_kernel(TcParams& P, cudaStream_t stream) {
     const Layout L = make_layout(NQ, P);
     const size_t smem = L.total + 1024;
-    auto kern = tc_fwd_kernel<NQ, BF16, BIAS_F32>;
+    auto kern = tc_fwd_kernel<NQ, VARLEN, BF16, BIAS_F32>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     int dev = 0;
@@ -916,7 +1014,40 @@ cudaError_t launch_kernel(TcParams& P, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+template <bool VARLEN, bool BF16, bool BIAS_F32>
+cudaError_t launch_nq(int NQ, TcParams& P, cudaStream_t stream) {
+    return NQ == 2 ? launch_kernel<2, VARLEN, BF16, BIAS_F32>(P, stream)
+                   : launch_kernel<1, VARLEN, BF16, BIAS_F32>(P, stream);
+}
+
 constexpr size_t kSmemLimit = 232448;  // 227 KB: the per-block opt-in maximum
+
+// Pick NQ and the pipeline depths: two query tiles per CTA when they fit next
+// to two K/V stages and one bias stage per tile, else one.  The MMA issues PV
+// of a tile after waiting for the next tile's K/V, so two K/V stages are the
+// minimum.
+bool choose_geometry(TcParams& P, bool varlen, int& NQ) {
+    const int prefs2[][2] = {{3, 2}, {2, 2}, {2, 1}};
+    const int prefs1[][2] = {{3, 3}, {3, 2}, {2, 2}, {2, 1}};
+    for (int nq = 2; nq >= 1; --nq) {
+        const int n = nq == 2 ? 3 : 4;
+        for (int i = 0; i < n; ++i) {
+            const int* pr = nq == 2 ? prefs2[i] : prefs1[i];
+            P.kv_stages = pr[0];
+            P.bias_stages = varlen ? 0 : pr[1];
+            const uint32_t cols = nq * 128 + nq * P.o_cols;
+            if (cols > 512) continue;
+            if (make_layout(nq, P).total + 1024 <= kSmemLimit) {
+                NQ = nq;
+                P.o_col0 = nq * 128;
+                P.tmem_cols = 32;
+                while (P.tmem_cols < cols) P.tmem_cols <<= 1;
+                return true;
+            }
+        }
+    }
+    return false;
+}
 
 }  // namespace
 
@@ -936,65 +1067,39 @@ cudaError_t launch_tc_fwd(const AttnParams& a, cudaStream_t stream) {
     P.idesc_qk = make_idesc(bf16, 128, 128, false);
     P.idesc_pv = make_idesc(bf16, 128, P.npv, true);
     const uint64_t rs = (uint64_t)D * 2;
-    int NQ;
     if (!a.varlen) {
-        NQ = 1;
-        P.nqt = (a.Q + kBM - 1) / kBM;
-        P.items_per_unit = (P.nqt + NQ - 1) / NQ;
-        const long long items = (long long)a.B * a.N * a.H * P.items_per_unit;
-        if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-        P.items = (int)items;
-        const uint64_t units = (uint64_t)a.B * a.N * a.H;
-        if (!make_map(&P.tm_q, dt, a.q, D, a.Q, units, rs, rs * a.Q, 64, kBM, 1) ||
-            !make_map(&P.tm_k, dt, a.k, D, a.K, units, rs, rs * a.K, 64, kBN, 1) ||
-            !make_map(&P.tm_v, dt, a.v, D, a.K, units, rs, rs * a.K, 64, kBN, 1))
-            return cudaErrorInvalidValue;
         const uint64_t eb = a.bias_f32 ? 4 : 2;
         P.bias_box_cols = a.bias_f32 ? 32 : 64;
         P.bias_boxes = kBN / P.bias_box_cols;
         P.bias_bytes = P.bias_boxes * kBox;
-        if (!make_map(&P.tm_bias, a.bias_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : dt, a.bias, a.K, a.Q,
+        P.mask_kind = a.kv_len ? 1 : (a.mask ? 2 : 0);
+        const uint64_t units = (uint64_t)a.B * a.N * a.H;
+        if (!make_map(&P.tm_q, dt, a.q, D, a.Q, units, rs, rs * a.Q, 64, kBM, 1) ||
+            !make_map(&P.tm_k, dt, a.k, D, a.K, units, rs, rs * a.K, 64, kBN, 1) ||
+            !make_map(&P.tm_v, dt, a.v, D, a.K, units, rs, rs * a.K, 64, kBN, 1) ||
+            !make_map(&P.tm_bias, a.bias_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : dt, a.bias, a.K, a.Q,
                       (uint64_t)a.B * a.H, a.K * eb, a.K * eb * a.Q, P.bias_box_cols, kBM, 1))
             return cudaErrorInvalidValue;
-        P.mask_kind = a.kv_len ? 1 : (a.mask ? 2 : 0);
+        P.nqt = (a.Q + kBM - 1) / kBM;
     } else {
-        NQ = 1;
-        P.nqt = (a.max_q + kBM - 1) / kBM;
-        const long long items = (long long)a.num_seqs * a.H * P.nqt;
-        if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-        P.items = (int)items;
-        P.items_per_unit = 1;
+        const uint64_t tk = a.total_k > 0 ? a.total_k : 1;
         if (!make_map(&P.tm_q, dt, a.q, D, a.H, a.total_q, rs, rs * a.H, 64, 1, kBM) ||
-            !make_map(&P.tm_k, dt, a.k, D, a.H, (a.total_k > 0 ? a.total_k : 1), rs, rs * a.H, 64, 1, kBN) ||
-            !make_map(&P.tm_v, dt, a.v, D, a.H, (a.total_k > 0 ? a.total_k : 1), rs, rs * a.H, 64, 1, kBN))
+            !make_map(&P.tm_k, dt, a.k, D, a.H, tk, rs, rs * a.H, 64, 1, kBN) ||
+            !make_map(&P.tm_v, dt, a.v, D, a.H, tk, rs, rs * a.H, 64, 1, kBN))
             return cudaErrorInvalidValue;
-        P.bias_bytes = 0;
-        P.bias_boxes = 0;
+        P.nqt = (a.max_q + kBM - 1) / kBM;
     }
-    // Pipeline depth: as many stages as fit in shared memory.  The MMA issues
-    // PV of tile j-1 after waiting for tile j's K/V, so at least two K/V
-    // stages are required.
-    const int prefs[][2] = {{3, 3}, {3, 2}, {2, 2}, {2, 1}};
-    P.kv_stages = 0;
-    for (auto& pr : prefs) {
-        P.kv_stages = pr[0];
-        P.bias_stages = a.varlen ? 0 : pr[1];
-        if (make_layout(NQ, P).total + 1024 <= kSmemLimit) break;
-        P.kv_stages = 0;
-    }
-    if (P.kv_stages < 2) return cudaErrorInvalidConfiguration;
-    P.o_col0 = NQ * 128;
-    uint32_t cols = NQ * 128 + NQ * P.o_cols;
-    P.tmem_cols = 32;
-    while (P.tmem_cols < cols) P.tmem_cols <<= 1;
-    if (P.tmem_cols > 512) return cudaErrorInvalidConfiguration;
+    int NQ = 1;
+    if (!choose_geometry(P, a.varlen != 0, NQ)) return cudaErrorInvalidConfiguration;
+    P.items_per_unit = (P.nqt + NQ - 1) / NQ;
+    const long long units = !a.varlen ? (long long)a.B * a.N * a.H : (long long)a.num_seqs * a.H;
+    const long long items = units * P.items_per_unit;
+    if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    P.items = (int)items;
 
-    if (bf16) {
-        if (a.varlen || !a.bias_f32) return launch_kernel<1, true, false>(P, stream);
-        return launch_kernel<1, true, true>(P, stream);
-    }
-    if (a.varlen || !a.bias_f32) return launch_kernel<1, false, false>(P, stream);
-    return launch_kernel<1, false, true>(P, stream);
+    if (a.varlen) return bf16 ? launch_nq<true, true, false>(NQ, P, stream) : launch_nq<true, false, false>(NQ, P, stream);
+    if (bf16) return a.bias_f32 ? launch_nq<false, true, true>(NQ, P, stream) : launch_nq<false, true, false>(NQ, P, stream);
+    return a.bias_f32 ? launch_nq<false, false, true>(NQ, P, stream) : launch_nq<false, false, false>(NQ, P, stream);
 }
 
 }  // namespace triattn
