@@ -1,7 +1,7 @@
 // tc_fwd.cu -- host side of the tcgen05 forward: TMA descriptors, geometry
 // (query tiles per CTA, pipeline depths, tensor-memory columns), the choice
-// between the folded softmax (bias added by the tensor core) and the plain
-// one, and the launch.  The kernel itself is in tc_kernel.cuh.
+// of the folded softmax for the packed form, and the launch.  The kernel
+// itself is in tc_kernel.cuh.
 
 #include <cudaTypedefs.h>
 
@@ -93,19 +93,6 @@ bool choose_geometry(TcParams& P, bool varlen, int& NQ) {
     return false;
 }
 
-// 1/s as a 16-bit pattern when s is a power of two whose inverse is a normal
-// number of the dtype (then bias * (1/s) is exact and the bias can be added by
-// the tensor core); 0 otherwise.
-uint32_t inverse_pow2_bits(float scale, bool bf16) {
-    if (!(scale > 0.f) || !std::isfinite(scale)) return 0;
-    int e = 0;
-    const float m = std::frexp(scale, &e);  // scale = m * 2^e, m in [0.5, 1)
-    if (m != 0.5f) return 0;
-    const int k = 1 - e;  // 1/scale = 2^k
-    if (bf16) return (k >= -126 && k <= 127) ? (uint32_t)(k + 127) << 7 : 0u;
-    return (k >= -14 && k <= 15) ? (uint32_t)(k + 15) << 10 : 0u;
-}
-
 template <bool VARLEN, bool BF16, bool BIAS_F32, bool FOLD>
 cudaError_t launch_nq(int NQ, const TcParams& P, int grid, cudaStream_t stream) {
     if constexpr (VARLEN) {
@@ -135,7 +122,6 @@ cudaError_t launch_tc_fwd(const AttnParams& a, cudaStream_t stream) {
     P.tile_bytes = P.nsub * kBox;
     P.idesc_qk = make_idesc(bf16, 128, 128, false);
     P.idesc_pv = make_idesc(bf16, 128, P.npv, true);
-    P.idesc_id = make_idesc(bf16, 128, 16, false);
     P.scale_log2e = a.scale * kLog2e;
     const uint64_t rs = (uint64_t)D * 2;
     bool fold;
@@ -153,9 +139,7 @@ cudaError_t launch_tc_fwd(const AttnParams& a, cudaStream_t stream) {
                       (uint64_t)a.B * a.H, a.K * eb, a.K * eb * a.Q, P.bias_box_cols, kBM, 1))
             return cudaErrorInvalidValue;
         P.nqt = (a.Q + kBM - 1) / kBM;
-        P.ident_bits = a.bias_f32 ? 0u : inverse_pow2_bits(a.scale, bf16);
-        fold = P.ident_bits != 0;
-        P.ident_bytes = fold ? 2048 : 0;
+        fold = false;  // the bias is added in the softmax
     } else {
         const uint64_t tk = a.total_k > 0 ? a.total_k : 1;
         if (!make_map(&P.tm_q, dt, a.q, D, a.H, a.total_q, rs, rs * a.H, 64, 1, kBM) ||
@@ -183,14 +167,11 @@ cudaError_t launch_tc_fwd(const AttnParams& a, cudaStream_t stream) {
         return fold ? launch_nq<true, false, false, true>(NQ, P, grid, stream)
                     : launch_nq<true, false, false, false>(NQ, P, grid, stream);
     }
-    if (bf16) {
-        if (a.bias_f32) return launch_nq<false, true, true, false>(NQ, P, grid, stream);
-        return fold ? launch_nq<false, true, false, true>(NQ, P, grid, stream)
-                    : launch_nq<false, true, false, false>(NQ, P, grid, stream);
-    }
-    if (a.bias_f32) return launch_nq<false, false, true, false>(NQ, P, grid, stream);
-    return fold ? launch_nq<false, false, false, true>(NQ, P, grid, stream)
-                : launch_nq<false, false, false, false>(NQ, P, grid, stream);
+    (void)fold;
+    if (bf16) return a.bias_f32 ? launch_nq<false, true, true, false>(NQ, P, grid, stream)
+                                : launch_nq<false, true, false, false>(NQ, P, grid, stream);
+    return a.bias_f32 ? launch_nq<false, false, true, false>(NQ, P, grid, stream)
+                      : launch_nq<false, false, false, false>(NQ, P, grid, stream);
 }
 
 }  // namespace triattn

@@ -6,10 +6,8 @@ namespace triattn {
 namespace tc {
 
 TRIATTN_TC_INSTANTIATE(1, false, true, false, false)
-TRIATTN_TC_INSTANTIATE(1, false, true, false, true)
 TRIATTN_TC_INSTANTIATE(1, false, true, true, false)
 TRIATTN_TC_INSTANTIATE(2, false, true, false, false)
-TRIATTN_TC_INSTANTIATE(2, false, true, false, true)
 TRIATTN_TC_INSTANTIATE(2, false, true, true, false)
 
 }  // namespace tc

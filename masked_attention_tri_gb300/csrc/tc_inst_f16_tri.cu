@@ -6,10 +6,8 @@ namespace triattn {
 namespace tc {
 
 TRIATTN_TC_INSTANTIATE(1, false, false, false, false)
-TRIATTN_TC_INSTANTIATE(1, false, false, false, true)
 TRIATTN_TC_INSTANTIATE(1, false, false, true, false)
 TRIATTN_TC_INSTANTIATE(2, false, false, false, false)
-TRIATTN_TC_INSTANTIATE(2, false, false, false, true)
 TRIATTN_TC_INSTANTIATE(2, false, false, true, false)
 
 }  // namespace tc

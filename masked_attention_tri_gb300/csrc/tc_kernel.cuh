@@ -12,14 +12,23 @@
 // adjacent 128-row q blocks of one (sequence, head) (packed form, where each
 // q block visits only the kv blocks its lists name).  Warp roles:
 //   warps 0 .. 4*NQ-1  softmax: warpgroup i owns query tile i, one thread per
-//                      row (= TMEM lane); online softmax in fp32 (packed
-//                      f32x2 arithmetic), P written back to TMEM as 16-bit,
-//                      epilogue O / l, lse, max;
-//   warp 4*NQ          producer: TMA loads of Q, K, V and bias tiles into a
-//                      128B-swizzled shared-memory ring (+ dense-mask bits);
+//                      row (= TMEM lane).  A tile's 128 logits of a row are
+//                      read from TMEM into registers at once; bias, mask,
+//                      row max and the exponentials (packed f32x2 arithmetic)
+//                      are formed there, and P goes back to TMEM as 16-bit
+//                      pairs; epilogue O / l, lse, max;
+//   warp 4*NQ          producer: TMA loads of Q, K and V tiles into a
+//                      128B-swizzled shared-memory ring;
 //   warp 4*NQ+1        MMA: one thread issues tcgen05.mma
 //                      S_i = Q_i K^T (both operands in shared memory, fp32 in
-//                      TMEM) and O_i += P_i V (P from TMEM, V from shared).
+//                      TMEM) and O_i += P_i V (P from TMEM, V from shared);
+//   warp 4*NQ+2        bias producer (triangle form): TMA loads of bias tiles
+//                      and the dense-mask bits, so that waiting for a free
+//                      bias stage never holds back a K/V load;
+//   warp 4*NQ+3        (NQ = 2 only) idle: it completes the third warpgroup.
+// With NQ = 2 the third warpgroup hands registers to the two softmax
+// warpgroups (setmaxnreg, executed inside each role's branch so that every
+// code region has one register limit).
 // Tensor memory: S_i at columns [128 i, 128 i + 128), O_i after all S tiles.
 // With NQ = 2 the MMAs of one tile run while the other tile's softmax does:
 // the tensor core alternates between the two query tiles.
@@ -28,10 +37,12 @@
 // its sequence (ragged tail) gets -inf and takes no part.  With kv_lengths,
 // key tiles past the prefix are not visited: they contribute exp(-1e9 - m)
 // = 0 exactly when the row has a valid key.  A row with no valid key has
-// every logit -1e9: its output is the mean of V over all keys, computed
-// directly.  The running max used for the exponentials is only raised when
-// the row max grows by more than 2^8 (in exp2 units), so O is rescaled
-// rarely; lse uses the same reference, so the result is unchanged.
+// every logit -1e9: its output is the mean of V over all keys (weights of
+// exactly 1 through the tensor core, or formed directly from V when some
+// key blocks were not visited).  The running max used for the exponentials
+// is only raised when the row max grows by more than 2^8 (in exp2 units), so
+// O is rescaled rarely; lse uses the same reference, so the result is
+// unchanged.
 //
 // Every mbarrier wait is bounded: after ~2 s the waiting thread records
 // TA_ERR_TIMEOUT in the status word, raises a CTA-wide abort flag and all
@@ -85,12 +96,9 @@ struct TcParams {
     uint32_t o_col0;    // first TMEM column of O_0
     uint32_t o_cols;    // TMEM columns per O tile
     int mask_kind;      // triangle: 0 none, 1 kv_lengths, 2 dense
-    // Folded softmax (scale > 0): the softmax reads raw S = Q K^T (+ bias / s,
-    // added by the tensor core) and applies s inside the exponent.
+    // Folded softmax (packed form, scale > 0): the softmax reads raw S = Q K^T
+    // and applies s inside the exponent.
     float scale_log2e;  // s * log2(e)
-    uint32_t ident_bytes;   // 2048 when the bias is added by MMA with (1/s) I, else 0
-    uint32_t ident_bits;    // 16-bit pattern of 1/s in the q/k/v dtype
-    uint32_t idesc_id;      // instruction descriptor of the M=128, N=16 bias MMA
 };
 
 // ---------------------------------------------------------------------------
@@ -98,14 +106,13 @@ struct TcParams {
 // ---------------------------------------------------------------------------
 
 struct Layout {
-    uint32_t ident, q, kv, bias, maskw, bars, tmem_slot, abort_flag, total;
+    uint32_t q, kv, bias, maskw, bars, tmem_slot, abort_flag, total;
     int nbars;
 };
 
 __host__ __device__ inline Layout make_layout(int NQ, const TcParams& P) {
     Layout L;
-    L.ident = 0;  // 16 x 16 identity (times 1/s) in the 128B-swizzled K-major layout
-    L.q = L.ident + P.ident_bytes;
+    L.q = 0;
     L.kv = L.q + NQ * P.q_bufs * P.tile_bytes;
     L.bias = L.kv + P.kv_stages * 2 * P.tile_bytes;
     L.maskw = L.bias + NQ * P.bias_stages * P.bias_bytes;
@@ -134,6 +141,18 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+// Non-blocking test of a phase.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 // A waiting thread is suspended (up to the hint, in ns) instead of spinning,
 // so it leaves issue slots to the warps that are computing.
 constexpr uint32_t kSuspendHintNs = 1000000;
@@ -150,8 +169,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded wait: returns false if the CTA is aborting or the wait ran out.
-static __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status) {
-    if (mbar_try_wait(bar, parity)) return true;
+// Inline everywhere (no calls: code regions after setmaxnreg must not call
+// functions compiled for another register limit).
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status) {
+    if (mbar_test(bar, parity)) return true;
     const long long t0 = clock64();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -167,7 +188,7 @@ static __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, vola
 }
 
 // Bounded wait that ignores the abort flag (teardown drains only).
-static __device__ __noinline__ bool wait_bar_drain(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool wait_bar_drain(uint32_t bar, uint32_t parity) {
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity))
         if (clock64() - t0 > kTimeoutCycles / 8) return false;
@@ -189,7 +210,8 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 
 // Shared-memory matrix descriptor (tcgen05 form): start >> 4 at [0,14), leading
 // byte offset >> 4 at [16,30), stride byte offset >> 4 at [32,46), fixed 0b001
-// at [46,49), swizzle mode at [61,64) (2 = 128-byte swizzle).
+// at [46,49), swizzle mode at [61,64) (2 = 128-byte swizzle).  Adding n to the
+// descriptor moves its start address by 16 n bytes.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
     uint64_t d = 0;
     d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
@@ -231,14 +253,6 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-__device__ __forceinline__ uint4 lds128(uint32_t saddr) {
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(saddr));
-    return v;
-}
-
 __device__ __forceinline__ float max3(float a, float b, float c) {
     float d;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
@@ -271,6 +285,10 @@ __device__ __forceinline__ float load16(const void* base, long long i) {
     const unsigned short u = static_cast<const unsigned short*>(base)[i];
     if constexpr (BF16) return __uint_as_float((uint32_t)u << 16);
     else return __half2float(__ushort_as_half(u));
+}
+
+__device__ __forceinline__ uint32_t low_bits(int n) {
+    return n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : ((1u << n) - 1u));
 }
 
 // ---------------------------------------------------------------------------
@@ -445,8 +463,32 @@ __device__ __forceinline__ void for_each_tile(const Item<NQ>& it, F&& f) {
 // The kernel
 // ---------------------------------------------------------------------------
 
+// Block size: NQ softmax warpgroups + producer, MMA and bias warps (with
+// NQ = 2, a full third warpgroup: 384 threads launched with 168 registers
+// each).
+template <int NQ>
+constexpr int kThreads = NQ == 2 ? 384 : NQ * 128 + 96;
+// Register split for NQ = 2: 2 x 128 x softmax + 128 x other equals the 384 x 168
+// registers of the launch.  The packed form's MMA thread walks the BlockMask
+// lists and needs more registers than the triangle form's.
+template <bool VARLEN>
+constexpr int kRegSoftmax = VARLEN ? 208 : 216;
+template <bool VARLEN>
+constexpr int kRegOther = VARLEN ? 88 : 72;
+static_assert(2 * 128 * kRegSoftmax<false> + 128 * kRegOther<false> <= 384 * 168, "register split exceeds the launch");
+static_assert(2 * 128 * kRegSoftmax<true> + 128 * kRegOther<true> <= 384 * 168, "register split exceeds the launch");
+
+template <int NQ, bool VARLEN>
+__device__ __forceinline__ void regs_other() {
+    if constexpr (NQ == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegOther<VARLEN>));
+}
+template <int NQ, bool VARLEN>
+__device__ __forceinline__ void regs_softmax() {
+    if constexpr (NQ == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegSoftmax<VARLEN>));
+}
+
 template <int NQ, bool VARLEN, bool BF16, bool BIAS_F32, bool FOLD>
-__global__ void __launch_bounds__(NQ * 128 + 64, 1) tc_fwd_kernel(const __grid_constant__ TcParams P) {
+__global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_constant__ TcParams P) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -457,6 +499,7 @@ __global__ void __launch_bounds__(NQ * 128 + 64, 1) tc_fwd_kernel(const __grid_c
     const int lane = threadIdx.x % 32;
     constexpr int kProducerWarp = NQ * 4;
     constexpr int kMmaWarp = NQ * 4 + 1;
+    constexpr int kBiasWarp = NQ * 4 + 2;
     const AttnParams& a = P.a;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L.abort_flag);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L.tmem_slot);
@@ -491,7 +534,7 @@ __global__ void __launch_bounds__(NQ * 128 + 64, 1) tc_fwd_kernel(const __grid_c
             mbar_init(o_full(i), 1);
             for (int s = 0; s < BS; ++s) {
                 mbar_init(bias_full(i, s), 1);
-                mbar_init(bias_empty(i, s), (FOLD && !VARLEN) ? 1 : 128);  // MMA commit, or every softmax thread
+                mbar_init(bias_empty(i, s), 128);  // every softmax thread of the tile
             }
         }
         for (int qb = 0; qb < QB; ++qb) mbar_init(q_empty(qb), 1);
@@ -502,17 +545,6 @@ __global__ void __launch_bounds__(NQ * 128 + 64, 1) tc_fwd_kernel(const __grid_c
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    }
-    if constexpr (FOLD && !VARLEN) {
-        // (1/s) I_16 as a 16 x 16 K-major operand in the 128B-swizzled layout:
-        // element (n, k) at byte n*128 + (((2k/16) ^ (n % 8)) * 16) + (2k % 16).
-        for (int i = threadIdx.x; i < 16 * 64; i += blockDim.x) {
-            const int n = i / 64, k = i % 64;
-            const uint32_t off = (uint32_t)n * 128u + ((((uint32_t)k * 2u / 16u) ^ ((uint32_t)n & 7u)) << 4) +
-                                 ((uint32_t)k * 2u) % 16u;
-            *reinterpret_cast<uint16_t*>(gbase + L.ident + off) = (n == k) ? (uint16_t)P.ident_bits : (uint16_t)0;
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the tensor core
     }
     if (warp == kMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -526,10 +558,9 @@ __global__ void __launch_bounds__(NQ * 128 + 64, 1) tc_fwd_kernel(const __grid_c
     const uint32_t tmem = *tmem_slot;
 
     if (warp == kProducerWarp) {
-        // ------------------------------------------------------------- producer
+        // ------------------------------------------------- producer: Q, K, V tiles
+        regs_other<NQ, VARLEN>();
         uint32_t kv_it = 0, q_it = 0;
-        uint32_t b_it[NQ];
-        for (int i = 0; i < NQ; ++i) b_it[i] = 0;
         bool ok = true;
         for (int item = blockIdx.x; item < P.items && ok; item += gridDim.x) {
             const Item<NQ> it = decode<NQ, VARLEN>(P, item);
@@ -555,7 +586,7 @@ __global__ void __launch_bounds__(NQ * 128 + 64, 1) tc_fwd_kernel(const __grid_c
                 }
             }
             ++q_it;
-            for_each_tile<NQ, VARLEN>(it, [&](int kb, uint32_t ps, uint32_t) -> bool {
+            for_each_tile<NQ, VARLEN>(it, [&](int kb, uint32_t, uint32_t) -> bool {
                 const int st = kv_it % S;
                 if (lane == 0 && kv_it >= (uint32_t)S)
                     ok = wait_bar(kv_empty(st), ((kv_it / S) - 1) & 1, abort_flag, a.status);
@@ -576,33 +607,47 @@ __global__ void __launch_bounds__(NQ * 128 + 64, 1) tc_fwd_kernel(const __grid_c
                     }
                 }
                 ++kv_it;
-                if constexpr (!VARLEN) {
-                    for (int i = 0; i < NQ; ++i) {
-                        if (!((ps >> i) & 1u)) continue;
-                        const int bs = b_it[i] % BS;
-                        if (lane == 0 && b_it[i] >= (uint32_t)BS)
-                            ok = wait_bar(bias_empty(i, bs), ((b_it[i] / BS) - 1) & 1, abort_flag, a.status);
-                        ok = __shfl_sync(0xffffffffu, ok, 0);
-                        if (!ok) return false;
-                        if (P.mask_kind == 2) {
-                            // 128 key-validity bits: word w, bit l <-> key kb*128 + 32w + l
-                            uint32_t* mw = reinterpret_cast<uint32_t*>(gbase + L.maskw + (uint32_t)(i * BS + bs) * 16u);
-                            for (int ww = 0; ww < 4; ++ww) {
-                                const int key = kb * kBN + 32 * ww + lane;
-                                const bool v = key < a.K && a.mask[it.bn * a.K + key] != 0;
-                                const uint32_t word = __ballot_sync(0xffffffffu, v);
-                                if (lane == ww) mw[ww] = word;
-                            }
-                            __syncwarp();
+                return true;
+            });
+        }
+        if (!ok) *abort_flag = 1;
+    } else if (!VARLEN && warp == kBiasWarp) {
+        // ---------------------------------- producer: bias tiles (+ dense-mask bits)
+        regs_other<NQ, VARLEN>();
+        uint32_t b_it[NQ];
+#pragma unroll
+        for (int i = 0; i < NQ; ++i) b_it[i] = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; item < P.items && ok; item += gridDim.x) {
+            const Item<NQ> it = decode<NQ, VARLEN>(P, item);
+            if (!it.any) continue;
+            for_each_tile<NQ, VARLEN>(it, [&](int kb, uint32_t ps, uint32_t) -> bool {
+#pragma unroll
+                for (int i = 0; i < NQ; ++i) {
+                    if (!((ps >> i) & 1u)) continue;
+                    const int bs = b_it[i] % BS;
+                    if (lane == 0 && b_it[i] >= (uint32_t)BS)
+                        ok = wait_bar(bias_empty(i, bs), ((b_it[i] / BS) - 1) & 1, abort_flag, a.status);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) return false;
+                    if (P.mask_kind == 2) {
+                        // 128 key-validity bits: word w, bit l <-> key kb*128 + 32w + l
+                        uint32_t* mw = reinterpret_cast<uint32_t*>(gbase + L.maskw + (uint32_t)(i * BS + bs) * 16u);
+                        for (int ww = 0; ww < 4; ++ww) {
+                            const int key = kb * kBN + 32 * ww + lane;
+                            const bool v = key < a.K && a.mask[it.bn * a.K + key] != 0;
+                            const uint32_t word = __ballot_sync(0xffffffffu, v);
+                            if (lane == ww) mw[ww] = word;
                         }
-                        if (lane == 0) {
-                            mbar_expect_tx(bias_full(i, bs), P.bias_bytes);
-                            for (int bx = 0; bx < P.bias_boxes; ++bx)
-                                tma_load_3d(bias_smem(i, bs) + bx * kBox, &P.tm_bias, kb * kBN + bx * P.bias_box_cols,
-                                            it.qt[i] * kBM, it.b * a.H + it.h, bias_full(i, bs));
-                        }
-                        ++b_it[i];
+                        __syncwarp();
                     }
+                    if (lane == 0) {
+                        mbar_expect_tx(bias_full(i, bs), P.bias_bytes);
+                        for (int bx = 0; bx < P.bias_boxes; ++bx)
+                            tma_load_3d(bias_smem(i, bs) + bx * kBox, &P.tm_bias, kb * kBN + bx * P.bias_box_cols,
+                                        it.qt[i] * kBM, it.b * a.H + it.h, bias_full(i, bs));
+                    }
+                    ++b_it[i];
                 }
                 return true;
             });
@@ -610,11 +655,17 @@ __global__ void __launch_bounds__(NQ * 128 + 64, 1) tc_fwd_kernel(const __grid_c
         if (!ok) *abort_flag = 1;
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------------ MMA
+        regs_other<NQ, VARLEN>();
         if (lane == 0) {
             uint32_t kv_it = 0, q_it = 0;
-            uint32_t p_it[NQ], bm_it[NQ];
-            for (int i = 0; i < NQ; ++i) p_it[i] = bm_it[i] = 0;
+            uint32_t p_it[NQ];
+#pragma unroll
+            for (int i = 0; i < NQ; ++i) p_it[i] = 0;
             bool ok = true;
+            // Descriptor steps (units of 16 B): a K step of 16 inside a 128-byte
+            // swizzle row is 32 bytes, the second 64-column box starts kBox
+            // bytes later; 16 rows of V are 2048 bytes.
+            auto kstep = [](int kk) -> uint64_t { return (uint64_t)(((kk >> 2) * kBox + (kk & 3) * 32) >> 4); };
             for (int item = blockIdx.x; item < P.items && ok; item += gridDim.x) {
                 const Item<NQ> it = decode<NQ, VARLEN>(P, item);
                 if (!it.any) continue;
@@ -622,30 +673,44 @@ __global__ void __launch_bounds__(NQ * 128 + 64, 1) tc_fwd_kernel(const __grid_c
                 for (int i = 0; i < NQ && ok; ++i) ok = wait_bar(q_full(i, qb), (q_it / QB) & 1, abort_flag, a.status);
                 ++q_it;
                 if (!ok) break;
+                uint64_t qd[NQ];
                 uint32_t pend = 0;  // bit i: P_i of slot i's last tile is still to be multiplied by V
                 int pst[NQ];
                 uint32_t npv[NQ];
+#pragma unroll
                 for (int i = 0; i < NQ; ++i) {
+                    qd[i] = sw128_desc(q_smem(i, qb), 16, 1024);
                     pst[i] = 0;
                     npv[i] = 0;
                 }
                 int prev = -1;
                 // O_i += P_i V, with V from stage `st` and P_i in S_i's columns.
                 auto issue_pv = [&](int i, int st) {
-                    for (int kk = 0; kk < kBN / 16; ++kk)
-                        mma_ts(tmem + P.o_col0 + i * P.o_cols, tmem + i * 128 + kk * 8,
-                               sw128_desc(v_smem(st) + kk * 16 * 128, kBox, 1024), P.idesc_pv,
-                               (npv[i] > 0 || kk > 0) ? 1u : 0u);
+                    const uint64_t vd = sw128_desc(v_smem(st), kBox, 1024);
+                    const uint32_t d = tmem + P.o_col0 + i * P.o_cols;
+                    const uint32_t pa = tmem + i * 128;
+                    mma_ts(d, pa, vd, P.idesc_pv, npv[i] > 0 ? 1u : 0u);
+#pragma unroll
+                    for (int kk = 1; kk < kBN / 16; ++kk) mma_ts(d, pa + kk * 8, vd + (uint64_t)kk * 128, P.idesc_pv, 1u);
                     ++npv[i];
                 };
                 for_each_tile<NQ, VARLEN>(it, [&](int, uint32_t ps, uint32_t) -> bool {
+                    // Per slot: PV of its previous tile (frees S_i; that V is
+                    // resident already), then QK of this tile.  Only QK waits for
+                    // this tile's K/V, so a late load never holds back a PV.
                     const int st = kv_it % S;
-                    ok = wait_bar(kv_full(st), (kv_it / S) & 1, abort_flag, a.status);
-                    if (!ok) return false;
-                    ++kv_it;
-                    tc_fence_after();
+                    bool kv_ready = false;
+                    auto wait_kv = [&]() -> bool {
+                        if (kv_ready) return true;
+                        kv_ready = true;
+                        if (!wait_bar(kv_full(st), (kv_it / S) & 1, abort_flag, a.status)) return false;
+                        tc_fence_after();
+                        return true;
+                    };
+                    const uint64_t kd = sw128_desc(k_smem(st), 16, 1024);
+#pragma unroll
                     for (int i = 0; i < NQ; ++i) {
-                        if ((pend >> i) & 1u) {  // PV of this slot's previous tile frees S_i
+                        if ((pend >> i) & 1u) {
                             ok = wait_bar(p_full(i), p_it[i]++ & 1, abort_flag, a.status);
                             if (!ok) return false;
                             tc_fence_after();
@@ -653,37 +718,29 @@ __global__ void __launch_bounds__(NQ * 128 + 64, 1) tc_fwd_kernel(const __grid_c
                             pend &= ~(1u << i);
                         }
                         if ((ps >> i) & 1u) {
-                            for (int kk = 0; kk < P.ksteps; ++kk) {
-                                const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-                                mma_ss(tmem + i * 128, sw128_desc(q_smem(i, qb) + off, 16, 1024),
-                                       sw128_desc(k_smem(st) + off, 16, 1024), P.idesc_qk, kk > 0 ? 1u : 0u);
-                            }
-                            if constexpr (FOLD && !VARLEN) {
-                                // S_i += bias_tile x ((1/s) I): adds bias / s exactly (one
-                                // nonzero product per entry), 16 key columns per MMA.
-                                const int bs = bm_it[i] % BS;
-                                ok = wait_bar(bias_full(i, bs), (bm_it[i] / BS) & 1, abort_flag, a.status);
-                                if (!ok) return false;
-                                tc_fence_after();
-                                for (int kk = 0; kk < kBN / 16; ++kk)
-                                    mma_ss(tmem + i * 128 + 16 * kk,
-                                           sw128_desc(bias_smem(i, bs) + (kk >> 2) * kBox + (kk & 3) * 32, 16, 1024),
-                                           sw128_desc(base + L.ident, 16, 1024), P.idesc_id, 1u);
-                                mma_commit(bias_empty(i, bs));
-                                ++bm_it[i];
-                            }
+                            ok = wait_kv();
+                            if (!ok) return false;
+                            const uint32_t sd = tmem + i * 128;
+                            mma_ss(sd, qd[i], kd, P.idesc_qk, 0u);
+                            for (int kk = 1; kk < P.ksteps; ++kk)
+                                mma_ss(sd, qd[i] + kstep(kk), kd + kstep(kk), P.idesc_qk, 1u);
                             mma_commit(s_full(i));
                             pend |= 1u << i;
                             pst[i] = st;
                         }
                     }
                     if (prev >= 0) mma_commit(kv_empty(prev));  // no pending PV reads stage `prev` any more
+                    ok = wait_kv();  // keeps the phases in step if no slot used this tile
+                    if (!ok) return false;
+                    ++kv_it;
                     prev = st;
                     return true;
                 });
                 if (!ok) break;
                 mma_commit(q_empty(qb));  // every QK of the item is issued: its Q buffers may be refilled
-                for (int i = 0; i < NQ && ok; ++i) {
+#pragma unroll
+                for (int i = 0; i < NQ; ++i) {
+                    if (!ok) break;
                     if ((pend >> i) & 1u) {
                         ok = wait_bar(p_full(i), p_it[i]++ & 1, abort_flag, a.status);
                         if (!ok) break;
@@ -703,43 +760,44 @@ __global__ void __launch_bounds__(NQ * 128 + 64, 1) tc_fwd_kernel(const __grid_c
         __syncwarp();
     } else if (warp < 4 * NQ) {
         // -------------------------------------------------------------- softmax
+        regs_softmax<NQ, VARLEN>();
         const int slot = warp / 4;
         const int wq = warp % 4;               // TMEM lane quarter
         const int r = wq * 32 + lane;          // row within the q tile
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const uint32_t s_taddr = tmem + lane_off + slot * 128;
         const uint32_t o_taddr = tmem + lane_off + P.o_col0 + slot * P.o_cols;
-        const uint32_t rsw = (uint32_t)(r & 7);  // 128B swizzle: chunk c of row r sits at chunk c ^ (r % 8)
+        // 128B swizzle: 16-byte chunk c of row r sits at chunk c ^ (r % 8).
+        const uint32_t rsw = (uint32_t)(r & 7);
         const uint32_t rrow = (uint32_t)r * 128u;
         uint32_t s_it = 0, bias_it = 0, o_it = 0;
         const float2 scale2 = make_float2(a.scale, a.scale);
+        // Folded form (packed sequences, no bias): values are in units of S
+        // (x = s S); a masked key holds -FLT_MAX there (its logit is -1e9).
+        constexpr float kMaskVal = FOLD ? -FLT_MAX : kMasked;
+        const float unit_l2e = FOLD ? P.scale_log2e : kLog2e;
         bool ok = true;
 
         for (int item = blockIdx.x; item < P.items && ok; item += gridDim.x) {
             const Item<NQ> it = decode<NQ, VARLEN>(P, item);
             if (VARLEN && it.bad && threadIdx.x == 0) atomicCAS(a.status, 0, kStatusDevice);
-            if (!it.on[slot]) continue;
-            const int qrow = it.qt[slot] * kBM + r;  // local query row
+            bool on_s = false;
+            int qt_s = 0;
+#pragma unroll
+            for (int i = 0; i < NQ; ++i) {  // this slot's fields (constant indices keep Item in registers)
+                if (i == slot) {
+                    on_s = it.on[i];
+                    qt_s = it.qt[i];
+                }
+            }
+            if (!on_s) continue;
+            const int qrow = qt_s * kBM + r;  // local query row
             float m_true = -INFINITY, m_ref = 0.f, l = 0.f;
             int jv = 0;
             for_each_tile<NQ, VARLEN>(it, [&](int kb, uint32_t ps, uint32_t fs) -> bool {
                 if (!((ps >> slot) & 1u)) return true;
                 const bool full = (fs >> slot) & 1u;
                 const int key0 = kb * kBN;
-                ok = __all_sync(0xffffffffu, wait_bar(s_full(slot), s_it & 1, abort_flag, a.status));
-                if (!ok) return false;
-                ++s_it;
-                tc_fence_after();
-
-                // ---- The tile's 128 keys in four chunks of 32.  Pass 1: logits (or raw S
-                // in the folded form), masking, running max; a chunk whose values
-                // changed goes back to its TMEM columns.  Pass 2: P = 2^((x - m_ref)
-                // log2 e), row sum, P packed to 16-bit pairs into columns [16c, 16c+16)
-                // (logits already read).  The TMEM load of chunk c+1 is in flight while
-                // chunk c is computed.
-                // Per chunk: vm bit j = key key0+32c+j is valid, em bit j = it exists.
-                // Folded form: values are in units of S (x = s * S); a masked key holds
-                // -FLT_MAX there (its logit is -1e9), an absent key -inf.
                 int vlim;
                 bool causal = false;
                 if constexpr (!VARLEN) {
@@ -749,32 +807,35 @@ __global__ void __launch_bounds__(NQ * 128 + 64, 1) tc_fwd_kernel(const __grid_c
                     causal = !full && a.mask_mod == TA_MASK_CAUSAL;
                 }
                 const bool all_valid = (VARLEN || P.mask_kind != 2) && key0 + kBN <= vlim &&
-                                       (!causal || key0 + kBN - 1 <= it.qt[slot] * kBM);
+                                       (!causal || key0 + kBN - 1 <= qt_s * kBM);
                 const int nexist = (VARLEN ? it.Lk : a.K) - key0;
-                constexpr float kMaskVal = FOLD ? -FLT_MAX : kMasked;
-                uint32_t brow = 0, mwbase = 0;
+
+                uint32_t boff = 0, mwoff = 0;  // this row's bias / the mask words, from the aligned base
                 int bs = 0;
                 if constexpr (!VARLEN) {
                     bs = bias_it % BS;
-                    if constexpr (!FOLD) {
-                        ok = __all_sync(0xffffffffu, wait_bar(bias_full(slot, bs), (bias_it / BS) & 1, abort_flag, a.status));
-                        if (!ok) return false;
-                        brow = bias_smem(slot, bs) + rrow;
-                    }
-                    mwbase = base + L.maskw + (uint32_t)(slot * BS + bs) * 16u;
+                    ok = __all_sync(0xffffffffu, wait_bar(bias_full(slot, bs), (bias_it / BS) & 1, abort_flag, a.status));
+                    if (!ok) return false;
+                    boff = bias_smem(slot, bs) - base + rrow;
+                    mwoff = L.maskw + (uint32_t)(slot * BS + bs) * 16u;
                 }
-                uint32_t bufA[32], bufB[32];
-                float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
-                auto pass1 = [&](int c, uint32_t(&sr)[32], uint32_t(&nxt)[32]) __attribute__((always_inline)) {
-                    tmem_wait_ld(sr);
-                    if (c < 3) tmem_ld_x32_nowait(s_taddr + 32 * (c + 1), nxt);
-                    float x[32];
+                ok = __all_sync(0xffffffffu, wait_bar(s_full(slot), s_it & 1, abort_flag, a.status));
+                if (!ok) return false;
+                ++s_it;
+                tc_fence_after();
+
+                // ---- x: the row's 128 values of this tile (logits, or raw S in
+                // the folded form), all in registers.
+                float x[128];
+                {
+                    uint32_t sr[128];
+                    tmem_ld_x128(s_taddr, sr);
                     if constexpr (FOLD) {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(sr[j]);
+                        for (int j = 0; j < 128; ++j) x[j] = __uint_as_float(sr[j]);
                     } else if constexpr (VARLEN) {
 #pragma unroll
-                        for (int j = 0; j < 32; j += 2) {
+                        for (int j = 0; j < 128; j += 2) {
                             const float2 r2 =
                                 __fmul2_rn(make_float2(__uint_as_float(sr[j]), __uint_as_float(sr[j + 1])), scale2);
                             x[j] = r2.x;
@@ -782,9 +843,9 @@ __global__ void __launch_bounds__(NQ * 128 + 64, 1) tc_fwd_kernel(const __grid_c
                         }
                     } else if constexpr (!BIAS_F32) {
 #pragma unroll
-                        for (int g = 0; g < 4; ++g) {  // 8 keys per 16-byte chunk
-                            const uint32_t col8 = 4 * c + g;
-                            const uint4 wv = lds128(brow + (col8 >> 3) * kBox + (((col8 & 7) ^ rsw) << 4));
+                        for (int g = 0; g < 16; ++g) {  // 8 keys per 16-byte chunk
+                            const uint4 wv = *reinterpret_cast<const uint4*>(
+                                gbase + boff + (g >> 3) * kBox + ((((uint32_t)g & 7u) ^ rsw) << 4));
                             const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
@@ -798,9 +859,9 @@ __global__ void __launch_bounds__(NQ * 128 + 64, 1) tc_fwd_kernel(const __grid_c
                         }
                     } else {
 #pragma unroll
-                        for (int g = 0; g < 8; ++g) {  // 4 keys per 16-byte chunk
-                            const uint32_t col4 = 8 * c + g;
-                            const uint4 wv = lds128(brow + (col4 >> 3) * kBox + (((col4 & 7) ^ rsw) << 4));
+                        for (int g = 0; g < 32; ++g) {  // 4 keys per 16-byte chunk
+                            const uint4 wv = *reinterpret_cast<const uint4*>(
+                                gbase + boff + (g >> 3) * kBox + ((((uint32_t)g & 7u) ^ rsw) << 4));
                             const int j = 4 * g;
                             const float2 r0 = __ffma2_rn(make_float2(__uint_as_float(sr[j]), __uint_as_float(sr[j + 1])),
                                                          scale2, make_float2(__uint_as_float(wv.x), __uint_as_float(wv.y)));
@@ -813,68 +874,47 @@ __global__ void __launch_bounds__(NQ * 128 + 64, 1) tc_fwd_kernel(const __grid_c
                             x[j + 3] = r1.y;
                         }
                     }
-                    bool changed = !FOLD;  // unfolded logits always go back to TMEM
-                    if (!all_valid) {
-                        auto low_bits = [](int n) -> uint32_t {
-                            return n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : ((1u << n) - 1u));
-                        };
+                }
+                // ---- Masking (tiles at a boundary only).  Per 32 keys: vm bit j =
+                // key key0+32c+j is valid, em bit j = it exists.
+                if (!all_valid) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
                         const int k0 = 32 * c;
                         const uint32_t em = low_bits(nexist - k0);
                         uint32_t vm = em & low_bits(vlim - key0 - k0);
                         if constexpr (!VARLEN) {
-                            if (P.mask_kind == 2) {
-                                uint32_t word;
-                                asm volatile("ld.shared.u32 %0, [%1];" : "=r"(word) : "r"(mwbase + (uint32_t)c * 4u));
-                                vm &= word;
-                            }
+                            if (P.mask_kind == 2) vm &= *reinterpret_cast<const uint32_t*>(gbase + mwoff + 4u * c);
                         } else {
                             if (causal) vm &= low_bits(qrow - key0 - k0 + 1);
                         }
                         if (vm != 0xffffffffu) {
-                            changed = true;
-                            if (vm == 0u && em == 0xffffffffu) {
 #pragma unroll
-                                for (int j = 0; j < 32; ++j) x[j] = kMaskVal;
-                            } else {
-#pragma unroll
-                                for (int j = 0; j < 32; ++j)
-                                    x[j] = ((vm >> j) & 1u) ? x[j] : (((em >> j) & 1u) ? kMaskVal : -INFINITY);
-                            }
+                            for (int j = 0; j < 32; ++j)
+                                x[k0 + j] = ((vm >> j) & 1u) ? x[k0 + j] : (((em >> j) & 1u) ? kMaskVal : -INFINITY);
                         }
                     }
-#pragma unroll
-                    for (int j = 0; j < 32; j += 8) {
-                        m0 = max3(m0, x[j], x[j + 1]);
-                        m1 = max3(m1, x[j + 2], x[j + 3]);
-                        m2 = max3(m2, x[j + 4], x[j + 5]);
-                        m3 = max3(m3, x[j + 6], x[j + 7]);
-                    }
-                    if (__any_sync(0xffffffffu, changed)) {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) sr[j] = __float_as_uint(x[j]);
-                        tmem_st_x32(s_taddr + 32 * c, sr);
-                    }
-                };
-                tmem_ld_x32_nowait(s_taddr, bufA);
-#pragma unroll 1
-                for (int c = 0; c < 4; c += 2) {
-                    pass1(c, bufA, bufB);
-                    pass1(c + 1, bufB, bufA);
                 }
-                if constexpr (!VARLEN && !FOLD) {
-                    mbar_arrive(bias_empty(slot, bs));  // the bias tile has been read
+                if constexpr (!VARLEN) {
+                    mbar_arrive(bias_empty(slot, bs));  // bias and mask words of this stage have been read
+                    ++bias_it;
                 }
-                if constexpr (!VARLEN) ++bias_it;
-                tmem_st_wait();  // written-back values must be in TMEM before pass 2 reads them
 
-                // tm: tile max in the units of this form; its logit in natural units.
+                // ---- Tile max (units of this form) and its logit in natural units.
+                float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+                for (int j = 0; j < 128; j += 8) {
+                    m0 = max3(m0, x[j], x[j + 1]);
+                    m1 = max3(m1, x[j + 2], x[j + 3]);
+                    m2 = max3(m2, x[j + 4], x[j + 5]);
+                    m3 = max3(m3, x[j + 6], x[j + 7]);
+                }
                 const float tm = fmaxf(max3(m0, m1, m2), m3);
                 float tm_nat;
                 if constexpr (FOLD) tm_nat = tm > -FLT_MAX ? tm * a.scale : (tm == -FLT_MAX ? kMasked : -INFINITY);
                 else tm_nat = tm;
                 m_true = fmaxf(m_true, tm_nat);
                 // Reference max m_ref (units of this form) used in the exponent.
-                const float unit_l2e = FOLD ? P.scale_log2e : kLog2e;
                 if (jv == 0) {
                     m_ref = tm;
                     l = 0.f;
@@ -883,7 +923,8 @@ __global__ void __launch_bounds__(NQ * 128 + 64, 1) tc_fwd_kernel(const __grid_c
                     const bool need = (m_new - m_ref) * unit_l2e > kRescaleLog2;
                     if (__any_sync(0xffffffffu, need)) {
                         // Raise the reference max to the current one; O (complete
-                        // through this slot's previous tile) and l scale by alpha.
+                        // through this slot's previous tile, whose PV finished
+                        // before this S was committed) and l scale by alpha.
                         const float alpha = ex2((m_ref - m_new) * unit_l2e);
                         l *= alpha;
                         m_ref = m_new;
@@ -897,42 +938,27 @@ __global__ void __launch_bounds__(NQ * 128 + 64, 1) tc_fwd_kernel(const __grid_c
                     }
                 }
 
+                // ---- P = 2^((x - m_ref) log2 e), packed to 16-bit pairs into
+                // columns [16c, 16c + 16).  A row with no real logit yet (every
+                // value masked or absent) takes weights of exactly 1 for masked
+                // keys and 0 for absent ones: x + (-kMaskVal) is then 0 or -inf.
+                const bool live = m_ref > kMaskVal;
+                const float2 ul2 = live ? make_float2(unit_l2e, unit_l2e) : make_float2(1.f, 1.f);
+                const float nb = live ? -m_ref * unit_l2e : -kMaskVal;
+                const float2 nb2 = make_float2(nb, nb);
                 float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-                const bool live = m_ref > kMaskVal;  // some key with a real logit seen
-                const float2 ul2 = make_float2(unit_l2e, unit_l2e);
-                const float2 nb2 = make_float2(-m_ref * unit_l2e, -m_ref * unit_l2e);
-                auto pass2 = [&](int c, uint32_t(&xr)[32], uint32_t(&nxt)[32]) __attribute__((always_inline)) {
-                    tmem_wait_ld(xr);
-                    if (c < 3) tmem_ld_x32_nowait(s_taddr + 32 * (c + 1), nxt);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
                     uint32_t pk[16];
-                    if (live) {
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const float2 y = __ffma2_rn(
-                                make_float2(__uint_as_float(xr[2 * j]), __uint_as_float(xr[2 * j + 1])), ul2, nb2);
-                            const float2 p = make_float2(ex2(y.x), ex2(y.y));
-                            if (j & 1) acc1 = __fadd2_rn(acc1, p);
-                            else acc0 = __fadd2_rn(acc0, p);
-                            pk[j] = pack2<BF16>(p.x, p.y);
-                        }
-                    } else {
-                        // No valid key seen yet (every logit so far is -1e9): the
-                        // weights are exactly 1 for masked keys and 0 for absent ones.
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const float2 p = make_float2(__uint_as_float(xr[2 * j]) == kMaskVal ? 1.f : 0.f,
-                                                         __uint_as_float(xr[2 * j + 1]) == kMaskVal ? 1.f : 0.f);
-                            acc0 = __fadd2_rn(acc0, p);
-                            pk[j] = pack2<BF16>(p.x, p.y);
-                        }
+                    for (int j = 0; j < 16; ++j) {
+                        const float2 y = __ffma2_rn(make_float2(x[32 * c + 2 * j], x[32 * c + 2 * j + 1]), ul2, nb2);
+                        const float2 p = make_float2(ex2(y.x), ex2(y.y));
+                        if (j & 1) acc1 = __fadd2_rn(acc1, p);
+                        else acc0 = __fadd2_rn(acc0, p);
+                        pk[j] = pack2<BF16>(p.x, p.y);
                     }
                     tmem_st_x16(s_taddr + 16 * c, pk);
-                };
-                tmem_ld_x32_nowait(s_taddr, bufA);
-#pragma unroll 1
-                for (int c = 0; c < 4; c += 2) {
-                    pass2(c, bufA, bufB);
-                    pass2(c + 1, bufB, bufA);
                 }
                 l += (acc0.x + acc0.y) + (acc1.x + acc1.y);
                 tmem_st_wait();
@@ -942,7 +968,6 @@ __global__ void __launch_bounds__(NQ * 128 + 64, 1) tc_fwd_kernel(const __grid_c
                 return true;
             });
             if (!ok) break;
-
             // ------------------------------------------------------- epilogue
             // A row that saw no valid key has every logit -1e9: uniform weights over
             // all keys, i.e. the mean of V.  If every key block was visited, the
@@ -1031,6 +1056,8 @@ __global__ void __launch_bounds__(NQ * 128 + 64, 1) tc_fwd_kernel(const __grid_c
             }
         }
         if (!ok) *abort_flag = 1;
+    } else {
+        regs_other<NQ, VARLEN>();  // idle warps of the third warpgroup
     }
 
     // ---------------------------------------------------------------- teardown
@@ -1048,6 +1075,7 @@ __global__ void __launch_bounds__(NQ * 128 + 64, 1) tc_fwd_kernel(const __grid_c
 }
 
 
+
 template <int NQ, bool VARLEN, bool BF16, bool BIAS_F32, bool FOLD>
 cudaError_t launch_kernel(const TcParams& P, int grid, cudaStream_t stream) {
     const Layout L = make_layout(NQ, P);
@@ -1055,23 +1083,20 @@ cudaError_t launch_kernel(const TcParams& P, int grid, cudaStream_t stream) {
     auto kern = tc_fwd_kernel<NQ, VARLEN, BF16, BIAS_F32, FOLD>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, NQ * 128 + 64, smem, stream>>>(P);
+    kern<<<grid, kThreads<NQ>, smem, stream>>>(P);
     return cudaGetLastError();
 }
 
-// The kernel variants the host launches (each instantiated in one tc_inst_*.cu file).
+// The kernel variants the host launches (each instantiated in one tc_inst_*.cu
+// file).  The folded softmax is used by the packed form only.
 #define TRIATTN_TC_VARIANTS(X)                  \
     X(1, false, true, false, false)             \
-    X(1, false, true, false, true)              \
     X(1, false, true, true, false)              \
     X(2, false, true, false, false)             \
-    X(2, false, true, false, true)              \
     X(2, false, true, true, false)              \
     X(1, false, false, false, false)            \
-    X(1, false, false, false, true)             \
     X(1, false, false, true, false)             \
     X(2, false, false, false, false)            \
-    X(2, false, false, false, true)             \
     X(2, false, false, true, false)             \
     X(2, true, true, false, false)              \
     X(2, true, true, false, true)               \
