@@ -527,18 +527,23 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
+#pragma unroll 1
         for (int i = 0; i < NQ; ++i) {
+#pragma unroll 1
             for (int qb = 0; qb < QB; ++qb) mbar_init(q_full(i, qb), 1);
             mbar_init(s_full(i), 1);
             mbar_init(p_full(i), 128);
             mbar_init(o_full(i), 1);
+#pragma unroll 1
             for (int s = 0; s < BS; ++s) {
                 mbar_init(bias_full(i, s), 1);
                 mbar_init(bias_empty(i, s), 128);  // every softmax thread of the tile
             }
         }
+#pragma unroll 1
         for (int qb = 0; qb < QB; ++qb) mbar_init(q_empty(qb), 1);
         mbar_init(drain, 1);
+#pragma unroll 1
         for (int s = 0; s < S; ++s) {
             mbar_init(kv_full(s), 1);
             mbar_init(kv_empty(s), 1);
@@ -875,10 +880,19 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
                         }
                     }
                 }
-                // ---- Masking (tiles at a boundary only).  Per 32 keys: vm bit j =
-                // key key0+32c+j is valid, em bit j = it exists.
+                // ---- Masking (tiles at a boundary only): the values make a round
+                // trip through TMEM so that this rarely taken path is a short
+                // loop over 32-key chunks instead of 128 unrolled selects.  Per
+                // chunk: vm bit j = key key0+32c+j is valid, em bit j = it exists.
                 if (!all_valid) {
+                    {
+                        uint32_t xs[128];
 #pragma unroll
+                        for (int j = 0; j < 128; ++j) xs[j] = __float_as_uint(x[j]);
+                        tmem_st_x128(s_taddr, xs);
+                        tmem_st_wait();
+                    }
+#pragma unroll 1
                     for (int c = 0; c < 4; ++c) {
                         const int k0 = 32 * c;
                         const uint32_t em = low_bits(nexist - k0);
@@ -888,11 +902,22 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
                         } else {
                             if (causal) vm &= low_bits(qrow - key0 - k0 + 1);
                         }
-                        if (vm != 0xffffffffu) {
+                        if (__any_sync(0xffffffffu, vm != 0xffffffffu)) {
+                            uint32_t xc[32];
+                            tmem_ld_x32(s_taddr + k0, xc);
 #pragma unroll
                             for (int j = 0; j < 32; ++j)
-                                x[k0 + j] = ((vm >> j) & 1u) ? x[k0 + j] : (((em >> j) & 1u) ? kMaskVal : -INFINITY);
+                                xc[j] = ((vm >> j) & 1u) ? xc[j]
+                                                         : __float_as_uint(((em >> j) & 1u) ? kMaskVal : -INFINITY);
+                            tmem_st_x32(s_taddr + k0, xc);
                         }
+                    }
+                    tmem_st_wait();
+                    {
+                        uint32_t xs[128];
+                        tmem_ld_x128(s_taddr, xs);
+#pragma unroll
+                        for (int j = 0; j < 128; ++j) x[j] = __uint_as_float(xs[j]);
                     }
                 }
                 if constexpr (!VARLEN) {
@@ -973,7 +998,9 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
             // all keys, i.e. the mean of V.  If every key block was visited, the
             // tensor-core result O / l is already that mean (P was 1 on every key);
             // otherwise (a packed q block whose lists skip blocks) it is formed
-            // here directly from V.
+            // here directly from V.  The loops stay rolled: this code runs once
+            // per work item and must not crowd the softmax out of the
+            // instruction cache.
             const bool seen = jv > 0 && m_true > kMasked;
             const bool covered = jv > 0 && jv == (it.Lk + kBN - 1) / kBN;
             const bool direct = !seen && !covered;
@@ -983,57 +1010,49 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
                 if (!ok) break;
                 tc_fence_after();
             }
-            // Lane l holds the means of columns l, l+32, l+64, l+96.
-            const bool any_unseen = __any_sync(0xffffffffu, direct);
-            float mv[4] = {0.f, 0.f, 0.f, 0.f};
-            if (any_unseen && it.Lk > 0) {
-                const long long vrow0 = !VARLEN ? it.unit * a.K : (long long)it.k_row0;
-                const long long vstride = !VARLEN ? a.D : (long long)a.H * a.D;
-                const long long vcol0 = !VARLEN ? 0 : (long long)it.h * a.D;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int d = lane + 32 * j;
-                    if (d >= a.D) continue;
-                    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-                    int key = 0;
-                    for (; key + 4 <= it.Lk; key += 4) {
-                        s0 += load16<BF16>(a.v, (vrow0 + key) * vstride + vcol0 + d);
-                        s1 += load16<BF16>(a.v, (vrow0 + key + 1) * vstride + vcol0 + d);
-                        s2 += load16<BF16>(a.v, (vrow0 + key + 2) * vstride + vcol0 + d);
-                        s3 += load16<BF16>(a.v, (vrow0 + key + 3) * vstride + vcol0 + d);
-                    }
-                    for (; key < it.Lk; ++key) s0 += load16<BF16>(a.v, (vrow0 + key) * vstride + vcol0 + d);
-                    mv[j] = ((s0 + s1) + (s2 + s3)) / (float)it.Lk;
-                }
-            }
             const bool row_ok = qrow < it.Lq;
             const long long orow = !VARLEN ? it.unit * a.Q + qrow : (long long)(it.q_row0 + qrow);
-            uint16_t* op = static_cast<uint16_t*>(a.out);
-            const long long obase = !VARLEN ? orow * a.D : (orow * a.H + it.h) * a.D;
+            uint16_t* op = static_cast<uint16_t*>(a.out) + (!VARLEN ? orow * a.D : (orow * a.H + it.h) * a.D);
             const float inv = (!direct && l > 0.f) ? 1.f / l : 0.f;
-#pragma unroll
-            for (int cc = 0; cc < 8; ++cc) {
-                const uint32_t c0 = cc * 16;
-                if (c0 >= P.o_cols) break;
-                uint32_t o[16];
-                if (jv > 0) tmem_ld_x16(o_taddr + c0, o);
-                float vals[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) vals[e] = __uint_as_float(o[e]) * inv;
-                if (any_unseen) {
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const float m = __shfl_sync(0xffffffffu, mv[(cc * 16 + e) >> 5], (cc * 16 + e) & 31);
-                        if (direct) vals[e] = m;
-                    }
-                }
-                if (row_ok && (int)c0 < a.D) {
+            if (jv > 0) {
+#pragma unroll 1
+                for (uint32_t c0 = 0; c0 < P.o_cols; c0 += 16) {
+                    uint32_t o[16];
+                    tmem_ld_x16(o_taddr + c0, o);
                     uint32_t wv[8];
 #pragma unroll
-                    for (int e = 0; e < 16; e += 2) wv[e / 2] = pack2<BF16>(vals[e], vals[e + 1]);
-                    uint4* dst = reinterpret_cast<uint4*>(op + obase + c0);
-                    dst[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-                    if ((int)c0 + 8 < a.D) dst[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
+                    for (int e = 0; e < 16; e += 2)
+                        wv[e / 2] = pack2<BF16>(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
+                    if (row_ok && !direct && (int)c0 < a.D) {
+                        uint4* dst = reinterpret_cast<uint4*>(op + c0);
+                        dst[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                        if ((int)c0 + 8 < a.D) dst[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
+                    }
+                }
+            }
+            if (__any_sync(0xffffffffu, direct || (jv == 0 && row_ok))) {
+                // Rare: rows with no valid key whose blocks were not all visited,
+                // and rows of a sequence with no keys (written as zeros).  Lane
+                // l forms the means of columns l, l + 32, ...; each row then
+                // takes its values by shuffles.
+#pragma unroll 1
+                for (int d0 = 0; d0 < a.D; d0 += 32) {
+                    float mv = 0.f;
+                    const int d = d0 + lane;
+                    if (it.Lk > 0 && d < a.D) {
+                        const long long vrow0 = !VARLEN ? it.unit * a.K : (long long)it.k_row0;
+                        const long long vstride = !VARLEN ? a.D : (long long)a.H * a.D;
+                        const long long vcol0 = !VARLEN ? 0 : (long long)it.h * a.D;
+                        float sum = 0.f;
+#pragma unroll 1
+                        for (int key = 0; key < it.Lk; ++key) sum += load16<BF16>(a.v, (vrow0 + key) * vstride + vcol0 + d);
+                        mv = sum / (float)it.Lk;
+                    }
+#pragma unroll 1
+                    for (int e = 0; e < 32 && d0 + e < a.D; ++e) {
+                        const float m = __shfl_sync(0xffffffffu, mv, e);
+                        if (row_ok && (direct || jv == 0)) op[d0 + e] = (uint16_t)(pack2<BF16>(m, 0.f) & 0xffffu);
+                    }
                 }
             }
             if (row_ok) {
@@ -1063,6 +1082,7 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
     // ---------------------------------------------------------------- teardown
     if (warp == kProducerWarp && lane == 0 && *abort_flag) {
         // Give TMA loads already issued time to land before the CTA exits.
+#pragma unroll 1
         for (int i = 0; i < 2000; ++i) __nanosleep(1000);
     }
     tc_fence_before();
