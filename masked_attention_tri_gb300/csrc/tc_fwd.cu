@@ -156,6 +156,11 @@ cudaError_t launch_tc_fwd(const AttnParams& a, cudaStream_t stream) {
     const long long items = units * P.items_per_unit;
     if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     P.items = (int)items;
+    // Divisors of the work-item decode (each at least 1; with no items nothing is launched).
+    P.fd_ipu = make_fastdiv((uint32_t)(P.items_per_unit > 0 ? P.items_per_unit : 1));
+    P.fd_h = make_fastdiv((uint32_t)(a.H > 0 ? a.H : 1));
+    P.fd_n = make_fastdiv((uint32_t)(!a.varlen && a.N > 0 ? a.N : 1));
+    P.fd_per = make_fastdiv((uint32_t)(a.varlen && units > 0 ? units : 1));
     const int sms = num_sms();
     if (sms <= 0) return cudaErrorInvalidDevice;
     const int grid = P.items < sms ? P.items : sms;

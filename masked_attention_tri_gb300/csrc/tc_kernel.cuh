@@ -25,10 +25,6 @@
 //   warp 4*NQ+2        bias producer (triangle form): TMA loads of bias tiles
 //                      and the dense-mask bits, so that waiting for a free
 //                      bias stage never holds back a K/V load;
-//   warp 4*NQ+3        (NQ = 2 only) idle: it completes the third warpgroup.
-// With NQ = 2 the third warpgroup hands registers to the two softmax
-// warpgroups (setmaxnreg, executed inside each role's branch so that every
-// code region has one register limit).
 // Tensor memory: S_i at columns [128 i, 128 i + 128), O_i after all S tiles.
 // With NQ = 2 the MMAs of one tile run while the other tile's softmax does:
 // the tensor core alternates between the two query tiles.
@@ -71,6 +67,24 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;        // rescale O when the row max grows by > 2^8
 constexpr long long kTimeoutCycles = 4000000000LL;
 
+// Division by a divisor fixed at launch, for 0 <= n < 2^31 (multiply-high
+// and shift with a host-computed magic number, Granlund and Montgomery's
+// round-up method): a handful of instructions instead of a full division.
+struct FastDiv {
+    uint32_t d, m, l;
+#ifdef __CUDACC__
+    __device__ __forceinline__ uint32_t div(uint32_t n) const { return (__umulhi(n, m) + n) >> l; }
+#endif
+};
+inline FastDiv make_fastdiv(uint32_t d) {
+    FastDiv f;
+    f.d = d;
+    f.l = 0;
+    while ((1ull << f.l) < d) ++f.l;
+    f.m = (uint32_t)((((1ull << 32) * ((1ull << f.l) - d)) / d) + 1);
+    return f;
+}
+
 struct TcParams {
     CUtensorMap tm_q;
     CUtensorMap tm_k;
@@ -96,6 +110,10 @@ struct TcParams {
     uint32_t o_col0;    // first TMEM column of O_0
     uint32_t o_cols;    // TMEM columns per O tile
     int mask_kind;      // triangle: 0 none, 1 kv_lengths, 2 dense
+    FastDiv fd_ipu;     // items_per_unit
+    FastDiv fd_n;       // N (triangle)
+    FastDiv fd_h;       // H
+    FastDiv fd_per;     // num_seqs * H (packed form)
     // Folded softmax (packed form, scale > 0): the softmax reads raw S = Q K^T
     // and applies s inside the exponent.
     float scale_log2e;  // s * log2(e)
@@ -169,10 +187,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded wait: returns false if the CTA is aborting or the wait ran out.
-// Inline everywhere (no calls: code regions after setmaxnreg must not call
-// functions compiled for another register limit).
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status) {
-    if (mbar_test(bar, parity)) return true;
+// The common case (phase already complete) is an inline test; the waiting
+// loop is one out-of-line function shared by every call site, which keeps
+// the code small.
+static __device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                  int* status) {
     const long long t0 = clock64();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -185,6 +204,9 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
             }
         }
     }
+}
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status) {
+    return mbar_test(bar, parity) || wait_bar_slow(bar, parity, abort_flag, status);
 }
 
 // Bounded wait that ignores the abort flag (teardown drains only).
@@ -332,11 +354,12 @@ __device__ Item<NQ> decode(const TcParams& P, int item) {
         it.n_part[i] = 0;
     }
     if constexpr (!VARLEN) {
-        const int qp = item % P.items_per_unit;
-        const int u2 = item / P.items_per_unit;  // ((b*H + h)*N + n): n fastest, so bias tiles are reused from L2
-        const int n = u2 % a.N;
-        it.h = (u2 / a.N) % a.H;
-        it.b = u2 / (a.N * a.H);
+        const uint32_t u2 = P.fd_ipu.div((uint32_t)item);  // ((b*H + h)*N + n): n fastest, so bias tiles are reused from L2
+        const int qp = item - (int)(u2 * P.fd_ipu.d);
+        const uint32_t bh = P.fd_n.div(u2);
+        const int n = (int)(u2 - bh * P.fd_n.d);
+        it.b = (int)P.fd_h.div(bh);
+        it.h = (int)(bh - (uint32_t)it.b * P.fd_h.d);
         it.bn = (long long)it.b * a.N + n;
         it.unit = it.bn * a.H + it.h;
         it.Lq = a.Q;
@@ -359,11 +382,11 @@ __device__ Item<NQ> decode(const TcParams& P, int item) {
         return it;
     } else {
         // Heaviest q blocks first (a later q block sees more causal kv blocks).
-        const int per = a.num_seqs * a.H;
-        const int qp = P.items_per_unit - 1 - item / per;
-        const int sh = item % per;
-        it.seq = sh / a.H;
-        it.h = sh % a.H;
+        const uint32_t qq = P.fd_per.div((uint32_t)item);
+        const int qp = P.items_per_unit - 1 - (int)qq;
+        const uint32_t sh = (uint32_t)item - qq * P.fd_per.d;
+        it.seq = (int)P.fd_h.div(sh);
+        it.h = (int)(sh - (uint32_t)it.seq * P.fd_h.d);
         it.b = 0;
         it.bn = 0;
         it.unit = 0;
@@ -463,29 +486,9 @@ __device__ __forceinline__ void for_each_tile(const Item<NQ>& it, F&& f) {
 // The kernel
 // ---------------------------------------------------------------------------
 
-// Block size: NQ softmax warpgroups + producer, MMA and bias warps (with
-// NQ = 2, a full third warpgroup: 384 threads launched with 168 registers
-// each).
+// Block size: NQ softmax warpgroups + producer, MMA and bias warps.
 template <int NQ>
-constexpr int kThreads = NQ == 2 ? 384 : NQ * 128 + 96;
-// Register split for NQ = 2: 2 x 128 x softmax + 128 x other equals the 384 x 168
-// registers of the launch.  The packed form's MMA thread walks the BlockMask
-// lists and needs more registers than the triangle form's.
-template <bool VARLEN>
-constexpr int kRegSoftmax = VARLEN ? 208 : 216;
-template <bool VARLEN>
-constexpr int kRegOther = VARLEN ? 88 : 72;
-static_assert(2 * 128 * kRegSoftmax<false> + 128 * kRegOther<false> <= 384 * 168, "register split exceeds the launch");
-static_assert(2 * 128 * kRegSoftmax<true> + 128 * kRegOther<true> <= 384 * 168, "register split exceeds the launch");
-
-template <int NQ, bool VARLEN>
-__device__ __forceinline__ void regs_other() {
-    if constexpr (NQ == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegOther<VARLEN>));
-}
-template <int NQ, bool VARLEN>
-__device__ __forceinline__ void regs_softmax() {
-    if constexpr (NQ == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegSoftmax<VARLEN>));
-}
+constexpr int kThreads = NQ * 128 + 96;
 
 template <int NQ, bool VARLEN, bool BF16, bool BIAS_F32, bool FOLD>
 __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_constant__ TcParams P) {
@@ -564,7 +567,6 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------- producer: Q, K, V tiles
-        regs_other<NQ, VARLEN>();
         uint32_t kv_it = 0, q_it = 0;
         bool ok = true;
         for (int item = blockIdx.x; item < P.items && ok; item += gridDim.x) {
@@ -618,7 +620,6 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
         if (!ok) *abort_flag = 1;
     } else if (!VARLEN && warp == kBiasWarp) {
         // ---------------------------------- producer: bias tiles (+ dense-mask bits)
-        regs_other<NQ, VARLEN>();
         uint32_t b_it[NQ];
 #pragma unroll
         for (int i = 0; i < NQ; ++i) b_it[i] = 0;
@@ -660,7 +661,6 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
         if (!ok) *abort_flag = 1;
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------------ MMA
-        regs_other<NQ, VARLEN>();
         if (lane == 0) {
             uint32_t kv_it = 0, q_it = 0;
             uint32_t p_it[NQ];
@@ -694,9 +694,9 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
                     const uint64_t vd = sw128_desc(v_smem(st), kBox, 1024);
                     const uint32_t d = tmem + P.o_col0 + i * P.o_cols;
                     const uint32_t pa = tmem + i * 128;
-                    mma_ts(d, pa, vd, P.idesc_pv, npv[i] > 0 ? 1u : 0u);
-#pragma unroll
-                    for (int kk = 1; kk < kBN / 16; ++kk) mma_ts(d, pa + kk * 8, vd + (uint64_t)kk * 128, P.idesc_pv, 1u);
+#pragma unroll 1
+                    for (int kk = 0; kk < kBN / 16; ++kk)
+                        mma_ts(d, pa + kk * 8, vd + (uint64_t)kk * 128, P.idesc_pv, (npv[i] > 0 || kk > 0) ? 1u : 0u);
                     ++npv[i];
                 };
                 for_each_tile<NQ, VARLEN>(it, [&](int, uint32_t ps, uint32_t) -> bool {
@@ -765,7 +765,6 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
         __syncwarp();
     } else if (warp < 4 * NQ) {
         // -------------------------------------------------------------- softmax
-        regs_softmax<NQ, VARLEN>();
         const int slot = warp / 4;
         const int wq = warp % 4;               // TMEM lane quarter
         const int r = wq * 32 + lane;          // row within the q tile
@@ -829,96 +828,110 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
                 ++s_it;
                 tc_fence_after();
 
-                // ---- x: the row's 128 values of this tile (logits, or raw S in
-                // the folded form), all in registers.
-                float x[128];
-                {
-                    uint32_t sr[128];
-                    tmem_ld_x128(s_taddr, sr);
-                    if constexpr (FOLD) {
+                // ---- Pass 1, two chunks of 64 keys: x = s S + bias (or raw S in the
+                // folded form), masking at a boundary, running max; x goes back to
+                // the chunk's TMEM columns.  The loops stay rolled so that the
+                // softmax code fits the instruction cache next to the other roles.
+                float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll 1
+                for (int c = 0; c < 2; ++c) {
+                    float x[64];
+                    {
+                        uint32_t sr[64];
+                        tmem_ld_x64(s_taddr + 64 * c, sr);
+                        if constexpr (FOLD) {
 #pragma unroll
-                        for (int j = 0; j < 128; ++j) x[j] = __uint_as_float(sr[j]);
-                    } else if constexpr (VARLEN) {
+                            for (int j = 0; j < 64; ++j) x[j] = __uint_as_float(sr[j]);
+                        } else if constexpr (VARLEN) {
 #pragma unroll
-                        for (int j = 0; j < 128; j += 2) {
-                            const float2 r2 =
-                                __fmul2_rn(make_float2(__uint_as_float(sr[j]), __uint_as_float(sr[j + 1])), scale2);
-                            x[j] = r2.x;
-                            x[j + 1] = r2.y;
-                        }
-                    } else if constexpr (!BIAS_F32) {
-#pragma unroll
-                        for (int g = 0; g < 16; ++g) {  // 8 keys per 16-byte chunk
-                            const uint4 wv = *reinterpret_cast<const uint4*>(
-                                gbase + boff + (g >> 3) * kBox + ((((uint32_t)g & 7u) ^ rsw) << 4));
-                            const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float2 b2 = unpack2<BF16>(ww[e]);
-                                const int j = 8 * g + 2 * e;
-                                const float2 r2 = __ffma2_rn(
-                                    make_float2(__uint_as_float(sr[j]), __uint_as_float(sr[j + 1])), scale2, b2);
+                            for (int j = 0; j < 64; j += 2) {
+                                const float2 r2 =
+                                    __fmul2_rn(make_float2(__uint_as_float(sr[j]), __uint_as_float(sr[j + 1])), scale2);
                                 x[j] = r2.x;
                                 x[j + 1] = r2.y;
                             }
-                        }
-                    } else {
+                        } else if constexpr (!BIAS_F32) {
+                            const uint32_t bbox = boff + (uint32_t)c * kBox;  // keys 64c .. 64c+63: box c
 #pragma unroll
-                        for (int g = 0; g < 32; ++g) {  // 4 keys per 16-byte chunk
-                            const uint4 wv = *reinterpret_cast<const uint4*>(
-                                gbase + boff + (g >> 3) * kBox + ((((uint32_t)g & 7u) ^ rsw) << 4));
-                            const int j = 4 * g;
-                            const float2 r0 = __ffma2_rn(make_float2(__uint_as_float(sr[j]), __uint_as_float(sr[j + 1])),
-                                                         scale2, make_float2(__uint_as_float(wv.x), __uint_as_float(wv.y)));
-                            const float2 r1 =
-                                __ffma2_rn(make_float2(__uint_as_float(sr[j + 2]), __uint_as_float(sr[j + 3])), scale2,
-                                           make_float2(__uint_as_float(wv.z), __uint_as_float(wv.w)));
-                            x[j] = r0.x;
-                            x[j + 1] = r0.y;
-                            x[j + 2] = r1.x;
-                            x[j + 3] = r1.y;
+                            for (int g = 0; g < 8; ++g) {  // 8 keys per 16-byte chunk
+                                const uint4 wv =
+                                    *reinterpret_cast<const uint4*>(gbase + bbox + ((((uint32_t)g) ^ rsw) << 4));
+                                const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const float2 b2 = unpack2<BF16>(ww[e]);
+                                    const int j = 8 * g + 2 * e;
+                                    const float2 r2 = __ffma2_rn(
+                                        make_float2(__uint_as_float(sr[j]), __uint_as_float(sr[j + 1])), scale2, b2);
+                                    x[j] = r2.x;
+                                    x[j + 1] = r2.y;
+                                }
+                            }
+                        } else {
+#pragma unroll
+                            for (int g = 0; g < 16; ++g) {  // 4 keys per 16-byte chunk; keys 64c.. in boxes 2c, 2c+1
+                                const uint4 wv = *reinterpret_cast<const uint4*>(
+                                    gbase + boff + (uint32_t)(2 * c + (g >> 3)) * kBox + ((((uint32_t)g & 7u) ^ rsw) << 4));
+                                const int j = 4 * g;
+                                const float2 r0 =
+                                    __ffma2_rn(make_float2(__uint_as_float(sr[j]), __uint_as_float(sr[j + 1])), scale2,
+                                               make_float2(__uint_as_float(wv.x), __uint_as_float(wv.y)));
+                                const float2 r1 =
+                                    __ffma2_rn(make_float2(__uint_as_float(sr[j + 2]), __uint_as_float(sr[j + 3])), scale2,
+                                               make_float2(__uint_as_float(wv.z), __uint_as_float(wv.w)));
+                                x[j] = r0.x;
+                                x[j + 1] = r0.y;
+                                x[j + 2] = r1.x;
+                                x[j + 3] = r1.y;
+                            }
                         }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 64; j += 8) {
+                        m0 = max3(m0, x[j], x[j + 1]);
+                        m1 = max3(m1, x[j + 2], x[j + 3]);
+                        m2 = max3(m2, x[j + 4], x[j + 5]);
+                        m3 = max3(m3, x[j + 6], x[j + 7]);
+                    }
+                    if constexpr (!FOLD) {  // the folded form's values are S itself
+                        uint32_t xs[64];
+#pragma unroll
+                        for (int j = 0; j < 64; ++j) xs[j] = __float_as_uint(x[j]);
+                        tmem_st_x64(s_taddr + 64 * c, xs);
                     }
                 }
-                // ---- Masking (tiles at a boundary only): the values make a round
-                // trip through TMEM so that this rarely taken path is a short
-                // loop over 32-key chunks instead of 128 unrolled selects.  Per
-                // chunk: vm bit j = key key0+32c+j is valid, em bit j = it exists.
+                tmem_st_wait();  // the masking pass and pass 2 read what pass 1 wrote
+                // ---- Masking (tiles at a boundary only), in place in TMEM, 8 keys at
+                // a time; the tile max is taken again over the masked values.
                 if (!all_valid) {
-                    {
-                        uint32_t xs[128];
-#pragma unroll
-                        for (int j = 0; j < 128; ++j) xs[j] = __float_as_uint(x[j]);
-                        tmem_st_x128(s_taddr, xs);
-                        tmem_st_wait();
-                    }
+                    m0 = m1 = m2 = m3 = -INFINITY;
 #pragma unroll 1
-                    for (int c = 0; c < 4; ++c) {
-                        const int k0 = 32 * c;
-                        const uint32_t em = low_bits(nexist - k0);
+                    for (int g = 0; g < kBN / 8; ++g) {
+                        const int k0 = 8 * g;
+                        const uint32_t em = low_bits(nexist - k0) & 0xffu;
                         uint32_t vm = em & low_bits(vlim - key0 - k0);
                         if constexpr (!VARLEN) {
-                            if (P.mask_kind == 2) vm &= *reinterpret_cast<const uint32_t*>(gbase + mwoff + 4u * c);
+                            if (P.mask_kind == 2)
+                                vm &= *reinterpret_cast<const uint32_t*>(gbase + mwoff + 4u * (uint32_t)(g >> 2)) >> (8 * (g & 3));
                         } else {
                             if (causal) vm &= low_bits(qrow - key0 - k0 + 1);
                         }
-                        if (__any_sync(0xffffffffu, vm != 0xffffffffu)) {
-                            uint32_t xc[32];
-                            tmem_ld_x32(s_taddr + k0, xc);
+                        uint32_t v[8];
+                        tmem_ld_x8(s_taddr + k0, v);
+                        // tcgen05.st is .sync.aligned: the whole warp takes this branch
+                        // or none of it (rows differ under a causal mask).
+                        if (__any_sync(0xffffffffu, (vm & 0xffu) != 0xffu)) {
 #pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                xc[j] = ((vm >> j) & 1u) ? xc[j]
-                                                         : __float_as_uint(((em >> j) & 1u) ? kMaskVal : -INFINITY);
-                            tmem_st_x32(s_taddr + k0, xc);
+                            for (int j = 0; j < 8; ++j)
+                                v[j] = ((vm >> j) & 1u) ? v[j] : __float_as_uint(((em >> j) & 1u) ? kMaskVal : -INFINITY);
+                            tmem_st_x8(s_taddr + k0, v);
                         }
+                        m0 = max3(m0, __uint_as_float(v[0]), __uint_as_float(v[1]));
+                        m1 = max3(m1, __uint_as_float(v[2]), __uint_as_float(v[3]));
+                        m2 = max3(m2, __uint_as_float(v[4]), __uint_as_float(v[5]));
+                        m3 = max3(m3, __uint_as_float(v[6]), __uint_as_float(v[7]));
                     }
                     tmem_st_wait();
-                    {
-                        uint32_t xs[128];
-                        tmem_ld_x128(s_taddr, xs);
-#pragma unroll
-                        for (int j = 0; j < 128; ++j) x[j] = __uint_as_float(xs[j]);
-                    }
                 }
                 if constexpr (!VARLEN) {
                     mbar_arrive(bias_empty(slot, bs));  // bias and mask words of this stage have been read
@@ -926,14 +939,6 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
                 }
 
                 // ---- Tile max (units of this form) and its logit in natural units.
-                float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
-#pragma unroll
-                for (int j = 0; j < 128; j += 8) {
-                    m0 = max3(m0, x[j], x[j + 1]);
-                    m1 = max3(m1, x[j + 2], x[j + 3]);
-                    m2 = max3(m2, x[j + 4], x[j + 5]);
-                    m3 = max3(m3, x[j + 6], x[j + 7]);
-                }
                 const float tm = fmaxf(max3(m0, m1, m2), m3);
                 float tm_nat;
                 if constexpr (FOLD) tm_nat = tm > -FLT_MAX ? tm * a.scale : (tm == -FLT_MAX ? kMasked : -INFINITY);
@@ -963,8 +968,8 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
                     }
                 }
 
-                // ---- P = 2^((x - m_ref) log2 e), packed to 16-bit pairs into
-                // columns [16c, 16c + 16).  A row with no real logit yet (every
+                // ---- P = 2^((x - m_ref) log2 e), packed to 16-bit pairs (keys 2i,
+                // 2i+1 in column i).  A row with no real logit yet (every
                 // value masked or absent) takes weights of exactly 1 for masked
                 // keys and 0 for absent ones: x + (-kMaskVal) is then 0 or -inf.
                 const bool live = m_ref > kMaskVal;
@@ -972,18 +977,23 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
                 const float nb = live ? -m_ref * unit_l2e : -kMaskVal;
                 const float2 nb2 = make_float2(nb, nb);
                 float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+                // ---- Pass 2, two chunks of 64 keys: P into columns [32c, 32c + 32)
+                // (chunk c's values were read before any of them is overwritten).
+#pragma unroll 1
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t xr[64];
+                    tmem_ld_x64(s_taddr + 64 * c, xr);
+                    uint32_t pk[32];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float2 y = __ffma2_rn(make_float2(x[32 * c + 2 * j], x[32 * c + 2 * j + 1]), ul2, nb2);
+                    for (int j = 0; j < 32; ++j) {
+                        const float2 y =
+                            __ffma2_rn(make_float2(__uint_as_float(xr[2 * j]), __uint_as_float(xr[2 * j + 1])), ul2, nb2);
                         const float2 p = make_float2(ex2(y.x), ex2(y.y));
                         if (j & 1) acc1 = __fadd2_rn(acc1, p);
                         else acc0 = __fadd2_rn(acc0, p);
                         pk[j] = pack2<BF16>(p.x, p.y);
                     }
-                    tmem_st_x16(s_taddr + 16 * c, pk);
+                    tmem_st_x32(s_taddr + 32 * c, pk);
                 }
                 l += (acc0.x + acc0.y) + (acc1.x + acc1.y);
                 tmem_st_wait();
@@ -1075,8 +1085,6 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
             }
         }
         if (!ok) *abort_flag = 1;
-    } else {
-        regs_other<NQ, VARLEN>();  // idle warps of the third warpgroup
     }
 
     // ---------------------------------------------------------------- teardown
