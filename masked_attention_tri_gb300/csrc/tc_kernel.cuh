@@ -886,6 +886,26 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
                             }
                         }
                     }
+                    // Masking (tiles at a boundary only; the branch is uniform across
+                    // the warp).  Per 32 keys: vm bit j = key valid, em bit j = key exists.
+                    if (!all_valid) {
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int k0 = 64 * c + 32 * h;
+                            const uint32_t em = low_bits(nexist - k0);
+                            uint32_t vm = em & low_bits(vlim - key0 - k0);
+                            if constexpr (!VARLEN) {
+                                if (P.mask_kind == 2)
+                                    vm &= *reinterpret_cast<const uint32_t*>(gbase + mwoff + 4u * (uint32_t)(2 * c + h));
+                            } else {
+                                if (causal) vm &= low_bits(qrow - key0 - k0 + 1);
+                            }
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                x[32 * h + j] =
+                                    ((vm >> j) & 1u) ? x[32 * h + j] : (((em >> j) & 1u) ? kMaskVal : -INFINITY);
+                        }
+                    }
 #pragma unroll
                     for (int j = 0; j < 64; j += 8) {
                         m0 = max3(m0, x[j], x[j + 1]);
@@ -893,50 +913,18 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
                         m2 = max3(m2, x[j + 4], x[j + 5]);
                         m3 = max3(m3, x[j + 6], x[j + 7]);
                     }
-                    if constexpr (!FOLD) {  // the folded form's values are S itself
+                    if (!FOLD || !all_valid) {  // unmasked folded values are S itself
                         uint32_t xs[64];
 #pragma unroll
                         for (int j = 0; j < 64; ++j) xs[j] = __float_as_uint(x[j]);
                         tmem_st_x64(s_taddr + 64 * c, xs);
                     }
                 }
-                tmem_st_wait();  // the masking pass and pass 2 read what pass 1 wrote
-                // ---- Masking (tiles at a boundary only), in place in TMEM, 8 keys at
-                // a time; the tile max is taken again over the masked values.
-                if (!all_valid) {
-                    m0 = m1 = m2 = m3 = -INFINITY;
-#pragma unroll 1
-                    for (int g = 0; g < kBN / 8; ++g) {
-                        const int k0 = 8 * g;
-                        const uint32_t em = low_bits(nexist - k0) & 0xffu;
-                        uint32_t vm = em & low_bits(vlim - key0 - k0);
-                        if constexpr (!VARLEN) {
-                            if (P.mask_kind == 2)
-                                vm &= *reinterpret_cast<const uint32_t*>(gbase + mwoff + 4u * (uint32_t)(g >> 2)) >> (8 * (g & 3));
-                        } else {
-                            if (causal) vm &= low_bits(qrow - key0 - k0 + 1);
-                        }
-                        uint32_t v[8];
-                        tmem_ld_x8(s_taddr + k0, v);
-                        // tcgen05.st is .sync.aligned: the whole warp takes this branch
-                        // or none of it (rows differ under a causal mask).
-                        if (__any_sync(0xffffffffu, (vm & 0xffu) != 0xffu)) {
-#pragma unroll
-                            for (int j = 0; j < 8; ++j)
-                                v[j] = ((vm >> j) & 1u) ? v[j] : __float_as_uint(((em >> j) & 1u) ? kMaskVal : -INFINITY);
-                            tmem_st_x8(s_taddr + k0, v);
-                        }
-                        m0 = max3(m0, __uint_as_float(v[0]), __uint_as_float(v[1]));
-                        m1 = max3(m1, __uint_as_float(v[2]), __uint_as_float(v[3]));
-                        m2 = max3(m2, __uint_as_float(v[4]), __uint_as_float(v[5]));
-                        m3 = max3(m3, __uint_as_float(v[6]), __uint_as_float(v[7]));
-                    }
-                    tmem_st_wait();
-                }
                 if constexpr (!VARLEN) {
                     mbar_arrive(bias_empty(slot, bs));  // bias and mask words of this stage have been read
                     ++bias_it;
                 }
+                tmem_st_wait();  // pass 2 reads what pass 1 wrote
 
                 // ---- Tile max (units of this form) and its logit in natural units.
                 const float tm = fmaxf(max3(m0, m1, m2), m3);
