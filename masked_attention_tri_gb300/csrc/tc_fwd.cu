@@ -75,10 +75,7 @@ bool choose_geometry(TcParams& P, bool varlen, int& NQ) {
     // (Q buffers, K/V stages, bias stages per query tile), in order of preference
     const int prefs[][3] = {{2, 3, 2}, {2, 3, 1}, {2, 2, 2}, {2, 2, 1}, {1, 3, 2}, {1, 3, 1}, {1, 2, 2}, {1, 2, 1}};
     for (int nq = 2; nq >= (varlen ? 2 : 1); --nq) {
-        // Triangle form, two query tiles, O of at most 64 columns: P gets
-        // columns of its own (S 2 x 128, P 2 x 64, O 2 x 64 fit the 512).
-        const bool sep = !varlen && nq == 2 && P.o_cols <= 64;
-        const uint32_t cols = nq * 128 + (sep ? nq * 64 : 0) + nq * P.o_cols;
+        const uint32_t cols = nq * 128 + nq * P.o_cols;
         if (cols > 512) continue;
         for (const auto& pr : prefs) {
             P.q_bufs = pr[0];
@@ -86,9 +83,7 @@ bool choose_geometry(TcParams& P, bool varlen, int& NQ) {
             P.bias_stages = varlen ? 0 : pr[2];
             if (make_layout(nq, P).total + 1024 <= kSmemLimit) {
                 NQ = nq;
-                P.sep_p = sep ? 1 : 0;
-                P.p_col0 = nq * 128;
-                P.o_col0 = nq * 128 + (sep ? nq * 64 : 0);
+                P.o_col0 = nq * 128;
                 P.tmem_cols = 32;
                 while (P.tmem_cols < cols) P.tmem_cols <<= 1;
                 return true;

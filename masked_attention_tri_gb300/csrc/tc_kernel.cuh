@@ -108,9 +108,6 @@ struct TcParams {
     uint32_t idesc_pv;
     uint32_t tmem_cols;
     uint32_t o_col0;    // first TMEM column of O_0
-    int sep_p;          // 1: P_i has columns of its own (p_col0 + 64 i), so the next S_i
-                        //    can be computed while PV of the current tile is pending
-    uint32_t p_col0;    // first TMEM column of P_0 (sep_p)
     uint32_t o_cols;    // TMEM columns per O tile
     int mask_kind;      // triangle: 0 none, 1 kv_lengths, 2 dense
     FastDiv fd_ipu;     // items_per_unit
@@ -138,7 +135,7 @@ __host__ __device__ inline Layout make_layout(int NQ, const TcParams& P) {
     L.bias = L.kv + P.kv_stages * 2 * P.tile_bytes;
     L.maskw = L.bias + NQ * P.bias_stages * P.bias_bytes;
     L.bars = L.maskw + NQ * (P.bias_stages > 0 ? P.bias_stages : 1) * 16;
-    L.nbars = NQ * P.q_bufs + P.q_bufs + 2 * P.kv_stages + 2 * NQ * P.bias_stages + 4 * NQ + 1;
+    L.nbars = NQ * P.q_bufs + P.q_bufs + 2 * P.kv_stages + 2 * NQ * P.bias_stages + 3 * NQ + 1;
     L.tmem_slot = L.bars + 8 * L.nbars;
     L.abort_flag = L.tmem_slot + 4;
     L.total = L.abort_flag + 4;
@@ -525,7 +522,6 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
     auto p_full = [&](int i) { return bar(b0 + 2 * S + 2 * NQ * BS + NQ + i); };
     auto o_full = [&](int i) { return bar(b0 + 2 * S + 2 * NQ * BS + 2 * NQ + i); };
     const uint32_t drain = bar(b0 + 2 * S + 2 * NQ * BS + 3 * NQ);
-    auto pv_done = [&](int i) { return bar(b0 + 2 * S + 2 * NQ * BS + 3 * NQ + 1 + i); };  // sep_p only
 
     auto q_smem = [&](int i, int qb) { return base + L.q + (uint32_t)(i * QB + qb) * P.tile_bytes; };
     auto k_smem = [&](int s) { return base + L.kv + (uint32_t)s * 2u * P.tile_bytes; };
@@ -541,7 +537,6 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
             mbar_init(s_full(i), 1);
             mbar_init(p_full(i), 128);
             mbar_init(o_full(i), 1);
-            mbar_init(pv_done(i), 1);
 #pragma unroll 1
             for (int s = 0; s < BS; ++s) {
                 mbar_init(bias_full(i, s), 1);
@@ -694,13 +689,11 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
                     npv[i] = 0;
                 }
                 int prev = -1;
-                // O_i += P_i V, with V from stage `st` and P_i in its own columns
-                // (sep_p) or in S_i's.
-                const bool sep = !VARLEN && P.sep_p;
+                // O_i += P_i V, with V from stage `st` and P_i in S_i's columns.
                 auto issue_pv = [&](int i, int st) {
                     const uint64_t vd = sw128_desc(v_smem(st), kBox, 1024);
                     const uint32_t d = tmem + P.o_col0 + i * P.o_cols;
-                    const uint32_t pa = tmem + (sep ? P.p_col0 + 64 * i : 128 * i);
+                    const uint32_t pa = tmem + i * 128;
 #pragma unroll 1
                     for (int kk = 0; kk < kBN / 16; ++kk)
                         mma_ts(d, pa + kk * 8, vd + (uint64_t)kk * 128, P.idesc_pv, (npv[i] > 0 || kk > 0) ? 1u : 0u);
@@ -722,12 +715,12 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
                     const uint64_t kd = sw128_desc(k_smem(st), 16, 1024);
 #pragma unroll
                     for (int i = 0; i < NQ; ++i) {
-                        const bool had = (pend >> i) & 1u;
-                        if (had) {  // the softmax of slot i's previous tile is done with S_i
+                        if ((pend >> i) & 1u) {
                             ok = wait_bar(p_full(i), p_it[i]++ & 1, abort_flag, a.status);
                             if (!ok) return false;
                             tc_fence_after();
-                            if (!sep) issue_pv(i, pst[i]);  // P_i lives in S_i: PV before the next QK
+                            issue_pv(i, pst[i]);
+                            pend &= ~(1u << i);
                         }
                         if ((ps >> i) & 1u) {
                             ok = wait_kv();
@@ -737,13 +730,6 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
                             for (int kk = 1; kk < P.ksteps; ++kk)
                                 mma_ss(sd, qd[i] + kstep(kk), kd + kstep(kk), P.idesc_qk, 1u);
                             mma_commit(s_full(i));
-                        }
-                        if (had && sep) {  // P_i has its own columns: the next S_i went first
-                            issue_pv(i, pst[i]);
-                            mma_commit(pv_done(i));
-                        }
-                        pend &= ~(1u << i);
-                        if ((ps >> i) & 1u) {
                             pend |= 1u << i;
                             pst[i] = st;
                         }
@@ -785,9 +771,6 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const uint32_t s_taddr = tmem + lane_off + slot * 128;
         const uint32_t o_taddr = tmem + lane_off + P.o_col0 + slot * P.o_cols;
-        const bool sep = !VARLEN && P.sep_p;
-        const uint32_t p_taddr = tmem + lane_off + (sep ? P.p_col0 + 64 * slot : slot * 128);
-        uint32_t pv_it = 0;
         // 128B swizzle: 16-byte chunk c of row r sits at chunk c ^ (r % 8).
         const uint32_t rsw = (uint32_t)(r & 7);
         const uint32_t rrow = (uint32_t)r * 128u;
@@ -949,14 +932,6 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
                 if constexpr (FOLD) tm_nat = tm > -FLT_MAX ? tm * a.scale : (tm == -FLT_MAX ? kMasked : -INFINITY);
                 else tm_nat = tm;
                 m_true = fmaxf(m_true, tm_nat);
-                if (sep && jv > 0) {
-                    // O (for a rescale) and P_i (about to be rewritten) need the PV of
-                    // this slot's previous tile to have finished.
-                    ok = __all_sync(0xffffffffu, wait_bar(pv_done(slot), pv_it & 1, abort_flag, a.status));
-                    ++pv_it;
-                    if (!ok) return false;
-                    tc_fence_after();
-                }
                 // Reference max m_ref (units of this form) used in the exponent.
                 if (jv == 0) {
                     m_ref = tm;
@@ -966,8 +941,8 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
                     const bool need = (m_new - m_ref) * unit_l2e > kRescaleLog2;
                     if (__any_sync(0xffffffffu, need)) {
                         // Raise the reference max to the current one; O (complete
-                        // through this slot's previous tile: its PV finished before
-                        // this S was committed, or pv_done said so) and l scale by alpha.
+                        // through this slot's previous tile, whose PV finished
+                        // before this S was committed) and l scale by alpha.
                         const float alpha = ex2((m_ref - m_new) * unit_l2e);
                         l *= alpha;
                         m_ref = m_new;
@@ -1006,7 +981,7 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
                         else acc0 = __fadd2_rn(acc0, p);
                         pk[j] = pack2<BF16>(p.x, p.y);
                     }
-                    tmem_st_x32(p_taddr + 32 * c, pk);
+                    tmem_st_x32(s_taddr + 32 * c, pk);
                 }
                 l += (acc0.x + acc0.y) + (acc1.x + acc1.y);
                 tmem_st_wait();
