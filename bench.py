@@ -43,6 +43,33 @@ L2_BYTES = 129 * 1024 * 1024
 ESIZE = {"f32": 4, "f16": 2, "bf16": 2}
 
 
+def kernel_source_hash() -> str:
+    """SHA-256 over the library's CUDA sources and public headers (path + content)."""
+    import glob
+    import hashlib
+    files = sorted(glob.glob(os.path.join(ROOT, "masked_attention_tri_gb300", "csrc", "*.cu")) +
+                   glob.glob(os.path.join(ROOT, "masked_attention_tri_gb300", "csrc", "*.cuh")) +
+                   glob.glob(os.path.join(ROOT, "masked_attention_tri_gb300", "csrc", "*.h")) +
+                   glob.glob(os.path.join(ROOT, "include", "*.h")))
+    h = hashlib.sha256()
+    for f in files:
+        h.update(os.path.relpath(f, ROOT).encode())
+        h.update(b"\0")
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def measured_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when the kernel has changed."""
+    path = os.path.join(ROOT, "profiles", f"tc_fwd_kernel_{workload}.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as fh:
+        rec = json.load(fh)
+    return rec["dram_bytes_per_launch"] if rec.get("source_sha256") == kernel_source_hash() else None
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -418,7 +445,7 @@ def main():
     if bound == "hbm":
         achieved = byts / (ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": None}
+                "frac": achieved / peaks["hbm_gbs"], "traffic": measured_traffic(args.workload)}
     else:
         achieved = flops / (ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
