@@ -269,6 +269,17 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                  : "memory");
 }
 
+// One lane of a converged warp (elect.sync); the same lane every time.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -661,7 +672,10 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
         if (!ok) *abort_flag = 1;
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------------ MMA
-        if (lane == 0) {
+        // The whole warp runs this loop, so descriptors and counters are
+        // warp-uniform values; one elected lane issues each tcgen05 instruction.
+        const bool leader = elect_one();
+        {
             uint32_t kv_it = 0, q_it = 0;
             uint32_t p_it[NQ];
 #pragma unroll
@@ -675,7 +689,8 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
                 const Item<NQ> it = decode<NQ, VARLEN>(P, item);
                 if (!it.any) continue;
                 const int qb = q_it % QB;
-                for (int i = 0; i < NQ && ok; ++i) ok = wait_bar(q_full(i, qb), (q_it / QB) & 1, abort_flag, a.status);
+                for (int i = 0; i < NQ && ok; ++i)
+                    ok = __all_sync(0xffffffffu, wait_bar(q_full(i, qb), (q_it / QB) & 1, abort_flag, a.status));
                 ++q_it;
                 if (!ok) break;
                 uint64_t qd[NQ];
@@ -696,7 +711,7 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
                     const uint32_t pa = tmem + i * 128;
 #pragma unroll 1
                     for (int kk = 0; kk < kBN / 16; ++kk)
-                        mma_ts(d, pa + kk * 8, vd + (uint64_t)kk * 128, P.idesc_pv, (npv[i] > 0 || kk > 0) ? 1u : 0u);
+                        if (leader) mma_ts(d, pa + kk * 8, vd + (uint64_t)kk * 128, P.idesc_pv, (npv[i] > 0 || kk > 0) ? 1u : 0u);
                     ++npv[i];
                 };
                 for_each_tile<NQ, VARLEN>(it, [&](int, uint32_t ps, uint32_t) -> bool {
@@ -708,7 +723,8 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
                     auto wait_kv = [&]() -> bool {
                         if (kv_ready) return true;
                         kv_ready = true;
-                        if (!wait_bar(kv_full(st), (kv_it / S) & 1, abort_flag, a.status)) return false;
+                        if (!__all_sync(0xffffffffu, wait_bar(kv_full(st), (kv_it / S) & 1, abort_flag, a.status)))
+                            return false;
                         tc_fence_after();
                         return true;
                     };
@@ -716,7 +732,7 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
 #pragma unroll
                     for (int i = 0; i < NQ; ++i) {
                         if ((pend >> i) & 1u) {
-                            ok = wait_bar(p_full(i), p_it[i]++ & 1, abort_flag, a.status);
+                            ok = __all_sync(0xffffffffu, wait_bar(p_full(i), p_it[i]++ & 1, abort_flag, a.status));
                             if (!ok) return false;
                             tc_fence_after();
                             issue_pv(i, pst[i]);
@@ -726,15 +742,17 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
                             ok = wait_kv();
                             if (!ok) return false;
                             const uint32_t sd = tmem + i * 128;
-                            mma_ss(sd, qd[i], kd, P.idesc_qk, 0u);
-                            for (int kk = 1; kk < P.ksteps; ++kk)
-                                mma_ss(sd, qd[i] + kstep(kk), kd + kstep(kk), P.idesc_qk, 1u);
-                            mma_commit(s_full(i));
+                            if (leader) {
+                                mma_ss(sd, qd[i], kd, P.idesc_qk, 0u);
+                                for (int kk = 1; kk < P.ksteps; ++kk)
+                                    mma_ss(sd, qd[i] + kstep(kk), kd + kstep(kk), P.idesc_qk, 1u);
+                                mma_commit(s_full(i));
+                            }
                             pend |= 1u << i;
                             pst[i] = st;
                         }
                     }
-                    if (prev >= 0) mma_commit(kv_empty(prev));  // no pending PV reads stage `prev` any more
+                    if (prev >= 0 && leader) mma_commit(kv_empty(prev));  // no pending PV reads stage `prev` any more
                     ok = wait_kv();  // keeps the phases in step if no slot used this tile
                     if (!ok) return false;
                     ++kv_it;
@@ -742,24 +760,24 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
                     return true;
                 });
                 if (!ok) break;
-                mma_commit(q_empty(qb));  // every QK of the item is issued: its Q buffers may be refilled
+                if (leader) mma_commit(q_empty(qb));  // every QK of the item is issued: its Q buffers may be refilled
 #pragma unroll
                 for (int i = 0; i < NQ; ++i) {
                     if (!ok) break;
                     if ((pend >> i) & 1u) {
-                        ok = wait_bar(p_full(i), p_it[i]++ & 1, abort_flag, a.status);
+                        ok = __all_sync(0xffffffffu, wait_bar(p_full(i), p_it[i]++ & 1, abort_flag, a.status));
                         if (!ok) break;
                         tc_fence_after();
                         issue_pv(i, pst[i]);
                     }
-                    if (npv[i] > 0) mma_commit(o_full(i));
+                    if (npv[i] > 0 && leader) mma_commit(o_full(i));
                 }
                 if (!ok) break;
-                if (prev >= 0) mma_commit(kv_empty(prev));
+                if (prev >= 0 && leader) mma_commit(kv_empty(prev));
             }
-            if (!ok) *abort_flag = 1;
+            if (!ok && leader) *abort_flag = 1;
             // Let every MMA issued so far finish before TMEM is released.
-            mma_commit(drain);
+            if (leader) mma_commit(drain);
             wait_bar_drain(drain, 0);
         }
         __syncwarp();
