@@ -546,12 +546,12 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
 #pragma unroll 1
             for (int qb = 0; qb < QB; ++qb) mbar_init(q_full(i, qb), 1);
             mbar_init(s_full(i), 1);
-            mbar_init(p_full(i), 128);
+            mbar_init(p_full(i), 4);  // one arrival per softmax warp
             mbar_init(o_full(i), 1);
 #pragma unroll 1
             for (int s = 0; s < BS; ++s) {
                 mbar_init(bias_full(i, s), 1);
-                mbar_init(bias_empty(i, s), 128);  // every softmax thread of the tile
+                mbar_init(bias_empty(i, s), 4);  // one arrival per softmax warp of the tile
             }
         }
 #pragma unroll 1
@@ -939,7 +939,8 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
                     }
                 }
                 if constexpr (!VARLEN) {
-                    mbar_arrive(bias_empty(slot, bs));  // bias and mask words of this stage have been read
+                    __syncwarp();  // every lane of the warp has read its bias row and the mask words
+                    if (lane == 0) mbar_arrive(bias_empty(slot, bs));
                     ++bias_it;
                 }
                 tmem_st_wait();  // pass 2 reads what pass 1 wrote
@@ -1004,7 +1005,8 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
                 l += (acc0.x + acc0.y) + (acc1.x + acc1.y);
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(p_full(slot));
+                __syncwarp();  // one arrival per warp once all its lanes' P is in TMEM
+                if (lane == 0) mbar_arrive(p_full(slot));
                 ++jv;
                 return true;
             });
