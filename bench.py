@@ -254,43 +254,69 @@ def time_varlen(ta, c, dev, steps, warmup, flush):
 
 
 def e2e_triangle(ta, c, dev, steps, warmup):
-    """Same metric through the public API with pinned host buffers; copies inside the timed region."""
+    """Same metric through the public API with pinned host buffers; copies inside the timed region.
+
+    Every step copies its inputs host -> device, runs `triangle_attention` and
+    copies O, lse and max device -> host.  Steps are pipelined the way a
+    server would run them: two sets of device buffers, the input copies of
+    step i+1 on one stream, the kernel of step i on the compute stream and the
+    result copies of step i-1 on a third, ordered by events.  The timed region
+    runs from the first input copy to the last result copy.
+    """
     hq, hk, hv, hb = (t.pin_memory() for t in (c.q, c.k, c.v, c.bias))
     hkl = c.kv_lengths.pin_memory() if c.kv_lengths is not None else None
     hm = c.mask.pin_memory() if c.mask is not None else None
-    dq, dk, dv, db = (torch.empty_like(t, device=dev) for t in (hq, hk, hv, hb))
-    dkl = torch.empty_like(hkl, device=dev) if hkl is not None else None
-    dm = torch.empty_like(hm, device=dev) if hm is not None else None
-    dout = torch.empty_like(dq)
-    ho = torch.empty_like(hq).pin_memory()
-    hl = torch.empty(c.B, c.N, c.H, c.Q, 1, dtype=torch.float32).pin_memory()
-    hmx = torch.empty_like(hl).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hb) + ((hkl,) if hkl is not None else ())
-              + ((hm,) if hm is not None else ()))
-    d2h = ho.numel() * ho.element_size() + 2 * hl.numel() * 4
+    h_in = [t for t in (hq, hk, hv, hb, hkl, hm) if t is not None]
+    d_in = [[torch.empty_like(t, device=dev) for t in h_in] for _ in range(2)]
+    d_out = [torch.empty_like(hq, device=dev) for _ in range(2)]
+    d_lse = [torch.empty(c.B, c.N, c.H, c.Q, 1, device=dev, dtype=torch.float32) for _ in range(2)]
+    d_mx = [torch.empty_like(d_lse[0]) for _ in range(2)]
+    ho = [torch.empty_like(hq).pin_memory() for _ in range(2)]
+    hl = [torch.empty(c.B, c.N, c.H, c.Q, 1, dtype=torch.float32).pin_memory() for _ in range(2)]
+    hmx = [torch.empty_like(hl[0]).pin_memory() for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = ho[0].numel() * ho[0].element_size() + 2 * hl[0].numel() * 4
 
-    def step():
-        for d, h in ((dq, hq), (dk, hk), (dv, hv), (db, hb)):
-            d.copy_(h, non_blocking=True)
-        if dkl is not None:
-            dkl.copy_(hkl, non_blocking=True)
-        if dm is not None:
-            dm.copy_(hm, non_blocking=True)
-        o, lse, mx = ta.triangle_attention(dq, dk, dv, db, mask=dm, scale=c.scale, return_aux=True, kv_lengths=dkl,
-                                           out=dout)
-        ho.copy_(o, non_blocking=True)
-        hl.copy_(lse, non_blocking=True)
-        hmx.copy_(mx, non_blocking=True)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    s_k = torch.cuda.current_stream(dev)
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    in_done, k_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+    started = [False, False]
 
-    for _ in range(warmup):
-        step()
+    def step(i):
+        b = i % 2
+        with torch.cuda.stream(s_in):
+            if started[b]:
+                s_in.wait_event(k_done[b])  # the kernel of step i-2 has read buffer b
+            for d, h in zip(d_in[b], h_in):
+                d.copy_(h, non_blocking=True)
+            in_done[b].record(s_in)
+        s_k.wait_event(in_done[b])
+        if started[b]:
+            s_k.wait_event(out_done[b])  # the results of step i-2 have left buffer b
+        it = iter(d_in[b])
+        dq, dk, dv, db = next(it), next(it), next(it), next(it)
+        dkl = next(it) if hkl is not None else None
+        dm = next(it) if hm is not None else None
+        ta.triangle_attention(dq, dk, dv, db, mask=dm, scale=c.scale, return_aux=True, kv_lengths=dkl,
+                              out=d_out[b], lse=d_lse[b], mx=d_mx[b])
+        k_done[b].record(s_k)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(k_done[b])
+            ho[b].copy_(d_out[b], non_blocking=True)
+            hl[b].copy_(d_lse[b], non_blocking=True)
+            hmx[b].copy_(d_mx[b], non_blocking=True)
+            out_done[b].record(s_out)
+        started[b] = True
+
+    for i in range(warmup):
+        step(i)
     torch.cuda.synchronize(dev)
-    stream = torch.cuda.current_stream(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
-        step()
-    e1.record(stream)
+    e0.record(s_in)
+    for i in range(warmup, warmup + steps):
+        step(i)
+    e1.record(s_out)
     torch.cuda.synchronize(dev)
     return e0.elapsed_time(e1) / steps, h2d, d2h
 

@@ -35,14 +35,17 @@ def _stream(device: torch.device) -> int:
     return torch.cuda.current_stream(device).cuda_stream
 
 
-def triangle_attention(q, k, v, bias, mask=None, scale=None, return_aux=False, *, kv_lengths=None, out=None):
+def triangle_attention(q, k, v, bias, mask=None, scale=None, return_aux=False, *, kv_lengths=None, out=None,
+                       lse=None, mx=None):
     """Triangle-attention forward (cuEquivariance triangle_attention page: formula, Parameters).
 
     q (B,N,H,Q,D), k/v (B,N,H,K,D), bias (B,1,H,Q,K); for B=1 the 4-D forms
     (N,H,Q,D) / (1,H,Q,K) / (N,1,1,K) are accepted.  mask: bool/uint8
     (B,N,1,1,K); kv_lengths: int32 (B,N,1,1,1) or (B,N); at most one of them.
     scale defaults to 1/sqrt(D).  Returns O, or (O, lse, max) with
-    return_aux (lse / max fp32 shaped (B,N,H,Q,1)).
+    return_aux (lse / max fp32 shaped (B,N,H,Q,1)).  out, lse, mx may be given
+    preallocated (contiguous, on q's device); lse / mx are written only with
+    return_aux.
     """
     if mask is not None and kv_lengths is not None:
         raise ValueError("pass either mask or kv_lengths, not both")
@@ -89,10 +92,18 @@ def triangle_attention(q, k, v, bias, mask=None, scale=None, return_aux=False, *
         out = torch.empty_like(q)
     else:
         _need(out, "out", dev)
-    lse = mx = None
     if return_aux:
-        lse = torch.empty(B, N, H, Q, 1, device=dev, dtype=torch.float32)
-        mx = torch.empty(B, N, H, Q, 1, device=dev, dtype=torch.float32)
+        for name, t in (("lse", lse), ("mx", mx)):
+            if t is not None:
+                _need(t, name, dev)
+                if t.dtype != torch.float32 or t.numel() != B * N * H * Q:
+                    raise ValueError(f"{name} must be float32 with B*N*H*Q elements")
+        if lse is None:
+            lse = torch.empty(B, N, H, Q, 1, device=dev, dtype=torch.float32)
+        if mx is None:
+            mx = torch.empty(B, N, H, Q, 1, device=dev, dtype=torch.float32)
+    else:
+        lse = mx = None
     with torch.cuda.device(dev):
         abi.tri_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _DT[q.dtype], _ptr(bias), _DT[bias.dtype], _ptr(m8), _ptr(kl),
                          B, N, H, Q, K, D, s, _ptr(out), _ptr(lse), _ptr(mx), _stream(dev))
