@@ -14,7 +14,10 @@
  *
  * Conventions shared by every entry point:
  *   - All tensors are dense, contiguous, row-major device buffers owned by the
- *     caller; every pointer must be 16-byte aligned.  The library allocates
+ *     caller.  q, k, v, bias and out must be 16-byte aligned (they are read
+ *     and written in 16-byte vectors and by the TMA); lse, max, kv_lengths,
+ *     the sequence offsets and the block lists need 4-byte alignment.  A
+ *     misaligned pointer returns TA_ERR_INVALID_ARG.  The library allocates
  *     no device memory per call and keeps no state between calls besides one
  *     device-side status word (see tri_attn_get_status).
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
