@@ -61,13 +61,16 @@ def kernel_source_hash() -> str:
 
 
 def measured_traffic(workload: str):
-    """DRAM bytes per launch from the committed ncu summary, or None when the kernel has changed."""
-    path = os.path.join(ROOT, "profiles", f"tc_fwd_kernel_{workload}.json")
-    if not os.path.exists(path):
-        return None
-    with open(path) as fh:
-        rec = json.load(fh)
-    return rec["dram_bytes_per_launch"] if rec.get("source_sha256") == kernel_source_hash() else None
+    """DRAM bytes per launch from a committed ncu summary (profiles/<kernel>_<workload>.json) taken
+    on the current sources, or None when the kernel has changed since the counters were taken."""
+    import glob
+    cur = kernel_source_hash()
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", f"*_{workload}.json"))):
+        with open(path) as fh:
+            rec = json.load(fh)
+        if rec.get("workload") == workload and rec.get("source_sha256") == cur:
+            return rec["dram_bytes_per_launch"]
+    return None
 
 
 def load_peaks():

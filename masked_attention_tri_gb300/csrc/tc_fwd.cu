@@ -1,19 +1,22 @@
 // tc_fwd.cu -- host side of the tcgen05 forward: TMA descriptors, geometry
 // (query tiles per CTA, pipeline depths, tensor-memory columns), the choice
 // of the folded softmax for the packed form, and the launch.  The kernel
-// itself is in tc_kernel.cuh.
+// itself is in tc_kernel.cuh; triangle problems with D <= 64 go to the
+// key-split kernel of tc_split.cuh.
 
 #include <cudaTypedefs.h>
 
 #include <cmath>
+#include <cstdlib>
 #include <mutex>
 
-#include "tc_kernel.cuh"
+#include "tc_split.cuh"
 
 namespace triattn {
 namespace tc {
 
 TRIATTN_TC_VARIANTS(TRIATTN_TC_EXTERN)
+TRIATTN_SPLIT_VARIANTS(TRIATTN_SPLIT_EXTERN)
 
 namespace {
 
@@ -93,6 +96,33 @@ bool choose_geometry(TcParams& P, bool varlen, int& NQ) {
     return false;
 }
 
+// The key-split kernel (triangle form, D <= 64): one query tile, three S
+// buffers and O in 512 tensor-memory columns; Q buffers, K/V stages and bias
+// stages as shared memory allows.
+bool choose_split_geometry(TcParams& P) {
+    const int prefs[][3] = {{2, 3, 2}, {2, 3, 1}, {2, 2, 2}, {2, 2, 1}, {1, 2, 1}};
+    for (const auto& pr : prefs) {
+        P.q_bufs = pr[0];
+        P.kv_stages = pr[1];
+        P.bias_stages = pr[2];
+        if (make_split_layout(P).total + 1024 <= kSmemLimit) {
+            P.o_col0 = 384;
+            P.tmem_cols = 512;
+            return true;
+        }
+    }
+    return false;
+}
+
+// TRIATTN_TRI_SPLIT=0 keeps D <= 64 triangle problems on the two-tile kernel.
+bool split_enabled() {
+    static const bool on = [] {
+        const char* e = getenv("TRIATTN_TRI_SPLIT");
+        return !(e && e[0] == '0');
+    }();
+    return on;
+}
+
 template <bool VARLEN, bool BF16, bool BIAS_F32, bool FOLD>
 cudaError_t launch_nq(int NQ, const TcParams& P, int grid, cudaStream_t stream) {
     if constexpr (VARLEN) {
@@ -150,7 +180,9 @@ cudaError_t launch_tc_fwd(const AttnParams& a, cudaStream_t stream) {
         fold = a.scale > 0.f && std::isfinite(a.scale);
     }
     int NQ = 1;
-    if (!choose_geometry(P, a.varlen != 0, NQ)) return cudaErrorInvalidConfiguration;
+    const bool split = !a.varlen && D <= 64 && split_enabled();
+    if (split ? !choose_split_geometry(P) : !choose_geometry(P, a.varlen != 0, NQ))
+        return cudaErrorInvalidConfiguration;
     P.items_per_unit = (P.nqt + NQ - 1) / NQ;
     const long long units = !a.varlen ? (long long)a.B * a.N * a.H : (long long)a.num_seqs * a.H;
     const long long items = units * P.items_per_unit;
@@ -173,6 +205,10 @@ cudaError_t launch_tc_fwd(const AttnParams& a, cudaStream_t stream) {
                     : launch_nq<true, false, false, false>(NQ, P, grid, stream);
     }
     (void)fold;
+    if (split) {
+        if (bf16) return a.bias_f32 ? launch_split<true, true>(P, grid, stream) : launch_split<true, false>(P, grid, stream);
+        return a.bias_f32 ? launch_split<false, true>(P, grid, stream) : launch_split<false, false>(P, grid, stream);
+    }
     if (bf16) return a.bias_f32 ? launch_nq<false, true, true, false>(NQ, P, grid, stream)
                                 : launch_nq<false, true, false, false>(NQ, P, grid, stream);
     return a.bias_f32 ? launch_nq<false, false, true, false>(NQ, P, grid, stream)
