@@ -324,6 +324,23 @@ __device__ __forceinline__ uint32_t low_bits(int n) {
     return n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : ((1u << n) - 1u));
 }
 
+// Position in a ring of n pipeline stages: the stage, the parity of the
+// current pass over the ring, and whether the stage was used before (its
+// "empty" barrier then has to complete first, in the previous pass's parity).
+// Advanced one use at a time, so the per-tile path has no runtime division.
+struct StageRing {
+    int idx;
+    uint32_t ph;
+    bool wrapped;
+    __device__ __forceinline__ void next(int n) {
+        if (++idx == n) {
+            idx = 0;
+            ph ^= 1u;
+            wrapped = true;
+        }
+    }
+};
+
 // ---------------------------------------------------------------------------
 // Work items and their key-tile streams
 // ---------------------------------------------------------------------------
@@ -578,16 +595,16 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------- producer: Q, K, V tiles
-        uint32_t kv_it = 0, q_it = 0;
+        StageRing kr = {0, 0u, false}, qr = {0, 0u, false};
         bool ok = true;
         for (int item = blockIdx.x; item < P.items && ok; item += gridDim.x) {
             const Item<NQ> it = decode<NQ, VARLEN>(P, item);
             if (!it.any) continue;
-            // Q of every slot goes to buffer set q_it % QB (a slot without rows
+            // Q of every slot goes to buffer set qr.idx (a slot without rows
             // gets an out-of-range, zero-filled box), so each q_full completes
             // once per item with work.
-            const int qb = q_it % QB;
-            if (lane == 0 && q_it >= (uint32_t)QB) ok = wait_bar(q_empty(qb), ((q_it / QB) - 1) & 1, abort_flag, a.status);
+            const int qb = qr.idx;
+            if (lane == 0 && qr.wrapped) ok = wait_bar(q_empty(qb), qr.ph ^ 1u, abort_flag, a.status);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             if (lane == 0) {
@@ -603,11 +620,10 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
                     }
                 }
             }
-            ++q_it;
+            qr.next(QB);
             for_each_tile<NQ, VARLEN>(it, [&](int kb, uint32_t, uint32_t) -> bool {
-                const int st = kv_it % S;
-                if (lane == 0 && kv_it >= (uint32_t)S)
-                    ok = wait_bar(kv_empty(st), ((kv_it / S) - 1) & 1, abort_flag, a.status);
+                const int st = kr.idx;
+                if (lane == 0 && kr.wrapped) ok = wait_bar(kv_empty(st), kr.ph ^ 1u, abort_flag, a.status);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) return false;
                 if (lane == 0) {
@@ -624,16 +640,16 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
                         }
                     }
                 }
-                ++kv_it;
+                kr.next(S);
                 return true;
             });
         }
         if (!ok) *abort_flag = 1;
     } else if (!VARLEN && warp == kBiasWarp) {
         // ---------------------------------- producer: bias tiles (+ dense-mask bits)
-        uint32_t b_it[NQ];
+        StageRing br[NQ];
 #pragma unroll
-        for (int i = 0; i < NQ; ++i) b_it[i] = 0;
+        for (int i = 0; i < NQ; ++i) br[i] = {0, 0u, false};
         bool ok = true;
         for (int item = blockIdx.x; item < P.items && ok; item += gridDim.x) {
             const Item<NQ> it = decode<NQ, VARLEN>(P, item);
@@ -642,9 +658,8 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
 #pragma unroll
                 for (int i = 0; i < NQ; ++i) {
                     if (!((ps >> i) & 1u)) continue;
-                    const int bs = b_it[i] % BS;
-                    if (lane == 0 && b_it[i] >= (uint32_t)BS)
-                        ok = wait_bar(bias_empty(i, bs), ((b_it[i] / BS) - 1) & 1, abort_flag, a.status);
+                    const int bs = br[i].idx;
+                    if (lane == 0 && br[i].wrapped) ok = wait_bar(bias_empty(i, bs), br[i].ph ^ 1u, abort_flag, a.status);
                     ok = __shfl_sync(0xffffffffu, ok, 0);
                     if (!ok) return false;
                     if (P.mask_kind == 2) {
@@ -664,7 +679,7 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
                             tma_load_3d(bias_smem(i, bs) + bx * kBox, &P.tm_bias, kb * kBN + bx * P.bias_box_cols,
                                         it.qt[i] * kBM, it.b * a.H + it.h, bias_full(i, bs));
                     }
-                    ++b_it[i];
+                    br[i].next(BS);
                 }
                 return true;
             });
@@ -676,7 +691,7 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
         // warp-uniform values; one elected lane issues each tcgen05 instruction.
         const bool leader = elect_one();
         {
-            uint32_t kv_it = 0, q_it = 0;
+            StageRing kr = {0, 0u, false}, qr = {0, 0u, false};
             uint32_t p_it[NQ];
 #pragma unroll
             for (int i = 0; i < NQ; ++i) p_it[i] = 0;
@@ -688,10 +703,10 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
             for (int item = blockIdx.x; item < P.items && ok; item += gridDim.x) {
                 const Item<NQ> it = decode<NQ, VARLEN>(P, item);
                 if (!it.any) continue;
-                const int qb = q_it % QB;
+                const int qb = qr.idx;
                 for (int i = 0; i < NQ && ok; ++i)
-                    ok = __all_sync(0xffffffffu, wait_bar(q_full(i, qb), (q_it / QB) & 1, abort_flag, a.status));
-                ++q_it;
+                    ok = __all_sync(0xffffffffu, wait_bar(q_full(i, qb), qr.ph, abort_flag, a.status));
+                qr.next(QB);
                 if (!ok) break;
                 uint64_t qd[NQ];
                 uint32_t pend = 0;  // bit i: P_i of slot i's last tile is still to be multiplied by V
@@ -718,12 +733,12 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
                     // Per slot: PV of its previous tile (frees S_i; that V is
                     // resident already), then QK of this tile.  Only QK waits for
                     // this tile's K/V, so a late load never holds back a PV.
-                    const int st = kv_it % S;
+                    const int st = kr.idx;
                     bool kv_ready = false;
                     auto wait_kv = [&]() -> bool {
                         if (kv_ready) return true;
                         kv_ready = true;
-                        if (!__all_sync(0xffffffffu, wait_bar(kv_full(st), (kv_it / S) & 1, abort_flag, a.status)))
+                        if (!__all_sync(0xffffffffu, wait_bar(kv_full(st), kr.ph, abort_flag, a.status)))
                             return false;
                         tc_fence_after();
                         return true;
@@ -755,7 +770,7 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
                     if (prev >= 0 && leader) mma_commit(kv_empty(prev));  // no pending PV reads stage `prev` any more
                     ok = wait_kv();  // keeps the phases in step if no slot used this tile
                     if (!ok) return false;
-                    ++kv_it;
+                    kr.next(S);
                     prev = st;
                     return true;
                 });
@@ -792,7 +807,8 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
         // 128B swizzle: 16-byte chunk c of row r sits at chunk c ^ (r % 8).
         const uint32_t rsw = (uint32_t)(r & 7);
         const uint32_t rrow = (uint32_t)r * 128u;
-        uint32_t s_it = 0, bias_it = 0, o_it = 0;
+        uint32_t s_it = 0, o_it = 0;
+        StageRing br = {0, 0u, false};
         const float2 scale2 = make_float2(a.scale, a.scale);
         // Folded form (packed sequences, no bias): values are in units of S
         // (x = s S); a masked key holds -FLT_MAX there (its logit is -1e9).
@@ -835,8 +851,8 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
                 uint32_t boff = 0, mwoff = 0;  // this row's bias / the mask words, from the aligned base
                 int bs = 0;
                 if constexpr (!VARLEN) {
-                    bs = bias_it % BS;
-                    ok = __all_sync(0xffffffffu, wait_bar(bias_full(slot, bs), (bias_it / BS) & 1, abort_flag, a.status));
+                    bs = br.idx;
+                    ok = __all_sync(0xffffffffu, wait_bar(bias_full(slot, bs), br.ph, abort_flag, a.status));
                     if (!ok) return false;
                     boff = bias_smem(slot, bs) - base + rrow;
                     mwoff = L.maskw + (uint32_t)(slot * BS + bs) * 16u;
@@ -941,7 +957,7 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
                 if constexpr (!VARLEN) {
                     __syncwarp();  // every lane of the warp has read its bias row and the mask words
                     if (lane == 0) mbar_arrive(bias_empty(slot, bs));
-                    ++bias_it;
+                    br.next(BS);
                 }
                 tmem_st_wait();  // pass 2 reads what pass 1 wrote
 

@@ -62,22 +62,6 @@ __host__ __device__ inline SplitLayout make_split_layout(const TcParams& P) {
     return L;
 }
 
-// Position in a ring of n pipeline stages: the stage, the parity of the
-// current pass over the ring, and whether the stage was used before (its
-// "empty" barrier then has to complete first, in the previous pass's parity).
-struct StageRing {
-    int idx;
-    uint32_t ph;
-    bool wrapped;
-    __device__ __forceinline__ void next(int n) {
-        if (++idx == n) {
-            idx = 0;
-            ph ^= 1u;
-            wrapped = true;
-        }
-    }
-};
-
 // A position in the CTA's stream of key tiles: the current item with work,
 // its key-tile count, the next tile in it and the item's number among the
 // CTA's items with work.
