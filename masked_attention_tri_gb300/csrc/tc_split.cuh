@@ -303,11 +303,14 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
         for (int i = 0; i < 3 && ok; ++i) ok = issue_qk();
         while (ok && has_p) {
             const int b = sp.idx;
-            ok = __all_sync(0xffffffffu, wait_bar(p_full(b), sp.ph, abort_flag, a.status));
-            if (!ok) break;
             const int st = vp.idx;
-            ok = __all_sync(0xffffffffu, wait_bar(v_full(st), vp.ph, abort_flag, a.status));
-            if (!ok) break;
+            const bool ready = mbar_test(p_full(b), sp.ph) & mbar_test(v_full(st), vp.ph);
+            if (!__all_sync(0xffffffffu, ready)) {
+                ok = __all_sync(0xffffffffu, wait_bar(p_full(b), sp.ph, abort_flag, a.status));
+                if (!ok) break;
+                ok = __all_sync(0xffffffffu, wait_bar(v_full(st), vp.ph, abort_flag, a.status));
+                if (!ok) break;
+            }
             tc_fence_after();
             const uint64_t vd = sw128_desc(v_smem(st), kBox, 1024);
             const uint32_t d = tmem + P.o_col0 + (pc.qi & 1u) * P.o_cols;
@@ -412,16 +415,32 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
             uint16_t* op = orow_p + (long long)h * half_o;
             const float inv = l_all > 0.f ? 1.f / l_all : 0.f;
             const int dlim = a.D - h * (int)half_o;  // columns of this half that exist
-#pragma unroll 1
-            for (uint32_t c0 = 0; c0 < half_o; c0 += 8) {
-                uint32_t o[8];
-                tmem_ld_x8(oa + c0, o);
-                uint32_t wv[4];
+            if (half_o == 32) {  // D in (48, 64]: this warp's 32 columns in one load
+                uint32_t o[32];
+                tmem_ld_x32(oa, o);
+                uint32_t wv[16];
 #pragma unroll
-                for (int e = 0; e < 8; e += 2)
-                    wv[e / 2] = pack2<BF16>(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
-                if (pe.row_ok && !pe.direct && (int)c0 < dlim)
-                    *reinterpret_cast<uint4*>(op + c0) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                for (int e = 0; e < 16; ++e)
+                    wv[e] = pack2<BF16>(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+                if (pe.row_ok && !pe.direct) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        if (8 * i < dlim)
+                            reinterpret_cast<uint4*>(op)[i] =
+                                make_uint4(wv[4 * i], wv[4 * i + 1], wv[4 * i + 2], wv[4 * i + 3]);
+                }
+            } else {
+#pragma unroll 1
+                for (uint32_t c0 = 0; c0 < half_o; c0 += 8) {
+                    uint32_t o[8];
+                    tmem_ld_x8(oa + c0, o);
+                    uint32_t wv[4];
+#pragma unroll
+                    for (int e = 0; e < 8; e += 2)
+                        wv[e / 2] = pack2<BF16>(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
+                    if (pe.row_ok && !pe.direct && (int)c0 < dlim)
+                        *reinterpret_cast<uint4*>(op + c0) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                }
             }
             if (h == 0 && __any_sync(0xffffffffu, pe.direct && pe.row_ok)) {
                 // Lane l forms the means of columns l and l + 32; rows take them by shuffles.
@@ -467,13 +486,17 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
                 const bool all_valid = P.mask_kind != 2 && key0 + kBN <= vlim;
                 const int nexist = a.K - key0;
                 const int bs = br.idx;
-                ok = __all_sync(0xffffffffu, wait_bar(bias_full(bs), br.ph, abort_flag, a.status));
-                if (!ok) break;
+                // Both barriers tested at once; the bounded waits only when one is not ready.
+                const bool ready = mbar_test(bias_full(bs), br.ph) & mbar_test(s_full(sb), (uint32_t)sph);
+                if (!__all_sync(0xffffffffu, ready)) {
+                    ok = __all_sync(0xffffffffu, wait_bar(bias_full(bs), br.ph, abort_flag, a.status));
+                    if (!ok) break;
+                    ok = __all_sync(0xffffffffu, wait_bar(s_full(sb), (uint32_t)sph, abort_flag, a.status));
+                    if (!ok) break;
+                }
                 const uint32_t boff = bias_smem(bs) - base + rrow;
                 const uint32_t mwoff = L.maskw + (uint32_t)bs * 16u;
                 const uint32_t s_taddr = tmem + lane_off + 128u * (uint32_t)sb;
-                ok = __all_sync(0xffffffffu, wait_bar(s_full(sb), (uint32_t)sph, abort_flag, a.status));
-                if (!ok) break;
                 tc_fence_after();
 
                 // ---- x: this warp's 64 values of the row (logits).
