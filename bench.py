@@ -229,16 +229,22 @@ def time_triangle(ta, c, dev, steps, warmup, flush=None):
     return tot / steps
 
 
-def time_varlen(ta, c, dev, steps, warmup, flush):
+def time_varlen(ta, c, dev, steps, warmup, flush, qkv_packed=False):
+    """qkv_packed: q, k, v read in place from one (total, 3, H, D) buffer (NVTE_QKV_INTERLEAVED)."""
     q, k, v = c.q.to(dev), c.k.to(dev), c.v.to(dev)
     cu = c.cu_seqlens.to(dev)
     bm = ta.BlockMask.from_kv_blocks(c.kv_num_blocks.to(dev), c.kv_indices.to(dev), c.full_kv_num_blocks.to(dev),
                                      c.full_kv_indices.to(dev), BLOCK_SIZE=c.block, mask_mod=c.mask_mod)
     out = torch.empty_like(q)
+    qkv = torch.stack([q, k, v], dim=1).contiguous() if qkv_packed else None
 
     def launch():
-        ta.varlen_attention(q, k, v, cu, cu, c.max_seqlen, c.max_seqlen, block_mask=bm, scale=c.scale, out=out,
-                            return_aux=True)
+        if qkv_packed:
+            ta.varlen_attention_qkvpacked(qkv, cu, c.max_seqlen, block_mask=bm, scale=c.scale, out=out,
+                                          return_aux=True)
+        else:
+            ta.varlen_attention(q, k, v, cu, cu, c.max_seqlen, c.max_seqlen, block_mask=bm, scale=c.scale, out=out,
+                                return_aux=True)
 
     for _ in range(warmup):
         launch()
@@ -507,6 +513,12 @@ def main():
                                      "two_term_roofline_frac": max(f / (peaks["bf16_tflops"] * 1e12),
                                                                    b / (peaks["hbm_gbs"] * 1e9)) / (t * 1e-3),
                                      "lengths": vc.lengths.tolist(), "l2": "flushed before each launch"}
+        t = time_varlen(ta, vc, dev, 50, 5, flush, qkv_packed=True)
+        per_config["bf16_varlen_qkvpacked"] = {
+            "us": 1e3 * t, "tflops": f / (t * 1e-3) / 1e12,
+            "pct_bf16_peak": 100 * f / (t * 1e-3) / (peaks["bf16_tflops"] * 1e12),
+            "two_term_roofline_frac": max(f / (peaks["bf16_tflops"] * 1e12), b / (peaks["hbm_gbs"] * 1e9)) / (t * 1e-3),
+            "layout": "one (total, 3, H, D) buffer read in place", "l2": "flushed before each launch"}
         per_config["bf16_long"] = {"us": 1e3 * ms, "tflops": flops / (ms * 1e-3) / 1e12,
                                    "pct_bf16_peak": 100 * flops / (ms * 1e-3) / (peaks["bf16_tflops"] * 1e12),
                                    "two_term_roofline_frac": roof["two_term_roofline_frac"],

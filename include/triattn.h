@@ -136,6 +136,38 @@ ta_status tri_attn_varlen_fwd(const void* q, const void* k, const void* v, ta_dt
                               void* out, float* lse, float* max, void* stream);
 
 /*
+ * tri_attn_varlen_fwd_strided -- tri_attn_varlen_fwd on q / k / v whose
+ * packed rows are `*_row_stride` elements apart.
+ * (Transformer Engine fused_attn.h, NVTE_QKV_Layout: NVTE_NOT_INTERLEAVED is
+ *  q, k, v each (total, H, D); NVTE_QKV_INTERLEAVED is one (total, 3, H, D)
+ *  buffer, i.e. q, k, v at element offsets 0, H*D, 2*H*D with row stride
+ *  3*H*D; NVTE_KV_INTERLEAVED keeps q (total_q, H, D) and packs k, v in one
+ *  (total_k, 2, H, D) buffer: offsets 0, H*D, row stride 2*H*D.)
+ *
+ *   q, k, v        row r, head h, element d at  base[r * row_stride + h * D + d]
+ *                  (heads contiguous within a row); every other argument,
+ *                  including the contiguous (total_q, H, D) `out`, as in
+ *                  tri_attn_varlen_fwd.
+ *   *_row_stride   elements between consecutive packed rows; 0 means H * D
+ *                  (no interleaving).  Must be >= H * D (else
+ *                  TA_ERR_INVALID_ARG) and a multiple of 16 bytes
+ *                  (fp16 / bf16: of 8 elements; fp32: of 4), else
+ *                  TA_ERR_UNSUPPORTED.  The pointers keep the 16-byte rule.
+ *   The buffers are read only; interleaved q / k / v may share memory.
+ */
+ta_status tri_attn_varlen_fwd_strided(const void* q, const void* k, const void* v, ta_dtype dtype,
+                                      const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                      int num_seqs, int total_q, int total_k,
+                                      int max_seqlen_q, int max_seqlen_k, int H, int D,
+                                      float scale,
+                                      const int32_t* kv_num_blocks, const int32_t* kv_indices,
+                                      const int32_t* full_kv_num_blocks, const int32_t* full_kv_indices,
+                                      int mask_heads, int max_q_blocks, int max_kv_blocks,
+                                      int block_q, int block_k, ta_mask_mod mask_mod,
+                                      long long q_row_stride, long long k_row_stride, long long v_row_stride,
+                                      void* out, float* lse, float* max, void* stream);
+
+/*
  * tri_attn_mask_to_kv_lengths -- dense key mask -> prefix lengths.
  * (triangle_attention page, Example: mask_to_kv_lengths(mask).)
  *

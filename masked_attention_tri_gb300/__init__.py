@@ -7,6 +7,8 @@ block-sparse (BlockMask) mask.  The work runs in libtriattn.so (hand-written
 CUDA, tcgen05 / TMA); this package only marshals tensors into its C ABI.
 """
 from . import abi
-from .api import BlockMask, get_status, mask_to_kv_lengths, triangle_attention, varlen_attention
+from .api import (BlockMask, get_status, mask_to_kv_lengths, triangle_attention, varlen_attention,
+                  varlen_attention_kvpacked, varlen_attention_qkvpacked)
 
-__all__ = ["abi", "BlockMask", "get_status", "mask_to_kv_lengths", "triangle_attention", "varlen_attention"]
+__all__ = ["abi", "BlockMask", "get_status", "mask_to_kv_lengths", "triangle_attention", "varlen_attention",
+           "varlen_attention_kvpacked", "varlen_attention_qkvpacked"]

@@ -205,11 +205,26 @@ class BlockMask:
         return 100.0 * (1.0 - float(dense.sum()) / max(1, dense.numel()))
 
 
+def _row_stride(t: torch.Tensor, name: str, device: torch.device) -> int:
+    """Row stride (elements) of a (total, H, D) view whose heads and elements are contiguous."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    _, H, D = t.shape
+    if t.stride(2) != 1 or (H > 1 and t.stride(1) != D):
+        raise ValueError(f"{name} must have contiguous heads and elements (strides (*, D, 1))")
+    return t.stride(0) if t.shape[0] > 1 else H * D
+
+
 def varlen_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, block_mask=None, scale=None,
                      return_aux=False, *, mask_mod=None, out=None):
-    """Packed-sequence forward (NVTE_NOT_INTERLEAVED layout) with an optional BlockMask.
+    """Packed-sequence forward with an optional BlockMask.
 
-    q (total_q,H,D), k/v (total_k,H,D), cu_seqlens int32 (S+1,).  Without a
+    q (total_q,H,D), k/v (total_k,H,D), cu_seqlens int32 (S+1,).  q, k, v may
+    be row-strided views (heads and elements contiguous), e.g. the slices of
+    an interleaved QKV or KV buffer (see ``varlen_attention_qkvpacked`` /
+    ``varlen_attention_kvpacked``); ``out`` is contiguous.  Without a
     block_mask every block is visited and ``mask_mod`` (None / "causal")
     applies everywhere.  Returns O, or (O, lse, max) with lse/max (H, total_q).
     """
@@ -221,7 +236,8 @@ def varlen_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seql
     dev = q.device
     if dev.type != "cuda":
         raise ValueError("varlen_attention runs on CUDA tensors only")
-    for t, nm in ((q, "q"), (k, "k"), (v, "v"), (cu_seqlens_q, "cu_seqlens_q"), (cu_seqlens_k, "cu_seqlens_k")):
+    q_rs, k_rs, v_rs = (_row_stride(t, nm, dev) for t, nm in ((q, "q"), (k, "k"), (v, "v")))
+    for t, nm in ((cu_seqlens_q, "cu_seqlens_q"), (cu_seqlens_k, "cu_seqlens_k")):
         _need(t, nm, dev)
     if q.dtype not in _DT or k.dtype != q.dtype or v.dtype != q.dtype:
         raise TypeError("q, k, v must share one dtype among float32 / float16 / bfloat16")
@@ -252,7 +268,7 @@ def varlen_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seql
         bq, bk = block_mask.BLOCK_SIZE
         mm = block_mask.mask_mod_code
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty(total_q, H, D, device=dev, dtype=q.dtype)
     else:
         _need(out, "out", dev)
     lse = mx = None
@@ -260,10 +276,34 @@ def varlen_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seql
         lse = torch.empty(H, total_q, device=dev, dtype=torch.float32)
         mx = torch.empty(H, total_q, device=dev, dtype=torch.float32)
     with torch.cuda.device(dev):
-        abi.tri_attn_varlen_fwd(_ptr(q), _ptr(k), _ptr(v), _DT[q.dtype], _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), S,
-                                total_q, k.shape[0], int(max_seqlen_q), int(max_seqlen_k), H, D, s, _ptr(kn), _ptr(ki), _ptr(fn), _ptr(fi),
-                                mask_heads, MQ, MK, bq, bk, mm, _ptr(out), _ptr(lse), _ptr(mx), _stream(dev))
+        abi.tri_attn_varlen_fwd_strided(_ptr(q), _ptr(k), _ptr(v), _DT[q.dtype], _ptr(cu_seqlens_q),
+                                        _ptr(cu_seqlens_k), S, total_q, k.shape[0], int(max_seqlen_q),
+                                        int(max_seqlen_k), H, D, s, _ptr(kn), _ptr(ki), _ptr(fn), _ptr(fi),
+                                        mask_heads, MQ, MK, bq, bk, mm, q_rs, k_rs, v_rs, _ptr(out), _ptr(lse),
+                                        _ptr(mx), _stream(dev))
     return (out, lse, mx) if return_aux else out
+
+
+def varlen_attention_qkvpacked(qkv, cu_seqlens, max_seqlen, block_mask=None, scale=None, return_aux=False, *,
+                               mask_mod=None, out=None):
+    """NVTE_QKV_INTERLEAVED (Transformer Engine fused_attn.h): one (total, 3, H, D) buffer, q and k sharing
+    cu_seqlens.  The kernels read q, k, v in place through row strides; no copy is made."""
+    if qkv.dim() != 4 or qkv.shape[1] != 3:
+        raise ValueError("expected qkv (total, 3, H, D)")
+    q, k, v = qkv.unbind(1)
+    return varlen_attention(q, k, v, cu_seqlens, cu_seqlens, max_seqlen, max_seqlen, block_mask, scale, return_aux,
+                            mask_mod=mask_mod, out=out)
+
+
+def varlen_attention_kvpacked(q, kv, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, block_mask=None,
+                              scale=None, return_aux=False, *, mask_mod=None, out=None):
+    """NVTE_KV_INTERLEAVED (Transformer Engine fused_attn.h): q (total_q, H, D) and one (total_k, 2, H, D)
+    buffer for k and v, read in place through row strides."""
+    if kv.dim() != 4 or kv.shape[1] != 2:
+        raise ValueError("expected kv (total_k, 2, H, D)")
+    k, v = kv.unbind(1)
+    return varlen_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, block_mask, scale,
+                            return_aux, mask_mod=mask_mod, out=out)
 
 
 def get_status(device=None) -> int:

@@ -116,6 +116,22 @@ TA_EXPORT ta_status tri_attn_varlen_fwd(const void* q, const void* k, const void
                                         int mask_heads, int max_q_blocks, int max_kv_blocks, int block_q,
                                         int block_k, ta_mask_mod mask_mod, void* out, float* lse, float* max,
                                         void* stream) {
+    return tri_attn_varlen_fwd_strided(q, k, v, dtype, cu_seqlens_q, cu_seqlens_k, num_seqs, total_q, total_k,
+                                       max_seqlen_q, max_seqlen_k, H, D, scale, kv_num_blocks, kv_indices,
+                                       full_kv_num_blocks, full_kv_indices, mask_heads, max_q_blocks, max_kv_blocks,
+                                       block_q, block_k, mask_mod, 0, 0, 0, out, lse, max, stream);
+}
+
+TA_EXPORT ta_status tri_attn_varlen_fwd_strided(const void* q, const void* k, const void* v, ta_dtype dtype,
+                                                const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                                int num_seqs, int total_q, int total_k, int max_seqlen_q,
+                                                int max_seqlen_k, int H, int D, float scale,
+                                                const int32_t* kv_num_blocks, const int32_t* kv_indices,
+                                                const int32_t* full_kv_num_blocks, const int32_t* full_kv_indices,
+                                                int mask_heads, int max_q_blocks, int max_kv_blocks, int block_q,
+                                                int block_k, ta_mask_mod mask_mod, long long q_row_stride,
+                                                long long k_row_stride, long long v_row_stride, void* out,
+                                                float* lse, float* max, void* stream) {
     if (!q || !k || !v || !out || !cu_seqlens_q || !cu_seqlens_k) return TA_ERR_INVALID_ARG;
     if (num_seqs <= 0 || H <= 0 || D <= 0 || max_seqlen_q < 0 || max_seqlen_k < 0) return TA_ERR_INVALID_ARG;
     if (total_q < 0 || total_k < 0) return TA_ERR_INVALID_ARG;
@@ -133,6 +149,17 @@ TA_EXPORT ta_status tri_attn_varlen_fwd(const void* q, const void* k, const void
     if (block_q != 128 || block_k != 128) return TA_ERR_UNSUPPORTED;
     if (!supported_d(dtype, D)) return TA_ERR_UNSUPPORTED;
     if ((long long)num_seqs * H * ((max_seqlen_q + 31) / 32) > 0x7fffffffLL) return TA_ERR_UNSUPPORTED;
+    // Packed-row strides (elements): 0 = H * D; at least one row of heads;
+    // 16-byte multiples (TMA row pitch, and the same rule for fp32).
+    const long long hd = (long long)H * D;
+    if (q_row_stride == 0) q_row_stride = hd;
+    if (k_row_stride == 0) k_row_stride = hd;
+    if (v_row_stride == 0) v_row_stride = hd;
+    if (q_row_stride < hd || k_row_stride < hd || v_row_stride < hd) return TA_ERR_INVALID_ARG;
+    if (q_row_stride > (1LL << 40) || k_row_stride > (1LL << 40) || v_row_stride > (1LL << 40))
+        return TA_ERR_UNSUPPORTED;
+    const int per16 = dtype == TA_F32 ? 4 : 8;
+    if (q_row_stride % per16 || k_row_stride % per16 || v_row_stride % per16) return TA_ERR_UNSUPPORTED;
     if (max_seqlen_q == 0 || total_q == 0) return TA_OK;
 
     int* status = triattn::status_word();
@@ -165,6 +192,9 @@ TA_EXPORT ta_status tri_attn_varlen_fwd(const void* q, const void* k, const void
     p.mask_mod = mask_mod;
     p.total_q = total_q;
     p.total_k = total_k;
+    p.q_rs = q_row_stride;
+    p.k_rs = k_row_stride;
+    p.v_rs = v_row_stride;
     return run(p, static_cast<cudaStream_t>(stream));
 }
 
@@ -200,4 +230,4 @@ TA_EXPORT const char* tri_attn_error_string(ta_status s) {
     }
 }
 
-TA_EXPORT int tri_attn_version(void) { return (1 << 16) | 0; }
+TA_EXPORT int tri_attn_version(void) { return (1 << 16) | 1; }

@@ -47,6 +47,7 @@ struct AttnParams {
     int mask_heads, MQ, MK, mask_mod;
     int total_q;            // rows of q/out (lse/max stride in varlen)
     int total_k;            // rows of k/v
+    long long q_rs, k_rs, v_rs;  // varlen: elements between packed rows of q, k, v (out: H * D)
 };
 
 // CUDA-core path: exact fp32 arithmetic, any dtype, both forms.

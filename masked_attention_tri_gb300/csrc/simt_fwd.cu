@@ -67,7 +67,7 @@ struct SimtState {
     float* Vs;
     float* Ps;  // this warp's [kRows][kKT]
     int D, Dp1, warp, lane;
-    long long kv_off, kv_rs;
+    long long k_off, k_rs, v_off, v_rs;
     int Lk;
     long long bias_row0;  // element offset of bias[b,0,h,q0,0] (triangle), -1 = none
     int bias_rs;
@@ -91,9 +91,8 @@ __device__ void simt_tile(SimtState<T, BT>& st, int key0, int mode) {
         int key = key0 + j;
         float kv = 0.f, vv = 0.f;
         if (key < st.Lk) {
-            long long off = st.kv_off + (long long)key * st.kv_rs + d;
-            kv = to_f(kp[off]);
-            vv = to_f(vp[off]);
+            kv = to_f(kp[st.k_off + (long long)key * st.k_rs + d]);
+            vv = to_f(vp[st.v_off + (long long)key * st.v_rs + d]);
         }
         st.Ks[j * Dp1 + d] = kv;
         st.Vs[j * D + d] = vv;
@@ -172,7 +171,7 @@ __global__ void __launch_bounds__(kWarps * 32) simt_fwd_kernel(const AttnParams 
     st.Ps = st.Vs + kKT * D + st.warp * kRows * kKT;
 
     const T* qp = static_cast<const T*>(p.q);
-    long long q_off, q_rs, lse_off;
+    long long q_off, q_rs, o_off, o_rs, lse_off;
     int Lq, qt;
     st.bias_row0 = -1;
     st.bias_rs = 0;
@@ -189,8 +188,10 @@ __global__ void __launch_bounds__(kWarps * 32) simt_fwd_kernel(const AttnParams 
         const int b = (int)(bn / p.N);
         q_off = u * p.Q * (long long)D;
         q_rs = D;
-        st.kv_off = u * p.K * (long long)D;
-        st.kv_rs = D;
+        o_off = q_off;
+        o_rs = q_rs;
+        st.k_off = st.v_off = u * p.K * (long long)D;
+        st.k_rs = st.v_rs = D;
         Lq = p.Q;
         st.Lk = p.K;
         st.bias_row0 = (((long long)b * p.H + h) * p.Q + (long long)qt * kQT) * p.K;
@@ -215,10 +216,15 @@ __global__ void __launch_bounds__(kWarps * 32) simt_fwd_kernel(const AttnParams 
             if (threadIdx.x == 0 && qt == 0 && h == 0) atomicCAS(p.status, 0, kStatusDevice);
             return;
         }
-        q_off = (long long)cq0 * p.H * D + (long long)h * D;
-        q_rs = (long long)p.H * D;
-        st.kv_off = (long long)ck0 * p.H * D + (long long)h * D;
-        st.kv_rs = (long long)p.H * D;
+        // Packed rows: q / k / v rows are q_rs / k_rs / v_rs elements apart, out rows H * D.
+        q_off = (long long)cq0 * p.q_rs + (long long)h * D;
+        q_rs = p.q_rs;
+        o_off = (long long)cq0 * p.H * D + (long long)h * D;
+        o_rs = (long long)p.H * D;
+        st.k_off = (long long)ck0 * p.k_rs + (long long)h * D;
+        st.k_rs = p.k_rs;
+        st.v_off = (long long)ck0 * p.v_rs + (long long)h * D;
+        st.v_rs = p.v_rs;
         lse_off = (long long)h * p.total_q + cq0;  // (H, total_q)
     }
     st.q0 = qt * kQT;
@@ -287,7 +293,7 @@ __global__ void __launch_bounds__(kWarps * 32) simt_fwd_kernel(const AttnParams 
 #pragma unroll
             for (int c = 0; c < kDPerLane; ++c) {
                 int d = st.lane + 32 * c;
-                if (d < D) meanv[c] += to_f(vp[st.kv_off + (long long)key * st.kv_rs + d]);
+                if (d < D) meanv[c] += to_f(vp[st.v_off + (long long)key * st.v_rs + d]);
             }
         }
 #pragma unroll
@@ -321,7 +327,7 @@ __global__ void __launch_bounds__(kWarps * 32) simt_fwd_kernel(const AttnParams 
 #pragma unroll
         for (int c = 0; c < kDPerLane; ++c) {
             int d = st.lane + 32 * c;
-            if (d < D) op[q_off + (long long)qrow * q_rs + d] = from_f<T>(o[c]);
+            if (d < D) op[o_off + (long long)qrow * o_rs + d] = from_f<T>(o[c]);
         }
         if (st.lane == 0) {
             if (p.lse) p.lse[lse_off + qrow] = lse;

@@ -172,9 +172,10 @@ cudaError_t launch_tc_fwd(const AttnParams& a, cudaStream_t stream) {
         fold = false;  // the bias is added in the softmax
     } else {
         const uint64_t tk = a.total_k > 0 ? a.total_k : 1;
-        if (!make_map(&P.tm_q, dt, a.q, D, a.H, a.total_q, rs, rs * a.H, 64, 1, kBM) ||
-            !make_map(&P.tm_k, dt, a.k, D, a.H, tk, rs, rs * a.H, 64, 1, kBN) ||
-            !make_map(&P.tm_v, dt, a.v, D, a.H, tk, rs, rs * a.H, 64, 1, kBN))
+        // Rows of the packed (total, H, D) views are q_rs / k_rs / v_rs elements apart.
+        if (!make_map(&P.tm_q, dt, a.q, D, a.H, a.total_q, rs, 2 * (uint64_t)a.q_rs, 64, 1, kBM) ||
+            !make_map(&P.tm_k, dt, a.k, D, a.H, tk, rs, 2 * (uint64_t)a.k_rs, 64, 1, kBN) ||
+            !make_map(&P.tm_v, dt, a.v, D, a.H, tk, rs, 2 * (uint64_t)a.v_rs, 64, 1, kBN))
             return cudaErrorInvalidValue;
         P.nqt = (a.max_q + kBM - 1) / kBM;
         fold = a.scale > 0.f && std::isfinite(a.scale);

@@ -1075,7 +1075,7 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
                     const int d = d0 + lane;
                     if (it.Lk > 0 && d < a.D) {
                         const long long vrow0 = !VARLEN ? it.unit * a.K : (long long)it.k_row0;
-                        const long long vstride = !VARLEN ? a.D : (long long)a.H * a.D;
+                        const long long vstride = !VARLEN ? a.D : a.v_rs;
                         const long long vcol0 = !VARLEN ? 0 : (long long)it.h * a.D;
                         // Eight independent sums keep eight loads in flight.
                         float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
