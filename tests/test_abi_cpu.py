@@ -104,6 +104,51 @@ def test_varlen_empty_is_noop(lib):
     _varlen(max_seqlen_q=0)()
 
 
+def _strided(**kw):
+    args = dict(q=A, k=A, v=A, dtype=abi.TA_BF16, cu_seqlens_q=A, cu_seqlens_k=A, num_seqs=2, total_q=400,
+                total_k=400, max_seqlen_q=256, max_seqlen_k=256, H=2, D=64, scale=0.125, kv_num_blocks=A,
+                kv_indices=A, full_kv_num_blocks=A, full_kv_indices=A, mask_heads=1, max_q_blocks=2,
+                max_kv_blocks=2, block_q=128, block_k=128, mask_mod=abi.TA_MASK_CAUSAL, q_row_stride=0,
+                k_row_stride=0, v_row_stride=0, out=A, lse=0, max_=0, stream=0)
+    args.update(kw)
+    return lambda: abi.tri_attn_varlen_fwd_strided(**args)
+
+
+@pytest.mark.parametrize("kw,exc", [
+    (dict(q_row_stride=64), ValueError),                       # shorter than H*D = 128
+    (dict(v_row_stride=-128), ValueError),
+    (dict(k_row_stride=132), NotImplementedError),             # bf16 rows must be 16-byte multiples
+    (dict(dtype=abi.TA_F32, q_row_stride=130), NotImplementedError),
+    (dict(q_row_stride=1 << 41), NotImplementedError),
+])
+def test_varlen_strided_host_checks(lib, kw, exc):
+    with pytest.raises(exc):
+        _strided(**kw)()
+
+
+@pytest.mark.parametrize("strides", [(0, 0, 0), (384, 384, 384), (128, 256, 256), (136, 144, 128)])
+def test_varlen_strided_accepts_packed_strides(lib, strides):
+    # QKV_INTERLEAVED (3*H*D), KV_INTERLEAVED (q H*D, k/v 2*H*D) and padded rows pass
+    # the host checks; with no query rows the call is a no-op before any device work.
+    q, k, v = strides
+    _strided(max_seqlen_q=0, q_row_stride=q, k_row_stride=k, v_row_stride=v)()
+
+
+def test_row_stride_of_packed_views():
+    import torch
+    from masked_attention_tri_gb300 import api
+    cpu = torch.device("cpu")
+    qkv = torch.zeros(10, 3, 2, 64)
+    q, k, v = qkv.unbind(1)
+    assert [api._row_stride(t, "x", cpu) for t in (q, k, v)] == [384, 384, 384]
+    assert api._row_stride(torch.zeros(10, 2, 64), "x", cpu) == 128
+    assert api._row_stride(torch.zeros(1, 2, 64)[:, :, :], "x", cpu) == 128
+    with pytest.raises(ValueError):  # heads not contiguous
+        api._row_stride(torch.zeros(10, 64, 2).transpose(1, 2), "x", cpu)
+    with pytest.raises(ValueError):  # elements not contiguous
+        api._row_stride(torch.zeros(10, 2, 128)[:, :, ::2], "x", cpu)
+
+
 def test_mask_to_kv_lengths_host_checks(lib):
     with pytest.raises(ValueError):
         abi.tri_attn_mask_to_kv_lengths(0, 1, 1, 8, A, 0, 0)
