@@ -8,7 +8,8 @@ CUDA library.
 ``triattn_oracle.c`` holds the arithmetic (one query row at a time, every key,
 index order, double precision); this module compiles it with gcc/OpenMP on
 first use and wraps it for numpy / torch CPU tensors.  ``brute`` holds an
-independent pure-Python restatement for tiny shapes.
+independent pure-Python restatement for tiny shapes; ``backward`` the
+gradients of the triangle form (fp64 numpy, chain rule through the formula).
 
 Each function follows the cuEquivariance ``triangle_attention`` API page
 (formula; Parameters: bias, mask, scale, kv_lengths) or, for the packed form,

@@ -1,0 +1,116 @@
+"""Pins of the backward oracle (``oracle.backward.tri_bwd``), CPU only.
+
+The gradients are checked against things other than their own formula:
+central finite differences of the independent pure-Python forward
+(``oracle.brute``, fp64), torch autograd through a separate torch restatement
+of the cuEquivariance triangle_attention formula, closed forms (one valid
+key, an all-masked row) and the shift invariance of the softmax (each row of
+dx sums to zero).
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import brute
+from oracle.backward import tri_bwd
+
+
+def _case(seed, B=1, N=2, H=2, Q=3, K=4, D=3, mask_kind="none"):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(B, N, H, Q, D, generator=g)
+    k = torch.randn(B, N, H, K, D, generator=g)
+    v = torch.randn(B, N, H, K, D, generator=g)
+    bias = torch.randn(B, 1, H, Q, K, generator=g)
+    d_out = torch.randn(B, N, H, Q, D, generator=g, dtype=torch.float64)
+    mask = kvl = None
+    if mask_kind == "kvlen":
+        kvl = torch.tensor([[2, 0][:N]] * B, dtype=torch.int32)  # a partial prefix and an all-masked row
+    elif mask_kind == "dense":
+        mask = (torch.rand(B, N, 1, 1, K, generator=g) < 0.6).to(torch.uint8)
+        mask[0, 0, 0, 0, 0] = 1
+    return q, k, v, bias, d_out, mask, kvl
+
+
+def _loss_brute(q, k, v, bias, d_out, mask, kvl, scale):
+    O, _, _ = brute.tri_fwd(q.tolist(), k.tolist(), v.tolist(), bias.tolist(),
+                            mask=None if mask is None else mask.tolist(),
+                            kv_lengths=None if kvl is None else kvl.tolist(), scale=scale)
+    return float((torch.tensor(O, dtype=torch.float64) * d_out).sum())
+
+
+@pytest.mark.parametrize("mask_kind", ["none", "kvlen", "dense"])
+def test_gradients_match_finite_differences(mask_kind):
+    q, k, v, bias, d_out, mask, kvl = _case(11, mask_kind=mask_kind)
+    scale = 0.7
+    grads = tri_bwd(q, k, v, bias, d_out, mask=mask, kv_lengths=kvl, scale=scale)
+    eps = 1e-6
+    for t, g in zip((q, k, v, bias), grads):
+        base = t.double()
+        flat = base.reshape(-1)
+        fd = np.zeros(flat.numel())
+        for i in range(flat.numel()):
+            plus, minus = flat.clone(), flat.clone()
+            plus[i] += eps
+            minus[i] -= eps
+            args = [q.double(), k.double(), v.double(), bias.double()]
+            idx = [id(x) for x in (q, k, v, bias)].index(id(t))
+            args[idx] = plus.reshape(base.shape)
+            lp = _loss_brute(*args, d_out, mask, kvl, scale)
+            args[idx] = minus.reshape(base.shape)
+            lm = _loss_brute(*args, d_out, mask, kvl, scale)
+            fd[i] = (lp - lm) / (2 * eps)
+        np.testing.assert_allclose(g.reshape(-1), fd, atol=2e-6, rtol=1e-5)
+
+
+def _torch_grads(q, k, v, bias, d_out, valid, scale):
+    s = float(np.float32(scale))
+    qd, kd, vd, bd = (t.double().clone().requires_grad_(True) for t in (q, k, v, bias))
+    x = s * torch.einsum("bnhqd,bnhkd->bnhqk", qd, kd) + bd  # bias broadcast over n
+    x = x.masked_fill(~valid[:, :, None, None, :], -1e9)
+    O = torch.einsum("bnhqk,bnhkd->bnhqd", torch.softmax(x, dim=-1), vd)
+    (O * d_out).sum().backward()
+    return [t.grad.numpy() for t in (qd, kd, vd, bd)]
+
+
+@pytest.mark.parametrize("mask_kind", ["none", "kvlen", "dense"])
+def test_gradients_match_torch_autograd(mask_kind):
+    q, k, v, bias, d_out, mask, kvl = _case(21, B=2, N=3, H=2, Q=5, K=6, D=8, mask_kind=mask_kind)
+    if kvl is not None:
+        kvl = torch.tensor([[3, 0, 6], [1, 7, 4]], dtype=torch.int32)
+    B, N, K = q.shape[0], q.shape[1], k.shape[3]
+    if mask is not None:
+        valid = mask.reshape(B, N, K) != 0
+    elif kvl is not None:
+        valid = torch.arange(K)[None, None, :] < kvl.clamp(0, K)[:, :, None]
+    else:
+        valid = torch.ones(B, N, K, dtype=torch.bool)
+    got = tri_bwd(q, k, v, bias, d_out, mask=mask, kv_lengths=kvl, scale=None)
+    ref = _torch_grads(q, k, v, bias, d_out, valid, 1.0 / np.sqrt(q.shape[-1]))
+    for g, r in zip(got, ref):
+        np.testing.assert_allclose(g, r, atol=1e-10, rtol=1e-9)
+
+
+def test_single_valid_key_passes_no_gradient_to_logits():
+    q, k, v, bias, d_out, _, _ = _case(31)
+    kvl = torch.ones(1, 2, dtype=torch.int32)
+    dQ, dK, dV, dB = tri_bwd(q, k, v, bias, d_out, kv_lengths=kvl)
+    assert np.abs(dQ).max() == 0 and np.abs(dK).max() == 0 and np.abs(dB).max() == 0
+    # all weight on key 0: dV[key 0] = sum over queries of dO, other keys 0
+    np.testing.assert_allclose(dV[:, :, :, 0], d_out.numpy().sum(axis=3), rtol=1e-14, atol=1e-14)
+    assert np.abs(dV[:, :, :, 1:]).max() == 0
+
+
+def test_all_masked_row_spreads_dv_uniformly():
+    q, k, v, bias, d_out, _, _ = _case(41)
+    kvl = torch.zeros(1, 2, dtype=torch.int32)
+    dQ, dK, dV, dB = tri_bwd(q, k, v, bias, d_out, kv_lengths=kvl)
+    assert np.abs(dQ).max() == 0 and np.abs(dK).max() == 0 and np.abs(dB).max() == 0
+    K = k.shape[3]
+    expect = d_out.numpy().sum(axis=3, keepdims=True) / K
+    np.testing.assert_allclose(dV, np.broadcast_to(expect, dV.shape), rtol=1e-13, atol=1e-14)
+
+
+def test_bias_gradient_rows_sum_to_zero():
+    q, k, v, bias, d_out, _, _ = _case(51, B=1, N=3, H=2, Q=4, K=7, D=5)
+    _, _, _, dB = tri_bwd(q, k, v, bias, d_out)
+    assert np.abs(dB.sum(axis=-1)).max() < 1e-12
