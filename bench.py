@@ -14,8 +14,10 @@ Metric: effective TFLOP/s = 4*B*N*H*Q*D*sum(K_valid) / time (varlen: 4*H*D
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-Under torchrun (N>1) every rank runs the full workload (weak scaling, no
-data-path collective); rank 0 prints the line with the max time over ranks.
+Under torchrun (N>1) each rank runs its contiguous range of the workload's
+(b, n) slabs with the bias replicated (strong scaling, no data-path
+collective); rank 0 prints the line with the max time over ranks.  The main
+number is the median over five timed regions of `--steps` launches.
 --impl reference times the fp64 CPU oracle on a bounded sample of the
 workload (rank 0 only).
 """
@@ -40,6 +42,7 @@ import synth  # noqa: E402
 METRIC = "fwd effective TFLOP/s and % of GB300 dense-bf16 peak, per config, 1 GPU"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129 * 1024 * 1024
+TIMED_REGIONS = 5
 ESIZE = {"f32": 4, "f16": 2, "bf16": 2}
 
 
@@ -187,8 +190,11 @@ def make_l2_flusher(dev):
     return flush
 
 
-def time_triangle(ta, c, dev, steps, warmup, flush=None):
-    """Device time (ms) per launch over `steps` launches, CUDA events on the launching stream."""
+def time_triangle(ta, c, dev, steps, warmup, flush=None, repeats=1, world=1):
+    """Device time (ms) per launch: `repeats` timed regions of `steps` back-to-back launches each
+    (CUDA events on the launching stream, every region bracketed by a barrier and a synchronize),
+    and the median over the regions.  With `flush`, the L2 is flushed before every launch and only
+    the launch itself is inside the events."""
     x = gpu_triangle_inputs(c, dev)
     out = torch.empty_like(x["q"])
     lse = torch.empty(c.B, c.N, c.H, c.Q, 1, device=dev, dtype=torch.float32)
@@ -209,24 +215,43 @@ def time_triangle(ta, c, dev, steps, warmup, flush=None):
         launch()
     torch.cuda.synchronize(dev)
     stream = torch.cuda.current_stream(dev)
-    if flush is None:
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(steps):
-            launch()
-        e1.record(stream)
+    per = []
+    for _ in range(repeats):
+        barrier(world)
         torch.cuda.synchronize(dev)
-        return e0.elapsed_time(e1) / steps
-    tot = 0.0
-    for _ in range(steps):
-        flush()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        launch()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        tot += e0.elapsed_time(e1)
-    return tot / steps
+        if flush is None:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(steps):
+                launch()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            per.append(e0.elapsed_time(e1) / steps)
+        else:
+            tot = 0.0
+            for _ in range(steps):
+                flush()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                launch()
+                e1.record(stream)
+                torch.cuda.synchronize(dev)
+                tot += e0.elapsed_time(e1)
+            per.append(tot / steps)
+        barrier(world)
+    return statistics.median(per)
+
+
+def shard_case(c, world, rank):
+    """This rank's contiguous range of (b, n) slabs of a B = 1 workload (the bias replicated)."""
+    from masked_attention_tri_gb300.shard import slab_range
+    if world == 1:
+        return c
+    assert c.B == 1, "the benchmark workloads have B = 1"
+    n0, n1 = slab_range(c.N, world, rank)
+    sl = lambda t: None if t is None else t[:, n0:n1].contiguous()  # noqa: E731
+    return synth.TriangleCase(c.name, 1, n1 - n0, c.H, c.Q, c.K, c.D, c.dtype, c.bias_dtype, sl(c.q), sl(c.k),
+                              sl(c.v), c.bias, sl(c.mask), sl(c.kv_lengths), c.scale)
 
 
 def time_varlen(ta, c, dev, steps, warmup, flush, qkv_packed=False):
@@ -414,14 +439,15 @@ def run_reference(args, world, rank):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(c),
+        "config": workload_config(c, world),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
-def workload_config(c):
+def workload_config(c, world=1):
+    """The `config` of the JSON line; both arms print the same dict for the same workload."""
     desc = {
         "bf16_long": "bf16 long: B=1,N=768,H=4,Q=K=768,D=64; q,k,v,bias ~N(0,1) bf16; kv_lengths U[0,768] incl. 0",
         "bf16_pairstack": "bf16 pair-stack: B=1,N=384,H=4,Q=K=384,D=32; bias ~N(0,4) bf16; kv_lengths U[192,384]",
@@ -429,9 +455,34 @@ def workload_config(c):
         "fp16_dense": "fp16: B=1,N=128,H=2,Q=K=128,D=32; bias fp32; dense Bernoulli(0.5) key mask",
         "tiny_fp32": "tiny fp32: B=1,N=32,H=2,Q=K=32,D=32; no mask",
     }.get(c.name, c.name)
+    big = 2 * c.B * c.N * c.H * (c.Q + c.K) * c.D * ESIZE[c.dtype] > L2_BYTES
     return {"workload": desc, "B": c.B, "N": c.N, "H": c.H, "Q": c.Q, "K": c.K, "D": c.D,
             "qkv_dtype": c.dtype, "bias_dtype": c.bias_dtype,
-            "mask": "kv_lengths" if c.kv_lengths is not None else ("dense" if c.mask is not None else "none")}
+            "mask": "kv_lengths" if c.kv_lengths is not None else ("dense" if c.mask is not None else "none"),
+            "global_batch": c.B, "parallelism": f"n_split{world}" if world > 1 else "single",
+            "l2": "inputs larger than L2 (q,k,v,O vs 129 MB)" if big else "L2 flushed before each launch"}
+
+
+def run_only(args):
+    """Launch one workload `warmup` + `steps` times (L2 flushed before each timed launch) and print
+    its time; used as the command under ncu."""
+    import masked_attention_tri_gb300 as ta
+    from masked_attention_tri_gb300 import build
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    build.build()
+    flush = make_l2_flusher(dev)
+    c = synth.WORKLOADS[args.only]()
+    if isinstance(c, synth.VarlenCase):
+        f, _ = varlen_work(c)
+        t = time_varlen(ta, c, dev, args.steps, args.warmup, flush)
+    else:
+        f, _ = triangle_work(c)
+        t = time_triangle(ta, c, dev, args.steps, args.warmup, flush=flush)
+    status = ta.get_status()
+    assert status == 0, f"device status {status}"
+    print(json.dumps({"only": args.only, "us": 1e3 * t, "tflops": f / (t * 1e-3) / 1e12, "steps": args.steps,
+                      "warmup": args.warmup}), flush=True)
 
 
 def main():
@@ -444,12 +495,18 @@ def main():
     ap.add_argument("--no-per-config", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--only", default=None, choices=sorted(synth.WORKLOADS),
+                    help="profiling mode: warm-up + timed launches of this one workload, a short JSON line, "
+                         "nothing else (no per-config, end-to-end or CPU legs)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank)
+        return
+    if args.only:
+        run_only(args)
         return
 
     import masked_attention_tri_gb300 as ta
@@ -458,7 +515,10 @@ def main():
     torch.cuda.set_device(dev)
     build.build()
     peaks, peak_kind = load_peaks()
-    c = synth.TRIANGLE_WORKLOADS[args.workload]()
+    c_all = synth.TRIANGLE_WORKLOADS[args.workload]()
+    flops_all, _ = triangle_work(c_all)
+    # Each rank runs its contiguous range of (b, n) slabs (the bias replicated); one GPU runs it all.
+    c = shard_case(c_all, world, rank)
     flops, byts = triangle_work(c)
 
     barrier(world)
@@ -466,14 +526,14 @@ def main():
     sampler = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else
                            int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
     sampler.start()
-    ms = time_triangle(ta, c, dev, args.steps, args.warmup)
+    ms = time_triangle(ta, c, dev, args.steps, args.warmup, repeats=TIMED_REGIONS, world=world)
     clocks = sampler.stop()
     status = ta.get_status()
     barrier(world)
     ms_max = max_over_ranks(ms, world, dev)
     assert status == 0, f"device status {status}"
 
-    value = world * flops / (ms_max * 1e-3) / 1e12
+    value = flops_all / (ms_max * 1e-3) / 1e12
     t_mma = flops / (peaks["bf16_tflops"] * 1e12)
     t_hbm = byts / (peaks["hbm_gbs"] * 1e9)
     bound = "hbm" if t_hbm >= t_mma else "tensor"
@@ -490,8 +550,11 @@ def main():
     roof["effective_flops"] = flops
     roof["two_term_roofline_frac"] = max(t_mma, t_hbm) / (ms * 1e-3)
 
+    barrier(world)
     e2e_ms, h2d, d2h = e2e_triangle(ta, c, dev, max(3, min(args.steps, 50)), 3)
     e2e_ms = max_over_ranks(e2e_ms, world, dev)
+    h2d = int(max_over_ranks(float(h2d), world, dev))
+    d2h = int(max_over_ranks(float(d2h), world, dev))
 
     per_config = {}
     if not args.no_per_config and rank == 0:
@@ -533,19 +596,17 @@ def main():
                          f"{fl:.3e} effective FLOP in {dt:.1f} s"}
 
     if rank == 0:
-        cfg = workload_config(c)
-        cfg.update({"global_batch": c.B * world, "parallelism": f"replicas{world}" if world > 1 else "single",
-                    "l2": "inputs larger than L2 (q,k,v,O 1.2 GB vs 129 MB)" if args.workload == "bf16_long"
-                    else "not flushed"})
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": c.dtype, "data": "synthetic", "config": cfg,
-            "pct_bf16_peak": 100 * flops / (ms_max * 1e-3) / (peaks["bf16_tflops"] * 1e12),
+            "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "strong",
+            "vs_baseline": None, "dtype": c.dtype, "data": "synthetic", "config": workload_config(c_all, world),
+            "pct_bf16_peak": 100 * flops_all / (ms_max * 1e-3) / (peaks["bf16_tflops"] * 1e12),
             "roofline": roof, "cpu_baseline": cpu,
-            "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+            "e2e": {"value": flops_all / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-            "gpu_launches": args.steps, "clocks": clocks, "per_config": per_config,
+            "gpu_launches": args.steps, "timed_regions": TIMED_REGIONS,
+            "timing": f"median over {TIMED_REGIONS} timed regions of {args.steps} launches (one launch per step)",
+            "clocks": clocks, "per_config": per_config,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -75,6 +75,12 @@ typedef enum { TA_MASK_NONE = 0, TA_MASK_CAUSAL = 1 } ta_mask_mod;
  *               "Pass either mask or kv_lengths, not both"); neither = no mask.
  *   scale       s in the formula, used as given (the Python binding applies
  *               the page's default 1/sqrt(D) when scale is None).
+ *               Precondition: every valid key's logit s*(Q.K) + bias stays
+ *               above -1e9 + 100 (true whenever |bias| and |s*Q.K| are far
+ *               below 1e9).  The kernels skip key tiles that hold only masked
+ *               keys, which is exact because such a key's weight
+ *               exp(-1e9 - max) is 0 in fp32; a row whose valid logits all
+ *               lie at or below -1e9 would instead need those masked keys.
  *   lse, max    optional (B, N, H, Q) fp32 outputs (return_aux); NULL skips.
  *
  * Supported: fp16/bf16 q/k/v with D % 8 == 0, D <= 128 and K % 8 == 0 (the

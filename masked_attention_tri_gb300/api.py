@@ -31,6 +31,15 @@ def _need(t: torch.Tensor, name: str, device: torch.device) -> None:
         raise ValueError(f"{name} must be contiguous")
 
 
+def _check_out(out, shape, dtype) -> None:
+    """A preallocated output must be exactly what the kernels write: they store whole rows of
+    `shape` in `dtype`, so a smaller or differently typed buffer would be overrun."""
+    if not isinstance(out, torch.Tensor):
+        raise TypeError("out must be a torch.Tensor")
+    if tuple(out.shape) != tuple(shape) or out.dtype != dtype:
+        raise ValueError(f"out must be {tuple(shape)} of {dtype}, got {tuple(out.shape)} of {out.dtype}")
+
+
 def _stream(device: torch.device) -> int:
     return torch.cuda.current_stream(device).cuda_stream
 
@@ -64,6 +73,8 @@ def triangle_attention(q, k, v, bias, mask=None, scale=None, return_aux=False, *
         raise ValueError(f"k/v must be {(B, N, H, K, D)}, got {tuple(k.shape)} / {tuple(v.shape)}")
     if tuple(bias.shape) != (B, 1, H, Q, K):
         raise ValueError(f"bias must be {(B, 1, H, Q, K)}, got {tuple(bias.shape)}")
+    if out is not None:
+        _check_out(out, tuple(q.shape), q.dtype)
     dev = q.device
     if dev.type != "cuda":
         raise ValueError("triangle_attention runs on CUDA tensors only")
@@ -144,20 +155,24 @@ class BlockMask:
     of each q block, where mask_mod applies; full_kv_* (optional, same shapes):
     blocks where every key is valid.  Indices are sequence-local 128-row
     blocks.  mask_mod is None or "causal" (a C ABI cannot take a callable).
+    seq_lengths (q_len, kv_len), as on the page's from_kv_blocks, fixes the
+    number of kv blocks, i.e. the columns of ``to_dense``; without it the
+    columns are the larger of MK and the highest listed block index + 1.
     """
 
     def __init__(self, kv_num_blocks, kv_indices, full_kv_num_blocks=None, full_kv_indices=None, BLOCK_SIZE=128,
-                 mask_mod=None):
+                 mask_mod=None, seq_lengths=None):
         self.kv_num_blocks = kv_num_blocks
         self.kv_indices = kv_indices
         self.full_kv_num_blocks = full_kv_num_blocks
         self.full_kv_indices = full_kv_indices
         self.BLOCK_SIZE = (BLOCK_SIZE, BLOCK_SIZE) if isinstance(BLOCK_SIZE, int) else tuple(BLOCK_SIZE)
         self.mask_mod = mask_mod
+        self.seq_lengths = None if seq_lengths is None else (int(seq_lengths[0]), int(seq_lengths[1]))
 
     @classmethod
     def from_kv_blocks(cls, kv_num_blocks, kv_indices, full_kv_num_blocks=None, full_kv_indices=None,
-                       BLOCK_SIZE=128, mask_mod=None):
+                       BLOCK_SIZE=128, mask_mod=None, seq_lengths=None):
         """Same error rules as the BlockMask page's from_kv_blocks (Raises)."""
         if kv_indices.dim() < 2:
             raise RuntimeError("BlockMask must have at least 2 dimensions")
@@ -165,37 +180,57 @@ class BlockMask:
             "full_kv_num_blocks and full_kv_indices must be both provided or omitted"
         if mask_mod not in (None, "causal", "none"):
             raise ValueError("mask_mod must be None or 'causal'")
-        return cls(kv_num_blocks, kv_indices, full_kv_num_blocks, full_kv_indices, BLOCK_SIZE, mask_mod)
+        return cls(kv_num_blocks, kv_indices, full_kv_num_blocks, full_kv_indices, BLOCK_SIZE, mask_mod,
+                   seq_lengths)
 
     @property
     def mask_mod_code(self) -> int:
         return abi.TA_MASK_CAUSAL if self.mask_mod == "causal" else abi.TA_MASK_NONE
 
-    def numel(self) -> int:
-        """Blocks in the mask, not accounting for sparsity (q blocks x kv blocks x leading dims)."""
-        *lead, mq = self.kv_num_blocks.shape
-        n = 1
-        for x in lead:
-            n *= int(x)
-        return n * int(mq) * int(self.kv_indices.shape[-1])
-
-    def to_dense(self) -> torch.Tensor:
-        """Dense (…, MQ, MK) block mask: 1 where a block is listed (partial or full)."""
-        num = self.kv_num_blocks.cpu()
-        idx = self.kv_indices.cpu()
-        MK = idx.shape[-1]
-        dense = torch.zeros(*num.shape, MK, dtype=torch.int32)
-        pairs = [(num, idx)]
+    def _lists(self):
+        pairs = [(self.kv_num_blocks.cpu(), self.kv_indices.cpu())]
         if self.full_kv_num_blocks is not None:
             pairs.append((self.full_kv_num_blocks.cpu(), self.full_kv_indices.cpu()))
-        for nb, ix in pairs:
+        return pairs
+
+    def num_kv_blocks(self) -> int:
+        """Columns of the dense block mask (kv blocks per row)."""
+        if self.seq_lengths is not None:
+            kb = self.BLOCK_SIZE[1] if len(self.BLOCK_SIZE) > 1 else self.BLOCK_SIZE[0]
+            return (self.seq_lengths[1] + kb - 1) // kb
+        cols = int(self.kv_indices.shape[-1])
+        for nb, ix in self._lists():
             flat_n = nb.reshape(-1)
-            flat_i = ix.reshape(-1, MK)
-            flat_d = dense.view(-1, MK)
+            flat_i = ix.reshape(flat_n.numel(), -1)
             for r in range(flat_n.numel()):
-                for t in range(int(flat_n[r])):
+                n = min(max(int(flat_n[r]), 0), flat_i.shape[1])
+                if n:
+                    cols = max(cols, int(flat_i[r, :n].max()) + 1)
+        return cols
+
+    def numel(self) -> int:
+        """Blocks in the mask, not accounting for sparsity (q blocks x kv blocks x leading dims)."""
+        n = 1
+        for x in self.kv_num_blocks.shape:
+            n *= int(x)
+        return n * self.num_kv_blocks()
+
+    def to_dense(self) -> torch.Tensor:
+        """Dense (..., MQ, num_kv_blocks) block mask: 1 where a block is listed (partial or full).
+
+        The page's reconstruction loop: for each row, the first kv_num_blocks[row]
+        entries of kv_indices[row] are set; later entries are never read."""
+        cols = self.num_kv_blocks()
+        num = self.kv_num_blocks.cpu()
+        dense = torch.zeros(*num.shape, cols, dtype=torch.int32)
+        flat_d = dense.view(-1, cols)
+        for nb, ix in self._lists():
+            flat_n = nb.reshape(-1)
+            flat_i = ix.reshape(flat_n.numel(), -1)
+            for r in range(flat_n.numel()):
+                for t in range(min(int(flat_n[r]), flat_i.shape[1])):
                     c = int(flat_i[r, t])
-                    if 0 <= c < MK:
+                    if 0 <= c < cols:
                         flat_d[r, c] = 1
         return dense
 
@@ -211,10 +246,17 @@ def _row_stride(t: torch.Tensor, name: str, device: torch.device) -> int:
         raise TypeError(f"{name} must be a torch.Tensor")
     if t.device != device:
         raise ValueError(f"{name} is on {t.device}, expected {device}")
-    _, H, D = t.shape
+    rows, H, D = t.shape
     if t.stride(2) != 1 or (H > 1 and t.stride(1) != D):
         raise ValueError(f"{name} must have contiguous heads and elements (strides (*, D, 1))")
-    return t.stride(0) if t.shape[0] > 1 else H * D
+    if rows <= 1:
+        return H * D
+    if t.stride(0) < H * D:
+        # Rows that overlap (an expanded or otherwise aliased view, stride 0 included) would make
+        # the kernels read rows*H*D elements from a smaller allocation.
+        raise ValueError(f"{name} rows overlap (row stride {t.stride(0)} < H*D = {H * D}); pass a "
+                         "contiguous tensor")
+    return t.stride(0)
 
 
 def varlen_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, block_mask=None, scale=None,
@@ -233,6 +275,8 @@ def varlen_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seql
     total_q, H, D = q.shape
     if tuple(k.shape[1:]) != (H, D) or tuple(v.shape) != tuple(k.shape):
         raise ValueError("k and v must be (total_k, H, D) with q's H and D")
+    if out is not None:
+        _check_out(out, (total_q, H, D), q.dtype)
     dev = q.device
     if dev.type != "cuda":
         raise ValueError("varlen_attention runs on CUDA tensors only")

@@ -78,7 +78,9 @@ TA_EXPORT ta_status tri_attn_fwd(const void* q, const void* k, const void* v, ta
     if (qkv_dtype != TA_F32 && K % 8 != 0) return TA_ERR_UNSUPPORTED;
     // Sizes: every flat element index must fit in 63 bits and the grid in 31.
     const long long units = (long long)B * N * H;
-    if (units > (1LL << 40) || (long long)Q * K > (1LL << 40) || units * ((Q + 31) / 32) > 0x7fffffffLL)
+    // The bias plane (Q x K elements of up to 4 bytes) is one stride of a tensor map, and tensor-map
+    // strides must stay below 2^40 bytes.
+    if (units > (1LL << 40) || (long long)Q * K * 4 >= (1LL << 40) || units * ((Q + 31) / 32) > 0x7fffffffLL)
         return TA_ERR_UNSUPPORTED;
 
     int* status = triattn::status_word();
@@ -156,7 +158,10 @@ TA_EXPORT ta_status tri_attn_varlen_fwd_strided(const void* q, const void* k, co
     if (k_row_stride == 0) k_row_stride = hd;
     if (v_row_stride == 0) v_row_stride = hd;
     if (q_row_stride < hd || k_row_stride < hd || v_row_stride < hd) return TA_ERR_INVALID_ARG;
-    if (q_row_stride > (1LL << 40) || k_row_stride > (1LL << 40) || v_row_stride > (1LL << 40))
+    // Row strides are tensor-map strides in bytes, which must stay below 2^40.
+    const long long esz = dtype == TA_F32 ? 4 : 2;
+    if (q_row_stride * esz >= (1LL << 40) || k_row_stride * esz >= (1LL << 40) ||
+        v_row_stride * esz >= (1LL << 40))
         return TA_ERR_UNSUPPORTED;
     const int per16 = dtype == TA_F32 ? 4 : 8;
     if (q_row_stride % per16 || k_row_stride % per16 || v_row_stride % per16) return TA_ERR_UNSUPPORTED;

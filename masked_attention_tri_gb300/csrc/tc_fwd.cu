@@ -114,15 +114,6 @@ bool choose_split_geometry(TcParams& P) {
     return false;
 }
 
-// TRIATTN_TRI_SPLIT=0 keeps D <= 64 triangle problems on the two-tile kernel.
-bool split_enabled() {
-    static const bool on = [] {
-        const char* e = getenv("TRIATTN_TRI_SPLIT");
-        return !(e && e[0] == '0');
-    }();
-    return on;
-}
-
 template <bool VARLEN, bool BF16, bool BIAS_F32, bool FOLD>
 cudaError_t launch_nq(int NQ, const TcParams& P, int grid, cudaStream_t stream) {
     if constexpr (VARLEN) {
@@ -181,7 +172,7 @@ cudaError_t launch_tc_fwd(const AttnParams& a, cudaStream_t stream) {
         fold = a.scale > 0.f && std::isfinite(a.scale);
     }
     int NQ = 1;
-    const bool split = !a.varlen && D <= 64 && split_enabled();
+    const bool split = !a.varlen && D <= 64;
     if (split ? !choose_split_geometry(P) : !choose_geometry(P, a.varlen != 0, NQ))
         return cudaErrorInvalidConfiguration;
     P.items_per_unit = (P.nqt + NQ - 1) / NQ;

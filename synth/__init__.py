@@ -72,6 +72,16 @@ class VarlenCase:
     block: int
     scale: float
     max_seqlen: int
+    # key side; the same as the query side unless drawn with lengths_k
+    lengths_k: Optional[torch.Tensor] = None
+    cu_seqlens_k: Optional[torch.Tensor] = None
+    max_seqlen_k: int = 0
+
+    def __post_init__(self):
+        if self.lengths_k is None:
+            self.lengths_k = self.lengths
+            self.cu_seqlens_k = self.cu_seqlens
+            self.max_seqlen_k = self.max_seqlen
 
 
 def _randn(gen, shape, std, dtype):
@@ -243,30 +253,44 @@ def make_varlen(
     lengths: list[int] | None = None,
     block_lists: str = "causal",
     scale: float | None = None,
+    lengths_k: list[int] | None = None,
 ) -> VarlenCase:
-    """Draw packed sequences (q and k share lengths) and their block mask.
+    """Draw packed sequences and their block mask.
 
+    q and k share lengths unless lengths_k gives the key lengths (then
+    block_lists must be "none": the causal lists assume equal lengths).
     block_lists: "causal" (full + partial lists of a causal mask), "none"
     (no lists: every block visited, mask_mod applied everywhere).
     """
     g = torch.Generator("cpu").manual_seed(seed)
     if lengths is None:
         lengths = torch.randint(lmin, lmax + 1, (num_seqs,), generator=g, dtype=torch.int64).tolist()
-    lens = torch.tensor(lengths, dtype=torch.int32)
-    cu = torch.zeros(len(lengths) + 1, dtype=torch.int32)
-    cu[1:] = torch.cumsum(lens, 0).to(torch.int32)
-    total = int(cu[-1])
+
+    def offsets(ls):
+        t = torch.tensor(ls, dtype=torch.int32)
+        cu = torch.zeros(len(ls) + 1, dtype=torch.int32)
+        cu[1:] = torch.cumsum(t, 0).to(torch.int32)
+        return t, cu
+
+    lens, cu = offsets(lengths)
+    lens_k, cu_k = offsets(lengths_k) if lengths_k is not None else (lens, cu)
+    if lengths_k is not None and (len(lengths_k) != len(lengths) or block_lists != "none"):
+        raise ValueError("lengths_k needs one key length per sequence and block_lists='none'")
+    total, total_k = int(cu[-1]), int(cu_k[-1])
     q = _randn(g, (total, H, D), 1.0, dtype)
-    k = _randn(g, (total, H, D), 1.0, dtype)
-    v = _randn(g, (total, H, D), 1.0, dtype)
+    k = _randn(g, (total_k, H, D), 1.0, dtype)
+    v = _randn(g, (total_k, H, D), 1.0, dtype)
     kv_num = kv_idx = full_num = full_idx = None
     if block_lists == "causal":
         kv_num, kv_idx, full_num, full_idx = causal_block_lists(lengths)
     elif block_lists != "none":
         raise ValueError(block_lists)
     s = 1.0 / math.sqrt(D) if scale is None else scale
+    if lengths_k is None:
+        return VarlenCase(name, H, D, dtype, lens, cu, q, k, v, kv_num, kv_idx, full_num, full_idx,
+                          mask_mod, 128, s, max(lengths))
     return VarlenCase(name, H, D, dtype, lens, cu, q, k, v, kv_num, kv_idx, full_num, full_idx,
-                      mask_mod, 128, s, max(lengths))
+                      mask_mod, 128, s, max(lengths), lens_k, cu_k, max(lengths_k))
 
 
 def bf16_varlen() -> VarlenCase:

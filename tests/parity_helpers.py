@@ -66,9 +66,9 @@ def run_varlen(case, return_aux=True):
         bm = ta.BlockMask.from_kv_blocks(to_gpu(case.kv_num_blocks), to_gpu(case.kv_indices),
                                          to_gpu(case.full_kv_num_blocks), to_gpu(case.full_kv_indices),
                                          BLOCK_SIZE=case.block, mask_mod=case.mask_mod)
-    cu = case.cu_seqlens.cuda()
-    res = ta.varlen_attention(case.q.cuda(), case.k.cuda(), case.v.cuda(), cu, cu, case.max_seqlen, case.max_seqlen,
-                              block_mask=bm, scale=case.scale, return_aux=return_aux,
+    cu, cuk = case.cu_seqlens.cuda(), case.cu_seqlens_k.cuda()
+    res = ta.varlen_attention(case.q.cuda(), case.k.cuda(), case.v.cuda(), cu, cuk, case.max_seqlen,
+                              case.max_seqlen_k, block_mask=bm, scale=case.scale, return_aux=return_aux,
                               mask_mod=case.mask_mod if bm is None else None)
     torch.cuda.synchronize()
     assert ta.get_status() == 0
@@ -77,7 +77,7 @@ def run_varlen(case, return_aux=True):
 
 def check_varlen(case):
     O, L, M = run_varlen(case)
-    rO, rL, rM = oracle.varlen_fwd(case.q, case.k, case.v, case.cu_seqlens, case.cu_seqlens, case.scale,
+    rO, rL, rM = oracle.varlen_fwd(case.q, case.k, case.v, case.cu_seqlens, case.cu_seqlens_k, case.scale,
                                    case.kv_num_blocks, case.kv_indices, case.full_kv_num_blocks,
                                    case.full_kv_indices, block=case.block, mask_mod=case.mask_mod)
     return compare(case.name, case.dtype, O, L, M, rO, rL, rM)

@@ -68,6 +68,7 @@ def _fwd(**kw):
     (dict(D=12), NotImplementedError),  # 16-bit needs D % 8
     (dict(K=60), NotImplementedError),  # 16-bit needs K % 8
     (dict(qkv_dtype=abi.TA_F32, bias_dtype=abi.TA_F32, D=6), NotImplementedError),
+    (dict(Q=1 << 19, K=1 << 19), NotImplementedError),  # a 2^40-byte bias plane: beyond a tensor-map stride
 ])
 def test_triangle_host_checks(lib, kw, exc):
     with pytest.raises(exc):
@@ -120,6 +121,8 @@ def _strided(**kw):
     (dict(k_row_stride=132), NotImplementedError),             # bf16 rows must be 16-byte multiples
     (dict(dtype=abi.TA_F32, q_row_stride=130), NotImplementedError),
     (dict(q_row_stride=1 << 41), NotImplementedError),
+    (dict(k_row_stride=1 << 39), NotImplementedError),         # 2^40 bytes: beyond a tensor-map stride
+    (dict(dtype=abi.TA_F32, v_row_stride=1 << 38), NotImplementedError),
 ])
 def test_varlen_strided_host_checks(lib, kw, exc):
     with pytest.raises(exc):
@@ -147,6 +150,43 @@ def test_row_stride_of_packed_views():
         api._row_stride(torch.zeros(10, 64, 2).transpose(1, 2), "x", cpu)
     with pytest.raises(ValueError):  # elements not contiguous
         api._row_stride(torch.zeros(10, 2, 128)[:, :, ::2], "x", cpu)
+    with pytest.raises(ValueError, match="overlap"):  # an expanded view: row stride 0
+        api._row_stride(torch.zeros(1, 2, 64).expand(10, 2, 64), "x", cpu)
+    with pytest.raises(ValueError, match="overlap"):  # rows that overlap by half a row
+        api._row_stride(torch.zeros(1000).as_strided((10, 2, 64), (64, 64, 1)), "x", cpu)
+
+
+def test_preallocated_out_must_match_q():
+    """A preallocated out of the wrong shape or dtype is rejected before any device work."""
+    import torch
+    from masked_attention_tri_gb300 import api
+    q = torch.zeros(1, 2, 2, 16, 8, dtype=torch.bfloat16)
+    bias = torch.zeros(1, 1, 2, 16, 16, dtype=torch.bfloat16)
+    k = torch.zeros(1, 2, 2, 16, 8, dtype=torch.bfloat16)
+    for bad in (torch.empty(1, 2, 2, 15, 8, dtype=torch.bfloat16), torch.empty(1, 2, 2, 16, 8, dtype=torch.float16),
+                torch.empty(2 * 2 * 16 * 8, dtype=torch.bfloat16)):
+        with pytest.raises(ValueError, match="out must be"):
+            api.triangle_attention(q, k, k, bias, out=bad)
+    qv = torch.zeros(40, 2, 8, dtype=torch.float32)
+    cu = torch.tensor([0, 40], dtype=torch.int32)
+    for bad in (torch.empty(39, 2, 8), torch.empty(40, 2, 8, dtype=torch.bfloat16)):
+        with pytest.raises(ValueError, match="out must be"):
+            api.varlen_attention(qv, qv, qv, cu, cu, 40, 40, out=bad)
+
+
+def test_block_mask_dense_columns_follow_kv_blocks():
+    """to_dense has one column per kv block, also when the lists are narrower than the block count."""
+    import torch
+    from masked_attention_tri_gb300 import api
+    kn = torch.tensor([[[1, 2, 1]]], dtype=torch.int32)                    # (S=1, Hm=1, MQ=3)
+    ki = torch.tensor([[[[0, 9], [1, 4], [3, 0]]]], dtype=torch.int32)    # MK = 2 < 5 kv blocks
+    bm = api.BlockMask.from_kv_blocks(kn, ki, seq_lengths=(384, 640))
+    d = bm.to_dense()
+    assert d.shape == (1, 1, 3, 5)
+    assert d[0, 0].tolist() == [[1, 0, 0, 0, 0], [0, 1, 0, 0, 1], [0, 0, 0, 1, 0]]
+    assert bm.numel() == 15 and abs(bm.sparsity() - 100.0 * (1 - 4 / 15)) < 1e-9
+    # without seq_lengths the columns reach the highest listed index
+    assert api.BlockMask.from_kv_blocks(kn, ki).to_dense().shape == (1, 1, 3, 5)
 
 
 def test_mask_to_kv_lengths_host_checks(lib):

@@ -34,20 +34,22 @@ def test_workload_full(name):
     check_triangle(synth.TRIANGLE_WORKLOADS[name]())
 
 
-def test_bf16_long_sampled_rows():
+def test_bf16_long_all_rows():
+    """The largest workload, every row, in the launch configuration the benchmark times.  The oracle
+    runs on the host's cores in slab chunks (about 15 s of CPU work on 16 cores)."""
     c = synth.bf16_long()
-    rng = np.random.default_rng(0)
-    total = c.B * c.N * c.H * c.Q
+    O, L, M = run_triangle(c)
+    O = O.reshape(-1, c.D)
+    L, M = L.reshape(-1), M.reshape(-1)
     per_n = c.H * c.Q
-    rows = set(rng.choice(total, 3000, replace=False).tolist())
-    # every row of the all-masked slab n=0 and the full-length slab n=1 (first head)
-    rows |= set(range(0, c.Q)) | set(range(per_n, per_n + c.Q))
-    # tile edges of a few other slabs
-    for n in (2, 100, 767):
-        for qi in (0, 127, 128, 255, 256, 511, 512, 767):
-            rows.add(n * per_n + 3 * c.Q + qi)
-    rows = np.array(sorted(rows), dtype=np.int64)
-    check_triangle(c, rows=rows)
+    chunk = 96  # (b, n) slabs per oracle call
+    worst = 0.0
+    for n0 in range(0, c.B * c.N, chunk):
+        rows = np.arange(n0 * per_n, min(c.B * c.N, n0 + chunk) * per_n, dtype=np.int64)
+        rO, rL, rM = oracle.tri_fwd(c.q, c.k, c.v, c.bias, kv_lengths=c.kv_lengths, scale=c.scale, rows=rows)
+        sel = torch.as_tensor(rows, device=O.device)
+        worst = max(worst, compare(f"{c.name}[n {n0}..]", c.dtype, O[sel], L[sel], M[sel], rO, rL, rM))
+    assert worst > 0.0
 
 
 def test_bf16_varlen_full():
@@ -91,6 +93,22 @@ def test_dense_mask_special_rows():
     check_triangle(c)
 
 
+# Dense masks on the two-tile kernel (D > 64): the bias warp's mask-bit words and the
+# masking of boundary tiles, with all-masked rows, one valid key in the ragged last
+# tile, a fully masked middle tile and an all-valid row.
+@pytest.mark.parametrize("D,dtype,bias_dtype", [(96, "bf16", "bf16"), (128, "bf16", "f32"), (96, "f16", "f32"),
+                                                (128, "f16", "f16")])
+def test_dense_mask_wide_heads(D, dtype, bias_dtype):
+    c = synth.make_triangle(f"dense_D{D}", 1, 6, 2, 150, 328, D, dtype, bias_dtype, seed=302 + D, mask="dense",
+                            mask_p=0.3)
+    c.mask[0, 0] = 0                 # all masked -> mean of V
+    c.mask[0, 1] = 0
+    c.mask[0, 1, ..., 327] = 1       # one valid key, in the ragged last tile
+    c.mask[0, 2] = 1                 # all valid
+    c.mask[0, 3, ..., 128:256] = 0   # middle tile fully masked
+    check_triangle(c)
+
+
 @pytest.mark.parametrize("D", [4, 12, 32, 100, 128])
 def test_fp32_head_dims(D):
     c = synth.make_triangle(f"f32_D{D}", 1, 2, 2, 45, 70, D, "f32", "f32", seed=400 + D, mask="kvlen",
@@ -130,6 +148,41 @@ def test_varlen_no_lists_full_and_causal():
     c = synth.make_varlen("vl_none", 3, 0, 0, 2, 64, "f16", seed=510, lengths=[77, 256, 5], block_lists="none",
                           mask_mod="none")
     check_varlen(c)
+    c.mask_mod = "causal"
+    check_varlen(c)
+
+
+@pytest.mark.parametrize("mask_mod", ["none", "causal"])
+@pytest.mark.parametrize("dtype,D", [("bf16", 64), ("f16", 128), ("f32", 32)])
+def test_varlen_key_lengths_differ(mask_mod, dtype, D):
+    """cu_seqlens_q != cu_seqlens_k, no lists: causal is top-left (k <= q, local indices)."""
+    c = synth.make_varlen(f"vl_lqlk_{mask_mod}_{D}", 4, 0, 0, 2, D, dtype, seed=560 + D,
+                          lengths=[200, 70, 129, 1], lengths_k=[90, 300, 129, 5], block_lists="none",
+                          mask_mod=mask_mod)
+    check_varlen(c)
+
+
+def test_varlen_key_lengths_differ_with_lists():
+    """Lq != Lk with full / partial lists over the Lq x Lk block grid (causal on partial blocks)."""
+    g = np.random.default_rng(7)
+    lq, lk = [300, 140, 260], [180, 390, 260]
+    c = synth.make_varlen("vl_lqlk_lists", 3, 0, 0, 2, 64, "bf16", seed=570, lengths=lq, lengths_k=lk,
+                          block_lists="none")
+    MQ, MK = 3, 4
+    kn = torch.zeros(3, 1, MQ, dtype=torch.int32)
+    ki = torch.full((3, 1, MQ, MK), 77, dtype=torch.int32)
+    fn = torch.zeros(3, 1, MQ, dtype=torch.int32)
+    fi = torch.full((3, 1, MQ, MK), 77, dtype=torch.int32)
+    for s in range(3):
+        nbq, nbk = (lq[s] + 127) // 128, (lk[s] + 127) // 128
+        for qb in range(nbq):
+            blocks = [int(x) for x in g.permutation(nbk)][:int(g.integers(1, nbk + 1))]
+            nf = int(g.integers(0, len(blocks) + 1))
+            fn[s, 0, qb] = nf
+            fi[s, 0, qb, :nf] = torch.tensor(blocks[:nf], dtype=torch.int32)
+            kn[s, 0, qb] = len(blocks) - nf
+            ki[s, 0, qb, :len(blocks) - nf] = torch.tensor(blocks[nf:], dtype=torch.int32)
+    c.kv_num_blocks, c.kv_indices, c.full_kv_num_blocks, c.full_kv_indices = kn, ki, fn, fi
     c.mask_mod = "causal"
     check_varlen(c)
 

@@ -409,3 +409,105 @@ def test_mask_to_kv_lengths_flags_holey_rows():
     kl, pre = oracle.mask_to_kv_lengths(m.view(1, 4, 1, 1, 4))
     assert kl.view(-1).tolist() == [2, 1, 0, 4]
     assert pre.view(-1).tolist() == [True, False, True, True]
+
+
+def _varlen_sdpa_pairs(c, keep_fn):
+    """Per (sequence, head) fp64 SDPA over Lq x Lk with keep_fn(seq, head, Lq, Lk) -> bool (Lq, Lk)."""
+    s = float(np.float32(c.scale))
+    out = torch.zeros(c.q.shape, dtype=torch.float64)
+    for i in range(len(c.lengths)):
+        a, b = int(c.cu_seqlens[i]), int(c.cu_seqlens[i + 1])
+        ka, kb = int(c.cu_seqlens_k[i]), int(c.cu_seqlens_k[i + 1])
+        for h in range(c.H):
+            keep = keep_fn(i, h, b - a, kb - ka)
+            out[a:b, h] = _sdpa(_f64(c.q[a:b, h]), _f64(c.k[ka:kb, h]), _f64(c.v[ka:kb, h]), keep, s)
+    return out.numpy()
+
+
+def test_varlen_causal_top_left_when_key_and_query_lengths_differ():
+    """Lq != Lk: causal keeps key k for query q when k <= q, both counted from the start of their
+    own sequence (top-left alignment); checked against SDPA with that element mask."""
+    c = synth.make_varlen("t", 3, 0, 0, 2, 8, "f32", seed=30, lengths=[200, 70, 130], lengths_k=[90, 260, 130],
+                          block_lists="none", mask_mod="causal")
+    O, L, M = oracle.varlen_fwd(c.q, c.k, c.v, c.cu_seqlens, c.cu_seqlens_k, c.scale, mask_mod="causal")
+    ref = _varlen_sdpa_pairs(c, lambda i, h, lq, lk: torch.arange(lk).view(1, -1) <= torch.arange(lq).view(-1, 1))
+    np.testing.assert_allclose(O, ref, atol=1e-12)
+    # a query row past every key (q >= Lk) sees the whole key sequence
+    a = int(c.cu_seqlens[0])
+    full = _sdpa(_f64(c.q[a + 150:a + 151, 0]), _f64(c.k[:90, 0]), _f64(c.v[:90, 0]), None,
+                 float(np.float32(c.scale)))
+    np.testing.assert_allclose(O[a + 150, 0], full[0].numpy(), atol=1e-12)
+    # no mask: plain attention over each sequence's own keys
+    O2, _, _ = oracle.varlen_fwd(c.q, c.k, c.v, c.cu_seqlens, c.cu_seqlens_k, c.scale, mask_mod="none")
+    np.testing.assert_allclose(O2, _varlen_sdpa_pairs(c, lambda i, h, lq, lk: None), atol=1e-12)
+
+
+def test_varlen_lists_with_key_and_query_lengths_differ():
+    """Random block lists over an Lq x Lk block grid equal their element mask (full | partial & causal)."""
+    g = np.random.default_rng(31)
+    lq, lk = [300, 140], [180, 390]
+    c = synth.make_varlen("t", 2, 0, 0, 2, 8, "bf16", seed=31, lengths=lq, lengths_k=lk, block_lists="none")
+    MQ, MK = 3, 4
+    kv_num = np.zeros((2, 1, MQ), np.int32)
+    kv_idx = np.full((2, 1, MQ, MK), 77, np.int32)
+    full_num = np.zeros((2, 1, MQ), np.int32)
+    full_idx = np.full((2, 1, MQ, MK), 77, np.int32)
+    for s in range(2):
+        nbq, nbk = (lq[s] + 127) // 128, (lk[s] + 127) // 128
+        for qb in range(nbq):
+            blocks = [int(x) for x in g.permutation(nbk)]
+            if 0 in blocks:  # block 0 always listed, so every row keeps key 0 under causal
+                blocks.remove(0)
+            blocks = [0] + blocks[:int(g.integers(0, len(blocks) + 1))]
+            nf = int(g.integers(0, len(blocks) + 1))
+            full_num[s, 0, qb] = nf
+            full_idx[s, 0, qb, :nf] = blocks[:nf]
+            kv_num[s, 0, qb] = len(blocks) - nf
+            kv_idx[s, 0, qb, :len(blocks) - nf] = blocks[nf:]
+    O, _, _ = oracle.varlen_fwd(c.q, c.k, c.v, c.cu_seqlens, c.cu_seqlens_k, c.scale, torch.from_numpy(kv_num),
+                                torch.from_numpy(kv_idx), torch.from_numpy(full_num), torch.from_numpy(full_idx),
+                                mask_mod="causal")
+
+    def keep(i, h, nq, nk):
+        qi = torch.arange(nq).view(-1, 1)
+        kj = torch.arange(nk).view(1, -1)
+        fb = torch.zeros(nq, nk, dtype=torch.bool)
+        pb = torch.zeros(nq, nk, dtype=torch.bool)
+        for qb in range((nq + 127) // 128):
+            for t in range(full_num[i, 0, qb]):
+                fb[qb * 128:(qb + 1) * 128, full_idx[i, 0, qb, t] * 128:(full_idx[i, 0, qb, t] + 1) * 128] = True
+            for t in range(kv_num[i, 0, qb]):
+                pb[qb * 128:(qb + 1) * 128, kv_idx[i, 0, qb, t] * 128:(kv_idx[i, 0, qb, t] + 1) * 128] = True
+        return fb | (pb & (kj <= qi))
+
+    np.testing.assert_allclose(O, _varlen_sdpa_pairs(c, keep), atol=1e-12)
+
+
+def test_varlen_per_head_lists_index_by_head():
+    """mask_heads = H: head h reads row [seq, h, q block] of the lists; per-head SDPA with the
+    element mask of that head's lists."""
+    lengths = [260, 200]
+    c = synth.make_varlen("t", 2, 0, 0, 3, 8, "f32", seed=32, lengths=lengths, block_lists="none")
+    kn, ki, fn, fi = synth.causal_block_lists(lengths, mask_heads=3)
+    fn[:, 1] = 0              # head 1: diagonal blocks only
+    kn[:, 2] = 0              # head 2: full blocks only (the diagonal block is unlisted)
+    O, _, _ = oracle.varlen_fwd(c.q, c.k, c.v, c.cu_seqlens, c.cu_seqlens, c.scale, kn, ki, fn, fi,
+                                mask_mod="causal")
+
+    def keep(i, h, nq, nk):
+        qi = torch.arange(nq).view(-1, 1)
+        kj = torch.arange(nk).view(1, -1)
+        same_block = (qi // 128) == (kj // 128)
+        earlier_block = (kj // 128) < (qi // 128)
+        if h == 0:
+            return kj <= qi
+        if h == 1:
+            return same_block & (kj <= qi)
+        return earlier_block
+
+    ref = _varlen_sdpa_pairs(c, keep)
+    # head 2, q block 0 lists nothing: every logit is -1e9 -> mean of V over the sequence (not SDPA's NaN)
+    for i, L in enumerate(lengths):
+        a = int(c.cu_seqlens[i])
+        ref[a:a + min(128, L), 2] = _f64(c.v[a:a + L, 2]).mean(0).numpy()
+    np.testing.assert_allclose(O, ref, atol=1e-12)
