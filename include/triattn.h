@@ -53,9 +53,18 @@ typedef enum {
 typedef enum { TA_F32 = 0, TA_F16 = 1, TA_BF16 = 2 } ta_dtype;
 
 /* Element predicate applied on partial blocks of a BlockMask (tensorplay
- * "BlockMask", Details 2: mask_mod is skipped on full blocks).  CAUSAL keeps
- * key k for query q when k <= q, both indices local to their sequence. */
-typedef enum { TA_MASK_NONE = 0, TA_MASK_CAUSAL = 1 } ta_mask_mod;
+ * "BlockMask", Details 2: mask_mod is skipped on full blocks), for query q and
+ * key k, both indices local to their sequence:
+ *   CAUSAL          k <= q
+ *   SLIDING_WINDOW  q - window < k <= q  (the query and the window - 1 keys before it)
+ *   PREFIX_LM       k <= q  or  k < prefix  (the sequence's prefix is seen by every query)
+ * The last two carry a parameter and are taken by tri_attn_varlen_fwd_masked only. */
+typedef enum {
+    TA_MASK_NONE = 0,
+    TA_MASK_CAUSAL = 1,
+    TA_MASK_SLIDING_WINDOW = 2,
+    TA_MASK_PREFIX_LM = 3
+} ta_mask_mod;
 
 /*
  * tri_attn_fwd -- triangle-attention forward.
@@ -172,6 +181,39 @@ ta_status tri_attn_varlen_fwd_strided(const void* q, const void* k, const void* 
                                       int block_q, int block_k, ta_mask_mod mask_mod,
                                       long long q_row_stride, long long k_row_stride, long long v_row_stride,
                                       void* out, float* lse, float* max, void* stream);
+
+/*
+ * tri_attn_varlen_fwd_masked -- tri_attn_varlen_fwd_strided with the
+ * parameterised mask_mods.
+ * (tensorplay nn.attention "BlockMask": from_kv_blocks(..., mask_mod=...) and
+ *  Details 2, mask_mod applied on partial blocks only; the sliding-window and
+ *  prefix-LM predicates are the two most common mask_mods besides causal.)
+ *
+ *   mask_mod        TA_MASK_NONE, TA_MASK_CAUSAL, TA_MASK_SLIDING_WINDOW or
+ *                   TA_MASK_PREFIX_LM (else TA_ERR_INVALID_ARG)
+ *   window          SLIDING_WINDOW: keys q - window < k <= q are kept; must be
+ *                   >= 1 (else TA_ERR_INVALID_ARG); ignored otherwise
+ *   prefix_lengths  PREFIX_LM: optional (num_seqs) int32 on the device, the
+ *                   prefix of each sequence (values <= 0 keep only causal
+ *                   keys); when NULL, `prefix_length` (>= 0, else
+ *                   TA_ERR_INVALID_ARG) applies to every sequence
+ *   every other argument as in tri_attn_varlen_fwd_strided (which takes
+ *   TA_MASK_NONE and TA_MASK_CAUSAL only).  A row whose visited keys are all
+ *   masked gets the mean of V over the sequence's keys (every logit -1e9), as
+ *   with any other mask.
+ */
+ta_status tri_attn_varlen_fwd_masked(const void* q, const void* k, const void* v, ta_dtype dtype,
+                                     const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                     int num_seqs, int total_q, int total_k,
+                                     int max_seqlen_q, int max_seqlen_k, int H, int D,
+                                     float scale,
+                                     const int32_t* kv_num_blocks, const int32_t* kv_indices,
+                                     const int32_t* full_kv_num_blocks, const int32_t* full_kv_indices,
+                                     int mask_heads, int max_q_blocks, int max_kv_blocks,
+                                     int block_q, int block_k, ta_mask_mod mask_mod,
+                                     int window, const int32_t* prefix_lengths, int prefix_length,
+                                     long long q_row_stride, long long k_row_stride, long long v_row_stride,
+                                     void* out, float* lse, float* max, void* stream);
 
 /*
  * tri_attn_mask_to_kv_lengths -- dense key mask -> prefix lengths.

@@ -16,11 +16,11 @@ LIB_PATH = os.path.join(_PKG, "libtriattn.so")
 
 TA_OK, TA_ERR_INVALID_ARG, TA_ERR_UNSUPPORTED, TA_ERR_CUDA, TA_ERR_TIMEOUT, TA_ERR_DEVICE = range(6)
 TA_F32, TA_F16, TA_BF16 = 0, 1, 2
-TA_MASK_NONE, TA_MASK_CAUSAL = 0, 1
+TA_MASK_NONE, TA_MASK_CAUSAL, TA_MASK_SLIDING_WINDOW, TA_MASK_PREFIX_LM = 0, 1, 2, 3
 
 # Every symbol include/triattn.h declares.
-EXPORTS = ("tri_attn_fwd", "tri_attn_varlen_fwd", "tri_attn_varlen_fwd_strided", "tri_attn_mask_to_kv_lengths",
-           "tri_attn_get_status", "tri_attn_error_string", "tri_attn_version")
+EXPORTS = ("tri_attn_fwd", "tri_attn_varlen_fwd", "tri_attn_varlen_fwd_strided", "tri_attn_varlen_fwd_masked",
+           "tri_attn_mask_to_kv_lengths", "tri_attn_get_status", "tri_attn_error_string", "tri_attn_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -52,6 +52,9 @@ def load() -> ctypes.CDLL:
         lib.tri_attn_varlen_fwd_strided.argtypes = [P, P, P, I, P, P, I, I, I, I, I, I, I, F, P, P, P, P, I, I, I, I,
                                                     I, I, L, L, L, P, P, P, P]
         lib.tri_attn_varlen_fwd_strided.restype = I
+        lib.tri_attn_varlen_fwd_masked.argtypes = [P, P, P, I, P, P, I, I, I, I, I, I, I, F, P, P, P, P, I, I, I, I,
+                                                   I, I, I, P, I, L, L, L, P, P, P, P]
+        lib.tri_attn_varlen_fwd_masked.restype = I
         lib.tri_attn_mask_to_kv_lengths.argtypes = [P, I, I, I, P, P, P]
         lib.tri_attn_mask_to_kv_lengths.restype = I
         lib.tri_attn_get_status.argtypes = [P]
@@ -109,6 +112,21 @@ def tri_attn_varlen_fwd_strided(q, k, v, dtype, cu_seqlens_q, cu_seqlens_k, num_
                                             int(q_row_stride), int(k_row_stride), int(v_row_stride), out,
                                             lse or None, max_ or None, stream or None)
     _check(st, "tri_attn_varlen_fwd_strided")
+
+
+def tri_attn_varlen_fwd_masked(q, k, v, dtype, cu_seqlens_q, cu_seqlens_k, num_seqs, total_q, total_k,
+                               max_seqlen_q, max_seqlen_k, H, D, scale, kv_num_blocks, kv_indices, full_kv_num_blocks,
+                               full_kv_indices, mask_heads, max_q_blocks, max_kv_blocks, block_q, block_k, mask_mod,
+                               window, prefix_lengths, prefix_length, q_row_stride, k_row_stride, v_row_stride, out,
+                               lse, max_, stream) -> None:
+    st = load().tri_attn_varlen_fwd_masked(q, k, v, dtype, cu_seqlens_q, cu_seqlens_k, num_seqs, total_q, total_k,
+                                           max_seqlen_q, max_seqlen_k, H, D, float(scale), kv_num_blocks or None,
+                                           kv_indices or None, full_kv_num_blocks or None, full_kv_indices or None,
+                                           mask_heads, max_q_blocks, max_kv_blocks, block_q, block_k, mask_mod,
+                                           int(window), prefix_lengths or None, int(prefix_length),
+                                           int(q_row_stride), int(k_row_stride), int(v_row_stride), out,
+                                           lse or None, max_ or None, stream or None)
+    _check(st, "tri_attn_varlen_fwd_masked")
 
 
 def tri_attn_mask_to_kv_lengths(mask, B, N, K, kv_lengths, nonprefix_count, stream) -> None:

@@ -16,6 +16,8 @@ import torch
 from . import abi
 
 _DT = {torch.float32: abi.TA_F32, torch.float16: abi.TA_F16, torch.bfloat16: abi.TA_BF16}
+_MASK_MODS = {None: abi.TA_MASK_NONE, "none": abi.TA_MASK_NONE, "causal": abi.TA_MASK_CAUSAL,
+              "sliding_window": abi.TA_MASK_SLIDING_WINDOW, "prefix_lm": abi.TA_MASK_PREFIX_LM}
 
 
 def _ptr(t: Optional[torch.Tensor]) -> int:
@@ -154,7 +156,9 @@ class BlockMask:
     kv_num_blocks (S, Hm, MQ) and kv_indices (S, Hm, MQ, MK): partial blocks
     of each q block, where mask_mod applies; full_kv_* (optional, same shapes):
     blocks where every key is valid.  Indices are sequence-local 128-row
-    blocks.  mask_mod is None or "causal" (a C ABI cannot take a callable).
+    blocks.  mask_mod is None, "causal", "sliding_window" or "prefix_lm" (a C
+    ABI cannot take a callable; the last two take their parameter from
+    ``varlen_attention``'s ``window`` / ``prefix_lengths``).
     seq_lengths (q_len, kv_len), as on the page's from_kv_blocks, fixes the
     number of kv blocks, i.e. the columns of ``to_dense``; without it the
     columns are the larger of MK and the highest listed block index + 1.
@@ -178,14 +182,14 @@ class BlockMask:
             raise RuntimeError("BlockMask must have at least 2 dimensions")
         assert (full_kv_num_blocks is None) == (full_kv_indices is None), \
             "full_kv_num_blocks and full_kv_indices must be both provided or omitted"
-        if mask_mod not in (None, "causal", "none"):
-            raise ValueError("mask_mod must be None or 'causal'")
+        if mask_mod not in _MASK_MODS:
+            raise ValueError(f"mask_mod must be one of {sorted(k for k in _MASK_MODS if k)} or None")
         return cls(kv_num_blocks, kv_indices, full_kv_num_blocks, full_kv_indices, BLOCK_SIZE, mask_mod,
                    seq_lengths)
 
     @property
     def mask_mod_code(self) -> int:
-        return abi.TA_MASK_CAUSAL if self.mask_mod == "causal" else abi.TA_MASK_NONE
+        return _MASK_MODS[self.mask_mod]
 
     def _lists(self):
         pairs = [(self.kv_num_blocks.cpu(), self.kv_indices.cpu())]
@@ -260,15 +264,18 @@ def _row_stride(t: torch.Tensor, name: str, device: torch.device) -> int:
 
 
 def varlen_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, block_mask=None, scale=None,
-                     return_aux=False, *, mask_mod=None, out=None):
+                     return_aux=False, *, mask_mod=None, out=None, window=0, prefix_lengths=None):
     """Packed-sequence forward with an optional BlockMask.
 
     q (total_q,H,D), k/v (total_k,H,D), cu_seqlens int32 (S+1,).  q, k, v may
     be row-strided views (heads and elements contiguous), e.g. the slices of
     an interleaved QKV or KV buffer (see ``varlen_attention_qkvpacked`` /
     ``varlen_attention_kvpacked``); ``out`` is contiguous.  Without a
-    block_mask every block is visited and ``mask_mod`` (None / "causal")
-    applies everywhere.  Returns O, or (O, lse, max) with lse/max (H, total_q).
+    block_mask every block is visited and ``mask_mod`` applies everywhere.
+    mask_mod: None, "causal" (k <= q), "sliding_window" (q - window < k <= q)
+    or "prefix_lm" (k <= q or k < the sequence's prefix; ``prefix_lengths`` is
+    an int or an int32 CUDA tensor with one length per sequence).
+    Returns O, or (O, lse, max) with lse/max (H, total_q).
     """
     if q.dim() != 3 or k.dim() != 3 or v.dim() != 3:
         raise ValueError("expected q (total_q,H,D), k/v (total_k,H,D)")
@@ -294,7 +301,9 @@ def varlen_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seql
     kn = ki = fn = fi = None
     mask_heads = MQ = MK = 0
     bq = bk = 128
-    mm = abi.TA_MASK_CAUSAL if mask_mod == "causal" else abi.TA_MASK_NONE
+    if mask_mod not in _MASK_MODS:
+        raise ValueError(f"mask_mod must be one of {sorted(k for k in _MASK_MODS if k)} or None")
+    mm = _MASK_MODS[mask_mod]
     if block_mask is not None:
         kn, ki = block_mask.kv_num_blocks, block_mask.kv_indices
         fn, fi = block_mask.full_kv_num_blocks, block_mask.full_kv_indices
@@ -319,35 +328,44 @@ def varlen_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seql
     if return_aux:
         lse = torch.empty(H, total_q, device=dev, dtype=torch.float32)
         mx = torch.empty(H, total_q, device=dev, dtype=torch.float32)
+    pl, p_all = None, 0
+    if isinstance(prefix_lengths, torch.Tensor):
+        _need(prefix_lengths, "prefix_lengths", dev)
+        if prefix_lengths.dtype != torch.int32 or prefix_lengths.numel() != S:
+            raise ValueError("prefix_lengths must be int32 with one entry per sequence")
+        pl = prefix_lengths
+    elif prefix_lengths is not None:
+        p_all = int(prefix_lengths)
     with torch.cuda.device(dev):
-        abi.tri_attn_varlen_fwd_strided(_ptr(q), _ptr(k), _ptr(v), _DT[q.dtype], _ptr(cu_seqlens_q),
-                                        _ptr(cu_seqlens_k), S, total_q, k.shape[0], int(max_seqlen_q),
-                                        int(max_seqlen_k), H, D, s, _ptr(kn), _ptr(ki), _ptr(fn), _ptr(fi),
-                                        mask_heads, MQ, MK, bq, bk, mm, q_rs, k_rs, v_rs, _ptr(out), _ptr(lse),
-                                        _ptr(mx), _stream(dev))
+        abi.tri_attn_varlen_fwd_masked(_ptr(q), _ptr(k), _ptr(v), _DT[q.dtype], _ptr(cu_seqlens_q),
+                                       _ptr(cu_seqlens_k), S, total_q, k.shape[0], int(max_seqlen_q),
+                                       int(max_seqlen_k), H, D, s, _ptr(kn), _ptr(ki), _ptr(fn), _ptr(fi),
+                                       mask_heads, MQ, MK, bq, bk, mm, int(window), _ptr(pl), p_all, q_rs, k_rs, v_rs,
+                                       _ptr(out), _ptr(lse), _ptr(mx), _stream(dev))
     return (out, lse, mx) if return_aux else out
 
 
 def varlen_attention_qkvpacked(qkv, cu_seqlens, max_seqlen, block_mask=None, scale=None, return_aux=False, *,
-                               mask_mod=None, out=None):
+                               mask_mod=None, out=None, window=0, prefix_lengths=None):
     """NVTE_QKV_INTERLEAVED (Transformer Engine fused_attn.h): one (total, 3, H, D) buffer, q and k sharing
     cu_seqlens.  The kernels read q, k, v in place through row strides; no copy is made."""
     if qkv.dim() != 4 or qkv.shape[1] != 3:
         raise ValueError("expected qkv (total, 3, H, D)")
     q, k, v = qkv.unbind(1)
     return varlen_attention(q, k, v, cu_seqlens, cu_seqlens, max_seqlen, max_seqlen, block_mask, scale, return_aux,
-                            mask_mod=mask_mod, out=out)
+                            mask_mod=mask_mod, out=out, window=window, prefix_lengths=prefix_lengths)
 
 
 def varlen_attention_kvpacked(q, kv, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, block_mask=None,
-                              scale=None, return_aux=False, *, mask_mod=None, out=None):
+                              scale=None, return_aux=False, *, mask_mod=None, out=None, window=0,
+                              prefix_lengths=None):
     """NVTE_KV_INTERLEAVED (Transformer Engine fused_attn.h): q (total_q, H, D) and one (total_k, 2, H, D)
     buffer for k and v, read in place through row strides."""
     if kv.dim() != 4 or kv.shape[1] != 2:
         raise ValueError("expected kv (total_k, 2, H, D)")
     k, v = kv.unbind(1)
     return varlen_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, block_mask, scale,
-                            return_aux, mask_mod=mask_mod, out=out)
+                            return_aux, mask_mod=mask_mod, out=out, window=window, prefix_lengths=prefix_lengths)
 
 
 def get_status(device=None) -> int:

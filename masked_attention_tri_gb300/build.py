@@ -77,5 +77,31 @@ def build(force: bool = False, verbose: bool = False) -> str:
     return LIB
 
 
+def build_variant(name: str, defines: list[str]) -> str:
+    """Compile the same sources with extra -D flags into _build/<name>/libtriattn_<name>.so (a
+    separate library with its own device status word); used by the tests of the failure path."""
+    nvcc = _nvcc()
+    out_dir = os.path.join(BUILD, name)
+    os.makedirs(out_dir, exist_ok=True)
+    lib = os.path.join(out_dir, f"libtriattn_{name}.so")
+    flags = [f"-D{d}" for d in defines]
+
+    def compile_one(src: str) -> str:
+        obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
+        r = subprocess.run([nvcc, *NVCC_FLAGS, *flags, "-c", src, "-o", obj], capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed on {os.path.basename(src)}:\n{r.stdout}\n{r.stderr}")
+        return obj
+
+    srcs = sources()
+    with ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
+        objs = list(ex.map(compile_one, srcs))
+    r = subprocess.run([nvcc, *ARCH, "-shared", "--cudart", "static", "-o", lib, *objs], capture_output=True,
+                       text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+    return lib
+
+
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))

@@ -134,11 +134,35 @@ TA_EXPORT ta_status tri_attn_varlen_fwd_strided(const void* q, const void* k, co
                                                 int block_k, ta_mask_mod mask_mod, long long q_row_stride,
                                                 long long k_row_stride, long long v_row_stride, void* out,
                                                 float* lse, float* max, void* stream) {
+    // The parameterised mask_mods take their parameter through tri_attn_varlen_fwd_masked.
+    if (mask_mod != TA_MASK_NONE && mask_mod != TA_MASK_CAUSAL) return TA_ERR_INVALID_ARG;
+    return tri_attn_varlen_fwd_masked(q, k, v, dtype, cu_seqlens_q, cu_seqlens_k, num_seqs, total_q, total_k,
+                                      max_seqlen_q, max_seqlen_k, H, D, scale, kv_num_blocks, kv_indices,
+                                      full_kv_num_blocks, full_kv_indices, mask_heads, max_q_blocks, max_kv_blocks,
+                                      block_q, block_k, mask_mod, 0, nullptr, 0, q_row_stride, k_row_stride,
+                                      v_row_stride, out, lse, max, stream);
+}
+
+TA_EXPORT ta_status tri_attn_varlen_fwd_masked(const void* q, const void* k, const void* v, ta_dtype dtype,
+                                               const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                               int num_seqs, int total_q, int total_k, int max_seqlen_q,
+                                               int max_seqlen_k, int H, int D, float scale,
+                                               const int32_t* kv_num_blocks, const int32_t* kv_indices,
+                                               const int32_t* full_kv_num_blocks, const int32_t* full_kv_indices,
+                                               int mask_heads, int max_q_blocks, int max_kv_blocks, int block_q,
+                                               int block_k, ta_mask_mod mask_mod, int window,
+                                               const int32_t* prefix_lengths, int prefix_length,
+                                               long long q_row_stride, long long k_row_stride,
+                                               long long v_row_stride, void* out, float* lse, float* max,
+                                               void* stream) {
     if (!q || !k || !v || !out || !cu_seqlens_q || !cu_seqlens_k) return TA_ERR_INVALID_ARG;
     if (num_seqs <= 0 || H <= 0 || D <= 0 || max_seqlen_q < 0 || max_seqlen_k < 0) return TA_ERR_INVALID_ARG;
     if (total_q < 0 || total_k < 0) return TA_ERR_INVALID_ARG;
     if (!valid_dtype(dtype)) return TA_ERR_INVALID_ARG;
-    if (mask_mod != TA_MASK_NONE && mask_mod != TA_MASK_CAUSAL) return TA_ERR_INVALID_ARG;
+    if (mask_mod < TA_MASK_NONE || mask_mod > TA_MASK_PREFIX_LM) return TA_ERR_INVALID_ARG;
+    if (mask_mod == TA_MASK_SLIDING_WINDOW && window <= 0) return TA_ERR_INVALID_ARG;
+    if (mask_mod == TA_MASK_PREFIX_LM && !prefix_lengths && prefix_length < 0) return TA_ERR_INVALID_ARG;
+    if (prefix_lengths && !aligned(prefix_lengths, 4)) return TA_ERR_INVALID_ARG;
     if ((kv_num_blocks == nullptr) != (kv_indices == nullptr)) return TA_ERR_INVALID_ARG;
     if ((full_kv_num_blocks == nullptr) != (full_kv_indices == nullptr)) return TA_ERR_INVALID_ARG;
     if (full_kv_num_blocks && !kv_num_blocks) return TA_ERR_INVALID_ARG;
@@ -195,6 +219,9 @@ TA_EXPORT ta_status tri_attn_varlen_fwd_strided(const void* q, const void* k, co
     p.MQ = kv_num_blocks ? max_q_blocks : 0;
     p.MK = kv_num_blocks ? max_kv_blocks : 0;
     p.mask_mod = mask_mod;
+    p.window = mask_mod == TA_MASK_SLIDING_WINDOW ? window : 0;
+    p.prefix_len = mask_mod == TA_MASK_PREFIX_LM ? prefix_lengths : nullptr;
+    p.prefix_all = mask_mod == TA_MASK_PREFIX_LM ? prefix_length : 0;
     p.total_q = total_q;
     p.total_k = total_k;
     p.q_rs = q_row_stride;
@@ -235,4 +262,4 @@ TA_EXPORT const char* tri_attn_error_string(ta_status s) {
     }
 }
 
-TA_EXPORT int tri_attn_version(void) { return (1 << 16) | 1; }
+TA_EXPORT int tri_attn_version(void) { return (1 << 16) | 2; }

@@ -45,6 +45,9 @@ struct AttnParams {
     const int32_t* full_num;
     const int32_t* full_idx;
     int mask_heads, MQ, MK, mask_mod;
+    int window;             // TA_MASK_SLIDING_WINDOW: keys q - window < k <= q
+    const int32_t* prefix_len;  // TA_MASK_PREFIX_LM: per-sequence prefix lengths, or NULL:
+    int prefix_all;         //   then prefix_all for every sequence
     int total_q;            // rows of q/out (lse/max stride in varlen)
     int total_k;            // rows of k/v
     long long q_rs, k_rs, v_rs;  // varlen: elements between packed rows of q, k, v (out: H * D)

@@ -57,7 +57,7 @@ __device__ __forceinline__ float warp_sum(float x) {
 }
 
 // Key validity modes of one tile.
-enum { kKeyAll = 0, kKeyPrefix = 1, kKeyDense = 2, kKeyCausal = 3 };
+enum { kKeyAll = 0, kKeyPrefix = 1, kKeyDense = 2, kKeyMod = 3 };
 
 template <typename T, typename BT>
 struct SimtState {
@@ -73,6 +73,7 @@ struct SimtState {
     int bias_rs;
     int q0;               // first query row of the CTA (local index)
     int prefix_len;
+    int prefix_lm;        // packed form, mask_mod prefix LM: the sequence's prefix length
     const uint8_t* dense;
     float m[kRows], l[kRows], acc[kRows][kDPerLane];
     bool seen[kRows];
@@ -115,7 +116,12 @@ __device__ void simt_tile(SimtState<T, BT>& st, int key0, int mode) {
         bool valid = exists;
         if (mode == kKeyPrefix) valid = valid && key < st.prefix_len;
         else if (mode == kKeyDense) valid = valid && st.dense[key] != 0;
-        else if (mode == kKeyCausal) valid = valid && key <= qrow;
+        else if (mode == kKeyMod) {
+            // BlockMask mask_mod on a partial block, local indices
+            if (p.mask_mod == TA_MASK_CAUSAL) valid = valid && key <= qrow;
+            else if (p.mask_mod == TA_MASK_SLIDING_WINDOW) valid = valid && key <= qrow && qrow - key < p.window;
+            else if (p.mask_mod == TA_MASK_PREFIX_LM) valid = valid && (key <= qrow || key < st.prefix_lm);
+        }
         float x;
         if (!exists) {
             x = -INFINITY;
@@ -226,6 +232,7 @@ __global__ void __launch_bounds__(kWarps * 32) simt_fwd_kernel(const AttnParams 
         st.v_off = (long long)ck0 * p.v_rs + (long long)h * D;
         st.v_rs = p.v_rs;
         lse_off = (long long)h * p.total_q + cq0;  // (H, total_q)
+        st.prefix_lm = p.prefix_len ? p.prefix_len[seq] : p.prefix_all;
     }
     st.q0 = qt * kQT;
     if (st.q0 >= Lq) return;
@@ -257,7 +264,7 @@ __global__ void __launch_bounds__(kWarps * 32) simt_fwd_kernel(const AttnParams 
             for (int kb = 0; kb < nbk; ++kb)
                 for (int t = 0; t < 4; ++t)
                     if (kb * 128 + t * kKT < st.Lk)
-                        simt_tile(st, kb * 128 + t * kKT, p.mask_mod == TA_MASK_CAUSAL ? kKeyCausal : kKeyAll);
+                        simt_tile(st, kb * 128 + t * kKT, p.mask_mod != TA_MASK_NONE ? kKeyMod : kKeyAll);
         } else if (qb < p.MQ) {
             const int hm = p.mask_heads == 1 ? 0 : h;
             const long long row = ((long long)seq * p.mask_heads + hm) * p.MQ + qb;
@@ -276,7 +283,7 @@ __global__ void __launch_bounds__(kWarps * 32) simt_fwd_kernel(const AttnParams 
                 if (kb < 0 || kb >= nbk) continue;
                 for (int s4 = 0; s4 < 4; ++s4)
                     if (kb * 128 + s4 * kKT < st.Lk)
-                        simt_tile(st, kb * 128 + s4 * kKT, p.mask_mod == TA_MASK_CAUSAL ? kKeyCausal : kKeyAll);
+                        simt_tile(st, kb * 128 + s4 * kKT, p.mask_mod != TA_MASK_NONE ? kKeyMod : kKeyAll);
             }
         }
     }

@@ -1,8 +1,8 @@
 // tc_fwd.cu -- host side of the tcgen05 forward: TMA descriptors, geometry
 // (query tiles per CTA, pipeline depths, tensor-memory columns), the choice
-// of the folded softmax for the packed form, and the launch.  The kernel
-// itself is in tc_kernel.cuh; triangle problems with D <= 64 go to the
-// key-split kernel of tc_split.cuh.
+// of the folded softmax for the packed form, and the launch.  Triangle
+// problems with D <= 64 and packed sequences (up to kSplitMaxSeqs of them) go
+// to the key-split kernel of tc_split.cuh, the rest to tc_kernel.cuh.
 
 #include <cudaTypedefs.h>
 
@@ -16,7 +16,8 @@ namespace triattn {
 namespace tc {
 
 TRIATTN_TC_VARIANTS(TRIATTN_TC_EXTERN)
-TRIATTN_SPLIT_VARIANTS(TRIATTN_SPLIT_EXTERN)
+TRIATTN_SPLIT_TRI_VARIANTS(TRIATTN_SPLIT_EXTERN)
+TRIATTN_SPLIT_VARLEN_VARIANTS(TRIATTN_SPLIT_EXTERN)
 
 namespace {
 
@@ -96,17 +97,20 @@ bool choose_geometry(TcParams& P, bool varlen, int& NQ) {
     return false;
 }
 
-// The key-split kernel (triangle form, D <= 64): one query tile, three S
-// buffers and O in 512 tensor-memory columns; Q buffers, K/V stages and bias
-// stages as shared memory allows.
-bool choose_split_geometry(TcParams& P) {
+// The key-split kernel (triangle form with D <= 64, packed form with D <=
+// 128): one query tile per item; three S buffers and two O accumulators of
+// up to 64 columns, or two S buffers and two O accumulators of 128 columns,
+// in 512 tensor-memory columns; Q buffers, K/V stages and bias stages as
+// shared memory allows.
+bool choose_split_geometry(TcParams& P, bool varlen) {
     const int prefs[][3] = {{2, 3, 2}, {2, 3, 1}, {2, 2, 2}, {2, 2, 1}, {1, 2, 1}};
+    P.s_bufs = P.o_cols <= 64 ? 3 : 2;
     for (const auto& pr : prefs) {
         P.q_bufs = pr[0];
         P.kv_stages = pr[1];
-        P.bias_stages = pr[2];
+        P.bias_stages = varlen ? 0 : pr[2];
         if (make_split_layout(P).total + 1024 <= kSmemLimit) {
-            P.o_col0 = 384;
+            P.o_col0 = 128u * (uint32_t)P.s_bufs;
             P.tmem_cols = 512;
             return true;
         }
@@ -172,12 +176,14 @@ cudaError_t launch_tc_fwd(const AttnParams& a, cudaStream_t stream) {
         fold = a.scale > 0.f && std::isfinite(a.scale);
     }
     int NQ = 1;
-    const bool split = !a.varlen && D <= 64;
-    if (split ? !choose_split_geometry(P) : !choose_geometry(P, a.varlen != 0, NQ))
+    // Triangle form with D <= 64, and packed sequences whose offsets fit the
+    // key-split kernel's schedule, run on the key-split kernel.
+    const bool split = a.varlen ? a.num_seqs <= kSplitMaxSeqs : D <= 64;
+    if (split ? !choose_split_geometry(P, a.varlen != 0) : !choose_geometry(P, a.varlen != 0, NQ))
         return cudaErrorInvalidConfiguration;
     P.items_per_unit = (P.nqt + NQ - 1) / NQ;
     const long long units = !a.varlen ? (long long)a.B * a.N * a.H : (long long)a.num_seqs * a.H;
-    const long long items = units * P.items_per_unit;
+    const long long items = units * P.items_per_unit;  // packed form: an upper bound (empty q blocks included)
     if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     P.items = (int)items;
     // Divisors of the work-item decode (each at least 1; with no items nothing is launched).
@@ -189,7 +195,14 @@ cudaError_t launch_tc_fwd(const AttnParams& a, cudaStream_t stream) {
     if (sms <= 0) return cudaErrorInvalidDevice;
     const int grid = P.items < sms ? P.items : sms;
     if (grid <= 0) return cudaSuccess;
+    P.fd_2g = make_fastdiv(2u * (uint32_t)grid);
 
+    if (a.varlen && split) {
+        if (bf16) return fold ? launch_split<true, false, true, true>(P, grid, stream)
+                              : launch_split<true, false, true, false>(P, grid, stream);
+        return fold ? launch_split<false, false, true, true>(P, grid, stream)
+                    : launch_split<false, false, true, false>(P, grid, stream);
+    }
     if (a.varlen) {
         if (bf16) return fold ? launch_nq<true, true, false, true>(NQ, P, grid, stream)
                               : launch_nq<true, true, false, false>(NQ, P, grid, stream);
@@ -198,8 +211,10 @@ cudaError_t launch_tc_fwd(const AttnParams& a, cudaStream_t stream) {
     }
     (void)fold;
     if (split) {
-        if (bf16) return a.bias_f32 ? launch_split<true, true>(P, grid, stream) : launch_split<true, false>(P, grid, stream);
-        return a.bias_f32 ? launch_split<false, true>(P, grid, stream) : launch_split<false, false>(P, grid, stream);
+        if (bf16) return a.bias_f32 ? launch_split<true, true, false, false>(P, grid, stream)
+                                    : launch_split<true, false, false, false>(P, grid, stream);
+        return a.bias_f32 ? launch_split<false, true, false, false>(P, grid, stream)
+                          : launch_split<false, false, false, false>(P, grid, stream);
     }
     if (bf16) return a.bias_f32 ? launch_nq<false, true, true, false>(NQ, P, grid, stream)
                                 : launch_nq<false, true, false, false>(NQ, P, grid, stream);

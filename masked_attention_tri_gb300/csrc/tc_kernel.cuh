@@ -65,7 +65,12 @@ constexpr uint32_t kBox = 128 * 128;        // one [128 rows][128 B] swizzled TM
 constexpr float kMasked = -1.0e9f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;        // rescale O when the row max grows by > 2^8
-constexpr long long kTimeoutCycles = 4000000000LL;
+// Cycles a bounded wait spins before it gives up (about 2 s).  Test builds of
+// the failure path shorten it with -DTRIATTN_WAIT_LIMIT_CYCLES.
+#ifndef TRIATTN_WAIT_LIMIT_CYCLES
+#define TRIATTN_WAIT_LIMIT_CYCLES 4000000000LL
+#endif
+constexpr long long kTimeoutCycles = TRIATTN_WAIT_LIMIT_CYCLES;
 
 // Division by a divisor fixed at launch, for 0 <= n < 2^31 (multiply-high
 // and shift with a host-computed magic number, Granlund and Montgomery's
@@ -117,6 +122,10 @@ struct TcParams {
     // Folded softmax (packed form, scale > 0): the softmax reads raw S = Q K^T
     // and applies s inside the exponent.
     float scale_log2e;  // s * log2(e)
+    // Key-split kernel only: S buffers (3 with D <= 64, 2 above), O accumulators
+    // (2), and the divisor 2 * grid of the packed form's serpentine deal.
+    int s_bufs;
+    FastDiv fd_2g;
 };
 
 // ---------------------------------------------------------------------------
@@ -322,6 +331,33 @@ __device__ __forceinline__ float load16(const void* base, long long i) {
 
 __device__ __forceinline__ uint32_t low_bits(int n) {
     return n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : ((1u << n) - 1u));
+}
+
+// BlockMask mask_mod on a partial block (tensorplay BlockMask page, Details 2),
+// local indices: bit j of the result says key kg + j is kept for query q.
+//   causal          k <= q
+//   sliding window  q - window < k <= q
+//   prefix LM       k <= q or k < prefix
+__device__ __forceinline__ uint32_t mod_bits(int mod, int q, int kg, int window, int prefix) {
+    const uint32_t causal = low_bits(q - kg + 1);
+    switch (mod) {
+    case TA_MASK_CAUSAL: return causal;
+    case TA_MASK_SLIDING_WINDOW: return causal & ~low_bits(q - window + 1 - kg);
+    case TA_MASK_PREFIX_LM: return causal | low_bits(prefix - kg);
+    default: return 0xffffffffu;
+    }
+}
+
+// True when mask_mod keeps every key of [key0, key0 + 128) for every query of
+// [q0, q0 + 128).
+__device__ __forceinline__ bool mod_tile_all(int mod, int q0, int key0, int window, int prefix) {
+    const bool causal = key0 + 127 <= q0;
+    switch (mod) {
+    case TA_MASK_CAUSAL: return causal;
+    case TA_MASK_SLIDING_WINDOW: return causal && (q0 + 127) - key0 < window;
+    case TA_MASK_PREFIX_LM: return causal || key0 + 128 <= prefix;
+    default: return true;
+    }
 }
 
 // Position in a ring of n pipeline stages: the stage, the parity of the
@@ -819,6 +855,7 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
         for (int item = blockIdx.x; item < P.items && ok; item += gridDim.x) {
             const Item<NQ> it = decode<NQ, VARLEN>(P, item);
             if (VARLEN && it.bad && threadIdx.x == 0) atomicCAS(a.status, 0, kStatusDevice);
+            const int prefix_lm = !VARLEN ? 0 : (a.prefix_len ? a.prefix_len[it.seq] : a.prefix_all);
             bool on_s = false;
             int qt_s = 0;
 #pragma unroll
@@ -837,15 +874,15 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
                 const bool full = (fs >> slot) & 1u;
                 const int key0 = kb * kBN;
                 int vlim;
-                bool causal = false;
+                bool modded = false;  // mask_mod applies (a partial block)
                 if constexpr (!VARLEN) {
                     vlim = P.mask_kind == 1 ? it.prefix : a.K;
                 } else {
                     vlim = it.Lk;
-                    causal = !full && a.mask_mod == TA_MASK_CAUSAL;
+                    modded = !full && a.mask_mod != TA_MASK_NONE;
                 }
                 const bool all_valid = (VARLEN || P.mask_kind != 2) && key0 + kBN <= vlim &&
-                                       (!causal || key0 + kBN - 1 <= qt_s * kBM);
+                                       (!modded || mod_tile_all(a.mask_mod, qt_s * kBM, key0, a.window, prefix_lm));
                 const int nexist = (VARLEN ? it.Lk : a.K) - key0;
 
                 uint32_t boff = 0, mwoff = 0;  // this row's bias / the mask words, from the aligned base
@@ -932,7 +969,7 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
                                 if (P.mask_kind == 2)
                                     vm &= *reinterpret_cast<const uint32_t*>(gbase + mwoff + 4u * (uint32_t)(2 * c + h));
                             } else {
-                                if (causal) vm &= low_bits(qrow - key0 - k0 + 1);
+                                if (modded) vm &= mod_bits(a.mask_mod, qrow, key0 + k0, a.window, prefix_lm);
                             }
 #pragma unroll
                             for (int j = 0; j < 32; ++j)

@@ -1,9 +1,10 @@
-// tc_split.cuh -- tcgen05 / TMA forward, triangle form with D <= 64: one
-// 128-row query tile per work item, its softmax split over eight warps, S
-// triple-buffered and O double-buffered in tensor memory.  Launched from
-// tc_fwd.cu, instantiated in tc_inst_split.cu.  Computes the same
+// tc_split.cuh -- tcgen05 / TMA forward with one 128-row query tile per work
+// item and its softmax split over eight warps: the triangle form with D <= 64,
+// and the packed-sequence (varlen) form with D <= 128.  Launched from
+// tc_fwd.cu, instantiated in tc_inst_split*.cu.  Computes the same
 // cuEquivariance triangle_attention formula as tc_kernel.cuh (see there for
-// masking and the lazy rescale).
+// masking and the lazy rescale); the packed form visits the kv blocks that a
+// tensorplay BlockMask lists for each q block (full blocks skip mask_mod).
 //
 // Warp roles:
 //   warps 0..7   softmax.  Warp w works on the 32 rows of TMEM lane quarter
@@ -15,19 +16,32 @@
 //                columns after swapping the partial row sums once per item.
 //   warp 8       producer: TMA of Q and K;
 //   warp 9       MMA (warp-wide loop, one elected lane issues);
-//   warp 10      bias producer: TMA of bias tiles and the dense-mask bits;
+//   warp 10      bias producer: TMA of bias tiles and the dense-mask bits
+//                (triangle form);
 //   warp 11      producer: TMA of V.
 // The MMA warp walks the CTA's key tiles as one stream across work items:
-// S of tile n + 3 goes into the buffer of tile n as soon as PV of tile n is
-// issued, also when tile n + 3 belongs to the next item, so the softmax
-// finds the next S ready at item boundaries too.  Items alternate between
-// two O accumulators, and the softmax writes out an item's O after the first
-// tile of the next item, when the last PV of the item has long finished.
-// Tensor memory: three S buffers at columns [0,384) (P overwrites the first 64
-// columns of its buffer), O_0 and O_1 at [384, 384 + 2 o_cols).  K and V
-// stages have their own barriers: a K stage is refilled once its QK^T is done,
-// a V stage once its PV is.  The softmax waits for a PV only before it
-// rescales O and before it reads O.
+// S of tile n + s_bufs goes into the buffer of tile n as soon as PV of tile n
+// is issued, also when that tile belongs to the next item, so the softmax
+// finds the next S ready at item boundaries too.  Items alternate between two
+// O accumulators, and the softmax writes out an item's O after the first tile
+// of the next item, when the last PV of the item has long finished.  Tensor
+// memory: s_bufs S buffers of 128 columns from column 0 (P overwrites the
+// first 64 columns of its buffer), O_0 and O_1 from column 128 s_bufs: three
+// S buffers with D <= 64 (O 2 x 64 columns), two with D in (64, 128] (O 2 x
+// 128 columns).  K and V stages have their own barriers: a K stage is
+// refilled once its QK^T is done, a V stage once its PV is.  The softmax
+// waits for a PV only before it rescales O and before it reads O.
+//
+// Work items.  Triangle form: one q tile of one (b, n, h) slab, in index
+// order, dealt round-robin over the CTAs (q tiles fastest, then n: the CTAs
+// running at once share K / V and bias tiles in L2).  Packed form: one
+// 128-row q block of one (sequence, head).  A causal q block visits about as
+// many kv blocks as its index + 1, so items are ordered by q block,
+// highest first (within one q block by sequence, then head) and dealt
+// serpentine (CTA c takes positions c, 2G - 1 - c, 2G + c, ... of G CTAs),
+// which balances the CTAs' key-tile counts much like a longest-first
+// schedule.  Every CTA reads the sequence offsets into shared memory once and
+// walks this order itself; every role walks it the same way.
 
 #pragma once
 
@@ -37,9 +51,12 @@ namespace triattn {
 namespace tc {
 
 constexpr int kSplitThreads = 12 * 32;
+// Packed form: sequences whose offsets the schedule keeps in shared memory
+// (more sequences go to the two-tile kernel).
+constexpr int kSplitMaxSeqs = 1024;
 
 struct SplitLayout {
-    uint32_t q, kv, bias, maskw, xbuf, xl, bars, tmem_slot, abort_flag, total;
+    uint32_t q, kv, bias, maskw, xbuf, xl, sched, bars, tmem_slot, abort_flag, total;
     int nbars;
 };
 
@@ -51,33 +68,260 @@ __host__ __device__ inline SplitLayout make_split_layout(const TcParams& P) {
     L.maskw = L.bias + P.bias_stages * P.bias_bytes;
     L.xbuf = L.maskw + P.bias_stages * 16;   // row maxima: [tile parity][key half][128 rows] fp32
     L.xl = L.xbuf + 2 * 2 * 128 * 4;           // row sums: [key half][128 rows] fp32
-    L.bars = L.xl + 2 * 128 * 4;
+    L.sched = L.xl + 2 * 128 * 4;              // packed form: cu_q[S+1], cu_k[S+1], q blocks[S] (int32)
+    const uint32_t sched_bytes = P.a.varlen ? (uint32_t)(3 * P.a.num_seqs + 2) * 4u : 0u;
+    L.bars = (L.sched + sched_bytes + 15u) & ~15u;
     // q_full, q_empty (QB each), k_full, k_empty, v_full, v_empty (S each),
-    // bias_full, bias_empty (BS each), s_full[3], p_full[3], pv_done[2],
-    // xchg[4], drain
-    L.nbars = 2 * P.q_bufs + 4 * P.kv_stages + 2 * P.bias_stages + 3 + 3 + 2 + 4 + 1;
+    // bias_full, bias_empty (BS each), s_full[s_bufs], p_full[s_bufs],
+    // pv_done[2], xchg[4], drain
+    L.nbars = 2 * P.q_bufs + 4 * P.kv_stages + 2 * P.bias_stages + 2 * P.s_bufs + 2 + 4 + 1;
     L.tmem_slot = L.bars + 8 * L.nbars;
     L.abort_flag = L.tmem_slot + 4;
     L.total = L.abort_flag + 4;
     return L;
 }
 
-// A position in the CTA's stream of key tiles: the current item with work,
-// its key-tile count, the next tile in it and the item's number among the
-// CTA's items with work.
+// One work item of the key-split kernel.
+struct SItem {
+    int qt;             // q tile (triangle) / q block (packed form)
+    long long unit;     // triangle: (b*N+n)*H+h
+    long long bn;       // triangle: b*N+n
+    int b, h, seq;
+    int Lq, Lk;         // query rows / keys of the unit
+    int q_row0, k_row0; // packed form: first row of the sequence
+    int prefix;         // triangle kv_lengths (clamped)
+    int nkb;            // key blocks of the unit
+    int nkt;            // key tiles the item visits
+    bool lists;         // packed form: BlockMask lists given
+    const int32_t* part_l;
+    const int32_t* full_l;
+    int n_part, n_full;
+    uint64_t part0, full0;  // packed form: visited blocks of window 0 (blocks 0..63)
+};
+
+// Packed form, blocks [64 w, 64 w + 64) of the item: `part` (mask_mod applies)
+// and `full` (mask_mod skipped).  Warp-cooperative (every lane of the warp
+// calls it and gets the same masks): lane t reads list entries t, t + 32, ...
+__device__ __forceinline__ void split_window(const SItem& it, int w, uint64_t& part, uint64_t& full) {
+    const int lo = 64 * w;
+    const int n = min(64, it.nkb - lo);
+    if (n <= 0) {
+        part = full = 0;
+        return;
+    }
+    const uint64_t range = n >= 64 ? ~0ull : ((1ull << n) - 1ull);
+    if (!it.lists) {
+        part = range;
+        full = 0;
+        return;
+    }
+    const int lane = threadIdx.x % 32;
+    uint64_t p = 0, f = 0;
+    for (int t = lane; t < it.n_part; t += 32) {
+        const int kb = it.part_l[t] - lo;
+        if (kb >= 0 && kb < n) p |= 1ull << kb;
+    }
+    for (int t = lane; t < it.n_full; t += 32) {
+        const int kb = it.full_l[t] - lo;
+        if (kb >= 0 && kb < n) f |= 1ull << kb;
+    }
+    const uint32_t plo = __reduce_or_sync(0xffffffffu, (uint32_t)p), phi = __reduce_or_sync(0xffffffffu, (uint32_t)(p >> 32));
+    const uint32_t flo = __reduce_or_sync(0xffffffffu, (uint32_t)f), fhi = __reduce_or_sync(0xffffffffu, (uint32_t)(f >> 32));
+    full = ((uint64_t)fhi << 32) | flo;
+    part = (((uint64_t)phi << 32) | plo) & ~full;
+}
+
+// The packed form's schedule: a cursor over (q block descending, sequence,
+// head) and the serpentine deal of those positions over the grid.
+struct VCursor {
+    int qb, s, hnext;
+    uint32_t cnt;  // positions before (qb, s)
+};
+
+__device__ __forceinline__ VCursor vcursor_begin(const TcParams& P) { return VCursor{P.nqt - 1, 0, 0, 0u}; }
+
+// Next item of this CTA: (sequence, head, q block).  `snb` holds each
+// sequence's q block count (0 for a sequence that breaks its contract).
+__device__ __forceinline__ bool vcursor_next(const TcParams& P, const int* snb, VCursor& c, int& seq, int& h,
+                                             int& qb) {
+    const int S = P.a.num_seqs, H = P.a.H;
+    const uint32_t G2 = P.fd_2g.d;
+    const uint32_t lo = blockIdx.x, hi = G2 - 1u - blockIdx.x;
+    while (c.qb >= 0) {
+        if (c.s >= S) {
+            c.s = 0;
+            --c.qb;
+            continue;
+        }
+        if (snb[c.s] > c.qb) {
+            const uint32_t x = c.cnt + (uint32_t)c.hnext;
+            const uint32_t base = P.fd_2g.div(x) * G2;
+            const uint32_t r = x - base;
+            const uint32_t pos = r <= lo ? base + lo : (r <= hi ? base + hi : base + G2 + lo);
+            if (pos < c.cnt + (uint32_t)H) {
+                seq = c.s;
+                h = (int)(pos - c.cnt);
+                qb = c.qb;
+                c.hnext = h + 1;
+                return true;
+            }
+            c.cnt += (uint32_t)H;
+        }
+        c.hnext = 0;
+        ++c.s;
+    }
+    return false;
+}
+
+// Triangle item from its index (kv_lengths resolved), or packed item from
+// (sequence, head, q block) with its visited-tile count (warp-cooperative).
+template <bool VARLEN>
+__device__ __forceinline__ SItem split_decode(const TcParams& P, const int* sched, int item, int seq, int h, int qb) {
+    SItem it;
+    const AttnParams& a = P.a;
+    it.lists = false;
+    it.part_l = it.full_l = nullptr;
+    it.n_part = it.n_full = 0;
+    it.part0 = it.full0 = 0;
+    it.prefix = 0;
+    it.q_row0 = it.k_row0 = 0;
+    if constexpr (!VARLEN) {
+        const Item<1> t = decode<1, false>(P, item);
+        it.qt = t.qt[0];
+        it.unit = t.unit;
+        it.bn = t.bn;
+        it.b = t.b;
+        it.h = t.h;
+        it.seq = 0;
+        it.Lq = t.Lq;
+        it.Lk = t.Lk;
+        it.prefix = t.prefix;
+        it.nkb = t.nkb;
+        it.nkt = t.any ? t.nkb : 0;
+    } else {
+        const int S = a.num_seqs;
+        const int* scq = sched;
+        const int* sck = sched + S + 1;
+        it.qt = qb;
+        it.unit = it.bn = 0;
+        it.b = 0;
+        it.h = h;
+        it.seq = seq;
+        it.q_row0 = scq[seq];
+        it.Lq = scq[seq + 1] - it.q_row0;
+        it.k_row0 = sck[seq];
+        it.Lk = sck[seq + 1] - it.k_row0;
+        it.nkb = (it.Lk + kBN - 1) / kBN;
+        if (a.kv_num != nullptr) {
+            it.lists = true;
+            if (qb < a.MQ) {
+                const int hm = a.mask_heads == 1 ? 0 : h;
+                const long long row = ((long long)seq * a.mask_heads + hm) * a.MQ + qb;
+                it.part_l = a.kv_idx + row * a.MK;
+                it.n_part = min(max(a.kv_num[row], 0), a.MK);
+                if (a.full_num) {
+                    it.full_l = a.full_idx + row * a.MK;
+                    it.n_full = min(max(a.full_num[row], 0), a.MK);
+                }
+            }
+        }
+        split_window(it, 0, it.part0, it.full0);
+        int nkt = __popcll(it.part0 | it.full0);
+        for (int w = 1; 64 * w < it.nkb; ++w) {
+            uint64_t pm, fm;
+            split_window(it, w, pm, fm);
+            nkt += __popcll(pm | fm);
+        }
+        it.nkt = nkt;
+    }
+    return it;
+}
+
+// The key tiles of one item in ascending order: kb and whether mask_mod is
+// skipped on it (a full block).
+struct TileWalk {
+    int w, t;
+    uint64_t rem, full;
+};
+
+template <bool VARLEN>
+__device__ __forceinline__ TileWalk tiles_begin(const SItem& it) {
+    TileWalk tw;
+    tw.w = 0;
+    tw.t = 0;
+    tw.rem = VARLEN ? (it.part0 | it.full0) : 0ull;
+    tw.full = VARLEN ? it.full0 : 0ull;
+    return tw;
+}
+
+template <bool VARLEN>
+__device__ __forceinline__ bool tiles_next(const SItem& it, TileWalk& tw, int& kb, bool& is_full) {
+    if constexpr (!VARLEN) {
+        if (tw.t >= it.nkt) return false;
+        kb = tw.t++;
+        is_full = false;
+        return true;
+    } else {
+        while (tw.rem == 0) {
+            ++tw.w;
+            if (64 * tw.w >= it.nkb) return false;
+            uint64_t pm, fm;
+            split_window(it, tw.w, pm, fm);
+            tw.rem = pm | fm;
+            tw.full = fm;
+        }
+        const int bit = __ffsll((long long)tw.rem) - 1;
+        tw.rem &= tw.rem - 1;
+        kb = 64 * tw.w + bit;
+        is_full = (tw.full >> bit) & 1ull;
+        ++tw.t;
+        return true;
+    }
+}
+
+// A role's walk over this CTA's items (all of them, also those without key
+// tiles).
+template <bool VARLEN>
+struct ItemWalk {
+    int item;      // triangle: item index
+    VCursor vc;    // packed form
+    __device__ __forceinline__ void begin(const TcParams& P) {
+        item = (int)blockIdx.x;
+        if constexpr (VARLEN) vc = vcursor_begin(P);
+    }
+    __device__ __forceinline__ bool next(const TcParams& P, const int* sched, SItem& it) {
+        if constexpr (!VARLEN) {
+            if (item >= P.items) return false;
+            it = split_decode<false>(P, sched, item, 0, 0, 0);
+            item += gridDim.x;
+            return true;
+        } else {
+            int seq, h, qb;
+            if (!vcursor_next(P, sched + 2 * (P.a.num_seqs + 1), vc, seq, h, qb)) return false;
+            it = split_decode<true>(P, sched, 0, seq, h, qb);
+            return true;
+        }
+    }
+};
+
+// A position in the CTA's stream of key tiles (MMA warp): the current item
+// with key tiles, its tile count, the next tile in it and the item's number
+// among the CTA's items with key tiles.
+template <bool VARLEN>
 struct SplitCursor {
-    int item;
+    ItemWalk<VARLEN> walk;
     int nkt;
     int t;
     uint32_t qi;
 };
 
-// Moves c.item forward (by the grid stride) to the next item with work.
-__device__ __forceinline__ bool split_seek(const TcParams& P, SplitCursor& c) {
-    for (; c.item < P.items; c.item += gridDim.x) {
-        const Item<1> it = decode<1, false>(P, c.item);
-        if (it.any) {
-            c.nkt = it.nkb;
+// Moves the cursor to the next item with key tiles.
+template <bool VARLEN>
+__device__ __forceinline__ bool split_seek(const TcParams& P, const int* sched, SplitCursor<VARLEN>& c) {
+    SItem it;
+    while (c.walk.next(P, sched, it)) {
+        if (it.nkt > 0) {
+            c.nkt = it.nkt;
             c.t = 0;
             return true;
         }
@@ -85,7 +329,7 @@ __device__ __forceinline__ bool split_seek(const TcParams& P, SplitCursor& c) {
     return false;
 }
 
-template <bool BF16, bool BIAS_F32>
+template <bool BF16, bool BIAS_F32, bool VARLEN, bool FOLD>
 __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid_constant__ TcParams P) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -102,10 +346,12 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
     const AttnParams& a = P.a;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L.abort_flag);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L.tmem_slot);
+    int* sched = reinterpret_cast<int*>(gbase + L.sched);
 
     const int S = P.kv_stages;
     const int BS = P.bias_stages;
     const int QB = P.q_bufs;
+    const int SB = P.s_bufs;
     auto bar = [&](int idx) -> uint32_t { return base + L.bars + 8u * (uint32_t)idx; };
     auto q_full = [&](int qb) { return bar(qb); };
     auto q_empty = [&](int qb) { return bar(QB + qb); };
@@ -117,16 +363,35 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
     auto bias_empty = [&](int s) { return bar(2 * QB + 4 * S + BS + s); };
     const int bx0 = 2 * QB + 4 * S + 2 * BS;
     auto s_full = [&](int b) { return bar(bx0 + b); };
-    auto p_full = [&](int b) { return bar(bx0 + 3 + b); };
-    auto pv_done = [&](uint32_t n) { return bar(bx0 + 6 + (int)(n & 1u)); };  // PV n: phase n / 2 of barrier n % 2
-    auto xchg = [&](int q) { return bar(bx0 + 8 + q); };
-    const uint32_t drain = bar(bx0 + 12);
+    auto p_full = [&](int b) { return bar(bx0 + SB + b); };
+    auto pv_done = [&](uint32_t n) { return bar(bx0 + 2 * SB + (int)(n & 1u)); };  // PV n: phase n / 2 of barrier n % 2
+    auto xchg = [&](int q) { return bar(bx0 + 2 * SB + 2 + q); };
+    const uint32_t drain = bar(bx0 + 2 * SB + 6);
 
     auto q_smem = [&](int qb) { return base + L.q + (uint32_t)qb * P.tile_bytes; };
     auto k_smem = [&](int s) { return base + L.kv + (uint32_t)s * 2u * P.tile_bytes; };
     auto v_smem = [&](int s) { return base + L.kv + (uint32_t)s * 2u * P.tile_bytes + P.tile_bytes; };
     auto bias_smem = [&](int s) { return base + L.bias + (uint32_t)s * P.bias_bytes; };
 
+    if constexpr (VARLEN) {
+        // Sequence offsets and q block counts, read once.  A sequence that
+        // breaks the max_seqlen / total contract gets no q blocks (skipped)
+        // and TA_ERR_DEVICE is recorded.
+        const int NS = a.num_seqs;
+        for (int i = threadIdx.x; i <= NS; i += blockDim.x) {
+            sched[i] = a.cu_q[i];
+            sched[NS + 1 + i] = a.cu_k[i];
+        }
+        __syncthreads();
+        for (int s = threadIdx.x; s < NS; s += blockDim.x) {
+            const int cq0 = sched[s], cq1 = sched[s + 1];
+            const int ck0 = sched[NS + 1 + s], ck1 = sched[NS + 2 + s];
+            const bool ok = cq0 >= 0 && ck0 >= 0 && cq1 >= cq0 && ck1 >= ck0 && cq1 - cq0 <= a.max_q &&
+                            ck1 - ck0 <= a.max_k && cq1 <= a.total_q && ck1 <= a.total_k;
+            sched[2 * (NS + 1) + s] = ok ? (cq1 - cq0 + kBM - 1) / kBM : 0;
+            if (!ok && blockIdx.x == 0) atomicCAS(a.status, 0, kStatusDevice);
+        }
+    }
     if (threadIdx.x == 0) {
         *abort_flag = 0;
 #pragma unroll 1
@@ -146,7 +411,8 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
             mbar_init(bias_full(s), 1);
             mbar_init(bias_empty(s), 8);  // one arrival per softmax warp
         }
-        for (int b = 0; b < 3; ++b) {
+#pragma unroll 1
+        for (int b = 0; b < SB; ++b) {
             mbar_init(s_full(b), 1);
             mbar_init(p_full(b), 8);  // one arrival per softmax warp
         }
@@ -172,28 +438,43 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
         // ---------------------------------------------------- producer: Q, K tiles
         StageRing kr = {0, 0u, false}, qr = {0, 0u, false};
         bool ok = true;
-        for (int item = blockIdx.x; item < P.items && ok; item += gridDim.x) {
-            const Item<1> it = decode<1, false>(P, item);
-            if (!it.any) continue;
+        ItemWalk<VARLEN> walk;
+        walk.begin(P);
+        SItem it;
+        while (ok && walk.next(P, sched, it)) {
+            if (it.nkt == 0) continue;
             const int qb = qr.idx;
             if (lane == 0 && qr.wrapped) ok = wait_bar(q_empty(qb), qr.ph ^ 1u, abort_flag, a.status);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             if (lane == 0) {
                 mbar_expect_tx(q_full(qb), P.tile_bytes);
-                for (int sb = 0; sb < P.nsub; ++sb)
-                    tma_load_3d(q_smem(qb) + sb * kBox, &P.tm_q, sb * 64, it.qt[0] * kBM, (int)it.unit, q_full(qb));
+                for (int sb = 0; sb < P.nsub; ++sb) {
+                    if constexpr (!VARLEN)
+                        tma_load_3d(q_smem(qb) + sb * kBox, &P.tm_q, sb * 64, it.qt * kBM, (int)it.unit, q_full(qb));
+                    else
+                        tma_load_3d(q_smem(qb) + sb * kBox, &P.tm_q, sb * 64, it.h, it.q_row0 + it.qt * kBM,
+                                    q_full(qb));
+                }
             }
             qr.next(QB);
-            for (int kb = 0; kb < it.nkb && ok; ++kb) {
+            TileWalk tw = tiles_begin<VARLEN>(it);
+            int kb;
+            bool fb;
+            while (ok && tiles_next<VARLEN>(it, tw, kb, fb)) {
                 const int st = kr.idx;
                 if (lane == 0 && kr.wrapped) ok = wait_bar(k_empty(st), kr.ph ^ 1u, abort_flag, a.status);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) break;
                 if (lane == 0) {
                     mbar_expect_tx(k_full(st), P.tile_bytes);
-                    for (int sb = 0; sb < P.nsub; ++sb)
-                        tma_load_3d(k_smem(st) + sb * kBox, &P.tm_k, sb * 64, kb * kBN, (int)it.unit, k_full(st));
+                    for (int sb = 0; sb < P.nsub; ++sb) {
+                        if constexpr (!VARLEN)
+                            tma_load_3d(k_smem(st) + sb * kBox, &P.tm_k, sb * 64, kb * kBN, (int)it.unit, k_full(st));
+                        else
+                            tma_load_3d(k_smem(st) + sb * kBox, &P.tm_k, sb * 64, it.h, it.k_row0 + kb * kBN,
+                                        k_full(st));
+                    }
                 }
                 kr.next(S);
             }
@@ -203,67 +484,78 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
         // ---------------------------------------------------------- producer: V tiles
         StageRing vr = {0, 0u, false};
         bool ok = true;
-        for (int item = blockIdx.x; item < P.items && ok; item += gridDim.x) {
-            const Item<1> it = decode<1, false>(P, item);
-            if (!it.any) continue;
-            for (int kb = 0; kb < it.nkb && ok; ++kb) {
+        ItemWalk<VARLEN> walk;
+        walk.begin(P);
+        SItem it;
+        while (ok && walk.next(P, sched, it)) {
+            TileWalk tw = tiles_begin<VARLEN>(it);
+            int kb;
+            bool fb;
+            while (ok && tiles_next<VARLEN>(it, tw, kb, fb)) {
                 const int st = vr.idx;
                 if (lane == 0 && vr.wrapped) ok = wait_bar(v_empty(st), vr.ph ^ 1u, abort_flag, a.status);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) break;
                 if (lane == 0) {
                     mbar_expect_tx(v_full(st), P.tile_bytes);
-                    for (int sb = 0; sb < P.nsub; ++sb)
-                        tma_load_3d(v_smem(st) + sb * kBox, &P.tm_v, sb * 64, kb * kBN, (int)it.unit, v_full(st));
+                    for (int sb = 0; sb < P.nsub; ++sb) {
+                        if constexpr (!VARLEN)
+                            tma_load_3d(v_smem(st) + sb * kBox, &P.tm_v, sb * 64, kb * kBN, (int)it.unit, v_full(st));
+                        else
+                            tma_load_3d(v_smem(st) + sb * kBox, &P.tm_v, sb * 64, it.h, it.k_row0 + kb * kBN,
+                                        v_full(st));
+                    }
                 }
                 vr.next(S);
             }
         }
         if (!ok) *abort_flag = 1;
     } else if (warp == kBiasWarp) {
-        // ---------------------------------- producer: bias tiles (+ dense-mask bits)
-        StageRing br = {0, 0u, false};
-        bool ok = true;
-        for (int item = blockIdx.x; item < P.items && ok; item += gridDim.x) {
-            const Item<1> it = decode<1, false>(P, item);
-            if (!it.any) continue;
-            for (int kb = 0; kb < it.nkb && ok; ++kb) {
-                const int bs = br.idx;
-                if (lane == 0 && br.wrapped) ok = wait_bar(bias_empty(bs), br.ph ^ 1u, abort_flag, a.status);
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) break;
-                if (P.mask_kind == 2) {
-                    // 128 key-validity bits: word w, bit l <-> key kb*128 + 32w + l
-                    uint32_t* mw = reinterpret_cast<uint32_t*>(gbase + L.maskw + (uint32_t)bs * 16u);
-                    for (int ww = 0; ww < 4; ++ww) {
-                        const int key = kb * kBN + 32 * ww + lane;
-                        const bool v = key < a.K && a.mask[it.bn * a.K + key] != 0;
-                        const uint32_t word = __ballot_sync(0xffffffffu, v);
-                        if (lane == ww) mw[ww] = word;
+        if constexpr (!VARLEN) {
+            // ---------------------------------- producer: bias tiles (+ dense-mask bits)
+            StageRing br = {0, 0u, false};
+            bool ok = true;
+            for (int item = blockIdx.x; item < P.items && ok; item += gridDim.x) {
+                const Item<1> it = decode<1, false>(P, item);
+                if (!it.any) continue;
+                for (int kb = 0; kb < it.nkb && ok; ++kb) {
+                    const int bs = br.idx;
+                    if (lane == 0 && br.wrapped) ok = wait_bar(bias_empty(bs), br.ph ^ 1u, abort_flag, a.status);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) break;
+                    if (P.mask_kind == 2) {
+                        // 128 key-validity bits: word w, bit l <-> key kb*128 + 32w + l
+                        uint32_t* mw = reinterpret_cast<uint32_t*>(gbase + L.maskw + (uint32_t)bs * 16u);
+                        for (int ww = 0; ww < 4; ++ww) {
+                            const int key = kb * kBN + 32 * ww + lane;
+                            const bool v = key < a.K && a.mask[it.bn * a.K + key] != 0;
+                            const uint32_t word = __ballot_sync(0xffffffffu, v);
+                            if (lane == ww) mw[ww] = word;
+                        }
+                        __syncwarp();
                     }
-                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_expect_tx(bias_full(bs), P.bias_bytes);
+                        for (int bx = 0; bx < P.bias_boxes; ++bx)
+                            tma_load_3d(bias_smem(bs) + bx * kBox, &P.tm_bias, kb * kBN + bx * P.bias_box_cols,
+                                        it.qt[0] * kBM, it.b * a.H + it.h, bias_full(bs));
+                    }
+                    br.next(BS);
                 }
-                if (lane == 0) {
-                    mbar_expect_tx(bias_full(bs), P.bias_bytes);
-                    for (int bx = 0; bx < P.bias_boxes; ++bx)
-                        tma_load_3d(bias_smem(bs) + bx * kBox, &P.tm_bias, kb * kBN + bx * P.bias_box_cols,
-                                    it.qt[0] * kBM, it.b * a.H + it.h, bias_full(bs));
-                }
-                br.next(BS);
             }
+            if (!ok) *abort_flag = 1;
         }
-        if (!ok) *abort_flag = 1;
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------------ MMA
-        // Two cursors over the CTA's items with work: `qc` for the next QK^T,
-        // `pc` for the next PV.  Tile n of the stream (counted over items) has
-        // S buffer n % 3 and K/V stage n % S; item number i has Q buffer i % QB
-        // and O accumulator i % 2.
+        // Two cursors over the CTA's items with key tiles: `qc` for the next
+        // QK^T, `pc` for the next PV.  Tile n of the stream (counted over
+        // items) has S buffer n % s_bufs and K/V stage n % S; item number i
+        // has Q buffer i % QB and O accumulator i % 2.
         const bool leader = elect_one();
-        SplitCursor qc, pc;
-        qc.item = blockIdx.x;
+        SplitCursor<VARLEN> qc, pc;
+        qc.walk.begin(P);
         qc.qi = 0;
-        bool has_q = split_seek(P, qc);
+        bool has_q = split_seek<VARLEN>(P, sched, qc);
         pc = qc;
         bool has_p = has_q;
         uint32_t np = 0;                                    // PV issued so far
@@ -290,17 +582,16 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
                 mma_commit(k_empty(st));
             }
             kq.next(S);
-            sq.next(3);
+            sq.next(SB);
             if (++qc.t == qc.nkt) {
                 if (leader) mma_commit(q_empty(qb));  // every QK^T of the item is issued
                 qr.next(QB);
                 ++qc.qi;
-                qc.item += gridDim.x;
-                has_q = split_seek(P, qc);
+                has_q = split_seek<VARLEN>(P, sched, qc);
             }
             return true;
         };
-        for (int i = 0; i < 3 && ok; ++i) ok = issue_qk();
+        for (int i = 0; i < SB && ok; ++i) ok = issue_qk();
         while (ok && has_p) {
             const int b = sp.idx;
             const int st = vp.idx;
@@ -323,14 +614,13 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
                 mma_commit(v_empty(st));
             }
             ++np;
-            sp.next(3);
+            sp.next(SB);
             vp.next(S);
             if (++pc.t == pc.nkt) {
                 ++pc.qi;
-                pc.item += gridDim.x;
-                has_p = split_seek(P, pc);
+                has_p = split_seek<VARLEN>(P, sched, pc);
             }
-            // The buffer just multiplied by V takes the S three tiles on.
+            // The buffer just multiplied by V takes the S s_bufs tiles on.
             ok = issue_qk();
         }
         if (!ok && leader) *abort_flag = 1;
@@ -348,9 +638,13 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
         const uint32_t rsw = (uint32_t)(r & 7);  // 128B swizzle: chunk c of row r sits at chunk c ^ (r % 8)
         const uint32_t rrow = (uint32_t)r * 128u;
         uint32_t sn = 0, x_it = 0;  // sn: key tiles so far (the PV index)
-        int sb = 0, sph = 0;        // sn % 3 and (sn / 3) & 1: S buffer and its phase
+        int sb = 0, sph = 0;        // sn % s_bufs and (sn / s_bufs) & 1: S buffer and its phase
         StageRing br = {0, 0u, false};
         const float2 scale2 = make_float2(a.scale, a.scale);
+        // Folded form (packed sequences, scale > 0): values are in units of S
+        // (x = s S); a masked key holds -FLT_MAX there (its logit is -1e9).
+        constexpr float kMaskVal = FOLD ? -FLT_MAX : kMasked;
+        const float unit_l2e = FOLD ? P.scale_log2e : kLog2e;
         float* xbuf = reinterpret_cast<float*>(gbase + L.xbuf);
         float* xl = reinterpret_cast<float*>(gbase + L.xl);
         bool ok = true;
@@ -376,9 +670,9 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
         // so a parity wait is exact while that barrier is neither a phase ahead
         // (PV n + 2 done) nor behind (PV n - 2 not done).  The callers hold:
         // this warp has not given P of tile n + 2, and PV n - 2 finished
-        // before the S it last read (S of tile m is issued after PV m - 3).
-        // With `prev`, PV n - 1 is waited for first, which covers a caller
-        // that only knows PV n - 3 finished.
+        // before the S it last read (S of tile m is issued after PV m - s_bufs,
+        // s_bufs <= 3).  With `prev`, PV n - 1 is waited for first, which
+        // covers a caller that only knows PV n - 3 finished.
         auto wait_pv = [&](uint32_t n, bool prev) -> bool {
             if (prev && n > 0 &&
                 !__all_sync(0xffffffffu, wait_bar(pv_done(n - 1u), ((n - 1u) >> 1) & 1, abort_flag, a.status)))
@@ -388,15 +682,70 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
             return true;
         };
 
+        // Mean of V over `nkeys` keys for the rows of this warp that need it
+        // (lane l forms the means of columns l, l + 32, ...; rows take them by
+        // shuffles), or zeros when there are no keys.
+        auto write_mean_v = [&](uint16_t* orow_p, long long v_base, long long v_stride, int nkeys, bool mine) {
+#pragma unroll 1
+            for (int d0 = 0; d0 < a.D; d0 += 32) {
+                const int d = d0 + lane;
+                float sum[4] = {0.f, 0.f, 0.f, 0.f};
+                if (d < a.D) {
+                    int key = 0;
+#pragma unroll 1
+                    for (; key + 4 <= nkeys; key += 4) {
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) sum[u] += load16<BF16>(a.v, v_base + (key + u) * v_stride + d);
+                    }
+#pragma unroll 1
+                    for (; key < nkeys; ++key) sum[0] += load16<BF16>(a.v, v_base + key * v_stride + d);
+                }
+                const float mv = nkeys > 0 ? ((sum[0] + sum[1]) + (sum[2] + sum[3])) / (float)nkeys : 0.f;
+#pragma unroll 1
+                for (int e = 0; e < 32 && d0 + e < a.D; ++e) {
+                    const float m = __shfl_sync(0xffffffffu, mv, e);
+                    if (mine) orow_p[d0 + e] = (uint16_t)(pack2<BF16>(m, 0.f) & 0xffffu);
+                }
+            }
+        };
+
         // The epilogue of the previous item, run after the first tile of the
         // next one (or at the end).  A row with no valid key has every logit
-        // -1e9; every key tile was then visited with unit weights and O / l is
-        // the mean of V.  A row whose valid keys all have logits at or below
-        // -1e9 (only with a bias of that size) visited only the prefix tiles:
-        // the h == 0 warp forms the mean of V over all keys for it directly.
+        // -1e9; when every key block was visited (with unit weights) O / l is
+        // the mean of V.  A row whose visited keys were all masked while some
+        // blocks were not visited (packed form: blocks its lists leave out;
+        // triangle form: only with a bias at or below -1e9) gets the mean of V
+        // over all keys, formed directly by the h == 0 warp.
+        // Where a row's outputs go: (out element offset, lse/max index, V's first
+        // element, V's key stride, keys).  Triangle form: row0 = the flat
+        // (b,n,h,q) row, unit0 = the (b,n,h) slab; packed form: row0 = the
+        // packed query row, unit0 = the sequence's first key row, hh = the head,
+        // nk = its keys.
+        struct RowAddr {
+            long long out_off, lse_idx, v_base, v_stride;
+            int nkeys;
+        };
+        auto row_addr = [&](long long row0, long long unit0, int hh, int nk) -> RowAddr {
+            RowAddr ra;
+            if constexpr (!VARLEN) {
+                ra.out_off = row0 * a.D;
+                ra.lse_idx = row0;
+                ra.v_base = unit0 * a.K * a.D;
+                ra.v_stride = a.D;
+                ra.nkeys = a.K;
+            } else {
+                ra.out_off = (row0 * a.H + hh) * a.D;
+                ra.lse_idx = (long long)hh * a.total_q + row0;
+                ra.v_base = unit0 * a.v_rs + (long long)hh * a.D;
+                ra.v_stride = a.v_rs;
+                ra.nkeys = nk;
+            }
+            return ra;
+        };
         struct Pending {
             float m_ref, l, m_true;
-            long long orow, unit;
+            long long row0, unit0;
+            int hh, nk;
             uint32_t n_last, ob;
             bool row_ok, direct;
         } pe = {};
@@ -404,30 +753,36 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
         auto epilogue = [&](bool at_end) -> bool {
             const float l_all = pe.l + swap(xl, pe.l);
             if (!ok) return false;
+            const RowAddr ra = row_addr(pe.row0, pe.unit0, pe.hh, pe.nk);
             if (pe.row_ok && h == 0) {
-                const float lse = pe.direct ? kMasked + logf((float)a.K) : pe.m_ref + logf(l_all);
-                if (a.lse) a.lse[pe.orow] = lse;
-                if (a.mx) a.mx[pe.orow] = pe.direct ? kMasked : pe.m_true;
+                float mr = pe.m_ref;
+                if constexpr (FOLD) mr = pe.m_ref > -FLT_MAX ? pe.m_ref * a.scale : kMasked;
+                const float lse = pe.direct ? kMasked + logf((float)ra.nkeys) : mr + logf(l_all);
+                if (a.lse) a.lse[ra.lse_idx] = lse;
+                if (a.mx) a.mx[ra.lse_idx] = pe.direct ? kMasked : pe.m_true;
             }
             if (!wait_pv(pe.n_last, at_end)) return false;
             const uint32_t oa = o_base + pe.ob * P.o_cols;
-            uint16_t* orow_p = static_cast<uint16_t*>(a.out) + pe.orow * a.D;
+            uint16_t* orow_p = static_cast<uint16_t*>(a.out) + ra.out_off;
             uint16_t* op = orow_p + (long long)h * half_o;
             const float inv = l_all > 0.f ? 1.f / l_all : 0.f;
             const int dlim = a.D - h * (int)half_o;  // columns of this half that exist
-            if (half_o == 32) {  // D in (48, 64]: this warp's 32 columns in one load
-                uint32_t o[32];
-                tmem_ld_x32(oa, o);
-                uint32_t wv[16];
+            if (half_o % 32 == 0) {  // 32 of this warp's columns per load
+#pragma unroll 1
+                for (uint32_t c0 = 0; c0 < half_o; c0 += 32) {
+                    uint32_t o[32];
+                    tmem_ld_x32(oa + c0, o);
+                    uint32_t wv[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    wv[e] = pack2<BF16>(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
-                if (pe.row_ok && !pe.direct) {
+                    for (int e = 0; e < 16; ++e)
+                        wv[e] = pack2<BF16>(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+                    if (pe.row_ok && !pe.direct) {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        if (8 * i < dlim)
-                            reinterpret_cast<uint4*>(op)[i] =
-                                make_uint4(wv[4 * i], wv[4 * i + 1], wv[4 * i + 2], wv[4 * i + 3]);
+                        for (int i = 0; i < 4; ++i)
+                            if ((int)c0 + 8 * i < dlim)
+                                reinterpret_cast<uint4*>(op + c0)[i] =
+                                    make_uint4(wv[4 * i], wv[4 * i + 1], wv[4 * i + 2], wv[4 * i + 3]);
+                    }
                 }
             } else {
 #pragma unroll 1
@@ -442,69 +797,94 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
                         *reinterpret_cast<uint4*>(op + c0) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
                 }
             }
-            if (h == 0 && __any_sync(0xffffffffu, pe.direct && pe.row_ok)) {
-                // Lane l forms the means of columns l and l + 32; rows take them by shuffles.
-#pragma unroll 1
-                for (int d0 = 0; d0 < a.D; d0 += 32) {
-                    const int d = d0 + lane;
-                    float sum[4] = {0.f, 0.f, 0.f, 0.f};
-                    if (d < a.D) {
-                        const long long vrow0 = pe.unit * a.K;
-                        int key = 0;
-#pragma unroll 1
-                        for (; key + 4 <= a.K; key += 4) {
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) sum[u] += load16<BF16>(a.v, (vrow0 + key + u) * a.D + d);
-                        }
-#pragma unroll 1
-                        for (; key < a.K; ++key) sum[0] += load16<BF16>(a.v, (vrow0 + key) * a.D + d);
-                    }
-                    const float mv = ((sum[0] + sum[1]) + (sum[2] + sum[3])) / (float)a.K;
-#pragma unroll 1
-                    for (int e = 0; e < 32 && d0 + e < a.D; ++e) {
-                        const float m = __shfl_sync(0xffffffffu, mv, e);
-                        if (pe.row_ok && pe.direct) orow_p[d0 + e] = (uint16_t)(pack2<BF16>(m, 0.f) & 0xffffu);
-                    }
-                }
-            }
+            if (h == 0 && __any_sync(0xffffffffu, pe.direct && pe.row_ok))
+                write_mean_v(orow_p, ra.v_base, ra.v_stride, ra.nkeys, pe.direct && pe.row_ok);
             return true;
         };
 
-        uint32_t qi = 0;  // items with work so far: O accumulator qi % 2
-        for (int item = blockIdx.x; item < P.items && ok; item += gridDim.x) {
-            const Item<1> it = decode<1, false>(P, item);
-            if (!it.any) continue;
+        uint32_t qi = 0;  // items with key tiles so far: O accumulator qi % 2
+        ItemWalk<VARLEN> walk;
+        walk.begin(P);
+        SItem it;
+        while (ok && walk.next(P, sched, it)) {
+            const int qrow = it.qt * kBM + r;  // local query row
+            const bool row_ok = qrow < it.Lq;
+            if (it.nkt == 0) {
+                // Packed form, a q block that visits no key block: every logit is
+                // -1e9 (mean of V over the sequence's keys), or there are no keys
+                // (O = 0, lse = max = -inf).
+                if (h == 0) {
+                    const RowAddr ra = row_addr((long long)it.q_row0 + qrow, it.k_row0, it.h, it.Lk);
+                    if (row_ok) {
+                        if (a.lse) a.lse[ra.lse_idx] = ra.nkeys > 0 ? kMasked + logf((float)ra.nkeys) : -INFINITY;
+                        if (a.mx) a.mx[ra.lse_idx] = ra.nkeys > 0 ? kMasked : -INFINITY;
+                    }
+                    if (__any_sync(0xffffffffu, row_ok))
+                        write_mean_v(static_cast<uint16_t*>(a.out) + ra.out_off, ra.v_base, ra.v_stride, ra.nkeys,
+                                     row_ok);
+                }
+                continue;
+            }
             const uint32_t ob = qi & 1u;
             ++qi;
             const uint32_t o_taddr = o_base + ob * P.o_cols;
-            const int qrow = it.qt[0] * kBM + r;
             float m_true = -INFINITY, m_ref = 0.f, l = 0.f;
             int jv = 0;
-            for (int kb = 0; kb < it.nkb && ok; ++kb) {
+            const int prefix_lm = !VARLEN ? 0 : (a.prefix_len ? a.prefix_len[it.seq] : a.prefix_all);
+            TileWalk tw = tiles_begin<VARLEN>(it);
+            int kb;
+            bool is_full;
+            while (ok && tiles_next<VARLEN>(it, tw, kb, is_full)) {
                 const int key0 = kb * kBN;
-                const int vlim = P.mask_kind == 1 ? it.prefix : a.K;
-                const bool all_valid = P.mask_kind != 2 && key0 + kBN <= vlim;
-                const int nexist = a.K - key0;
-                const int bs = br.idx;
-                // Both barriers tested at once; the bounded waits only when one is not ready.
-                const bool ready = mbar_test(bias_full(bs), br.ph) & mbar_test(s_full(sb), (uint32_t)sph);
-                if (!__all_sync(0xffffffffu, ready)) {
-                    ok = __all_sync(0xffffffffu, wait_bar(bias_full(bs), br.ph, abort_flag, a.status));
-                    if (!ok) break;
+                int vlim;
+                bool modded = false;  // mask_mod applies (a partial block)
+                if constexpr (!VARLEN) {
+                    vlim = P.mask_kind == 1 ? it.prefix : a.K;
+                } else {
+                    vlim = it.Lk;
+                    modded = !is_full && a.mask_mod != TA_MASK_NONE;
+                }
+                const bool all_valid = (VARLEN || P.mask_kind != 2) && key0 + kBN <= vlim &&
+                                       (!modded || mod_tile_all(a.mask_mod, it.qt * kBM, key0, a.window, prefix_lm));
+                const int nexist = (VARLEN ? it.Lk : a.K) - key0;
+                int bs = 0;
+                uint32_t boff = 0, mwoff = 0;
+                if constexpr (!VARLEN) {
+                    bs = br.idx;
+                    // Both barriers tested at once; the bounded waits only when one is not ready.
+                    const bool ready = mbar_test(bias_full(bs), br.ph) & mbar_test(s_full(sb), (uint32_t)sph);
+                    if (!__all_sync(0xffffffffu, ready)) {
+                        ok = __all_sync(0xffffffffu, wait_bar(bias_full(bs), br.ph, abort_flag, a.status));
+                        if (!ok) break;
+                        ok = __all_sync(0xffffffffu, wait_bar(s_full(sb), (uint32_t)sph, abort_flag, a.status));
+                        if (!ok) break;
+                    }
+                    boff = bias_smem(bs) - base + rrow;
+                    mwoff = L.maskw + (uint32_t)bs * 16u;
+                } else {
                     ok = __all_sync(0xffffffffu, wait_bar(s_full(sb), (uint32_t)sph, abort_flag, a.status));
                     if (!ok) break;
                 }
-                const uint32_t boff = bias_smem(bs) - base + rrow;
-                const uint32_t mwoff = L.maskw + (uint32_t)bs * 16u;
                 const uint32_t s_taddr = tmem + lane_off + 128u * (uint32_t)sb;
                 tc_fence_after();
 
-                // ---- x: this warp's 64 values of the row (logits).
+                // ---- x: this warp's 64 values of the row (logits, or raw S in the folded form).
                 float x[64];
                 {
                     uint32_t sr[64];
                     tmem_ld_x64(s_taddr + 64u * (uint32_t)h, sr);
-                    if constexpr (!BIAS_F32) {
+                    if constexpr (FOLD) {
+#pragma unroll
+                        for (int j = 0; j < 64; ++j) x[j] = __uint_as_float(sr[j]);
+                    } else if constexpr (VARLEN) {
+#pragma unroll
+                        for (int j = 0; j < 64; j += 2) {
+                            const float2 r2 =
+                                __fmul2_rn(make_float2(__uint_as_float(sr[j]), __uint_as_float(sr[j + 1])), scale2);
+                            x[j] = r2.x;
+                            x[j + 1] = r2.y;
+                        }
+                    } else if constexpr (!BIAS_F32) {
                         const uint32_t bbox = boff + (uint32_t)h * kBox;  // keys 64h .. 64h+63: box h
 #pragma unroll
                         for (int g = 0; g < 8; ++g) {
@@ -539,25 +919,32 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
                     }
                 }
                 // ---- Masking (boundary tiles only; uniform across the warp).
+                // Per 32 keys: vm bit j = key valid, em bit j = key exists.
                 if (!all_valid) {
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
                         const int k0 = 64 * h + 32 * hh;
                         const uint32_t em = low_bits(nexist - k0);
                         uint32_t vm = em & low_bits(vlim - key0 - k0);
-                        if (P.mask_kind == 2)
-                            vm &= *reinterpret_cast<const uint32_t*>(gbase + mwoff + 4u * (uint32_t)(2 * h + hh));
+                        if constexpr (!VARLEN) {
+                            if (P.mask_kind == 2)
+                                vm &= *reinterpret_cast<const uint32_t*>(gbase + mwoff + 4u * (uint32_t)(2 * h + hh));
+                        } else {
+                            if (modded) vm &= mod_bits(a.mask_mod, qrow, key0 + k0, a.window, prefix_lm);
+                        }
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
                             x[32 * hh + j] =
-                                ((vm >> j) & 1u) ? x[32 * hh + j] : (((em >> j) & 1u) ? kMasked : -INFINITY);
+                                ((vm >> j) & 1u) ? x[32 * hh + j] : (((em >> j) & 1u) ? kMaskVal : -INFINITY);
                     }
                 }
-                __syncwarp();  // every lane of the warp has read its bias and the mask words
-                if (lane == 0) mbar_arrive(bias_empty(bs));
-                br.next(BS);
+                if constexpr (!VARLEN) {
+                    __syncwarp();  // every lane of the warp has read its bias and the mask words
+                    if (lane == 0) mbar_arrive(bias_empty(bs));
+                    br.next(BS);
+                }
 
-                // ---- Row max of the tile: this half's, then the partner's.
+                // ---- Row max of the tile (units of this form): this half's, then the partner's.
                 float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
 #pragma unroll
                 for (int j = 0; j < 64; j += 8) {
@@ -569,20 +956,23 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
                 const float mh = fmaxf(max3(m0, m1, m2), m3);
                 const float tm = fmaxf(mh, swap(xbuf + (sn & 1u) * 256u, mh));
                 if (!ok) break;
-                m_true = fmaxf(m_true, tm);
+                float tm_nat;  // the tile max as a logit (natural units)
+                if constexpr (FOLD) tm_nat = tm > -FLT_MAX ? tm * a.scale : (tm == -FLT_MAX ? kMasked : -INFINITY);
+                else tm_nat = tm;
+                m_true = fmaxf(m_true, tm_nat);
                 if (jv == 0) {
                     m_ref = tm;
                     l = 0.f;
                 } else {
                     const float m_new = fmaxf(m_ref, tm);
-                    const bool need = (m_new - m_ref) * kLog2e > kRescaleLog2;
+                    const bool need = (m_new - m_ref) * unit_l2e > kRescaleLog2;
                     if (__any_sync(0xffffffffu, need)) {
                         // Both warps of the lane quarter take this branch for the same
                         // rows (same tm, same m_ref); each scales its O columns once
                         // O holds the previous tile.
                         ok = wait_pv(sn - 1u, false);
                         if (!ok) break;
-                        const float alpha = ex2((m_ref - m_new) * kLog2e);
+                        const float alpha = ex2((m_ref - m_new) * unit_l2e);
                         l *= alpha;
                         m_ref = m_new;
                         for (uint32_t c0 = 0; c0 < half_o; c0 += 8) {
@@ -596,10 +986,12 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
                 }
 
                 // ---- P for this warp's 64 keys into columns [32h, 32h + 32) of the
-                // buffer (after the swap, so the partner has read its logits).
-                const bool live = m_ref > kMasked;
-                const float2 ul2 = live ? make_float2(kLog2e, kLog2e) : make_float2(1.f, 1.f);
-                const float nb = live ? -m_ref * kLog2e : -kMasked;
+                // buffer (after the swap, so the partner has read its logits).  A row
+                // with no real logit yet takes weights of exactly 1 for masked keys
+                // and 0 for absent ones: x + (-kMaskVal) is then 0 or -inf.
+                const bool live = m_ref > kMaskVal;
+                const float2 ul2 = live ? make_float2(unit_l2e, unit_l2e) : make_float2(1.f, 1.f);
+                const float nb = live ? -m_ref * unit_l2e : -kMaskVal;
                 const float2 nb2 = make_float2(nb, nb);
                 float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
                 uint32_t pk[32];
@@ -616,9 +1008,17 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(p_full(sb));
+#ifdef TRIATTN_TEST_MISSING_ARRIVAL
+                // Test builds of the failure path only: softmax warp 0 of CTA 0 withholds
+                // its arrival for the first P, so the MMA warp's bounded wait for it runs
+                // out and the CTA takes the abort path (status TA_ERR_TIMEOUT).
+                const bool give = !(blockIdx.x == 0 && warp == 0 && sn == 0);
+#else
+                constexpr bool give = true;
+#endif
+                if (lane == 0 && give) mbar_arrive(p_full(sb));
                 ++sn;
-                if (++sb == 3) {
+                if (++sb == SB) {
                     sb = 0;
                     sph ^= 1;
                 }
@@ -631,12 +1031,20 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
             pe.m_ref = m_ref;
             pe.l = l;
             pe.m_true = m_true;
-            pe.orow = it.unit * a.Q + qrow;
-            pe.unit = it.unit;
+            if constexpr (!VARLEN) {
+                pe.row0 = it.unit * a.Q + qrow;
+                pe.unit0 = it.unit;
+            } else {
+                pe.row0 = (long long)it.q_row0 + qrow;
+                pe.unit0 = it.k_row0;
+                pe.hh = it.h;
+                pe.nk = it.Lk;
+            }
             pe.n_last = sn - 1u;
             pe.ob = ob;
-            pe.row_ok = qrow < it.Lq;
-            pe.direct = !(m_true > kMasked) && jv != (a.K + kBN - 1) / kBN;
+            pe.row_ok = row_ok;
+            // (triangle form: every key block of K; packed form: of the sequence)
+            pe.direct = !(m_true > kMasked) && jv != (VARLEN ? it.nkb : (a.K + kBN - 1) / kBN);
             pend = true;
         }
         if (ok && pend) ok = epilogue(true);
@@ -657,20 +1065,26 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
     }
 }
 
-template <bool BF16, bool BIAS_F32>
+template <bool BF16, bool BIAS_F32, bool VARLEN, bool FOLD>
 cudaError_t launch_split(const TcParams& P, int grid, cudaStream_t stream) {
     const SplitLayout L = make_split_layout(P);
     const size_t smem = L.total + 1024;
-    auto kern = tc_split_kernel<BF16, BIAS_F32>;
+    auto kern = tc_split_kernel<BF16, BIAS_F32, VARLEN, FOLD>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, kSplitThreads, smem, stream>>>(P);
     return cudaGetLastError();
 }
 
-#define TRIATTN_SPLIT_VARIANTS(X) X(true, false) X(true, true) X(false, false) X(false, true)
-#define TRIATTN_SPLIT_EXTERN(b, f) extern template cudaError_t launch_split<b, f>(const TcParams&, int, cudaStream_t);
-#define TRIATTN_SPLIT_INSTANTIATE(b, f) template cudaError_t launch_split<b, f>(const TcParams&, int, cudaStream_t);
+// Triangle form (bias dtype) and packed form (folded scale or not).
+#define TRIATTN_SPLIT_TRI_VARIANTS(X) X(true, false, false, false) X(true, true, false, false) \
+    X(false, false, false, false) X(false, true, false, false)
+#define TRIATTN_SPLIT_VARLEN_VARIANTS(X) X(true, false, true, true) X(true, false, true, false) \
+    X(false, false, true, true) X(false, false, true, false)
+#define TRIATTN_SPLIT_EXTERN(b, f, v, fo) \
+    extern template cudaError_t launch_split<b, f, v, fo>(const TcParams&, int, cudaStream_t);
+#define TRIATTN_SPLIT_INSTANTIATE(b, f, v, fo) \
+    template cudaError_t launch_split<b, f, v, fo>(const TcParams&, int, cudaStream_t);
 
 }  // namespace tc
 }  // namespace triattn

@@ -34,7 +34,7 @@ _lock = threading.Lock()
 _lib = None
 
 DT = {"f32": 0, "f16": 1, "bf16": 2}
-MASK_MOD = {"none": 0, "causal": 1}
+MASK_MOD = {"none": 0, "causal": 1, "sliding_window": 2, "prefix_lm": 3}
 
 
 def build(force: bool = False) -> str:
@@ -60,7 +60,7 @@ def _load():
                                            P, LL, P, P, P, I]
             lib.oracle_tri_fwd.restype = I
             lib.oracle_varlen_fwd.argtypes = [P, P, P, I, P, P, I, I, I, ctypes.c_double,
-                                              P, P, P, P, I, I, I, I, I, P, P, P, I]
+                                              P, P, P, P, I, I, I, I, I, I, P, I, P, P, P, I]
             lib.oracle_varlen_fwd.restype = I
             lib.oracle_mask_to_kv_lengths.argtypes = [P, LL, I, P, P]
             lib.oracle_mask_to_kv_lengths.restype = None
@@ -154,11 +154,14 @@ def mask_to_kv_lengths(mask):
 
 def varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, scale=None, kv_num_blocks=None, kv_indices=None,
                full_kv_num_blocks=None, full_kv_indices=None, block=128, mask_mod="none",
-               threads=None):
+               threads=None, window=0, prefix_lengths=None):
     """Packed-sequence forward in fp64 with a BlockMask.
 
     q (total_q,H,D), k/v (total_k,H,D); cu_seqlens (S+1,) int.  Block lists are
     (S, mask_heads, MQ) / (S, mask_heads, MQ, MK) int, sequence-local.
+    mask_mod on partial blocks: "none", "causal" (k <= q), "sliding_window"
+    (q - window < k <= q) or "prefix_lm" (k <= q or k < the sequence's prefix
+    length; prefix_lengths is an int or one int per sequence).
     Returns numpy (O (total_q,H,D), lse (H,total_q), max (H,total_q)).
     """
     lib = _load()
@@ -179,12 +182,19 @@ def varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, scale=None, kv_num_blocks=No
     if kn is not None:
         mask_heads, MQ = kn.shape[1], kn.shape[2]
         MK = ki.shape[3]
+    pl, p_all = None, 0
+    if prefix_lengths is not None:
+        if isinstance(prefix_lengths, int):
+            p_all = prefix_lengths
+        else:
+            pl = torch.as_tensor(prefix_lengths).to(torch.int32).contiguous()
     out = np.zeros((total_q, H, D), np.float64)
     lse = np.zeros((H, total_q), np.float64)
     mx = np.zeros((H, total_q), np.float64)
     rc = lib.oracle_varlen_fwd(_ptr(q), _ptr(k), _ptr(v), DT[_dtname(q)], _ptr(cq), _ptr(ck), S, H, D, s,
                                _ptr(kn), _ptr(ki), _ptr(fn), _ptr(fi), mask_heads, MQ, MK, block,
-                               MASK_MOD[mask_mod], out.ctypes.data_as(ctypes.c_void_p),
+                               MASK_MOD[mask_mod], int(window), _ptr(pl), int(p_all),
+                               out.ctypes.data_as(ctypes.c_void_p),
                                lse.ctypes.data_as(ctypes.c_void_p), mx.ctypes.data_as(ctypes.c_void_p),
                                int(threads or default_threads()))
     if rc != 0:

@@ -28,7 +28,9 @@
  *     loop (set semantics, entries past the count ignored, out-of-range block
  *     indices ignored);
  *   - a block from the full list is valid everywhere; a block from the partial
- *     list is valid where mask_mod holds (causal: k <= q, local indices);
+ *     list is valid where mask_mod holds, with local indices: causal k <= q;
+ *     sliding window q - W < k <= q (the query and the W - 1 keys before it);
+ *     prefix LM k <= q or k < P (P: the sequence's prefix length);
  *   - keys outside every listed block get -1e9, as in the triangle formula;
  *   - with no lists at all every block is partial.
  * Keys k >= Lk do not exist and take no part.
@@ -42,7 +44,7 @@
 #endif
 
 enum { OR_F32 = 0, OR_F16 = 1, OR_BF16 = 2 };
-enum { OR_MASK_NONE = 0, OR_MASK_CAUSAL = 1 };
+enum { OR_MASK_NONE = 0, OR_MASK_CAUSAL = 1, OR_MASK_SLIDING_WINDOW = 2, OR_MASK_PREFIX_LM = 3 };
 
 #define OR_MASKED (-1.0e9)
 
@@ -184,10 +186,22 @@ void oracle_mask_to_kv_lengths(const uint8_t* mask, long long rows, int K, int32
     }
 }
 
+/* The mask_mod predicate for local query qi and key kk of a partial block. */
+static int or_mask_mod(int mask_mod, int qi, int kk, int window, int prefix) {
+    switch (mask_mod) {
+    case OR_MASK_CAUSAL: return kk <= qi;
+    case OR_MASK_SLIDING_WINDOW: return kk <= qi && qi - kk < window;
+    case OR_MASK_PREFIX_LM: return kk <= qi || kk < prefix;
+    default: return 1;
+    }
+}
+
 /*
  * Varlen form.  q/out (total_q, H, D); k/v (total_k, H, D); lse/mx (H, total_q).
  * kv_num (S, mask_heads, MQ), kv_idx (S, mask_heads, MQ, MK); full_* the same or NULL.
- * kv_num == NULL: every block is partial.  Returns 0 or -1.
+ * kv_num == NULL: every block is partial.  window: the sliding window's width
+ * (mask_mod 2); prefix_len (S,) or NULL, then prefix_all for every sequence
+ * (mask_mod 3).  Returns 0 or -1.
  */
 int oracle_varlen_fwd(const void* q, const void* k, const void* v, int dt,
                       const int32_t* cu_q, const int32_t* cu_k, int num_seqs, int H, int D,
@@ -195,8 +209,10 @@ int oracle_varlen_fwd(const void* q, const void* k, const void* v, int dt,
                       const int32_t* kv_num, const int32_t* kv_idx,
                       const int32_t* full_num, const int32_t* full_idx,
                       int mask_heads, int MQ, int MK, int block, int mask_mod,
+                      int window, const int32_t* prefix_len, int prefix_all,
                       double* out, double* lse, double* mx, int nthreads) {
     if (num_seqs <= 0 || H <= 0 || D <= 0 || block <= 0) return -1;
+    if (mask_mod == OR_MASK_SLIDING_WINDOW && window <= 0) return -1;
     if ((full_num == NULL) != (full_idx == NULL)) return -1;
     long long total_q = cu_q[num_seqs];
 #ifdef _OPENMP
@@ -235,11 +251,12 @@ int oracle_varlen_fwd(const void* q, const void* k, const void* v, int dt,
         }
         double* x = (double*)malloc(sizeof(double) * (size_t)(Lk > 0 ? Lk : 1));
         double* w = (double*)malloc(sizeof(double) * (size_t)(Lk > 0 ? Lk : 1));
+        int prefix = prefix_len ? prefix_len[s] : prefix_all;
         for (int qi = 0; qi < Lq; ++qi) {
             size_t q_off = (((size_t)(q0 + qi)) * H + h) * D;
             for (int kk = 0; kk < Lk; ++kk) {
                 int st = state[(size_t)(qi / block) * nbk + kk / block];
-                int valid = st == 2 || (st == 1 && (mask_mod != OR_MASK_CAUSAL || kk <= qi));
+                int valid = st == 2 || (st == 1 && or_mask_mod(mask_mod, qi, kk, window, prefix));
                 if (!valid) {
                     x[kk] = OR_MASKED;
                     continue;

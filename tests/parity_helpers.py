@@ -59,7 +59,7 @@ def check_triangle(case, rows=None):
     return compare(case.name, case.dtype, O, L, M, rO, rL, rM)
 
 
-def run_varlen(case, return_aux=True):
+def run_varlen(case, return_aux=True, window=0, prefix=None):
     import masked_attention_tri_gb300 as ta
     bm = None
     if case.kv_num_blocks is not None:
@@ -69,15 +69,18 @@ def run_varlen(case, return_aux=True):
     cu, cuk = case.cu_seqlens.cuda(), case.cu_seqlens_k.cuda()
     res = ta.varlen_attention(case.q.cuda(), case.k.cuda(), case.v.cuda(), cu, cuk, case.max_seqlen,
                               case.max_seqlen_k, block_mask=bm, scale=case.scale, return_aux=return_aux,
-                              mask_mod=case.mask_mod if bm is None else None)
+                              mask_mod=case.mask_mod if bm is None else None, window=window,
+                              prefix_lengths=prefix if not isinstance(prefix, list) else
+                              torch.tensor(prefix, dtype=torch.int32, device="cuda"))
     torch.cuda.synchronize()
     assert ta.get_status() == 0
     return res
 
 
-def check_varlen(case):
-    O, L, M = run_varlen(case)
+def check_varlen(case, window=0, prefix=None):
+    O, L, M = run_varlen(case, window=window, prefix=prefix)
     rO, rL, rM = oracle.varlen_fwd(case.q, case.k, case.v, case.cu_seqlens, case.cu_seqlens_k, case.scale,
                                    case.kv_num_blocks, case.kv_indices, case.full_kv_num_blocks,
-                                   case.full_kv_indices, block=case.block, mask_mod=case.mask_mod)
+                                   case.full_kv_indices, block=case.block, mask_mod=case.mask_mod,
+                                   window=window, prefix_lengths=prefix)
     return compare(case.name, case.dtype, O, L, M, rO, rL, rM)

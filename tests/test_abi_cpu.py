@@ -137,6 +137,39 @@ def test_varlen_strided_accepts_packed_strides(lib, strides):
     _strided(max_seqlen_q=0, q_row_stride=q, k_row_stride=k, v_row_stride=v)()
 
 
+def _masked(**kw):
+    args = dict(q=A, k=A, v=A, dtype=abi.TA_BF16, cu_seqlens_q=A, cu_seqlens_k=A, num_seqs=2, total_q=400,
+                total_k=400, max_seqlen_q=256, max_seqlen_k=256, H=2, D=64, scale=0.125, kv_num_blocks=0,
+                kv_indices=0, full_kv_num_blocks=0, full_kv_indices=0, mask_heads=1, max_q_blocks=2,
+                max_kv_blocks=2, block_q=128, block_k=128, mask_mod=abi.TA_MASK_SLIDING_WINDOW, window=16,
+                prefix_lengths=0, prefix_length=0, q_row_stride=0, k_row_stride=0, v_row_stride=0, out=A, lse=0,
+                max_=0, stream=0)
+    args.update(kw)
+    return lambda: abi.tri_attn_varlen_fwd_masked(**args)
+
+
+@pytest.mark.parametrize("kw,exc", [
+    (dict(window=0), ValueError),                                   # a window keeps at least the query itself
+    (dict(window=-3), ValueError),
+    (dict(mask_mod=4), ValueError),
+    (dict(mask_mod=abi.TA_MASK_PREFIX_LM, prefix_length=-1), ValueError),
+    (dict(mask_mod=abi.TA_MASK_PREFIX_LM, prefix_lengths=MIS + 2), ValueError),  # 4-byte alignment
+    (dict(block_q=64), NotImplementedError),
+])
+def test_varlen_masked_host_checks(lib, kw, exc):
+    with pytest.raises(exc):
+        _masked(**kw)()
+
+
+def test_varlen_masked_accepts_parameters_and_older_entries_refuse_them(lib):
+    _masked(max_seqlen_q=0)()                                              # window 16: accepted (no rows: no-op)
+    _masked(max_seqlen_q=0, mask_mod=abi.TA_MASK_PREFIX_LM, prefix_lengths=A)()
+    with pytest.raises(ValueError):  # the strided entry has no parameter for them
+        _strided(max_seqlen_q=0, mask_mod=abi.TA_MASK_SLIDING_WINDOW)()
+    with pytest.raises(ValueError):
+        _varlen(max_seqlen_q=0, mask_mod=abi.TA_MASK_PREFIX_LM)()
+
+
 def test_row_stride_of_packed_views():
     import torch
     from masked_attention_tri_gb300 import api

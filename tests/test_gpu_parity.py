@@ -187,6 +187,49 @@ def test_varlen_key_lengths_differ_with_lists():
     check_varlen(c)
 
 
+def test_varlen_many_short_sequences():
+    """More sequences than the key-split kernel's schedule keeps in shared memory (1024): the
+    two-tile kernel runs them; lengths 0..40, causal lists."""
+    g = torch.Generator().manual_seed(11)
+    lengths = torch.randint(0, 41, (1100,), generator=g).tolist()
+    c = synth.make_varlen("vl_many", len(lengths), 0, 0, 2, 32, "bf16", seed=580, lengths=lengths)
+    check_varlen(c)
+
+
+# The parameterised mask_mods (BlockMask page, mask_mod on partial blocks): on the
+# key-split kernel (16-bit), the two-tile kernel (more than 1024 sequences) and the
+# fp32 CUDA-core kernel.
+@pytest.mark.parametrize("dtype,D", [("bf16", 128), ("f16", 64), ("f32", 32)])
+@pytest.mark.parametrize("window", [1, 37, 200])
+def test_varlen_sliding_window(dtype, D, window):
+    c = synth.make_varlen(f"vl_sw{window}_{D}", 3, 0, 0, 2, D, dtype, seed=590 + window, lengths=[300, 1, 260],
+                          block_lists="none", mask_mod="sliding_window")
+    check_varlen(c, window=window)
+
+
+@pytest.mark.parametrize("dtype,D", [("bf16", 64), ("f16", 128), ("f32", 16)])
+@pytest.mark.parametrize("prefix", [0, 100, 300, [5, 0, 140, 1000]])
+def test_varlen_prefix_lm(dtype, D, prefix):
+    c = synth.make_varlen(f"vl_plm_{D}", 4, 0, 0, 2, D, dtype, seed=600 + D, lengths=[300, 129, 200, 64],
+                          block_lists="none", mask_mod="prefix_lm")
+    check_varlen(c, prefix=prefix)
+
+
+def test_varlen_sliding_window_with_lists_and_many_sequences():
+    """Causal block lists (earlier blocks full, the diagonal partial) with the window on the diagonal;
+    and more than 1024 short sequences (the two-tile kernel)."""
+    c = synth.make_varlen("vl_sw_lists", 3, 0, 0, 2, 64, "bf16", seed=610, lengths=[400, 260, 129],
+                          mask_mod="sliding_window")
+    check_varlen(c, window=50)
+    g = torch.Generator().manual_seed(12)
+    lengths = torch.randint(1, 41, (1030,), generator=g).tolist()
+    c2 = synth.make_varlen("vl_sw_many", len(lengths), 0, 0, 1, 32, "bf16", seed=611, lengths=lengths,
+                           block_lists="none", mask_mod="sliding_window")
+    check_varlen(c2, window=7)
+    c2.mask_mod = "prefix_lm"
+    check_varlen(c2, prefix=[int(x) % 9 for x in range(1030)])
+
+
 def test_varlen_fp32():
     c = synth.make_varlen("vl_f32", 3, 0, 0, 2, 32, "f32", seed=520, lengths=[40, 200, 131])
     check_varlen(c)

@@ -511,3 +511,64 @@ def test_varlen_per_head_lists_index_by_head():
         a = int(c.cu_seqlens[i])
         ref[a:a + min(128, L), 2] = _f64(c.v[a:a + L, 2]).mean(0).numpy()
     np.testing.assert_allclose(O, ref, atol=1e-12)
+
+
+@pytest.mark.parametrize("window", [1, 5, 130, 1000])
+def test_varlen_sliding_window_equals_banded_attention(window):
+    """mask_mod sliding_window(W): query q keeps keys q - W < k <= q (itself and the W - 1 before
+    it), local indices; W = 1 keeps only the diagonal, W >= L is plain causal."""
+    c = synth.make_varlen("t", 3, 0, 0, 2, 8, "f32", seed=33, lengths=[200, 7, 300], block_lists="none",
+                          mask_mod="sliding_window")
+    O, L, M = oracle.varlen_fwd(c.q, c.k, c.v, c.cu_seqlens, c.cu_seqlens, c.scale, mask_mod="sliding_window",
+                                window=window)
+
+    def keep(i, h, nq, nk):
+        qi = torch.arange(nq).view(-1, 1)
+        kj = torch.arange(nk).view(1, -1)
+        return (kj <= qi) & (qi - kj < window)
+
+    np.testing.assert_allclose(O, _varlen_sdpa_pairs(c, keep), atol=1e-12)
+    if window == 1:  # one key per row: O is that key's value, lse = max = its logit
+        np.testing.assert_allclose(O, _f64(c.v).numpy(), atol=1e-12)
+        np.testing.assert_allclose(L, M, atol=1e-12)
+
+
+def test_varlen_sliding_window_with_block_lists():
+    """The window applies on partial blocks only; full blocks keep every key."""
+    lengths = [300, 260]
+    c = synth.make_varlen("t", 2, 0, 0, 2, 8, "bf16", seed=34, lengths=lengths, block_lists="none")
+    kn, ki, fn, fi = synth.causal_block_lists(lengths)   # diagonal partial, earlier blocks full
+    W = 40
+    O, _, _ = oracle.varlen_fwd(c.q, c.k, c.v, c.cu_seqlens, c.cu_seqlens, c.scale, kn, ki, fn, fi,
+                                mask_mod="sliding_window", window=W)
+
+    def keep(i, h, nq, nk):
+        qi = torch.arange(nq).view(-1, 1)
+        kj = torch.arange(nk).view(1, -1)
+        diag = (qi // 128) == (kj // 128)
+        earlier = (kj // 128) < (qi // 128)
+        return earlier | (diag & (kj <= qi) & (qi - kj < W))
+
+    np.testing.assert_allclose(O, _varlen_sdpa_pairs(c, keep), atol=1e-12)
+
+
+@pytest.mark.parametrize("prefix", [0, 1, 50, 129, [10, 0, 400]])
+def test_varlen_prefix_lm_equals_prefix_plus_causal(prefix):
+    """mask_mod prefix_lm(P): query q keeps keys k <= q or k < P (the prefix is seen by every
+    query of the sequence); P = 0 is plain causal; P may differ per sequence."""
+    lengths = [200, 70, 300]
+    c = synth.make_varlen("t", 3, 0, 0, 2, 8, "f32", seed=35, lengths=lengths, block_lists="none",
+                          mask_mod="prefix_lm")
+    O, _, _ = oracle.varlen_fwd(c.q, c.k, c.v, c.cu_seqlens, c.cu_seqlens, c.scale, mask_mod="prefix_lm",
+                                prefix_lengths=prefix)
+    per = prefix if isinstance(prefix, list) else [prefix] * 3
+
+    def keep(i, h, nq, nk):
+        qi = torch.arange(nq).view(-1, 1)
+        kj = torch.arange(nk).view(1, -1)
+        return (kj <= qi) | (kj < per[i])
+
+    np.testing.assert_allclose(O, _varlen_sdpa_pairs(c, keep), atol=1e-12)
+    if per == [0, 0, 0]:
+        Oc, _, _ = oracle.varlen_fwd(c.q, c.k, c.v, c.cu_seqlens, c.cu_seqlens, c.scale, mask_mod="causal")
+        np.testing.assert_array_equal(O, Oc)
