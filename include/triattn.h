@@ -106,6 +106,28 @@ ta_status tri_attn_fwd(const void* q, const void* k, const void* v, ta_dtype qkv
                        void* out, float* lse, float* max, void* stream);
 
 /*
+ * tri_attn_fwd_strided -- tri_attn_fwd on q / k / v given as strided views.
+ * (cuEquivariance triangle_attention page: the same operation on the same
+ *  (B, N, H, Q|K, D) tensors; views such as a (B, N, Q, H, D) buffer read as
+ *  (B, N, H, Q, D), or rows padded past D, are read in place.)
+ *
+ *   q_strides, k_strides, v_strides  optional host arrays of 4 element strides
+ *                  {b, n, h, row} of q, k, v (row = the q / key index); the D
+ *                  elements of a row are contiguous.  NULL = contiguous.  Each
+ *                  stride must be >= 1 and the row stride >= D (else
+ *                  TA_ERR_INVALID_ARG), and a multiple of 16 bytes below 2^40
+ *                  bytes (else TA_ERR_UNSUPPORTED).  The inputs are only read,
+ *                  so views may overlap one another.
+ *   every other argument, including the contiguous `out`, as in tri_attn_fwd.
+ */
+ta_status tri_attn_fwd_strided(const void* q, const void* k, const void* v, ta_dtype qkv_dtype,
+                               const void* bias, ta_dtype bias_dtype,
+                               const uint8_t* mask, const int32_t* kv_lengths,
+                               int B, int N, int H, int Q, int K, int D, float scale,
+                               const long long* q_strides, const long long* k_strides, const long long* v_strides,
+                               void* out, float* lse, float* max, void* stream);
+
+/*
  * tri_attn_varlen_fwd -- packed-sequence forward with a block-sparse mask.
  * (Transformer Engine 0.9 fused_attn.h: NVTE_NOT_INTERLEAVED layout,
  *  cu_seqlens_q / cu_seqlens_kv, max_seqlen_q / max_seqlen_kv; tensorplay

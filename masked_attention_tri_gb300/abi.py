@@ -19,7 +19,7 @@ TA_F32, TA_F16, TA_BF16 = 0, 1, 2
 TA_MASK_NONE, TA_MASK_CAUSAL, TA_MASK_SLIDING_WINDOW, TA_MASK_PREFIX_LM = 0, 1, 2, 3
 
 # Every symbol include/triattn.h declares.
-EXPORTS = ("tri_attn_fwd", "tri_attn_varlen_fwd", "tri_attn_varlen_fwd_strided", "tri_attn_varlen_fwd_masked",
+EXPORTS = ("tri_attn_fwd", "tri_attn_fwd_strided", "tri_attn_varlen_fwd", "tri_attn_varlen_fwd_strided", "tri_attn_varlen_fwd_masked",
            "tri_attn_mask_to_kv_lengths", "tri_attn_get_status", "tri_attn_error_string", "tri_attn_version")
 
 _lock = threading.Lock()
@@ -45,6 +45,8 @@ def load() -> ctypes.CDLL:
         P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
         lib.tri_attn_fwd.argtypes = [P, P, P, I, P, I, P, P, I, I, I, I, I, I, F, P, P, P, P]
         lib.tri_attn_fwd.restype = I
+        lib.tri_attn_fwd_strided.argtypes = [P, P, P, I, P, I, P, P, I, I, I, I, I, I, F, P, P, P, P, P, P, P]
+        lib.tri_attn_fwd_strided.restype = I
         lib.tri_attn_varlen_fwd.argtypes = [P, P, P, I, P, P, I, I, I, I, I, I, I, F, P, P, P, P, I, I, I, I, I, I,
                                             P, P, P, P]
         lib.tri_attn_varlen_fwd.restype = I
@@ -88,6 +90,21 @@ def tri_attn_fwd(q, k, v, qkv_dtype, bias, bias_dtype, mask, kv_lengths, B, N, H
     st = load().tri_attn_fwd(q, k, v, qkv_dtype, bias, bias_dtype, mask or None, kv_lengths or None, B, N, H, Q, K,
                              D, float(scale), out, lse or None, max_ or None, stream or None)
     _check(st, "tri_attn_fwd")
+
+
+def _strides4(st):
+    """A host array of 4 element strides (b, n, h, row) for the C call, or None (contiguous)."""
+    return None if st is None else (ctypes.c_longlong * 4)(*[int(x) for x in st])
+
+
+def tri_attn_fwd_strided(q, k, v, qkv_dtype, bias, bias_dtype, mask, kv_lengths, B, N, H, Q, K, D, scale, q_strides,
+                         k_strides, v_strides, out, lse, max_, stream) -> None:
+    """q_strides / k_strides / v_strides: 4 element strides (b, n, h, row) each, or None."""
+    qs, ks, vs = _strides4(q_strides), _strides4(k_strides), _strides4(v_strides)
+    st = load().tri_attn_fwd_strided(q, k, v, qkv_dtype, bias, bias_dtype, mask or None, kv_lengths or None, B, N, H,
+                                     Q, K, D, float(scale), qs, ks, vs, out, lse or None, max_ or None,
+                                     stream or None)
+    _check(st, "tri_attn_fwd_strided")
 
 
 def tri_attn_varlen_fwd(q, k, v, dtype, cu_seqlens_q, cu_seqlens_k, num_seqs, total_q, total_k, max_seqlen_q,

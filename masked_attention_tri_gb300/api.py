@@ -51,7 +51,9 @@ def triangle_attention(q, k, v, bias, mask=None, scale=None, return_aux=False, *
     """Triangle-attention forward (cuEquivariance triangle_attention page: formula, Parameters).
 
     q (B,N,H,Q,D), k/v (B,N,H,K,D), bias (B,1,H,Q,K); for B=1 the 4-D forms
-    (N,H,Q,D) / (1,H,Q,K) / (N,1,1,K) are accepted.  mask: bool/uint8
+    (N,H,Q,D) / (1,H,Q,K) / (N,1,1,K) are accepted.  q, k, v may be strided
+    views whose last dimension is contiguous (e.g. a (B,N,Q,H,D) buffer
+    transposed to (B,N,H,Q,D)); they are read in place.  mask: bool/uint8
     (B,N,1,1,K); kv_lengths: int32 (B,N,1,1,1) or (B,N); at most one of them.
     scale defaults to 1/sqrt(D).  Returns O, or (O, lse, max) with
     return_aux (lse / max fp32 shaped (B,N,H,Q,1)).  out, lse, mx may be given
@@ -80,8 +82,15 @@ def triangle_attention(q, k, v, bias, mask=None, scale=None, return_aux=False, *
     dev = q.device
     if dev.type != "cuda":
         raise ValueError("triangle_attention runs on CUDA tensors only")
-    for t, nm in ((q, "q"), (k, "k"), (v, "v"), (bias, "bias")):
-        _need(t, nm, dev)
+    _need(bias, "bias", dev)
+    strides = []
+    for t, nm in ((q, "q"), (k, "k"), (v, "v")):
+        if not isinstance(t, torch.Tensor) or t.device != dev:
+            raise ValueError(f"{nm} must be a tensor on {dev}")
+        if t.stride(4) != 1:
+            raise ValueError(f"{nm}: the last dimension (D) must be contiguous")
+        # None = contiguous (the plain entry point)
+        strides.append(None if t.is_contiguous() else tuple(t.stride(i) for i in range(4)))
     if q.dtype not in _DT or k.dtype != q.dtype or v.dtype != q.dtype:
         raise TypeError("q, k, v must share one dtype among float32 / float16 / bfloat16")
     if bias.dtype not in (torch.float32, q.dtype):
@@ -102,7 +111,7 @@ def triangle_attention(q, k, v, bias, mask=None, scale=None, return_aux=False, *
         kl = kv_lengths
     s = 1.0 / math.sqrt(D) if scale is None else float(scale)
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty(q.shape, dtype=q.dtype, device=dev)
     else:
         _need(out, "out", dev)
     if return_aux:
@@ -118,8 +127,14 @@ def triangle_attention(q, k, v, bias, mask=None, scale=None, return_aux=False, *
     else:
         lse = mx = None
     with torch.cuda.device(dev):
-        abi.tri_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _DT[q.dtype], _ptr(bias), _DT[bias.dtype], _ptr(m8), _ptr(kl),
-                         B, N, H, Q, K, D, s, _ptr(out), _ptr(lse), _ptr(mx), _stream(dev))
+        if strides == [None, None, None]:
+            abi.tri_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _DT[q.dtype], _ptr(bias), _DT[bias.dtype], _ptr(m8),
+                             _ptr(kl), B, N, H, Q, K, D, s, _ptr(out), _ptr(lse), _ptr(mx), _stream(dev))
+        else:
+            full = [st if st is not None else tuple(t.stride(i) for i in range(4)) for st, t in zip(strides, (q, k, v))]
+            abi.tri_attn_fwd_strided(_ptr(q), _ptr(k), _ptr(v), _DT[q.dtype], _ptr(bias), _DT[bias.dtype], _ptr(m8),
+                                     _ptr(kl), B, N, H, Q, K, D, s, full[0], full[1], full[2], _ptr(out), _ptr(lse),
+                                     _ptr(mx), _stream(dev))
     if four_d:
         out = out.squeeze(0)
         if return_aux:

@@ -61,10 +61,42 @@ ta_status run(const AttnParams& p, cudaStream_t stream) {
 
 }  // namespace
 
+// Element strides {b, n, h, row} of a (B, N, H, rows, D) tensor whose D elements are contiguous:
+// the given ones (checked) or, for NULL, the contiguous layout.
+ta_status triangle_strides(const long long* given, int B, int N, int H, int rows, int D, int esz, long long (&st)[4]) {
+    if (!given) {
+        st[3] = D;
+        st[2] = (long long)rows * D;
+        st[1] = st[2] * H;
+        st[0] = st[1] * N;
+        return TA_OK;
+    }
+    const long long ext[4] = {B, N, H, rows};
+    for (int i = 0; i < 4; ++i) {
+        st[i] = given[i];
+        if (st[i] < 1) return TA_ERR_INVALID_ARG;
+        // tensor-map strides: 16-byte multiples below 2^40 bytes; every offset fits in 62 bits
+        if ((st[i] * esz) % 16 != 0 || st[i] * esz >= (1LL << 40)) return TA_ERR_UNSUPPORTED;
+        if (ext[i] > 1 && st[i] > ((1LL << 60) / (ext[i] - 1))) return TA_ERR_UNSUPPORTED;
+    }
+    if (st[3] < D) return TA_ERR_INVALID_ARG;  // the D elements of one row may not overlap the next row
+    return TA_OK;
+}
+
 TA_EXPORT ta_status tri_attn_fwd(const void* q, const void* k, const void* v, ta_dtype qkv_dtype, const void* bias,
                                  ta_dtype bias_dtype, const uint8_t* mask, const int32_t* kv_lengths, int B, int N,
                                  int H, int Q, int K, int D, float scale, void* out, float* lse, float* max,
                                  void* stream) {
+    return tri_attn_fwd_strided(q, k, v, qkv_dtype, bias, bias_dtype, mask, kv_lengths, B, N, H, Q, K, D, scale,
+                                nullptr, nullptr, nullptr, out, lse, max, stream);
+}
+
+TA_EXPORT ta_status tri_attn_fwd_strided(const void* q, const void* k, const void* v, ta_dtype qkv_dtype,
+                                         const void* bias, ta_dtype bias_dtype, const uint8_t* mask,
+                                         const int32_t* kv_lengths, int B, int N, int H, int Q, int K, int D,
+                                         float scale, const long long* q_strides, const long long* k_strides,
+                                         const long long* v_strides, void* out, float* lse, float* max,
+                                         void* stream) {
     if (!q || !k || !v || !bias || !out) return TA_ERR_INVALID_ARG;
     if (B <= 0 || N <= 0 || H <= 0 || Q <= 0 || K <= 0 || D <= 0) return TA_ERR_INVALID_ARG;
     if (mask && kv_lengths) return TA_ERR_INVALID_ARG;
@@ -83,9 +115,15 @@ TA_EXPORT ta_status tri_attn_fwd(const void* q, const void* k, const void* v, ta
     if (units > (1LL << 40) || (long long)Q * K * 4 >= (1LL << 40) || units * ((Q + 31) / 32) > 0x7fffffffLL)
         return TA_ERR_UNSUPPORTED;
 
+    AttnParams p{};
+    const int esz = qkv_dtype == TA_F32 ? 4 : 2;
+    ta_status sst;
+    if ((sst = triangle_strides(q_strides, B, N, H, Q, D, esz, p.qs)) != TA_OK) return sst;
+    if ((sst = triangle_strides(k_strides, B, N, H, K, D, esz, p.ks)) != TA_OK) return sst;
+    if ((sst = triangle_strides(v_strides, B, N, H, K, D, esz, p.vs)) != TA_OK) return sst;
+
     int* status = triattn::status_word();
     if (!status) return TA_ERR_CUDA;
-    AttnParams p{};
     p.q = q;
     p.k = k;
     p.v = v;

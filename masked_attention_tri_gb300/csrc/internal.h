@@ -34,6 +34,9 @@ struct AttnParams {
 
     // triangle sizes
     int B, N, H, Q, K, D;
+    // triangle q, k, v: element strides of the b, n, h and row (q / key) indices; the D elements of
+    // a row are contiguous.  Contiguous tensors: {N*H*rows*D, H*rows*D, rows*D, D}.
+    long long qs[4], ks[4], vs[4];
 
     // varlen
     int varlen;

@@ -192,12 +192,15 @@ __global__ void __launch_bounds__(kWarps * 32) simt_fwd_kernel(const AttnParams 
         h = (int)(u % p.H);
         const long long bn = u / p.H;
         const int b = (int)(bn / p.N);
-        q_off = u * p.Q * (long long)D;
-        q_rs = D;
-        o_off = q_off;
-        o_rs = q_rs;
-        st.k_off = st.v_off = u * p.K * (long long)D;
-        st.k_rs = st.v_rs = D;
+        const long long n = bn - (long long)b * p.N;
+        q_off = b * p.qs[0] + n * p.qs[1] + h * p.qs[2];
+        q_rs = p.qs[3];
+        o_off = u * p.Q * (long long)D;
+        o_rs = D;
+        st.k_off = b * p.ks[0] + n * p.ks[1] + h * p.ks[2];
+        st.k_rs = p.ks[3];
+        st.v_off = b * p.vs[0] + n * p.vs[1] + h * p.vs[2];
+        st.v_rs = p.vs[3];
         Lq = p.Q;
         st.Lk = p.K;
         st.bias_row0 = (((long long)b * p.H + h) * p.Q + (long long)qt * kQT) * p.K;

@@ -60,6 +60,20 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t 
     return r == CUDA_SUCCESS;
 }
 
+// 5-D tiled map of a triangle-form q / k / v: dims {D, rows, H, N, B} with the
+// element strides st = {b, n, h, row}; boxes of 64 elements x 128 rows.
+bool make_map5(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t D, uint64_t rows, const AttnParams& a,
+               const long long (&st)[4]) {
+    cuuint64_t dims[5] = {D, rows, (cuuint64_t)a.H, (cuuint64_t)a.N, (cuuint64_t)a.B};
+    cuuint64_t strides[4] = {(cuuint64_t)st[3] * 2, (cuuint64_t)st[2] * 2, (cuuint64_t)st[1] * 2, (cuuint64_t)st[0] * 2};
+    cuuint32_t box[5] = {64, 128, 1, 1, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = g_encode(m, dt, 5, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // Instruction descriptor of kind::f16: D fp32 at [4,6), A/B type at [7,10) /
 // [10,13) (0 f16, 1 bf16), B major at bit 16 (0 K-major, 1 MN-major), N>>3
 // at [17,23), M>>4 at [24,29).
@@ -98,13 +112,13 @@ bool choose_geometry(TcParams& P, bool varlen, int& NQ) {
 }
 
 // The key-split kernel (triangle form with D <= 64, packed form with D <=
-// 128): one query tile per item; three S buffers and two O accumulators of
-// up to 64 columns, or two S buffers and two O accumulators of 128 columns,
-// in 512 tensor-memory columns; Q buffers, K/V stages and bias stages as
-// shared memory allows.
+// 128): one query tile per item; three S buffers, and two O accumulators of
+// up to 64 columns or one of 128, in 512 tensor-memory columns; Q buffers,
+// K/V stages and bias stages as shared memory allows.
 bool choose_split_geometry(TcParams& P, bool varlen) {
     const int prefs[][3] = {{2, 3, 2}, {2, 3, 1}, {2, 2, 2}, {2, 2, 1}, {1, 2, 1}};
-    P.s_bufs = P.o_cols <= 64 ? 3 : 2;
+    P.s_bufs = 3;
+    P.o_bufs = P.o_cols <= 64 ? 2 : 1;
     for (const auto& pr : prefs) {
         P.q_bufs = pr[0];
         P.kv_stages = pr[1];
@@ -156,10 +170,20 @@ cudaError_t launch_tc_fwd(const AttnParams& a, cudaStream_t stream) {
         P.bias_boxes = kBN / P.bias_box_cols;
         P.bias_bytes = P.bias_boxes * kBox;
         P.mask_kind = a.kv_len ? 1 : (a.mask ? 2 : 0);
+        // Contiguous q / k / v (strides {N*H*rows*D, H*rows*D, rows*D, D}) keep 3-D maps over the
+        // (b, n, h) slabs; strided views take 5-D maps.
+        auto contiguous = [&](const long long (&st)[4], int rows) {
+            return st[3] == D && st[2] == (long long)rows * D && st[1] == st[2] * a.H && st[0] == st[1] * a.N;
+        };
+        P.tri5d = !(contiguous(a.qs, a.Q) && contiguous(a.ks, a.K) && contiguous(a.vs, a.K));
         const uint64_t units = (uint64_t)a.B * a.N * a.H;
-        if (!make_map(&P.tm_q, dt, a.q, D, a.Q, units, rs, rs * a.Q, 64, kBM, 1) ||
-            !make_map(&P.tm_k, dt, a.k, D, a.K, units, rs, rs * a.K, 64, kBN, 1) ||
-            !make_map(&P.tm_v, dt, a.v, D, a.K, units, rs, rs * a.K, 64, kBN, 1) ||
+        const bool maps_ok =
+            P.tri5d ? make_map5(&P.tm_q, dt, a.q, D, a.Q, a, a.qs) && make_map5(&P.tm_k, dt, a.k, D, a.K, a, a.ks) &&
+                          make_map5(&P.tm_v, dt, a.v, D, a.K, a, a.vs)
+                    : make_map(&P.tm_q, dt, a.q, D, a.Q, units, rs, rs * a.Q, 64, kBM, 1) &&
+                          make_map(&P.tm_k, dt, a.k, D, a.K, units, rs, rs * a.K, 64, kBN, 1) &&
+                          make_map(&P.tm_v, dt, a.v, D, a.K, units, rs, rs * a.K, 64, kBN, 1);
+        if (!maps_ok ||
             !make_map(&P.tm_bias, a.bias_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : dt, a.bias, a.K, a.Q,
                       (uint64_t)a.B * a.H, a.K * eb, a.K * eb * a.Q, P.bias_box_cols, kBM, 1))
             return cudaErrorInvalidValue;

@@ -125,7 +125,11 @@ struct TcParams {
     // Key-split kernel only: S buffers (3 with D <= 64, 2 above), O accumulators
     // (2), and the divisor 2 * grid of the packed form's serpentine deal.
     int s_bufs;
+    int o_bufs;
     FastDiv fd_2g;
+    // Triangle form: q / k / v maps are 5-D {D, rows, H, N, B} (strided views), or
+    // 3-D {D, rows, B*N*H} for contiguous tensors.
+    int tri5d;
 };
 
 // ---------------------------------------------------------------------------
@@ -233,6 +237,23 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm,
         "[%5];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
         : "memory");
+}
+
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* tm, int c0, int c1, int c2, int c3,
+                                            int c4, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+        "%5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar)
+        : "memory");
+}
+
+// A triangle-form q / k / v tile: rows [row, row + 128) of slab (b, n, h) from
+// the 3-D (contiguous) or 5-D (strided) map.
+__device__ __forceinline__ void tma_load_tri(const TcParams& P, uint32_t dst, const CUtensorMap* tm, int c0, int row,
+                                             long long unit, int h, int n, int b, uint32_t bar) {
+    if (P.tri5d) tma_load_5d(dst, tm, c0, row, h, n, b, bar);
+    else tma_load_3d(dst, tm, c0, row, (int)unit, bar);
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -648,8 +669,8 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
                     mbar_expect_tx(q_full(i, qb), P.tile_bytes);
                     for (int sb = 0; sb < P.nsub; ++sb) {
                         if constexpr (!VARLEN)
-                            tma_load_3d(q_smem(i, qb) + sb * kBox, &P.tm_q, sb * 64, it.qt[i] * kBM, (int)it.unit,
-                                        q_full(i, qb));
+                            tma_load_tri(P, q_smem(i, qb) + sb * kBox, &P.tm_q, sb * 64, it.qt[i] * kBM, it.unit,
+                                         it.h, (int)(it.bn - (long long)it.b * a.N), it.b, q_full(i, qb));
                         else
                             tma_load_3d(q_smem(i, qb) + sb * kBox, &P.tm_q, sb * 64, it.h, it.q_row0 + it.qt[i] * kBM,
                                         q_full(i, qb));
@@ -666,8 +687,11 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
                     mbar_expect_tx(kv_full(st), 2 * P.tile_bytes);
                     for (int sb = 0; sb < P.nsub; ++sb) {
                         if constexpr (!VARLEN) {
-                            tma_load_3d(k_smem(st) + sb * kBox, &P.tm_k, sb * 64, kb * kBN, (int)it.unit, kv_full(st));
-                            tma_load_3d(v_smem(st) + sb * kBox, &P.tm_v, sb * 64, kb * kBN, (int)it.unit, kv_full(st));
+                            const int n = (int)(it.bn - (long long)it.b * a.N);
+                            tma_load_tri(P, k_smem(st) + sb * kBox, &P.tm_k, sb * 64, kb * kBN, it.unit, it.h, n, it.b,
+                                         kv_full(st));
+                            tma_load_tri(P, v_smem(st) + sb * kBox, &P.tm_v, sb * 64, kb * kBN, it.unit, it.h, n, it.b,
+                                         kv_full(st));
                         } else {
                             tma_load_3d(k_smem(st) + sb * kBox, &P.tm_k, sb * 64, it.h, it.k_row0 + kb * kBN,
                                         kv_full(st));
@@ -1111,9 +1135,13 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
                     float mv = 0.f;
                     const int d = d0 + lane;
                     if (it.Lk > 0 && d < a.D) {
-                        const long long vrow0 = !VARLEN ? it.unit * a.K : (long long)it.k_row0;
-                        const long long vstride = !VARLEN ? a.D : a.v_rs;
-                        const long long vcol0 = !VARLEN ? 0 : (long long)it.h * a.D;
+                        // V(key, d) at vcol0 + (vrow0 + key) * vstride + d
+                        const long long vrow0 = !VARLEN ? 0 : (long long)it.k_row0;
+                        const long long vstride = !VARLEN ? a.vs[3] : a.v_rs;
+                        const long long vcol0 = !VARLEN ? (long long)it.b * a.vs[0] +
+                                                              (it.bn - (long long)it.b * a.N) * a.vs[1] +
+                                                              (long long)it.h * a.vs[2]
+                                                        : (long long)it.h * a.D;
                         // Eight independent sums keep eight loads in flight.
                         float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
                         int key = 0;

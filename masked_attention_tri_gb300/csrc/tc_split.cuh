@@ -19,18 +19,21 @@
 //   warp 10      bias producer: TMA of bias tiles and the dense-mask bits
 //                (triangle form);
 //   warp 11      producer: TMA of V.
-// The MMA warp walks the CTA's key tiles as one stream across work items:
-// S of tile n + s_bufs goes into the buffer of tile n as soon as PV of tile n
-// is issued, also when that tile belongs to the next item, so the softmax
-// finds the next S ready at item boundaries too.  Items alternate between two
-// O accumulators, and the softmax writes out an item's O after the first tile
-// of the next item, when the last PV of the item has long finished.  Tensor
-// memory: s_bufs S buffers of 128 columns from column 0 (P overwrites the
-// first 64 columns of its buffer), O_0 and O_1 from column 128 s_bufs: three
-// S buffers with D <= 64 (O 2 x 64 columns), two with D in (64, 128] (O 2 x
-// 128 columns).  K and V stages have their own barriers: a K stage is
-// refilled once its QK^T is done, a V stage once its PV is.  The softmax
-// waits for a PV only before it rescales O and before it reads O.
+// The MMA warp walks the CTA's key tiles as one stream across work items.
+// Triangle form: when P of tile n is ready, PV of tile n is issued and then
+// QK^T of tile n + 3 into the buffer it read.  Packed form: PV of tile n and
+// QK^T of tile n + 2 are issued interleaved, k step by k step (two
+// independent accumulations the tensor core overlaps).  Either way the next
+// S is issued also when it belongs to the next item, so the softmax finds it
+// ready at item boundaries too.  Tensor memory: three S buffers of 128 columns from column 0 (P
+// overwrites the first 64 columns of its buffer) and, from column 384, two O
+// accumulators of up to 64 columns (D <= 64; items alternate between them)
+// or one of 128 (D in (64, 128]; an item's first PV waits until the softmax
+// has read the previous item's O).  The softmax writes out an item's O after
+// the first tile of the next item, when the last PV of the item has long
+// finished.  K and V stages have their own barriers: a K stage is refilled
+// once its QK^T is done, a V stage once its PV is.  The softmax waits for a
+// PV only before it rescales O and before it reads O.
 //
 // Work items.  Triangle form: one q tile of one (b, n, h) slab, in index
 // order, dealt round-robin over the CTAs (q tiles fastest, then n: the CTAs
@@ -55,8 +58,20 @@ constexpr int kSplitThreads = 12 * 32;
 // (more sequences go to the two-tile kernel).
 constexpr int kSplitMaxSeqs = 1024;
 
+// Packed form: decoded work items, handed from the scheduler warp to the
+// other roles through a ring in shared memory.
+constexpr int kRing = 8;
+struct VEntry {
+    int seq, h, qb, nkt;       // nkt < 0: no more items
+    int q_row0, Lq, k_row0, Lk;
+    int nkb, n_part, n_full, lists;
+    const int32_t* part_l;
+    const int32_t* full_l;
+    unsigned long long part0, full0;
+};
+
 struct SplitLayout {
-    uint32_t q, kv, bias, maskw, xbuf, xl, sched, bars, tmem_slot, abort_flag, total;
+    uint32_t q, kv, bias, maskw, xbuf, xl, sched, ring, bars, tmem_slot, abort_flag, total;
     int nbars;
 };
 
@@ -70,11 +85,13 @@ __host__ __device__ inline SplitLayout make_split_layout(const TcParams& P) {
     L.xl = L.xbuf + 2 * 2 * 128 * 4;           // row sums: [key half][128 rows] fp32
     L.sched = L.xl + 2 * 128 * 4;              // packed form: cu_q[S+1], cu_k[S+1], q blocks[S] (int32)
     const uint32_t sched_bytes = P.a.varlen ? (uint32_t)(3 * P.a.num_seqs + 2) * 4u : 0u;
-    L.bars = (L.sched + sched_bytes + 15u) & ~15u;
+    // ring: ring_full[kRing], ring_empty[kRing] (8-byte mbarriers), then the entries
+    L.ring = (L.sched + sched_bytes + 15u) & ~15u;
+    L.bars = L.ring + (P.a.varlen ? (uint32_t)(16 * kRing + kRing * sizeof(VEntry)) : 0u);
     // q_full, q_empty (QB each), k_full, k_empty, v_full, v_empty (S each),
     // bias_full, bias_empty (BS each), s_full[s_bufs], p_full[s_bufs],
-    // pv_done[2], xchg[4], drain
-    L.nbars = 2 * P.q_bufs + 4 * P.kv_stages + 2 * P.bias_stages + 2 * P.s_bufs + 2 + 4 + 1;
+    // pv_done[2], xchg[4], drain, o_empty
+    L.nbars = 2 * P.q_bufs + 4 * P.kv_stages + 2 * P.bias_stages + 2 * P.s_bufs + 2 + 4 + 1 + 1;
     L.tmem_slot = L.bars + 8 * L.nbars;
     L.abort_flag = L.tmem_slot + 4;
     L.total = L.abort_flag + 4;
@@ -279,28 +296,70 @@ __device__ __forceinline__ bool tiles_next(const SItem& it, TileWalk& tw, int& k
     }
 }
 
+// Where the roles of the packed form read their work items: the ring's
+// shared-memory address (barriers ring_full[i] at ring + 8 i, ring_empty[i] at
+// ring + 8 (kRing + i), entries from ring + 16 kRing) and the CTA's abort flag.
+struct RingRef {
+    uint32_t ring;
+    volatile int* abort_flag;
+};
+
+// Consumers of one entry: the Q/K and V producers, the MMA warp's two cursors
+// and the eight softmax warps.
+constexpr int kRingConsumers = 12;
+
 // A role's walk over this CTA's items (all of them, also those without key
-// tiles).
+// tiles).  Triangle form: item indices blockIdx.x + k * gridDim.x, decoded by
+// every role.  Packed form: the entries the scheduler warp decodes in turn.
 template <bool VARLEN>
-struct ItemWalk {
-    int item;      // triangle: item index
-    VCursor vc;    // packed form
-    __device__ __forceinline__ void begin(const TcParams& P) {
-        item = (int)blockIdx.x;
-        if constexpr (VARLEN) vc = vcursor_begin(P);
+struct ItemWalk;
+
+template <>
+struct ItemWalk<false> {
+    int item;
+    __device__ __forceinline__ void begin(const TcParams&, const RingRef&) { item = (int)blockIdx.x; }
+    __device__ __forceinline__ bool next(const TcParams& P, const RingRef&, SItem& it) {
+        if (item >= P.items) return false;
+        it = split_decode<false>(P, nullptr, item, 0, 0, 0);
+        item += gridDim.x;
+        return true;
     }
-    __device__ __forceinline__ bool next(const TcParams& P, const int* sched, SItem& it) {
-        if constexpr (!VARLEN) {
-            if (item >= P.items) return false;
-            it = split_decode<false>(P, sched, item, 0, 0, 0);
-            item += gridDim.x;
-            return true;
-        } else {
-            int seq, h, qb;
-            if (!vcursor_next(P, sched + 2 * (P.a.num_seqs + 1), vc, seq, h, qb)) return false;
-            it = split_decode<true>(P, sched, 0, seq, h, qb);
-            return true;
-        }
+};
+
+template <>
+struct ItemWalk<true> {
+    StageRing rr;
+    __device__ __forceinline__ void begin(const TcParams&, const RingRef&) { rr = {0, 0u, false}; }
+    __device__ __forceinline__ bool next(const TcParams& P, const RingRef& r, SItem& it) {
+        const int slot = rr.idx;
+        // A wait that runs out raises the abort flag; the role then leaves like every other.
+        if (!__all_sync(0xffffffffu, wait_bar(r.ring + 8u * (uint32_t)slot, rr.ph, r.abort_flag, P.a.status)))
+            return false;
+        const VEntry* v = reinterpret_cast<const VEntry*>(
+            __cvta_shared_to_generic(r.ring + 16u * kRing + (uint32_t)(slot * sizeof(VEntry))));
+        it.nkt = v->nkt;
+        it.qt = v->qb;
+        it.h = v->h;
+        it.seq = v->seq;
+        it.q_row0 = v->q_row0;
+        it.Lq = v->Lq;
+        it.k_row0 = v->k_row0;
+        it.Lk = v->Lk;
+        it.nkb = v->nkb;
+        it.lists = v->lists != 0;
+        it.part_l = v->part_l;
+        it.full_l = v->full_l;
+        it.n_part = v->n_part;
+        it.n_full = v->n_full;
+        it.part0 = v->part0;
+        it.full0 = v->full0;
+        it.unit = it.bn = 0;
+        it.b = 0;
+        it.prefix = 0;
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) mbar_arrive(r.ring + 8u * (uint32_t)(kRing + slot));
+        rr.next(kRing);
+        return it.nkt >= 0;
     }
 };
 
@@ -317,9 +376,9 @@ struct SplitCursor {
 
 // Moves the cursor to the next item with key tiles.
 template <bool VARLEN>
-__device__ __forceinline__ bool split_seek(const TcParams& P, const int* sched, SplitCursor<VARLEN>& c) {
+__device__ __forceinline__ bool split_seek(const TcParams& P, const RingRef& r, SplitCursor<VARLEN>& c) {
     SItem it;
-    while (c.walk.next(P, sched, it)) {
+    while (c.walk.next(P, r, it)) {
         if (it.nkt > 0) {
             c.nkt = it.nkt;
             c.t = 0;
@@ -327,6 +386,38 @@ __device__ __forceinline__ bool split_seek(const TcParams& P, const int* sched, 
         }
     }
     return false;
+}
+
+// Rows with no valid key among the visited ones (rare): the mean of V over
+// `nkeys` keys (V(key, d) at v[v_base + key * v_stride + d]), or zeros when
+// there are no keys, into the rows of this warp for which `mine` holds.  Lane
+// l forms the means of columns l, l + 32, ...; rows take them by shuffles.
+// Out of line so the per-item epilogue stays small in the instruction cache.
+template <bool BF16>
+static __device__ __noinline__ void split_mean_v(const AttnParams& a, uint16_t* orow_p, long long v_base,
+                                                 long long v_stride, int nkeys, bool mine) {
+    const int lane = threadIdx.x % 32;
+#pragma unroll 1
+    for (int d0 = 0; d0 < a.D; d0 += 32) {
+        const int d = d0 + lane;
+        float sum[4] = {0.f, 0.f, 0.f, 0.f};
+        if (d < a.D) {
+            int key = 0;
+#pragma unroll 1
+            for (; key + 4 <= nkeys; key += 4) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) sum[u] += load16<BF16>(a.v, v_base + (key + u) * v_stride + d);
+            }
+#pragma unroll 1
+            for (; key < nkeys; ++key) sum[0] += load16<BF16>(a.v, v_base + key * v_stride + d);
+        }
+        const float mv = nkeys > 0 ? ((sum[0] + sum[1]) + (sum[2] + sum[3])) / (float)nkeys : 0.f;
+#pragma unroll 1
+        for (int e = 0; e < 32 && d0 + e < a.D; ++e) {
+            const float m = __shfl_sync(0xffffffffu, mv, e);
+            if (mine) orow_p[d0 + e] = (uint16_t)(pack2<BF16>(m, 0.f) & 0xffffu);
+        }
+    }
 }
 
 template <bool BF16, bool BIAS_F32, bool VARLEN, bool FOLD>
@@ -351,7 +442,8 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
     const int S = P.kv_stages;
     const int BS = P.bias_stages;
     const int QB = P.q_bufs;
-    const int SB = P.s_bufs;
+    constexpr int SB = 3;                        // S buffers (P.s_bufs)
+    const int OB = VARLEN ? P.o_bufs : 2;        // O accumulators: 2 with D <= 64, else 1
     auto bar = [&](int idx) -> uint32_t { return base + L.bars + 8u * (uint32_t)idx; };
     auto q_full = [&](int qb) { return bar(qb); };
     auto q_empty = [&](int qb) { return bar(QB + qb); };
@@ -367,6 +459,10 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
     auto pv_done = [&](uint32_t n) { return bar(bx0 + 2 * SB + (int)(n & 1u)); };  // PV n: phase n / 2 of barrier n % 2
     auto xchg = [&](int q) { return bar(bx0 + 2 * SB + 2 + q); };
     const uint32_t drain = bar(bx0 + 2 * SB + 6);
+    const uint32_t o_empty = bar(bx0 + 2 * SB + 7);  // one O accumulator: the softmax has read it
+    const RingRef ring = {base + L.ring, abort_flag};
+    auto ring_full = [&](int i) { return base + L.ring + 8u * (uint32_t)i; };
+    auto ring_empty = [&](int i) { return base + L.ring + 8u * (uint32_t)(kRing + i); };
 
     auto q_smem = [&](int qb) { return base + L.q + (uint32_t)qb * P.tile_bytes; };
     auto k_smem = [&](int s) { return base + L.kv + (uint32_t)s * 2u * P.tile_bytes; };
@@ -420,6 +516,14 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
         mbar_init(pv_done(1), 1);
         for (int q = 0; q < 4; ++q) mbar_init(xchg(q), 2);  // the two warps of a lane quarter
         mbar_init(drain, 1);
+        mbar_init(o_empty, 8);  // one arrival per softmax warp
+        if (VARLEN) {
+#pragma unroll 1
+            for (int i = 0; i < kRing; ++i) {
+                mbar_init(ring_full(i), 1);
+                mbar_init(ring_empty(i), kRingConsumers);
+            }
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
@@ -439,9 +543,9 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
         StageRing kr = {0, 0u, false}, qr = {0, 0u, false};
         bool ok = true;
         ItemWalk<VARLEN> walk;
-        walk.begin(P);
+        walk.begin(P, ring);
         SItem it;
-        while (ok && walk.next(P, sched, it)) {
+        while (ok && walk.next(P, ring, it)) {
             if (it.nkt == 0) continue;
             const int qb = qr.idx;
             if (lane == 0 && qr.wrapped) ok = wait_bar(q_empty(qb), qr.ph ^ 1u, abort_flag, a.status);
@@ -451,7 +555,8 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
                 mbar_expect_tx(q_full(qb), P.tile_bytes);
                 for (int sb = 0; sb < P.nsub; ++sb) {
                     if constexpr (!VARLEN)
-                        tma_load_3d(q_smem(qb) + sb * kBox, &P.tm_q, sb * 64, it.qt * kBM, (int)it.unit, q_full(qb));
+                        tma_load_tri(P, q_smem(qb) + sb * kBox, &P.tm_q, sb * 64, it.qt * kBM, it.unit, it.h,
+                                     (int)(it.bn - (long long)it.b * a.N), it.b, q_full(qb));
                     else
                         tma_load_3d(q_smem(qb) + sb * kBox, &P.tm_q, sb * 64, it.h, it.q_row0 + it.qt * kBM,
                                     q_full(qb));
@@ -470,7 +575,8 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
                     mbar_expect_tx(k_full(st), P.tile_bytes);
                     for (int sb = 0; sb < P.nsub; ++sb) {
                         if constexpr (!VARLEN)
-                            tma_load_3d(k_smem(st) + sb * kBox, &P.tm_k, sb * 64, kb * kBN, (int)it.unit, k_full(st));
+                            tma_load_tri(P, k_smem(st) + sb * kBox, &P.tm_k, sb * 64, kb * kBN, it.unit, it.h,
+                                         (int)(it.bn - (long long)it.b * a.N), it.b, k_full(st));
                         else
                             tma_load_3d(k_smem(st) + sb * kBox, &P.tm_k, sb * 64, it.h, it.k_row0 + kb * kBN,
                                         k_full(st));
@@ -485,9 +591,9 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
         StageRing vr = {0, 0u, false};
         bool ok = true;
         ItemWalk<VARLEN> walk;
-        walk.begin(P);
+        walk.begin(P, ring);
         SItem it;
-        while (ok && walk.next(P, sched, it)) {
+        while (ok && walk.next(P, ring, it)) {
             TileWalk tw = tiles_begin<VARLEN>(it);
             int kb;
             bool fb;
@@ -500,7 +606,8 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
                     mbar_expect_tx(v_full(st), P.tile_bytes);
                     for (int sb = 0; sb < P.nsub; ++sb) {
                         if constexpr (!VARLEN)
-                            tma_load_3d(v_smem(st) + sb * kBox, &P.tm_v, sb * 64, kb * kBN, (int)it.unit, v_full(st));
+                            tma_load_tri(P, v_smem(st) + sb * kBox, &P.tm_v, sb * 64, kb * kBN, it.unit, it.h,
+                                         (int)(it.bn - (long long)it.b * a.N), it.b, v_full(st));
                         else
                             tma_load_3d(v_smem(st) + sb * kBox, &P.tm_v, sb * 64, it.h, it.k_row0 + kb * kBN,
                                         v_full(st));
@@ -511,7 +618,53 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
         }
         if (!ok) *abort_flag = 1;
     } else if (warp == kBiasWarp) {
-        if constexpr (!VARLEN) {
+        if constexpr (VARLEN) {
+            // ------------------------------------------------------------ scheduler
+            // Walks this CTA's (sequence, head, q block) items, decodes each (its
+            // lists and visited-tile count, warp-cooperatively) and hands it to
+            // the other roles through the ring; an entry with nkt < 0 ends it.
+            StageRing rr = {0, 0u, false};
+            VCursor vc = vcursor_begin(P);
+            VEntry* ents = reinterpret_cast<VEntry*>(gbase + L.ring + 16u * kRing);
+            bool ok = true;
+            for (;;) {
+                int seq = 0, hh = 0, qb = 0;
+                const bool more = vcursor_next(P, sched + 2 * (a.num_seqs + 1), vc, seq, hh, qb);
+                const int slot = rr.idx;
+                if (rr.wrapped) {
+                    ok = __all_sync(0xffffffffu, wait_bar(ring_empty(slot), rr.ph ^ 1u, abort_flag, a.status));
+                    if (!ok) break;
+                }
+                SItem it;
+                if (more) it = split_decode<true>(P, sched, 0, seq, hh, qb);
+                if (lane == 0) {
+                    VEntry* e = ents + slot;
+                    e->nkt = more ? it.nkt : -1;
+                    if (more) {
+                        e->seq = seq;
+                        e->h = hh;
+                        e->qb = qb;
+                        e->q_row0 = it.q_row0;
+                        e->Lq = it.Lq;
+                        e->k_row0 = it.k_row0;
+                        e->Lk = it.Lk;
+                        e->nkb = it.nkb;
+                        e->n_part = it.n_part;
+                        e->n_full = it.n_full;
+                        e->lists = it.lists ? 1 : 0;
+                        e->part_l = it.part_l;
+                        e->full_l = it.full_l;
+                        e->part0 = it.part0;
+                        e->full0 = it.full0;
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ring_full(slot));  // release: the entry is written
+                rr.next(kRing);
+                if (!more) break;
+            }
+            if (!ok) *abort_flag = 1;
+        } else {
             // ---------------------------------- producer: bias tiles (+ dense-mask bits)
             StageRing br = {0, 0u, false};
             bool ok = true;
@@ -549,49 +702,77 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
         // ------------------------------------------------------------------ MMA
         // Two cursors over the CTA's items with key tiles: `qc` for the next
         // QK^T, `pc` for the next PV.  Tile n of the stream (counted over
-        // items) has S buffer n % s_bufs and K/V stage n % S; item number i
-        // has Q buffer i % QB and O accumulator i % 2.
+        // items) has S buffer n % 3 and K/V stage n % S; item number i has Q
+        // buffer i % QB and O accumulator i % o_bufs.  QK^T runs two tiles
+        // ahead: once P of tile n is in TMEM, PV of tile n (reading S buffer
+        // n % 3) and QK^T of tile n + 2 (into buffer (n + 2) % 3, whose PV was
+        // issued before) are issued interleaved, k step by k step.  The two
+        // chains have different accumulators, so the tensor core overlaps
+        // them instead of waiting on each chain's own accumulation.
         const bool leader = elect_one();
         SplitCursor<VARLEN> qc, pc;
-        qc.walk.begin(P);
+        qc.walk.begin(P, ring);
         qc.qi = 0;
-        bool has_q = split_seek<VARLEN>(P, sched, qc);
+        bool has_q = split_seek<VARLEN>(P, ring, qc);
         pc = qc;
         bool has_p = has_q;
         uint32_t np = 0;                                    // PV issued so far
         StageRing qr = {0, 0u, false};                      // Q buffer of qc's item
         StageRing kq = {0, 0u, false}, sq = {0, 0u, false};  // K stage / S buffer of the next QK^T
         StageRing vp = {0, 0u, false}, sp = {0, 0u, false};  // V stage / S buffer of the next PV
+        StageRing oe = {0, 0u, false};                      // single O accumulator: its "read" barrier
         bool ok = true;
         auto kstep = [](int kk) -> uint64_t { return (uint64_t)(((kk >> 2) * kBox + (kk & 3) * 32) >> 4); };
-        auto issue_qk = [&]() -> bool {
-            if (!has_q) return true;
-            const int qb = qr.idx;
-            if (qc.t == 0 && !__all_sync(0xffffffffu, wait_bar(q_full(qb), qr.ph, abort_flag, a.status))) return false;
-            const int st = kq.idx;
-            if (!__all_sync(0xffffffffu, wait_bar(k_full(st), kq.ph, abort_flag, a.status))) return false;
-            tc_fence_after();
-            const uint64_t qd = sw128_desc(q_smem(qb), 16, 1024);
-            const uint64_t kd = sw128_desc(k_smem(st), 16, 1024);
-            const int b = sq.idx;
-            const uint32_t sd = tmem + 128u * (uint32_t)b;
+        // QK^T of the next tile: wait for its Q (first tile of an item) and K stage.
+        uint64_t qd = 0, kd = 0;
+        uint32_t sd = 0;
+        int q_qb = 0, q_st = 0, q_b = 0;
+        auto qk_ready = [&]() -> bool {
+            q_qb = qr.idx;
+            if (qc.t == 0 && !__all_sync(0xffffffffu, wait_bar(q_full(q_qb), qr.ph, abort_flag, a.status)))
+                return false;
+            q_st = kq.idx;
+            if (!__all_sync(0xffffffffu, wait_bar(k_full(q_st), kq.ph, abort_flag, a.status))) return false;
+            qd = sw128_desc(q_smem(q_qb), 16, 1024);
+            kd = sw128_desc(k_smem(q_st), 16, 1024);
+            q_b = sq.idx;
+            sd = tmem + 128u * (uint32_t)q_b;
+            return true;
+        };
+        // Commits and cursor moves once the QK^T's MMAs are issued.
+        auto qk_done = [&]() {
             if (leader) {
-                mma_ss(sd, qd, kd, P.idesc_qk, 0u);
-                for (int kk = 1; kk < P.ksteps; ++kk) mma_ss(sd, qd + kstep(kk), kd + kstep(kk), P.idesc_qk, 1u);
-                mma_commit(s_full(b));
-                mma_commit(k_empty(st));
+                mma_commit(s_full(q_b));
+                mma_commit(k_empty(q_st));
             }
             kq.next(S);
             sq.next(SB);
             if (++qc.t == qc.nkt) {
-                if (leader) mma_commit(q_empty(qb));  // every QK^T of the item is issued
+                if (leader) mma_commit(q_empty(q_qb));  // every QK^T of the item is issued
                 qr.next(QB);
                 ++qc.qi;
-                has_q = split_seek<VARLEN>(P, sched, qc);
+                has_q = split_seek<VARLEN>(P, ring, qc);
             }
-            return true;
         };
-        for (int i = 0; i < SB && ok; ++i) ok = issue_qk();
+        auto qk_alone = [&]() {
+            tc_fence_after();
+            if (leader) {
+#pragma unroll 1
+                for (int kk = 0; kk < P.ksteps; ++kk)
+                    mma_ss(sd, qd + kstep(kk), kd + kstep(kk), P.idesc_qk, kk > 0 ? 1u : 0u);
+            }
+            qk_done();
+        };
+        // Packed form (D up to 128, the MMA warp sets the pace): PV of tile n and
+        // QK^T of tile n + 2 interleaved.  Triangle form (D <= 64, the softmax sets
+        // the pace): PV of tile n, then QK^T of tile n + 3 into the buffer it read,
+        // which keeps three tiles of S ahead of the softmax.
+        constexpr bool kInterleave = VARLEN;
+        for (int i = 0; i < (kInterleave ? 2 : 3) && ok && has_q; ++i) {
+            ok = qk_ready();
+            if (!ok) break;
+            qk_alone();
+        }
         while (ok && has_p) {
             const int b = sp.idx;
             const int st = vp.idx;
@@ -602,26 +783,45 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
                 ok = __all_sync(0xffffffffu, wait_bar(v_full(st), vp.ph, abort_flag, a.status));
                 if (!ok) break;
             }
+            // With one O accumulator, the first PV of an item waits until the
+            // softmax has read out the previous item's O.
+            if (OB == 1 && pc.t == 0 && pc.qi > 0) {
+                ok = __all_sync(0xffffffffu, wait_bar(o_empty, oe.ph, abort_flag, a.status));
+                if (!ok) break;
+                oe.next(1);
+            }
+            const bool qk = kInterleave && has_q;
+            if (qk) {
+                ok = qk_ready();
+                if (!ok) break;
+            }
             tc_fence_after();
             const uint64_t vd = sw128_desc(v_smem(st), kBox, 1024);
-            const uint32_t d = tmem + P.o_col0 + (pc.qi & 1u) * P.o_cols;
+            const uint32_t d = tmem + P.o_col0 + (OB == 1 ? 0u : (pc.qi & 1u)) * P.o_cols;
             const uint32_t pa = tmem + 128u * (uint32_t)b;
             if (leader) {
+                const int nk = qk ? P.ksteps : 0;
 #pragma unroll 1
-                for (int kk = 0; kk < kBN / 16; ++kk)
+                for (int kk = 0; kk < kBN / 16; ++kk) {
                     mma_ts(d, pa + kk * 8, vd + (uint64_t)kk * 128, P.idesc_pv, (pc.t > 0 || kk > 0) ? 1u : 0u);
+                    if (kk < nk) mma_ss(sd, qd + kstep(kk), kd + kstep(kk), P.idesc_qk, kk > 0 ? 1u : 0u);
+                }
                 mma_commit(pv_done(np));
                 mma_commit(v_empty(st));
             }
+            if (qk) qk_done();
             ++np;
             sp.next(SB);
             vp.next(S);
             if (++pc.t == pc.nkt) {
                 ++pc.qi;
-                has_p = split_seek<VARLEN>(P, sched, pc);
+                has_p = split_seek<VARLEN>(P, ring, pc);
             }
-            // The buffer just multiplied by V takes the S s_bufs tiles on.
-            ok = issue_qk();
+            if (!kInterleave && has_q) {  // the buffer just multiplied by V takes the S three tiles on
+                ok = qk_ready();
+                if (!ok) break;
+                qk_alone();
+            }
         }
         if (!ok && leader) *abort_flag = 1;
         if (leader) mma_commit(drain);
@@ -670,9 +870,11 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
         // so a parity wait is exact while that barrier is neither a phase ahead
         // (PV n + 2 done) nor behind (PV n - 2 not done).  The callers hold:
         // this warp has not given P of tile n + 2, and PV n - 2 finished
-        // before the S it last read (S of tile m is issued after PV m - s_bufs,
-        // s_bufs <= 3).  With `prev`, PV n - 1 is waited for first, which
-        // covers a caller that only knows PV n - 3 finished.
+        // before the S it last read (QK^T of tile m is issued after PV m - 3,
+        // or with PV m - 2 in the interleaved order, and its commit completes
+        // only when every MMA issued before it has).  With `prev`, PV n - 1 is
+        // waited for first, which covers a caller that only knows PV n - 3
+        // finished.
         auto wait_pv = [&](uint32_t n, bool prev) -> bool {
             if (prev && n > 0 &&
                 !__all_sync(0xffffffffu, wait_bar(pv_done(n - 1u), ((n - 1u) >> 1) & 1, abort_flag, a.status)))
@@ -680,33 +882,6 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
             if (!__all_sync(0xffffffffu, wait_bar(pv_done(n), (n >> 1) & 1, abort_flag, a.status))) return false;
             tc_fence_after();
             return true;
-        };
-
-        // Mean of V over `nkeys` keys for the rows of this warp that need it
-        // (lane l forms the means of columns l, l + 32, ...; rows take them by
-        // shuffles), or zeros when there are no keys.
-        auto write_mean_v = [&](uint16_t* orow_p, long long v_base, long long v_stride, int nkeys, bool mine) {
-#pragma unroll 1
-            for (int d0 = 0; d0 < a.D; d0 += 32) {
-                const int d = d0 + lane;
-                float sum[4] = {0.f, 0.f, 0.f, 0.f};
-                if (d < a.D) {
-                    int key = 0;
-#pragma unroll 1
-                    for (; key + 4 <= nkeys; key += 4) {
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) sum[u] += load16<BF16>(a.v, v_base + (key + u) * v_stride + d);
-                    }
-#pragma unroll 1
-                    for (; key < nkeys; ++key) sum[0] += load16<BF16>(a.v, v_base + key * v_stride + d);
-                }
-                const float mv = nkeys > 0 ? ((sum[0] + sum[1]) + (sum[2] + sum[3])) / (float)nkeys : 0.f;
-#pragma unroll 1
-                for (int e = 0; e < 32 && d0 + e < a.D; ++e) {
-                    const float m = __shfl_sync(0xffffffffu, mv, e);
-                    if (mine) orow_p[d0 + e] = (uint16_t)(pack2<BF16>(m, 0.f) & 0xffffu);
-                }
-            }
         };
 
         // The epilogue of the previous item, run after the first tile of the
@@ -718,7 +893,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
         // over all keys, formed directly by the h == 0 warp.
         // Where a row's outputs go: (out element offset, lse/max index, V's first
         // element, V's key stride, keys).  Triangle form: row0 = the flat
-        // (b,n,h,q) row, unit0 = the (b,n,h) slab; packed form: row0 = the
+        // (b,n,h,q) row, unit0 = the slab's first V element; packed form: row0 = the
         // packed query row, unit0 = the sequence's first key row, hh = the head,
         // nk = its keys.
         struct RowAddr {
@@ -730,8 +905,8 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
             if constexpr (!VARLEN) {
                 ra.out_off = row0 * a.D;
                 ra.lse_idx = row0;
-                ra.v_base = unit0 * a.K * a.D;
-                ra.v_stride = a.D;
+                ra.v_base = unit0;  // the slab's first V element (the caller passes it)
+                ra.v_stride = a.vs[3];
                 ra.nkeys = a.K;
             } else {
                 ra.out_off = (row0 * a.H + hh) * a.D;
@@ -767,7 +942,21 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
             uint16_t* op = orow_p + (long long)h * half_o;
             const float inv = l_all > 0.f ? 1.f / l_all : 0.f;
             const int dlim = a.D - h * (int)half_o;  // columns of this half that exist
-            if (half_o % 32 == 0) {  // 32 of this warp's columns per load
+            if (half_o == 32) {  // D in (48, 64]: this warp's 32 columns in one load
+                uint32_t o[32];
+                tmem_ld_x32(oa, o);
+                uint32_t wv[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    wv[e] = pack2<BF16>(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+                if (pe.row_ok && !pe.direct) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        if (8 * i < dlim)
+                            reinterpret_cast<uint4*>(op)[i] =
+                                make_uint4(wv[4 * i], wv[4 * i + 1], wv[4 * i + 2], wv[4 * i + 3]);
+                }
+            } else if (VARLEN && half_o % 32 == 0) {  // D > 64: 32 of this warp's columns per load
 #pragma unroll 1
                 for (uint32_t c0 = 0; c0 < half_o; c0 += 32) {
                     uint32_t o[32];
@@ -797,19 +986,26 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
                         *reinterpret_cast<uint4*>(op + c0) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
                 }
             }
+            if (OB == 1) {
+                // Every load of O has completed (tcgen05.wait::ld in the loads): the
+                // accumulator may take the next item's first PV.
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(o_empty);
+            }
             if (h == 0 && __any_sync(0xffffffffu, pe.direct && pe.row_ok))
-                write_mean_v(orow_p, ra.v_base, ra.v_stride, ra.nkeys, pe.direct && pe.row_ok);
+                split_mean_v<BF16>(a, orow_p, ra.v_base, ra.v_stride, ra.nkeys, pe.direct && pe.row_ok);
             return true;
         };
 
         uint32_t qi = 0;  // items with key tiles so far: O accumulator qi % 2
         ItemWalk<VARLEN> walk;
-        walk.begin(P);
+        walk.begin(P, ring);
         SItem it;
-        while (ok && walk.next(P, sched, it)) {
+        while (ok && walk.next(P, ring, it)) {
             const int qrow = it.qt * kBM + r;  // local query row
             const bool row_ok = qrow < it.Lq;
-            if (it.nkt == 0) {
+            if (VARLEN && it.nkt == 0) {
                 // Packed form, a q block that visits no key block: every logit is
                 // -1e9 (mean of V over the sequence's keys), or there are no keys
                 // (O = 0, lse = max = -inf).
@@ -820,12 +1016,12 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
                         if (a.mx) a.mx[ra.lse_idx] = ra.nkeys > 0 ? kMasked : -INFINITY;
                     }
                     if (__any_sync(0xffffffffu, row_ok))
-                        write_mean_v(static_cast<uint16_t*>(a.out) + ra.out_off, ra.v_base, ra.v_stride, ra.nkeys,
-                                     row_ok);
+                        split_mean_v<BF16>(a, static_cast<uint16_t*>(a.out) + ra.out_off, ra.v_base, ra.v_stride,
+                                           ra.nkeys, row_ok);
                 }
                 continue;
             }
-            const uint32_t ob = qi & 1u;
+            const uint32_t ob = OB == 1 ? 0u : (qi & 1u);
             ++qi;
             const uint32_t o_taddr = o_base + ob * P.o_cols;
             float m_true = -INFINITY, m_ref = 0.f, l = 0.f;
@@ -1033,7 +1229,8 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
             pe.m_true = m_true;
             if constexpr (!VARLEN) {
                 pe.row0 = it.unit * a.Q + qrow;
-                pe.unit0 = it.unit;
+                pe.unit0 = (long long)it.b * a.vs[0] + (it.bn - (long long)it.b * a.N) * a.vs[1] +
+                           (long long)it.h * a.vs[2];
             } else {
                 pe.row0 = (long long)it.q_row0 + qrow;
                 pe.unit0 = it.k_row0;

@@ -75,6 +75,26 @@ def test_triangle_host_checks(lib, kw, exc):
         _fwd(**kw)()
 
 
+def _fwd_strided(**kw):
+    args = dict(q=A, k=A, v=A, qkv_dtype=abi.TA_BF16, bias=A, bias_dtype=abi.TA_BF16, mask=0, kv_lengths=0, B=1, N=2,
+                H=2, Q=64, K=64, D=64, scale=0.125, q_strides=None, k_strides=None, v_strides=None, out=A, lse=0,
+                max_=0, stream=0)
+    args.update(kw)
+    return lambda: abi.tri_attn_fwd_strided(**args)
+
+
+@pytest.mark.parametrize("kw,exc", [
+    (dict(q_strides=(8192, 4096, 64, 0)), ValueError),           # a stride below 1
+    (dict(k_strides=(8192, 4096, 2048, 32)), ValueError),        # rows of 64 elements 32 apart overlap
+    (dict(v_strides=(8192, 4096, 2048, 68)), NotImplementedError),  # 136-byte rows: not a 16-byte multiple
+    (dict(q_strides=(1 << 40, 4096, 2048, 64)), NotImplementedError),
+    (dict(q=MIS, q_strides=(8192, 4096, 2048, 64)), ValueError),
+])
+def test_triangle_strided_host_checks(lib, kw, exc):
+    with pytest.raises(exc):
+        _fwd_strided(**kw)()
+
+
 def _varlen(**kw):
     args = dict(q=A, k=A, v=A, dtype=abi.TA_BF16, cu_seqlens_q=A, cu_seqlens_k=A, num_seqs=2, total_q=400, total_k=400, max_seqlen_q=256,
                 max_seqlen_k=256, H=2, D=64, scale=0.125, kv_num_blocks=A, kv_indices=A, full_kv_num_blocks=A,

@@ -109,6 +109,34 @@ def test_dense_mask_wide_heads(D, dtype, bias_dtype):
     check_triangle(c)
 
 
+# Strided q / k / v (the triangle form read in place): a (B,N,Q,H,D) buffer viewed as
+# (B,N,H,Q,D), and rows padded past D; on the key-split kernel (D <= 64), the two-tile
+# kernel (D > 64) and the fp32 CUDA-core kernel.  Same result as the contiguous copy.
+@pytest.mark.parametrize("D,dtype", [(64, "bf16"), (32, "f16"), (128, "bf16"), (16, "f32")])
+def test_triangle_strided_views(D, dtype):
+    c = synth.make_triangle(f"strided_D{D}", 2, 3, 2, 150, 136, D, dtype, dtype, seed=720 + D, mask="kvlen",
+                            kv_range=(0, 136))
+    import masked_attention_tri_gb300 as ta
+    q, k, v, bias, kl = (t.cuda() for t in (c.q, c.k, c.v, c.bias, c.kv_lengths))
+    # q: transposed from (B,N,Q,H,D); k: rows padded to D + 8; v: transposed and padded
+    qt = torch.empty(c.B, c.N, c.Q, c.H, D, dtype=q.dtype, device="cuda")
+    qt.copy_(q.transpose(2, 3))
+    kp = torch.full((c.B, c.N, c.H, c.K, D + 8), 7.0, dtype=k.dtype, device="cuda")
+    kp[..., :D] = k
+    vt = torch.full((c.B, c.N, c.K, c.H, D + 8), -3.0, dtype=v.dtype, device="cuda")
+    vt[..., :D].copy_(v.transpose(2, 3))
+    qv, kv_, vv = qt.transpose(2, 3), kp[..., :D], vt[..., :D].transpose(2, 3)
+    assert not qv.is_contiguous() and not kv_.is_contiguous() and not vv.is_contiguous()
+    o1, l1, m1 = ta.triangle_attention(qv, kv_, vv, bias, scale=c.scale, return_aux=True, kv_lengths=kl)
+    o0, l0, m0 = ta.triangle_attention(q, k, v, bias, scale=c.scale, return_aux=True, kv_lengths=kl)
+    torch.cuda.synchronize()
+    assert ta.get_status() == 0
+    assert o1.is_contiguous()
+    assert torch.equal(o1, o0) and torch.equal(l1, l0) and torch.equal(m1, m0)
+    rO, rL, rM = oracle.tri_fwd(c.q, c.k, c.v, c.bias, kv_lengths=c.kv_lengths, scale=c.scale)
+    compare(c.name, c.dtype, o1, l1, m1, rO, rL, rM)
+
+
 @pytest.mark.parametrize("D", [4, 12, 32, 100, 128])
 def test_fp32_head_dims(D):
     c = synth.make_triangle(f"f32_D{D}", 1, 2, 2, 45, 70, D, "f32", "f32", seed=400 + D, mask="kvlen",
