@@ -118,7 +118,11 @@ bool choose_geometry(TcParams& P, bool varlen, int& NQ) {
 bool choose_split_geometry(TcParams& P, bool varlen) {
     const int prefs[][3] = {{2, 3, 2}, {2, 3, 1}, {2, 2, 2}, {2, 2, 1}, {1, 2, 1}};
     P.s_bufs = 3;
-    P.o_bufs = P.o_cols <= 64 ? 2 : 1;
+    // 128 columns for O after the S buffers: packed form, one O of o_cols per set; triangle
+    // form, one per key half (two per set)
+    const uint32_t per_set = (varlen ? 1u : 2u) * P.o_cols;
+    P.o_bufs = per_set * 2 <= 128 ? 2 : 1;
+    if (per_set > 128) return false;
     for (const auto& pr : prefs) {
         P.q_bufs = pr[0];
         P.kv_stages = pr[1];

@@ -81,8 +81,10 @@ __host__ __device__ inline SplitLayout make_split_layout(const TcParams& P) {
     L.kv = L.q + P.q_bufs * P.tile_bytes;
     L.bias = L.kv + P.kv_stages * 2 * P.tile_bytes;
     L.maskw = L.bias + P.bias_stages * P.bias_bytes;
-    L.xbuf = L.maskw + P.bias_stages * 16;   // row maxima: [tile parity][key half][128 rows] fp32
-    L.xl = L.xbuf + 2 * 2 * 128 * 4;           // row sums: [key half][128 rows] fp32
+    // shared O: row maxima [tile parity][key half][128 rows]; split O: the epilogue's
+    // (reference max, sum, max) [item parity][key half][3][128 rows] (fp32)
+    L.xbuf = L.maskw + P.bias_stages * 16;
+    L.xl = L.xbuf + 2 * 2 * 3 * 128 * 4;       // row sums: [key half][128 rows] fp32
     L.sched = L.xl + 2 * 128 * 4;              // packed form: cu_q[S+1], cu_k[S+1], q blocks[S] (int32)
     const uint32_t sched_bytes = P.a.varlen ? (uint32_t)(3 * P.a.num_seqs + 2) * 4u : 0u;
     // ring: ring_full[kRing], ring_empty[kRing] (8-byte mbarriers), then the entries
@@ -443,7 +445,12 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
     const int BS = P.bias_stages;
     const int QB = P.q_bufs;
     constexpr int SB = 3;                        // S buffers (P.s_bufs)
-    const int OB = VARLEN ? P.o_bufs : 2;        // O accumulators: 2 with D <= 64, else 1
+    const int OB = P.o_bufs;                     // O accumulator sets (items alternate between them)
+    // Triangle form: each key half accumulates its own O (P of keys [64h, 64h + 64)
+    // times those V rows), so the two softmax warps of a lane quarter need no
+    // shared row max per tile; the halves are combined once per item.  Packed
+    // form (D up to 128, no room for two halves): one O, shared row max.
+    constexpr bool kSplitO = !VARLEN;
     auto bar = [&](int idx) -> uint32_t { return base + L.bars + 8u * (uint32_t)idx; };
     auto q_full = [&](int qb) { return bar(qb); };
     auto q_empty = [&](int qb) { return bar(QB + qb); };
@@ -797,14 +804,26 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
             }
             tc_fence_after();
             const uint64_t vd = sw128_desc(v_smem(st), kBox, 1024);
-            const uint32_t d = tmem + P.o_col0 + (OB == 1 ? 0u : (pc.qi & 1u)) * P.o_cols;
+            const uint32_t oset = OB == 1 ? 0u : (pc.qi & 1u);
+            const uint32_t d = tmem + P.o_col0 + oset * (kSplitO ? 2u : 1u) * P.o_cols;
             const uint32_t pa = tmem + 128u * (uint32_t)b;
             if (leader) {
-                const int nk = qk ? P.ksteps : 0;
+                if constexpr (kSplitO) {
+                    // keys 0-63 into O_0, 64-127 into O_1, alternating (two independent chains)
 #pragma unroll 1
-                for (int kk = 0; kk < kBN / 16; ++kk) {
-                    mma_ts(d, pa + kk * 8, vd + (uint64_t)kk * 128, P.idesc_pv, (pc.t > 0 || kk > 0) ? 1u : 0u);
-                    if (kk < nk) mma_ss(sd, qd + kstep(kk), kd + kstep(kk), P.idesc_qk, kk > 0 ? 1u : 0u);
+                    for (int j = 0; j < kBN / 16; ++j) {
+                        const int kk = (j >> 1) + 4 * (j & 1);
+                        // P of key half 1 sits in that half's own logit columns [64, 96)
+                        mma_ts(d + (uint32_t)(j & 1) * P.o_cols, pa + kk * 8 + (kk & 4) * 8, vd + (uint64_t)kk * 128,
+                               P.idesc_pv, (pc.t > 0 || (kk & 3) > 0) ? 1u : 0u);
+                    }
+                } else {
+                    const int nk = qk ? P.ksteps : 0;
+#pragma unroll 1
+                    for (int kk = 0; kk < kBN / 16; ++kk) {
+                        mma_ts(d, pa + kk * 8, vd + (uint64_t)kk * 128, P.idesc_pv, (pc.t > 0 || kk > 0) ? 1u : 0u);
+                        if (kk < nk) mma_ss(sd, qd + kstep(kk), kd + kstep(kk), P.idesc_qk, kk > 0 ? 1u : 0u);
+                    }
                 }
                 mma_commit(pv_done(np));
                 mma_commit(v_empty(st));
@@ -833,8 +852,11 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
         const int h = warp / 4;                // key half: keys [64h, 64h + 64) of each tile
         const int r = wq * 32 + lane;          // row within the q tile
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-        const uint32_t half_o = P.o_cols / 2;  // this warp's O columns: [h half_o, (h + 1) half_o)
-        const uint32_t o_base = tmem + lane_off + P.o_col0 + (uint32_t)h * half_o;  // + accumulator * o_cols
+        const uint32_t half_o = P.o_cols / 2;  // this warp's output columns: [h half_o, (h + 1) half_o)
+        // Split O (triangle): this warp's accumulator O_h of set ob at o_col0 + (2 ob + h) o_cols.
+        // Shared O (packed): this warp's columns of set ob at o_col0 + ob o_cols + h half_o.
+        const uint32_t o_base = tmem + lane_off + P.o_col0 + (uint32_t)h * (kSplitO ? P.o_cols : half_o);
+        const uint32_t o_set = (kSplitO ? 2u : 1u) * P.o_cols;  // columns between accumulator sets
         const uint32_t rsw = (uint32_t)(r & 7);  // 128B swizzle: chunk c of row r sits at chunk c ^ (r % 8)
         const uint32_t rrow = (uint32_t)r * 128u;
         uint32_t sn = 0, x_it = 0;  // sn: key tiles so far (the PV index)
@@ -926,30 +948,71 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
         } pe = {};
         bool pend = false;
         auto epilogue = [&](bool at_end) -> bool {
-            const float l_all = pe.l + swap(xl, pe.l);
-            if (!ok) return false;
+            // Combine the two key halves' (reference max, row sum, max).  Shared O:
+            // one reference max, the sums add.  Split O: each half's O and sum are
+            // scaled to the larger reference max (alpha = 2^((m_h - M) log2 e)).
+            float l_all, m_ref_all, m_true_all, a_own = 1.f, a_oth = 1.f;
+            if constexpr (kSplitO) {
+                float* xe = xbuf + (x_it & 1u) * 768u;  // [item parity][half][3][128 rows]
+                xe[(h * 3 + 0) * 128 + r] = pe.m_ref;
+                xe[(h * 3 + 1) * 128 + r] = pe.l;
+                xe[(h * 3 + 2) * 128 + r] = pe.m_true;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(xchg(wq));
+                const bool w_ok = __all_sync(0xffffffffu, wait_bar(xchg(wq), x_it & 1, abort_flag, a.status));
+                ++x_it;
+                if (!w_ok) return ok = false;
+                const int o3 = (1 - h) * 3;
+                const float m_oth = xe[(o3 + 0) * 128 + r], l_oth = xe[(o3 + 1) * 128 + r];
+                const float mt_oth = xe[(o3 + 2) * 128 + r];
+                m_ref_all = fmaxf(pe.m_ref, m_oth);
+                a_own = pe.m_ref == m_ref_all ? 1.f : ex2((pe.m_ref - m_ref_all) * kLog2e);
+                a_oth = m_oth == m_ref_all ? 1.f : ex2((m_oth - m_ref_all) * kLog2e);
+                l_all = a_own * pe.l + a_oth * l_oth;
+                m_true_all = fmaxf(pe.m_true, mt_oth);
+            } else {
+                l_all = pe.l + swap(xl, pe.l);
+                if (!ok) return false;
+                m_ref_all = pe.m_ref;
+                m_true_all = pe.m_true;
+            }
+            // (the two item-parity buffers: a warp overwrites a buffer only after the
+            // partner's next arrival, which follows its read of that buffer)
+            const bool direct = kSplitO ? (!(m_true_all > kMasked) && pe.direct) : pe.direct;
             const RowAddr ra = row_addr(pe.row0, pe.unit0, pe.hh, pe.nk);
             if (pe.row_ok && h == 0) {
-                float mr = pe.m_ref;
-                if constexpr (FOLD) mr = pe.m_ref > -FLT_MAX ? pe.m_ref * a.scale : kMasked;
-                const float lse = pe.direct ? kMasked + logf((float)ra.nkeys) : mr + logf(l_all);
+                float mr = m_ref_all;
+                if constexpr (FOLD) mr = m_ref_all > -FLT_MAX ? m_ref_all * a.scale : kMasked;
+                const float lse = direct ? kMasked + logf((float)ra.nkeys) : mr + logf(l_all);
                 if (a.lse) a.lse[ra.lse_idx] = lse;
-                if (a.mx) a.mx[ra.lse_idx] = pe.direct ? kMasked : pe.m_true;
+                if (a.mx) a.mx[ra.lse_idx] = direct ? kMasked : m_true_all;
             }
             if (!wait_pv(pe.n_last, at_end)) return false;
-            const uint32_t oa = o_base + pe.ob * P.o_cols;
+            // split O: this warp's output columns of O_0 (oa0) and O_1 (oa0 + o_cols)
+            const uint32_t oa = kSplitO ? tmem + lane_off + P.o_col0 + pe.ob * o_set + (uint32_t)h * half_o
+                                        : o_base + pe.ob * o_set;
             uint16_t* orow_p = static_cast<uint16_t*>(a.out) + ra.out_off;
             uint16_t* op = orow_p + (long long)h * half_o;
             const float inv = l_all > 0.f ? 1.f / l_all : 0.f;
+            // weights of O_0 and O_1 (split O), folded with 1 / l
+            const float w0 = (h == 0 ? a_own : a_oth) * inv, w1 = (h == 0 ? a_oth : a_own) * inv;
             const int dlim = a.D - h * (int)half_o;  // columns of this half that exist
             if (half_o == 32) {  // D in (48, 64]: this warp's 32 columns in one load
                 uint32_t o[32];
                 tmem_ld_x32(oa, o);
+                if constexpr (kSplitO) {
+                    uint32_t o1[32];
+                    tmem_ld_x32(oa + P.o_cols, o1);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        o[e] = __float_as_uint(__uint_as_float(o[e]) * w0 + __uint_as_float(o1[e]) * w1);
+                }
+                const float sc = kSplitO ? 1.f : inv;
                 uint32_t wv[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
-                    wv[e] = pack2<BF16>(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
-                if (pe.row_ok && !pe.direct) {
+                    wv[e] = pack2<BF16>(__uint_as_float(o[2 * e]) * sc, __uint_as_float(o[2 * e + 1]) * sc);
+                if (pe.row_ok && !direct) {
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
                         if (8 * i < dlim)
@@ -965,7 +1028,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
                         wv[e] = pack2<BF16>(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
-                    if (pe.row_ok && !pe.direct) {
+                    if (pe.row_ok && !direct) {
 #pragma unroll
                         for (int i = 0; i < 4; ++i)
                             if ((int)c0 + 8 * i < dlim)
@@ -978,11 +1041,19 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
                 for (uint32_t c0 = 0; c0 < half_o; c0 += 8) {
                     uint32_t o[8];
                     tmem_ld_x8(oa + c0, o);
+                    if constexpr (kSplitO) {
+                        uint32_t o1[8];
+                        tmem_ld_x8(oa + P.o_cols + c0, o1);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            o[e] = __float_as_uint(__uint_as_float(o[e]) * w0 + __uint_as_float(o1[e]) * w1);
+                    }
+                    const float sc = kSplitO ? 1.f : inv;
                     uint32_t wv[4];
 #pragma unroll
                     for (int e = 0; e < 8; e += 2)
-                        wv[e / 2] = pack2<BF16>(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
-                    if (pe.row_ok && !pe.direct && (int)c0 < dlim)
+                        wv[e / 2] = pack2<BF16>(__uint_as_float(o[e]) * sc, __uint_as_float(o[e + 1]) * sc);
+                    if (pe.row_ok && !direct && (int)c0 < dlim)
                         *reinterpret_cast<uint4*>(op + c0) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
                 }
             }
@@ -993,8 +1064,8 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
                 __syncwarp();
                 if (lane == 0) mbar_arrive(o_empty);
             }
-            if (h == 0 && __any_sync(0xffffffffu, pe.direct && pe.row_ok))
-                split_mean_v<BF16>(a, orow_p, ra.v_base, ra.v_stride, ra.nkeys, pe.direct && pe.row_ok);
+            if (h == 0 && __any_sync(0xffffffffu, direct && pe.row_ok))
+                split_mean_v<BF16>(a, orow_p, ra.v_base, ra.v_stride, ra.nkeys, direct && pe.row_ok);
             return true;
         };
 
@@ -1023,7 +1094,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
             }
             const uint32_t ob = OB == 1 ? 0u : (qi & 1u);
             ++qi;
-            const uint32_t o_taddr = o_base + ob * P.o_cols;
+            const uint32_t o_taddr = o_base + ob * o_set;
             float m_true = -INFINITY, m_ref = 0.f, l = 0.f;
             int jv = 0;
             const int prefix_lm = !VARLEN ? 0 : (a.prefix_len ? a.prefix_len[it.seq] : a.prefix_all);
@@ -1150,7 +1221,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
                     m3 = max3(m3, x[j + 6], x[j + 7]);
                 }
                 const float mh = fmaxf(max3(m0, m1, m2), m3);
-                const float tm = fmaxf(mh, swap(xbuf + (sn & 1u) * 256u, mh));
+                const float tm = kSplitO ? mh : fmaxf(mh, swap(xbuf + (sn & 1u) * 256u, mh));
                 if (!ok) break;
                 float tm_nat;  // the tile max as a logit (natural units)
                 if constexpr (FOLD) tm_nat = tm > -FLT_MAX ? tm * a.scale : (tm == -FLT_MAX ? kMasked : -INFINITY);
@@ -1171,7 +1242,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
                         const float alpha = ex2((m_ref - m_new) * unit_l2e);
                         l *= alpha;
                         m_ref = m_new;
-                        for (uint32_t c0 = 0; c0 < half_o; c0 += 8) {
+                        for (uint32_t c0 = 0; c0 < (kSplitO ? P.o_cols : half_o); c0 += 8) {
                             uint32_t o[8];
                             tmem_ld_x8(o_taddr + c0, o);
 #pragma unroll
@@ -1181,8 +1252,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
                     }
                 }
 
-                // ---- P for this warp's 64 keys into columns [32h, 32h + 32) of the
-                // buffer (after the swap, so the partner has read its logits).  A row
+                // ---- P for this warp's 64 keys into the S buffer (16-bit pairs).  A row
                 // with no real logit yet takes weights of exactly 1 for masked keys
                 // and 0 for absent ones: x + (-kMaskVal) is then 0 or -inf.
                 const bool live = m_ref > kMaskVal;
@@ -1199,7 +1269,10 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
                     else acc0 = __fadd2_rn(acc0, p);
                     pk[j] = pack2<BF16>(p.x, p.y);
                 }
-                tmem_st_x32(s_taddr + 32u * (uint32_t)h, pk);
+                // Split O: each key half writes P into the first 32 of its own 64 logit
+                // columns, so no warp overwrites values its partner has yet to read.
+                // Shared O: P of both halves in columns [0, 64), after the exchange.
+                tmem_st_x32(s_taddr + (kSplitO ? 64u : 32u) * (uint32_t)h, pk);
                 l += (acc0.x + acc0.y) + (acc1.x + acc1.y);
                 tmem_st_wait();
                 tc_fence_before();
@@ -1240,8 +1313,9 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
             pe.n_last = sn - 1u;
             pe.ob = ob;
             pe.row_ok = row_ok;
-            // (triangle form: every key block of K; packed form: of the sequence)
-            pe.direct = !(m_true > kMasked) && jv != (VARLEN ? it.nkb : (a.K + kBN - 1) / kBN);
+            // (triangle form: every key block of K; packed form: of the sequence).  Split O:
+            // only the "not every block" part here; the epilogue adds the combined max.
+            pe.direct = (kSplitO || !(m_true > kMasked)) && jv != (VARLEN ? it.nkb : (a.K + kBN - 1) / kBN);
             pend = true;
         }
         if (ok && pend) ok = epilogue(true);
