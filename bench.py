@@ -282,7 +282,8 @@ def time_varlen(ta, c, dev, steps, warmup, flush, qkv_packed=False):
     mm = {"causal": abi.TA_MASK_CAUSAL, "none": abi.TA_MASK_NONE}[c.mask_mod]
     argv = (_ptr(qq), _ptr(kk), _ptr(vv), _DT[q.dtype], _ptr(cu), _ptr(cu), len(c.lengths), q.shape[0], k.shape[0],
             c.max_seqlen, c.max_seqlen, H, D, c.scale, _ptr(kn), _ptr(ki), _ptr(fn), _ptr(fi), kn.shape[1],
-            kn.shape[2], ki.shape[3], c.block, c.block, mm, 0, None, 0, rs, rs, rs, _ptr(out), _ptr(lse), _ptr(mx),
+            kn.shape[2], ki.shape[3], c.block, c.block, mm, 0, None, 0, None, abi.TA_F32, rs, rs, rs, _ptr(out),
+            _ptr(lse), _ptr(mx),
             torch.cuda.current_stream(dev).cuda_stream)
 
     def launch():

@@ -155,7 +155,7 @@ ta_status tri_attn_fwd_strided(const void* q, const void* k, const void* v, ta_d
  *   mask_heads    1 (one mask for all heads) or H.
  *   block_q, block_k  must both be 128 (else TA_ERR_UNSUPPORTED).
  *   lse, max      optional (H, total_q) fp32.
- *   No bias.  A key row past the end of its sequence takes no part.  A
+ *   No bias here (tri_attn_varlen_fwd_masked takes one).  A key row past the end of its sequence takes no part.  A
  *   sequence with no keys gets O = 0 and lse = max = -inf.
  *
  * Supported: fp16/bf16 with D % 8 == 0, D <= 128 (tcgen05), fp32 with
@@ -206,7 +206,7 @@ ta_status tri_attn_varlen_fwd_strided(const void* q, const void* k, const void* 
 
 /*
  * tri_attn_varlen_fwd_masked -- tri_attn_varlen_fwd_strided with the
- * parameterised mask_mods.
+ * parameterised mask_mods and an optional post-scale bias.
  * (tensorplay nn.attention "BlockMask": from_kv_blocks(..., mask_mod=...) and
  *  Details 2, mask_mod applied on partial blocks only; the sliding-window and
  *  prefix-LM predicates are the two most common mask_mods besides causal.)
@@ -219,10 +219,18 @@ ta_status tri_attn_varlen_fwd_strided(const void* q, const void* k, const void* 
  *                   prefix of each sequence (values <= 0 keep only causal
  *                   keys); when NULL, `prefix_length` (>= 0, else
  *                   TA_ERR_INVALID_ARG) applies to every sequence
+ *   bias            optional post-scale bias (Transformer Engine fused_attn.h,
+ *                   NVTE_Bias_Type NVTE_POST_SCALE_BIAS): (H, max_seqlen_q,
+ *                   max_seqlen_k) of `bias_dtype` (TA_F32 or `dtype`, else
+ *                   TA_ERR_UNSUPPORTED), shared by every sequence and indexed
+ *                   by local positions: x = s * (Q . K) + bias[h, q, k] for a
+ *                   valid key (a masked key's logit is -1e9 as always).  16-byte
+ *                   aligned, and max_seqlen_k * its element size a multiple of
+ *                   16 bytes (else TA_ERR_UNSUPPORTED).  NULL = no bias.
  *   every other argument as in tri_attn_varlen_fwd_strided (which takes
- *   TA_MASK_NONE and TA_MASK_CAUSAL only).  A row whose visited keys are all
- *   masked gets the mean of V over the sequence's keys (every logit -1e9), as
- *   with any other mask.
+ *   TA_MASK_NONE and TA_MASK_CAUSAL only, and no bias).  A row whose visited
+ *   keys are all masked gets the mean of V over the sequence's keys (every
+ *   logit -1e9), as with any other mask.
  */
 ta_status tri_attn_varlen_fwd_masked(const void* q, const void* k, const void* v, ta_dtype dtype,
                                      const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
@@ -234,6 +242,7 @@ ta_status tri_attn_varlen_fwd_masked(const void* q, const void* k, const void* v
                                      int mask_heads, int max_q_blocks, int max_kv_blocks,
                                      int block_q, int block_k, ta_mask_mod mask_mod,
                                      int window, const int32_t* prefix_lengths, int prefix_length,
+                                     const void* bias, ta_dtype bias_dtype,
                                      long long q_row_stride, long long k_row_stride, long long v_row_stride,
                                      void* out, float* lse, float* max, void* stream);
 

@@ -55,7 +55,7 @@ def load() -> ctypes.CDLL:
                                                     I, I, L, L, L, P, P, P, P]
         lib.tri_attn_varlen_fwd_strided.restype = I
         lib.tri_attn_varlen_fwd_masked.argtypes = [P, P, P, I, P, P, I, I, I, I, I, I, I, F, P, P, P, P, I, I, I, I,
-                                                   I, I, I, P, I, L, L, L, P, P, P, P]
+                                                   I, I, I, P, I, P, I, L, L, L, P, P, P, P]
         lib.tri_attn_varlen_fwd_masked.restype = I
         lib.tri_attn_mask_to_kv_lengths.argtypes = [P, I, I, I, P, P, P]
         lib.tri_attn_mask_to_kv_lengths.restype = I
@@ -134,14 +134,14 @@ def tri_attn_varlen_fwd_strided(q, k, v, dtype, cu_seqlens_q, cu_seqlens_k, num_
 def tri_attn_varlen_fwd_masked(q, k, v, dtype, cu_seqlens_q, cu_seqlens_k, num_seqs, total_q, total_k,
                                max_seqlen_q, max_seqlen_k, H, D, scale, kv_num_blocks, kv_indices, full_kv_num_blocks,
                                full_kv_indices, mask_heads, max_q_blocks, max_kv_blocks, block_q, block_k, mask_mod,
-                               window, prefix_lengths, prefix_length, q_row_stride, k_row_stride, v_row_stride, out,
-                               lse, max_, stream) -> None:
+                               window, prefix_lengths, prefix_length, bias, bias_dtype, q_row_stride, k_row_stride,
+                               v_row_stride, out, lse, max_, stream) -> None:
     st = load().tri_attn_varlen_fwd_masked(q, k, v, dtype, cu_seqlens_q, cu_seqlens_k, num_seqs, total_q, total_k,
                                            max_seqlen_q, max_seqlen_k, H, D, float(scale), kv_num_blocks or None,
                                            kv_indices or None, full_kv_num_blocks or None, full_kv_indices or None,
                                            mask_heads, max_q_blocks, max_kv_blocks, block_q, block_k, mask_mod,
-                                           int(window), prefix_lengths or None, int(prefix_length),
-                                           int(q_row_stride), int(k_row_stride), int(v_row_stride), out,
+                                           int(window), prefix_lengths or None, int(prefix_length), bias or None,
+                                           int(bias_dtype), int(q_row_stride), int(k_row_stride), int(v_row_stride), out,
                                            lse or None, max_ or None, stream or None)
     _check(st, "tri_attn_varlen_fwd_masked")
 

@@ -279,7 +279,7 @@ def _row_stride(t: torch.Tensor, name: str, device: torch.device) -> int:
 
 
 def varlen_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, block_mask=None, scale=None,
-                     return_aux=False, *, mask_mod=None, out=None, window=0, prefix_lengths=None):
+                     return_aux=False, *, mask_mod=None, out=None, window=0, prefix_lengths=None, bias=None):
     """Packed-sequence forward with an optional BlockMask.
 
     q (total_q,H,D), k/v (total_k,H,D), cu_seqlens int32 (S+1,).  q, k, v may
@@ -289,7 +289,9 @@ def varlen_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seql
     block_mask every block is visited and ``mask_mod`` applies everywhere.
     mask_mod: None, "causal" (k <= q), "sliding_window" (q - window < k <= q)
     or "prefix_lm" (k <= q or k < the sequence's prefix; ``prefix_lengths`` is
-    an int or an int32 CUDA tensor with one length per sequence).
+    an int or an int32 CUDA tensor with one length per sequence).  bias: an
+    optional post-scale bias (H, max_seqlen_q, max_seqlen_k), float32 or q's
+    dtype, indexed by each sequence's local positions.
     Returns O, or (O, lse, max) with lse/max (H, total_q).
     """
     if q.dim() != 3 or k.dim() != 3 or v.dim() != 3:
@@ -343,6 +345,12 @@ def varlen_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seql
     if return_aux:
         lse = torch.empty(H, total_q, device=dev, dtype=torch.float32)
         mx = torch.empty(H, total_q, device=dev, dtype=torch.float32)
+    if bias is not None:
+        _need(bias, "bias", dev)
+        if tuple(bias.shape) != (H, int(max_seqlen_q), int(max_seqlen_k)):
+            raise ValueError(f"bias must be (H, max_seqlen_q, max_seqlen_k) = {(H, int(max_seqlen_q), int(max_seqlen_k))}")
+        if bias.dtype not in (torch.float32, q.dtype):
+            raise TypeError("bias must be float32 or q's dtype")
     pl, p_all = None, 0
     if isinstance(prefix_lengths, torch.Tensor):
         _need(prefix_lengths, "prefix_lengths", dev)
@@ -355,7 +363,8 @@ def varlen_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seql
         abi.tri_attn_varlen_fwd_masked(_ptr(q), _ptr(k), _ptr(v), _DT[q.dtype], _ptr(cu_seqlens_q),
                                        _ptr(cu_seqlens_k), S, total_q, k.shape[0], int(max_seqlen_q),
                                        int(max_seqlen_k), H, D, s, _ptr(kn), _ptr(ki), _ptr(fn), _ptr(fi),
-                                       mask_heads, MQ, MK, bq, bk, mm, int(window), _ptr(pl), p_all, q_rs, k_rs, v_rs,
+                                       mask_heads, MQ, MK, bq, bk, mm, int(window), _ptr(pl), p_all, _ptr(bias),
+                                       _DT[bias.dtype] if bias is not None else abi.TA_F32, q_rs, k_rs, v_rs,
                                        _ptr(out), _ptr(lse), _ptr(mx), _stream(dev))
     return (out, lse, mx) if return_aux else out
 

@@ -177,8 +177,8 @@ TA_EXPORT ta_status tri_attn_varlen_fwd_strided(const void* q, const void* k, co
     return tri_attn_varlen_fwd_masked(q, k, v, dtype, cu_seqlens_q, cu_seqlens_k, num_seqs, total_q, total_k,
                                       max_seqlen_q, max_seqlen_k, H, D, scale, kv_num_blocks, kv_indices,
                                       full_kv_num_blocks, full_kv_indices, mask_heads, max_q_blocks, max_kv_blocks,
-                                      block_q, block_k, mask_mod, 0, nullptr, 0, q_row_stride, k_row_stride,
-                                      v_row_stride, out, lse, max, stream);
+                                      block_q, block_k, mask_mod, 0, nullptr, 0, nullptr, TA_F32, q_row_stride,
+                                      k_row_stride, v_row_stride, out, lse, max, stream);
 }
 
 TA_EXPORT ta_status tri_attn_varlen_fwd_masked(const void* q, const void* k, const void* v, ta_dtype dtype,
@@ -190,6 +190,7 @@ TA_EXPORT ta_status tri_attn_varlen_fwd_masked(const void* q, const void* k, con
                                                int mask_heads, int max_q_blocks, int max_kv_blocks, int block_q,
                                                int block_k, ta_mask_mod mask_mod, int window,
                                                const int32_t* prefix_lengths, int prefix_length,
+                                               const void* bias, ta_dtype bias_dtype,
                                                long long q_row_stride, long long k_row_stride,
                                                long long v_row_stride, void* out, float* lse, float* max,
                                                void* stream) {
@@ -201,6 +202,15 @@ TA_EXPORT ta_status tri_attn_varlen_fwd_masked(const void* q, const void* k, con
     if (mask_mod == TA_MASK_SLIDING_WINDOW && window <= 0) return TA_ERR_INVALID_ARG;
     if (mask_mod == TA_MASK_PREFIX_LM && !prefix_lengths && prefix_length < 0) return TA_ERR_INVALID_ARG;
     if (prefix_lengths && !aligned(prefix_lengths, 4)) return TA_ERR_INVALID_ARG;
+    if (bias) {
+        // (H, max_seqlen_q, max_seqlen_k) of bias_dtype, read by the TMA: 16-byte aligned base
+        // and a 16-byte multiple for the row of max_seqlen_k elements
+        if (!valid_dtype(bias_dtype) || !aligned(bias, 16)) return TA_ERR_INVALID_ARG;
+        if (bias_dtype != TA_F32 && bias_dtype != dtype) return TA_ERR_UNSUPPORTED;
+        const int ebias = bias_dtype == TA_F32 ? 4 : 2;
+        if (((long long)max_seqlen_k * ebias) % 16 != 0) return TA_ERR_UNSUPPORTED;
+        if ((long long)max_seqlen_q * max_seqlen_k * 4 >= (1LL << 40)) return TA_ERR_UNSUPPORTED;
+    }
     if ((kv_num_blocks == nullptr) != (kv_indices == nullptr)) return TA_ERR_INVALID_ARG;
     if ((full_kv_num_blocks == nullptr) != (full_kv_indices == nullptr)) return TA_ERR_INVALID_ARG;
     if (full_kv_num_blocks && !kv_num_blocks) return TA_ERR_INVALID_ARG;
@@ -260,6 +270,8 @@ TA_EXPORT ta_status tri_attn_varlen_fwd_masked(const void* q, const void* k, con
     p.window = mask_mod == TA_MASK_SLIDING_WINDOW ? window : 0;
     p.prefix_len = mask_mod == TA_MASK_PREFIX_LM ? prefix_lengths : nullptr;
     p.prefix_all = mask_mod == TA_MASK_PREFIX_LM ? prefix_length : 0;
+    p.bias = bias;
+    p.bias_f32 = bias && bias_dtype == TA_F32;
     p.total_q = total_q;
     p.total_k = total_k;
     p.q_rs = q_row_stride;

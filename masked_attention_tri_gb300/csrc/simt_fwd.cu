@@ -69,8 +69,9 @@ struct SimtState {
     int D, Dp1, warp, lane;
     long long k_off, k_rs, v_off, v_rs;
     int Lk;
-    long long bias_row0;  // element offset of bias[b,0,h,q0,0] (triangle), -1 = none
+    long long bias_row0;  // element offset of the bias row of query q0 (key 0), -1 = none
     int bias_rs;
+    int rows;             // query rows of this CTA that exist (Lq - q0, at most kQT)
     int q0;               // first query row of the CTA (local index)
     int prefix_len;
     int prefix_lm;        // packed form, mask_mod prefix LM: the sequence's prefix length
@@ -129,7 +130,8 @@ __device__ void simt_tile(SimtState<T, BT>& st, int key0, int mode) {
             x = kMasked;
         } else {
             float b = 0.f;
-            if (st.bias_row0 >= 0) {
+            // (rows past the end of the queries read no bias: they may lie past the buffer)
+            if (st.bias_row0 >= 0 && st.warp * kRows + i < st.rows) {
                 const BT* bp = static_cast<const BT*>(p.bias);
                 b = to_f(bp[st.bias_row0 + (long long)(st.warp * kRows + i) * st.bias_rs + key]);
             }
@@ -239,6 +241,12 @@ __global__ void __launch_bounds__(kWarps * 32) simt_fwd_kernel(const AttnParams 
     }
     st.q0 = qt * kQT;
     if (st.q0 >= Lq) return;
+    st.rows = Lq - st.q0;
+    if (p.varlen && p.bias) {
+        // packed form: post-scale bias (H, max_seqlen_q, max_seqlen_k) at local positions
+        st.bias_row0 = ((long long)h * p.max_q + st.q0) * p.max_k;
+        st.bias_rs = p.max_k;
+    }
 
     for (int e = threadIdx.x; e < kQT * D; e += blockDim.x) {
         int r = e / D, d = e - r * D;

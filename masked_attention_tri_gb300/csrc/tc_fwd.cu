@@ -18,6 +18,7 @@ namespace tc {
 TRIATTN_TC_VARIANTS(TRIATTN_TC_EXTERN)
 TRIATTN_SPLIT_TRI_VARIANTS(TRIATTN_SPLIT_EXTERN)
 TRIATTN_SPLIT_VARLEN_VARIANTS(TRIATTN_SPLIT_EXTERN)
+TRIATTN_SPLIT_VARLEN_BIAS_VARIANTS(TRIATTN_SPLIT_EXTERN)
 
 namespace {
 
@@ -116,7 +117,7 @@ bool choose_geometry(TcParams& P, bool varlen, int& NQ) {
 // up to 64 columns or one of 128, in 512 tensor-memory columns; Q buffers,
 // K/V stages and bias stages as shared memory allows.
 bool choose_split_geometry(TcParams& P, bool varlen) {
-    const int prefs[][3] = {{2, 3, 2}, {2, 3, 1}, {2, 2, 2}, {2, 2, 1}, {1, 2, 1}};
+    const int prefs[][3] = {{2, 3, 2}, {2, 3, 1}, {2, 2, 2}, {2, 2, 1}, {1, 2, 2}, {1, 2, 1}, {1, 1, 1}};
     P.s_bufs = 3;
     // 128 columns for O after the S buffers: packed form, one O of o_cols per set; triangle
     // form, one per key half (two per set)
@@ -126,7 +127,7 @@ bool choose_split_geometry(TcParams& P, bool varlen) {
     for (const auto& pr : prefs) {
         P.q_bufs = pr[0];
         P.kv_stages = pr[1];
-        P.bias_stages = varlen ? 0 : pr[2];
+        P.bias_stages = (varlen && !P.a.bias) ? 0 : pr[2];
         if (make_split_layout(P).total + 1024 <= kSmemLimit) {
             P.o_col0 = 128u * (uint32_t)P.s_bufs;
             P.tmem_cols = 512;
@@ -201,12 +202,24 @@ cudaError_t launch_tc_fwd(const AttnParams& a, cudaStream_t stream) {
             !make_map(&P.tm_v, dt, a.v, D, a.H, tk, rs, 2 * (uint64_t)a.v_rs, 64, 1, kBN))
             return cudaErrorInvalidValue;
         P.nqt = (a.max_q + kBM - 1) / kBM;
-        fold = a.scale > 0.f && std::isfinite(a.scale);
+        fold = a.scale > 0.f && std::isfinite(a.scale) && !a.bias;  // a bias is added after the scale
+        if (a.bias) {
+            // post-scale bias (H, max_seqlen_q, max_seqlen_k), read as (K, Q, H) boxes
+            const uint64_t eb = a.bias_f32 ? 4 : 2;
+            P.bias_box_cols = a.bias_f32 ? 32 : 64;
+            P.bias_boxes = kBN / P.bias_box_cols;
+            P.bias_bytes = P.bias_boxes * kBox;
+            if (!make_map(&P.tm_bias, a.bias_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : dt, a.bias, a.max_k, a.max_q,
+                          a.H, a.max_k * eb, a.max_k * eb * a.max_q, P.bias_box_cols, kBM, 1))
+                return cudaErrorInvalidValue;
+        }
     }
     int NQ = 1;
     // Triangle form with D <= 64, and packed sequences whose offsets fit the
     // key-split kernel's schedule, run on the key-split kernel.
-    const bool split = a.varlen ? a.num_seqs <= kSplitMaxSeqs : D <= 64;
+    // (a packed problem with a bias always takes the key-split kernel)
+    const bool split = a.varlen ? (a.num_seqs <= kSplitMaxSeqs || a.bias) : D <= 64;
+    if (a.varlen && a.bias && a.num_seqs > kSplitMaxSeqs) return cudaErrorNotSupported;
     if (split ? !choose_split_geometry(P, a.varlen != 0) : !choose_geometry(P, a.varlen != 0, NQ))
         return cudaErrorInvalidConfiguration;
     P.items_per_unit = (P.nqt + NQ - 1) / NQ;
@@ -225,11 +238,17 @@ cudaError_t launch_tc_fwd(const AttnParams& a, cudaStream_t stream) {
     if (grid <= 0) return cudaSuccess;
     P.fd_2g = make_fastdiv(2u * (uint32_t)grid);
 
+    if (a.varlen && split && a.bias) {
+        if (bf16) return a.bias_f32 ? launch_split<true, true, true, false, true>(P, grid, stream)
+                                    : launch_split<true, false, true, false, true>(P, grid, stream);
+        return a.bias_f32 ? launch_split<false, true, true, false, true>(P, grid, stream)
+                          : launch_split<false, false, true, false, true>(P, grid, stream);
+    }
     if (a.varlen && split) {
-        if (bf16) return fold ? launch_split<true, false, true, true>(P, grid, stream)
-                              : launch_split<true, false, true, false>(P, grid, stream);
-        return fold ? launch_split<false, false, true, true>(P, grid, stream)
-                    : launch_split<false, false, true, false>(P, grid, stream);
+        if (bf16) return fold ? launch_split<true, false, true, true, false>(P, grid, stream)
+                              : launch_split<true, false, true, false, false>(P, grid, stream);
+        return fold ? launch_split<false, false, true, true, false>(P, grid, stream)
+                    : launch_split<false, false, true, false, false>(P, grid, stream);
     }
     if (a.varlen) {
         if (bf16) return fold ? launch_nq<true, true, false, true>(NQ, P, grid, stream)
@@ -239,10 +258,10 @@ cudaError_t launch_tc_fwd(const AttnParams& a, cudaStream_t stream) {
     }
     (void)fold;
     if (split) {
-        if (bf16) return a.bias_f32 ? launch_split<true, true, false, false>(P, grid, stream)
-                                    : launch_split<true, false, false, false>(P, grid, stream);
-        return a.bias_f32 ? launch_split<false, true, false, false>(P, grid, stream)
-                          : launch_split<false, false, false, false>(P, grid, stream);
+        if (bf16) return a.bias_f32 ? launch_split<true, true, false, false, true>(P, grid, stream)
+                                    : launch_split<true, false, false, false, true>(P, grid, stream);
+        return a.bias_f32 ? launch_split<false, true, false, false, true>(P, grid, stream)
+                          : launch_split<false, false, false, false, true>(P, grid, stream);
     }
     if (bf16) return a.bias_f32 ? launch_nq<false, true, true, false>(NQ, P, grid, stream)
                                 : launch_nq<false, true, false, false>(NQ, P, grid, stream);

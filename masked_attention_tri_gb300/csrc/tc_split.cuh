@@ -84,7 +84,7 @@ __host__ __device__ inline SplitLayout make_split_layout(const TcParams& P) {
     // shared O: row maxima [tile parity][key half][128 rows]; split O: the epilogue's
     // (reference max, sum, max) [item parity][key half][3][128 rows] (fp32)
     L.xbuf = L.maskw + P.bias_stages * 16;
-    L.xl = L.xbuf + 2 * 2 * 3 * 128 * 4;       // row sums: [key half][128 rows] fp32
+    L.xl = L.xbuf + (P.a.varlen ? 2 * 2 : 2 * 2 * 3) * 128 * 4;  // row sums: [key half][128 rows] fp32
     L.sched = L.xl + 2 * 128 * 4;              // packed form: cu_q[S+1], cu_k[S+1], q blocks[S] (int32)
     const uint32_t sched_bytes = P.a.varlen ? (uint32_t)(3 * P.a.num_seqs + 2) * 4u : 0u;
     // ring: ring_full[kRing], ring_empty[kRing] (8-byte mbarriers), then the entries
@@ -422,7 +422,7 @@ static __device__ __noinline__ void split_mean_v(const AttnParams& a, uint16_t* 
     }
 }
 
-template <bool BF16, bool BIAS_F32, bool VARLEN, bool FOLD>
+template <bool BF16, bool BIAS_F32, bool VARLEN, bool FOLD, bool BIAS>
 __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid_constant__ TcParams P) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -595,7 +595,9 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
         if (!ok) *abort_flag = 1;
     } else if (warp == kVWarp) {
         // ---------------------------------------------------------- producer: V tiles
+        // (packed form with a bias: also the bias tiles; warp 10 is the scheduler there)
         StageRing vr = {0, 0u, false};
+        StageRing br = {0, 0u, false};
         bool ok = true;
         ItemWalk<VARLEN> walk;
         walk.begin(P, ring);
@@ -605,6 +607,20 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
             int kb;
             bool fb;
             while (ok && tiles_next<VARLEN>(it, tw, kb, fb)) {
+                if constexpr (VARLEN && BIAS) {
+                    const int bs = br.idx;
+                    if (lane == 0 && br.wrapped) ok = wait_bar(bias_empty(bs), br.ph ^ 1u, abort_flag, a.status);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) break;
+                    if (lane == 0) {
+                        // bias (H, max_seqlen_q, max_seqlen_k): keys kb*128.., local rows qt*128.., head h
+                        mbar_expect_tx(bias_full(bs), P.bias_bytes);
+                        for (int bx = 0; bx < P.bias_boxes; ++bx)
+                            tma_load_3d(bias_smem(bs) + bx * kBox, &P.tm_bias, kb * kBN + bx * P.bias_box_cols,
+                                        it.qt * kBM, it.h, bias_full(bs));
+                    }
+                    br.next(BS);
+                }
                 const int st = vr.idx;
                 if (lane == 0 && vr.wrapped) ok = wait_bar(v_empty(st), vr.ph ^ 1u, abort_flag, a.status);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -1116,7 +1132,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
                 const int nexist = (VARLEN ? it.Lk : a.K) - key0;
                 int bs = 0;
                 uint32_t boff = 0, mwoff = 0;
-                if constexpr (!VARLEN) {
+                if constexpr (BIAS) {
                     bs = br.idx;
                     // Both barriers tested at once; the bounded waits only when one is not ready.
                     const bool ready = mbar_test(bias_full(bs), br.ph) & mbar_test(s_full(sb), (uint32_t)sph);
@@ -1143,7 +1159,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
                     if constexpr (FOLD) {
 #pragma unroll
                         for (int j = 0; j < 64; ++j) x[j] = __uint_as_float(sr[j]);
-                    } else if constexpr (VARLEN) {
+                    } else if constexpr (!BIAS) {
 #pragma unroll
                         for (int j = 0; j < 64; j += 2) {
                             const float2 r2 =
@@ -1205,7 +1221,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
                                 ((vm >> j) & 1u) ? x[32 * hh + j] : (((em >> j) & 1u) ? kMaskVal : -INFINITY);
                     }
                 }
-                if constexpr (!VARLEN) {
+                if constexpr (BIAS) {
                     __syncwarp();  // every lane of the warp has read its bias and the mask words
                     if (lane == 0) mbar_arrive(bias_empty(bs));
                     br.next(BS);
@@ -1336,11 +1352,11 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
     }
 }
 
-template <bool BF16, bool BIAS_F32, bool VARLEN, bool FOLD>
+template <bool BF16, bool BIAS_F32, bool VARLEN, bool FOLD, bool BIAS>
 cudaError_t launch_split(const TcParams& P, int grid, cudaStream_t stream) {
     const SplitLayout L = make_split_layout(P);
     const size_t smem = L.total + 1024;
-    auto kern = tc_split_kernel<BF16, BIAS_F32, VARLEN, FOLD>;
+    auto kern = tc_split_kernel<BF16, BIAS_F32, VARLEN, FOLD, BIAS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, kSplitThreads, smem, stream>>>(P);
@@ -1348,14 +1364,18 @@ cudaError_t launch_split(const TcParams& P, int grid, cudaStream_t stream) {
 }
 
 // Triangle form (bias dtype) and packed form (folded scale or not).
-#define TRIATTN_SPLIT_TRI_VARIANTS(X) X(true, false, false, false) X(true, true, false, false) \
-    X(false, false, false, false) X(false, true, false, false)
-#define TRIATTN_SPLIT_VARLEN_VARIANTS(X) X(true, false, true, true) X(true, false, true, false) \
-    X(false, false, true, true) X(false, false, true, false)
-#define TRIATTN_SPLIT_EXTERN(b, f, v, fo) \
-    extern template cudaError_t launch_split<b, f, v, fo>(const TcParams&, int, cudaStream_t);
-#define TRIATTN_SPLIT_INSTANTIATE(b, f, v, fo) \
-    template cudaError_t launch_split<b, f, v, fo>(const TcParams&, int, cudaStream_t);
+// Triangle form (bias dtype); packed form without a bias (folded scale or not) and
+// with a post-scale bias (bias dtype).
+#define TRIATTN_SPLIT_TRI_VARIANTS(X) X(true, false, false, false, true) X(true, true, false, false, true) \
+    X(false, false, false, false, true) X(false, true, false, false, true)
+#define TRIATTN_SPLIT_VARLEN_VARIANTS(X) X(true, false, true, true, false) X(true, false, true, false, false) \
+    X(false, false, true, true, false) X(false, false, true, false, false)
+#define TRIATTN_SPLIT_VARLEN_BIAS_VARIANTS(X) X(true, false, true, false, true) X(true, true, true, false, true) \
+    X(false, false, true, false, true) X(false, true, true, false, true)
+#define TRIATTN_SPLIT_EXTERN(b, f, v, fo, bi) \
+    extern template cudaError_t launch_split<b, f, v, fo, bi>(const TcParams&, int, cudaStream_t);
+#define TRIATTN_SPLIT_INSTANTIATE(b, f, v, fo, bi) \
+    template cudaError_t launch_split<b, f, v, fo, bi>(const TcParams&, int, cudaStream_t);
 
 }  // namespace tc
 }  // namespace triattn

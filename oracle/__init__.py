@@ -60,7 +60,7 @@ def _load():
                                            P, LL, P, P, P, I]
             lib.oracle_tri_fwd.restype = I
             lib.oracle_varlen_fwd.argtypes = [P, P, P, I, P, P, I, I, I, ctypes.c_double,
-                                              P, P, P, P, I, I, I, I, I, I, P, I, P, P, P, I]
+                                              P, P, P, P, I, I, I, I, I, I, P, I, P, I, I, I, P, P, P, I]
             lib.oracle_varlen_fwd.restype = I
             lib.oracle_mask_to_kv_lengths.argtypes = [P, LL, I, P, P]
             lib.oracle_mask_to_kv_lengths.restype = None
@@ -154,14 +154,15 @@ def mask_to_kv_lengths(mask):
 
 def varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, scale=None, kv_num_blocks=None, kv_indices=None,
                full_kv_num_blocks=None, full_kv_indices=None, block=128, mask_mod="none",
-               threads=None, window=0, prefix_lengths=None):
+               threads=None, window=0, prefix_lengths=None, bias=None):
     """Packed-sequence forward in fp64 with a BlockMask.
 
     q (total_q,H,D), k/v (total_k,H,D); cu_seqlens (S+1,) int.  Block lists are
     (S, mask_heads, MQ) / (S, mask_heads, MQ, MK) int, sequence-local.
     mask_mod on partial blocks: "none", "causal" (k <= q), "sliding_window"
     (q - window < k <= q) or "prefix_lm" (k <= q or k < the sequence's prefix
-    length; prefix_lengths is an int or one int per sequence).
+    length; prefix_lengths is an int or one int per sequence).  bias: optional
+    (H, max_seqlen_q, max_seqlen_k) post-scale bias indexed by local positions.
     Returns numpy (O (total_q,H,D), lse (H,total_q), max (H,total_q)).
     """
     lib = _load()
@@ -182,6 +183,9 @@ def varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, scale=None, kv_num_blocks=No
     if kn is not None:
         mask_heads, MQ = kn.shape[1], kn.shape[2]
         MK = ki.shape[3]
+    bias_t = _cpu(bias)
+    bq = bias_t.shape[1] if bias_t is not None else 0
+    bk = bias_t.shape[2] if bias_t is not None else 0
     pl, p_all = None, 0
     if prefix_lengths is not None:
         if isinstance(prefix_lengths, int):
@@ -194,6 +198,7 @@ def varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, scale=None, kv_num_blocks=No
     rc = lib.oracle_varlen_fwd(_ptr(q), _ptr(k), _ptr(v), DT[_dtname(q)], _ptr(cq), _ptr(ck), S, H, D, s,
                                _ptr(kn), _ptr(ki), _ptr(fn), _ptr(fi), mask_heads, MQ, MK, block,
                                MASK_MOD[mask_mod], int(window), _ptr(pl), int(p_all),
+                               _ptr(bias_t), DT[_dtname(bias_t)] if bias_t is not None else 0, bq, bk,
                                out.ctypes.data_as(ctypes.c_void_p),
                                lse.ctypes.data_as(ctypes.c_void_p), mx.ctypes.data_as(ctypes.c_void_p),
                                int(threads or default_threads()))

@@ -33,7 +33,10 @@
  *     prefix LM k <= q or k < P (P: the sequence's prefix length);
  *   - keys outside every listed block get -1e9, as in the triangle formula;
  *   - with no lists at all every block is partial.
- * Keys k >= Lk do not exist and take no part.
+ * Keys k >= Lk do not exist and take no part.  An optional post-scale bias
+ * (Transformer Engine fused_attn.h, NVTE_POST_SCALE_BIAS), shaped
+ * (H, max_seqlen_q, max_seqlen_k) and indexed by local positions, is added to
+ * the logit of every valid key: x = s * (Q . K) + bias[h, q, k].
  */
 #include <math.h>
 #include <stdint.h>
@@ -201,7 +204,7 @@ static int or_mask_mod(int mask_mod, int qi, int kk, int window, int prefix) {
  * kv_num (S, mask_heads, MQ), kv_idx (S, mask_heads, MQ, MK); full_* the same or NULL.
  * kv_num == NULL: every block is partial.  window: the sliding window's width
  * (mask_mod 2); prefix_len (S,) or NULL, then prefix_all for every sequence
- * (mask_mod 3).  Returns 0 or -1.
+ * (mask_mod 3).  bias (H, max_q, max_k) of bias_dt, or NULL.  Returns 0 or -1.
  */
 int oracle_varlen_fwd(const void* q, const void* k, const void* v, int dt,
                       const int32_t* cu_q, const int32_t* cu_k, int num_seqs, int H, int D,
@@ -210,6 +213,7 @@ int oracle_varlen_fwd(const void* q, const void* k, const void* v, int dt,
                       const int32_t* full_num, const int32_t* full_idx,
                       int mask_heads, int MQ, int MK, int block, int mask_mod,
                       int window, const int32_t* prefix_len, int prefix_all,
+                      const void* bias, int bias_dt, int max_q, int max_k,
                       double* out, double* lse, double* mx, int nthreads) {
     if (num_seqs <= 0 || H <= 0 || D <= 0 || block <= 0) return -1;
     if (mask_mod == OR_MASK_SLIDING_WINDOW && window <= 0) return -1;
@@ -265,6 +269,7 @@ int oracle_varlen_fwd(const void* q, const void* k, const void* v, int dt,
                 double dot = 0.0;
                 for (int d = 0; d < D; ++d) dot += or_load(q, dt, q_off + d) * or_load(k, dt, k_off + d);
                 x[kk] = scale * dot;
+                if (bias) x[kk] += or_load(bias, bias_dt, ((size_t)h * max_q + qi) * (size_t)max_k + kk);
             }
             size_t row_out = (size_t)(q0 + qi);
             size_t a = (size_t)h * total_q + row_out;

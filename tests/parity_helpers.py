@@ -59,7 +59,7 @@ def check_triangle(case, rows=None):
     return compare(case.name, case.dtype, O, L, M, rO, rL, rM)
 
 
-def run_varlen(case, return_aux=True, window=0, prefix=None):
+def run_varlen(case, return_aux=True, window=0, prefix=None, bias=None):
     import masked_attention_tri_gb300 as ta
     bm = None
     if case.kv_num_blocks is not None:
@@ -71,16 +71,17 @@ def run_varlen(case, return_aux=True, window=0, prefix=None):
                               case.max_seqlen_k, block_mask=bm, scale=case.scale, return_aux=return_aux,
                               mask_mod=case.mask_mod if bm is None else None, window=window,
                               prefix_lengths=prefix if not isinstance(prefix, list) else
-                              torch.tensor(prefix, dtype=torch.int32, device="cuda"))
+                              torch.tensor(prefix, dtype=torch.int32, device="cuda"),
+                              bias=None if bias is None else bias.cuda())
     torch.cuda.synchronize()
     assert ta.get_status() == 0
     return res
 
 
-def check_varlen(case, window=0, prefix=None):
-    O, L, M = run_varlen(case, window=window, prefix=prefix)
+def check_varlen(case, window=0, prefix=None, bias=None):
+    O, L, M = run_varlen(case, window=window, prefix=prefix, bias=bias)
     rO, rL, rM = oracle.varlen_fwd(case.q, case.k, case.v, case.cu_seqlens, case.cu_seqlens_k, case.scale,
                                    case.kv_num_blocks, case.kv_indices, case.full_kv_num_blocks,
                                    case.full_kv_indices, block=case.block, mask_mod=case.mask_mod,
-                                   window=window, prefix_lengths=prefix)
+                                   window=window, prefix_lengths=prefix, bias=bias)
     return compare(case.name, case.dtype, O, L, M, rO, rL, rM)

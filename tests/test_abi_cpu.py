@@ -162,8 +162,8 @@ def _masked(**kw):
                 total_k=400, max_seqlen_q=256, max_seqlen_k=256, H=2, D=64, scale=0.125, kv_num_blocks=0,
                 kv_indices=0, full_kv_num_blocks=0, full_kv_indices=0, mask_heads=1, max_q_blocks=2,
                 max_kv_blocks=2, block_q=128, block_k=128, mask_mod=abi.TA_MASK_SLIDING_WINDOW, window=16,
-                prefix_lengths=0, prefix_length=0, q_row_stride=0, k_row_stride=0, v_row_stride=0, out=A, lse=0,
-                max_=0, stream=0)
+                prefix_lengths=0, prefix_length=0, bias=0, bias_dtype=abi.TA_F32, q_row_stride=0, k_row_stride=0,
+                v_row_stride=0, out=A, lse=0, max_=0, stream=0)
     args.update(kw)
     return lambda: abi.tri_attn_varlen_fwd_masked(**args)
 
@@ -175,6 +175,10 @@ def _masked(**kw):
     (dict(mask_mod=abi.TA_MASK_PREFIX_LM, prefix_length=-1), ValueError),
     (dict(mask_mod=abi.TA_MASK_PREFIX_LM, prefix_lengths=MIS + 2), ValueError),  # 4-byte alignment
     (dict(block_q=64), NotImplementedError),
+    (dict(bias=MIS), ValueError),                                   # bias 16-byte alignment
+    (dict(bias=A, bias_dtype=abi.TA_F16), NotImplementedError),     # bf16 q: bias f32 or bf16
+    (dict(bias=A, bias_dtype=abi.TA_BF16, max_seqlen_k=250), NotImplementedError),  # 500-byte bias rows
+    (dict(bias=A, bias_dtype=7), ValueError),
 ])
 def test_varlen_masked_host_checks(lib, kw, exc):
     with pytest.raises(exc):

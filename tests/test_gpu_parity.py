@@ -258,6 +258,31 @@ def test_varlen_sliding_window_with_lists_and_many_sequences():
     check_varlen(c2, prefix=[int(x) % 9 for x in range(1030)])
 
 
+# Post-scale bias on the packed form (H, max_seqlen_q, max_seqlen_k), indexed by local
+# positions: key-split kernel (16-bit, with bf16 / fp16 / fp32 bias) and the fp32 kernel.
+@pytest.mark.parametrize("dtype,bias_dtype,D", [("bf16", "bf16", 64), ("bf16", "f32", 128), ("f16", "f16", 32),
+                                                ("f16", "f32", 64), ("f32", "f32", 32)])
+@pytest.mark.parametrize("lists", ["causal", "none"])
+def test_varlen_bias(dtype, bias_dtype, D, lists):
+    lengths = [300, 129, 64, 1]
+    c = synth.make_varlen(f"vl_bias_{D}_{lists}", 4, 0, 0, 2, D, dtype, seed=620 + D, lengths=lengths,
+                          block_lists=lists, mask_mod="causal")
+    g = torch.Generator().manual_seed(621)
+    bias = (2.0 * torch.randn(2, 304, 304, generator=g)).to(synth.TORCH_DTYPES[bias_dtype])
+    c.max_seqlen = c.max_seqlen_k = 304  # the bias's (and the call's) max_seqlen
+    check_varlen(c, bias=bias)
+
+
+def test_varlen_bias_key_lengths_differ_and_window():
+    """Lq != Lk with a bias (max_seqlen_q != max_seqlen_k) and the sliding window."""
+    c = synth.make_varlen("vl_bias_lqlk", 3, 0, 0, 2, 64, "bf16", seed=630, lengths=[200, 70, 129],
+                          lengths_k=[90, 300, 129], block_lists="none", mask_mod="sliding_window")
+    g = torch.Generator().manual_seed(631)
+    c.max_seqlen, c.max_seqlen_k = 208, 304
+    bias = torch.randn(2, 208, 304, generator=g).to(torch.bfloat16)
+    check_varlen(c, window=40, bias=bias)
+
+
 def test_varlen_fp32():
     c = synth.make_varlen("vl_f32", 3, 0, 0, 2, 32, "f32", seed=520, lengths=[40, 200, 131])
     check_varlen(c)

@@ -572,3 +572,34 @@ def test_varlen_prefix_lm_equals_prefix_plus_causal(prefix):
     if per == [0, 0, 0]:
         Oc, _, _ = oracle.varlen_fwd(c.q, c.k, c.v, c.cu_seqlens, c.cu_seqlens, c.scale, mask_mod="causal")
         np.testing.assert_array_equal(O, Oc)
+
+
+@pytest.mark.parametrize("mask_mod", ["none", "causal"])
+def test_varlen_bias_equals_sdpa_with_additive_bias(mask_mod):
+    """Post-scale bias on the packed form (Transformer Engine fused_attn.h, NVTE_POST_SCALE_BIAS):
+    bias (H, max_q, max_k) indexed by each sequence's local positions, added to the scaled
+    logits of valid keys; SDPA with the sliced bias (and -inf off the causal triangle)."""
+    lengths, lk = [70, 130, 9], [50, 140, 16]
+    c = synth.make_varlen("t", 3, 0, 0, 2, 8, "f32", seed=36, lengths=lengths, lengths_k=lk, block_lists="none",
+                          mask_mod=mask_mod)
+    g = torch.Generator().manual_seed(37)
+    bias = (2.0 * torch.randn(2, 136, 144, generator=g)).to(torch.bfloat16)
+    O, L, M = oracle.varlen_fwd(c.q, c.k, c.v, c.cu_seqlens, c.cu_seqlens_k, c.scale, mask_mod=mask_mod, bias=bias)
+    s = float(np.float32(c.scale))
+    ref = torch.zeros(c.q.shape, dtype=torch.float64)
+    for i in range(3):
+        a, b = int(c.cu_seqlens[i]), int(c.cu_seqlens[i + 1])
+        ka, kb = int(c.cu_seqlens_k[i]), int(c.cu_seqlens_k[i + 1])
+        nq, nk = b - a, kb - ka
+        for h in range(2):
+            add = _f64(bias[h, :nq, :nk]).clone()
+            if mask_mod == "causal":
+                add[torch.arange(nk).view(1, -1) > torch.arange(nq).view(-1, 1)] = float("-inf")
+            ref[a:b, h] = _sdpa(_f64(c.q[a:b, h]), _f64(c.k[ka:kb, h]), _f64(c.v[ka:kb, h]), add, s)
+    np.testing.assert_allclose(O, ref.numpy(), atol=1e-12)
+    O0, L0, _ = oracle.varlen_fwd(c.q, c.k, c.v, c.cu_seqlens, c.cu_seqlens_k, c.scale, mask_mod=mask_mod,
+                                  bias=torch.zeros(2, 136, 144))
+    O1, L1, _ = oracle.varlen_fwd(c.q, c.k, c.v, c.cu_seqlens, c.cu_seqlens_k, c.scale, mask_mod=mask_mod,
+                                  bias=torch.full((2, 136, 144), 3.0))
+    np.testing.assert_allclose(O1, O0, atol=1e-13)        # a constant bias leaves O unchanged ...
+    np.testing.assert_allclose(L1, L0 + 3.0, atol=1e-12)  # ... and shifts lse by that constant
