@@ -92,10 +92,11 @@ typedef enum {
  *               lie at or below -1e9 would instead need those masked keys.
  *   lse, max    optional (B, N, H, Q) fp32 outputs (return_aux); NULL skips.
  *
- * Supported: fp16/bf16 q/k/v with D % 8 == 0, D <= 128 and K % 8 == 0 (the
- * page's Notes 3-4 bounds for the half-precision kernels), on tcgen05 tensor
- * cores; fp32 q/k/v with D % 4 == 0, D <= 128 on exact-fp32 CUDA-core
- * arithmetic (no TF32).  fp32 bias with 16-bit q/k/v additionally needs
+ * Supported: fp16/bf16 q/k/v with D % 8 == 0, D <= 256 and K % 8 == 0 (the
+ * page's Notes 3-4 bounds for the half-precision forward: hidden_dim <= 256),
+ * on tcgen05 tensor cores for D <= 128 and on the exact-fp32 CUDA-core kernel
+ * for D in (128, 256]; fp32 q/k/v with D % 4 == 0, D <= 256 on exact-fp32
+ * CUDA-core arithmetic (no TF32).  fp32 bias with 16-bit q/k/v additionally needs
  * K % 4 == 0 (met by K % 8).  Anything else -> TA_ERR_UNSUPPORTED; there is
  * no fallback path.
  */
@@ -158,8 +159,8 @@ ta_status tri_attn_fwd_strided(const void* q, const void* k, const void* v, ta_d
  *   No bias here (tri_attn_varlen_fwd_masked takes one).  A key row past the end of its sequence takes no part.  A
  *   sequence with no keys gets O = 0 and lse = max = -inf.
  *
- * Supported: fp16/bf16 with D % 8 == 0, D <= 128 (tcgen05), fp32 with
- * D % 4 == 0, D <= 128 (CUDA cores).
+ * Supported: fp16/bf16 with D % 8 == 0, D <= 256 (tcgen05 up to 128, the
+ * CUDA-core kernel above), fp32 with D % 4 == 0, D <= 256 (CUDA cores).
  */
 ta_status tri_attn_varlen_fwd(const void* q, const void* k, const void* v, ta_dtype dtype,
                               const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,

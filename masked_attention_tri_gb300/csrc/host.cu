@@ -48,14 +48,17 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 bool valid_dtype(int d) { return d == TA_F32 || d == TA_F16 || d == TA_BF16; }
 
-// Head-dimension rules: 16-bit inputs D % 8 == 0 and D <= 128; fp32 D % 4 == 0 and D <= 128.
+// Head-dimension rules: 16-bit inputs D % 8 == 0 and D <= 256; fp32 D % 4 == 0 and D <= 256.
 bool supported_d(int dtype, int D) {
-    if (D > 128) return false;
+    if (D > 256) return false;
     return dtype == TA_F32 ? (D % 4 == 0) : (D % 8 == 0);
 }
 
+// fp32 inputs, and 16-bit inputs with D > 128, run on the CUDA-core kernel; the
+// rest on the tensor-core kernels.
 ta_status run(const AttnParams& p, cudaStream_t stream) {
-    cudaError_t e = p.dtype == TA_F32 ? triattn::launch_simt_fwd(p, stream) : triattn::launch_tc_fwd(p, stream);
+    cudaError_t e = (p.dtype == TA_F32 || p.D > 128) ? triattn::launch_simt_fwd(p, stream)
+                                                     : triattn::launch_tc_fwd(p, stream);
     return e == cudaSuccess ? TA_OK : TA_ERR_CUDA;
 }
 

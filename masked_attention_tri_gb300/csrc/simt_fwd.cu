@@ -10,7 +10,9 @@
 //
 // Layout: one CTA = 32 query rows of one (b,n,h) slab (triangle) or one
 // (sequence, head) pair (varlen); 4 warps x 8 rows; each lane owns one key of
-// the current tile for the logits and D/32 output columns for the accumulate.
+// the current tile for the logits and D/32 output columns for the accumulate
+// (DPL = 4 columns per lane for D <= 128, 8 for D <= 256).  It also carries
+// 16-bit inputs with D in (128, 256], which the tensor-core kernels do not take.
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -24,7 +26,6 @@ constexpr int kQT = 32;
 constexpr int kKT = 32;
 constexpr int kWarps = 4;
 constexpr int kRows = kQT / kWarps;  // rows per warp
-constexpr int kDPerLane = 4;         // D <= 128
 constexpr float kMasked = -1.0e9f;
 
 template <typename T>
@@ -59,7 +60,7 @@ __device__ __forceinline__ float warp_sum(float x) {
 // Key validity modes of one tile.
 enum { kKeyAll = 0, kKeyPrefix = 1, kKeyDense = 2, kKeyMod = 3 };
 
-template <typename T, typename BT>
+template <typename T, typename BT, int DPL>
 struct SimtState {
     const AttnParams* p;
     float* Qs;
@@ -76,13 +77,13 @@ struct SimtState {
     int prefix_len;
     int prefix_lm;        // packed form, mask_mod prefix LM: the sequence's prefix length
     const uint8_t* dense;
-    float m[kRows], l[kRows], acc[kRows][kDPerLane];
+    float m[kRows], l[kRows], acc[kRows][DPL];
     bool seen[kRows];
 };
 
 // Process keys [key0, key0 + 32) ∩ [0, Lk) with the given validity mode.
-template <typename T, typename BT>
-__device__ void simt_tile(SimtState<T, BT>& st, int key0, int mode) {
+template <typename T, typename BT, int DPL>
+__device__ void simt_tile(SimtState<T, BT, DPL>& st, int key0, int mode) {
     const AttnParams& p = *st.p;
     const T* kp = static_cast<const T*>(p.k);
     const T* vp = static_cast<const T*>(p.v);
@@ -146,12 +147,12 @@ __device__ void simt_tile(SimtState<T, BT>& st, int key0, int mode) {
         st.m[i] = mn;
         st.Ps[i * kKT + st.lane] = pr;
 #pragma unroll
-        for (int j = 0; j < kDPerLane; ++j) st.acc[i][j] *= alpha;
+        for (int j = 0; j < DPL; ++j) st.acc[i][j] *= alpha;
     }
     __syncwarp();
     for (int j = 0; j < kKT; ++j) {
 #pragma unroll
-        for (int c = 0; c < kDPerLane; ++c) {
+        for (int c = 0; c < DPL; ++c) {
             int d = st.lane + 32 * c;
             if (d < D) {
                 float vv = st.Vs[j * D + d];
@@ -163,11 +164,11 @@ __device__ void simt_tile(SimtState<T, BT>& st, int key0, int mode) {
     __syncwarp();
 }
 
-template <typename T, typename BT>
+template <typename T, typename BT, int DPL>
 __global__ void __launch_bounds__(kWarps * 32) simt_fwd_kernel(const AttnParams p) {
     extern __shared__ float smem[];
     const int D = p.D, Dp1 = D + 1;
-    SimtState<T, BT> st;
+    SimtState<T, BT, DPL> st;
     st.p = &p;
     st.D = D;
     st.Dp1 = Dp1;
@@ -259,7 +260,7 @@ __global__ void __launch_bounds__(kWarps * 32) simt_fwd_kernel(const AttnParams 
         st.l[i] = 0.f;
         st.seen[i] = false;
 #pragma unroll
-        for (int c = 0; c < kDPerLane; ++c) st.acc[i][c] = 0.f;
+        for (int c = 0; c < DPL; ++c) st.acc[i][c] = 0.f;
     }
 
     if (!p.varlen) {
@@ -304,18 +305,20 @@ __global__ void __launch_bounds__(kWarps * 32) simt_fwd_kernel(const AttnParams 
     bool any_unseen = false;
 #pragma unroll
     for (int i = 0; i < kRows; ++i) any_unseen = any_unseen || !st.seen[i];
-    float meanv[kDPerLane] = {0.f, 0.f, 0.f, 0.f};
+    float meanv[DPL];
+#pragma unroll
+    for (int c = 0; c < DPL; ++c) meanv[c] = 0.f;
     if (any_unseen && st.Lk > 0) {
         const T* vp = static_cast<const T*>(p.v);
         for (int key = 0; key < st.Lk; ++key) {
 #pragma unroll
-            for (int c = 0; c < kDPerLane; ++c) {
+            for (int c = 0; c < DPL; ++c) {
                 int d = st.lane + 32 * c;
                 if (d < D) meanv[c] += to_f(vp[st.v_off + (long long)key * st.v_rs + d]);
             }
         }
 #pragma unroll
-        for (int c = 0; c < kDPerLane; ++c) meanv[c] /= (float)st.Lk;
+        for (int c = 0; c < DPL; ++c) meanv[c] /= (float)st.Lk;
     }
 
     T* op = static_cast<T*>(p.out);
@@ -324,26 +327,26 @@ __global__ void __launch_bounds__(kWarps * 32) simt_fwd_kernel(const AttnParams 
         const int qrow = st.q0 + st.warp * kRows + i;
         if (qrow >= Lq) continue;
         float lse, mx;
-        float o[kDPerLane];
+        float o[DPL];
         if (st.Lk == 0) {
 #pragma unroll
-            for (int c = 0; c < kDPerLane; ++c) o[c] = 0.f;
+            for (int c = 0; c < DPL; ++c) o[c] = 0.f;
             lse = -INFINITY;
             mx = -INFINITY;
         } else if (!st.seen[i]) {
 #pragma unroll
-            for (int c = 0; c < kDPerLane; ++c) o[c] = meanv[c];
+            for (int c = 0; c < DPL; ++c) o[c] = meanv[c];
             mx = kMasked;
             lse = kMasked + logf((float)st.Lk);
         } else {
             float inv = 1.f / st.l[i];
 #pragma unroll
-            for (int c = 0; c < kDPerLane; ++c) o[c] = st.acc[i][c] * inv;
+            for (int c = 0; c < DPL; ++c) o[c] = st.acc[i][c] * inv;
             mx = st.m[i];
             lse = st.m[i] + logf(st.l[i]);
         }
 #pragma unroll
-        for (int c = 0; c < kDPerLane; ++c) {
+        for (int c = 0; c < DPL; ++c) {
             int d = st.lane + 32 * c;
             if (d < D) op[o_off + (long long)qrow * o_rs + d] = from_f<T>(o[c]);
         }
@@ -359,7 +362,7 @@ cudaError_t launch_typed(const AttnParams& p, cudaStream_t stream) {
     const int D = p.D;
     size_t smem = sizeof(float) * ((size_t)kQT * (D + 1) + (size_t)kKT * (D + 1) + (size_t)kKT * D +
                                    (size_t)kWarps * kRows * kKT);
-    auto kern = simt_fwd_kernel<T, BT>;
+    auto kern = D <= 128 ? simt_fwd_kernel<T, BT, 4> : simt_fwd_kernel<T, BT, 8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     long long grid;

@@ -48,16 +48,17 @@ int num_sms() {
 }
 
 // 3-D tiled map: dims {d0, d1, d2} (d0 innermost), byte strides of d1 and d2,
-// box {b0, b1, b2}; 128-byte swizzle, out-of-range elements read as zero.
+// box {b0, b1, b2}; 128-byte swizzle unless given, out-of-range elements read
+// as zero (and are not written by a store).
 bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2,
-              uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2) {
+              uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2,
+              CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B) {
     cuuint64_t dims[3] = {d0, d1, d2};
     cuuint64_t strides[2] = {s1, s2};
     cuuint32_t box[3] = {b0, b1, b2};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = g_encode(m, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                          sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -194,6 +195,14 @@ cudaError_t launch_tc_fwd(const AttnParams& a, cudaStream_t stream) {
             return cudaErrorInvalidValue;
         P.nqt = (a.Q + kBM - 1) / kBM;
         fold = false;  // the bias is added in the softmax
+        // O rows of 32, 64 or 128 bytes (D = 16, 32, 64) leave through a TMA store
+        // (rows past Q are clipped by the map); other D store rows directly.
+        if (D == 16 || D == 32 || D == 64) {
+            const CUtensorMapSwizzle sw = D == 64 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                                  : (D == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
+            P.o_tma = make_map(&P.tm_o, dt, a.out, D, a.Q, units, rs, rs * a.Q, D, 32, 1, sw) ? 1 : 0;
+            P.o_rowb = (int)rs;
+        }
     } else {
         const uint64_t tk = a.total_k > 0 ? a.total_k : 1;
         // Rows of the packed (total, H, D) views are q_rs / k_rs / v_rs elements apart.

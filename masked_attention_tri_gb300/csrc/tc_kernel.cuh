@@ -130,6 +130,12 @@ struct TcParams {
     // Triangle form: q / k / v maps are 5-D {D, rows, H, N, B} (strided views), or
     // 3-D {D, rows, B*N*H} for contiguous tensors.
     int tri5d;
+    // Key-split kernel, triangle form: O leaves through shared memory and a TMA
+    // tensor store of 32 rows x D per TMEM lane quarter (o_tma = 1; map
+    // {D, Q, B*N*H}, rows of o_rowb = 2 D bytes, swizzled by the row width).
+    CUtensorMap tm_o;
+    int o_tma;
+    int o_rowb;
 };
 
 // ---------------------------------------------------------------------------
@@ -237,6 +243,26 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm,
         "[%5];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
         : "memory");
+}
+
+// TMA tensor store of a shared-memory box (bulk-group completion) and the
+// bulk-group waits: `.read` waits until the source may be overwritten.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* tm, uint32_t src, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(tm)),
+                 "r"(src), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Generic-proxy shared-memory writes made visible to the async proxy (TMA).
+__device__ __forceinline__ void fence_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void named_barrier(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
 __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* tm, int c0, int c1, int c2, int c3,
@@ -422,8 +448,21 @@ struct Item {
     int n_part[NQ];
 };
 
+// The kv_lengths entry of triangle item `item` (0 without kv_lengths or past
+// the last item).  The roles that walk items load it one item ahead, so the
+// load's latency overlaps the current item instead of stalling the next decode.
+__device__ __forceinline__ int tri_item_len(const TcParams& P, int item) {
+    if (P.mask_kind != 1 || item >= P.items) return 0;
+    const uint32_t u2 = P.fd_ipu.div((uint32_t)item);
+    const uint32_t bh = P.fd_n.div(u2);
+    const int n = (int)(u2 - bh * P.fd_n.d);
+    const int b = (int)P.fd_h.div(bh);
+    return __ldg(P.a.kv_len + ((long long)b * P.a.N + n));
+}
+constexpr int kNoLen = -0x7fffffff - 1;  // decode loads the kv_lengths entry itself
+
 template <int NQ, bool VARLEN>
-__device__ Item<NQ> decode(const TcParams& P, int item) {
+__device__ Item<NQ> decode(const TcParams& P, int item, int pre_len = kNoLen) {
     Item<NQ> it;
     const AttnParams& a = P.a;
     it.bad = false;
@@ -459,7 +498,7 @@ __device__ Item<NQ> decode(const TcParams& P, int item) {
         if (P.mask_kind == 1) {
             // Key tiles past the prefix are skipped.  With no valid key at all,
             // every tile is visited with every logit at -1e9 (uniform weights).
-            const int L = a.kv_len[it.bn];
+            const int L = pre_len != kNoLen ? pre_len : a.kv_len[it.bn];
             it.prefix = L < 0 ? 0 : (L > a.K ? a.K : L);
             if (it.prefix > 0) it.nkb = (it.prefix + kBN - 1) / kBN;
         }

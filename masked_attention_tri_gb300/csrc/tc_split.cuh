@@ -71,7 +71,7 @@ struct VEntry {
 };
 
 struct SplitLayout {
-    uint32_t q, kv, bias, maskw, xbuf, xl, sched, ring, bars, tmem_slot, abort_flag, total;
+    uint32_t q, kv, bias, ostage, maskw, xbuf, xl, sched, ring, bars, tmem_slot, abort_flag, total;
     int nbars;
 };
 
@@ -80,7 +80,10 @@ __host__ __device__ inline SplitLayout make_split_layout(const TcParams& P) {
     L.q = 0;
     L.kv = L.q + P.q_bufs * P.tile_bytes;
     L.bias = L.kv + P.kv_stages * 2 * P.tile_bytes;
-    L.maskw = L.bias + P.bias_stages * P.bias_bytes;
+    // O staging for the TMA store: 4 lane quarters x 32 rows x o_rowb bytes (1024-aligned:
+    // the bias stages are whole 16 KB boxes)
+    L.ostage = L.bias + P.bias_stages * P.bias_bytes;
+    L.maskw = L.ostage + (P.o_tma ? 4u * 32u * (uint32_t)P.o_rowb : 0u);
     // shared O: row maxima [tile parity][key half][128 rows]; split O: the epilogue's
     // (reference max, sum, max) [item parity][key half][3][128 rows] (fp32)
     L.xbuf = L.maskw + P.bias_stages * 16;
@@ -195,7 +198,8 @@ __device__ __forceinline__ bool vcursor_next(const TcParams& P, const int* snb, 
 // Triangle item from its index (kv_lengths resolved), or packed item from
 // (sequence, head, q block) with its visited-tile count (warp-cooperative).
 template <bool VARLEN>
-__device__ __forceinline__ SItem split_decode(const TcParams& P, const int* sched, int item, int seq, int h, int qb) {
+__device__ __forceinline__ SItem split_decode(const TcParams& P, const int* sched, int item, int seq, int h, int qb,
+                                              int pre_len = kNoLen) {
     SItem it;
     const AttnParams& a = P.a;
     it.lists = false;
@@ -205,7 +209,7 @@ __device__ __forceinline__ SItem split_decode(const TcParams& P, const int* sche
     it.prefix = 0;
     it.q_row0 = it.k_row0 = 0;
     if constexpr (!VARLEN) {
-        const Item<1> t = decode<1, false>(P, item);
+        const Item<1> t = decode<1, false>(P, item, pre_len);
         it.qt = t.qt[0];
         it.unit = t.unit;
         it.bn = t.bn;
@@ -319,11 +323,16 @@ struct ItemWalk;
 template <>
 struct ItemWalk<false> {
     int item;
-    __device__ __forceinline__ void begin(const TcParams&, const RingRef&) { item = (int)blockIdx.x; }
+    int len;  // kv_lengths entry of `item`, loaded one item ahead
+    __device__ __forceinline__ void begin(const TcParams& P, const RingRef&) {
+        item = (int)blockIdx.x;
+        len = tri_item_len(P, item);
+    }
     __device__ __forceinline__ bool next(const TcParams& P, const RingRef&, SItem& it) {
         if (item >= P.items) return false;
-        it = split_decode<false>(P, nullptr, item, 0, 0, 0);
+        it = split_decode<false>(P, nullptr, item, 0, 0, 0, len);
         item += gridDim.x;
+        len = tri_item_len(P, item);
         return true;
     }
 };
@@ -419,6 +428,40 @@ static __device__ __noinline__ void split_mean_v(const AttnParams& a, uint16_t* 
             const float m = __shfl_sync(0xffffffffu, mv, e);
             if (mine) orow_p[d0 + e] = (uint16_t)(pack2<BF16>(m, 0.f) & 0xffffu);
         }
+    }
+}
+
+// MMA issue sequences.  The k-step loops stay rolled: issuing the MMAs back to
+// back (unrolled, compile-time offsets) measured slower here, as the tensor
+// core's bursts then contend with the softmax warps' tensor-memory traffic.
+// QK^T k step kk reads D elements [16 kk, 16 kk + 16) of the 128B-swizzled
+// Q and K tiles: box kk / 4, 32 bytes per step within the box.
+__device__ __forceinline__ uint64_t qk_koff(int kk) { return (uint64_t)(((kk >> 2) * kBox + (kk & 3) * 32) >> 4); }
+__device__ __forceinline__ void issue_qk_n(int ks, uint32_t sd, uint64_t qd, uint64_t kd, uint32_t idesc) {
+#pragma unroll 1
+    for (int kk = 0; kk < ks; ++kk) mma_ss(sd, qd + qk_koff(kk), kd + qk_koff(kk), idesc, kk > 0 ? 1u : 0u);
+}
+// PV of one tile into one O accumulator d (P from TMEM at pa, 8 columns per 16
+// keys; V MN-major, 2 KB per 16 keys), with the first ks k steps of the next
+// QK^T interleaved (independent accumulators, so the tensor core overlaps them).
+__device__ __forceinline__ void issue_pv_qk_n(int ks, uint32_t d, uint32_t pa, uint64_t vd, uint32_t idesc_pv,
+                                              bool first, uint32_t sd, uint64_t qd, uint64_t kd, uint32_t idesc_qk) {
+#pragma unroll 1
+    for (int kk = 0; kk < kBN / 16; ++kk) {
+        mma_ts(d, pa + kk * 8, vd + (uint64_t)kk * 128, idesc_pv, (!first || kk > 0) ? 1u : 0u);
+        if (kk < ks) mma_ss(sd, qd + qk_koff(kk), kd + qk_koff(kk), idesc_qk, kk > 0 ? 1u : 0u);
+    }
+}
+// Split O: keys 0-63 of the tile into O_0 (d0), keys 64-127 into O_1 (d1),
+// alternating so the two chains overlap.  P of key half 1 sits in that half's
+// own logit columns [64, 96).
+__device__ __forceinline__ void issue_pv_split(uint32_t d0, uint32_t d1, uint32_t pa, uint64_t vd, uint32_t idesc_pv,
+                                               bool first) {
+#pragma unroll 1
+    for (int j = 0; j < kBN / 16; ++j) {
+        const int kk = (j >> 1) + 4 * (j & 1);
+        mma_ts((j & 1) ? d1 : d0, pa + kk * 8 + (kk & 4) * 8, vd + (uint64_t)kk * 128, idesc_pv,
+               (!first || (kk & 3) > 0) ? 1u : 0u);
     }
 }
 
@@ -691,8 +734,10 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
             // ---------------------------------- producer: bias tiles (+ dense-mask bits)
             StageRing br = {0, 0u, false};
             bool ok = true;
+            int len = tri_item_len(P, (int)blockIdx.x);  // loaded one item ahead
             for (int item = blockIdx.x; item < P.items && ok; item += gridDim.x) {
-                const Item<1> it = decode<1, false>(P, item);
+                const Item<1> it = decode<1, false>(P, item, len);
+                len = tri_item_len(P, item + (int)gridDim.x);
                 if (!it.any) continue;
                 for (int kb = 0; kb < it.nkb && ok; ++kb) {
                     const int bs = br.idx;
@@ -745,7 +790,6 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
         StageRing vp = {0, 0u, false}, sp = {0, 0u, false};  // V stage / S buffer of the next PV
         StageRing oe = {0, 0u, false};                      // single O accumulator: its "read" barrier
         bool ok = true;
-        auto kstep = [](int kk) -> uint64_t { return (uint64_t)(((kk >> 2) * kBox + (kk & 3) * 32) >> 4); };
         // QK^T of the next tile: wait for its Q (first tile of an item) and K stage.
         uint64_t qd = 0, kd = 0;
         uint32_t sd = 0;
@@ -779,11 +823,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
         };
         auto qk_alone = [&]() {
             tc_fence_after();
-            if (leader) {
-#pragma unroll 1
-                for (int kk = 0; kk < P.ksteps; ++kk)
-                    mma_ss(sd, qd + kstep(kk), kd + kstep(kk), P.idesc_qk, kk > 0 ? 1u : 0u);
-            }
+            if (leader) issue_qk_n(P.ksteps, sd, qd, kd, P.idesc_qk);
             qk_done();
         };
         // Packed form (D up to 128, the MMA warp sets the pace): PV of tile n and
@@ -824,23 +864,10 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
             const uint32_t d = tmem + P.o_col0 + oset * (kSplitO ? 2u : 1u) * P.o_cols;
             const uint32_t pa = tmem + 128u * (uint32_t)b;
             if (leader) {
-                if constexpr (kSplitO) {
-                    // keys 0-63 into O_0, 64-127 into O_1, alternating (two independent chains)
-#pragma unroll 1
-                    for (int j = 0; j < kBN / 16; ++j) {
-                        const int kk = (j >> 1) + 4 * (j & 1);
-                        // P of key half 1 sits in that half's own logit columns [64, 96)
-                        mma_ts(d + (uint32_t)(j & 1) * P.o_cols, pa + kk * 8 + (kk & 4) * 8, vd + (uint64_t)kk * 128,
-                               P.idesc_pv, (pc.t > 0 || (kk & 3) > 0) ? 1u : 0u);
-                    }
-                } else {
-                    const int nk = qk ? P.ksteps : 0;
-#pragma unroll 1
-                    for (int kk = 0; kk < kBN / 16; ++kk) {
-                        mma_ts(d, pa + kk * 8, vd + (uint64_t)kk * 128, P.idesc_pv, (pc.t > 0 || kk > 0) ? 1u : 0u);
-                        if (kk < nk) mma_ss(sd, qd + kstep(kk), kd + kstep(kk), P.idesc_qk, kk > 0 ? 1u : 0u);
-                    }
-                }
+                if constexpr (kSplitO)
+                    issue_pv_split(d, d + P.o_cols, pa, vd, P.idesc_pv, pc.t == 0);
+                else
+                    issue_pv_qk_n(qk ? P.ksteps : 0, d, pa, vd, P.idesc_pv, pc.t == 0, sd, qd, kd, P.idesc_qk);
                 mma_commit(pv_done(np));
                 mma_commit(v_empty(st));
             }
@@ -959,9 +986,15 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
             float m_ref, l, m_true;
             long long row0, unit0;
             int hh, nk;
+            int box_row, box_unit;  // triangle form: the O store box of this lane quarter
             uint32_t n_last, ob;
             bool row_ok, direct;
         } pe = {};
+        // O staging rows of this lane quarter: row `lane` holds 16-byte chunk c at
+        // chunk c ^ swz (the map's 128 / 64 / 32-byte swizzle of 128 / 64 / 32-byte rows).
+        const uint32_t o_stage = base + L.ostage + (uint32_t)(wq * 32 * P.o_rowb) + (uint32_t)(lane * P.o_rowb);
+        const uint32_t o_swz = P.o_rowb == 128 ? (uint32_t)(lane & 7)
+                                               : (P.o_rowb == 64 ? (uint32_t)((lane >> 1) & 3) : (uint32_t)((lane >> 2) & 1));
         bool pend = false;
         auto epilogue = [&](bool at_end) -> bool {
             // Combine the two key halves' (reference max, row sum, max).  Shared O:
@@ -973,6 +1006,9 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
                 xe[(h * 3 + 0) * 128 + r] = pe.m_ref;
                 xe[(h * 3 + 1) * 128 + r] = pe.l;
                 xe[(h * 3 + 2) * 128 + r] = pe.m_true;
+                // The partner writes O staging rows only after this arrival, so the previous
+                // item's O store must have read them by then.
+                if (P.o_tma && h == 0 && lane == 0) bulk_wait_read_all();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(xchg(wq));
                 const bool w_ok = __all_sync(0xffffffffu, wait_bar(xchg(wq), x_it & 1, abort_flag, a.status));
@@ -1013,6 +1049,12 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
             // weights of O_0 and O_1 (split O), folded with 1 / l
             const float w0 = (h == 0 ? a_own : a_oth) * inv, w1 = (h == 0 ? a_oth : a_own) * inv;
             const int dlim = a.D - h * (int)half_o;  // columns of this half that exist
+            // Triangle form: the lane quarter's 32 rows go to shared memory and leave in one
+            // TMA store, unless a row takes the mean of V (then rows are stored directly).
+            const bool o_tma = kSplitO && P.o_tma && !__any_sync(0xffffffffu, direct && pe.row_ok);
+            auto stage16 = [&](uint32_t c, uint32_t w0_, uint32_t w1_, uint32_t w2_, uint32_t w3_) {
+                st_shared_v4(o_stage + ((c ^ o_swz) << 4), w0_, w1_, w2_, w3_);
+            };
             if (half_o == 32) {  // D in (48, 64]: this warp's 32 columns in one load
                 uint32_t o[32];
                 tmem_ld_x32(oa, o);
@@ -1028,7 +1070,11 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
                     wv[e] = pack2<BF16>(__uint_as_float(o[2 * e]) * sc, __uint_as_float(o[2 * e + 1]) * sc);
-                if (pe.row_ok && !direct) {
+                if (o_tma) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        stage16((uint32_t)(4 * h + i), wv[4 * i], wv[4 * i + 1], wv[4 * i + 2], wv[4 * i + 3]);
+                } else if (pe.row_ok && !direct) {
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
                         if (8 * i < dlim)
@@ -1069,8 +1115,21 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
 #pragma unroll
                     for (int e = 0; e < 8; e += 2)
                         wv[e / 2] = pack2<BF16>(__uint_as_float(o[e]) * sc, __uint_as_float(o[e + 1]) * sc);
-                    if (pe.row_ok && !direct && (int)c0 < dlim)
+                    if (o_tma)
+                        stage16(((uint32_t)h * half_o + c0) >> 3, wv[0], wv[1], wv[2], wv[3]);
+                    else if (pe.row_ok && !direct && (int)c0 < dlim)
                         *reinterpret_cast<uint4*>(op + c0) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                }
+            }
+            if (o_tma) {
+                // Both warps of the lane quarter have staged their columns: one store of
+                // 32 rows x D (rows past Q are not written).
+                fence_async_shared();
+                named_barrier(1 + wq, 64);
+                if (h == 0 && lane == 0 && pe.box_row < a.Q) {
+                    tma_store_3d(&P.tm_o, base + L.ostage + (uint32_t)(wq * 32 * P.o_rowb), 0, pe.box_row,
+                                 pe.box_unit);
+                    bulk_commit();
                 }
             }
             if (OB == 1) {
@@ -1215,10 +1274,18 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
                         } else {
                             if (modded) vm &= mod_bits(a.mask_mod, qrow, key0 + k0, a.window, prefix_lm);
                         }
+                        // (em and vm are uniform across the warp: the branches do not diverge)
+                        if (em == 0xffffffffu) {  // every key exists: valid, or masked to -1e9
+                            if (vm != em) {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            x[32 * hh + j] =
-                                ((vm >> j) & 1u) ? x[32 * hh + j] : (((em >> j) & 1u) ? kMaskVal : -INFINITY);
+                                for (int j = 0; j < 32; ++j) x[32 * hh + j] = ((vm >> j) & 1u) ? x[32 * hh + j] : kMaskVal;
+                            }
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                x[32 * hh + j] =
+                                    ((vm >> j) & 1u) ? x[32 * hh + j] : (((em >> j) & 1u) ? kMaskVal : -INFINITY);
+                        }
                     }
                 }
                 if constexpr (BIAS) {
@@ -1317,6 +1384,8 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
             pe.l = l;
             pe.m_true = m_true;
             if constexpr (!VARLEN) {
+                pe.box_row = it.qt * kBM + wq * 32;
+                pe.box_unit = (int)it.unit;
                 pe.row0 = it.unit * a.Q + qrow;
                 pe.unit0 = (long long)it.b * a.vs[0] + (it.bn - (long long)it.b * a.N) * a.vs[1] +
                            (long long)it.h * a.vs[2];
@@ -1335,6 +1404,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
             pend = true;
         }
         if (ok && pend) ok = epilogue(true);
+        if (P.o_tma && h == 0 && lane == 0) bulk_wait_all();  // this lane quarter's O stores are done
         if (!ok) *abort_flag = 1;
     }
 

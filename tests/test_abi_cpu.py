@@ -64,7 +64,8 @@ def _fwd(**kw):
     (dict(q=MIS), ValueError),
     (dict(qkv_dtype=7), ValueError),
     (dict(bias_dtype=abi.TA_F16), NotImplementedError),  # bias must be fp32 or the q dtype
-    (dict(D=136), NotImplementedError),
+    (dict(D=264), NotImplementedError),  # D <= 256
+    (dict(qkv_dtype=abi.TA_F32, bias_dtype=abi.TA_F32, D=260), NotImplementedError),
     (dict(D=12), NotImplementedError),  # 16-bit needs D % 8
     (dict(K=60), NotImplementedError),  # 16-bit needs K % 8
     (dict(qkv_dtype=abi.TA_F32, bias_dtype=abi.TA_F32, D=6), NotImplementedError),
@@ -114,7 +115,7 @@ def _varlen(**kw):
     (dict(mask_heads=3), ValueError),
     (dict(mask_mod=5), ValueError),
     (dict(block_q=64), NotImplementedError),
-    (dict(D=256), NotImplementedError),
+    (dict(D=264), NotImplementedError),  # D <= 256
 ])
 def test_varlen_host_checks(lib, kw, exc):
     with pytest.raises(exc):

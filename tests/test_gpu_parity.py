@@ -137,6 +137,31 @@ def test_triangle_strided_views(D, dtype):
     compare(c.name, c.dtype, o1, l1, m1, rO, rL, rM)
 
 
+# D in (128, 256] (the page's forward bound for half precision): the CUDA-core kernel,
+# exact fp32 arithmetic, for every input dtype; ragged tiles and kv_lengths extremes.
+@pytest.mark.parametrize("dtype,bias_dtype,D", [("bf16", "bf16", 136), ("bf16", "f32", 192), ("bf16", "bf16", 256),
+                                                ("f16", "f32", 256), ("f16", "f16", 200), ("f32", "f32", 256)])
+def test_wide_head_dims(dtype, bias_dtype, D):
+    c = synth.make_triangle(f"wide_{dtype}_D{D}", 1, 3, 2, 70, 136, D, dtype, bias_dtype, seed=470 + D, mask="kvlen",
+                            kv_range=(0, 136))
+    c.kv_lengths.view(-1)[:3] = torch.tensor([0, 136, 1], dtype=torch.int32)
+    check_triangle(c)
+
+
+def test_wide_head_dim_dense_mask():
+    c = synth.make_triangle("wide_dense", 2, 2, 2, 33, 80, 256, "bf16", "f32", seed=480, mask="dense")
+    c.mask[1, 1] = 0
+    check_triangle(c)
+
+
+@pytest.mark.parametrize("dtype,D", [("bf16", 256), ("f16", 192)])
+@pytest.mark.parametrize("lists", ["causal", "none"])
+def test_varlen_wide_head_dims(dtype, D, lists):
+    c = synth.make_varlen(f"vl_wide_{dtype}_{D}_{lists}", 3, 0, 0, 2, D, dtype, seed=490 + D, lengths=[150, 1, 70],
+                          block_lists=lists, mask_mod="causal")
+    check_varlen(c)
+
+
 @pytest.mark.parametrize("D", [4, 12, 32, 100, 128])
 def test_fp32_head_dims(D):
     c = synth.make_triangle(f"f32_D{D}", 1, 2, 2, 45, 70, D, "f32", "f32", seed=400 + D, mask="kvlen",
