@@ -34,6 +34,7 @@
 #ifndef TRIATTN_H
 #define TRIATTN_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -127,6 +128,52 @@ ta_status tri_attn_fwd_strided(const void* q, const void* k, const void* v, ta_d
                                int B, int N, int H, int Q, int K, int D, float scale,
                                const long long* q_strides, const long long* k_strides, const long long* v_strides,
                                void* out, float* lse, float* max, void* stream);
+
+/*
+ * tri_attn_bwd -- gradients of tri_attn_fwd: dQ, dK, dV and dBias.
+ * (cuEquivariance triangle_attention page, Notes 1: the context is saved for
+ *  backward, and its Example reads q.grad, k.grad, v.grad and bias.grad.)
+ * For a loss L with dL/dO = d_out, per (b, n, h) slab and query row q:
+ *     P = exp(x - lse) (x the forward's logits, -1e9 at masked keys),
+ *     dV[k] = sum_q P dO[q],  dP = dO[q] . V[k],
+ *     dx = P (dP - sum_k' P dP) at valid keys, 0 at masked keys,
+ *     dQ[q] = s sum_k dx K[k],  dK[k] = s sum_q dx Q[q],
+ *     dBias[b, 0, h, q, k] = sum over n of dx[b, n, h, q, k].
+ * A row whose keys are all masked passes no gradient to q, k or the bias; its
+ * uniform weights 1/K still reach dV (such a row is recognised by its stored
+ * lse, -1e9 in fp32; any row with a valid key has lse above -1e9 + 100 by the
+ * forward's precondition on the logits).
+ *
+ *   q, k, v, qkv_dtype, bias, bias_dtype, mask, kv_lengths, B..D, scale
+ *               as given to tri_attn_fwd (contiguous tensors).
+ *   lse         (B, N, H, Q) fp32, the forward's lse output (required).
+ *   d_out       (B, N, H, Q, D) in qkv_dtype: dL/dO.
+ *   dq, dk, dv  (B, N, H, Q|K, D) outputs in qkv_dtype.
+ *   dbias       (B, 1, H, Q, K) output in bias_dtype, or NULL to skip it.
+ *   workspace   device scratch of at least tri_attn_bwd_workspace_size(...)
+ *               bytes, 256-byte aligned, owned by the caller; its contents on
+ *               entry are ignored and on return are unspecified.  Two calls in
+ *               flight must not share a workspace.
+ * Arithmetic: exact fp32 on CUDA cores for every dtype (three kernels: the
+ * per-row sum of P dP, the per-key-tile gradients with dQ and dBias added
+ * atomically in fp32, the conversion to the output dtypes); the summation
+ * order of dQ and dBias therefore varies from run to run within fp32 rounding.
+ * Supported: as tri_attn_fwd (D <= 256).  Errors: NULL required pointer,
+ * misalignment (16 bytes for tensors, 4 for lse / kv_lengths, 256 for the
+ * workspace) or a workspace below the required size -> TA_ERR_INVALID_ARG;
+ * unsupported sizes or dtypes -> TA_ERR_UNSUPPORTED; a launch failure ->
+ * TA_ERR_CUDA.  Asynchronous on `stream`.
+ */
+ta_status tri_attn_bwd(const void* q, const void* k, const void* v, ta_dtype qkv_dtype,
+                       const void* bias, ta_dtype bias_dtype,
+                       const uint8_t* mask, const int32_t* kv_lengths,
+                       int B, int N, int H, int Q, int K, int D, float scale,
+                       const float* lse, const void* d_out,
+                       void* dq, void* dk, void* dv, void* dbias,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace tri_attn_bwd needs for these sizes (0 for a non-positive size). */
+size_t tri_attn_bwd_workspace_size(int B, int N, int H, int Q, int K, int D);
 
 /*
  * tri_attn_varlen_fwd -- packed-sequence forward with a block-sparse mask.

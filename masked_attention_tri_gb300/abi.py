@@ -20,6 +20,7 @@ TA_MASK_NONE, TA_MASK_CAUSAL, TA_MASK_SLIDING_WINDOW, TA_MASK_PREFIX_LM = 0, 1, 
 
 # Every symbol include/triattn.h declares.
 EXPORTS = ("tri_attn_fwd", "tri_attn_fwd_strided", "tri_attn_varlen_fwd", "tri_attn_varlen_fwd_strided", "tri_attn_varlen_fwd_masked",
+           "tri_attn_bwd", "tri_attn_bwd_workspace_size",
            "tri_attn_mask_to_kv_lengths", "tri_attn_get_status", "tri_attn_error_string", "tri_attn_version")
 
 _lock = threading.Lock()
@@ -57,6 +58,11 @@ def load() -> ctypes.CDLL:
         lib.tri_attn_varlen_fwd_masked.argtypes = [P, P, P, I, P, P, I, I, I, I, I, I, I, F, P, P, P, P, I, I, I, I,
                                                    I, I, I, P, I, P, I, L, L, L, P, P, P, P]
         lib.tri_attn_varlen_fwd_masked.restype = I
+        Z = ctypes.c_size_t
+        lib.tri_attn_bwd.argtypes = [P, P, P, I, P, I, P, P, I, I, I, I, I, I, F, P, P, P, P, P, P, P, Z, P]
+        lib.tri_attn_bwd.restype = I
+        lib.tri_attn_bwd_workspace_size.argtypes = [I, I, I, I, I, I]
+        lib.tri_attn_bwd_workspace_size.restype = Z
         lib.tri_attn_mask_to_kv_lengths.argtypes = [P, I, I, I, P, P, P]
         lib.tri_attn_mask_to_kv_lengths.restype = I
         lib.tri_attn_get_status.argtypes = [P]
@@ -90,6 +96,19 @@ def tri_attn_fwd(q, k, v, qkv_dtype, bias, bias_dtype, mask, kv_lengths, B, N, H
     st = load().tri_attn_fwd(q, k, v, qkv_dtype, bias, bias_dtype, mask or None, kv_lengths or None, B, N, H, Q, K,
                              D, float(scale), out, lse or None, max_ or None, stream or None)
     _check(st, "tri_attn_fwd")
+
+
+def tri_attn_bwd(q, k, v, qkv_dtype, bias, bias_dtype, mask, kv_lengths, B, N, H, Q, K, D, scale, lse, d_out, dq, dk,
+                 dv, dbias, workspace, workspace_bytes, stream) -> None:
+    """Gradients of tri_attn_fwd; pointers are ints (0 = NULL), workspace_bytes an int."""
+    st = load().tri_attn_bwd(q, k, v, qkv_dtype, bias, bias_dtype, mask or None, kv_lengths or None, B, N, H, Q, K, D,
+                             float(scale), lse, d_out, dq, dk, dv, dbias or None, workspace, int(workspace_bytes),
+                             stream or None)
+    _check(st, "tri_attn_bwd")
+
+
+def tri_attn_bwd_workspace_size(B, N, H, Q, K, D) -> int:
+    return int(load().tri_attn_bwd_workspace_size(B, N, H, Q, K, D))
 
 
 def _strides4(st):

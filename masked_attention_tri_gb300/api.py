@@ -1,6 +1,7 @@
 """PyTorch-facing API over the C ABI.
 
-Mirrors the cuEquivariance ``triangle_attention`` signature (forward only)
+Mirrors the cuEquivariance ``triangle_attention`` signature (with its
+backward through ``triangle_attention_autograd`` / ``triangle_attention_backward``)
 and adds the packed-sequence entry with a tensorplay-style ``BlockMask``.
 PyTorch provides device memory and the current stream; the work is done by
 libtriattn.so's kernels.  Inputs are used in place (no casts or copies): they
@@ -140,6 +141,98 @@ def triangle_attention(q, k, v, bias, mask=None, scale=None, return_aux=False, *
         if return_aux:
             lse, mx = lse.squeeze(0), mx.squeeze(0)
     return (out, lse, mx) if return_aux else out
+
+
+def triangle_attention_backward(q, k, v, bias, lse, d_out, mask=None, scale=None, *, kv_lengths=None,
+                                need_dbias=True):
+    """Gradients (dq, dk, dv, dbias) of triangle_attention for dL/dO = d_out.
+
+    q, k, v, bias, mask / kv_lengths and scale as given to the forward
+    (contiguous 5-D tensors); lse: the forward's lse (return_aux), fp32 with
+    B*N*H*Q elements; d_out like q.  dbias has the bias's shape and dtype (the
+    sum over n), or is None without need_dbias.  The fp32 workspace is taken
+    from PyTorch's allocator on q's device.
+    """
+    if mask is not None and kv_lengths is not None:
+        raise ValueError("pass either mask or kv_lengths, not both")
+    if q.dim() != 5 or k.dim() != 5 or v.dim() != 5 or bias.dim() != 5:
+        raise ValueError("expected q/k/v (B,N,H,Q|K,D) and bias (B,1,H,Q,K)")
+    B, N, H, Q, D = q.shape
+    K = k.shape[3]
+    if tuple(k.shape) != (B, N, H, K, D) or tuple(v.shape) != (B, N, H, K, D):
+        raise ValueError(f"k/v must be {(B, N, H, K, D)}")
+    if tuple(bias.shape) != (B, 1, H, Q, K):
+        raise ValueError(f"bias must be {(B, 1, H, Q, K)}")
+    if tuple(d_out.shape) != tuple(q.shape) or d_out.dtype != q.dtype:
+        raise ValueError("d_out must have q's shape and dtype")
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("triangle_attention_backward runs on CUDA tensors only")
+    for t, nm in ((q, "q"), (k, "k"), (v, "v"), (bias, "bias"), (lse, "lse"), (d_out, "d_out")):
+        _need(t, nm, dev)
+    if q.dtype not in _DT or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share one dtype among float32 / float16 / bfloat16")
+    if bias.dtype not in (torch.float32, q.dtype):
+        raise TypeError("bias must be float32 or q's dtype")
+    if lse.dtype != torch.float32 or lse.numel() != B * N * H * Q:
+        raise ValueError("lse must be float32 with B*N*H*Q elements")
+    m8 = kl = None
+    if mask is not None:
+        if tuple(mask.shape) != (B, N, 1, 1, K) or mask.dtype not in (torch.bool, torch.uint8, torch.int8):
+            raise ValueError(f"mask must be bool/uint8/int8 {(B, N, 1, 1, K)}")
+        _need(mask, "mask", dev)
+        m8 = mask.view(torch.uint8)
+    if kv_lengths is not None:
+        if kv_lengths.dtype != torch.int32 or kv_lengths.numel() != B * N:
+            raise ValueError("kv_lengths must be int32 with B*N elements")
+        _need(kv_lengths, "kv_lengths", dev)
+        kl = kv_lengths
+    s = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dbias = torch.empty_like(bias) if need_dbias else None
+    nbytes = abi.tri_attn_bwd_workspace_size(B, N, H, Q, K, D)
+    ws = torch.empty(nbytes // 4, dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        abi.tri_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _DT[q.dtype], _ptr(bias), _DT[bias.dtype], _ptr(m8), _ptr(kl),
+                         B, N, H, Q, K, D, s, _ptr(lse), _ptr(d_out), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias),
+                         _ptr(ws), nbytes, _stream(dev))
+    return dq, dk, dv, dbias
+
+
+class _TriangleAttentionFn(torch.autograd.Function):
+    """Autograd node: the forward saves q, k, v, bias, the mask and lse; the
+    backward runs tri_attn_bwd (the page's Notes 1: context saved for backward)."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, bias, mask, kv_lengths, scale):
+        o, lse, mx = triangle_attention(q, k, v, bias, mask, scale, True, kv_lengths=kv_lengths)
+        ctx.save_for_backward(q, k, v, bias, mask, kv_lengths, lse)
+        ctx.scale = scale
+        ctx.mark_non_differentiable(lse, mx)
+        return o, lse, mx
+
+    @staticmethod
+    def backward(ctx, d_out, _d_lse, _d_mx):
+        q, k, v, bias, mask, kv_lengths, lse = ctx.saved_tensors
+        dq, dk, dv, dbias = triangle_attention_backward(q, k, v, bias, lse, d_out.contiguous(), mask, ctx.scale,
+                                                        kv_lengths=kv_lengths, need_dbias=ctx.needs_input_grad[3])
+        return dq, dk, dv, dbias, None, None, None
+
+
+def triangle_attention_autograd(q, k, v, bias, mask=None, scale=None, return_aux=False, *, kv_lengths=None):
+    """triangle_attention with gradients for q, k, v and bias (contiguous 5-D inputs, or the
+    B=1 4-D forms).  Returns O, or (O, lse, max) with return_aux."""
+    four_d = q.dim() == 4
+    if four_d:
+        q, k, v = q.unsqueeze(0), k.unsqueeze(0), v.unsqueeze(0)
+        if bias.dim() == 4:
+            bias = bias.unsqueeze(0)
+        if mask is not None and mask.dim() == 4:
+            mask = mask.unsqueeze(0)
+    o, lse, mx = _TriangleAttentionFn.apply(q, k, v, bias, mask, kv_lengths, scale)
+    if four_d:
+        o, lse, mx = o.squeeze(0), lse.squeeze(0), mx.squeeze(0)
+    return (o, lse, mx) if return_aux else o
 
 
 def mask_to_kv_lengths(mask: torch.Tensor, return_nonprefix: bool = False):

@@ -293,6 +293,65 @@ TA_EXPORT ta_status tri_attn_mask_to_kv_lengths(const uint8_t* mask, int B, int 
     return e == cudaSuccess ? TA_OK : TA_ERR_CUDA;
 }
 
+TA_EXPORT size_t tri_attn_bwd_workspace_size(int B, int N, int H, int Q, int K, int D) {
+    if (B <= 0 || N <= 0 || H <= 0 || Q <= 0 || K <= 0 || D <= 0) return 0;
+    return triattn::bwd_workspace_floats(B, N, H, Q, K, D) * sizeof(float);
+}
+
+TA_EXPORT ta_status tri_attn_bwd(const void* q, const void* k, const void* v, ta_dtype qkv_dtype, const void* bias,
+                                 ta_dtype bias_dtype, const uint8_t* mask, const int32_t* kv_lengths, int B, int N,
+                                 int H, int Q, int K, int D, float scale, const float* lse, const void* d_out,
+                                 void* dq, void* dk, void* dv, void* dbias, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+    if (!q || !k || !v || !bias || !lse || !d_out || !dq || !dk || !dv || !workspace) return TA_ERR_INVALID_ARG;
+    if (B <= 0 || N <= 0 || H <= 0 || Q <= 0 || K <= 0 || D <= 0) return TA_ERR_INVALID_ARG;
+    if (mask && kv_lengths) return TA_ERR_INVALID_ARG;
+    if (!valid_dtype(qkv_dtype) || !valid_dtype(bias_dtype)) return TA_ERR_INVALID_ARG;
+    const void* ptrs16[] = {q, k, v, bias, d_out, dq, dk, dv};
+    for (const void* ptr : ptrs16)
+        if (!aligned(ptr, 16)) return TA_ERR_INVALID_ARG;
+    if ((dbias && !aligned(dbias, 16)) || !aligned(lse, 4) || !aligned(workspace, 256) ||
+        (kv_lengths && !aligned(kv_lengths, 4)))
+        return TA_ERR_INVALID_ARG;
+    if (bias_dtype != TA_F32 && bias_dtype != qkv_dtype) return TA_ERR_UNSUPPORTED;
+    if (!supported_d(qkv_dtype, D)) return TA_ERR_UNSUPPORTED;
+    const long long units = (long long)B * N * H;
+    if (units > (1LL << 40) || units * ((Q + 31) / 32) > 0x7fffffffLL || units * ((K + 31) / 32) > 0x7fffffffLL ||
+        (long long)Q * K >= (1LL << 40))
+        return TA_ERR_UNSUPPORTED;
+    if (workspace_bytes < tri_attn_bwd_workspace_size(B, N, H, Q, K, D)) return TA_ERR_INVALID_ARG;
+
+    triattn::BwdParams p{};
+    float* ws = static_cast<float*>(workspace);
+    auto up = [](size_t n) { return (n + 63) & ~(size_t)63; };
+    p.dq_acc = ws;
+    p.dbias_acc = dbias ? ws + up((size_t)units * Q * D) : nullptr;
+    p.delta = ws + up((size_t)units * Q * D) + up((size_t)B * H * Q * K);
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.bias = bias;
+    p.d_out = d_out;
+    p.mask = mask;
+    p.kv_len = kv_lengths;
+    p.lse = lse;
+    p.dq = dq;
+    p.dk = dk;
+    p.dv = dv;
+    p.dbias = dbias;
+    p.dtype = qkv_dtype;
+    p.bias_f32 = bias_dtype == TA_F32;
+    p.scale = scale;
+    p.B = B;
+    p.N = N;
+    p.H = H;
+    p.Q = Q;
+    p.K = K;
+    p.D = D;
+    const cudaError_t e = triattn::launch_simt_bwd(p, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TA_OK : TA_ERR_CUDA;
+}
+
 TA_EXPORT ta_status tri_attn_get_status(void* stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return TA_ERR_CUDA;
     int* w = triattn::status_word();
@@ -315,4 +374,4 @@ TA_EXPORT const char* tri_attn_error_string(ta_status s) {
     }
 }
 
-TA_EXPORT int tri_attn_version(void) { return (1 << 16) | 2; }
+TA_EXPORT int tri_attn_version(void) { return (1 << 16) | 3; }

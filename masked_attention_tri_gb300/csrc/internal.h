@@ -56,6 +56,31 @@ struct AttnParams {
     long long q_rs, k_rs, v_rs;  // varlen: elements between packed rows of q, k, v (out: H * D)
 };
 
+// Backward of the triangle form (CUDA cores, exact fp32 arithmetic).
+struct BwdParams {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* bias;
+    const void* d_out;
+    const uint8_t* mask;
+    const int32_t* kv_len;
+    const float* lse;       // (B, N, H, Q) from the forward
+    void* dq;
+    void* dk;
+    void* dv;
+    void* dbias;            // (B, 1, H, Q, K) or NULL
+    float* dq_acc;          // workspace: fp32 dQ (B, N, H, Q, D)
+    float* dbias_acc;       // workspace: fp32 dBias (B, H, Q, K), NULL with dbias
+    float* delta;           // workspace: sum_k P dP per query row (B, N, H, Q)
+    int dtype, bias_f32;
+    float scale;
+    int B, N, H, Q, K, D;
+};
+// Workspace of the backward in floats (three pieces, each a multiple of 64 floats).
+size_t bwd_workspace_floats(int B, int N, int H, int Q, int K, int D);
+cudaError_t launch_simt_bwd(const BwdParams& p, cudaStream_t stream);
+
 // CUDA-core path: exact fp32 arithmetic, any dtype, both forms.
 cudaError_t launch_simt_fwd(const AttnParams& p, cudaStream_t stream);
 

@@ -1,0 +1,345 @@
+// simt_bwd.cu -- backward of the triangle-attention forward on CUDA cores
+// (exact fp32 arithmetic for every input dtype).
+//
+// The forward (cuEquivariance triangle_attention page) is
+//     x = s Q.K + bias at valid keys, -1e9 at masked keys;  P = softmax_k(x);  O = P V
+// and its context is saved for backward.  For a loss with dL/dO = dO the chain
+// rule gives, per (b, n, h) slab and query row q:
+//     dV[k]  = sum_q P[q,k] dO[q]
+//     dP     = dO[q] . V[k]
+//     dx     = P (dP - sum_k' P[q,k'] dP[q,k'])   at valid keys, 0 at masked keys
+//     dQ[q]  = s sum_k dx K[k],   dK[k] = s sum_q dx Q[q]
+//     dBias[b,0,h,q,k] = sum_n dx[b,n,h,q,k]
+// P is recomputed from the forward's saved lse: P = exp(x - lse).  A row whose
+// keys are all masked has every logit at -1e9 and lse = -1e9 + ln K, which is
+// -1e9 once stored in fp32; such a row (lse at or below -1e9 + 64, while any
+// valid logit lies above -1e9 + 100) takes its exact weights 1/K.
+//
+// Three kernels:
+//   delta   one CTA per (slab, 32 query rows): delta[q] = sum_k P dP over every key
+//           (the exact definition, not dO . O of the rounded output); zeroes the
+//           fp32 dQ accumulator rows and (grid-stride) the dBias accumulator.
+//   main    one CTA per (slab, 32 keys), looping over the query tiles: dK and dV
+//           of its keys in registers, dQ and dBias added atomically (fp32) into
+//           the caller's workspace.
+//   finish  dQ and dBias accumulators converted to the output dtypes.
+// Layout of one CTA: 4 warps; in the score steps warp w owns query rows
+// 8w..8w+7 and lane j key j; in the accumulation steps warp w owns keys (dK, dV)
+// or rows (dQ) 8w..8w+7 and lane l the columns l + 32c, c < DPL (D <= 32 DPL).
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+
+namespace triattn {
+namespace {
+
+constexpr int kT = 32;      // query rows / keys per tile
+constexpr int kBW = 4;      // warps per CTA
+constexpr int kBR = kT / kBW;  // rows (or keys) per warp
+constexpr float kMaskedLogit = -1.0e9f;
+
+template <typename T>
+__device__ __forceinline__ float ld_f(const T* p, long long i);
+template <>
+__device__ __forceinline__ float ld_f<float>(const float* p, long long i) { return p[i]; }
+template <>
+__device__ __forceinline__ float ld_f<__half>(const __half* p, long long i) { return __half2float(p[i]); }
+template <>
+__device__ __forceinline__ float ld_f<__nv_bfloat16>(const __nv_bfloat16* p, long long i) {
+    return __bfloat162float(p[i]);
+}
+template <typename T>
+__device__ __forceinline__ T to_t(float x);
+template <>
+__device__ __forceinline__ float to_t<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __half to_t<__half>(float x) { return __float2half_rn(x); }
+template <>
+__device__ __forceinline__ __nv_bfloat16 to_t<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+// Softmax weight of an existing key from its logit x and the row's stored lse.
+__device__ __forceinline__ float weight(float x, float lse, float inv_k) {
+    return lse <= kMaskedLogit + 64.f ? inv_k : expf(x - lse);
+}
+
+// Key `key` of (b, n) row bn takes part (kv_lengths prefix, dense mask or every key).
+__device__ __forceinline__ bool key_valid(const BwdParams& p, long long bn, int key) {
+    if (p.kv_len) {
+        int L = p.kv_len[bn];
+        L = L < 0 ? 0 : (L > p.K ? p.K : L);
+        return key < L;
+    }
+    if (p.mask) return p.mask[bn * p.K + key] != 0;
+    return true;
+}
+
+// Loads rows [r0, r0 + 32) of a (rows x D) slab matrix into smem [32][D + 1] as fp32 (zeros past `rows`).
+template <typename T>
+__device__ __forceinline__ void load_tile(float* dst, const T* src, long long base, int r0, int rows, int D) {
+    const int Dp1 = D + 1;
+    for (int e = threadIdx.x; e < kT * D; e += blockDim.x) {
+        const int r = e / D, d = e - r * D;
+        dst[r * Dp1 + d] = (r0 + r < rows) ? ld_f(src, base + (long long)(r0 + r) * D + d) : 0.f;
+    }
+}
+
+// Scores of the tile pair: for warp rows i (query q0 + 8w + i) and lane key j
+// (key k0 + lane) returns x (logit, -1e9 if masked) in x[i] and dP in dp[i].
+__device__ __forceinline__ void scores(const float* Qs, const float* Ks, const float* dOs, const float* Vs, int D,
+                                       int warp, int lane, float (&qk)[kBR], float (&dp)[kBR]) {
+    const int Dp1 = D + 1;
+#pragma unroll
+    for (int i = 0; i < kBR; ++i) qk[i] = dp[i] = 0.f;
+    for (int d = 0; d < D; ++d) {
+        const float kd = Ks[lane * Dp1 + d], vd = Vs[lane * Dp1 + d];
+#pragma unroll
+        for (int i = 0; i < kBR; ++i) {
+            qk[i] = fmaf(Qs[(warp * kBR + i) * Dp1 + d], kd, qk[i]);
+            dp[i] = fmaf(dOs[(warp * kBR + i) * Dp1 + d], vd, dp[i]);
+        }
+    }
+}
+
+template <typename T, typename BT>
+__global__ void __launch_bounds__(kBW * 32) bwd_delta_kernel(const BwdParams p) {
+    extern __shared__ float sm[];
+    const int D = p.D, Dp1 = D + 1;
+    float* Qs = sm;
+    float* dOs = Qs + kT * Dp1;
+    float* Ks = dOs + kT * Dp1;
+    float* Vs = Ks + kT * Dp1;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int nqt = (p.Q + kT - 1) / kT;
+    const long long unit = blockIdx.x / nqt;  // (b*N + n)*H + h
+    const int q0 = (int)(blockIdx.x - unit * nqt) * kT;
+    const int h = (int)(unit % p.H);
+    const long long bn = unit / p.H;
+    const int b = (int)(bn / p.N);
+
+    // dBias accumulator zeroed grid-stride (the main kernel runs after this one).
+    if (p.dbias_acc) {
+        const long long tot = (long long)p.B * p.H * p.Q * p.K;
+        for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < tot; e += (long long)gridDim.x * blockDim.x)
+            p.dbias_acc[e] = 0.f;
+    }
+    const long long qbase = unit * p.Q * D, kbase = unit * (long long)p.K * D;
+    for (int e = threadIdx.x; e < kT * D; e += blockDim.x) {
+        const int r = e / D;
+        if (q0 + r < p.Q) p.dq_acc[qbase + (long long)(q0 + r) * D + (e - r * D)] = 0.f;
+    }
+    load_tile(Qs, static_cast<const T*>(p.q), qbase, q0, p.Q, D);
+    load_tile(dOs, static_cast<const T*>(p.d_out), qbase, q0, p.Q, D);
+    float lse[kBR], acc[kBR];
+#pragma unroll
+    for (int i = 0; i < kBR; ++i) {
+        const int q = q0 + warp * kBR + i;
+        lse[i] = q < p.Q ? p.lse[unit * p.Q + q] : 0.f;
+        acc[i] = 0.f;
+    }
+    const BT* bias = static_cast<const BT*>(p.bias);
+    const long long brow = ((long long)b * p.H + h) * p.Q;
+    for (int k0 = 0; k0 < p.K; k0 += kT) {
+        __syncthreads();
+        load_tile(Ks, static_cast<const T*>(p.k), kbase, k0, p.K, D);
+        load_tile(Vs, static_cast<const T*>(p.v), kbase, k0, p.K, D);
+        __syncthreads();
+        float qk[kBR], dp[kBR];
+        scores(Qs, Ks, dOs, Vs, D, warp, lane, qk, dp);
+        const int key = k0 + lane;
+        const bool exists = key < p.K;
+        const bool valid = exists && key_valid(p, bn, key);
+#pragma unroll
+        for (int i = 0; i < kBR; ++i) {
+            const int q = q0 + warp * kBR + i;
+            if (!exists || q >= p.Q) continue;
+            const float x = valid ? fmaf(p.scale, qk[i], ld_f(bias, (brow + q) * p.K + key)) : kMaskedLogit;
+            acc[i] = fmaf(weight(x, lse[i], 1.f / (float)p.K), dp[i], acc[i]);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < kBR; ++i) {
+        float v = acc[i];
+#pragma unroll
+        for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        const int q = q0 + warp * kBR + i;
+        if (lane == 0 && q < p.Q) p.delta[unit * p.Q + q] = v;
+    }
+}
+
+template <typename T, typename BT, int DPL>
+__global__ void __launch_bounds__(kBW * 32) bwd_main_kernel(const BwdParams p) {
+    extern __shared__ float sm[];
+    const int D = p.D, Dp1 = D + 1;
+    float* Ks = sm;
+    float* Vs = Ks + kT * Dp1;
+    float* Qs = Vs + kT * Dp1;
+    float* dOs = Qs + kT * Dp1;
+    float* Ps = dOs + kT * Dp1;       // [32 rows][33]
+    float* dSs = Ps + kT * (kT + 1);  // [32 rows][33]
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int nkt = (p.K + kT - 1) / kT;
+    const long long unit = blockIdx.x / nkt;
+    const int k0 = (int)(blockIdx.x - unit * nkt) * kT;
+    const int h = (int)(unit % p.H);
+    const long long bn = unit / p.H;
+    const int b = (int)(bn / p.N);
+    const long long qbase = unit * p.Q * D, kbase = unit * (long long)p.K * D;
+
+    load_tile(Ks, static_cast<const T*>(p.k), kbase, k0, p.K, D);
+    load_tile(Vs, static_cast<const T*>(p.v), kbase, k0, p.K, D);
+    const int key = k0 + lane;  // this lane's key in the score steps
+    const bool exists = key < p.K;
+    const bool valid = exists && key_valid(p, bn, key);
+    float dk[kBR][DPL], dv[kBR][DPL];
+#pragma unroll
+    for (int j = 0; j < kBR; ++j)
+#pragma unroll
+        for (int c = 0; c < DPL; ++c) dk[j][c] = dv[j][c] = 0.f;
+    const BT* bias = static_cast<const BT*>(p.bias);
+    const long long brow = ((long long)b * p.H + h) * p.Q;
+
+    for (int q0 = 0; q0 < p.Q; q0 += kT) {
+        __syncthreads();  // the previous tile's Qs, dOs, Ps, dSs are no longer read
+        load_tile(Qs, static_cast<const T*>(p.q), qbase, q0, p.Q, D);
+        load_tile(dOs, static_cast<const T*>(p.d_out), qbase, q0, p.Q, D);
+        __syncthreads();
+        float qk[kBR], dp[kBR];
+        scores(Qs, Ks, dOs, Vs, D, warp, lane, qk, dp);
+#pragma unroll
+        for (int i = 0; i < kBR; ++i) {
+            const int r = warp * kBR + i, q = q0 + r;
+            float P = 0.f, dS = 0.f;
+            if (exists && q < p.Q) {
+                const long long row = unit * p.Q + q;
+                const float x = valid ? fmaf(p.scale, qk[i], ld_f(bias, (brow + q) * p.K + key)) : kMaskedLogit;
+                P = weight(x, p.lse[row], 1.f / (float)p.K);
+                if (valid) {
+                    dS = P * (dp[i] - p.delta[row]);
+                    if (p.dbias_acc) atomicAdd(p.dbias_acc + (brow + q) * p.K + key, dS);
+                }
+            }
+            Ps[r * (kT + 1) + lane] = P;
+            dSs[r * (kT + 1) + lane] = dS;
+        }
+        __syncthreads();
+        // dV[j] += sum_i P[i,j] dO[i],  dK[j] += sum_i dS[i,j] Q[i]   (keys j = 8 warp + jj)
+        for (int i = 0; i < kT; ++i) {
+            float qv[DPL], ov[DPL];
+#pragma unroll
+            for (int c = 0; c < DPL; ++c) {
+                const int d = lane + 32 * c;
+                qv[c] = d < D ? Qs[i * Dp1 + d] : 0.f;
+                ov[c] = d < D ? dOs[i * Dp1 + d] : 0.f;
+            }
+#pragma unroll
+            for (int jj = 0; jj < kBR; ++jj) {
+                const float pv = Ps[i * (kT + 1) + warp * kBR + jj], sv = dSs[i * (kT + 1) + warp * kBR + jj];
+#pragma unroll
+                for (int c = 0; c < DPL; ++c) {
+                    dv[jj][c] = fmaf(pv, ov[c], dv[jj][c]);
+                    dk[jj][c] = fmaf(sv, qv[c], dk[jj][c]);
+                }
+            }
+        }
+        // dQ[i] += s sum_j dS[i,j] K[j]   (rows i = 8 warp + ii), added to the fp32 accumulator
+        float dq[kBR][DPL];
+#pragma unroll
+        for (int ii = 0; ii < kBR; ++ii)
+#pragma unroll
+            for (int c = 0; c < DPL; ++c) dq[ii][c] = 0.f;
+        for (int j = 0; j < kT; ++j) {
+            float kv[DPL];
+#pragma unroll
+            for (int c = 0; c < DPL; ++c) {
+                const int d = lane + 32 * c;
+                kv[c] = d < D ? Ks[j * Dp1 + d] : 0.f;
+            }
+#pragma unroll
+            for (int ii = 0; ii < kBR; ++ii) {
+                const float sv = dSs[(warp * kBR + ii) * (kT + 1) + j];
+#pragma unroll
+                for (int c = 0; c < DPL; ++c) dq[ii][c] = fmaf(sv, kv[c], dq[ii][c]);
+            }
+        }
+#pragma unroll
+        for (int ii = 0; ii < kBR; ++ii) {
+            const int q = q0 + warp * kBR + ii;
+            if (q >= p.Q) continue;
+#pragma unroll
+            for (int c = 0; c < DPL; ++c) {
+                const int d = lane + 32 * c;
+                if (d < D && dq[ii][c] != 0.f) atomicAdd(p.dq_acc + qbase + (long long)q * D + d, p.scale * dq[ii][c]);
+            }
+        }
+    }
+    T* dkp = static_cast<T*>(p.dk);
+    T* dvp = static_cast<T*>(p.dv);
+#pragma unroll
+    for (int jj = 0; jj < kBR; ++jj) {
+        const int kk = k0 + warp * kBR + jj;
+        if (kk >= p.K) continue;
+#pragma unroll
+        for (int c = 0; c < DPL; ++c) {
+            const int d = lane + 32 * c;
+            if (d < D) {
+                dkp[kbase + (long long)kk * D + d] = to_t<T>(p.scale * dk[jj][c]);
+                dvp[kbase + (long long)kk * D + d] = to_t<T>(dv[jj][c]);
+            }
+        }
+    }
+}
+
+template <typename T, typename BT>
+__global__ void bwd_finish_kernel(const BwdParams p) {
+    const long long nq = (long long)p.B * p.N * p.H * p.Q * p.D;
+    const long long nb = p.dbias ? (long long)p.B * p.H * p.Q * p.K : 0;
+    T* dq = static_cast<T*>(p.dq);
+    BT* db = static_cast<BT*>(p.dbias);
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < nq; e += stride) dq[e] = to_t<T>(p.dq_acc[e]);
+    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < nb; e += stride)
+        db[e] = to_t<BT>(p.dbias_acc[e]);
+}
+
+template <typename T, typename BT>
+cudaError_t launch_typed(const BwdParams& p, cudaStream_t stream) {
+    const int D = p.D;
+    const long long units = (long long)p.B * p.N * p.H;
+    const size_t sm1 = sizeof(float) * 4 * kT * (size_t)(D + 1);
+    const size_t sm2 = sm1 + sizeof(float) * 2 * kT * (kT + 1);
+    auto k1 = bwd_delta_kernel<T, BT>;
+    auto k2 = D <= 128 ? bwd_main_kernel<T, BT, 4> : bwd_main_kernel<T, BT, 8>;
+    cudaError_t e;
+    if ((e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1)) != cudaSuccess) return e;
+    if ((e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2)) != cudaSuccess) return e;
+    const long long g1 = units * ((p.Q + kT - 1) / kT), g2 = units * ((p.K + kT - 1) / kT);
+    if (g1 > 0x7fffffffLL || g2 > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    k1<<<(unsigned)g1, kBW * 32, sm1, stream>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    k2<<<(unsigned)g2, kBW * 32, sm2, stream>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    bwd_finish_kernel<T, BT><<<1024, 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t bwd_workspace_floats(int B, int N, int H, int Q, int K, int D) {
+    auto up = [](size_t n) { return (n + 63) & ~(size_t)63; };  // 256-byte pieces
+    const size_t units = (size_t)B * N * H;
+    return up(units * Q * D) + up((size_t)B * H * Q * K) + up(units * Q);
+}
+
+cudaError_t launch_simt_bwd(const BwdParams& p, cudaStream_t stream) {
+    switch (p.dtype) {
+    case TA_F32: return launch_typed<float, float>(p, stream);
+    case TA_F16: return p.bias_f32 ? launch_typed<__half, float>(p, stream) : launch_typed<__half, __half>(p, stream);
+    default:
+        return p.bias_f32 ? launch_typed<__nv_bfloat16, float>(p, stream)
+                          : launch_typed<__nv_bfloat16, __nv_bfloat16>(p, stream);
+    }
+}
+
+}  // namespace triattn

@@ -142,6 +142,12 @@ def make_triangle(
     return TriangleCase(name, B, N, H, Q, K, D, dtype, bias_dtype, q, k, v, bias, m, kvl, s)
 
 
+def grad_out(case: TriangleCase, seed: int, std: float = 1.0) -> torch.Tensor:
+    """A seeded dL/dO for a triangle case: standard normal (times std) in the case's dtype, q's shape."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    return _randn(g, tuple(case.q.shape), std, case.dtype)
+
+
 def page_example_kv_lengths(seq_len: int = 128, valid: int = 96) -> torch.Tensor:
     """The key mask of the triangle_attention API page's example (row_valid & col_valid).
 

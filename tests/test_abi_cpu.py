@@ -76,6 +76,42 @@ def test_triangle_host_checks(lib, kw, exc):
         _fwd(**kw)()
 
 
+def _bwd(**kw):
+    ws = abi.tri_attn_bwd_workspace_size(1, 2, 2, 64, 64, 64)
+    args = dict(q=A, k=A, v=A, qkv_dtype=abi.TA_BF16, bias=A, bias_dtype=abi.TA_BF16, mask=0, kv_lengths=0, B=1, N=2,
+                H=2, Q=64, K=64, D=64, scale=0.125, lse=A, d_out=A, dq=A, dk=A, dv=A, dbias=A, workspace=A,
+                workspace_bytes=ws, stream=0)
+    args.update(kw)
+    return lambda: abi.tri_attn_bwd(**args)
+
+
+def test_bwd_workspace_size(lib):
+    # fp32 dQ (B*N*H*Q*D), dBias (B*H*Q*K) and the per-row sums (B*N*H*Q), each rounded up to 64 floats
+    up = lambda n: (n + 63) // 64 * 64
+    assert abi.tri_attn_bwd_workspace_size(1, 2, 3, 70, 90, 40) == 4 * (up(6 * 70 * 40) + up(3 * 70 * 90) + up(6 * 70))
+    assert abi.tri_attn_bwd_workspace_size(0, 2, 3, 70, 90, 40) == 0
+
+
+@pytest.mark.parametrize("kw,exc", [
+    (dict(q=0), ValueError),
+    (dict(lse=0), ValueError),          # the forward's lse is required
+    (dict(d_out=0), ValueError),
+    (dict(dk=0), ValueError),
+    (dict(workspace=0), ValueError),
+    (dict(workspace=A + 16), ValueError),  # 256-byte aligned workspace
+    (dict(workspace_bytes=1024), ValueError),  # below the required size
+    (dict(dq=MIS), ValueError),
+    (dict(mask=A, kv_lengths=A), ValueError),
+    (dict(Q=0), ValueError),
+    (dict(bias_dtype=abi.TA_F16), NotImplementedError),
+    (dict(D=264), NotImplementedError),
+    (dict(D=12), NotImplementedError),
+])
+def test_bwd_host_checks(lib, kw, exc):
+    with pytest.raises(exc):
+        _bwd(**kw)()
+
+
 def _fwd_strided(**kw):
     args = dict(q=A, k=A, v=A, qkv_dtype=abi.TA_BF16, bias=A, bias_dtype=abi.TA_BF16, mask=0, kv_lengths=0, B=1, N=2,
                 H=2, Q=64, K=64, D=64, scale=0.125, q_strides=None, k_strides=None, v_strides=None, out=A, lse=0,

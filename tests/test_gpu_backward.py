@@ -1,0 +1,111 @@
+"""GPU parity of the backward (tri_attn_bwd) with the fp64 backward oracle.
+
+The oracle (oracle/backward.py) is the chain rule through the triangle_attention
+page's formula, pinned on the CPU by finite differences, torch autograd and
+closed forms.  The library recomputes P from the forward's own lse and works in
+fp32 on CUDA cores; dQ and dBias are summed with fp32 atomics.
+
+Tolerance, per gradient g against the oracle r (element-wise):
+    |g - r| <= atol * max|r| + rtol * |r|
+with (atol, rtol) = (1e-4, 1e-3) for fp32 inputs (fp32 arithmetic, summation
+order varies) and (1e-2, 1e-2) for fp16 / bf16 inputs (one rounding of each
+output to the 16-bit type, 2^-9 relative for bf16, on top of fp32 arithmetic).
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.backward as obwd
+import synth
+from parity_helpers import to_gpu
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": (1e-4, 1e-3), "f16": (1e-2, 1e-2), "bf16": (1e-2, 1e-2)}
+
+
+def _close(name, dtype, got, ref):
+    atol, rtol = TOL[dtype]
+    g = got.detach().float().cpu().double().numpy().reshape(ref.shape)
+    assert np.isfinite(g).all(), f"{name}: non-finite values"
+    scale = max(float(np.abs(ref).max()), 1e-30)
+    err = np.abs(g - ref)
+    bound = atol * scale + rtol * np.abs(ref)
+    worst = np.unravel_index(np.argmax(err - bound), err.shape)
+    assert (err <= bound).all(), (f"{name}: |g - r| = {err[worst]:.3e} > {bound[worst]:.3e} at {worst} "
+                                  f"(g {g[worst]:.6e}, r {ref[worst]:.6e}, max|r| {scale:.3e})")
+
+
+def _run(case, seed, need_dbias=True, use_autograd=False):
+    import masked_attention_tri_gb300 as ta
+    d_out = synth.grad_out(case, seed)
+    q, k, v, bias = (to_gpu(x) for x in (case.q, case.k, case.v, case.bias))
+    mask, kl = to_gpu(case.mask), to_gpu(case.kv_lengths)
+    if use_autograd:
+        q, k, v, bias = (t.clone().requires_grad_(True) for t in (q, k, v, bias))
+        o = ta.triangle_attention_autograd(q, k, v, bias, mask, case.scale, kv_lengths=kl)
+        o.backward(d_out.cuda())
+        torch.cuda.synchronize()
+        grads = (q.grad, k.grad, v.grad, bias.grad)
+    else:
+        _, lse, _ = ta.triangle_attention(q, k, v, bias, mask, case.scale, True, kv_lengths=kl)
+        grads = ta.triangle_attention_backward(q, k, v, bias, lse, d_out.cuda(), mask, case.scale, kv_lengths=kl,
+                                               need_dbias=need_dbias)
+        torch.cuda.synchronize()
+    assert ta.get_status() == 0
+    ref = obwd.tri_bwd(case.q, case.k, case.v, case.bias, d_out, mask=case.mask, kv_lengths=case.kv_lengths,
+                       scale=case.scale)
+    return grads, ref
+
+
+def _check(case, seed, **kw):
+    grads, ref = _run(case, seed, **kw)
+    for nm, g, r in zip(("dq", "dk", "dv", "dbias"), grads, ref):
+        if g is None:
+            continue
+        assert g.dtype == (case.bias.dtype if nm == "dbias" else case.q.dtype), nm
+        _close(f"{case.name}:{nm}", case.dtype, g, r)
+
+
+# dtypes x bias dtypes x masks; ragged Q and K (not multiples of the 32-row tiles), N > 1 for
+# the sum of dBias over n, kv_lengths extremes (0: every key masked, K, beyond K).
+@pytest.mark.parametrize("dtype,bias_dtype,mask,D", [
+    ("bf16", "bf16", "kvlen", 64), ("bf16", "f32", "dense", 32), ("f16", "f32", "none", 128),
+    ("f16", "f16", "kvlen", 16), ("f32", "f32", "kvlen", 40), ("f32", "f32", "dense", 8),
+])
+def test_backward_matches_oracle(dtype, bias_dtype, mask, D):
+    K = 70 if dtype == "f32" else 72  # 16-bit inputs need K % 8 == 0 (the forward's rule)
+    c = synth.make_triangle(f"bwd_{dtype}_{bias_dtype}_{mask}_{D}", 2, 3, 2, 45, K, D, dtype, bias_dtype,
+                            seed=700 + D, mask=mask, kv_range=(0, K))
+    if mask == "kvlen":
+        c.kv_lengths.view(-1)[:3] = torch.tensor([0, K, 1000], dtype=torch.int32)
+    if mask == "dense":
+        c.mask[0, 1] = 0  # a row block with every key masked
+    _check(c, 710 + D)
+
+
+@pytest.mark.parametrize("D", [136, 256])
+def test_backward_wide_head_dims(D):
+    c = synth.make_triangle(f"bwd_wide_{D}", 1, 2, 2, 33, 40, D, "bf16", "f32", seed=720 + D, mask="kvlen",
+                            kv_range=(1, 40))
+    _check(c, 730 + D)
+
+
+def test_backward_without_dbias_and_large_logits():
+    c = synth.make_triangle("bwd_large", 1, 2, 2, 64, 96, 64, "bf16", "bf16", seed=740, bias_std=8.0, scale=0.5,
+                            mask="kvlen", kv_range=(10, 96))
+    _check(c, 741, need_dbias=False)
+
+
+def test_autograd_wrapper():
+    """torch autograd through triangle_attention_autograd gives the same gradients."""
+    c = synth.make_triangle("bwd_autograd", 1, 2, 3, 50, 64, 32, "bf16", "f32", seed=750, mask="dense")
+    _check(c, 751, use_autograd=True)
+
+
+def test_backward_page_example_shape():
+    """The page's Example shapes at a smaller sequence length: fp16, bias and mask from kv_lengths."""
+    c = synth.make_triangle("bwd_page", 1, 4, 2, 64, 64, 32, "f16", "f16", seed=760, mask="kvlen", kv_range=(48, 64))
+    _check(c, 761)
