@@ -175,6 +175,33 @@ ta_status tri_attn_bwd(const void* q, const void* k, const void* v, ta_dtype qkv
 /* Bytes of workspace tri_attn_bwd needs for these sizes (0 for a non-positive size). */
 size_t tri_attn_bwd_workspace_size(int B, int N, int H, int Q, int K, int D);
 
+/* Size of the fixed device scratch tri_attn_bwd_noalloc works in (bytes). */
+#define TRI_ATTN_BWD_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * tri_attn_bwd_noalloc -- tri_attn_bwd without a caller workspace and without
+ * any allocation.  The source pages have no counterpart of this call: it is a
+ * library-side variant of tri_attn_bwd for callers that may not allocate.
+ *
+ * Arguments, results and errors as tri_attn_bwd, minus workspace and
+ * workspace_bytes.  The scratch is a static device array of
+ * TRI_ATTN_BWD_NOALLOC_SCRATCH_BYTES bytes inside the library (one per
+ * device); its address is looked up once per device.  The call itself
+ * allocates no memory of any kind.  It needs no zeroed scratch: the backward's
+ * first kernel zeroes the accumulators it uses on every call.
+ *   A problem whose tri_attn_bwd_workspace_size exceeds the scratch ->
+ *   TA_ERR_UNSUPPORTED (nothing is launched); use tri_attn_bwd then.
+ *   Calls in flight at the same time on one device (on any streams, from any
+ *   threads) share the scratch and race: the caller must order them, e.g. by
+ *   issuing them on one stream.
+ */
+ta_status tri_attn_bwd_noalloc(const void* q, const void* k, const void* v, ta_dtype qkv_dtype,
+                               const void* bias, ta_dtype bias_dtype,
+                               const uint8_t* mask, const int32_t* kv_lengths,
+                               int B, int N, int H, int Q, int K, int D, float scale,
+                               const float* lse, const void* d_out,
+                               void* dq, void* dk, void* dv, void* dbias, void* stream);
+
 /*
  * tri_attn_varlen_fwd -- packed-sequence forward with a block-sparse mask.
  * (Transformer Engine 0.9 fused_attn.h: NVTE_NOT_INTERLEAVED layout,

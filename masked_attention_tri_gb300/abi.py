@@ -20,7 +20,7 @@ TA_MASK_NONE, TA_MASK_CAUSAL, TA_MASK_SLIDING_WINDOW, TA_MASK_PREFIX_LM = 0, 1, 
 
 # Every symbol include/triattn.h declares.
 EXPORTS = ("tri_attn_fwd", "tri_attn_fwd_strided", "tri_attn_varlen_fwd", "tri_attn_varlen_fwd_strided", "tri_attn_varlen_fwd_masked",
-           "tri_attn_bwd", "tri_attn_bwd_workspace_size",
+           "tri_attn_bwd", "tri_attn_bwd_workspace_size", "tri_attn_bwd_noalloc",
            "tri_attn_mask_to_kv_lengths", "tri_attn_get_status", "tri_attn_error_string", "tri_attn_version")
 
 _lock = threading.Lock()
@@ -61,6 +61,8 @@ def load() -> ctypes.CDLL:
         Z = ctypes.c_size_t
         lib.tri_attn_bwd.argtypes = [P, P, P, I, P, I, P, P, I, I, I, I, I, I, F, P, P, P, P, P, P, P, Z, P]
         lib.tri_attn_bwd.restype = I
+        lib.tri_attn_bwd_noalloc.argtypes = [P, P, P, I, P, I, P, P, I, I, I, I, I, I, F, P, P, P, P, P, P, P]
+        lib.tri_attn_bwd_noalloc.restype = I
         lib.tri_attn_bwd_workspace_size.argtypes = [I, I, I, I, I, I]
         lib.tri_attn_bwd_workspace_size.restype = Z
         lib.tri_attn_mask_to_kv_lengths.argtypes = [P, I, I, I, P, P, P]
@@ -105,6 +107,18 @@ def tri_attn_bwd(q, k, v, qkv_dtype, bias, bias_dtype, mask, kv_lengths, B, N, H
                              float(scale), lse, d_out, dq, dk, dv, dbias or None, workspace, int(workspace_bytes),
                              stream or None)
     _check(st, "tri_attn_bwd")
+
+
+def tri_attn_bwd_noalloc(q, k, v, qkv_dtype, bias, bias_dtype, mask, kv_lengths, B, N, H, Q, K, D, scale, lse, d_out,
+                         dq, dk, dv, dbias, stream) -> None:
+    """tri_attn_bwd in the library's own static scratch (no workspace, no allocation)."""
+    st = load().tri_attn_bwd_noalloc(q, k, v, qkv_dtype, bias, bias_dtype, mask or None, kv_lengths or None, B, N, H,
+                                     Q, K, D, float(scale), lse, d_out, dq, dk, dv, dbias or None, stream or None)
+    _check(st, "tri_attn_bwd_noalloc")
+
+
+# Bytes of the static scratch tri_attn_bwd_noalloc works in (TRI_ATTN_BWD_NOALLOC_SCRATCH_BYTES).
+BWD_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 def tri_attn_bwd_workspace_size(B, N, H, Q, K, D) -> int:

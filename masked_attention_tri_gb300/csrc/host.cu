@@ -352,6 +352,42 @@ TA_EXPORT ta_status tri_attn_bwd(const void* q, const void* k, const void* v, ta
     return e == cudaSuccess ? TA_OK : TA_ERR_CUDA;
 }
 
+// Scratch of tri_attn_bwd_noalloc: a fixed-size array that is part of the
+// library's device image (one copy per device, present from module load), so a
+// call allocates nothing.  Its address is looked up once per device.
+static __device__ __align__(256) float g_bwd_noalloc_scratch[TRI_ATTN_BWD_NOALLOC_SCRATCH_BYTES / sizeof(float)];
+
+namespace {
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {};
+
+void* bwd_noalloc_scratch() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_bwd_noalloc_scratch) != cudaSuccess) return nullptr;
+        g_noalloc_ptr[dev] = ptr;
+    }
+    return g_noalloc_ptr[dev];
+}
+}  // namespace
+
+TA_EXPORT ta_status tri_attn_bwd_noalloc(const void* q, const void* k, const void* v, ta_dtype qkv_dtype,
+                                         const void* bias, ta_dtype bias_dtype, const uint8_t* mask,
+                                         const int32_t* kv_lengths, int B, int N, int H, int Q, int K, int D,
+                                         float scale, const float* lse, const void* d_out, void* dq, void* dk,
+                                         void* dv, void* dbias, void* stream) {
+    // A problem whose workspace exceeds the static scratch is refused before anything runs.
+    if (tri_attn_bwd_workspace_size(B, N, H, Q, K, D) > (size_t)TRI_ATTN_BWD_NOALLOC_SCRATCH_BYTES)
+        return TA_ERR_UNSUPPORTED;
+    void* ws = bwd_noalloc_scratch();
+    if (!ws) return TA_ERR_CUDA;
+    return tri_attn_bwd(q, k, v, qkv_dtype, bias, bias_dtype, mask, kv_lengths, B, N, H, Q, K, D, scale, lse, d_out,
+                        dq, dk, dv, dbias, ws, (size_t)TRI_ATTN_BWD_NOALLOC_SCRATCH_BYTES, stream);
+}
+
 TA_EXPORT ta_status tri_attn_get_status(void* stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return TA_ERR_CUDA;
     int* w = triattn::status_word();
