@@ -962,11 +962,15 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
                 ++s_it;
                 tc_fence_after();
 
-                // ---- Pass 1, two chunks of 64 keys: x = s S + bias (or raw S in the
-                // folded form), masking at a boundary, running max; x goes back to
-                // the chunk's TMEM columns.  The loops stay rolled so that the
-                // softmax code fits the instruction cache next to the other roles.
-                float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+                // ---- Two chunks of 64 keys, one pass each: x = s S + bias (or raw S in
+                // the folded form), masking at a boundary, the chunk max, then
+                // P = 2^((x - m_ref) log2 e) into columns [32c, 32c + 32) as 16-bit
+                // pairs (chunk c's values are in registers before any is overwritten).
+                // The reference max m_ref follows the running max lazily: it is raised
+                // only when the max grows by more than 2^kRescaleLog2, and raising it
+                // scales O (complete through this slot's previous tile), l and, within
+                // a tile, chunk 0's P.  The loops stay rolled so that the softmax code
+                // fits the instruction cache next to the other roles.
 #pragma unroll 1
                 for (int c = 0; c < 2; ++c) {
                     float x[64];
@@ -1040,6 +1044,12 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
                                     ((vm >> j) & 1u) ? x[32 * h + j] : (((em >> j) & 1u) ? kMaskVal : -INFINITY);
                         }
                     }
+                    if (!VARLEN && c == 1) {
+                        __syncwarp();  // every lane of the warp has read its bias row and the mask words
+                        if (lane == 0) mbar_arrive(bias_empty(slot, bs));
+                        br.next(BS);
+                    }
+                    float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
 #pragma unroll
                     for (int j = 0; j < 64; j += 8) {
                         m0 = max3(m0, x[j], x[j + 1]);
@@ -1047,78 +1057,64 @@ __global__ void __launch_bounds__(kThreads<NQ>, 1) tc_fwd_kernel(const __grid_co
                         m2 = max3(m2, x[j + 4], x[j + 5]);
                         m3 = max3(m3, x[j + 6], x[j + 7]);
                     }
-                    if (!FOLD || !all_valid) {  // unmasked folded values are S itself
-                        uint32_t xs[64];
+                    // Chunk max (units of this form) and its logit in natural units.
+                    const float cm = fmaxf(max3(m0, m1, m2), m3);
+                    float cm_nat;
+                    if constexpr (FOLD) cm_nat = cm > -FLT_MAX ? cm * a.scale : (cm == -FLT_MAX ? kMasked : -INFINITY);
+                    else cm_nat = cm;
+                    m_true = fmaxf(m_true, cm_nat);
+                    if (jv == 0 && c == 0) {
+                        m_ref = cm;
+                        l = 0.f;
+                    } else {
+                        const float m_new = fmaxf(m_ref, cm);
+                        const bool need = (m_new - m_ref) * unit_l2e > kRescaleLog2;
+                        if (__any_sync(0xffffffffu, need)) {
+                            const float alpha = ex2((m_ref - m_new) * unit_l2e);
+                            l *= alpha;
+                            m_ref = m_new;
+                            if (jv > 0) {
+                                for (uint32_t c0 = 0; c0 < P.o_cols; c0 += 16) {
+                                    uint32_t o[16];
+                                    tmem_ld_x16(o_taddr + c0, o);
 #pragma unroll
-                        for (int j = 0; j < 64; ++j) xs[j] = __float_as_uint(x[j]);
-                        tmem_st_x64(s_taddr + 64 * c, xs);
-                    }
-                }
-                if constexpr (!VARLEN) {
-                    __syncwarp();  // every lane of the warp has read its bias row and the mask words
-                    if (lane == 0) mbar_arrive(bias_empty(slot, bs));
-                    br.next(BS);
-                }
-                tmem_st_wait();  // pass 2 reads what pass 1 wrote
-
-                // ---- Tile max (units of this form) and its logit in natural units.
-                const float tm = fmaxf(max3(m0, m1, m2), m3);
-                float tm_nat;
-                if constexpr (FOLD) tm_nat = tm > -FLT_MAX ? tm * a.scale : (tm == -FLT_MAX ? kMasked : -INFINITY);
-                else tm_nat = tm;
-                m_true = fmaxf(m_true, tm_nat);
-                // Reference max m_ref (units of this form) used in the exponent.
-                if (jv == 0) {
-                    m_ref = tm;
-                    l = 0.f;
-                } else {
-                    const float m_new = fmaxf(m_ref, tm);
-                    const bool need = (m_new - m_ref) * unit_l2e > kRescaleLog2;
-                    if (__any_sync(0xffffffffu, need)) {
-                        // Raise the reference max to the current one; O (complete
-                        // through this slot's previous tile, whose PV finished
-                        // before this S was committed) and l scale by alpha.
-                        const float alpha = ex2((m_ref - m_new) * unit_l2e);
-                        l *= alpha;
-                        m_ref = m_new;
-                        for (uint32_t c0 = 0; c0 < P.o_cols; c0 += 16) {
-                            uint32_t o[16];
-                            tmem_ld_x16(o_taddr + c0, o);
+                                    for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                                    tmem_st_x16(o_taddr + c0, o);
+                                }
+                            }
+                            if (c == 1) {  // chunk 0's P, already in columns [0, 32)
+                                tmem_st_wait();
+                                uint32_t pr[32];
+                                tmem_ld_x32(s_taddr, pr);
 #pragma unroll
-                            for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                            tmem_st_x16(o_taddr + c0, o);
+                                for (int j = 0; j < 32; ++j) {
+                                    const float2 pv = unpack2<BF16>(pr[j]);
+                                    pr[j] = pack2<BF16>(pv.x * alpha, pv.y * alpha);
+                                }
+                                tmem_st_x32(s_taddr, pr);
+                            }
                         }
                     }
-                }
-
-                // ---- P = 2^((x - m_ref) log2 e), packed to 16-bit pairs (keys 2i,
-                // 2i+1 in column i).  A row with no real logit yet (every
-                // value masked or absent) takes weights of exactly 1 for masked
-                // keys and 0 for absent ones: x + (-kMaskVal) is then 0 or -inf.
-                const bool live = m_ref > kMaskVal;
-                const float2 ul2 = live ? make_float2(unit_l2e, unit_l2e) : make_float2(1.f, 1.f);
-                const float nb = live ? -m_ref * unit_l2e : -kMaskVal;
-                const float2 nb2 = make_float2(nb, nb);
-                float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-                // ---- Pass 2, two chunks of 64 keys: P into columns [32c, 32c + 32)
-                // (chunk c's values were read before any of them is overwritten).
-#pragma unroll 1
-                for (int c = 0; c < 2; ++c) {
-                    uint32_t xr[64];
-                    tmem_ld_x64(s_taddr + 64 * c, xr);
+                    // A row with no real logit yet (every value masked or absent) takes
+                    // weights of exactly 1 for masked keys and 0 for absent ones:
+                    // x + (-kMaskVal) is then 0 or -inf.
+                    const bool live = m_ref > kMaskVal;
+                    const float2 ul2 = live ? make_float2(unit_l2e, unit_l2e) : make_float2(1.f, 1.f);
+                    const float nb = live ? -m_ref * unit_l2e : -kMaskVal;
+                    const float2 nb2 = make_float2(nb, nb);
+                    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
                     uint32_t pk[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
-                        const float2 y =
-                            __ffma2_rn(make_float2(__uint_as_float(xr[2 * j]), __uint_as_float(xr[2 * j + 1])), ul2, nb2);
+                        const float2 y = __ffma2_rn(make_float2(x[2 * j], x[2 * j + 1]), ul2, nb2);
                         const float2 p = make_float2(ex2(y.x), ex2(y.y));
                         if (j & 1) acc1 = __fadd2_rn(acc1, p);
                         else acc0 = __fadd2_rn(acc0, p);
                         pk[j] = pack2<BF16>(p.x, p.y);
                     }
                     tmem_st_x32(s_taddr + 32 * c, pk);
+                    l += (acc0.x + acc0.y) + (acc1.x + acc1.y);
                 }
-                l += (acc0.x + acc0.y) + (acc1.x + acc1.y);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();  // one arrival per warp once all its lanes' P is in TMEM
