@@ -47,13 +47,14 @@ ESIZE = {"f32": 4, "f16": 2, "bf16": 2}
 
 
 def kernel_source_hash() -> str:
-    """SHA-256 over the library's CUDA sources and public headers (path + content)."""
+    """SHA-256 over the sources of the tensor-core forward kernels (path + content): tc_*.cu,
+    tc_*.cuh, tmem_io.h and internal.h.  The CUDA-core kernels, the backward and the host entry
+    points do not change what the measured kernels do, so they are left out."""
     import glob
     import hashlib
-    files = sorted(glob.glob(os.path.join(ROOT, "masked_attention_tri_gb300", "csrc", "*.cu")) +
-                   glob.glob(os.path.join(ROOT, "masked_attention_tri_gb300", "csrc", "*.cuh")) +
-                   glob.glob(os.path.join(ROOT, "masked_attention_tri_gb300", "csrc", "*.h")) +
-                   glob.glob(os.path.join(ROOT, "include", "*.h")))
+    cs = os.path.join(ROOT, "masked_attention_tri_gb300", "csrc")
+    files = sorted(glob.glob(os.path.join(cs, "tc_*.cu")) + glob.glob(os.path.join(cs, "tc_*.cuh")) +
+                   [os.path.join(cs, "tmem_io.h"), os.path.join(cs, "internal.h")])
     h = hashlib.sha256()
     for f in files:
         h.update(os.path.relpath(f, ROOT).encode())
