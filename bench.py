@@ -374,9 +374,10 @@ def e2e_triangle(ta, c, dev, steps, warmup):
     return e0.elapsed_time(e1) / steps, h2d, d2h
 
 
-def cpu_oracle_sample(c, budget_s: float, max_slabs=None):
+def cpu_oracle_sample(c, budget_s: float, max_slabs=None, t_slab=None):
     """Time the oracle (as it stands) on whole (b,n) slabs of the workload; returns
-    (effective TFLOP/s, seconds, slabs, threads)."""
+    (effective TFLOP/s, seconds, slabs, threads).  The sample size comes from the time of one
+    slab: measured here, or `t_slab` seconds when the caller measured it already."""
     import numpy as np
     import oracle
     threads = oracle.default_threads()
@@ -390,10 +391,13 @@ def cpu_oracle_sample(c, budget_s: float, max_slabs=None):
     kv = kv_valid(c).reshape(-1)
     order = [int(i) for i in torch.argsort(kv, descending=True)[: max(1, nslab_total)]]
     probe = [order[len(order) // 2]]
-    t0 = time.perf_counter()
-    oracle.tri_fwd(c.q, c.k, c.v, c.bias, mask=c.mask, kv_lengths=c.kv_lengths, scale=c.scale, rows=rows_of(probe),
-                   threads=threads)
-    t1 = time.perf_counter() - t0
+    if t_slab is None:
+        t0 = time.perf_counter()
+        oracle.tri_fwd(c.q, c.k, c.v, c.bias, mask=c.mask, kv_lengths=c.kv_lengths, scale=c.scale,
+                       rows=rows_of(probe), threads=threads)
+        t1 = time.perf_counter() - t0
+    else:
+        t1 = t_slab
     n = max(1, min(nslab_total, int(budget_s / max(t1, 1e-6))))
     if max_slabs:
         n = min(n, max_slabs)
@@ -440,12 +444,15 @@ def run_reference(args, world, rank):
     if rank != 0:
         return
     c = synth.TRIANGLE_WORKLOADS[args.workload]()
-    budget = max(1.0, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    # The whole run stays near 150 s of oracle work: each step is a sample of
+    # 150 / (steps + warmup) seconds (at least one slab), sized from one slab's time.
+    budget = min(10.0, 150.0 / max(1, args.steps + args.warmup))
+    _, t_slab, _, _ = cpu_oracle_sample(c, 0.0, max_slabs=1)
     vals = []
     times = []
     info = None
     for i in range(args.warmup + args.steps):
-        v, dt, slabs, threads = cpu_oracle_sample(c, budget)
+        v, dt, slabs, threads = cpu_oracle_sample(c, budget, t_slab=t_slab)
         if i >= args.warmup:
             vals.append(v)
             times.append(dt)
