@@ -147,6 +147,10 @@ ta_status tri_attn_fwd_strided(const void* q, const void* k, const void* v, ta_d
  *   q, k, v, qkv_dtype, bias, bias_dtype, mask, kv_lengths, B..D, scale
  *               as given to tri_attn_fwd (contiguous tensors).
  *   lse         (B, N, H, Q) fp32, the forward's lse output (required).
+ *   out         the forward's O (B, N, H, Q, D) in qkv_dtype, or NULL.  Given,
+ *               sum_k' P dP is formed as the row sum of dO * O (fp32 from the
+ *               stored O, one pass over two (Q, D) tensors); NULL, it is formed
+ *               exactly from its definition, a second pass over every key.
  *   d_out       (B, N, H, Q, D) in qkv_dtype: dL/dO.
  *   dq, dk, dv  (B, N, H, Q|K, D) outputs in qkv_dtype.
  *   dbias       (B, 1, H, Q, K) output in bias_dtype, or NULL to skip it.
@@ -154,10 +158,12 @@ ta_status tri_attn_fwd_strided(const void* q, const void* k, const void* v, ta_d
  *               bytes, 256-byte aligned, owned by the caller; its contents on
  *               entry are ignored and on return are unspecified.  Two calls in
  *               flight must not share a workspace.
- * Arithmetic: exact fp32 on CUDA cores for every dtype (three kernels: the
- * per-row sum of P dP, the per-key-tile gradients with dQ and dBias added
- * atomically in fp32, the conversion to the output dtypes); the summation
- * order of dQ and dBias therefore varies from run to run within fp32 rounding.
+ * Arithmetic (three kernels: the per-row sum of P dP, the per-key-tile
+ * gradients with dQ and dBias added atomically in fp32, the conversion to the
+ * output dtypes): fp16 / bf16 inputs with D in {16, 32, 64} and K % 8 == 0 take
+ * the per-key-tile gradients on tcgen05 tensor cores (P^T and dS^T in 16 bits,
+ * fp32 accumulation); every other case runs exact fp32 on CUDA cores.  The
+ * summation order of dQ and dBias varies from run to run within fp32 rounding.
  * Supported: as tri_attn_fwd (D <= 256).  Errors: NULL required pointer,
  * misalignment (16 bytes for tensors, 4 for lse / kv_lengths, 256 for the
  * workspace) or a workspace below the required size -> TA_ERR_INVALID_ARG;
@@ -168,7 +174,7 @@ ta_status tri_attn_bwd(const void* q, const void* k, const void* v, ta_dtype qkv
                        const void* bias, ta_dtype bias_dtype,
                        const uint8_t* mask, const int32_t* kv_lengths,
                        int B, int N, int H, int Q, int K, int D, float scale,
-                       const float* lse, const void* d_out,
+                       const float* lse, const void* out, const void* d_out,
                        void* dq, void* dk, void* dv, void* dbias,
                        void* workspace, size_t workspace_bytes, void* stream);
 
@@ -199,7 +205,7 @@ ta_status tri_attn_bwd_noalloc(const void* q, const void* k, const void* v, ta_d
                                const void* bias, ta_dtype bias_dtype,
                                const uint8_t* mask, const int32_t* kv_lengths,
                                int B, int N, int H, int Q, int K, int D, float scale,
-                               const float* lse, const void* d_out,
+                               const float* lse, const void* out, const void* d_out,
                                void* dq, void* dk, void* dv, void* dbias, void* stream);
 
 /*

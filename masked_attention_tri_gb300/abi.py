@@ -59,9 +59,9 @@ def load() -> ctypes.CDLL:
                                                    I, I, I, P, I, P, I, L, L, L, P, P, P, P]
         lib.tri_attn_varlen_fwd_masked.restype = I
         Z = ctypes.c_size_t
-        lib.tri_attn_bwd.argtypes = [P, P, P, I, P, I, P, P, I, I, I, I, I, I, F, P, P, P, P, P, P, P, Z, P]
+        lib.tri_attn_bwd.argtypes = [P, P, P, I, P, I, P, P, I, I, I, I, I, I, F, P, P, P, P, P, P, P, P, Z, P]
         lib.tri_attn_bwd.restype = I
-        lib.tri_attn_bwd_noalloc.argtypes = [P, P, P, I, P, I, P, P, I, I, I, I, I, I, F, P, P, P, P, P, P, P]
+        lib.tri_attn_bwd_noalloc.argtypes = [P, P, P, I, P, I, P, P, I, I, I, I, I, I, F, P, P, P, P, P, P, P, P]
         lib.tri_attn_bwd_noalloc.restype = I
         lib.tri_attn_bwd_workspace_size.argtypes = [I, I, I, I, I, I]
         lib.tri_attn_bwd_workspace_size.restype = Z
@@ -100,20 +100,21 @@ def tri_attn_fwd(q, k, v, qkv_dtype, bias, bias_dtype, mask, kv_lengths, B, N, H
     _check(st, "tri_attn_fwd")
 
 
-def tri_attn_bwd(q, k, v, qkv_dtype, bias, bias_dtype, mask, kv_lengths, B, N, H, Q, K, D, scale, lse, d_out, dq, dk,
-                 dv, dbias, workspace, workspace_bytes, stream) -> None:
+def tri_attn_bwd(q, k, v, qkv_dtype, bias, bias_dtype, mask, kv_lengths, B, N, H, Q, K, D, scale, lse, out, d_out,
+                 dq, dk, dv, dbias, workspace, workspace_bytes, stream) -> None:
     """Gradients of tri_attn_fwd; pointers are ints (0 = NULL), workspace_bytes an int."""
     st = load().tri_attn_bwd(q, k, v, qkv_dtype, bias, bias_dtype, mask or None, kv_lengths or None, B, N, H, Q, K, D,
-                             float(scale), lse, d_out, dq, dk, dv, dbias or None, workspace, int(workspace_bytes),
-                             stream or None)
+                             float(scale), lse, out or None, d_out, dq, dk, dv, dbias or None, workspace,
+                             int(workspace_bytes), stream or None)
     _check(st, "tri_attn_bwd")
 
 
-def tri_attn_bwd_noalloc(q, k, v, qkv_dtype, bias, bias_dtype, mask, kv_lengths, B, N, H, Q, K, D, scale, lse, d_out,
-                         dq, dk, dv, dbias, stream) -> None:
+def tri_attn_bwd_noalloc(q, k, v, qkv_dtype, bias, bias_dtype, mask, kv_lengths, B, N, H, Q, K, D, scale, lse, out,
+                         d_out, dq, dk, dv, dbias, stream) -> None:
     """tri_attn_bwd in the library's own static scratch (no workspace, no allocation)."""
     st = load().tri_attn_bwd_noalloc(q, k, v, qkv_dtype, bias, bias_dtype, mask or None, kv_lengths or None, B, N, H,
-                                     Q, K, D, float(scale), lse, d_out, dq, dk, dv, dbias or None, stream or None)
+                                     Q, K, D, float(scale), lse, out or None, d_out, dq, dk, dv, dbias or None,
+                                     stream or None)
     _check(st, "tri_attn_bwd_noalloc")
 
 

@@ -144,13 +144,15 @@ def triangle_attention(q, k, v, bias, mask=None, scale=None, return_aux=False, *
 
 
 def triangle_attention_backward(q, k, v, bias, lse, d_out, mask=None, scale=None, *, kv_lengths=None,
-                                need_dbias=True):
+                                need_dbias=True, out=None):
     """Gradients (dq, dk, dv, dbias) of triangle_attention for dL/dO = d_out.
 
     q, k, v, bias, mask / kv_lengths and scale as given to the forward
     (contiguous 5-D tensors); lse: the forward's lse (return_aux), fp32 with
-    B*N*H*Q elements; d_out like q.  dbias has the bias's shape and dtype (the
-    sum over n), or is None without need_dbias.  The fp32 workspace is taken
+    B*N*H*Q elements; d_out like q; out, optional, the forward's O (then the
+    per-row sum of P dP is the row sum of dO * O, else it is formed exactly).
+    dbias has the bias's shape and dtype (the sum over n), or is None without
+    need_dbias.  The fp32 workspace is taken
     from PyTorch's allocator on q's device.
     """
     if mask is not None and kv_lengths is not None:
@@ -170,6 +172,10 @@ def triangle_attention_backward(q, k, v, bias, lse, d_out, mask=None, scale=None
         raise ValueError("triangle_attention_backward runs on CUDA tensors only")
     for t, nm in ((q, "q"), (k, "k"), (v, "v"), (bias, "bias"), (lse, "lse"), (d_out, "d_out")):
         _need(t, nm, dev)
+    if out is not None:
+        _need(out, "out", dev)
+        if tuple(out.shape) != tuple(q.shape) or out.dtype != q.dtype:
+            raise ValueError("out must have q's shape and dtype")
     if q.dtype not in _DT or k.dtype != q.dtype or v.dtype != q.dtype:
         raise TypeError("q, k, v must share one dtype among float32 / float16 / bfloat16")
     if bias.dtype not in (torch.float32, q.dtype):
@@ -194,7 +200,8 @@ def triangle_attention_backward(q, k, v, bias, lse, d_out, mask=None, scale=None
     ws = torch.empty(nbytes // 4, dtype=torch.float32, device=dev)
     with torch.cuda.device(dev):
         abi.tri_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _DT[q.dtype], _ptr(bias), _DT[bias.dtype], _ptr(m8), _ptr(kl),
-                         B, N, H, Q, K, D, s, _ptr(lse), _ptr(d_out), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias),
+                         B, N, H, Q, K, D, s, _ptr(lse), _ptr(out), _ptr(d_out), _ptr(dq), _ptr(dk), _ptr(dv),
+                         _ptr(dbias),
                          _ptr(ws), nbytes, _stream(dev))
     return dq, dk, dv, dbias
 
@@ -206,16 +213,17 @@ class _TriangleAttentionFn(torch.autograd.Function):
     @staticmethod
     def forward(ctx, q, k, v, bias, mask, kv_lengths, scale):
         o, lse, mx = triangle_attention(q, k, v, bias, mask, scale, True, kv_lengths=kv_lengths)
-        ctx.save_for_backward(q, k, v, bias, mask, kv_lengths, lse)
+        ctx.save_for_backward(q, k, v, bias, mask, kv_lengths, lse, o)
         ctx.scale = scale
         ctx.mark_non_differentiable(lse, mx)
         return o, lse, mx
 
     @staticmethod
     def backward(ctx, d_out, _d_lse, _d_mx):
-        q, k, v, bias, mask, kv_lengths, lse = ctx.saved_tensors
+        q, k, v, bias, mask, kv_lengths, lse, o = ctx.saved_tensors
         dq, dk, dv, dbias = triangle_attention_backward(q, k, v, bias, lse, d_out.contiguous(), mask, ctx.scale,
-                                                        kv_lengths=kv_lengths, need_dbias=ctx.needs_input_grad[3])
+                                                        kv_lengths=kv_lengths, need_dbias=ctx.needs_input_grad[3],
+                                                        out=o)
         return dq, dk, dv, dbias, None, None, None
 
 

@@ -300,8 +300,8 @@ TA_EXPORT size_t tri_attn_bwd_workspace_size(int B, int N, int H, int Q, int K, 
 
 TA_EXPORT ta_status tri_attn_bwd(const void* q, const void* k, const void* v, ta_dtype qkv_dtype, const void* bias,
                                  ta_dtype bias_dtype, const uint8_t* mask, const int32_t* kv_lengths, int B, int N,
-                                 int H, int Q, int K, int D, float scale, const float* lse, const void* d_out,
-                                 void* dq, void* dk, void* dv, void* dbias, void* workspace,
+                                 int H, int Q, int K, int D, float scale, const float* lse, const void* out,
+                                 const void* d_out, void* dq, void* dk, void* dv, void* dbias, void* workspace,
                                  size_t workspace_bytes, void* stream) {
     if (!q || !k || !v || !bias || !lse || !d_out || !dq || !dk || !dv || !workspace) return TA_ERR_INVALID_ARG;
     if (B <= 0 || N <= 0 || H <= 0 || Q <= 0 || K <= 0 || D <= 0) return TA_ERR_INVALID_ARG;
@@ -310,7 +310,7 @@ TA_EXPORT ta_status tri_attn_bwd(const void* q, const void* k, const void* v, ta
     const void* ptrs16[] = {q, k, v, bias, d_out, dq, dk, dv};
     for (const void* ptr : ptrs16)
         if (!aligned(ptr, 16)) return TA_ERR_INVALID_ARG;
-    if ((dbias && !aligned(dbias, 16)) || !aligned(lse, 4) || !aligned(workspace, 256) ||
+    if ((dbias && !aligned(dbias, 16)) || (out && !aligned(out, 16)) || !aligned(lse, 4) || !aligned(workspace, 256) ||
         (kv_lengths && !aligned(kv_lengths, 4)))
         return TA_ERR_INVALID_ARG;
     if (bias_dtype != TA_F32 && bias_dtype != qkv_dtype) return TA_ERR_UNSUPPORTED;
@@ -335,6 +335,7 @@ TA_EXPORT ta_status tri_attn_bwd(const void* q, const void* k, const void* v, ta
     p.mask = mask;
     p.kv_len = kv_lengths;
     p.lse = lse;
+    p.out = out;
     p.dq = dq;
     p.dk = dk;
     p.dv = dv;
@@ -348,6 +349,7 @@ TA_EXPORT ta_status tri_attn_bwd(const void* q, const void* k, const void* v, ta
     p.Q = Q;
     p.K = K;
     p.D = D;
+    p.tc_main = triattn::tc_bwd_supported(p) ? 1 : 0;
     const cudaError_t e = triattn::launch_simt_bwd(p, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TA_OK : TA_ERR_CUDA;
 }
@@ -377,14 +379,15 @@ void* bwd_noalloc_scratch() {
 TA_EXPORT ta_status tri_attn_bwd_noalloc(const void* q, const void* k, const void* v, ta_dtype qkv_dtype,
                                          const void* bias, ta_dtype bias_dtype, const uint8_t* mask,
                                          const int32_t* kv_lengths, int B, int N, int H, int Q, int K, int D,
-                                         float scale, const float* lse, const void* d_out, void* dq, void* dk,
+                                         float scale, const float* lse, const void* out, const void* d_out,
+                                         void* dq, void* dk,
                                          void* dv, void* dbias, void* stream) {
     // A problem whose workspace exceeds the static scratch is refused before anything runs.
     if (tri_attn_bwd_workspace_size(B, N, H, Q, K, D) > (size_t)TRI_ATTN_BWD_NOALLOC_SCRATCH_BYTES)
         return TA_ERR_UNSUPPORTED;
     void* ws = bwd_noalloc_scratch();
     if (!ws) return TA_ERR_CUDA;
-    return tri_attn_bwd(q, k, v, qkv_dtype, bias, bias_dtype, mask, kv_lengths, B, N, H, Q, K, D, scale, lse, d_out,
+    return tri_attn_bwd(q, k, v, qkv_dtype, bias, bias_dtype, mask, kv_lengths, B, N, H, Q, K, D, scale, lse, out, d_out,
                         dq, dk, dv, dbias, ws, (size_t)TRI_ATTN_BWD_NOALLOC_SCRATCH_BYTES, stream);
 }
 

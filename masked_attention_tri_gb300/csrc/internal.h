@@ -66,6 +66,7 @@ struct BwdParams {
     const uint8_t* mask;
     const int32_t* kv_len;
     const float* lse;       // (B, N, H, Q) from the forward
+    const void* out;        // the forward's O (q dtype) or NULL: delta = rowsum(dO * O) if given
     void* dq;
     void* dk;
     void* dv;
@@ -76,10 +77,15 @@ struct BwdParams {
     int dtype, bias_f32;
     float scale;
     int B, N, H, Q, K, D;
+    int tc_main;            // 1: the per-key-tile gradients on tensor cores (tc_bwd.cu)
 };
 // Workspace of the backward in floats (three pieces, each a multiple of 64 floats).
 size_t bwd_workspace_floats(int B, int N, int H, int Q, int K, int D);
 cudaError_t launch_simt_bwd(const BwdParams& p, cudaStream_t stream);
+// The tensor-core form of the backward's per-key-tile kernel (16-bit, D % 16 == 0,
+// D <= 64, K % 8 == 0); the caller runs the per-row sums before and the conversion after.
+cudaError_t launch_tc_bwd_main(const BwdParams& p, cudaStream_t stream);
+bool tc_bwd_supported(const BwdParams& p);
 
 // CUDA-core path: exact fp32 arithmetic, any dtype, both forms.
 cudaError_t launch_simt_fwd(const AttnParams& p, cudaStream_t stream);

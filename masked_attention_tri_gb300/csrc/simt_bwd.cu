@@ -17,11 +17,14 @@
 //
 // Three kernels:
 //   delta   one CTA per (slab, 32 query rows): delta[q] = sum_k P dP over every key
-//           (the exact definition, not dO . O of the rounded output); zeroes the
-//           fp32 dQ accumulator rows and (grid-stride) the dBias accumulator.
+//           (the exact definition); zeroes the fp32 dQ accumulator rows and
+//           (grid-stride) the dBias accumulator.  When the caller passes the
+//           forward's O, delta[q] = dO[q] . O[q] instead (sum_k P dP = dO . O),
+//           one pass over two (Q, D) tensors.
 //   main    one CTA per (slab, 32 keys), looping over the query tiles: dK and dV
 //           of its keys in registers, dQ and dBias added atomically (fp32) into
-//           the caller's workspace.
+//           the caller's workspace.  16-bit inputs with D % 16 == 0, D <= 64 and
+//           K % 8 == 0 take the tensor-core form of this step (tc_bwd.cu).
 //   finish  dQ and dBias accumulators converted to the output dtypes.
 // Layout of one CTA: 4 warps; in the score steps warp w owns query rows
 // 8w..8w+7 and lane j key j; in the accumulation steps warp w owns keys (dK, dV)
@@ -166,6 +169,40 @@ __global__ void __launch_bounds__(kBW * 32) bwd_delta_kernel(const BwdParams p) 
         const int q = q0 + warp * kBR + i;
         if (lane == 0 && q < p.Q) p.delta[unit * p.Q + q] = v;
     }
+}
+
+// delta[row] = sum_d dO[row, d] O[row, d] from the forward's stored O (eight
+// lanes per row, 16-byte loads); zeroes the row's fp32 dQ accumulator and,
+// grid-stride, the dBias accumulator.
+template <typename T>
+__global__ void __launch_bounds__(256) bwd_delta_out_kernel(const BwdParams p) {
+    constexpr int kE = 16 / (int)sizeof(T);  // elements per 16-byte chunk
+    const long long rows = (long long)p.B * p.N * p.H * p.Q;
+    const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) / 8;
+    const int g = threadIdx.x % 8;
+    if (p.dbias_acc) {
+        const long long tot = (long long)p.B * p.H * p.Q * p.K;
+        for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < tot; e += (long long)gridDim.x * blockDim.x)
+            p.dbias_acc[e] = 0.f;
+    }
+    float acc = 0.f;
+    if (row < rows) {
+        const T* o = static_cast<const T*>(p.out) + row * p.D;
+        const T* d = static_cast<const T*>(p.d_out) + row * p.D;
+        for (int c = g; c * kE < p.D; c += 8) {
+            const uint4 ov = reinterpret_cast<const uint4*>(o)[c];
+            const uint4 dv = reinterpret_cast<const uint4*>(d)[c];
+            const T* oe = reinterpret_cast<const T*>(&ov);
+            const T* de = reinterpret_cast<const T*>(&dv);
+#pragma unroll
+            for (int e = 0; e < kE; ++e) acc = fmaf(ld_f(oe, e), ld_f(de, e), acc);
+        }
+        float4* dq = reinterpret_cast<float4*>(p.dq_acc + row * p.D);
+        for (int c = g; c * 4 < p.D; c += 8) dq[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int o = 4; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (g == 0 && row < rows) p.delta[row] = acc;
 }
 
 template <typename T, typename BT, int DPL>
@@ -316,10 +353,21 @@ cudaError_t launch_typed(const BwdParams& p, cudaStream_t stream) {
     if ((e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2)) != cudaSuccess) return e;
     const long long g1 = units * ((p.Q + kT - 1) / kT), g2 = units * ((p.K + kT - 1) / kT);
     if (g1 > 0x7fffffffLL || g2 > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    k1<<<(unsigned)g1, kBW * 32, sm1, stream>>>(p);
+    if (p.out) {
+        const long long rows = units * p.Q;
+        const long long gd = (rows * 8 + 255) / 256;
+        if (gd > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+        bwd_delta_out_kernel<T><<<(unsigned)gd, 256, 0, stream>>>(p);
+    } else {
+        k1<<<(unsigned)g1, kBW * 32, sm1, stream>>>(p);
+    }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    k2<<<(unsigned)g2, kBW * 32, sm2, stream>>>(p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (p.tc_main) {
+        if ((e = launch_tc_bwd_main(p, stream)) != cudaSuccess) return e;
+    } else {
+        k2<<<(unsigned)g2, kBW * 32, sm2, stream>>>(p);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     bwd_finish_kernel<T, BT><<<1024, 256, 0, stream>>>(p);
     return cudaGetLastError();
 }

@@ -1,0 +1,464 @@
+// tc_bwd.cu -- the backward's per-key-tile gradients on tcgen05 tensor cores
+// (16-bit q/k/v with D % 16 == 0, D <= 64, K % 8 == 0; triangle form).
+//
+// The forward (cuEquivariance triangle_attention page) has its context saved for
+// backward.  With P recomputed from the saved lse and delta[q] = sum_k P dP (the
+// per-row sums, formed before this kernel), per (b, n, h) slab:
+//     dV = P^T dO,  dP = dO V^T,  dS = P (dP - delta) at valid keys (0 at masked),
+//     dK = s dS^T Q,  dQ = s dS K,  dBias[b, h] += dS (summed over n).
+// One CTA per (slab, 128-key tile), looping over the slab's 128-row query tiles.
+// Per query tile, five MMAs with 128 keys on the TMEM lanes:
+//     S^T  = K Q^T     (A = K, B = Q, both K-major in shared memory)   TMEM [0, 128)
+//     dP^T = V dO^T    (A = V, B = dO)                                   TMEM [128, 256)
+//     dV  += P^T dO    (A = P^T from TMEM, B = dO read MN-major)          TMEM [256, 256 + D)
+//     dK  += dS^T Q    (A = dS^T from TMEM, B = Q read MN-major)          TMEM [256 + D, 256 + 2D)
+//     dQ_j = dS K      (A = dS from shared memory, M = queries, MN-major;
+//                       B = K read MN-major)                             TMEM [256 + 2D, 256 + 3D)
+// Warps 0-3 (one thread per key row = TMEM lane) turn S^T and dP^T into P^T and
+// dS^T (16-bit pairs back into TMEM, dS also into shared memory as the A
+// operand of dQ), add dS to the fp32 dBias accumulator (coalesced over keys),
+// then read dQ_j (one thread per query row) and add it to the fp32 dQ
+// accumulator with a TMA reduce-add; at the end they write dK and dV.  Warp 4
+// loads K and V once and Q, dO, the bias tile and the rows' lse / delta per
+// query tile; warp 5 issues the MMAs.  Every wait is bounded (TA_ERR_TIMEOUT).
+
+#include "tc_kernel.cuh"
+
+namespace triattn {
+namespace tc {
+namespace {
+
+struct BwdTc {
+    CUtensorMap tm_q, tm_k, tm_v, tm_do, tm_bias, tm_dq;
+    const float* lse;
+    const float* delta;
+    float* dbias_acc;
+    const uint8_t* mask;
+    const int32_t* kv_len;
+    void* dk;
+    void* dv;
+    int* status;
+    float scale;
+    int B, N, H, Q, K, D;
+    int nkt, nqt, ksteps;
+    uint32_t idesc_s;   // M 128, N 128: K-major A and B
+    uint32_t idesc_g;   // M 128, N D: A from TMEM, B MN-major
+    uint32_t idesc_q;   // M 128, N D: A and B MN-major in shared memory
+    uint32_t bias_bytes;
+    int bias_boxes, bias_box_cols;
+};
+
+// Shared memory (offsets from a 1024-byte aligned base).
+struct BwdLayout {
+    uint32_t k, v, q, dO, ds, bias, dqst, lse, delta, bars, tmem_slot, abort_flag, total;
+};
+constexpr int kBwdBars = 9;  // kv_full, q_full, q_empty, s_full, p_full, dq_full, dq_empty, fin, drain
+__host__ __device__ inline BwdLayout bwd_layout(const BwdTc& P) {
+    BwdLayout L;
+    L.k = 0;
+    L.v = L.k + kBox;
+    L.q = L.v + kBox;
+    L.dO = L.q + kBox;
+    L.ds = L.dO + kBox;                 // dS as [key][query]: two 64-query boxes
+    L.bias = L.ds + 2 * kBox;
+    L.dqst = L.bias + P.bias_bytes;     // dQ staging: 4 warps x 32 rows x D fp32
+    L.lse = L.dqst + 4u * 32u * (uint32_t)P.D * 4u;
+    L.delta = L.lse + 128 * 4;
+    L.bars = L.delta + 128 * 4;
+    L.tmem_slot = L.bars + 8 * kBwdBars;
+    L.abort_flag = L.tmem_slot + 4;
+    L.total = L.abort_flag + 4;
+    return L;
+}
+
+// TMA reduce-add (fp32 add into global) of a shared-memory box.
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* tm, uint32_t src, int c0, int c1, int c2) {
+    asm volatile("cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(tm)),
+                 "r"(src), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
+__device__ __forceinline__ float bwd_weight(float x, float lse, float inv_k) {
+    // A row with every key masked has lse -1e9 in fp32 (its -1e9 + ln K rounds
+    // there); its weights are 1 / K.  Any row with a valid key has lse above -1e9 + 100.
+    return lse <= kMasked + 64.f ? inv_k : __expf(x - lse);
+}
+
+constexpr int kBwdThreads = 6 * 32;
+
+template <bool BF16, bool BIAS_F32>
+__global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_constant__ BwdTc P) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+    const BwdLayout L = bwd_layout(P);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L.abort_flag);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L.tmem_slot);
+    auto bar = [&](int i) { return base + L.bars + 8u * (uint32_t)i; };
+    const uint32_t kv_full = bar(0), q_full = bar(1), q_empty = bar(2), s_full = bar(3), p_full = bar(4);
+    const uint32_t dq_full = bar(5), dq_empty = bar(6), fin = bar(7), drain = bar(8);
+
+    const long long unit = blockIdx.x / P.nkt;  // (b*N + n)*H + h
+    const int k0 = (int)(blockIdx.x - unit * P.nkt) * kBN;
+    const int h = (int)(unit % P.H);
+    const long long bn = unit / P.H;
+    const int b = (int)(bn / P.N);
+
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        mbar_init(kv_full, 1);
+        mbar_init(q_full, 2);  // expect_tx arrival + the lse / delta rows
+        mbar_init(q_empty, 1);
+        mbar_init(s_full, 1);
+        mbar_init(p_full, 4);
+        mbar_init(dq_full, 1);
+        mbar_init(dq_empty, 4);
+        mbar_init(fin, 1);
+        mbar_init(drain, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 5) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(tmem_slot))
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t D = (uint32_t)P.D;
+    const uint32_t tS = tmem, tDP = tmem + 128, tDV = tmem + 256, tDK = tmem + 256 + D, tDQ = tmem + 256 + 2 * D;
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ producer
+        bool ok = true;
+        if (lane == 0) {
+            mbar_expect_tx(kv_full, 2 * kBox);
+            tma_load_3d(base + L.k, &P.tm_k, 0, k0, (int)unit, kv_full);
+            tma_load_3d(base + L.v, &P.tm_v, 0, k0, (int)unit, kv_full);
+        }
+        float* lse_s = reinterpret_cast<float*>(gbase + L.lse);
+        float* del_s = reinterpret_cast<float*>(gbase + L.delta);
+        for (int j = 0; j < P.nqt && ok; ++j) {
+            const int q0 = j * kBM;
+            if (j > 0) {
+                ok = __all_sync(0xffffffffu, wait_bar(q_empty, (uint32_t)(j - 1) & 1u, abort_flag, P.status));
+                if (!ok) break;
+            }
+            if (lane == 0) {
+                mbar_expect_tx(q_full, 2 * kBox + P.bias_bytes);
+                tma_load_3d(base + L.q, &P.tm_q, 0, q0, (int)unit, q_full);
+                tma_load_3d(base + L.dO, &P.tm_do, 0, q0, (int)unit, q_full);
+                for (int bx = 0; bx < P.bias_boxes; ++bx)
+                    tma_load_3d(base + L.bias + (uint32_t)bx * kBox, &P.tm_bias, k0 + bx * P.bias_box_cols, q0,
+                                b * P.H + h, q_full);
+            }
+            for (int i = lane; i < kBM; i += 32) {
+                const int q = q0 + i;
+                lse_s[i] = q < P.Q ? P.lse[unit * P.Q + q] : 0.f;
+                del_s[i] = q < P.Q ? P.delta[unit * P.Q + q] : 0.f;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(q_full);  // release: the rows are written
+        }
+        if (!ok) *abort_flag = 1;
+    } else if (warp == 5) {
+        // ----------------------------------------------------------------- MMA
+        const bool leader = elect_one();
+        bool ok = __all_sync(0xffffffffu, wait_bar(kv_full, 0, abort_flag, P.status));
+        const uint64_t kK = sw128_desc(base + L.k, 16, 1024), vK = sw128_desc(base + L.v, 16, 1024);
+        const uint64_t qK = sw128_desc(base + L.q, 16, 1024), doK = sw128_desc(base + L.dO, 16, 1024);
+        const uint64_t kM = sw128_desc(base + L.k, kBox, 1024), qM = sw128_desc(base + L.q, kBox, 1024);
+        const uint64_t doM = sw128_desc(base + L.dO, kBox, 1024), dsM = sw128_desc(base + L.ds, kBox, 1024);
+        for (int j = 0; j < P.nqt && ok; ++j) {
+            const uint32_t ph = (uint32_t)j & 1u;
+            ok = __all_sync(0xffffffffu, wait_bar(q_full, ph, abort_flag, P.status));
+            if (!ok) break;
+            tc_fence_after();
+            if (leader) {
+#pragma unroll 1
+                for (int kk = 0; kk < P.ksteps; ++kk)  // S^T = K Q^T
+                    mma_ss(tS, kK + 2u * (uint32_t)kk, qK + 2u * (uint32_t)kk, P.idesc_s, kk > 0 ? 1u : 0u);
+#pragma unroll 1
+                for (int kk = 0; kk < P.ksteps; ++kk)  // dP^T = V dO^T
+                    mma_ss(tDP, vK + 2u * (uint32_t)kk, doK + 2u * (uint32_t)kk, P.idesc_s, kk > 0 ? 1u : 0u);
+                mma_commit(s_full);
+            }
+            ok = __all_sync(0xffffffffu, wait_bar(p_full, ph, abort_flag, P.status));
+            if (!ok) break;
+            tc_fence_after();
+            if (leader) {
+#pragma unroll 1
+                for (int kk = 0; kk < kBM / 16; ++kk) {  // 16 queries per k step
+                    const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
+                    mma_ts(tDV, tS + 8u * (uint32_t)kk, doM + 128u * (uint32_t)kk, P.idesc_g, acc);
+                    mma_ts(tDK, tDP + 8u * (uint32_t)kk, qM + 128u * (uint32_t)kk, P.idesc_g, acc);
+                }
+            }
+            if (j > 0) {  // the compute warps have read dQ of the previous query tile
+                ok = __all_sync(0xffffffffu, wait_bar(dq_empty, ph ^ 1u, abort_flag, P.status));
+                if (!ok) break;
+                tc_fence_after();
+            }
+            if (leader) {
+#pragma unroll 1
+                for (int kk = 0; kk < kBN / 16; ++kk)  // dQ_j = dS K, 16 keys per k step
+                    mma_ss(tDQ, dsM + 128u * (uint32_t)kk, kM + 128u * (uint32_t)kk, P.idesc_q, kk > 0 ? 1u : 0u);
+                mma_commit(dq_full);
+                mma_commit(q_empty);
+            }
+        }
+        if (leader) {
+            if (ok) mma_commit(fin);
+            else *abort_flag = 1;
+            mma_commit(drain);
+        }
+        wait_bar_drain(drain, 0);
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------- compute
+        const int wq = warp;              // TMEM lane quarter: keys (and later query rows) 32 wq ..
+        const int kr = wq * 32 + lane;    // key row of the tile
+        const int key = k0 + kr;
+        const bool exists = key < P.K;
+        bool valid = exists;
+        if (exists) {
+            if (P.kv_len) {
+                int Lk = P.kv_len[bn];
+                Lk = Lk < 0 ? 0 : (Lk > P.K ? P.K : Lk);
+                valid = key < Lk;
+            } else if (P.mask) {
+                valid = P.mask[bn * P.K + key] != 0;
+            }
+        }
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        const float inv_k = 1.f / (float)P.K;
+        const float* lse_s = reinterpret_cast<const float*>(gbase + L.lse);
+        const float* del_s = reinterpret_cast<const float*>(gbase + L.delta);
+        const uint32_t rsw = (uint32_t)(kr & 7);
+        // bias element (query row ql, key kr) of the tile: 128B-swizzled boxes of bias_box_cols keys
+        const uint32_t bbox = base + L.bias + (uint32_t)(kr / P.bias_box_cols) * kBox;
+        const uint32_t bcol_b = (uint32_t)(kr % P.bias_box_cols) * (BIAS_F32 ? 4u : 2u);
+        float* dbias_row = P.dbias_acc ? P.dbias_acc + ((long long)b * P.H + h) * P.Q * (long long)P.K + key : nullptr;
+        // dQ staging of this warp: boxes of `inner` fp32 columns x 32 rows, swizzled by their row width
+        const int inner = P.D < 32 ? P.D : 32;
+        const uint32_t rowb = (uint32_t)inner * 4u;
+        const uint32_t dq_stage = base + L.dqst + (uint32_t)(wq * 32 * P.D * 4);
+        const uint32_t qsw = rowb == 128 ? (uint32_t)(lane & 7) : (uint32_t)((lane >> 1) & 3);
+        bool ok = true;
+        for (int j = 0; j < P.nqt && ok; ++j) {
+            const uint32_t ph = (uint32_t)j & 1u;
+            const int q0 = j * kBM;
+            ok = __all_sync(0xffffffffu, wait_bar(q_full, ph, abort_flag, P.status));
+            if (!ok) break;
+            ok = __all_sync(0xffffffffu, wait_bar(s_full, ph, abort_flag, P.status));
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {  // 32 queries per chunk
+                uint32_t sr[32], dr[32];
+                tmem_ld_x32(tS + lane_off + 32u * (uint32_t)c, sr);
+                tmem_ld_x32(tDP + lane_off + 32u * (uint32_t)c, dr);
+                uint32_t pp[16], dd[16];
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    float pv[2], sv[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int ql = 32 * c + i + u;  // query row within the tile
+                        const int qq = q0 + ql;
+                        float x = kMasked;
+                        if (valid) {
+                            const uint32_t ba = bbox + (uint32_t)ql * 128u +
+                                                ((((bcol_b >> 4) ^ ((uint32_t)ql & 7u))) << 4) + (bcol_b & 15u);
+                            float bv;
+                            if constexpr (BIAS_F32) {
+                                bv = *reinterpret_cast<const float*>(gbase + (ba - base));
+                            } else {
+                                const unsigned short hb = *reinterpret_cast<const unsigned short*>(gbase + (ba - base));
+                                bv = unpack2<BF16>((uint32_t)hb).x;
+                            }
+                            x = fmaf(P.scale, __uint_as_float(sr[i + u]), bv);
+                        }
+                        const bool live = exists && qq < P.Q;
+                        const float p = live ? bwd_weight(x, lse_s[ql], inv_k) : 0.f;
+                        const float ds = (live && valid) ? p * (__uint_as_float(dr[i + u]) - del_s[ql]) : 0.f;
+                        if (dbias_row && ds != 0.f) atomicAdd(dbias_row + (long long)qq * P.K, ds);
+                        pv[u] = p;
+                        sv[u] = ds;
+                    }
+                    pp[i / 2] = pack2<BF16>(pv[0], pv[1]);
+                    dd[i / 2] = pack2<BF16>(sv[0], sv[1]);
+                }
+                // P^T and dS^T as 16-bit query pairs into columns [16c, 16c + 16) (read already)
+                tmem_st_x16(tS + lane_off + 16u * (uint32_t)c, pp);
+                tmem_st_x16(tDP + lane_off + 16u * (uint32_t)c, dd);
+                // dS as [key][query] in shared memory: box c / 2, 16-byte chunks of 8 queries
+                const uint32_t drow = base + L.ds + (uint32_t)(c >> 1) * kBox + (uint32_t)kr * 128u;
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    const uint32_t ch = (uint32_t)(4 * (c & 1) + g);
+                    st_shared_v4(drow + ((ch ^ rsw) << 4), dd[4 * g], dd[4 * g + 1], dd[4 * g + 2], dd[4 * g + 3]);
+                }
+            }
+            tmem_st_wait();
+            fence_async_shared();  // dS in shared memory is read by the tensor core
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full);
+
+            // dQ_j: thread = query row q0 + 32 wq + lane, D fp32 columns, added into the accumulator.
+            ok = __all_sync(0xffffffffu, wait_bar(dq_full, ph, abort_flag, P.status));
+            if (!ok) break;
+            tc_fence_after();
+            if (lane == 0) bulk_wait_read_all();  // the previous reduce has read the staging rows
+            __syncwarp();
+#pragma unroll 1
+            for (int d0 = 0; d0 < P.D; d0 += 16) {
+                uint32_t o[16];
+                tmem_ld_x16(tDQ + lane_off + (uint32_t)d0, o);
+                const int bxi = d0 / inner, cb = (d0 % inner) / 4;  // box, first 16-byte chunk in it
+                const uint32_t rowa = dq_stage + (uint32_t)bxi * 32u * rowb + (uint32_t)lane * rowb;
+#pragma unroll
+                for (int g = 0; g < 4; ++g)
+                    st_shared_v4(rowa + ((((uint32_t)(cb + g)) ^ qsw) << 4),
+                                 __float_as_uint(__uint_as_float(o[4 * g]) * P.scale),
+                                 __float_as_uint(__uint_as_float(o[4 * g + 1]) * P.scale),
+                                 __float_as_uint(__uint_as_float(o[4 * g + 2]) * P.scale),
+                                 __float_as_uint(__uint_as_float(o[4 * g + 3]) * P.scale));
+            }
+            tc_fence_before();
+            fence_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(dq_empty);
+                if (q0 + 32 * wq < P.Q) {
+                    for (int bxi = 0; bxi * inner < P.D; ++bxi)
+                        tma_reduce_add_3d(&P.tm_dq, dq_stage + (uint32_t)bxi * 32u * rowb, bxi * inner, q0 + 32 * wq,
+                                          (int)unit);
+                    bulk_commit();
+                }
+            }
+        }
+        if (ok) ok = __all_sync(0xffffffffu, wait_bar(fin, 0, abort_flag, P.status));
+        if (ok) {
+            tc_fence_after();
+            uint16_t* dkp = static_cast<uint16_t*>(P.dk) + (unit * P.K + key) * (long long)P.D;
+            uint16_t* dvp = static_cast<uint16_t*>(P.dv) + (unit * P.K + key) * (long long)P.D;
+#pragma unroll 1
+            for (int d0 = 0; d0 < P.D; d0 += 16) {
+                uint32_t ov[16], ok16[16];
+                tmem_ld_x16(tDV + lane_off + (uint32_t)d0, ov);
+                tmem_ld_x16(tDK + lane_off + (uint32_t)d0, ok16);
+                uint32_t wv[8], wk[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    wv[e] = pack2<BF16>(__uint_as_float(ov[2 * e]), __uint_as_float(ov[2 * e + 1]));
+                    wk[e] = pack2<BF16>(__uint_as_float(ok16[2 * e]) * P.scale, __uint_as_float(ok16[2 * e + 1]) * P.scale);
+                }
+                if (exists) {
+                    reinterpret_cast<uint4*>(dvp + d0)[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                    reinterpret_cast<uint4*>(dvp + d0)[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
+                    reinterpret_cast<uint4*>(dkp + d0)[0] = make_uint4(wk[0], wk[1], wk[2], wk[3]);
+                    reinterpret_cast<uint4*>(dkp + d0)[1] = make_uint4(wk[4], wk[5], wk[6], wk[7]);
+                }
+            }
+        }
+        if (lane == 0) bulk_wait_all();  // this warp's dQ reduce-adds are done
+        if (!ok) *abort_flag = 1;
+    }
+
+    // ---------------------------------------------------------------- teardown
+    if (warp == 4 && lane == 0 && *abort_flag) {
+#pragma unroll 1
+        for (int i = 0; i < 2000; ++i) __nanosleep(1000);  // TMA loads already issued land first
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
+    }
+}
+
+// Instruction descriptor of kind::f16 with fp32 accumulation: A / B type at [7,10) /
+// [10,13) (0 f16, 1 bf16), A major at bit 15 and B major at bit 16 (1 = MN-major),
+// N >> 3 at [17,23), M >> 4 at [24,29).
+uint32_t bwd_idesc(bool bf16, int M, int N, bool a_mn, bool b_mn) {
+    const uint32_t ab = bf16 ? 1u : 0u;
+    return (1u << 4) | (ab << 7) | (ab << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+}  // namespace
+}  // namespace tc
+
+bool tc_bwd_supported(const BwdParams& p) {
+    return p.dtype != TA_F32 && (p.D == 16 || p.D == 32 || p.D == 64) && p.K % 8 == 0;
+}
+
+cudaError_t launch_tc_bwd_main(const BwdParams& p, cudaStream_t stream) {
+    using namespace tc;
+    if (!tc_bwd_supported(p)) return cudaErrorInvalidValue;
+    const bool bf16 = p.dtype == TA_BF16;
+    const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    BwdTc P;
+    memset(&P, 0, sizeof(P));
+    const int D = p.D;
+    const uint64_t units = (uint64_t)p.B * p.N * p.H;
+    const uint64_t rs = (uint64_t)D * 2;
+    const auto sw128 = CU_TENSOR_MAP_SWIZZLE_128B;
+    P.bias_box_cols = p.bias_f32 ? 32 : 64;
+    P.bias_boxes = kBN / P.bias_box_cols;
+    P.bias_bytes = (uint32_t)P.bias_boxes * kBox;
+    const uint64_t eb = p.bias_f32 ? 4 : 2;
+    const int inner = D < 32 ? D : 32;  // fp32 dQ columns per reduce box (128 or 64 bytes)
+    const bool maps_ok =
+        encode_map_3d(&P.tm_q, dt, p.q, D, p.Q, units, rs, rs * p.Q, 64, kBM, 1, sw128) &&
+        encode_map_3d(&P.tm_do, dt, p.d_out, D, p.Q, units, rs, rs * p.Q, 64, kBM, 1, sw128) &&
+        encode_map_3d(&P.tm_k, dt, p.k, D, p.K, units, rs, rs * p.K, 64, kBN, 1, sw128) &&
+        encode_map_3d(&P.tm_v, dt, p.v, D, p.K, units, rs, rs * p.K, 64, kBN, 1, sw128) &&
+        encode_map_3d(&P.tm_bias, p.bias_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : dt, p.bias, p.K, p.Q,
+                      (uint64_t)p.B * p.H, p.K * eb, p.K * eb * p.Q, P.bias_box_cols, kBM, 1, sw128) &&
+        encode_map_3d(&P.tm_dq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.dq_acc, D, p.Q, units, (uint64_t)D * 4,
+                      (uint64_t)D * 4 * p.Q, inner, 32, 1, inner == 32 ? sw128 : CU_TENSOR_MAP_SWIZZLE_64B);
+    if (!maps_ok) return cudaErrorInvalidValue;
+    P.lse = p.lse;
+    P.delta = p.delta;
+    P.dbias_acc = p.dbias_acc;
+    P.mask = p.mask;
+    P.kv_len = p.kv_len;
+    P.dk = p.dk;
+    P.dv = p.dv;
+    P.status = status_word();
+    if (!P.status) return cudaErrorInvalidValue;
+    P.scale = p.scale;
+    P.B = p.B;
+    P.N = p.N;
+    P.H = p.H;
+    P.Q = p.Q;
+    P.K = p.K;
+    P.D = D;
+    P.nkt = (p.K + kBN - 1) / kBN;
+    P.nqt = (p.Q + kBM - 1) / kBM;
+    P.ksteps = D / 16;
+    P.idesc_s = bwd_idesc(bf16, 128, 128, false, false);
+    P.idesc_g = bwd_idesc(bf16, 128, D, false, true);
+    P.idesc_q = bwd_idesc(bf16, 128, D, true, true);
+    const long long grid = (long long)units * P.nkt;
+    if (grid <= 0) return cudaSuccess;
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const size_t smem = bwd_layout(P).total + 1024;
+    auto kern = bf16 ? (p.bias_f32 ? tc_bwd_kernel<true, true> : tc_bwd_kernel<true, false>)
+                     : (p.bias_f32 ? tc_bwd_kernel<false, true> : tc_bwd_kernel<false, false>);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<(unsigned)grid, kBwdThreads, smem, stream>>>(P);
+    return cudaGetLastError();
+}
+
+}  // namespace triattn

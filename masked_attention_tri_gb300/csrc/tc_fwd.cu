@@ -149,6 +149,15 @@ cudaError_t launch_nq(int NQ, const TcParams& P, int grid, cudaStream_t stream) 
 }
 
 }  // namespace
+
+// Shared with the backward (tc_bwd.cu): a 3-D tensor map through the driver
+// entry point, and the SM count of the current device.
+bool encode_map_3d(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2,
+                   uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2, CUtensorMapSwizzle sw) {
+    return get_encode() && make_map(m, dt, ptr, d0, d1, d2, s1, s2, b0, b1, b2, sw);
+}
+int device_sm_count() { return num_sms(); }
+
 }  // namespace tc
 
 cudaError_t launch_tc_fwd(const AttnParams& a, cudaStream_t stream) {

@@ -59,6 +59,11 @@
 namespace triattn {
 namespace tc {
 
+// Host helpers defined in tc_fwd.cu.
+bool encode_map_3d(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2,
+                   uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2, CUtensorMapSwizzle sw);
+int device_sm_count();
+
 constexpr int kBM = 128;                    // query rows per tile
 constexpr int kBN = 128;                    // keys per tile
 constexpr uint32_t kBox = 128 * 128;        // one [128 rows][128 B] swizzled TMA box

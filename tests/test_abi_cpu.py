@@ -79,7 +79,7 @@ def test_triangle_host_checks(lib, kw, exc):
 def _bwd(**kw):
     ws = abi.tri_attn_bwd_workspace_size(1, 2, 2, 64, 64, 64)
     args = dict(q=A, k=A, v=A, qkv_dtype=abi.TA_BF16, bias=A, bias_dtype=abi.TA_BF16, mask=0, kv_lengths=0, B=1, N=2,
-                H=2, Q=64, K=64, D=64, scale=0.125, lse=A, d_out=A, dq=A, dk=A, dv=A, dbias=A, workspace=A,
+                H=2, Q=64, K=64, D=64, scale=0.125, lse=A, out=0, d_out=A, dq=A, dk=A, dv=A, dbias=A, workspace=A,
                 workspace_bytes=ws, stream=0)
     args.update(kw)
     return lambda: abi.tri_attn_bwd(**args)
@@ -101,6 +101,7 @@ def test_bwd_workspace_size(lib):
     (dict(workspace=A + 16), ValueError),  # 256-byte aligned workspace
     (dict(workspace_bytes=1024), ValueError),  # below the required size
     (dict(dq=MIS), ValueError),
+    (dict(out=MIS), ValueError),        # the forward's O, when given, 16-byte aligned
     (dict(mask=A, kv_lengths=A), ValueError),
     (dict(Q=0), ValueError),
     (dict(bias_dtype=abi.TA_F16), NotImplementedError),

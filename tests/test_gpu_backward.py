@@ -38,7 +38,7 @@ def _close(name, dtype, got, ref):
                                   f"(g {g[worst]:.6e}, r {ref[worst]:.6e}, max|r| {scale:.3e})")
 
 
-def _run(case, seed, need_dbias=True, use_autograd=False):
+def _run(case, seed, need_dbias=True, use_autograd=False, with_out=False):
     import masked_attention_tri_gb300 as ta
     d_out = synth.grad_out(case, seed)
     q, k, v, bias = (to_gpu(x) for x in (case.q, case.k, case.v, case.bias))
@@ -50,9 +50,9 @@ def _run(case, seed, need_dbias=True, use_autograd=False):
         torch.cuda.synchronize()
         grads = (q.grad, k.grad, v.grad, bias.grad)
     else:
-        _, lse, _ = ta.triangle_attention(q, k, v, bias, mask, case.scale, True, kv_lengths=kl)
+        o, lse, _ = ta.triangle_attention(q, k, v, bias, mask, case.scale, True, kv_lengths=kl)
         grads = ta.triangle_attention_backward(q, k, v, bias, lse, d_out.cuda(), mask, case.scale, kv_lengths=kl,
-                                               need_dbias=need_dbias)
+                                               need_dbias=need_dbias, out=o if with_out else None)
         torch.cuda.synchronize()
     assert ta.get_status() == 0
     ref = obwd.tri_bwd(case.q, case.k, case.v, case.bias, d_out, mask=case.mask, kv_lengths=case.kv_lengths,
@@ -70,12 +70,15 @@ def _check(case, seed, **kw):
 
 
 # dtypes x bias dtypes x masks; ragged Q and K (not multiples of the 32-row tiles), N > 1 for
-# the sum of dBias over n, kv_lengths extremes (0: every key masked, K, beyond K).
+# the sum of dBias over n, kv_lengths extremes (0: every key masked, K, beyond K).  16-bit
+# inputs with D in {16, 32, 64} take the tensor-core gradients, the others the CUDA-core
+# kernel; with_out: sum_k P dP from the forward's O instead of the exact pass.
+@pytest.mark.parametrize("with_out", [False, True])
 @pytest.mark.parametrize("dtype,bias_dtype,mask,D", [
     ("bf16", "bf16", "kvlen", 64), ("bf16", "f32", "dense", 32), ("f16", "f32", "none", 128),
     ("f16", "f16", "kvlen", 16), ("f32", "f32", "kvlen", 40), ("f32", "f32", "dense", 8),
 ])
-def test_backward_matches_oracle(dtype, bias_dtype, mask, D):
+def test_backward_matches_oracle(dtype, bias_dtype, mask, D, with_out):
     K = 70 if dtype == "f32" else 72  # 16-bit inputs need K % 8 == 0 (the forward's rule)
     c = synth.make_triangle(f"bwd_{dtype}_{bias_dtype}_{mask}_{D}", 2, 3, 2, 45, K, D, dtype, bias_dtype,
                             seed=700 + D, mask=mask, kv_range=(0, K))
@@ -83,7 +86,7 @@ def test_backward_matches_oracle(dtype, bias_dtype, mask, D):
         c.kv_lengths.view(-1)[:3] = torch.tensor([0, K, 1000], dtype=torch.int32)
     if mask == "dense":
         c.mask[0, 1] = 0  # a row block with every key masked
-    _check(c, 710 + D)
+    _check(c, 710 + D, with_out=with_out)
 
 
 @pytest.mark.parametrize("D", [136, 256])
@@ -93,14 +96,24 @@ def test_backward_wide_head_dims(D):
     _check(c, 730 + D)
 
 
-def test_backward_without_dbias_and_large_logits():
+@pytest.mark.parametrize("with_out", [False, True])
+def test_backward_without_dbias_and_large_logits(with_out):
     c = synth.make_triangle("bwd_large", 1, 2, 2, 64, 96, 64, "bf16", "bf16", seed=740, bias_std=8.0, scale=0.5,
                             mask="kvlen", kv_range=(10, 96))
-    _check(c, 741, need_dbias=False)
+    _check(c, 741, need_dbias=False, with_out=with_out)
+
+
+def test_backward_several_tiles():
+    """Several 128-key and 128-row tiles per slab (ragged), tensor-core gradients, both delta forms."""
+    c = synth.make_triangle("bwd_tiles", 1, 2, 2, 300, 264, 64, "bf16", "bf16", seed=745, mask="kvlen",
+                            kv_range=(100, 264))
+    _check(c, 746)
+    _check(c, 747, with_out=True)
 
 
 def test_autograd_wrapper():
-    """torch autograd through triangle_attention_autograd gives the same gradients."""
+    """torch autograd through triangle_attention_autograd gives the same gradients (it passes the
+    forward's O, so the per-row sums come from dO . O)."""
     c = synth.make_triangle("bwd_autograd", 1, 2, 3, 50, 64, 32, "bf16", "f32", seed=750, mask="dense")
     _check(c, 751, use_autograd=True)
 

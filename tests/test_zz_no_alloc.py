@@ -35,8 +35,8 @@ def test_noalloc_refuses_problems_beyond_its_scratch():
     need = abi.tri_attn_bwd_workspace_size(1, 8, 4, 512, 512, 256)
     assert need > abi.BWD_NOALLOC_SCRATCH_BYTES
     with pytest.raises(NotImplementedError):
-        abi.tri_attn_bwd_noalloc(A, A, A, abi.TA_BF16, A, abi.TA_BF16, 0, 0, 1, 8, 4, 512, 512, 256, 0.0625, A, A, A,
-                                 A, A, A, 0)
+        abi.tri_attn_bwd_noalloc(A, A, A, abi.TA_BF16, A, abi.TA_BF16, 0, 0, 1, 8, 4, 512, 512, 256, 0.0625, A, 0, A,
+                                 A, A, A, A, 0)
 
 
 @pytest.mark.gpu
@@ -53,8 +53,8 @@ def test_noalloc_matches_workspace_entry_twice(dtype, bias_dtype, mask):
     m8 = None if mask is None else mask.view(torch.uint8)
     kl = None if c.kv_lengths is None else c.kv_lengths.to(dev)
     d_out = synth.grad_out(c, 801).to(dev)
-    _, lse, _ = ta.triangle_attention(q, k, v, bias, mask, c.scale, True, kv_lengths=kl)
-    ref = ta.triangle_attention_backward(q, k, v, bias, lse, d_out, mask, c.scale, kv_lengths=kl)
+    o, lse, _ = ta.triangle_attention(q, k, v, bias, mask, c.scale, True, kv_lengths=kl)
+    ref = ta.triangle_attention_backward(q, k, v, bias, lse, d_out, mask, c.scale, kv_lengths=kl, out=o)
     B, N, H, Q, D = q.shape
     K = k.shape[3]
     outs = [tuple(torch.empty_like(t) for t in (q, k, v, bias)) for _ in range(2)]
@@ -63,7 +63,7 @@ def test_noalloc_matches_workspace_entry_twice(dtype, bias_dtype, mask):
     before = torch.cuda.memory_stats(dev).get("allocation.all.allocated", 0)
     for dq, dk, dv, db in outs:
         abi.tri_attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _DT[q.dtype], _ptr(bias), _DT[bias.dtype], _ptr(m8),
-                                 _ptr(kl), B, N, H, Q, K, D, c.scale, _ptr(lse), _ptr(d_out), _ptr(dq), _ptr(dk),
+                                 _ptr(kl), B, N, H, Q, K, D, c.scale, _ptr(lse), _ptr(o), _ptr(d_out), _ptr(dq), _ptr(dk),
                                  _ptr(dv), _ptr(db), stream.cuda_stream)
     torch.cuda.synchronize(dev)
     assert torch.cuda.memory_stats(dev).get("allocation.all.allocated", 0) == before
