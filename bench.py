@@ -243,6 +243,52 @@ def time_triangle(ta, c, dev, steps, warmup, flush=None, repeats=1, world=1):
     return statistics.median(per)
 
 
+def time_backward(ta, c, dev, steps, warmup, repeats=3):
+    """Device time (ms) of one backward (dQ, dK, dV, dBias) through the C ABI, with the
+    forward's O given (per-row sums dO . O); median of `repeats` timed regions."""
+    from masked_attention_tri_gb300 import abi
+    from masked_attention_tri_gb300.api import _DT, _ptr
+    x = gpu_triangle_inputs(c, dev)
+    B, N, H, Q, D = c.q.shape
+    K = c.k.shape[3]
+    o, lse, _ = ta.triangle_attention(x["q"], x["k"], x["v"], x["bias"], x["mask"], c.scale, True,
+                                      kv_lengths=x["kv_lengths"])
+    g = torch.Generator("cpu").manual_seed(11)
+    d_out = torch.randn(tuple(c.q.shape), generator=g).to(x["q"].dtype).to(dev)
+    dq, dk, dv, db = (torch.empty_like(t) for t in (x["q"], x["k"], x["v"], x["bias"]))
+    nbytes = abi.tri_attn_bwd_workspace_size(B, N, H, Q, K, D)
+    ws = torch.empty(nbytes // 4, dtype=torch.float32, device=dev)
+    m8 = None if x["mask"] is None else x["mask"].view(torch.uint8)
+    argv = (_ptr(x["q"]), _ptr(x["k"]), _ptr(x["v"]), _DT[x["q"].dtype], _ptr(x["bias"]), _DT[x["bias"].dtype],
+            _ptr(m8), _ptr(x["kv_lengths"]), B, N, H, Q, K, D, c.scale, _ptr(lse), _ptr(o), _ptr(d_out), _ptr(dq),
+            _ptr(dk), _ptr(dv), _ptr(db), _ptr(ws), nbytes, torch.cuda.current_stream(dev).cuda_stream)
+    for _ in range(warmup):
+        abi.tri_attn_bwd(*argv)
+    torch.cuda.synchronize(dev)
+    stream = torch.cuda.current_stream(dev)
+    per = []
+    for _ in range(repeats):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            abi.tri_attn_bwd(*argv)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        per.append(e0.elapsed_time(e1) / steps)
+    return statistics.median(per)
+
+
+def backward_entry(ta, c, dev, peaks, steps=5, warmup=2):
+    """The backward of the triangle workload `c`: ms and effective TFLOP/s over its five
+    contractions (S, dP, dV, dK, dQ: 10 * B*N*H*Q*K_valid*D, 2.5x the forward's count)."""
+    t = time_backward(ta, c, dev, steps, warmup)
+    f = 2.5 * triangle_work(c)[0]
+    return {"ms": t, "tflops": f / (t * 1e-3) / 1e12,
+            "pct_bf16_peak": 100 * f / (t * 1e-3) / (peaks["bf16_tflops"] * 1e12),
+            "outputs": "dQ, dK, dV, dBias (summed over N)",
+            "path": "per-row sums from the forward's O, per-key-tile gradients on tcgen05 (16-bit, D <= 64)"}
+
+
 def shard_case(c, world, rank):
     """This rank's contiguous range of (b, n) slabs of a B = 1 workload (the bias replicated)."""
     from masked_attention_tri_gb300.shard import slab_range
@@ -521,6 +567,10 @@ def main():
     ap.add_argument("--no-per-config", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--only-backward", action="store_true",
+                    help="time only the backward of the bf16_long workload (one JSON line)")
+    ap.add_argument("--backward-n", type=int, default=None,
+                    help="with --only-backward: the first N of the workload's 768 n rows only (a small case)")
     ap.add_argument("--only", default=None, choices=sorted(synth.WORKLOADS),
                     help="profiling mode: warm-up + timed launches of this one workload, a short JSON line, "
                          "nothing else (no per-config, end-to-end or CPU legs)")
@@ -530,6 +580,19 @@ def main():
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank)
+        return
+    if args.only_backward:
+        import masked_attention_tri_gb300 as ta
+        dev = torch.device("cuda", 0)
+        c = synth.bf16_long()
+        if args.backward_n:
+            n = args.backward_n
+            c.q, c.k, c.v = (t[:, :n].contiguous() for t in (c.q, c.k, c.v))
+            c.kv_lengths = c.kv_lengths[:, :n].contiguous()
+            c.N = n
+        line = backward_entry(ta, c, dev, load_peaks()[0], args.steps, args.warmup)
+        line["workload"] = f"bf16_long backward, first {c.N} of 768 n rows" if args.backward_n else "bf16_long backward"
+        print(json.dumps(line))
         return
     if args.only:
         run_only(args)
@@ -612,6 +675,7 @@ def main():
                                    "pct_bf16_peak": 100 * flops / (ms * 1e-3) / (peaks["bf16_tflops"] * 1e12),
                                    "two_term_roofline_frac": roof["two_term_roofline_frac"],
                                    "l2": "inputs larger than L2"}
+        per_config["bf16_long_backward"] = backward_entry(ta, c, dev, peaks)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -10,17 +10,20 @@
 // Per query tile, five MMAs with 128 keys on the TMEM lanes:
 //     S^T  = K Q^T     (A = K, B = Q, both K-major in shared memory)   TMEM [0, 128)
 //     dP^T = V dO^T    (A = V, B = dO)                                   TMEM [128, 256)
-//     dV  += P^T dO    (A = P^T from TMEM, B = dO read MN-major)          TMEM [256, 256 + D)
-//     dK  += dS^T Q    (A = dS^T from TMEM, B = Q read MN-major)          TMEM [256 + D, 256 + 2D)
+//     dV  += P^T dO    (A = P^T, TMEM [256 + 2D + 64, +64); B = dO read MN-major)
+//                                                                        TMEM [256, 256 + D)
+//     dK  += dS^T Q    (A = dS^T, TMEM [256 + 2D, +64); B = Q read MN-major)
+//                                                                        TMEM [256 + D, 256 + 2D)
 //     dQ_j = dS K      (A = dS from shared memory, M = queries, MN-major;
-//                       B = K read MN-major)                             TMEM [256 + 2D, 256 + 3D)
-// Warps 0-3 (one thread per key row = TMEM lane) turn S^T and dP^T into P^T and
-// dS^T (16-bit pairs back into TMEM, dS also into shared memory as the A
-// operand of dQ), add dS to the fp32 dBias accumulator (coalesced over keys),
-// then read dQ_j (one thread per query row) and add it to the fp32 dQ
-// accumulator with a TMA reduce-add; at the end they write dK and dV.  Warp 4
-// loads K and V once and Q, dO, the bias tile and the rows' lse / delta per
-// query tile; warp 5 issues the MMAs.  Every wait is bounded (TA_ERR_TIMEOUT).
+//                       B = K read MN-major)     TMEM [256 + 2D, 256 + 3D), dS^T's columns
+// Warps 0-7 (one thread per key row = TMEM lane; warps w and w + 4 take the
+// two query halves of the tile) turn S^T and dP^T into P^T and dS^T (16-bit
+// pairs into their own TMEM columns, dS also into shared memory as the A
+// operand of dQ) and add dS to the fp32 dBias accumulator (coalesced over
+// keys); warps 0-3 then read dQ_j (one thread per query row) and add it to the
+// fp32 dQ accumulator with a TMA reduce-add, and at the end write dK and dV.
+// Warp 8 loads K and V once and Q, dO, the bias tile and the rows' lse / delta
+// per query tile; warp 9 issues the MMAs.  Every wait is bounded (TA_ERR_TIMEOUT).
 
 #include "tc_kernel.cuh"
 
@@ -85,7 +88,7 @@ __device__ __forceinline__ float bwd_weight(float x, float lse, float inv_k) {
     return lse <= kMasked + 64.f ? inv_k : __expf(x - lse);
 }
 
-constexpr int kBwdThreads = 6 * 32;
+constexpr int kBwdThreads = 10 * 32;
 
 template <bool BF16, bool BIAS_F32>
 __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_constant__ BwdTc P) {
@@ -113,7 +116,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
         mbar_init(q_full, 2);  // expect_tx arrival + the lse / delta rows
         mbar_init(q_empty, 1);
         mbar_init(s_full, 1);
-        mbar_init(p_full, 4);
+        mbar_init(p_full, 8);
         mbar_init(dq_full, 1);
         mbar_init(dq_empty, 4);
         mbar_init(fin, 1);
@@ -121,7 +124,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
-    if (warp == 5) {
+    if (warp == 9) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(tmem_slot))
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
@@ -131,9 +134,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t D = (uint32_t)P.D;
+    // S^T, dP^T, dV, dK, then dQ_j (which shares its 64 columns with dS^T: MMA 4 reads dS^T before
+    // MMA 5 writes dQ_j, and dS^T of the next tile is written after dQ_j is read), then P^T.
     const uint32_t tS = tmem, tDP = tmem + 128, tDV = tmem + 256, tDK = tmem + 256 + D, tDQ = tmem + 256 + 2 * D;
+    const uint32_t tDS = tDQ, tP = tDQ + 64;
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ------------------------------------------------------------ producer
         bool ok = true;
         if (lane == 0) {
@@ -166,7 +172,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
             if (lane == 0) mbar_arrive(q_full);  // release: the rows are written
         }
         if (!ok) *abort_flag = 1;
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // ----------------------------------------------------------------- MMA
         const bool leader = elect_one();
         bool ok = __all_sync(0xffffffffu, wait_bar(kv_full, 0, abort_flag, P.status));
@@ -195,8 +201,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
 #pragma unroll 1
                 for (int kk = 0; kk < kBM / 16; ++kk) {  // 16 queries per k step
                     const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
-                    mma_ts(tDV, tS + 8u * (uint32_t)kk, doM + 128u * (uint32_t)kk, P.idesc_g, acc);
-                    mma_ts(tDK, tDP + 8u * (uint32_t)kk, qM + 128u * (uint32_t)kk, P.idesc_g, acc);
+                    mma_ts(tDV, tP + 8u * (uint32_t)kk, doM + 128u * (uint32_t)kk, P.idesc_g, acc);
+                    mma_ts(tDK, tDS + 8u * (uint32_t)kk, qM + 128u * (uint32_t)kk, P.idesc_g, acc);
                 }
             }
             if (j > 0) {  // the compute warps have read dQ of the previous query tile
@@ -221,7 +227,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
         __syncwarp();
     } else {
         // ------------------------------------------------------------- compute
-        const int wq = warp;              // TMEM lane quarter: keys (and later query rows) 32 wq ..
+        const int wq = warp & 3;          // TMEM lane quarter: keys (and later query rows) 32 wq ..
+        const int hq = warp >> 2;         // query half of every tile: chunks 2 hq, 2 hq + 1
         const int kr = wq * 32 + lane;    // key row of the tile
         const int key = k0 + kr;
         const bool exists = key < P.K;
@@ -243,6 +250,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
         // bias element (query row ql, key kr) of the tile: 128B-swizzled boxes of bias_box_cols keys
         const uint32_t bbox = base + L.bias + (uint32_t)(kr / P.bias_box_cols) * kBox;
         const uint32_t bcol_b = (uint32_t)(kr % P.bias_box_cols) * (BIAS_F32 ? 4u : 2u);
+        // swizzled byte offset of this key's column in query row r, by r % 8 (128B swizzle)
+        uint32_t xo[8];
+#pragma unroll
+        for (int r8 = 0; r8 < 8; ++r8) xo[r8] = ((((bcol_b >> 4) ^ (uint32_t)r8)) << 4) + (bcol_b & 15u);
         float* dbias_row = P.dbias_acc ? P.dbias_acc + ((long long)b * P.H + h) * P.Q * (long long)P.K + key : nullptr;
         // dQ staging of this warp: boxes of `inner` fp32 columns x 32 rows, swizzled by their row width
         const int inner = P.D < 32 ? P.D : 32;
@@ -257,37 +268,47 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
             if (!ok) break;
             ok = __all_sync(0xffffffffu, wait_bar(s_full, ph, abort_flag, P.status));
             if (!ok) break;
+            if (hq == 1 && j > 0) {  // warps 0-3 have read dQ of the previous tile out of the dS^T columns
+                ok = __all_sync(0xffffffffu, wait_bar(dq_empty, ph ^ 1u, abort_flag, P.status));
+                if (!ok) break;
+            }
             tc_fence_after();
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {  // 32 queries per chunk
+            for (int c = 2 * hq; c < 2 * hq + 2; ++c) {  // 32 queries per chunk
                 uint32_t sr[32], dr[32];
                 tmem_ld_x32(tS + lane_off + 32u * (uint32_t)c, sr);
                 tmem_ld_x32(tDP + lane_off + 32u * (uint32_t)c, dr);
+                // The chunk's lse and delta (shared-memory broadcasts, four at a time) and this
+                // key's bias column: query row ql = 32c + i lives at bcb + 128 i + xo[i % 8].
+                float ls[32], dl[32];
+#pragma unroll
+                for (int i = 0; i < 32; i += 4) {
+                    const float4 l4 = *reinterpret_cast<const float4*>(lse_s + 32 * c + i);
+                    const float4 d4 = *reinterpret_cast<const float4*>(del_s + 32 * c + i);
+                    ls[i] = l4.x, ls[i + 1] = l4.y, ls[i + 2] = l4.z, ls[i + 3] = l4.w;
+                    dl[i] = d4.x, dl[i + 1] = d4.y, dl[i + 2] = d4.z, dl[i + 3] = d4.w;
+                }
+                const uint8_t* bcb = gbase + (bbox - base) + (uint32_t)(32 * c) * 128u;
+                const int nq = P.Q - (q0 + 32 * c);  // queries of the chunk that exist
                 uint32_t pp[16], dd[16];
 #pragma unroll
                 for (int i = 0; i < 32; i += 2) {
                     float pv[2], sv[2];
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
-                        const int ql = 32 * c + i + u;  // query row within the tile
-                        const int qq = q0 + ql;
+                        const int ii = i + u;
                         float x = kMasked;
                         if (valid) {
-                            const uint32_t ba = bbox + (uint32_t)ql * 128u +
-                                                ((((bcol_b >> 4) ^ ((uint32_t)ql & 7u))) << 4) + (bcol_b & 15u);
+                            const uint8_t* ba = bcb + ii * 128 + xo[ii & 7];
                             float bv;
-                            if constexpr (BIAS_F32) {
-                                bv = *reinterpret_cast<const float*>(gbase + (ba - base));
-                            } else {
-                                const unsigned short hb = *reinterpret_cast<const unsigned short*>(gbase + (ba - base));
-                                bv = unpack2<BF16>((uint32_t)hb).x;
-                            }
-                            x = fmaf(P.scale, __uint_as_float(sr[i + u]), bv);
+                            if constexpr (BIAS_F32) bv = *reinterpret_cast<const float*>(ba);
+                            else bv = unpack2<BF16>((uint32_t)*reinterpret_cast<const unsigned short*>(ba)).x;
+                            x = fmaf(P.scale, __uint_as_float(sr[ii]), bv);
                         }
-                        const bool live = exists && qq < P.Q;
-                        const float p = live ? bwd_weight(x, lse_s[ql], inv_k) : 0.f;
-                        const float ds = (live && valid) ? p * (__uint_as_float(dr[i + u]) - del_s[ql]) : 0.f;
-                        if (dbias_row && ds != 0.f) atomicAdd(dbias_row + (long long)qq * P.K, ds);
+                        const bool live = exists && ii < nq;
+                        const float p = live ? bwd_weight(x, ls[ii], inv_k) : 0.f;
+                        const float ds = (live && valid) ? p * (__uint_as_float(dr[ii]) - dl[ii]) : 0.f;
+                        if (dbias_row && ds != 0.f) atomicAdd(dbias_row + (long long)(q0 + 32 * c + ii) * P.K, ds);
                         pv[u] = p;
                         sv[u] = ds;
                     }
@@ -295,8 +316,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
                     dd[i / 2] = pack2<BF16>(sv[0], sv[1]);
                 }
                 // P^T and dS^T as 16-bit query pairs into columns [16c, 16c + 16) (read already)
-                tmem_st_x16(tS + lane_off + 16u * (uint32_t)c, pp);
-                tmem_st_x16(tDP + lane_off + 16u * (uint32_t)c, dd);
+                tmem_st_x16(tP + lane_off + 16u * (uint32_t)c, pp);
+                tmem_st_x16(tDS + lane_off + 16u * (uint32_t)c, dd);
                 // dS as [key][query] in shared memory: box c / 2, 16-byte chunks of 8 queries
                 const uint32_t drow = base + L.ds + (uint32_t)(c >> 1) * kBox + (uint32_t)kr * 128u;
 #pragma unroll
@@ -310,8 +331,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full);
+            if (hq == 1) continue;
 
-            // dQ_j: thread = query row q0 + 32 wq + lane, D fp32 columns, added into the accumulator.
+            // dQ_j (warps 0-3): thread = query row q0 + 32 wq + lane, D fp32 columns, added into the
+            // accumulator.
             ok = __all_sync(0xffffffffu, wait_bar(dq_full, ph, abort_flag, P.status));
             if (!ok) break;
             tc_fence_after();
@@ -345,7 +368,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
             }
         }
         if (ok) ok = __all_sync(0xffffffffu, wait_bar(fin, 0, abort_flag, P.status));
-        if (ok) {
+        if (ok && hq == 0) {
             tc_fence_after();
             uint16_t* dkp = static_cast<uint16_t*>(P.dk) + (unit * P.K + key) * (long long)P.D;
             uint16_t* dvp = static_cast<uint16_t*>(P.dv) + (unit * P.K + key) * (long long)P.D;
@@ -373,13 +396,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
     }
 
     // ---------------------------------------------------------------- teardown
-    if (warp == 4 && lane == 0 && *abort_flag) {
+    if (warp == 8 && lane == 0 && *abort_flag) {
 #pragma unroll 1
         for (int i = 0; i < 2000; ++i) __nanosleep(1000);  // TMA loads already issued land first
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
     }
