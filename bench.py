@@ -243,7 +243,7 @@ def time_triangle(ta, c, dev, steps, warmup, flush=None, repeats=1, world=1):
     return statistics.median(per)
 
 
-def time_backward(ta, c, dev, steps, warmup, repeats=3):
+def time_backward(ta, c, dev, steps, warmup, repeats=3, with_dbias=True):
     """Device time (ms) of one backward (dQ, dK, dV, dBias) through the C ABI, with the
     forward's O given (per-row sums dO . O); median of `repeats` timed regions."""
     from masked_attention_tri_gb300 import abi
@@ -261,7 +261,8 @@ def time_backward(ta, c, dev, steps, warmup, repeats=3):
     m8 = None if x["mask"] is None else x["mask"].view(torch.uint8)
     argv = (_ptr(x["q"]), _ptr(x["k"]), _ptr(x["v"]), _DT[x["q"].dtype], _ptr(x["bias"]), _DT[x["bias"].dtype],
             _ptr(m8), _ptr(x["kv_lengths"]), B, N, H, Q, K, D, c.scale, _ptr(lse), _ptr(o), _ptr(d_out), _ptr(dq),
-            _ptr(dk), _ptr(dv), _ptr(db), _ptr(ws), nbytes, torch.cuda.current_stream(dev).cuda_stream)
+            _ptr(dk), _ptr(dv), _ptr(db) if with_dbias else 0, _ptr(ws), nbytes,
+            torch.cuda.current_stream(dev).cuda_stream)
     for _ in range(warmup):
         abi.tri_attn_bwd(*argv)
     torch.cuda.synchronize(dev)
@@ -278,14 +279,14 @@ def time_backward(ta, c, dev, steps, warmup, repeats=3):
     return statistics.median(per)
 
 
-def backward_entry(ta, c, dev, peaks, steps=5, warmup=2):
+def backward_entry(ta, c, dev, peaks, steps=5, warmup=2, with_dbias=True):
     """The backward of the triangle workload `c`: ms and effective TFLOP/s over its five
     contractions (S, dP, dV, dK, dQ: 10 * B*N*H*Q*K_valid*D, 2.5x the forward's count)."""
-    t = time_backward(ta, c, dev, steps, warmup)
+    t = time_backward(ta, c, dev, steps, warmup, with_dbias=with_dbias)
     f = 2.5 * triangle_work(c)[0]
     return {"ms": t, "tflops": f / (t * 1e-3) / 1e12,
             "pct_bf16_peak": 100 * f / (t * 1e-3) / (peaks["bf16_tflops"] * 1e12),
-            "outputs": "dQ, dK, dV, dBias (summed over N)",
+            "outputs": "dQ, dK, dV, dBias (summed over N)" if with_dbias else "dQ, dK, dV",
             "path": "per-row sums from the forward's O, per-key-tile gradients on tcgen05 (16-bit, D <= 64)"}
 
 
@@ -569,6 +570,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--only-backward", action="store_true",
                     help="time only the backward of the bf16_long workload (one JSON line)")
+    ap.add_argument("--backward-no-dbias", action="store_true", help="with --only-backward: skip dBias")
     ap.add_argument("--backward-n", type=int, default=None,
                     help="with --only-backward: the first N of the workload's 768 n rows only (a small case)")
     ap.add_argument("--only", default=None, choices=sorted(synth.WORKLOADS),
@@ -590,7 +592,8 @@ def main():
             c.q, c.k, c.v = (t[:, :n].contiguous() for t in (c.q, c.k, c.v))
             c.kv_lengths = c.kv_lengths[:, :n].contiguous()
             c.N = n
-        line = backward_entry(ta, c, dev, load_peaks()[0], args.steps, args.warmup)
+        line = backward_entry(ta, c, dev, load_peaks()[0], args.steps, args.warmup,
+                              with_dbias=not args.backward_no_dbias)
         line["workload"] = f"bf16_long backward, first {c.N} of 768 n rows" if args.backward_n else "bf16_long backward"
         print(json.dumps(line))
         return

@@ -49,25 +49,26 @@ struct BwdTc {
     uint32_t idesc_q;   // M 128, N D: A and B MN-major in shared memory
     uint32_t bias_bytes;
     int bias_boxes, bias_box_cols;
+    int qs;             // stages of (Q, dO, lse, delta): 2 when shared memory allows, else 1
 };
 
 // Shared memory (offsets from a 1024-byte aligned base).
+// Stage s of the query-tile ring: Q at q + s * 2 kBox, dO after it; lse / delta at lse + s * 1024.
 struct BwdLayout {
-    uint32_t k, v, q, dO, ds, bias, dqst, lse, delta, bars, tmem_slot, abort_flag, total;
+    uint32_t k, v, q, ds, bias, dqst, lse, bars, tmem_slot, abort_flag, total;
 };
-constexpr int kBwdBars = 9;  // kv_full, q_full, q_empty, s_full, p_full, dq_full, dq_empty, fin, drain
+// kv_full, q_full[2], q_empty[2], bias_full, bias_empty, s_full, p_full, dq_full, dq_empty, fin, drain
+constexpr int kBwdBars = 13;
 __host__ __device__ inline BwdLayout bwd_layout(const BwdTc& P) {
     BwdLayout L;
     L.k = 0;
     L.v = L.k + kBox;
     L.q = L.v + kBox;
-    L.dO = L.q + kBox;
-    L.ds = L.dO + kBox;                 // dS as [key][query]: two 64-query boxes
+    L.ds = L.q + (uint32_t)P.qs * 2 * kBox;  // dS as [key][query]: two 64-query boxes
     L.bias = L.ds + 2 * kBox;
-    L.dqst = L.bias + P.bias_bytes;     // dQ staging: 4 warps x 32 rows x D fp32
+    L.dqst = L.bias + P.bias_bytes;          // dQ staging: 4 warps x 32 rows x D fp32
     L.lse = L.dqst + 4u * 32u * (uint32_t)P.D * 4u;
-    L.delta = L.lse + 128 * 4;
-    L.bars = L.delta + 128 * 4;
+    L.bars = L.lse + (uint32_t)P.qs * 1024u;
     L.tmem_slot = L.bars + 8 * kBwdBars;
     L.abort_flag = L.tmem_slot + 4;
     L.total = L.abort_flag + 4;
@@ -101,8 +102,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L.abort_flag);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L.tmem_slot);
     auto bar = [&](int i) { return base + L.bars + 8u * (uint32_t)i; };
-    const uint32_t kv_full = bar(0), q_full = bar(1), q_empty = bar(2), s_full = bar(3), p_full = bar(4);
-    const uint32_t dq_full = bar(5), dq_empty = bar(6), fin = bar(7), drain = bar(8);
+    const uint32_t kv_full = bar(0);
+    auto q_full = [&](int st) { return bar(1 + st); };
+    auto q_empty = [&](int st) { return bar(3 + st); };
+    const uint32_t bias_full = bar(5), bias_empty = bar(6), s_full = bar(7), p_full = bar(8);
+    const uint32_t dq_full = bar(9), dq_empty = bar(10), fin = bar(11), drain = bar(12);
+    auto q_smem = [&](int st) { return base + L.q + (uint32_t)st * 2u * kBox; };
+    auto do_smem = [&](int st) { return base + L.q + (uint32_t)st * 2u * kBox + kBox; };
 
     const long long unit = blockIdx.x / P.nkt;  // (b*N + n)*H + h
     const int k0 = (int)(blockIdx.x - unit * P.nkt) * kBN;
@@ -113,8 +119,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
     if (threadIdx.x == 0) {
         *abort_flag = 0;
         mbar_init(kv_full, 1);
-        mbar_init(q_full, 2);  // expect_tx arrival + the lse / delta rows
-        mbar_init(q_empty, 1);
+        for (int st = 0; st < 2; ++st) {
+            mbar_init(q_full(st), 2);  // expect_tx arrival + the lse / delta rows
+            mbar_init(q_empty(st), 1);
+        }
+        mbar_init(bias_full, 1);
+        mbar_init(bias_empty, 8);
         mbar_init(s_full, 1);
         mbar_init(p_full, 8);
         mbar_init(dq_full, 1);
@@ -147,29 +157,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
             tma_load_3d(base + L.k, &P.tm_k, 0, k0, (int)unit, kv_full);
             tma_load_3d(base + L.v, &P.tm_v, 0, k0, (int)unit, kv_full);
         }
-        float* lse_s = reinterpret_cast<float*>(gbase + L.lse);
-        float* del_s = reinterpret_cast<float*>(gbase + L.delta);
         for (int j = 0; j < P.nqt && ok; ++j) {
-            const int q0 = j * kBM;
-            if (j > 0) {
-                ok = __all_sync(0xffffffffu, wait_bar(q_empty, (uint32_t)(j - 1) & 1u, abort_flag, P.status));
+            const int q0 = j * kBM, st = j % P.qs, use = j / P.qs;
+            if (j >= P.qs) {  // stage st held tile j - qs: its MMAs are done
+                ok = __all_sync(0xffffffffu, wait_bar(q_empty(st), (uint32_t)(use - 1) & 1u, abort_flag, P.status));
                 if (!ok) break;
             }
             if (lane == 0) {
-                mbar_expect_tx(q_full, 2 * kBox + P.bias_bytes);
-                tma_load_3d(base + L.q, &P.tm_q, 0, q0, (int)unit, q_full);
-                tma_load_3d(base + L.dO, &P.tm_do, 0, q0, (int)unit, q_full);
-                for (int bx = 0; bx < P.bias_boxes; ++bx)
-                    tma_load_3d(base + L.bias + (uint32_t)bx * kBox, &P.tm_bias, k0 + bx * P.bias_box_cols, q0,
-                                b * P.H + h, q_full);
+                mbar_expect_tx(q_full(st), 2 * kBox);
+                tma_load_3d(q_smem(st), &P.tm_q, 0, q0, (int)unit, q_full(st));
+                tma_load_3d(do_smem(st), &P.tm_do, 0, q0, (int)unit, q_full(st));
             }
+            float* lse_s = reinterpret_cast<float*>(gbase + L.lse + (uint32_t)st * 1024u);
+            float* del_s = lse_s + 128;
             for (int i = lane; i < kBM; i += 32) {
                 const int q = q0 + i;
                 lse_s[i] = q < P.Q ? P.lse[unit * P.Q + q] : 0.f;
                 del_s[i] = q < P.Q ? P.delta[unit * P.Q + q] : 0.f;
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(q_full);  // release: the rows are written
+            if (lane == 0) mbar_arrive(q_full(st));  // release: the rows are written
+            if (j > 0) {  // the compute warps have read the previous tile's bias
+                ok = __all_sync(0xffffffffu, wait_bar(bias_empty, (uint32_t)(j - 1) & 1u, abort_flag, P.status));
+                if (!ok) break;
+            }
+            if (lane == 0) {
+                mbar_expect_tx(bias_full, P.bias_bytes);
+                for (int bx = 0; bx < P.bias_boxes; ++bx)
+                    tma_load_3d(base + L.bias + (uint32_t)bx * kBox, &P.tm_bias, k0 + bx * P.bias_box_cols, q0,
+                                b * P.H + h, bias_full);
+            }
         }
         if (!ok) *abort_flag = 1;
     } else if (warp == 9) {
@@ -177,12 +194,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
         const bool leader = elect_one();
         bool ok = __all_sync(0xffffffffu, wait_bar(kv_full, 0, abort_flag, P.status));
         const uint64_t kK = sw128_desc(base + L.k, 16, 1024), vK = sw128_desc(base + L.v, 16, 1024);
-        const uint64_t qK = sw128_desc(base + L.q, 16, 1024), doK = sw128_desc(base + L.dO, 16, 1024);
-        const uint64_t kM = sw128_desc(base + L.k, kBox, 1024), qM = sw128_desc(base + L.q, kBox, 1024);
-        const uint64_t doM = sw128_desc(base + L.dO, kBox, 1024), dsM = sw128_desc(base + L.ds, kBox, 1024);
+        const uint64_t kM = sw128_desc(base + L.k, kBox, 1024), dsM = sw128_desc(base + L.ds, kBox, 1024);
         for (int j = 0; j < P.nqt && ok; ++j) {
             const uint32_t ph = (uint32_t)j & 1u;
-            ok = __all_sync(0xffffffffu, wait_bar(q_full, ph, abort_flag, P.status));
+            const int st = j % P.qs;
+            const uint64_t qK = sw128_desc(q_smem(st), 16, 1024), doK = sw128_desc(do_smem(st), 16, 1024);
+            const uint64_t qM = sw128_desc(q_smem(st), kBox, 1024), doM = sw128_desc(do_smem(st), kBox, 1024);
+            ok = __all_sync(0xffffffffu, wait_bar(q_full(st), (uint32_t)(j / P.qs) & 1u, abort_flag, P.status));
             if (!ok) break;
             tc_fence_after();
             if (leader) {
@@ -215,7 +233,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
                 for (int kk = 0; kk < kBN / 16; ++kk)  // dQ_j = dS K, 16 keys per k step
                     mma_ss(tDQ, dsM + 128u * (uint32_t)kk, kM + 128u * (uint32_t)kk, P.idesc_q, kk > 0 ? 1u : 0u);
                 mma_commit(dq_full);
-                mma_commit(q_empty);
+                mma_commit(q_empty(st));
             }
         }
         if (leader) {
@@ -244,8 +262,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
         }
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const float inv_k = 1.f / (float)P.K;
-        const float* lse_s = reinterpret_cast<const float*>(gbase + L.lse);
-        const float* del_s = reinterpret_cast<const float*>(gbase + L.delta);
         const uint32_t rsw = (uint32_t)(kr & 7);
         // bias element (query row ql, key kr) of the tile: 128B-swizzled boxes of bias_box_cols keys
         const uint32_t bbox = base + L.bias + (uint32_t)(kr / P.bias_box_cols) * kBox;
@@ -263,8 +279,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
         bool ok = true;
         for (int j = 0; j < P.nqt && ok; ++j) {
             const uint32_t ph = (uint32_t)j & 1u;
-            const int q0 = j * kBM;
-            ok = __all_sync(0xffffffffu, wait_bar(q_full, ph, abort_flag, P.status));
+            const int q0 = j * kBM, st = j % P.qs;
+            const float* lse_s = reinterpret_cast<const float*>(gbase + L.lse + (uint32_t)st * 1024u);
+            const float* del_s = lse_s + 128;
+            ok = __all_sync(0xffffffffu, wait_bar(q_full(st), (uint32_t)(j / P.qs) & 1u, abort_flag, P.status));
+            if (!ok) break;
+            ok = __all_sync(0xffffffffu, wait_bar(bias_full, ph, abort_flag, P.status));
             if (!ok) break;
             ok = __all_sync(0xffffffffu, wait_bar(s_full, ph, abort_flag, P.status));
             if (!ok) break;
@@ -326,6 +346,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
                     st_shared_v4(drow + ((ch ^ rsw) << 4), dd[4 * g], dd[4 * g + 1], dd[4 * g + 2], dd[4 * g + 3]);
                 }
             }
+            __syncwarp();  // every lane has read its bias values
+            if (lane == 0) mbar_arrive(bias_empty);
             tmem_st_wait();
             fence_async_shared();  // dS in shared memory is read by the tensor core
             tc_fence_before();
@@ -475,6 +497,8 @@ cudaError_t launch_tc_bwd_main(const BwdParams& p, cudaStream_t stream) {
     const long long grid = (long long)units * P.nkt;
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    P.qs = 2;
+    if (bwd_layout(P).total + 1024 > 232448) P.qs = 1;  // the 227 KB per-block limit
     const size_t smem = bwd_layout(P).total + 1024;
     auto kern = bf16 ? (p.bias_f32 ? tc_bwd_kernel<true, true> : tc_bwd_kernel<true, false>)
                      : (p.bias_f32 ? tc_bwd_kernel<false, true> : tc_bwd_kernel<false, false>);
