@@ -78,3 +78,90 @@ def tri_bwd(q, k, v, bias, d_out, mask=None, kv_lengths=None, scale=None):
                 dK[b, n, h] = s * (dx.T @ qm)
                 dBias[b, 0, h] += dx
     return dQ, dK, dV, dBias
+
+
+def _np(t, dtype=np.int64):
+    return None if t is None else np.asarray(t.detach().cpu().numpy() if hasattr(t, "detach") else t, dtype=dtype)
+
+
+def varlen_bwd(q, k, v, cu_seqlens_q, cu_seqlens_k, d_out, scale=None, kv_num_blocks=None, kv_indices=None,
+               full_kv_num_blocks=None, full_kv_indices=None, block=128, mask_mod="none", window=0,
+               prefix_lengths=None, bias=None):
+    """Gradients (dQ, dK, dV, dBias or None) of the packed-sequence forward, fp64 numpy.
+
+    Inputs as for ``oracle.varlen_fwd``; d_out (total_q, H, D).  Per sequence and
+    head the element mask follows the BlockMask page: the block lists rebuilt by
+    the page's reconstruction loop (full blocks win over partial ones, mask_mod
+    applies to partial blocks; without lists every block is partial), mask_mod
+    on local indices (causal k <= q; sliding window q - window < k <= q; prefix
+    LM k <= q or k < the prefix).  Masked keys have the constant logit -1e9, so
+    their dx is 0; keys past a sequence's end take no part.  dBias (H,
+    max_seqlen_q, max_seqlen_k) sums each sequence's dx at local positions.
+    """
+    from . import to_dense
+    Qa, Ka, Va = widen(q), widen(k), widen(v)
+    dO = np.asarray(d_out.detach().cpu().double().numpy() if hasattr(d_out, "detach") else d_out, dtype=np.float64)
+    total_q, H, D = Qa.shape
+    cq, ck = _np(cu_seqlens_q), _np(cu_seqlens_k)
+    S = len(cq) - 1
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    s = float(np.float32(scale))
+    Ba = widen(bias) if bias is not None else None
+    kn, ki, fn, fi = _np(kv_num_blocks), _np(kv_indices), _np(full_kv_num_blocks), _np(full_kv_indices)
+    dQ, dK, dV = np.zeros_like(Qa), np.zeros_like(Ka), np.zeros_like(Va)
+    dBias = np.zeros_like(Ba) if Ba is not None else None
+    for si in range(S):
+        q0, q1, k0, k1 = int(cq[si]), int(cq[si + 1]), int(ck[si]), int(ck[si + 1])
+        Lq, Lk = q1 - q0, k1 - k0
+        if Lq <= 0 or Lk <= 0:
+            continue
+        if prefix_lengths is None:
+            pre = 0
+        elif isinstance(prefix_lengths, int):
+            pre = prefix_lengths
+        else:
+            pre = int(_np(prefix_lengths)[si])
+        qi, kj = np.arange(Lq)[:, None], np.arange(Lk)[None, :]
+        if mask_mod == "causal":
+            mod = kj <= qi
+        elif mask_mod == "sliding_window":
+            mod = (kj <= qi) & (kj > qi - window)
+        elif mask_mod == "prefix_lm":
+            mod = (kj <= qi) | (kj < pre)
+        else:
+            mod = np.ones((Lq, Lk), dtype=bool)
+        nqb, nkb = (Lq + block - 1) // block, (Lk + block - 1) // block
+        for h in range(H):
+            if kn is None:
+                part = np.ones((nqb, nkb), dtype=bool)
+                full = np.zeros((nqb, nkb), dtype=bool)
+            else:
+                hm = 0 if kn.shape[1] == 1 else h
+                MQ = kn.shape[2]
+                part = np.zeros((nqb, nkb), dtype=bool)
+                full = np.zeros((nqb, nkb), dtype=bool)
+                rows = min(nqb, MQ)
+                part[:rows] = to_dense(kn[si, hm, :rows], ki[si, hm, :rows], nkb).astype(bool)
+                if fn is not None:
+                    full[:rows] = to_dense(fn[si, hm, :rows], fi[si, hm, :rows], nkb).astype(bool)
+                part &= ~full
+            bf = np.repeat(np.repeat(full, block, 0), block, 1)[:Lq, :Lk]
+            bp = np.repeat(np.repeat(part, block, 0), block, 1)[:Lq, :Lk]
+            valid = bf | (bp & mod)
+            qm, km, vm, do = Qa[q0:q1, h], Ka[k0:k1, h], Va[k0:k1, h], dO[q0:q1, h]
+            x = s * (qm @ km.T)
+            if Ba is not None:
+                x = x + Ba[h, :Lq, :Lk]
+            x[~valid] = MASKED
+            e = np.exp(x - x.max(axis=1, keepdims=True))
+            P = e / e.sum(axis=1, keepdims=True)
+            dV[k0:k1, h] += P.T @ do
+            dP = do @ vm.T
+            dx = P * (dP - (P * dP).sum(axis=1, keepdims=True))
+            dx[~valid] = 0.0
+            dQ[q0:q1, h] += s * (dx @ km)
+            dK[k0:k1, h] += s * (dx.T @ qm)
+            if dBias is not None:
+                dBias[h, :Lq, :Lk] += dx
+    return dQ, dK, dV, dBias

@@ -114,3 +114,94 @@ def test_bias_gradient_rows_sum_to_zero():
     q, k, v, bias, d_out, _, _ = _case(51, B=1, N=3, H=2, Q=4, K=7, D=5)
     _, _, _, dB = tri_bwd(q, k, v, bias, d_out)
     assert np.abs(dB.sum(axis=-1)).max() < 1e-12
+
+
+# ---------------------------------------------------------------------------
+# Packed sequences (oracle.backward.varlen_bwd)
+# ---------------------------------------------------------------------------
+
+from oracle.backward import varlen_bwd  # noqa: E402
+
+
+def test_varlen_bwd_one_sequence_is_the_triangle_backward():
+    """One sequence, no lists, mask_mod none: the (B=N=1) triangle problem."""
+    g = torch.Generator().manual_seed(41)
+    Lq, Lk, H, D = 37, 29, 2, 8
+    q, k, v = (torch.randn(L, H, D, generator=g) for L in (Lq, Lk, Lk))
+    bias = torch.randn(H, Lq, Lk, generator=g)
+    do = torch.randn(Lq, H, D, generator=g, dtype=torch.float64)
+    r = varlen_bwd(q, k, v, torch.tensor([0, Lq]), torch.tensor([0, Lk]), do, scale=0.3, bias=bias)
+    tri = lambda t: t.permute(1, 0, 2)[None, None].contiguous()
+    t = tri_bwd(tri(q), tri(k), tri(v), bias[None, None].contiguous(), tri(do), scale=0.3)
+    for a, b in zip(r[:3], t[:3]):
+        np.testing.assert_allclose(a, b[0, 0].transpose(1, 0, 2), atol=1e-12)
+    np.testing.assert_allclose(r[3], t[3][0, 0], atol=1e-12)
+
+
+def _element_mask(Lq, Lk, block, part_sets, full_sets, mod, window, prefix):
+    """(Lq, Lk) bool built key by key from block sets (dicts qb -> set of kb) and the
+    mask_mod rule, written out directly; no lists (part_sets None) = every block partial."""
+    m = torch.zeros(Lq, Lk, dtype=torch.bool)
+    for qq in range(Lq):
+        for kk in range(Lk):
+            qb, kb = qq // block, kk // block
+            if part_sets is None:
+                full, part = False, True
+            else:
+                full = kb in full_sets.get(qb, set())
+                part = (kb in part_sets.get(qb, set())) and not full
+            keep = {"none": True, "causal": kk <= qq, "sliding_window": qq - window < kk <= qq,
+                    "prefix_lm": kk <= qq or kk < prefix}[mod]
+            m[qq, kk] = full or (part and keep)
+    return m
+
+
+@pytest.mark.parametrize("mod", ["none", "causal", "sliding_window", "prefix_lm"])
+@pytest.mark.parametrize("lists", [False, True])
+def test_varlen_bwd_matches_torch_autograd(mod, lists):
+    """Several sequences (Lq != Lk, one of them all masked when lists skip its blocks), block
+    size 4, a post-scale bias: fp64 autograd through a masked softmax with the element
+    mask of `_element_mask`."""
+    g = torch.Generator().manual_seed(51)
+    lq, lk, H, D, block, window = [9, 6, 5], [7, 10, 5], 2, 4, 4, 3
+    cq = torch.tensor([0, 9, 15, 20]); ck = torch.tensor([0, 7, 17, 22])
+    q, k, v = torch.randn(20, H, D, generator=g), torch.randn(22, H, D, generator=g), torch.randn(22, H, D, generator=g)
+    bias = torch.randn(H, 9, 10, generator=g)
+    do = torch.randn(20, H, D, generator=g, dtype=torch.float64)
+    prefix = [2, 0, 4]
+    kn = ki = fn = fi = None
+    part_sets = full_sets = None
+    if lists:
+        MQ, MK = 3, 3
+        # per sequence (mask_heads 1): q block -> partial / full kv blocks (entries past the count unread)
+        P = [{0: [0], 1: [1, 0], 2: [1]}, {0: [0, 2], 1: []}, {0: [], 1: [1]}]
+        F = [{1: [0]}, {0: [1]}, {}]
+        kn = torch.zeros(3, 1, MQ, dtype=torch.int32); ki = torch.full((3, 1, MQ, MK), 7, dtype=torch.int32)
+        fn = torch.zeros(3, 1, MQ, dtype=torch.int32); fi = torch.full((3, 1, MQ, MK), 7, dtype=torch.int32)
+        for s_ in range(3):
+            for qb, kbs in P[s_].items():
+                kn[s_, 0, qb] = len(kbs)
+                ki[s_, 0, qb, :len(kbs)] = torch.tensor(kbs, dtype=torch.int32) if kbs else ki[s_, 0, qb, :0]
+            for qb, kbs in F[s_].items():
+                fn[s_, 0, qb] = len(kbs)
+                fi[s_, 0, qb, :len(kbs)] = torch.tensor(kbs, dtype=torch.int32)
+        part_sets = [{qb: set(v_) for qb, v_ in P[s_].items()} for s_ in range(3)]
+        full_sets = [{qb: set(v_) for qb, v_ in F[s_].items()} for s_ in range(3)]
+    scale = 0.375  # exact in fp32 (the oracle takes the scale as the kernels' float)
+    got = varlen_bwd(q, k, v, cq, ck, do, scale=scale, kv_num_blocks=kn, kv_indices=ki, full_kv_num_blocks=fn,
+                     full_kv_indices=fi, block=block, mask_mod=mod, window=window,
+                     prefix_lengths=torch.tensor(prefix), bias=bias)
+    qd, kd, vd, bd = (t.double().clone().requires_grad_(True) for t in (q, k, v, bias))
+    loss = 0.0
+    for s_ in range(3):
+        q0, k0, Lq, Lk = int(cq[s_]), int(ck[s_]), lq[s_], lk[s_]
+        m = _element_mask(Lq, Lk, block, None if part_sets is None else part_sets[s_],
+                          None if full_sets is None else full_sets[s_], mod, window, prefix[s_])
+        for h in range(H):
+            x = scale * (qd[q0:q0 + Lq, h] @ kd[k0:k0 + Lk, h].T) + bd[h, :Lq, :Lk]
+            x = torch.where(m, x, torch.full_like(x, -1e9))
+            o = torch.softmax(x, dim=-1) @ vd[k0:k0 + Lk, h]
+            loss = loss + (o * do[q0:q0 + Lq, h]).sum()
+    loss.backward()
+    for a, t in zip(got, (qd, kd, vd, bd)):
+        np.testing.assert_allclose(a, t.grad.numpy(), atol=1e-10, rtol=1e-9)
