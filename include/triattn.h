@@ -328,6 +328,51 @@ ta_status tri_attn_varlen_fwd_masked(const void* q, const void* k, const void* v
                                      void* out, float* lse, float* max, void* stream);
 
 /*
+ * tri_attn_varlen_bwd -- gradients of the packed-sequence forward
+ * (tri_attn_varlen_fwd_masked with contiguous rows): dQ, dK, dV and, with a
+ * bias, dBias.  (cuEquivariance triangle_attention page, Notes 1: context saved
+ * for backward; tensorplay BlockMask page, Details 1-4: the block lists decide
+ * which (query, key) blocks take part, full blocks skip mask_mod.)
+ * Per sequence and head, with P = exp(x - lse) from the forward's lse:
+ *     dV = P^T dO,  dx = P (dP - sum_k P dP) at valid keys (0 at masked ones),
+ *     dQ = s dx K,  dK = s dx^T Q,  dBias[h, q, k] = sum over sequences of dx.
+ * A key is valid for a query when its block is a full block, or a partial
+ * block (every block without lists) whose mask_mod keeps it; keys of blocks
+ * the lists leave out are masked.
+ *   q, k, v, dtype, cu_seqlens_*, num_seqs, total_*, max_seqlen_*, H, D, scale,
+ *   the block lists, mask_mod, window, prefix_lengths / prefix_length, bias,
+ *   bias_dtype    as given to tri_attn_varlen_fwd_masked; q / k / v contiguous
+ *                 (total, H, D).
+ *   lse           (H, total_q) fp32 from the forward (required).
+ *   out           the forward's O (total_q, H, D) (required: sum_k P dP is the
+ *                 row sum of dO * O).
+ *   d_out         (total_q, H, D) in dtype.
+ *   dq, dk, dv    outputs shaped like q, k, v.
+ *   dbias         (H, max_seqlen_q, max_seqlen_k) in bias_dtype, or NULL (needs a bias).
+ *   workspace     device scratch of tri_attn_varlen_bwd_workspace_size(...,
+ *                 with_bias = dbias != NULL) bytes, 256-byte aligned, owned by
+ *                 the caller.
+ * Arithmetic: exact fp32 on CUDA cores for every dtype (one CTA per sequence,
+ * head and 32 keys; dQ and dBias added with fp32 atomics, so their summation
+ * order varies from run to run).  Errors as tri_attn_bwd; a sequence that
+ * breaks the max_seqlen / total contract is skipped and TA_ERR_DEVICE recorded.
+ */
+ta_status tri_attn_varlen_bwd(const void* q, const void* k, const void* v, ta_dtype dtype,
+                              const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int num_seqs,
+                              int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int H, int D,
+                              float scale, const int32_t* kv_num_blocks, const int32_t* kv_indices,
+                              const int32_t* full_kv_num_blocks, const int32_t* full_kv_indices,
+                              int mask_heads, int max_q_blocks, int max_kv_blocks, int block_q, int block_k,
+                              ta_mask_mod mask_mod, int window, const int32_t* prefix_lengths, int prefix_length,
+                              const void* bias, ta_dtype bias_dtype, const float* lse, const void* out,
+                              const void* d_out, void* dq, void* dk, void* dv, void* dbias, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace tri_attn_varlen_bwd needs (0 for a negative size). */
+size_t tri_attn_varlen_bwd_workspace_size(int total_q, int H, int D, int max_seqlen_q, int max_seqlen_k,
+                                          int with_bias);
+
+/*
  * tri_attn_mask_to_kv_lengths -- dense key mask -> prefix lengths.
  * (triangle_attention page, Example: mask_to_kv_lengths(mask).)
  *

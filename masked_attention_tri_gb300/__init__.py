@@ -8,7 +8,9 @@ CUDA, tcgen05 / TMA); this package only marshals tensors into its C ABI.
 """
 from . import abi
 from .api import (BlockMask, get_status, mask_to_kv_lengths, triangle_attention, triangle_attention_autograd,
-                  triangle_attention_backward, varlen_attention, varlen_attention_kvpacked, varlen_attention_qkvpacked)
+                  triangle_attention_backward, varlen_attention, varlen_attention_backward,
+                  varlen_attention_kvpacked, varlen_attention_qkvpacked)
 
 __all__ = ["abi", "BlockMask", "get_status", "mask_to_kv_lengths", "triangle_attention", "triangle_attention_autograd",
-           "triangle_attention_backward", "varlen_attention", "varlen_attention_kvpacked", "varlen_attention_qkvpacked"]
+           "triangle_attention_backward", "varlen_attention", "varlen_attention_backward", "varlen_attention_kvpacked",
+           "varlen_attention_qkvpacked"]

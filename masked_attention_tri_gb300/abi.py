@@ -20,7 +20,8 @@ TA_MASK_NONE, TA_MASK_CAUSAL, TA_MASK_SLIDING_WINDOW, TA_MASK_PREFIX_LM = 0, 1, 
 
 # Every symbol include/triattn.h declares.
 EXPORTS = ("tri_attn_fwd", "tri_attn_fwd_strided", "tri_attn_varlen_fwd", "tri_attn_varlen_fwd_strided", "tri_attn_varlen_fwd_masked",
-           "tri_attn_bwd", "tri_attn_bwd_workspace_size", "tri_attn_bwd_noalloc",
+           "tri_attn_bwd", "tri_attn_bwd_workspace_size", "tri_attn_bwd_noalloc", "tri_attn_varlen_bwd",
+           "tri_attn_varlen_bwd_workspace_size",
            "tri_attn_mask_to_kv_lengths", "tri_attn_get_status", "tri_attn_error_string", "tri_attn_version")
 
 _lock = threading.Lock()
@@ -63,6 +64,11 @@ def load() -> ctypes.CDLL:
         lib.tri_attn_bwd.restype = I
         lib.tri_attn_bwd_noalloc.argtypes = [P, P, P, I, P, I, P, P, I, I, I, I, I, I, F, P, P, P, P, P, P, P, P]
         lib.tri_attn_bwd_noalloc.restype = I
+        lib.tri_attn_varlen_bwd.argtypes = [P, P, P, I, P, P, I, I, I, I, I, I, I, F, P, P, P, P, I, I, I, I, I, I,
+                                            I, P, I, P, I, P, P, P, P, P, P, P, P, Z, P]
+        lib.tri_attn_varlen_bwd.restype = I
+        lib.tri_attn_varlen_bwd_workspace_size.argtypes = [I, I, I, I, I, I]
+        lib.tri_attn_varlen_bwd_workspace_size.restype = Z
         lib.tri_attn_bwd_workspace_size.argtypes = [I, I, I, I, I, I]
         lib.tri_attn_bwd_workspace_size.restype = Z
         lib.tri_attn_mask_to_kv_lengths.argtypes = [P, I, I, I, P, P, P]
@@ -120,6 +126,26 @@ def tri_attn_bwd_noalloc(q, k, v, qkv_dtype, bias, bias_dtype, mask, kv_lengths,
 
 # Bytes of the static scratch tri_attn_bwd_noalloc works in (TRI_ATTN_BWD_NOALLOC_SCRATCH_BYTES).
 BWD_NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def tri_attn_varlen_bwd(q, k, v, dtype, cu_seqlens_q, cu_seqlens_k, num_seqs, total_q, total_k, max_seqlen_q,
+                        max_seqlen_k, H, D, scale, kv_num_blocks, kv_indices, full_kv_num_blocks, full_kv_indices,
+                        mask_heads, max_q_blocks, max_kv_blocks, block_q, block_k, mask_mod, window,
+                        prefix_lengths, prefix_length, bias, bias_dtype, lse, out, d_out, dq, dk, dv, dbias,
+                        workspace, workspace_bytes, stream) -> None:
+    st = load().tri_attn_varlen_bwd(q, k, v, dtype, cu_seqlens_q, cu_seqlens_k, num_seqs, total_q, total_k,
+                                    max_seqlen_q, max_seqlen_k, H, D, float(scale), kv_num_blocks or None,
+                                    kv_indices or None, full_kv_num_blocks or None, full_kv_indices or None,
+                                    mask_heads, max_q_blocks, max_kv_blocks, block_q, block_k, mask_mod, window,
+                                    prefix_lengths or None, prefix_length, bias or None, bias_dtype, lse, out,
+                                    d_out, dq, dk, dv, dbias or None, workspace, int(workspace_bytes),
+                                    stream or None)
+    _check(st, "tri_attn_varlen_bwd")
+
+
+def tri_attn_varlen_bwd_workspace_size(total_q, H, D, max_seqlen_q, max_seqlen_k, with_bias) -> int:
+    return int(load().tri_attn_varlen_bwd_workspace_size(total_q, H, D, max_seqlen_q, max_seqlen_k,
+                                                         1 if with_bias else 0))
 
 
 def tri_attn_bwd_workspace_size(B, N, H, Q, K, D) -> int:

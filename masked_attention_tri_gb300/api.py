@@ -379,6 +379,43 @@ def _row_stride(t: torch.Tensor, name: str, device: torch.device) -> int:
     return t.stride(0)
 
 
+def _mask_args(block_mask, mask_mod, dev):
+    """The C ABI's block-mask arguments of a BlockMask (or none) and a mask_mod name."""
+    kn = ki = fn = fi = None
+    mask_heads = MQ = MK = 0
+    bq = bk = 128
+    if mask_mod not in _MASK_MODS:
+        raise ValueError(f"mask_mod must be one of {sorted(k for k in _MASK_MODS if k)} or None")
+    mm = _MASK_MODS[mask_mod]
+    if block_mask is not None:
+        kn, ki = block_mask.kv_num_blocks, block_mask.kv_indices
+        fn, fi = block_mask.full_kv_num_blocks, block_mask.full_kv_indices
+        for t, nm in ((kn, "kv_num_blocks"), (ki, "kv_indices"), (fn, "full_kv_num_blocks"),
+                      (fi, "full_kv_indices")):
+            if t is not None:
+                _need(t, nm, dev)
+                if t.dtype != torch.int32:
+                    raise TypeError(f"{nm} must be int32")
+        if kn.dim() != 3 or ki.dim() != 4:
+            raise ValueError("kv_num_blocks must be (S, Hm, MQ) and kv_indices (S, Hm, MQ, MK)")
+        mask_heads, MQ, MK = kn.shape[1], kn.shape[2], ki.shape[3]
+        if fn is not None and (tuple(fn.shape) != tuple(kn.shape) or tuple(fi.shape) != tuple(ki.shape)):
+            raise ValueError("full_kv_* must have the shapes of kv_*")
+        bq, bk = block_mask.BLOCK_SIZE
+        mm = block_mask.mask_mod_code
+    return kn, ki, fn, fi, mask_heads, MQ, MK, bq, bk, mm
+
+
+def _prefix_args(prefix_lengths, S, dev):
+    """(per-sequence tensor or None, one length for all) for the prefix-LM mask_mod."""
+    if isinstance(prefix_lengths, torch.Tensor):
+        _need(prefix_lengths, "prefix_lengths", dev)
+        if prefix_lengths.dtype != torch.int32 or prefix_lengths.numel() != S:
+            raise ValueError("prefix_lengths must be int32 with one entry per sequence")
+        return prefix_lengths, 0
+    return None, (0 if prefix_lengths is None else int(prefix_lengths))
+
+
 def varlen_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, block_mask=None, scale=None,
                      return_aux=False, *, mask_mod=None, out=None, window=0, prefix_lengths=None, bias=None):
     """Packed-sequence forward with an optional BlockMask.
@@ -416,28 +453,7 @@ def varlen_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seql
     if cu_seqlens_k.numel() != S + 1 or S <= 0:
         raise ValueError("cu_seqlens_q / cu_seqlens_k must both have num_seqs + 1 entries")
     s = 1.0 / math.sqrt(D) if scale is None else float(scale)
-    kn = ki = fn = fi = None
-    mask_heads = MQ = MK = 0
-    bq = bk = 128
-    if mask_mod not in _MASK_MODS:
-        raise ValueError(f"mask_mod must be one of {sorted(k for k in _MASK_MODS if k)} or None")
-    mm = _MASK_MODS[mask_mod]
-    if block_mask is not None:
-        kn, ki = block_mask.kv_num_blocks, block_mask.kv_indices
-        fn, fi = block_mask.full_kv_num_blocks, block_mask.full_kv_indices
-        for t, nm in ((kn, "kv_num_blocks"), (ki, "kv_indices"), (fn, "full_kv_num_blocks"),
-                      (fi, "full_kv_indices")):
-            if t is not None:
-                _need(t, nm, dev)
-                if t.dtype != torch.int32:
-                    raise TypeError(f"{nm} must be int32")
-        if kn.dim() != 3 or ki.dim() != 4:
-            raise ValueError("kv_num_blocks must be (S, Hm, MQ) and kv_indices (S, Hm, MQ, MK)")
-        mask_heads, MQ, MK = kn.shape[1], kn.shape[2], ki.shape[3]
-        if fn is not None and (tuple(fn.shape) != tuple(kn.shape) or tuple(fi.shape) != tuple(ki.shape)):
-            raise ValueError("full_kv_* must have the shapes of kv_*")
-        bq, bk = block_mask.BLOCK_SIZE
-        mm = block_mask.mask_mod_code
+    kn, ki, fn, fi, mask_heads, MQ, MK, bq, bk, mm = _mask_args(block_mask, mask_mod, dev)
     if out is None:
         out = torch.empty(total_q, H, D, device=dev, dtype=q.dtype)
     else:
@@ -452,14 +468,7 @@ def varlen_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seql
             raise ValueError(f"bias must be (H, max_seqlen_q, max_seqlen_k) = {(H, int(max_seqlen_q), int(max_seqlen_k))}")
         if bias.dtype not in (torch.float32, q.dtype):
             raise TypeError("bias must be float32 or q's dtype")
-    pl, p_all = None, 0
-    if isinstance(prefix_lengths, torch.Tensor):
-        _need(prefix_lengths, "prefix_lengths", dev)
-        if prefix_lengths.dtype != torch.int32 or prefix_lengths.numel() != S:
-            raise ValueError("prefix_lengths must be int32 with one entry per sequence")
-        pl = prefix_lengths
-    elif prefix_lengths is not None:
-        p_all = int(prefix_lengths)
+    pl, p_all = _prefix_args(prefix_lengths, S, dev)
     with torch.cuda.device(dev):
         abi.tri_attn_varlen_fwd_masked(_ptr(q), _ptr(k), _ptr(v), _DT[q.dtype], _ptr(cu_seqlens_q),
                                        _ptr(cu_seqlens_k), S, total_q, k.shape[0], int(max_seqlen_q),
@@ -491,6 +500,62 @@ def varlen_attention_kvpacked(q, kv, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, m
     k, v = kv.unbind(1)
     return varlen_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, block_mask, scale,
                             return_aux, mask_mod=mask_mod, out=out, window=window, prefix_lengths=prefix_lengths)
+
+
+def varlen_attention_backward(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, out, lse, d_out,
+                              block_mask=None, scale=None, *, mask_mod=None, window=0, prefix_lengths=None,
+                              bias=None, need_dbias=True):
+    """Gradients (dq, dk, dv, dbias) of ``varlen_attention`` for dL/dO = d_out.
+
+    Arguments as given to the forward (q / k / v contiguous (total, H, D)), plus
+    its O (``out``) and lse (H, total_q).  dbias (bias's shape and dtype, the sum
+    over sequences) is returned when a bias is given and need_dbias, else None.
+    """
+    if q.dim() != 3 or k.dim() != 3 or v.dim() != 3:
+        raise ValueError("expected q (total_q,H,D), k/v (total_k,H,D)")
+    total_q, H, D = q.shape
+    if tuple(k.shape[1:]) != (H, D) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("k and v must be (total_k, H, D) with q's H and D")
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("varlen_attention_backward runs on CUDA tensors only")
+    for t, nm in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (lse, "lse"), (d_out, "d_out"),
+                  (cu_seqlens_q, "cu_seqlens_q"), (cu_seqlens_k, "cu_seqlens_k")):
+        _need(t, nm, dev)
+    if q.dtype not in _DT or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share one dtype among float32 / float16 / bfloat16")
+    for t, nm in ((out, "out"), (d_out, "d_out")):
+        if tuple(t.shape) != tuple(q.shape) or t.dtype != q.dtype:
+            raise ValueError(f"{nm} must have q's shape and dtype")
+    if lse.dtype != torch.float32 or lse.numel() != H * total_q:
+        raise ValueError("lse must be float32 (H, total_q)")
+    if cu_seqlens_q.dtype != torch.int32 or cu_seqlens_k.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
+    S = cu_seqlens_q.numel() - 1
+    if cu_seqlens_k.numel() != S + 1 or S <= 0:
+        raise ValueError("cu_seqlens_q / cu_seqlens_k must both have num_seqs + 1 entries")
+    s = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    kn, ki, fn, fi, mask_heads, MQ, MK, bq, bk, mm = _mask_args(block_mask, mask_mod, dev)
+    pl, p_all = _prefix_args(prefix_lengths, S, dev)
+    if bias is not None:
+        _need(bias, "bias", dev)
+        if tuple(bias.shape) != (H, int(max_seqlen_q), int(max_seqlen_k)):
+            raise ValueError(f"bias must be (H, max_seqlen_q, max_seqlen_k) = {(H, int(max_seqlen_q), int(max_seqlen_k))}")
+        if bias.dtype not in (torch.float32, q.dtype):
+            raise TypeError("bias must be float32 or q's dtype")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dbias = torch.empty_like(bias) if (bias is not None and need_dbias) else None
+    nbytes = abi.tri_attn_varlen_bwd_workspace_size(total_q, H, D, int(max_seqlen_q), int(max_seqlen_k),
+                                                    dbias is not None)
+    ws = torch.empty(max(nbytes // 4, 1), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        abi.tri_attn_varlen_bwd(_ptr(q), _ptr(k), _ptr(v), _DT[q.dtype], _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), S,
+                                total_q, k.shape[0], int(max_seqlen_q), int(max_seqlen_k), H, D, s, _ptr(kn),
+                                _ptr(ki), _ptr(fn), _ptr(fi), mask_heads, MQ, MK, bq, bk, mm, int(window),
+                                _ptr(pl), p_all, _ptr(bias), _DT[bias.dtype] if bias is not None else abi.TA_F32,
+                                _ptr(lse), _ptr(out), _ptr(d_out), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias),
+                                _ptr(ws), nbytes, _stream(dev))
+    return dq, dk, dv, dbias
 
 
 def get_status(device=None) -> int:

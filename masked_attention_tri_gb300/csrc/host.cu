@@ -349,7 +349,120 @@ TA_EXPORT ta_status tri_attn_bwd(const void* q, const void* k, const void* v, ta
     p.Q = Q;
     p.K = K;
     p.D = D;
+    p.dq_elems = units * Q * D;
+    p.dbias_elems = (long long)B * H * Q * K;
+    p.delta_rows = units * Q;
+    p.status = triattn::status_word();
+    if (!p.status) return TA_ERR_CUDA;
     p.tc_main = triattn::tc_bwd_supported(p) ? 1 : 0;
+    const cudaError_t e = triattn::launch_simt_bwd(p, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TA_OK : TA_ERR_CUDA;
+}
+
+TA_EXPORT size_t tri_attn_varlen_bwd_workspace_size(int total_q, int H, int D, int max_seqlen_q, int max_seqlen_k,
+                                                   int with_bias) {
+    if (total_q < 0 || H <= 0 || D <= 0 || max_seqlen_q < 0 || max_seqlen_k < 0) return 0;
+    const long long rows = (long long)total_q * H;
+    const long long nb = with_bias ? (long long)H * max_seqlen_q * max_seqlen_k : 0;
+    return triattn::bwd_workspace_floats_n(rows * D, nb, rows) * sizeof(float);
+}
+
+TA_EXPORT ta_status tri_attn_varlen_bwd(const void* q, const void* k, const void* v, ta_dtype dtype,
+                                        const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int num_seqs,
+                                        int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int H, int D,
+                                        float scale, const int32_t* kv_num_blocks, const int32_t* kv_indices,
+                                        const int32_t* full_kv_num_blocks, const int32_t* full_kv_indices,
+                                        int mask_heads, int max_q_blocks, int max_kv_blocks, int block_q,
+                                        int block_k, ta_mask_mod mask_mod, int window,
+                                        const int32_t* prefix_lengths, int prefix_length, const void* bias,
+                                        ta_dtype bias_dtype, const float* lse, const void* out, const void* d_out,
+                                        void* dq, void* dk, void* dv, void* dbias, void* workspace,
+                                        size_t workspace_bytes, void* stream) {
+    if (!q || !k || !v || !cu_seqlens_q || !cu_seqlens_k || !lse || !out || !d_out || !dq || !dk || !dv ||
+        !workspace)
+        return TA_ERR_INVALID_ARG;
+    if (num_seqs <= 0 || H <= 0 || D <= 0 || max_seqlen_q < 0 || max_seqlen_k < 0) return TA_ERR_INVALID_ARG;
+    if (total_q < 0 || total_k < 0) return TA_ERR_INVALID_ARG;
+    if (!valid_dtype(dtype)) return TA_ERR_INVALID_ARG;
+    if (mask_mod < TA_MASK_NONE || mask_mod > TA_MASK_PREFIX_LM) return TA_ERR_INVALID_ARG;
+    if (mask_mod == TA_MASK_SLIDING_WINDOW && window <= 0) return TA_ERR_INVALID_ARG;
+    if (mask_mod == TA_MASK_PREFIX_LM && !prefix_lengths && prefix_length < 0) return TA_ERR_INVALID_ARG;
+    if (prefix_lengths && !aligned(prefix_lengths, 4)) return TA_ERR_INVALID_ARG;
+    if ((kv_num_blocks == nullptr) != (kv_indices == nullptr)) return TA_ERR_INVALID_ARG;
+    if ((full_kv_num_blocks == nullptr) != (full_kv_indices == nullptr)) return TA_ERR_INVALID_ARG;
+    if (full_kv_num_blocks && !kv_num_blocks) return TA_ERR_INVALID_ARG;
+    if (kv_num_blocks) {
+        if (mask_heads != 1 && mask_heads != H) return TA_ERR_INVALID_ARG;
+        if (max_q_blocks <= 0 || max_kv_blocks <= 0) return TA_ERR_INVALID_ARG;
+    }
+    if (dbias && !bias) return TA_ERR_INVALID_ARG;
+    if (bias) {
+        if (!valid_dtype(bias_dtype) || !aligned(bias, 16) || (dbias && !aligned(dbias, 16))) return TA_ERR_INVALID_ARG;
+        if (bias_dtype != TA_F32 && bias_dtype != dtype) return TA_ERR_UNSUPPORTED;
+    }
+    const void* ptrs16[] = {q, k, v, out, d_out, dq, dk, dv};
+    for (const void* ptr : ptrs16)
+        if (!aligned(ptr, 16)) return TA_ERR_INVALID_ARG;
+    if (!aligned(lse, 4) || !aligned(workspace, 256)) return TA_ERR_INVALID_ARG;
+    if (block_q != 128 || block_k != 128) return TA_ERR_UNSUPPORTED;
+    if (!supported_d(dtype, D)) return TA_ERR_UNSUPPORTED;
+    if ((long long)num_seqs * H * ((max_seqlen_k + 31) / 32) > 0x7fffffffLL) return TA_ERR_UNSUPPORTED;
+    if (workspace_bytes < tri_attn_varlen_bwd_workspace_size(total_q, H, D, max_seqlen_q, max_seqlen_k, dbias != nullptr))
+        return TA_ERR_INVALID_ARG;
+    if (total_q == 0) return TA_OK;
+
+    triattn::BwdParams p{};
+    const long long rows = (long long)total_q * H;
+    p.dq_elems = rows * D;
+    p.dbias_elems = dbias ? (long long)H * max_seqlen_q * max_seqlen_k : 0;
+    p.delta_rows = rows;
+    float* ws = static_cast<float*>(workspace);
+    auto up = [](long long n) { return (n + 63) & ~63LL; };
+    p.dq_acc = ws;
+    p.dbias_acc = dbias ? ws + up(p.dq_elems) : nullptr;
+    p.delta = ws + up(p.dq_elems) + up(p.dbias_elems);
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.bias = bias;
+    p.d_out = d_out;
+    p.lse = lse;
+    p.out = out;
+    p.dq = dq;
+    p.dk = dk;
+    p.dv = dv;
+    p.dbias = dbias;
+    p.dtype = dtype;
+    p.bias_f32 = bias && bias_dtype == TA_F32;
+    p.scale = scale;
+    p.B = 1;
+    p.N = 1;
+    p.H = H;
+    p.D = D;
+    p.Q = 0;
+    p.K = 0;
+    p.varlen = 1;
+    p.cu_q = cu_seqlens_q;
+    p.cu_k = cu_seqlens_k;
+    p.num_seqs = num_seqs;
+    p.total_q = total_q;
+    p.total_k = total_k;
+    p.max_q = max_seqlen_q;
+    p.max_k = max_seqlen_k;
+    p.kv_num = kv_num_blocks;
+    p.kv_idx = kv_indices;
+    p.full_num = full_kv_num_blocks;
+    p.full_idx = full_kv_indices;
+    p.mask_heads = kv_num_blocks ? mask_heads : 1;
+    p.MQ = kv_num_blocks ? max_q_blocks : 0;
+    p.MK = kv_num_blocks ? max_kv_blocks : 0;
+    p.mask_mod = mask_mod;
+    p.window = mask_mod == TA_MASK_SLIDING_WINDOW ? window : 0;
+    p.prefix_len = mask_mod == TA_MASK_PREFIX_LM ? prefix_lengths : nullptr;
+    p.prefix_all = mask_mod == TA_MASK_PREFIX_LM ? prefix_length : 0;
+    p.status = triattn::status_word();
+    if (!p.status) return TA_ERR_CUDA;
+    p.tc_main = 0;
     const cudaError_t e = triattn::launch_simt_bwd(p, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TA_OK : TA_ERR_CUDA;
 }

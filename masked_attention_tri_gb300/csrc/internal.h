@@ -78,9 +78,27 @@ struct BwdParams {
     float scale;
     int B, N, H, Q, K, D;
     int tc_main;            // 1: the per-key-tile gradients on tensor cores (tc_bwd.cu)
+    // Element counts of dQ and dBias and the number of per-row sums (either form).
+    long long dq_elems, dbias_elems, delta_rows;
+    // Packed sequences (varlen = 1): q / k / v / O / dO (total, H, D), lse / delta (H, total_q),
+    // the optional bias and dBias (H, max_seqlen_q, max_seqlen_k), the BlockMask lists.
+    int varlen;
+    const int32_t* cu_q;
+    const int32_t* cu_k;
+    int num_seqs, total_q, total_k, max_q, max_k;
+    const int32_t* kv_num;
+    const int32_t* kv_idx;
+    const int32_t* full_num;
+    const int32_t* full_idx;
+    int mask_heads, MQ, MK, mask_mod, window;
+    const int32_t* prefix_len;
+    int prefix_all;
+    int* status;
 };
-// Workspace of the backward in floats (three pieces, each a multiple of 64 floats).
+// Workspace of the backward in floats: dQ, dBias and the per-row sums, each rounded up
+// to a multiple of 64 floats.
 size_t bwd_workspace_floats(int B, int N, int H, int Q, int K, int D);
+size_t bwd_workspace_floats_n(long long dq_elems, long long dbias_elems, long long delta_rows);
 cudaError_t launch_simt_bwd(const BwdParams& p, cudaStream_t stream);
 // The tensor-core form of the backward's per-key-tile kernel (16-bit, D % 16 == 0,
 // D <= 64, K % 8 == 0); the caller runs the per-row sums before and the conversion after.

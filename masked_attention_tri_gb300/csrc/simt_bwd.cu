@@ -15,6 +15,11 @@
 // -1e9 once stored in fp32; such a row (lse at or below -1e9 + 64, while any
 // valid logit lies above -1e9 + 100) takes its exact weights 1/K.
 //
+// The same kernels serve packed sequences (q / k / v / O / dO (total, H, D),
+// lse / delta (H, total_q), the BlockMask lists and mask_mod deciding each
+// (query, key) pair, an optional (H, max_seqlen_q, max_seqlen_k) bias whose
+// gradient sums over the sequences); there the per-row sums come from O.
+//
 // Three kernels:
 //   delta   one CTA per (slab, 32 query rows): delta[q] = sum_k P dP over every key
 //           (the exact definition); zeroes the fp32 dQ accumulator rows and
@@ -79,12 +84,47 @@ __device__ __forceinline__ bool key_valid(const BwdParams& p, long long bn, int 
 }
 
 // Loads rows [r0, r0 + 32) of a (rows x D) slab matrix into smem [32][D + 1] as fp32 (zeros past `rows`).
+// Rows `rs` elements apart (D for the triangle form, H * D for packed sequences).
 template <typename T>
-__device__ __forceinline__ void load_tile(float* dst, const T* src, long long base, int r0, int rows, int D) {
+__device__ __forceinline__ void load_tile(float* dst, const T* src, long long base, int r0, int rows, int D,
+                                          long long rs) {
     const int Dp1 = D + 1;
     for (int e = threadIdx.x; e < kT * D; e += blockDim.x) {
         const int r = e / D, d = e - r * D;
-        dst[r * Dp1 + d] = (r0 + r < rows) ? ld_f(src, base + (long long)(r0 + r) * D + d) : 0.f;
+        dst[r * Dp1 + d] = (r0 + r < rows) ? ld_f(src, base + (long long)(r0 + r) * rs + d) : 0.f;
+    }
+}
+template <typename T>
+__device__ __forceinline__ void load_tile(float* dst, const T* src, long long base, int r0, int rows, int D) {
+    load_tile(dst, src, base, r0, rows, D, (long long)D);
+}
+
+// Packed sequences: the BlockMask status of q block qb and kv block kb (tensorplay
+// BlockMask page, Details 1-2): 2 = full (mask_mod skipped), 1 = partial (mask_mod
+// applies; also every block when no lists are given), 0 = not visited (masked).
+__device__ __forceinline__ int block_status(const BwdParams& p, int seq, int h, int qb, int kb) {
+    if (!p.kv_num) return 1;
+    if (qb >= p.MQ) return 0;
+    const int hm = p.mask_heads == 1 ? 0 : h;
+    const long long row = ((long long)seq * p.mask_heads + hm) * p.MQ + qb;
+    if (p.full_num) {
+        const int n = min(max(p.full_num[row], 0), p.MK);
+        for (int t = 0; t < n; ++t)
+            if (p.full_idx[row * p.MK + t] == kb) return 2;
+    }
+    const int n = min(max(p.kv_num[row], 0), p.MK);
+    for (int t = 0; t < n; ++t)
+        if (p.kv_idx[row * p.MK + t] == kb) return 1;
+    return 0;
+}
+// mask_mod on a partial block, local indices: causal k <= q; sliding window
+// q - window < k <= q; prefix LM k <= q or k < prefix.
+__device__ __forceinline__ bool mod_keep(int mod, int q, int k, int window, int prefix) {
+    switch (mod) {
+    case TA_MASK_CAUSAL: return k <= q;
+    case TA_MASK_SLIDING_WINDOW: return k <= q && k > q - window;
+    case TA_MASK_PREFIX_LM: return k <= q || k < prefix;
+    default: return true;
     }
 }
 
@@ -177,12 +217,12 @@ __global__ void __launch_bounds__(kBW * 32) bwd_delta_kernel(const BwdParams p) 
 template <typename T>
 __global__ void __launch_bounds__(256) bwd_delta_out_kernel(const BwdParams p) {
     constexpr int kE = 16 / (int)sizeof(T);  // elements per 16-byte chunk
-    const long long rows = (long long)p.B * p.N * p.H * p.Q;
+    const long long rows = p.delta_rows;  // (b,n,h,q) rows, or (token, head) rows of packed sequences
     const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) / 8;
     const int g = threadIdx.x % 8;
     if (p.dbias_acc) {
-        const long long tot = (long long)p.B * p.H * p.Q * p.K;
-        for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < tot; e += (long long)gridDim.x * blockDim.x)
+        for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < p.dbias_elems;
+             e += (long long)gridDim.x * blockDim.x)
             p.dbias_acc[e] = 0.f;
     }
     float acc = 0.f;
@@ -202,10 +242,10 @@ __global__ void __launch_bounds__(256) bwd_delta_out_kernel(const BwdParams p) {
     }
 #pragma unroll
     for (int o = 4; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (g == 0 && row < rows) p.delta[row] = acc;
+    if (g == 0 && row < rows) p.delta[p.varlen ? (row % p.H) * p.total_q + row / p.H : row] = acc;
 }
 
-template <typename T, typename BT, int DPL>
+template <typename T, typename BT, int DPL, bool VARLEN>
 __global__ void __launch_bounds__(kBW * 32) bwd_main_kernel(const BwdParams p) {
     extern __shared__ float sm[];
     const int D = p.D, Dp1 = D + 1;
@@ -216,31 +256,66 @@ __global__ void __launch_bounds__(kBW * 32) bwd_main_kernel(const BwdParams p) {
     float* Ps = dOs + kT * Dp1;       // [32 rows][33]
     float* dSs = Ps + kT * (kT + 1);  // [32 rows][33]
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int nkt = (p.K + kT - 1) / kT;
-    const long long unit = blockIdx.x / nkt;
-    const int k0 = (int)(blockIdx.x - unit * nkt) * kT;
-    const int h = (int)(unit % p.H);
-    const long long bn = unit / p.H;
-    const int b = (int)(bn / p.N);
-    const long long qbase = unit * p.Q * D, kbase = unit * (long long)p.K * D;
+    // The unit's rows: queries q at qbase + q * rs, keys k at kbase + k * rs, lse / delta at
+    // lrow0 + q, bias / dBias at brow0 + q * bstride + k.
+    long long qbase, kbase, rs, lrow0, brow0, bstride, bn = 0;
+    int Lq, Lk, k0, h, seq = 0, prefix = 0;
+    if constexpr (!VARLEN) {
+        const int nkt = (p.K + kT - 1) / kT;
+        const long long unit = blockIdx.x / nkt;
+        k0 = (int)(blockIdx.x - unit * nkt) * kT;
+        h = (int)(unit % p.H);
+        bn = unit / p.H;
+        const int b = (int)(bn / p.N);
+        qbase = unit * p.Q * D;
+        kbase = unit * (long long)p.K * D;
+        rs = D;
+        Lq = p.Q;
+        Lk = p.K;
+        lrow0 = unit * p.Q;
+        brow0 = ((long long)b * p.H + h) * p.Q * p.K;
+        bstride = p.K;
+    } else {
+        const int nkt = (p.max_k + kT - 1) / kT;
+        seq = blockIdx.x / (p.H * nkt);
+        h = (blockIdx.x / nkt) % p.H;
+        k0 = (blockIdx.x % nkt) * kT;
+        const int cq0 = p.cu_q[seq], cq1 = p.cu_q[seq + 1], ck0 = p.cu_k[seq], ck1 = p.cu_k[seq + 1];
+        Lq = cq1 - cq0;
+        Lk = ck1 - ck0;
+        if (Lq > p.max_q || Lk > p.max_k || Lq < 0 || Lk < 0 || cq0 < 0 || ck0 < 0 || cq1 > p.total_q ||
+            ck1 > p.total_k) {
+            if (threadIdx.x == 0 && k0 == 0 && h == 0) atomicCAS(p.status, 0, kStatusDevice);
+            return;
+        }
+        rs = (long long)p.H * D;
+        qbase = (long long)cq0 * rs + (long long)h * D;
+        kbase = (long long)ck0 * rs + (long long)h * D;
+        lrow0 = (long long)h * p.total_q + cq0;
+        brow0 = (long long)h * p.max_q * p.max_k;
+        bstride = p.max_k;
+        prefix = p.prefix_len ? p.prefix_len[seq] : p.prefix_all;
+    }
+    if (k0 >= Lk) return;
 
-    load_tile(Ks, static_cast<const T*>(p.k), kbase, k0, p.K, D);
-    load_tile(Vs, static_cast<const T*>(p.v), kbase, k0, p.K, D);
+    load_tile(Ks, static_cast<const T*>(p.k), kbase, k0, Lk, D, rs);
+    load_tile(Vs, static_cast<const T*>(p.v), kbase, k0, Lk, D, rs);
     const int key = k0 + lane;  // this lane's key in the score steps
-    const bool exists = key < p.K;
-    const bool valid = exists && key_valid(p, bn, key);
+    const bool exists = key < Lk;
+    const bool key_ok = !VARLEN ? (exists && key_valid(p, bn, key)) : exists;
+    const float inv_k = 1.f / (float)Lk;
     float dk[kBR][DPL], dv[kBR][DPL];
 #pragma unroll
     for (int j = 0; j < kBR; ++j)
 #pragma unroll
         for (int c = 0; c < DPL; ++c) dk[j][c] = dv[j][c] = 0.f;
     const BT* bias = static_cast<const BT*>(p.bias);
-    const long long brow = ((long long)b * p.H + h) * p.Q;
 
-    for (int q0 = 0; q0 < p.Q; q0 += kT) {
+    for (int q0 = 0; q0 < Lq; q0 += kT) {
         __syncthreads();  // the previous tile's Qs, dOs, Ps, dSs are no longer read
-        load_tile(Qs, static_cast<const T*>(p.q), qbase, q0, p.Q, D);
-        load_tile(dOs, static_cast<const T*>(p.d_out), qbase, q0, p.Q, D);
+        load_tile(Qs, static_cast<const T*>(p.q), qbase, q0, Lq, D, rs);
+        load_tile(dOs, static_cast<const T*>(p.d_out), qbase, q0, Lq, D, rs);
+        const int bstat = VARLEN ? block_status(p, seq, h, q0 / 128, k0 / 128) : 1;
         __syncthreads();
         float qk[kBR], dp[kBR];
         scores(Qs, Ks, dOs, Vs, D, warp, lane, qk, dp);
@@ -248,13 +323,18 @@ __global__ void __launch_bounds__(kBW * 32) bwd_main_kernel(const BwdParams p) {
         for (int i = 0; i < kBR; ++i) {
             const int r = warp * kBR + i, q = q0 + r;
             float P = 0.f, dS = 0.f;
-            if (exists && q < p.Q) {
-                const long long row = unit * p.Q + q;
-                const float x = valid ? fmaf(p.scale, qk[i], ld_f(bias, (brow + q) * p.K + key)) : kMaskedLogit;
-                P = weight(x, p.lse[row], 1.f / (float)p.K);
+            if (exists && q < Lq) {
+                const long long row = lrow0 + q;
+                bool valid = key_ok;
+                if constexpr (VARLEN)
+                    valid = bstat == 2 || (bstat == 1 && mod_keep(p.mask_mod, q, key, p.window, prefix));
+                const long long bi = brow0 + (long long)q * bstride + key;
+                const float bv = bias ? ld_f(bias, bi) : 0.f;
+                const float x = valid ? fmaf(p.scale, qk[i], bv) : kMaskedLogit;
+                P = weight(x, p.lse[row], inv_k);
                 if (valid) {
                     dS = P * (dp[i] - p.delta[row]);
-                    if (p.dbias_acc) atomicAdd(p.dbias_acc + (brow + q) * p.K + key, dS);
+                    if (p.dbias_acc) atomicAdd(p.dbias_acc + bi, dS);
                 }
             }
             Ps[r * (kT + 1) + lane] = P;
@@ -303,11 +383,11 @@ __global__ void __launch_bounds__(kBW * 32) bwd_main_kernel(const BwdParams p) {
 #pragma unroll
         for (int ii = 0; ii < kBR; ++ii) {
             const int q = q0 + warp * kBR + ii;
-            if (q >= p.Q) continue;
+            if (q >= Lq) continue;
 #pragma unroll
             for (int c = 0; c < DPL; ++c) {
                 const int d = lane + 32 * c;
-                if (d < D && dq[ii][c] != 0.f) atomicAdd(p.dq_acc + qbase + (long long)q * D + d, p.scale * dq[ii][c]);
+                if (d < D && dq[ii][c] != 0.f) atomicAdd(p.dq_acc + qbase + (long long)q * rs + d, p.scale * dq[ii][c]);
             }
         }
     }
@@ -316,13 +396,13 @@ __global__ void __launch_bounds__(kBW * 32) bwd_main_kernel(const BwdParams p) {
 #pragma unroll
     for (int jj = 0; jj < kBR; ++jj) {
         const int kk = k0 + warp * kBR + jj;
-        if (kk >= p.K) continue;
+        if (kk >= Lk) continue;
 #pragma unroll
         for (int c = 0; c < DPL; ++c) {
             const int d = lane + 32 * c;
             if (d < D) {
-                dkp[kbase + (long long)kk * D + d] = to_t<T>(p.scale * dk[jj][c]);
-                dvp[kbase + (long long)kk * D + d] = to_t<T>(dv[jj][c]);
+                dkp[kbase + (long long)kk * rs + d] = to_t<T>(p.scale * dk[jj][c]);
+                dvp[kbase + (long long)kk * rs + d] = to_t<T>(dv[jj][c]);
             }
         }
     }
@@ -330,8 +410,8 @@ __global__ void __launch_bounds__(kBW * 32) bwd_main_kernel(const BwdParams p) {
 
 template <typename T, typename BT>
 __global__ void bwd_finish_kernel(const BwdParams p) {
-    const long long nq = (long long)p.B * p.N * p.H * p.Q * p.D;
-    const long long nb = p.dbias ? (long long)p.B * p.H * p.Q * p.K : 0;
+    const long long nq = p.dq_elems;
+    const long long nb = p.dbias ? p.dbias_elems : 0;
     T* dq = static_cast<T*>(p.dq);
     BT* db = static_cast<BT*>(p.dbias);
     const long long stride = (long long)gridDim.x * blockDim.x;
@@ -347,15 +427,18 @@ cudaError_t launch_typed(const BwdParams& p, cudaStream_t stream) {
     const size_t sm1 = sizeof(float) * 4 * kT * (size_t)(D + 1);
     const size_t sm2 = sm1 + sizeof(float) * 2 * kT * (kT + 1);
     auto k1 = bwd_delta_kernel<T, BT>;
-    auto k2 = D <= 128 ? bwd_main_kernel<T, BT, 4> : bwd_main_kernel<T, BT, 8>;
+    auto k2 = p.varlen ? (D <= 128 ? bwd_main_kernel<T, BT, 4, true> : bwd_main_kernel<T, BT, 8, true>)
+                       : (D <= 128 ? bwd_main_kernel<T, BT, 4, false> : bwd_main_kernel<T, BT, 8, false>);
     cudaError_t e;
     if ((e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1)) != cudaSuccess) return e;
     if ((e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2)) != cudaSuccess) return e;
-    const long long g1 = units * ((p.Q + kT - 1) / kT), g2 = units * ((p.K + kT - 1) / kT);
+    const long long g1 = units * ((p.Q + kT - 1) / kT);
+    const long long g2 = p.varlen ? (long long)p.num_seqs * p.H * ((p.max_k + kT - 1) / kT)
+                                  : units * ((p.K + kT - 1) / kT);
     if (g1 > 0x7fffffffLL || g2 > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    if (p.varlen && !p.out) return cudaErrorInvalidValue;  // packed sequences: the sums come from O
     if (p.out) {
-        const long long rows = units * p.Q;
-        const long long gd = (rows * 8 + 255) / 256;
+        const long long gd = (p.delta_rows * 8 + 255) / 256;
         if (gd > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
         bwd_delta_out_kernel<T><<<(unsigned)gd, 256, 0, stream>>>(p);
     } else {
@@ -364,7 +447,7 @@ cudaError_t launch_typed(const BwdParams& p, cudaStream_t stream) {
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (p.tc_main) {
         if ((e = launch_tc_bwd_main(p, stream)) != cudaSuccess) return e;
-    } else {
+    } else if (g2 > 0) {
         k2<<<(unsigned)g2, kBW * 32, sm2, stream>>>(p);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
@@ -374,10 +457,14 @@ cudaError_t launch_typed(const BwdParams& p, cudaStream_t stream) {
 
 }  // namespace
 
-size_t bwd_workspace_floats(int B, int N, int H, int Q, int K, int D) {
+size_t bwd_workspace_floats_n(long long dq_elems, long long dbias_elems, long long delta_rows) {
     auto up = [](size_t n) { return (n + 63) & ~(size_t)63; };  // 256-byte pieces
-    const size_t units = (size_t)B * N * H;
-    return up(units * Q * D) + up((size_t)B * H * Q * K) + up(units * Q);
+    return up((size_t)dq_elems) + up((size_t)dbias_elems) + up((size_t)delta_rows);
+}
+
+size_t bwd_workspace_floats(int B, int N, int H, int Q, int K, int D) {
+    const long long units = (long long)B * N * H;
+    return bwd_workspace_floats_n(units * Q * D, (long long)B * H * Q * K, units * Q);
 }
 
 cudaError_t launch_simt_bwd(const BwdParams& p, cudaStream_t stream) {

@@ -443,7 +443,7 @@ uint32_t bwd_idesc(bool bf16, int M, int N, bool a_mn, bool b_mn) {
 }  // namespace tc
 
 bool tc_bwd_supported(const BwdParams& p) {
-    return p.dtype != TA_F32 && (p.D == 16 || p.D == 32 || p.D == 64) && p.K % 8 == 0;
+    return !p.varlen && p.dtype != TA_F32 && (p.D == 16 || p.D == 32 || p.D == 64) && p.K % 8 == 0;
 }
 
 cudaError_t launch_tc_bwd_main(const BwdParams& p, cudaStream_t stream) {

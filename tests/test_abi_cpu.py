@@ -113,6 +113,44 @@ def test_bwd_host_checks(lib, kw, exc):
         _bwd(**kw)()
 
 
+def _vbwd(**kw):
+    ws = abi.tri_attn_varlen_bwd_workspace_size(100, 2, 64, 64, 64, False)
+    args = dict(q=A, k=A, v=A, dtype=abi.TA_BF16, cu_seqlens_q=A, cu_seqlens_k=A, num_seqs=2, total_q=100,
+                total_k=100, max_seqlen_q=64, max_seqlen_k=64, H=2, D=64, scale=0.125, kv_num_blocks=0,
+                kv_indices=0, full_kv_num_blocks=0, full_kv_indices=0, mask_heads=1, max_q_blocks=1,
+                max_kv_blocks=1, block_q=128, block_k=128, mask_mod=abi.TA_MASK_CAUSAL, window=0,
+                prefix_lengths=0, prefix_length=0, bias=0, bias_dtype=abi.TA_F32, lse=A, out=A, d_out=A, dq=A,
+                dk=A, dv=A, dbias=0, workspace=A, workspace_bytes=ws, stream=0)
+    args.update(kw)
+    return lambda: abi.tri_attn_varlen_bwd(**args)
+
+
+def test_varlen_bwd_workspace_size(lib):
+    up = lambda n: (n + 63) // 64 * 64
+    assert abi.tri_attn_varlen_bwd_workspace_size(100, 2, 64, 64, 80, False) == 4 * (up(200 * 64) + up(200))
+    assert abi.tri_attn_varlen_bwd_workspace_size(100, 2, 64, 64, 80, True) == 4 * (up(200 * 64) + up(2 * 64 * 80) +
+                                                                                  up(200))
+
+
+@pytest.mark.parametrize("kw,exc", [
+    (dict(out=0), ValueError),           # the forward's O is required for the packed form
+    (dict(lse=0), ValueError),
+    (dict(dbias=A), ValueError),         # dBias without a bias
+    (dict(workspace_bytes=64), ValueError),
+    (dict(workspace=A + 64), ValueError),
+    (dict(dq=MIS), ValueError),
+    (dict(mask_mod=9), ValueError),
+    (dict(mask_mod=abi.TA_MASK_SLIDING_WINDOW, window=0), ValueError),
+    (dict(kv_num_blocks=A), ValueError),  # lists come in pairs
+    (dict(block_q=64), NotImplementedError),
+    (dict(D=264), NotImplementedError),
+    (dict(bias=A, bias_dtype=abi.TA_F16), NotImplementedError),
+])
+def test_varlen_bwd_host_checks(lib, kw, exc):
+    with pytest.raises(exc):
+        _vbwd(**kw)()
+
+
 def _fwd_strided(**kw):
     args = dict(q=A, k=A, v=A, qkv_dtype=abi.TA_BF16, bias=A, bias_dtype=abi.TA_BF16, mask=0, kv_lengths=0, B=1, N=2,
                 H=2, Q=64, K=64, D=64, scale=0.125, q_strides=None, k_strides=None, v_strides=None, out=A, lse=0,

@@ -122,3 +122,90 @@ def test_backward_page_example_shape():
     """The page's Example shapes at a smaller sequence length: fp16, bias and mask from kv_lengths."""
     c = synth.make_triangle("bwd_page", 1, 4, 2, 64, 64, 32, "f16", "f16", seed=760, mask="kvlen", kv_range=(48, 64))
     _check(c, 761)
+
+
+# ---------------------------------------------------------------------------
+# Packed sequences (tri_attn_varlen_bwd), against oracle.backward.varlen_bwd
+# ---------------------------------------------------------------------------
+
+def _check_varlen(case, seed, window=0, prefix=None, bias=None):
+    import masked_attention_tri_gb300 as ta
+    bm = None
+    if case.kv_num_blocks is not None:
+        bm = ta.BlockMask.from_kv_blocks(to_gpu(case.kv_num_blocks), to_gpu(case.kv_indices),
+                                         to_gpu(case.full_kv_num_blocks), to_gpu(case.full_kv_indices),
+                                         BLOCK_SIZE=case.block, mask_mod=case.mask_mod)
+    mm = case.mask_mod if bm is None else None
+    pl = None if prefix is None else torch.tensor(prefix, dtype=torch.int32, device="cuda")
+    q, k, v = case.q.cuda(), case.k.cuda(), case.v.cuda()
+    cu, cuk = case.cu_seqlens.cuda(), case.cu_seqlens_k.cuda()
+    bg = None if bias is None else bias.cuda()
+    o, lse, _ = ta.varlen_attention(q, k, v, cu, cuk, case.max_seqlen, case.max_seqlen_k, block_mask=bm,
+                                    scale=case.scale, return_aux=True, mask_mod=mm, window=window,
+                                    prefix_lengths=pl, bias=bg)
+    g = torch.Generator().manual_seed(seed)
+    d_out = torch.randn(tuple(case.q.shape), generator=g).to(case.q.dtype)
+    grads = ta.varlen_attention_backward(q, k, v, cu, cuk, case.max_seqlen, case.max_seqlen_k, o, lse,
+                                         d_out.cuda(), block_mask=bm, scale=case.scale, mask_mod=mm,
+                                         window=window, prefix_lengths=pl, bias=bg)
+    torch.cuda.synchronize()
+    assert ta.get_status() == 0
+    ref = obwd.varlen_bwd(case.q, case.k, case.v, case.cu_seqlens, case.cu_seqlens_k, d_out, scale=case.scale,
+                          kv_num_blocks=case.kv_num_blocks, kv_indices=case.kv_indices,
+                          full_kv_num_blocks=case.full_kv_num_blocks, full_kv_indices=case.full_kv_indices,
+                          block=case.block, mask_mod=case.mask_mod, window=window,
+                          prefix_lengths=prefix, bias=bias)
+    for nm, gr, r in zip(("dq", "dk", "dv", "dbias"), grads, ref):
+        if r is None:
+            assert gr is None
+            continue
+        _close(f"{case.name}:{nm}", case.dtype, gr, r)
+
+
+@pytest.mark.parametrize("dtype,D,lists", [("bf16", 64, "causal"), ("f16", 32, "none"), ("f32", 16, "causal")])
+def test_varlen_backward_matches_oracle(dtype, D, lists):
+    c = synth.make_varlen(f"vbwd_{dtype}_{D}_{lists}", 4, 0, 0, 2, D, dtype, seed=770 + D, lengths=[300, 129, 64, 1],
+                          block_lists=lists, mask_mod="causal")
+    _check_varlen(c, 771 + D)
+
+
+def test_varlen_backward_random_lists_and_unlisted_blocks():
+    """Random full / partial lists, a q block with no listed block (its rows all masked), D = 128."""
+    c = synth.make_varlen("vbwd_rand", 2, 0, 0, 2, 128, "bf16", seed=785, lengths=[400, 260])
+    g = np.random.default_rng(3)
+    S, MQ = 2, 4
+    kn = torch.zeros(S, 1, MQ, dtype=torch.int32)
+    ki = torch.full((S, 1, MQ, MQ), 77, dtype=torch.int32)
+    fn = torch.zeros(S, 1, MQ, dtype=torch.int32)
+    fi = torch.full((S, 1, MQ, MQ), 77, dtype=torch.int32)
+    for s_, L in enumerate([400, 260]):
+        nb = (L + 127) // 128
+        for qb in range(nb):
+            if qb == 1:
+                continue
+            perm = g.permutation(nb).tolist()
+            nf = int(g.integers(0, nb + 1))
+            fn[s_, 0, qb] = nf
+            fi[s_, 0, qb, :nf] = torch.tensor(perm[:nf], dtype=torch.int32)
+            kn[s_, 0, qb] = nb - nf
+            ki[s_, 0, qb, :nb - nf] = torch.tensor(perm[nf:], dtype=torch.int32)
+    c.kv_num_blocks, c.kv_indices, c.full_kv_num_blocks, c.full_kv_indices = kn, ki, fn, fi
+    _check_varlen(c, 786)
+
+
+def test_varlen_backward_lq_ne_lk_window_and_bias():
+    c = synth.make_varlen("vbwd_lqlk", 3, 0, 0, 2, 64, "bf16", seed=780, lengths=[200, 70, 129],
+                          lengths_k=[90, 300, 129], block_lists="none", mask_mod="sliding_window")
+    c.max_seqlen, c.max_seqlen_k = 208, 304
+    g = torch.Generator().manual_seed(781)
+    bias = torch.randn(2, 208, 304, generator=g).to(torch.bfloat16)
+    _check_varlen(c, 782, window=40, bias=bias)
+
+
+def test_varlen_backward_prefix_lm_fp32_bias():
+    c = synth.make_varlen("vbwd_prefix", 3, 0, 0, 1, 32, "f16", seed=790, lengths=[150, 40, 260],
+                          block_lists="none", mask_mod="prefix_lm")
+    c.max_seqlen = c.max_seqlen_k = 264
+    g = torch.Generator().manual_seed(791)
+    bias = torch.randn(1, 264, 264, generator=g)
+    _check_varlen(c, 792, prefix=[20, 0, 300], bias=bias)
