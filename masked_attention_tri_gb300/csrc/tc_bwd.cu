@@ -83,6 +83,13 @@ __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* tm, uint32_
                  : "memory");
 }
 
+// fp32 add into global memory with no result.  The global state space is explicit: a generic
+// atomic could address shared memory, and the compiler would then keep every later shared
+// load of the bias tile behind it.
+__device__ __forceinline__ void red_add_global(float* p, float v) {
+    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v));
+}
+
 __device__ __forceinline__ float bwd_weight(float x, float lse, float inv_k) {
     // A row with every key masked has lse -1e9 in fp32 (its -1e9 + ln K rounds
     // there); its weights are 1 / K.  Any row with a valid key has lse above -1e9 + 100.
@@ -115,6 +122,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
     const int h = (int)(unit % P.H);
     const long long bn = unit / P.H;
     const int b = (int)(bn / P.N);
+
+    if (P.kv_len) {
+        // A key tile wholly past a kv_length of at least 1: its keys have weight 0 in every
+        // row (each row has a valid key), so dK = dV = 0 there and nothing reaches dQ or
+        // dBias.  (With kv_length 0 every key has weight 1 / K and the tile is computed.)
+        int Lk = P.kv_len[bn];
+        Lk = Lk < 0 ? 0 : (Lk > P.K ? P.K : Lk);
+        if (Lk > 0 && k0 >= Lk) {
+            const int rows = P.K - k0 < kBN ? P.K - k0 : kBN;
+            const long long n16 = (long long)rows * P.D / 8;  // 16-byte pieces of each tensor
+            const long long off = (unit * P.K + k0) * (long long)P.D;
+            uint4* dkz = reinterpret_cast<uint4*>(static_cast<uint16_t*>(P.dk) + off);
+            uint4* dvz = reinterpret_cast<uint4*>(static_cast<uint16_t*>(P.dv) + off);
+            for (long long i = threadIdx.x; i < n16; i += blockDim.x) {
+                dkz[i] = make_uint4(0u, 0u, 0u, 0u);
+                dvz[i] = make_uint4(0u, 0u, 0u, 0u);
+            }
+            return;
+        }
+    }
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
@@ -204,19 +231,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
             if (!ok) break;
             tc_fence_after();
             if (leader) {
-#pragma unroll 1
-                for (int kk = 0; kk < P.ksteps; ++kk)  // S^T = K Q^T
-                    mma_ss(tS, kK + 2u * (uint32_t)kk, qK + 2u * (uint32_t)kk, P.idesc_s, kk > 0 ? 1u : 0u);
-#pragma unroll 1
-                for (int kk = 0; kk < P.ksteps; ++kk)  // dP^T = V dO^T
-                    mma_ss(tDP, vK + 2u * (uint32_t)kk, doK + 2u * (uint32_t)kk, P.idesc_s, kk > 0 ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)  // S^T = K Q^T (D / 16 <= 4 k steps)
+                    if (kk < P.ksteps)
+                        mma_ss(tS, kK + 2u * (uint32_t)kk, qK + 2u * (uint32_t)kk, P.idesc_s, kk > 0 ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)  // dP^T = V dO^T
+                    if (kk < P.ksteps)
+                        mma_ss(tDP, vK + 2u * (uint32_t)kk, doK + 2u * (uint32_t)kk, P.idesc_s, kk > 0 ? 1u : 0u);
                 mma_commit(s_full);
             }
             ok = __all_sync(0xffffffffu, wait_bar(p_full, ph, abort_flag, P.status));
             if (!ok) break;
             tc_fence_after();
             if (leader) {
-#pragma unroll 1
+#pragma unroll
                 for (int kk = 0; kk < kBM / 16; ++kk) {  // 16 queries per k step
                     const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
                     mma_ts(tDV, tP + 8u * (uint32_t)kk, doM + 128u * (uint32_t)kk, P.idesc_g, acc);
@@ -229,7 +258,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
                 tc_fence_after();
             }
             if (leader) {
-#pragma unroll 1
+#pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk)  // dQ_j = dS K, 16 keys per k step
                     mma_ss(tDQ, dsM + 128u * (uint32_t)kk, kM + 128u * (uint32_t)kk, P.idesc_q, kk > 0 ? 1u : 0u);
                 mma_commit(dq_full);
@@ -293,30 +322,65 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
                 if (!ok) break;
             }
             tc_fence_after();
+            // Chunks of 16 queries (few live registers, so the compiler can overlap the
+            // chunk's independent elements): warp half hq takes chunks 4 hq .. 4 hq + 3.
+            constexpr int CW = 16;
 #pragma unroll 1
-            for (int c = 2 * hq; c < 2 * hq + 2; ++c) {  // 32 queries per chunk
-                uint32_t sr[32], dr[32];
-                tmem_ld_x32(tS + lane_off + 32u * (uint32_t)c, sr);
-                tmem_ld_x32(tDP + lane_off + 32u * (uint32_t)c, dr);
+            for (int c = 4 * hq; c < 4 * hq + 4; ++c) {
+                uint32_t sr[CW], dr[CW];
+                tmem_ld_x16(tS + lane_off + (uint32_t)(CW * c), sr);
+                tmem_ld_x16(tDP + lane_off + (uint32_t)(CW * c), dr);
                 // The chunk's lse and delta (shared-memory broadcasts, four at a time) and this
-                // key's bias column: query row ql = 32c + i lives at bcb + 128 i + xo[i % 8].
-                float ls[32], dl[32];
+                // key's bias column: query row ql = CW c + i lives at bcb + 128 i + xo[i % 8].
+                float ls[CW], dl[CW];
 #pragma unroll
-                for (int i = 0; i < 32; i += 4) {
-                    const float4 l4 = *reinterpret_cast<const float4*>(lse_s + 32 * c + i);
-                    const float4 d4 = *reinterpret_cast<const float4*>(del_s + 32 * c + i);
+                for (int i = 0; i < CW; i += 4) {
+                    const float4 l4 = *reinterpret_cast<const float4*>(lse_s + CW * c + i);
+                    const float4 d4 = *reinterpret_cast<const float4*>(del_s + CW * c + i);
                     ls[i] = l4.x, ls[i + 1] = l4.y, ls[i + 2] = l4.z, ls[i + 3] = l4.w;
                     dl[i] = d4.x, dl[i + 1] = d4.y, dl[i + 2] = d4.z, dl[i + 3] = d4.w;
                 }
-                const uint8_t* bcb = gbase + (bbox - base) + (uint32_t)(32 * c) * 128u;
-                const int nq = P.Q - (q0 + 32 * c);  // queries of the chunk that exist
-                uint32_t pp[16], dd[16];
+                const uint8_t* bcb = gbase + (bbox - base) + (uint32_t)(CW * c) * 128u;
+                const int nq = P.Q - (q0 + CW * c);  // queries of the chunk that exist
+                uint32_t pp[CW / 2], dd[CW / 2];
+                if (__all_sync(0xffffffffu, valid) && nq >= CW) {
+                    // Every key of the warp valid and every query of the chunk present: each row
+                    // has a valid key, so its lse is a plain log-sum-exp and P = 2^(x log2e - lse log2e).
+                    const float2 sl2 = make_float2(P.scale * kLog2e, P.scale * kLog2e);
+                    const float2 l2e2 = make_float2(kLog2e, kLog2e);
+                    float* dbp = dbias_row ? dbias_row + (long long)(q0 + CW * c) * P.K : nullptr;
 #pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    float pv[2], sv[2];
+                    for (int i = 0; i < CW; i += 2) {
+                        float2 bv;
+                        if constexpr (BIAS_F32) {
+                            bv = make_float2(*reinterpret_cast<const float*>(bcb + i * 128 + xo[i & 7]),
+                                             *reinterpret_cast<const float*>(bcb + (i + 1) * 128 + xo[(i + 1) & 7]));
+                        } else {
+                            const uint32_t b0 = *reinterpret_cast<const unsigned short*>(bcb + i * 128 + xo[i & 7]);
+                            const uint32_t b1 =
+                                *reinterpret_cast<const unsigned short*>(bcb + (i + 1) * 128 + xo[(i + 1) & 7]);
+                            bv = unpack2<BF16>(b0 | (b1 << 16));
+                        }
+                        // y = s S log2e + b log2e - lse log2e
+                        const float2 nl = __fmul2_rn(make_float2(ls[i], ls[i + 1]), make_float2(-kLog2e, -kLog2e));
+                        const float2 y = __ffma2_rn(
+                            make_float2(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1])), sl2,
+                            __ffma2_rn(bv, l2e2, nl));
+                        const float2 pr = make_float2(ex2(y.x), ex2(y.y));
+                        const float2 ds = __fmul2_rn(
+                            pr, __fadd2_rn(make_float2(__uint_as_float(dr[i]), __uint_as_float(dr[i + 1])),
+                                           make_float2(-dl[i], -dl[i + 1])));
+                        pp[i / 2] = pack2<BF16>(pr.x, pr.y);
+                        dd[i / 2] = pack2<BF16>(ds.x, ds.y);
+                        if (dbp) {
+                            red_add_global(dbp + (long long)i * P.K, ds.x);
+                            red_add_global(dbp + (long long)(i + 1) * P.K, ds.y);
+                        }
+                    }
+                } else {
+                    // Logits first (every read of the bias tile before any reduction into dBias).
 #pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int ii = i + u;
+                    for (int ii = 0; ii < CW; ++ii) {
                         float x = kMasked;
                         if (valid) {
                             const uint8_t* ba = bcb + ii * 128 + xo[ii & 7];
@@ -325,24 +389,41 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
                             else bv = unpack2<BF16>((uint32_t)*reinterpret_cast<const unsigned short*>(ba)).x;
                             x = fmaf(P.scale, __uint_as_float(sr[ii]), bv);
                         }
-                        const bool live = exists && ii < nq;
-                        const float p = live ? bwd_weight(x, ls[ii], inv_k) : 0.f;
-                        const float ds = (live && valid) ? p * (__uint_as_float(dr[ii]) - dl[ii]) : 0.f;
-                        if (dbias_row && ds != 0.f) atomicAdd(dbias_row + (long long)(q0 + 32 * c + ii) * P.K, ds);
-                        pv[u] = p;
-                        sv[u] = ds;
+                        sr[ii] = __float_as_uint(x);
                     }
-                    pp[i / 2] = pack2<BF16>(pv[0], pv[1]);
-                    dd[i / 2] = pack2<BF16>(sv[0], sv[1]);
-                }
-                // P^T and dS^T as 16-bit query pairs into columns [16c, 16c + 16) (read already)
-                tmem_st_x16(tP + lane_off + 16u * (uint32_t)c, pp);
-                tmem_st_x16(tDS + lane_off + 16u * (uint32_t)c, dd);
-                // dS as [key][query] in shared memory: box c / 2, 16-byte chunks of 8 queries
-                const uint32_t drow = base + L.ds + (uint32_t)(c >> 1) * kBox + (uint32_t)kr * 128u;
+                    // P and dS (dS kept in dr for the dBias reduction).
 #pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    const uint32_t ch = (uint32_t)(4 * (c & 1) + g);
+                    for (int i = 0; i < CW; i += 2) {
+                        float pv[2], sv[2];
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const int ii = i + u;
+                            const bool live = exists && ii < nq;
+                            const float p = live ? bwd_weight(__uint_as_float(sr[ii]), ls[ii], inv_k) : 0.f;
+                            const float ds = (live && valid) ? p * (__uint_as_float(dr[ii]) - dl[ii]) : 0.f;
+                            pv[u] = p;
+                            sv[u] = ds;
+                            dr[ii] = __float_as_uint(ds);
+                        }
+                        pp[i / 2] = pack2<BF16>(pv[0], pv[1]);
+                        dd[i / 2] = pack2<BF16>(sv[0], sv[1]);
+                    }
+                    if (dbias_row) {
+#pragma unroll
+                        for (int ii = 0; ii < CW; ++ii)
+                            if (__uint_as_float(dr[ii]) != 0.f)
+                                red_add_global(dbias_row + (long long)(q0 + CW * c + ii) * P.K,
+                                               __uint_as_float(dr[ii]));
+                    }
+                }
+                // P^T and dS^T as 16-bit query pairs into columns [8c, 8c + 8) (read already)
+                tmem_st_x8(tP + lane_off + (uint32_t)(CW / 2 * c), pp);
+                tmem_st_x8(tDS + lane_off + (uint32_t)(CW / 2 * c), dd);
+                // dS as [key][query] in shared memory: box (CW c) / 64, 16-byte chunks of 8 queries
+                const uint32_t drow = base + L.ds + (uint32_t)((CW * c) / 64) * kBox + (uint32_t)kr * 128u;
+#pragma unroll
+                for (int g = 0; g < CW / 8; ++g) {
+                    const uint32_t ch = (uint32_t)(((CW * c) % 64) / 8 + g);
                     st_shared_v4(drow + ((ch ^ rsw) << 4), dd[4 * g], dd[4 * g + 1], dd[4 * g + 2], dd[4 * g + 3]);
                 }
             }

@@ -111,6 +111,20 @@ def test_backward_several_tiles():
     _check(c, 747, with_out=True)
 
 
+@pytest.mark.parametrize("dtype,D", [("bf16", 32), ("f16", 64)])
+def test_backward_padded_key_tiles(dtype, D):
+    """kv_lengths that leave whole 128-key tiles past the valid prefix (their dK / dV are zero and
+    they add nothing to dQ or dBias), next to 0 (every key weighted 1 / K), 1, tile edges, K and
+    beyond K, and a negative value."""
+    K = 264
+    lens = [0, 1, 127, 128, 129, 256, 264, 300, -3]
+    c = synth.make_triangle(f"bwd_pad_{dtype}_{D}", 1, len(lens), 2, 140, K, D, dtype, "f32", seed=760 + D,
+                            mask="kvlen", kv_range=(0, K))
+    c.kv_lengths.view(-1)[:] = torch.tensor(lens, dtype=torch.int32)
+    _check(c, 761 + D)
+    _check(c, 762 + D, with_out=True)
+
+
 def test_autograd_wrapper():
     """torch autograd through triangle_attention_autograd gives the same gradients (it passes the
     forward's O, so the per-row sums come from dO . O)."""
