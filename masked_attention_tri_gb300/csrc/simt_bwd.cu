@@ -408,16 +408,44 @@ __global__ void __launch_bounds__(kBW * 32) bwd_main_kernel(const BwdParams p) {
     }
 }
 
+__device__ __forceinline__ uint32_t pack_pair(__half, float a, float b) {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t pack_pair(__nv_bfloat16, float a, float b) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// dst[e] = src[e] in T, e < n, grid-stride.  16-bit outputs with 16-byte aligned
+// buffers: eight elements per step (two 16-byte loads, one 16-byte store).
+template <typename T>
+__device__ __forceinline__ void convert_range(const float* src, void* dstv, long long n, long long tid,
+                                              long long stride) {
+    T* dst = static_cast<T*>(dstv);
+    long long done = 0;
+    if constexpr (sizeof(T) == 2) {
+        if (((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src)) & 15u) == 0) {
+            const long long n8 = n / 8;
+            const float4* s4 = reinterpret_cast<const float4*>(src);
+            uint4* d8 = reinterpret_cast<uint4*>(dst);
+            for (long long i = tid; i < n8; i += stride) {
+                const float4 a = s4[2 * i], b = s4[2 * i + 1];
+                d8[i] = make_uint4(pack_pair(T(), a.x, a.y), pack_pair(T(), a.z, a.w), pack_pair(T(), b.x, b.y),
+                                   pack_pair(T(), b.z, b.w));
+            }
+            done = n8 * 8;
+        }
+    }
+    for (long long e = done + tid; e < n; e += stride) dst[e] = to_t<T>(src[e]);
+}
+
 template <typename T, typename BT>
 __global__ void bwd_finish_kernel(const BwdParams p) {
-    const long long nq = p.dq_elems;
-    const long long nb = p.dbias ? p.dbias_elems : 0;
-    T* dq = static_cast<T*>(p.dq);
-    BT* db = static_cast<BT*>(p.dbias);
     const long long stride = (long long)gridDim.x * blockDim.x;
-    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < nq; e += stride) dq[e] = to_t<T>(p.dq_acc[e]);
-    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < nb; e += stride)
-        db[e] = to_t<BT>(p.dbias_acc[e]);
+    const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    convert_range<T>(p.dq_acc, p.dq, p.dq_elems, tid, stride);
+    if (p.dbias) convert_range<BT>(p.dbias_acc, p.dbias, p.dbias_elems, tid, stride);
 }
 
 template <typename T, typename BT>
