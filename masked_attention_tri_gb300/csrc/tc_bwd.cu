@@ -57,8 +57,9 @@ struct BwdTc {
 struct BwdLayout {
     uint32_t k, v, q, ds, bias, dqst, lse, bars, tmem_slot, abort_flag, total;
 };
-// kv_full, q_full[2], q_empty[2], bias_full, bias_empty, s_full, p_full, dq_full, dq_empty, fin, drain
-constexpr int kBwdBars = 13;
+// kv_full, q_full[2], q_empty[2], bias_full, bias_empty, s_full, p_full, dq_full, dq_empty, fin, drain,
+// lse_full[2]
+constexpr int kBwdBars = 15;
 __host__ __device__ inline BwdLayout bwd_layout(const BwdTc& P) {
     BwdLayout L;
     L.k = 0;
@@ -114,6 +115,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
     auto q_empty = [&](int st) { return bar(3 + st); };
     const uint32_t bias_full = bar(5), bias_empty = bar(6), s_full = bar(7), p_full = bar(8);
     const uint32_t dq_full = bar(9), dq_empty = bar(10), fin = bar(11), drain = bar(12);
+    auto lse_full = [&](int st) { return bar(13 + st); };
     auto q_smem = [&](int st) { return base + L.q + (uint32_t)st * 2u * kBox; };
     auto do_smem = [&](int st) { return base + L.q + (uint32_t)st * 2u * kBox + kBox; };
 
@@ -147,7 +149,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
         *abort_flag = 0;
         mbar_init(kv_full, 1);
         for (int st = 0; st < 2; ++st) {
-            mbar_init(q_full(st), 2);  // expect_tx arrival + the lse / delta rows
+            mbar_init(q_full(st), 1);    // the expect_tx arrival of Q and dO
+            mbar_init(lse_full(st), 1);  // the lse / delta rows written
             mbar_init(q_empty(st), 1);
         }
         mbar_init(bias_full, 1);
@@ -195,16 +198,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
                 tma_load_3d(q_smem(st), &P.tm_q, 0, q0, (int)unit, q_full(st));
                 tma_load_3d(do_smem(st), &P.tm_do, 0, q0, (int)unit, q_full(st));
             }
-            float* lse_s = reinterpret_cast<float*>(gbase + L.lse + (uint32_t)st * 1024u);
-            float* del_s = lse_s + 128;
-            for (int i = lane; i < kBM; i += 32) {
-                const int q = q0 + i;
-                lse_s[i] = q < P.Q ? P.lse[unit * P.Q + q] : 0.f;
-                del_s[i] = q < P.Q ? P.delta[unit * P.Q + q] : 0.f;
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(q_full(st));  // release: the rows are written
-            if (j > 0) {  // the compute warps have read the previous tile's bias
+            // The bias tile (single-buffered) as soon as the compute warps have read the previous one,
+            // then the rows' lse / delta (only the compute warps wait for them).
+            if (j > 0) {
                 ok = __all_sync(0xffffffffu, wait_bar(bias_empty, (uint32_t)(j - 1) & 1u, abort_flag, P.status));
                 if (!ok) break;
             }
@@ -214,6 +210,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
                     tma_load_3d(base + L.bias + (uint32_t)bx * kBox, &P.tm_bias, k0 + bx * P.bias_box_cols, q0,
                                 b * P.H + h, bias_full);
             }
+            float* lse_s = reinterpret_cast<float*>(gbase + L.lse + (uint32_t)st * 1024u);
+            float* del_s = lse_s + 128;
+            float lv[kBM / 32], dv[kBM / 32];  // every load in flight before the first store
+#pragma unroll
+            for (int t = 0; t < kBM / 32; ++t) {
+                const int q = q0 + lane + 32 * t;
+                lv[t] = q < P.Q ? P.lse[unit * P.Q + q] : 0.f;
+                dv[t] = q < P.Q ? P.delta[unit * P.Q + q] : 0.f;
+            }
+#pragma unroll
+            for (int t = 0; t < kBM / 32; ++t) {
+                lse_s[lane + 32 * t] = lv[t];
+                del_s[lane + 32 * t] = dv[t];
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(lse_full(st));  // release: the rows are written
         }
         if (!ok) *abort_flag = 1;
     } else if (warp == 9) {
@@ -311,7 +323,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
             const int q0 = j * kBM, st = j % P.qs;
             const float* lse_s = reinterpret_cast<const float*>(gbase + L.lse + (uint32_t)st * 1024u);
             const float* del_s = lse_s + 128;
-            ok = __all_sync(0xffffffffu, wait_bar(q_full(st), (uint32_t)(j / P.qs) & 1u, abort_flag, P.status));
+            ok = __all_sync(0xffffffffu, wait_bar(lse_full(st), (uint32_t)(j / P.qs) & 1u, abort_flag, P.status));
             if (!ok) break;
             ok = __all_sync(0xffffffffu, wait_bar(bias_full, ph, abort_flag, P.status));
             if (!ok) break;
