@@ -20,8 +20,9 @@
 // two query halves of the tile) turn S^T and dP^T into P^T and dS^T (16-bit
 // pairs into their own TMEM columns, dS also into shared memory as the A
 // operand of dQ) and add dS to the fp32 dBias accumulator (coalesced over
-// keys); warps 0-3 then read dQ_j (one thread per query row) and add it to the
-// fp32 dQ accumulator with a TMA reduce-add, and at the end write dK and dV.
+// keys); then each reads its 32 columns of dQ_j (one thread per query row) and
+// adds them to the fp32 dQ accumulator with a TMA reduce-add; warps 0-3 write dK
+// and dV at the end.
 // Warp 8 loads K and V once and Q, dO, the bias tile and the rows' lse / delta
 // per query tile; warp 9 issues the MMAs.  Every wait is bounded (TA_ERR_TIMEOUT).
 
@@ -67,7 +68,7 @@ __host__ __device__ inline BwdLayout bwd_layout(const BwdTc& P) {
     L.q = L.v + kBox;
     L.ds = L.q + (uint32_t)P.qs * 2 * kBox;  // dS as [key][query]: two 64-query boxes
     L.bias = L.ds + 2 * kBox;
-    L.dqst = L.bias + P.bias_bytes;          // dQ staging: 4 warps x 32 rows x D fp32
+    L.dqst = L.bias + P.bias_bytes;          // dQ staging: 4 lane quarters x 32 rows x D fp32
     L.lse = L.dqst + 4u * 32u * (uint32_t)P.D * 4u;
     L.bars = L.lse + (uint32_t)P.qs * 1024u;
     L.tmem_slot = L.bars + 8 * kBwdBars;
@@ -158,7 +159,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
         mbar_init(s_full, 1);
         mbar_init(p_full, 8);
         mbar_init(dq_full, 1);
-        mbar_init(dq_empty, 4);
+        mbar_init(dq_empty, P.D > 32 ? 8 : 4);  // the warps that read dQ_j
         mbar_init(fin, 1);
         mbar_init(drain, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -329,10 +330,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
             if (!ok) break;
             ok = __all_sync(0xffffffffu, wait_bar(s_full, ph, abort_flag, P.status));
             if (!ok) break;
-            if (hq == 1 && j > 0) {  // warps 0-3 have read dQ of the previous tile out of the dS^T columns
-                ok = __all_sync(0xffffffffu, wait_bar(dq_empty, ph ^ 1u, abort_flag, P.status));
-                if (!ok) break;
-            }
+            // (dS^T of this warp's chunks goes to dQ_j's columns [32 hq, 32 hq + 32), which this
+            // warp itself read out of the previous tile's dQ_j.)
             tc_fence_after();
             // Chunks of 16 queries (few live registers, so the compiler can overlap the
             // chunk's independent elements): warp half hq takes chunks 4 hq .. 4 hq + 3.
@@ -446,17 +445,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full);
-            if (hq == 1) continue;
-
-            // dQ_j (warps 0-3): thread = query row q0 + 32 wq + lane, D fp32 columns, added into the
-            // accumulator.
+            // dQ_j: thread = query row q0 + 32 wq + lane; warp half hq reads columns [32 hq, 32 hq + 32)
+            // (D <= 32: warps 4-7 have none) and adds them into the accumulator.
+            const int dc0 = 32 * hq, dc1 = P.D < dc0 + 32 ? P.D : dc0 + 32;
+            if (dc0 >= P.D) continue;
             ok = __all_sync(0xffffffffu, wait_bar(dq_full, ph, abort_flag, P.status));
             if (!ok) break;
             tc_fence_after();
             if (lane == 0) bulk_wait_read_all();  // the previous reduce has read the staging rows
             __syncwarp();
 #pragma unroll 1
-            for (int d0 = 0; d0 < P.D; d0 += 16) {
+            for (int d0 = dc0; d0 < dc1; d0 += 16) {
                 uint32_t o[16];
                 tmem_ld_x16(tDQ + lane_off + (uint32_t)d0, o);
                 const int bxi = d0 / inner, cb = (d0 % inner) / 4;  // box, first 16-byte chunk in it
@@ -475,7 +474,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
             if (lane == 0) {
                 mbar_arrive(dq_empty);
                 if (q0 + 32 * wq < P.Q) {
-                    for (int bxi = 0; bxi * inner < P.D; ++bxi)
+                    for (int bxi = dc0 / inner; bxi * inner < dc1; ++bxi)
                         tma_reduce_add_3d(&P.tm_dq, dq_stage + (uint32_t)bxi * 32u * rowb, bxi * inner, q0 + 32 * wq,
                                           (int)unit);
                     bulk_commit();
