@@ -1171,6 +1171,18 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
             ++qi;
             const uint32_t o_taddr = o_base + ob * o_set;
             float m_true = -INFINITY, m_ref = 0.f, l = 0.f;
+            // O *= alpha in this warp's columns, once PV of the previous tile is in O.
+            auto rescale_o = [&](float alpha) -> bool {
+                if (!wait_pv(sn - 1u, false)) return false;
+                for (uint32_t c0 = 0; c0 < (kSplitO ? P.o_cols : half_o); c0 += 8) {
+                    uint32_t o[8];
+                    tmem_ld_x8(o_taddr + c0, o);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    tmem_st_x8(o_taddr + c0, o);
+                }
+                return true;
+            };
             int jv = 0;
             const int prefix_lm = !VARLEN ? 0 : (a.prefix_len ? a.prefix_len[it.seq] : a.prefix_all);
             TileWalk tw = tiles_begin<VARLEN>(it);
@@ -1310,6 +1322,13 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
                 if constexpr (FOLD) tm_nat = tm > -FLT_MAX ? tm * a.scale : (tm == -FLT_MAX ? kMasked : -INFINITY);
                 else tm_nat = tm;
                 m_true = fmaxf(m_true, tm_nat);
+                // A new reference max (rows whose max grew by more than 2^8): l and O are
+                // scaled by alpha.  Both warps of the lane quarter take this branch for the
+                // same rows (same tile max, same reference); each scales its O columns once O
+                // holds the previous tile.  Packed form: O after this tile's P is in tensor
+                // memory (the logits are no longer live there, which spares registers).
+                float alpha = 1.f;
+                bool rescale = false;
                 if (jv == 0) {
                     m_ref = tm;
                     l = 0.f;
@@ -1317,20 +1336,13 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
                     const float m_new = fmaxf(m_ref, tm);
                     const bool need = (m_new - m_ref) * unit_l2e > kRescaleLog2;
                     if (__any_sync(0xffffffffu, need)) {
-                        // Both warps of the lane quarter take this branch for the same
-                        // rows (same tm, same m_ref); each scales its O columns once
-                        // O holds the previous tile.
-                        ok = wait_pv(sn - 1u, false);
-                        if (!ok) break;
-                        const float alpha = ex2((m_ref - m_new) * unit_l2e);
+                        rescale = true;
+                        alpha = ex2((m_ref - m_new) * unit_l2e);
                         l *= alpha;
                         m_ref = m_new;
-                        for (uint32_t c0 = 0; c0 < (kSplitO ? P.o_cols : half_o); c0 += 8) {
-                            uint32_t o[8];
-                            tmem_ld_x8(o_taddr + c0, o);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                            tmem_st_x8(o_taddr + c0, o);
+                        if constexpr (!VARLEN) {
+                            ok = rescale_o(alpha);
+                            if (!ok) break;
                         }
                     }
                 }
@@ -1357,6 +1369,10 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
                 // Shared O: P of both halves in columns [0, 64), after the exchange.
                 tmem_st_x32(s_taddr + (kSplitO ? 64u : 32u) * (uint32_t)h, pk);
                 l += (acc0.x + acc0.y) + (acc1.x + acc1.y);
+                if (VARLEN && rescale) {  // (this tile's P is not given yet)
+                    ok = rescale_o(alpha);
+                    if (!ok) break;
+                }
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
