@@ -114,17 +114,19 @@ bool choose_geometry(TcParams& P, bool varlen, int& NQ) {
 }
 
 // The key-split kernel (triangle form with D <= 64, packed form with D <=
-// 128): one query tile per item; three S buffers, and two O accumulators of
-// up to 64 columns or one of 128, in 512 tensor-memory columns; Q buffers,
-// K/V stages and bias stages as shared memory allows.
+// 128): one query tile per item; S buffers (three for the triangle form, two
+// for the packed form) and two O accumulator sets when the remaining columns
+// hold them (else one), in 512 tensor-memory columns; Q buffers, K/V stages and
+// bias stages as shared memory allows.
 bool choose_split_geometry(TcParams& P, bool varlen) {
     const int prefs[][3] = {{2, 3, 2}, {2, 3, 1}, {2, 2, 2}, {2, 2, 1}, {1, 2, 2}, {1, 2, 1}, {1, 1, 1}};
-    P.s_bufs = 3;
-    // 128 columns for O after the S buffers: packed form, one O of o_cols per set; triangle
+    P.s_bufs = varlen ? 2 : 3;
+    // The columns after the S buffers hold O: packed form, one O of o_cols per set; triangle
     // form, one per key half (two per set)
     const uint32_t per_set = (varlen ? 1u : 2u) * P.o_cols;
-    P.o_bufs = per_set * 2 <= 128 ? 2 : 1;
-    if (per_set > 128) return false;
+    const uint32_t avail = 512u - 128u * (uint32_t)P.s_bufs;
+    P.o_bufs = per_set * 2 <= avail ? 2 : 1;
+    if (per_set > avail) return false;
     for (const auto& pr : prefs) {
         P.q_bufs = pr[0];
         P.kv_stages = pr[1];

@@ -19,17 +19,16 @@
 //   warp 10      bias producer: TMA of bias tiles and the dense-mask bits
 //                (triangle form);
 //   warp 11      producer: TMA of V.
-// The MMA warp walks the CTA's key tiles as one stream across work items.
-// Triangle form: when P of tile n is ready, PV of tile n is issued and then
-// QK^T of tile n + 3 into the buffer it read.  Packed form: PV of tile n and
-// QK^T of tile n + 2 are issued interleaved, k step by k step (two
-// independent accumulations the tensor core overlaps).  Either way the next
-// S is issued also when it belongs to the next item, so the softmax finds it
-// ready at item boundaries too.  Tensor memory: three S buffers of 128 columns from column 0 (P
-// overwrites the first 64 columns of its buffer) and, from column 384, two O
-// accumulators of up to 64 columns (D <= 64; items alternate between them)
-// or one of 128 (D in (64, 128]; an item's first PV waits until the softmax
-// has read the previous item's O).  The softmax writes out an item's O after
+// The MMA warp walks the CTA's key tiles as one stream across work items:
+// when P of tile n is ready, PV of tile n is issued and then QK^T of tile
+// n + SB into the S buffer it read (SB = 3 S buffers for the triangle form,
+// 2 for the packed form), also when that tile belongs to the next item, so
+// the softmax finds S ready at item boundaries too.  Tensor memory: the S
+// buffers of 128 columns from column 0 (P overwrites the first 64 columns of
+// its buffer) and, after them, two O accumulator sets (items alternate
+// between them): triangle form, two halves of up to 64 columns each per set;
+// packed form, one O of up to 128 columns per set.  (With one set, an item's
+// first PV waits until the softmax has read the previous item's O.)  The softmax writes out an item's O after
 // the first tile of the next item, when the last PV of the item has long
 // finished.  K and V stages have their own barriers: a K stage is refilled
 // once its QK^T is done, a V stage once its PV is.  The softmax waits for a
@@ -88,8 +87,9 @@ __host__ __device__ inline SplitLayout make_split_layout(const TcParams& P) {
     // (reference max, sum, max) [item parity][key half][3][128 rows] (fp32)
     L.xbuf = L.maskw + P.bias_stages * 16;
     L.xl = L.xbuf + (P.a.varlen ? 2 * 2 : 2 * 2 * 3) * 128 * 4;  // row sums: [key half][128 rows] fp32
-    L.sched = L.xl + 2 * 128 * 4;              // packed form: cu_q[S+1], cu_k[S+1], q blocks[S] (int32)
-    const uint32_t sched_bytes = P.a.varlen ? (uint32_t)(3 * P.a.num_seqs + 2) * 4u : 0u;
+    // packed form: cu_q[S+1], cu_k[S+1], q blocks[S], sequences per q block level[nqt] (int32)
+    L.sched = L.xl + 2 * 128 * 4;
+    const uint32_t sched_bytes = P.a.varlen ? (uint32_t)(3 * P.a.num_seqs + 2 + P.nqt) * 4u : 0u;
     // ring: ring_full[kRing], ring_empty[kRing] (8-byte mbarriers), then the entries
     L.ring = (L.sched + sched_bytes + 15u) & ~15u;
     L.bars = L.ring + (P.a.varlen ? (uint32_t)(16 * kRing + kRing * sizeof(VEntry)) : 0u);
@@ -124,7 +124,9 @@ struct SItem {
 // Packed form, blocks [64 w, 64 w + 64) of the item: `part` (mask_mod applies)
 // and `full` (mask_mod skipped).  Warp-cooperative (every lane of the warp
 // calls it and gets the same masks): lane t reads list entries t, t + 32, ...
-__device__ __forceinline__ void split_window(const SItem& it, int w, uint64_t& part, uint64_t& full) {
+// pre_p / pre_f: entries `lane` of the two lists when the caller has loaded them already (else < 0).
+__device__ __forceinline__ void split_window(const SItem& it, int w, uint64_t& part, uint64_t& full, int pre_p = -1,
+                                             int pre_f = -1) {
     const int lo = 64 * w;
     const int n = min(64, it.nkb - lo);
     if (n <= 0) {
@@ -140,11 +142,11 @@ __device__ __forceinline__ void split_window(const SItem& it, int w, uint64_t& p
     const int lane = threadIdx.x % 32;
     uint64_t p = 0, f = 0;
     for (int t = lane; t < it.n_part; t += 32) {
-        const int kb = it.part_l[t] - lo;
+        const int kb = (t == lane && pre_p >= 0 ? pre_p : it.part_l[t]) - lo;
         if (kb >= 0 && kb < n) p |= 1ull << kb;
     }
     for (int t = lane; t < it.n_full; t += 32) {
-        const int kb = it.full_l[t] - lo;
+        const int kb = (t == lane && pre_f >= 0 ? pre_f : it.full_l[t]) - lo;
         if (kb >= 0 && kb < n) f |= 1ull << kb;
     }
     const uint32_t plo = __reduce_or_sync(0xffffffffu, (uint32_t)p), phi = __reduce_or_sync(0xffffffffu, (uint32_t)(p >> 32));
@@ -163,23 +165,36 @@ struct VCursor {
 __device__ __forceinline__ VCursor vcursor_begin(const TcParams& P) { return VCursor{P.nqt - 1, 0, 0, 0u}; }
 
 // Next item of this CTA: (sequence, head, q block).  `snb` holds each
-// sequence's q block count (0 for a sequence that breaks its contract).
-__device__ __forceinline__ bool vcursor_next(const TcParams& P, const int* snb, VCursor& c, int& seq, int& h,
-                                             int& qb) {
+// sequence's q block count (0 for a sequence that breaks its contract) and
+// `lvl` the number of sequences with more than qb q blocks, for each qb.  The
+// CTA's next position in the deal is fixed by the positions before the
+// cursor, so it is found once; q block levels that end before it are skipped
+// whole, then the level's (sequence, head) groups are walked.
+__device__ __forceinline__ bool vcursor_next(const TcParams& P, const int* snb, const int* lvl, VCursor& c, int& seq,
+                                             int& h, int& qb) {
     const int S = P.a.num_seqs, H = P.a.H;
     const uint32_t G2 = P.fd_2g.d;
     const uint32_t lo = blockIdx.x, hi = G2 - 1u - blockIdx.x;
+    const uint32_t x = c.cnt + (uint32_t)c.hnext;
+    const uint32_t base = P.fd_2g.div(x) * G2;
+    const uint32_t r = x - base;
+    const uint32_t pos = r <= lo ? base + lo : (r <= hi ? base + hi : base + G2 + lo);
     while (c.qb >= 0) {
+        if (c.s == 0) {
+            const uint32_t lv = (uint32_t)lvl[c.qb] * (uint32_t)H;  // the level's positions
+            if (pos >= c.cnt + lv) {
+                c.cnt += lv;
+                c.hnext = 0;
+                --c.qb;
+                continue;
+            }
+        }
         if (c.s >= S) {
             c.s = 0;
             --c.qb;
             continue;
         }
         if (snb[c.s] > c.qb) {
-            const uint32_t x = c.cnt + (uint32_t)c.hnext;
-            const uint32_t base = P.fd_2g.div(x) * G2;
-            const uint32_t r = x - base;
-            const uint32_t pos = r <= lo ? base + lo : (r <= hi ? base + hi : base + G2 + lo);
             if (pos < c.cnt + (uint32_t)H) {
                 seq = c.s;
                 h = (int)(pos - c.cnt);
@@ -235,20 +250,26 @@ __device__ __forceinline__ SItem split_decode(const TcParams& P, const int* sche
         it.k_row0 = sck[seq];
         it.Lk = sck[seq + 1] - it.k_row0;
         it.nkb = (it.Lk + kBN - 1) / kBN;
+        int pre_p = -1, pre_f = -1;
         if (a.kv_num != nullptr) {
             it.lists = true;
             if (qb < a.MQ) {
                 const int hm = a.mask_heads == 1 ? 0 : h;
                 const long long row = ((long long)seq * a.mask_heads + hm) * a.MQ + qb;
+                const int lane = threadIdx.x % 32;
                 it.part_l = a.kv_idx + row * a.MK;
-                it.n_part = min(max(a.kv_num[row], 0), a.MK);
-                if (a.full_num) {
-                    it.full_l = a.full_idx + row * a.MK;
-                    it.n_full = min(max(a.full_num[row], 0), a.MK);
+                if (a.full_num) it.full_l = a.full_idx + row * a.MK;
+                // The row's first 32 list entries are read together with the counts (one
+                // memory round trip instead of two); entries past the count are unused.
+                if (lane < a.MK) {
+                    pre_p = max(it.part_l[lane], -1);
+                    if (a.full_num) pre_f = max(it.full_l[lane], -1);
                 }
+                it.n_part = min(max(a.kv_num[row], 0), a.MK);
+                if (a.full_num) it.n_full = min(max(a.full_num[row], 0), a.MK);
             }
         }
-        split_window(it, 0, it.part0, it.full0);
+        split_window(it, 0, it.part0, it.full0, pre_p, pre_f);
         int nkt = __popcll(it.part0 | it.full0);
         for (int w = 1; 64 * w < it.nkb; ++w) {
             uint64_t pm, fm;
@@ -442,15 +463,11 @@ __device__ __forceinline__ void issue_qk_n(int ks, uint32_t sd, uint64_t qd, uin
     for (int kk = 0; kk < ks; ++kk) mma_ss(sd, qd + qk_koff(kk), kd + qk_koff(kk), idesc, kk > 0 ? 1u : 0u);
 }
 // PV of one tile into one O accumulator d (P from TMEM at pa, 8 columns per 16
-// keys; V MN-major, 2 KB per 16 keys), with the first ks k steps of the next
-// QK^T interleaved (independent accumulators, so the tensor core overlaps them).
-__device__ __forceinline__ void issue_pv_qk_n(int ks, uint32_t d, uint32_t pa, uint64_t vd, uint32_t idesc_pv,
-                                              bool first, uint32_t sd, uint64_t qd, uint64_t kd, uint32_t idesc_qk) {
+// keys; V MN-major, 2 KB per 16 keys).
+__device__ __forceinline__ void issue_pv(uint32_t d, uint32_t pa, uint64_t vd, uint32_t idesc_pv, bool first) {
 #pragma unroll 1
-    for (int kk = 0; kk < kBN / 16; ++kk) {
+    for (int kk = 0; kk < kBN / 16; ++kk)
         mma_ts(d, pa + kk * 8, vd + (uint64_t)kk * 128, idesc_pv, (!first || kk > 0) ? 1u : 0u);
-        if (kk < ks) mma_ss(sd, qd + qk_koff(kk), kd + qk_koff(kk), idesc_qk, kk > 0 ? 1u : 0u);
-    }
 }
 // Split O: keys 0-63 of the tile into O_0 (d0), keys 64-127 into O_1 (d1),
 // alternating so the two chains overlap.  P of key half 1 sits in that half's
@@ -487,7 +504,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
     const int S = P.kv_stages;
     const int BS = P.bias_stages;
     const int QB = P.q_bufs;
-    constexpr int SB = 3;                        // S buffers (P.s_bufs)
+    constexpr int SB = VARLEN ? 2 : 3;           // S buffers (P.s_bufs)
     const int OB = P.o_bufs;                     // O accumulator sets (items alternate between them)
     // Triangle form: each key half accumulates its own O (P of keys [64h, 64h + 64)
     // times those V rows), so the two softmax warps of a lane quarter need no
@@ -692,10 +709,17 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
             StageRing rr = {0, 0u, false};
             VCursor vc = vcursor_begin(P);
             VEntry* ents = reinterpret_cast<VEntry*>(gbase + L.ring + 16u * kRing);
+            const int* snb = sched + 2 * (a.num_seqs + 1);
+            int* lvl = sched + 3 * a.num_seqs + 2;
+            for (int qb = lane; qb < P.nqt; qb += 32) lvl[qb] = 0;
+            __syncwarp();
+            for (int sq = lane; sq < a.num_seqs; sq += 32)
+                for (int qb = 0; qb < snb[sq]; ++qb) atomicAdd(&lvl[qb], 1);
+            __syncwarp();
             bool ok = true;
             for (;;) {
                 int seq = 0, hh = 0, qb = 0;
-                const bool more = vcursor_next(P, sched + 2 * (a.num_seqs + 1), vc, seq, hh, qb);
+                const bool more = vcursor_next(P, snb, lvl, vc, seq, hh, qb);
                 const int slot = rr.idx;
                 if (rr.wrapped) {
                     ok = __all_sync(0xffffffffu, wait_bar(ring_empty(slot), rr.ph ^ 1u, abort_flag, a.status));
@@ -770,13 +794,11 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
         // ------------------------------------------------------------------ MMA
         // Two cursors over the CTA's items with key tiles: `qc` for the next
         // QK^T, `pc` for the next PV.  Tile n of the stream (counted over
-        // items) has S buffer n % 3 and K/V stage n % S; item number i has Q
-        // buffer i % QB and O accumulator i % o_bufs.  QK^T runs two tiles
-        // ahead: once P of tile n is in TMEM, PV of tile n (reading S buffer
-        // n % 3) and QK^T of tile n + 2 (into buffer (n + 2) % 3, whose PV was
-        // issued before) are issued interleaved, k step by k step.  The two
-        // chains have different accumulators, so the tensor core overlaps
-        // them instead of waiting on each chain's own accumulation.
+        // items) has S buffer n % SB and K/V stage n % S; item number i has Q
+        // buffer i % QB and O accumulator set i % o_bufs.  QK^T runs SB tiles
+        // ahead: once P of tile n is in TMEM, PV of tile n is issued, then
+        // QK^T of tile n + SB into the buffer PV n reads (the tensor core runs
+        // them in order).
         const bool leader = elect_one();
         SplitCursor<VARLEN> qc, pc;
         qc.walk.begin(P, ring);
@@ -826,12 +848,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
             if (leader) issue_qk_n(P.ksteps, sd, qd, kd, P.idesc_qk);
             qk_done();
         };
-        // Packed form (D up to 128, the MMA warp sets the pace): PV of tile n and
-        // QK^T of tile n + 2 interleaved.  Triangle form (D <= 64, the softmax sets
-        // the pace): PV of tile n, then QK^T of tile n + 3 into the buffer it read,
-        // which keeps three tiles of S ahead of the softmax.
-        constexpr bool kInterleave = VARLEN;
-        for (int i = 0; i < (kInterleave ? 2 : 3) && ok && has_q; ++i) {
+        for (int i = 0; i < SB && ok && has_q; ++i) {
             ok = qk_ready();
             if (!ok) break;
             qk_alone();
@@ -853,11 +870,6 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
                 if (!ok) break;
                 oe.next(1);
             }
-            const bool qk = kInterleave && has_q;
-            if (qk) {
-                ok = qk_ready();
-                if (!ok) break;
-            }
             tc_fence_after();
             const uint64_t vd = sw128_desc(v_smem(st), kBox, 1024);
             const uint32_t oset = OB == 1 ? 0u : (pc.qi & 1u);
@@ -867,11 +879,10 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
                 if constexpr (kSplitO)
                     issue_pv_split(d, d + P.o_cols, pa, vd, P.idesc_pv, pc.t == 0);
                 else
-                    issue_pv_qk_n(qk ? P.ksteps : 0, d, pa, vd, P.idesc_pv, pc.t == 0, sd, qd, kd, P.idesc_qk);
+                    issue_pv(d, pa, vd, P.idesc_pv, pc.t == 0);
                 mma_commit(pv_done(np));
                 mma_commit(v_empty(st));
             }
-            if (qk) qk_done();
             ++np;
             sp.next(SB);
             vp.next(S);
@@ -879,7 +890,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
                 ++pc.qi;
                 has_p = split_seek<VARLEN>(P, ring, pc);
             }
-            if (!kInterleave && has_q) {  // the buffer just multiplied by V takes the S three tiles on
+            if (has_q) {  // the buffer just multiplied by V takes the S SB tiles on
                 ok = qk_ready();
                 if (!ok) break;
                 qk_alone();
@@ -935,9 +946,9 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
         // so a parity wait is exact while that barrier is neither a phase ahead
         // (PV n + 2 done) nor behind (PV n - 2 not done).  The callers hold:
         // this warp has not given P of tile n + 2, and PV n - 2 finished
-        // before the S it last read (QK^T of tile m is issued after PV m - 3,
-        // or with PV m - 2 in the interleaved order, and its commit completes
-        // only when every MMA issued before it has).  With `prev`, PV n - 1 is
+        // before the S it last read (QK^T of tile m is issued after PV m - SB,
+        // SB >= 2, and its commit completes only when every MMA issued before
+        // it has).  With `prev`, PV n - 1 is
         // waited for first, which covers a caller that only knows PV n - 3
         // finished.
         auto wait_pv = [&](uint32_t n, bool prev) -> bool {
