@@ -6,25 +6,25 @@
 // per-row sums, formed before this kernel), per (b, n, h) slab:
 //     dV = P^T dO,  dP = dO V^T,  dS = P (dP - delta) at valid keys (0 at masked),
 //     dK = s dS^T Q,  dQ = s dS K,  dBias[b, h] += dS (summed over n).
-// One CTA per (slab, 128-key tile), looping over the slab's 128-row query tiles.
-// Per query tile, five MMAs with 128 keys on the TMEM lanes:
-//     S^T  = K Q^T     (A = K, B = Q, both K-major in shared memory)   TMEM [0, 128)
-//     dP^T = V dO^T    (A = V, B = dO)                                   TMEM [128, 256)
-//     dV  += P^T dO    (A = P^T, TMEM [256 + 2D + 64, +64); B = dO read MN-major)
-//                                                                        TMEM [256, 256 + D)
-//     dK  += dS^T Q    (A = dS^T, TMEM [256 + 2D, +64); B = Q read MN-major)
-//                                                                        TMEM [256 + D, 256 + 2D)
-//     dQ_j = dS K      (A = dS from shared memory, M = queries, MN-major;
-//                       B = K read MN-major)     TMEM [256 + 2D, 256 + 3D), dS^T's columns
-// Warps 0-7 (one thread per key row = TMEM lane; warps w and w + 4 take the
-// two query halves of the tile) turn S^T and dP^T into P^T and dS^T (16-bit
-// pairs into their own TMEM columns, dS also into shared memory as the A
-// operand of dQ) and add dS to the fp32 dBias accumulator (coalesced over
-// keys); then each reads its 32 columns of dQ_j (one thread per query row) and
-// adds them to the fp32 dQ accumulator with a TMA reduce-add; warps 0-3 write dK
-// and dV at the end.
-// Warp 8 loads K and V once and Q, dO, the bias tile and the rows' lse / delta
-// per query tile; warp 9 issues the MMAs.  Every wait is bounded (TA_ERR_TIMEOUT).
+// One CTA per (slab, 128-key tile), looping over the slab's 128-row query tiles,
+// each taken as two halves of 64 queries.  MMAs, with 128 keys on the TMEM lanes:
+//     S^T  = K Q_h^T   (A = K, B = Q rows of half h, both K-major)  TMEM [64 h, +64)
+//     dP^T = V dO_h^T  (A = V, B = dO rows of half h)                TMEM [128 + 64 h, +64)
+//     dV  += P^T dO_h  (A = P^T from TMEM, over S^T; B = dO read MN-major)  TMEM [256, 256 + D)
+//     dK  += dS^T Q_h  (A = dS^T from TMEM, over dP^T; B = Q read MN-major) TMEM [256 + D, 256 + 2D)
+//     dQ_j = dS K      (per tile: A = dS from shared memory, M = queries, MN-major;
+//                       B = K read MN-major)                          TMEM [256 + 2D, 256 + 3D)
+// The two halves use separate S^T / dP^T columns, so the tensor core computes one
+// half's S^T / dP^T while the compute warps work on the other.  Warps 0-7 (one thread
+// per key row = TMEM lane; warps w and w + 4 take 32 queries each of every half) turn
+// S^T and dP^T into P^T and dS^T (16-bit pairs written over the columns just read; dS
+// also into shared memory as the A operand of dQ) and add dS to the fp32 dBias
+// accumulator (coalesced over keys); between the halves of tile j each reads its 32
+// columns of dQ_{j-1} (one thread per query row) and adds them to the fp32 dQ
+// accumulator with a TMA reduce-add; warps 0-3 write dK and dV at the end.
+// Warp 8 loads K and V once and, per query tile, Q, dO, the rows' lse / delta and
+// the two bias halves (each as soon as the previous tile's half is read); warp 9
+// issues the MMAs.  Every wait is bounded (TA_ERR_TIMEOUT).
 
 #include "tc_kernel.cuh"
 
@@ -45,7 +45,7 @@ struct BwdTc {
     float scale;
     int B, N, H, Q, K, D;
     int nkt, nqt, ksteps;
-    uint32_t idesc_s;   // M 128, N 128: K-major A and B
+    uint32_t idesc_s;   // M 128, N 64: K-major A and B
     uint32_t idesc_g;   // M 128, N D: A from TMEM, B MN-major
     uint32_t idesc_q;   // M 128, N D: A and B MN-major in shared memory
     uint32_t bias_bytes;
@@ -58,9 +58,9 @@ struct BwdTc {
 struct BwdLayout {
     uint32_t k, v, q, ds, bias, dqst, lse, bars, tmem_slot, abort_flag, total;
 };
-// kv_full, q_full[2], q_empty[2], bias_full, bias_empty, s_full, p_full, dq_full, dq_empty, fin, drain,
-// lse_full[2]
-constexpr int kBwdBars = 15;
+// kv_full, q_full[2], q_empty[2], lse_full[2], bias_full[2], bias_empty[2], s_full[2], p_full[2],
+// dq_full, dq_empty, ds_free, fin, drain
+constexpr int kBwdBars = 20;
 __host__ __device__ inline BwdLayout bwd_layout(const BwdTc& P) {
     BwdLayout L;
     L.k = 0;
@@ -114,11 +114,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
     const uint32_t kv_full = bar(0);
     auto q_full = [&](int st) { return bar(1 + st); };
     auto q_empty = [&](int st) { return bar(3 + st); };
-    const uint32_t bias_full = bar(5), bias_empty = bar(6), s_full = bar(7), p_full = bar(8);
-    const uint32_t dq_full = bar(9), dq_empty = bar(10), fin = bar(11), drain = bar(12);
-    auto lse_full = [&](int st) { return bar(13 + st); };
+    auto lse_full = [&](int st) { return bar(5 + st); };
+    auto bias_full = [&](int hh) { return bar(7 + hh); };
+    auto bias_empty = [&](int hh) { return bar(9 + hh); };
+    auto s_full = [&](int hh) { return bar(11 + hh); };
+    auto p_full = [&](int hh) { return bar(13 + hh); };
+    const uint32_t dq_full = bar(15), dq_empty = bar(16), ds_free = bar(17), fin = bar(18), drain = bar(19);
     auto q_smem = [&](int st) { return base + L.q + (uint32_t)st * 2u * kBox; };
     auto do_smem = [&](int st) { return base + L.q + (uint32_t)st * 2u * kBox + kBox; };
+    // bias rows [64 hh, 64 hh + 64) of the tile: boxes of bias_box_cols keys x 64 rows (8 KB each)
+    auto bias_half = [&](int hh) { return base + L.bias + (uint32_t)hh * (P.bias_bytes / 2u); };
 
     const long long unit = blockIdx.x / P.nkt;  // (b*N + n)*H + h
     const int k0 = (int)(blockIdx.x - unit * P.nkt) * kBN;
@@ -149,17 +154,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
     if (threadIdx.x == 0) {
         *abort_flag = 0;
         mbar_init(kv_full, 1);
-        for (int st = 0; st < 2; ++st) {
-            mbar_init(q_full(st), 1);    // the expect_tx arrival of Q and dO
-            mbar_init(lse_full(st), 1);  // the lse / delta rows written
-            mbar_init(q_empty(st), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(q_full(i), 1);      // the expect_tx arrival of Q and dO
+            mbar_init(q_empty(i), 1);
+            mbar_init(lse_full(i), 1);    // the lse / delta rows written
+            mbar_init(bias_full(i), 1);
+            mbar_init(bias_empty(i), 8);  // every compute warp has read the bias half
+            mbar_init(s_full(i), 1);
+            mbar_init(p_full(i), 8);
         }
-        mbar_init(bias_full, 1);
-        mbar_init(bias_empty, 8);
-        mbar_init(s_full, 1);
-        mbar_init(p_full, 8);
         mbar_init(dq_full, 1);
         mbar_init(dq_empty, P.D > 32 ? 8 : 4);  // the warps that read dQ_j
+        mbar_init(ds_free, 1);
         mbar_init(fin, 1);
         mbar_init(drain, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -175,10 +181,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t D = (uint32_t)P.D;
-    // S^T, dP^T, dV, dK, then dQ_j (which shares its 64 columns with dS^T: MMA 4 reads dS^T before
-    // MMA 5 writes dQ_j, and dS^T of the next tile is written after dQ_j is read), then P^T.
+    // S^T of query half hh at tS + 64 hh, dP^T at tDP + 64 hh (P^T and dS^T written over them in
+    // place), then dV, dK and dQ_j.
     const uint32_t tS = tmem, tDP = tmem + 128, tDV = tmem + 256, tDK = tmem + 256 + D, tDQ = tmem + 256 + 2 * D;
-    const uint32_t tDS = tDQ, tP = tDQ + 64;
 
     if (warp == 8) {
         // ------------------------------------------------------------ producer
@@ -190,7 +195,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
         }
         for (int j = 0; j < P.nqt && ok; ++j) {
             const int q0 = j * kBM, st = j % P.qs, use = j / P.qs;
-            if (j >= P.qs) {  // stage st held tile j - qs: its MMAs are done
+            // This tile's Q / dO, bias half 0 (as soon as the compute warps have read half 0 of
+            // tile j - 1), the rows' lse / delta, then bias half 1.
+            auto bias_load = [&](int hh) -> bool {
+                if (j > 0 &&
+                    !__all_sync(0xffffffffu, wait_bar(bias_empty(hh), (uint32_t)(j - 1) & 1u, abort_flag, P.status)))
+                    return false;
+                if (lane == 0) {
+                    mbar_expect_tx(bias_full(hh), P.bias_bytes / 2u);
+                    for (int bx = 0; bx < P.bias_boxes; ++bx)
+                        tma_load_3d(bias_half(hh) + (uint32_t)bx * 8192u, &P.tm_bias, k0 + bx * P.bias_box_cols,
+                                    q0 + 64 * hh, b * P.H + h, bias_full(hh));
+                }
+                return true;
+            };
+            if (j >= P.qs) {  // stage st held tile j - qs: its MMAs and its compute are done
                 ok = __all_sync(0xffffffffu, wait_bar(q_empty(st), (uint32_t)(use - 1) & 1u, abort_flag, P.status));
                 if (!ok) break;
             }
@@ -199,18 +218,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
                 tma_load_3d(q_smem(st), &P.tm_q, 0, q0, (int)unit, q_full(st));
                 tma_load_3d(do_smem(st), &P.tm_do, 0, q0, (int)unit, q_full(st));
             }
-            // The bias tile (single-buffered) as soon as the compute warps have read the previous one,
-            // then the rows' lse / delta (only the compute warps wait for them).
-            if (j > 0) {
-                ok = __all_sync(0xffffffffu, wait_bar(bias_empty, (uint32_t)(j - 1) & 1u, abort_flag, P.status));
-                if (!ok) break;
-            }
-            if (lane == 0) {
-                mbar_expect_tx(bias_full, P.bias_bytes);
-                for (int bx = 0; bx < P.bias_boxes; ++bx)
-                    tma_load_3d(base + L.bias + (uint32_t)bx * kBox, &P.tm_bias, k0 + bx * P.bias_box_cols, q0,
-                                b * P.H + h, bias_full);
-            }
+            ok = bias_load(0);
+            if (!ok) break;
             float* lse_s = reinterpret_cast<float*>(gbase + L.lse + (uint32_t)st * 1024u);
             float* del_s = lse_s + 128;
             float lv[kBM / 32], dv[kBM / 32];  // every load in flight before the first store
@@ -227,55 +236,82 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(lse_full(st));  // release: the rows are written
+            ok = bias_load(1);
         }
         if (!ok) *abort_flag = 1;
     } else if (warp == 9) {
         // ----------------------------------------------------------------- MMA
+        // Per query tile j and half hh (64 queries): S^T and dP^T of (j, hh) into buffer hh;
+        // once P^T / dS^T of (j, hh) are written, dV and dK take them, then S^T / dP^T of
+        // (j + 1, hh) go into the same buffer (the tensor core runs them in order), so the
+        // compute warps find the next half ready.  After half 1, dQ_j = dS K.  With one Q / dO
+        // stage, tile j + 1's S^T / dP^T wait until tile j's MMAs are all issued.
         const bool leader = elect_one();
         bool ok = __all_sync(0xffffffffu, wait_bar(kv_full, 0, abort_flag, P.status));
         const uint64_t kK = sw128_desc(base + L.k, 16, 1024), vK = sw128_desc(base + L.v, 16, 1024);
         const uint64_t kM = sw128_desc(base + L.k, kBox, 1024), dsM = sw128_desc(base + L.ds, kBox, 1024);
-        for (int j = 0; j < P.nqt && ok; ++j) {
-            const uint32_t ph = (uint32_t)j & 1u;
+        auto mma1 = [&](int j, int hh) -> bool {
             const int st = j % P.qs;
-            const uint64_t qK = sw128_desc(q_smem(st), 16, 1024), doK = sw128_desc(do_smem(st), 16, 1024);
-            const uint64_t qM = sw128_desc(q_smem(st), kBox, 1024), doM = sw128_desc(do_smem(st), kBox, 1024);
-            ok = __all_sync(0xffffffffu, wait_bar(q_full(st), (uint32_t)(j / P.qs) & 1u, abort_flag, P.status));
-            if (!ok) break;
-            tc_fence_after();
+            if (hh == 0) {
+                if (!__all_sync(0xffffffffu, wait_bar(q_full(st), (uint32_t)(j / P.qs) & 1u, abort_flag, P.status)))
+                    return false;
+                tc_fence_after();
+            }
+            // rows 64 hh .. 64 hh + 63 of the K-major Q / dO tiles: 8 KB on (a whole number of swizzle atoms)
+            const uint64_t qK = sw128_desc(q_smem(st), 16, 1024) + 512u * (uint32_t)hh;
+            const uint64_t doK = sw128_desc(do_smem(st), 16, 1024) + 512u * (uint32_t)hh;
             if (leader) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)  // S^T = K Q^T (D / 16 <= 4 k steps)
                     if (kk < P.ksteps)
-                        mma_ss(tS, kK + 2u * (uint32_t)kk, qK + 2u * (uint32_t)kk, P.idesc_s, kk > 0 ? 1u : 0u);
+                        mma_ss(tS + 64u * (uint32_t)hh, kK + 2u * (uint32_t)kk, qK + 2u * (uint32_t)kk, P.idesc_s,
+                               kk > 0 ? 1u : 0u);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)  // dP^T = V dO^T
                     if (kk < P.ksteps)
-                        mma_ss(tDP, vK + 2u * (uint32_t)kk, doK + 2u * (uint32_t)kk, P.idesc_s, kk > 0 ? 1u : 0u);
-                mma_commit(s_full);
+                        mma_ss(tDP + 64u * (uint32_t)hh, vK + 2u * (uint32_t)kk, doK + 2u * (uint32_t)kk, P.idesc_s,
+                               kk > 0 ? 1u : 0u);
+                mma_commit(s_full(hh));
             }
-            ok = __all_sync(0xffffffffu, wait_bar(p_full, ph, abort_flag, P.status));
-            if (!ok) break;
-            tc_fence_after();
-            if (leader) {
-#pragma unroll
-                for (int kk = 0; kk < kBM / 16; ++kk) {  // 16 queries per k step
-                    const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
-                    mma_ts(tDV, tP + 8u * (uint32_t)kk, doM + 128u * (uint32_t)kk, P.idesc_g, acc);
-                    mma_ts(tDK, tDS + 8u * (uint32_t)kk, qM + 128u * (uint32_t)kk, P.idesc_g, acc);
-                }
-            }
-            if (j > 0) {  // the compute warps have read dQ of the previous query tile
-                ok = __all_sync(0xffffffffu, wait_bar(dq_empty, ph ^ 1u, abort_flag, P.status));
+            return true;
+        };
+        if (ok && P.nqt > 0) ok = mma1(0, 0) && mma1(0, 1);
+        for (int j = 0; j < P.nqt && ok; ++j) {
+            const int st = j % P.qs;
+            const uint64_t qM = sw128_desc(q_smem(st), kBox, 1024), doM = sw128_desc(do_smem(st), kBox, 1024);
+            for (int hh = 0; hh < 2 && ok; ++hh) {
+                ok = __all_sync(0xffffffffu, wait_bar(p_full(hh), (uint32_t)j & 1u, abort_flag, P.status));
                 if (!ok) break;
                 tc_fence_after();
-            }
-            if (leader) {
+                if (leader) {
 #pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk)  // dQ_j = dS K, 16 keys per k step
-                    mma_ss(tDQ, dsM + 128u * (uint32_t)kk, kM + 128u * (uint32_t)kk, P.idesc_q, kk > 0 ? 1u : 0u);
-                mma_commit(dq_full);
-                mma_commit(q_empty(st));
+                    for (int kk = 0; kk < 4; ++kk) {  // 16 queries per k step; P^T / dS^T at 16 kk
+                        const uint32_t acc = (j > 0 || hh > 0 || kk > 0) ? 1u : 0u;
+                        const uint32_t qs16 = (uint32_t)(4 * hh + kk);  // 16-query step within the tile
+                        mma_ts(tDV, tS + 64u * (uint32_t)hh + 16u * (uint32_t)kk, doM + 128u * qs16, P.idesc_g, acc);
+                        mma_ts(tDK, tDP + 64u * (uint32_t)hh + 16u * (uint32_t)kk, qM + 128u * qs16, P.idesc_g, acc);
+                    }
+                }
+                if (hh == 1) {
+                    if (j > 0) {  // the compute warps have read dQ of the previous tile
+                        ok = __all_sync(0xffffffffu, wait_bar(dq_empty, (uint32_t)(j - 1) & 1u, abort_flag, P.status));
+                        if (!ok) break;
+                        tc_fence_after();
+                    }
+                    if (leader) {
+#pragma unroll
+                        for (int kk = 0; kk < kBN / 16; ++kk)  // dQ_j = dS K, 16 keys per k step
+                            mma_ss(tDQ, dsM + 128u * (uint32_t)kk, kM + 128u * (uint32_t)kk, P.idesc_q,
+                                   kk > 0 ? 1u : 0u);
+                        mma_commit(dq_full);
+                        mma_commit(ds_free);
+                        mma_commit(q_empty(st));
+                    }
+                }
+                if (j + 1 < P.nqt) {
+                    if (P.qs > 1) ok = mma1(j + 1, hh);
+                    else if (hh == 1) ok = mma1(j + 1, 0) && mma1(j + 1, 1);
+                }
             }
         }
         if (leader) {
@@ -288,7 +324,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
     } else {
         // ------------------------------------------------------------- compute
         const int wq = warp & 3;          // TMEM lane quarter: keys (and later query rows) 32 wq ..
-        const int hq = warp >> 2;         // query half of every tile: chunks 2 hq, 2 hq + 1
+        const int hq = warp >> 2;         // within each 64-query half: queries 32 hq .. 32 hq + 31
         const int kr = wq * 32 + lane;    // key row of the tile
         const int key = k0 + kr;
         const bool exists = key < P.K;
@@ -305,152 +341,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const float inv_k = 1.f / (float)P.K;
         const uint32_t rsw = (uint32_t)(kr & 7);
-        // bias element (query row ql, key kr) of the tile: 128B-swizzled boxes of bias_box_cols keys
-        const uint32_t bbox = base + L.bias + (uint32_t)(kr / P.bias_box_cols) * kBox;
+        // this key's column in the bias halves: boxes of bias_box_cols keys x 64 rows, 128B-swizzled
+        const uint32_t bbox_off = (uint32_t)(kr / P.bias_box_cols) * 8192u;
         const uint32_t bcol_b = (uint32_t)(kr % P.bias_box_cols) * (BIAS_F32 ? 4u : 2u);
         // swizzled byte offset of this key's column in query row r, by r % 8 (128B swizzle)
         uint32_t xo[8];
 #pragma unroll
         for (int r8 = 0; r8 < 8; ++r8) xo[r8] = ((((bcol_b >> 4) ^ (uint32_t)r8)) << 4) + (bcol_b & 15u);
         float* dbias_row = P.dbias_acc ? P.dbias_acc + ((long long)b * P.H + h) * P.Q * (long long)P.K + key : nullptr;
-        // dQ staging of this warp: boxes of `inner` fp32 columns x 32 rows, swizzled by their row width
+        // dQ staging of this lane quarter: boxes of `inner` fp32 columns x 32 rows, swizzled by their row width
         const int inner = P.D < 32 ? P.D : 32;
         const uint32_t rowb = (uint32_t)inner * 4u;
         const uint32_t dq_stage = base + L.dqst + (uint32_t)(wq * 32 * P.D * 4);
         const uint32_t qsw = rowb == 128 ? (uint32_t)(lane & 7) : (uint32_t)((lane >> 1) & 3);
-        bool ok = true;
-        for (int j = 0; j < P.nqt && ok; ++j) {
-            const uint32_t ph = (uint32_t)j & 1u;
-            const int q0 = j * kBM, st = j % P.qs;
-            const float* lse_s = reinterpret_cast<const float*>(gbase + L.lse + (uint32_t)st * 1024u);
-            const float* del_s = lse_s + 128;
-            ok = __all_sync(0xffffffffu, wait_bar(lse_full(st), (uint32_t)(j / P.qs) & 1u, abort_flag, P.status));
-            if (!ok) break;
-            ok = __all_sync(0xffffffffu, wait_bar(bias_full, ph, abort_flag, P.status));
-            if (!ok) break;
-            ok = __all_sync(0xffffffffu, wait_bar(s_full, ph, abort_flag, P.status));
-            if (!ok) break;
-            // (dS^T of this warp's chunks goes to dQ_j's columns [32 hq, 32 hq + 32), which this
-            // warp itself read out of the previous tile's dQ_j.)
-            tc_fence_after();
-            // Chunks of 16 queries (few live registers, so the compiler can overlap the
-            // chunk's independent elements): warp half hq takes chunks 4 hq .. 4 hq + 3.
-            constexpr int CW = 16;
-#pragma unroll 1
-            for (int c = 4 * hq; c < 4 * hq + 4; ++c) {
-                uint32_t sr[CW], dr[CW];
-                tmem_ld_x16(tS + lane_off + (uint32_t)(CW * c), sr);
-                tmem_ld_x16(tDP + lane_off + (uint32_t)(CW * c), dr);
-                // The chunk's lse and delta (shared-memory broadcasts, four at a time) and this
-                // key's bias column: query row ql = CW c + i lives at bcb + 128 i + xo[i % 8].
-                float ls[CW], dl[CW];
-#pragma unroll
-                for (int i = 0; i < CW; i += 4) {
-                    const float4 l4 = *reinterpret_cast<const float4*>(lse_s + CW * c + i);
-                    const float4 d4 = *reinterpret_cast<const float4*>(del_s + CW * c + i);
-                    ls[i] = l4.x, ls[i + 1] = l4.y, ls[i + 2] = l4.z, ls[i + 3] = l4.w;
-                    dl[i] = d4.x, dl[i + 1] = d4.y, dl[i + 2] = d4.z, dl[i + 3] = d4.w;
-                }
-                const uint8_t* bcb = gbase + (bbox - base) + (uint32_t)(CW * c) * 128u;
-                const int nq = P.Q - (q0 + CW * c);  // queries of the chunk that exist
-                uint32_t pp[CW / 2], dd[CW / 2];
-                if (__all_sync(0xffffffffu, valid) && nq >= CW) {
-                    // Every key of the warp valid and every query of the chunk present: each row
-                    // has a valid key, so its lse is a plain log-sum-exp and P = 2^(x log2e - lse log2e).
-                    const float2 sl2 = make_float2(P.scale * kLog2e, P.scale * kLog2e);
-                    const float2 l2e2 = make_float2(kLog2e, kLog2e);
-                    float* dbp = dbias_row ? dbias_row + (long long)(q0 + CW * c) * P.K : nullptr;
-#pragma unroll
-                    for (int i = 0; i < CW; i += 2) {
-                        float2 bv;
-                        if constexpr (BIAS_F32) {
-                            bv = make_float2(*reinterpret_cast<const float*>(bcb + i * 128 + xo[i & 7]),
-                                             *reinterpret_cast<const float*>(bcb + (i + 1) * 128 + xo[(i + 1) & 7]));
-                        } else {
-                            const uint32_t b0 = *reinterpret_cast<const unsigned short*>(bcb + i * 128 + xo[i & 7]);
-                            const uint32_t b1 =
-                                *reinterpret_cast<const unsigned short*>(bcb + (i + 1) * 128 + xo[(i + 1) & 7]);
-                            bv = unpack2<BF16>(b0 | (b1 << 16));
-                        }
-                        // y = s S log2e + b log2e - lse log2e
-                        const float2 nl = __fmul2_rn(make_float2(ls[i], ls[i + 1]), make_float2(-kLog2e, -kLog2e));
-                        const float2 y = __ffma2_rn(
-                            make_float2(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1])), sl2,
-                            __ffma2_rn(bv, l2e2, nl));
-                        const float2 pr = make_float2(ex2(y.x), ex2(y.y));
-                        const float2 ds = __fmul2_rn(
-                            pr, __fadd2_rn(make_float2(__uint_as_float(dr[i]), __uint_as_float(dr[i + 1])),
-                                           make_float2(-dl[i], -dl[i + 1])));
-                        pp[i / 2] = pack2<BF16>(pr.x, pr.y);
-                        dd[i / 2] = pack2<BF16>(ds.x, ds.y);
-                        if (dbp) {
-                            red_add_global(dbp + (long long)i * P.K, ds.x);
-                            red_add_global(dbp + (long long)(i + 1) * P.K, ds.y);
-                        }
-                    }
-                } else {
-                    // Logits first (every read of the bias tile before any reduction into dBias).
-#pragma unroll
-                    for (int ii = 0; ii < CW; ++ii) {
-                        float x = kMasked;
-                        if (valid) {
-                            const uint8_t* ba = bcb + ii * 128 + xo[ii & 7];
-                            float bv;
-                            if constexpr (BIAS_F32) bv = *reinterpret_cast<const float*>(ba);
-                            else bv = unpack2<BF16>((uint32_t)*reinterpret_cast<const unsigned short*>(ba)).x;
-                            x = fmaf(P.scale, __uint_as_float(sr[ii]), bv);
-                        }
-                        sr[ii] = __float_as_uint(x);
-                    }
-                    // P and dS (dS kept in dr for the dBias reduction).
-#pragma unroll
-                    for (int i = 0; i < CW; i += 2) {
-                        float pv[2], sv[2];
-#pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            const int ii = i + u;
-                            const bool live = exists && ii < nq;
-                            const float p = live ? bwd_weight(__uint_as_float(sr[ii]), ls[ii], inv_k) : 0.f;
-                            const float ds = (live && valid) ? p * (__uint_as_float(dr[ii]) - dl[ii]) : 0.f;
-                            pv[u] = p;
-                            sv[u] = ds;
-                            dr[ii] = __float_as_uint(ds);
-                        }
-                        pp[i / 2] = pack2<BF16>(pv[0], pv[1]);
-                        dd[i / 2] = pack2<BF16>(sv[0], sv[1]);
-                    }
-                    if (dbias_row) {
-#pragma unroll
-                        for (int ii = 0; ii < CW; ++ii)
-                            if (__uint_as_float(dr[ii]) != 0.f)
-                                red_add_global(dbias_row + (long long)(q0 + CW * c + ii) * P.K,
-                                               __uint_as_float(dr[ii]));
-                    }
-                }
-                // P^T and dS^T as 16-bit query pairs into columns [8c, 8c + 8) (read already)
-                tmem_st_x8(tP + lane_off + (uint32_t)(CW / 2 * c), pp);
-                tmem_st_x8(tDS + lane_off + (uint32_t)(CW / 2 * c), dd);
-                // dS as [key][query] in shared memory: box (CW c) / 64, 16-byte chunks of 8 queries
-                const uint32_t drow = base + L.ds + (uint32_t)((CW * c) / 64) * kBox + (uint32_t)kr * 128u;
-#pragma unroll
-                for (int g = 0; g < CW / 8; ++g) {
-                    const uint32_t ch = (uint32_t)(((CW * c) % 64) / 8 + g);
-                    st_shared_v4(drow + ((ch ^ rsw) << 4), dd[4 * g], dd[4 * g + 1], dd[4 * g + 2], dd[4 * g + 3]);
-                }
-            }
-            __syncwarp();  // every lane has read its bias values
-            if (lane == 0) mbar_arrive(bias_empty);
-            tmem_st_wait();
-            fence_async_shared();  // dS in shared memory is read by the tensor core
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(p_full);
-            // dQ_j: thread = query row q0 + 32 wq + lane; warp half hq reads columns [32 hq, 32 hq + 32)
-            // (D <= 32: warps 4-7 have none) and adds them into the accumulator.
+
+        // dQ_j read out (thread = query row 128 j + 32 wq + lane; warp half hq takes columns
+        // [32 hq, 32 hq + 32), none for D <= 32 and hq = 1) and added into the accumulator.
+        auto readout = [&](int jr) -> bool {
             const int dc0 = 32 * hq, dc1 = P.D < dc0 + 32 ? P.D : dc0 + 32;
-            if (dc0 >= P.D) continue;
-            ok = __all_sync(0xffffffffu, wait_bar(dq_full, ph, abort_flag, P.status));
-            if (!ok) break;
+            if (dc0 >= P.D) return true;
+            if (!__all_sync(0xffffffffu, wait_bar(dq_full, (uint32_t)jr & 1u, abort_flag, P.status))) return false;
             tc_fence_after();
             if (lane == 0) bulk_wait_read_all();  // the previous reduce has read the staging rows
             __syncwarp();
@@ -473,14 +383,154 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(dq_empty);
-                if (q0 + 32 * wq < P.Q) {
+                if (jr * kBM + 32 * wq < P.Q) {
                     for (int bxi = dc0 / inner; bxi * inner < dc1; ++bxi)
-                        tma_reduce_add_3d(&P.tm_dq, dq_stage + (uint32_t)bxi * 32u * rowb, bxi * inner, q0 + 32 * wq,
-                                          (int)unit);
+                        tma_reduce_add_3d(&P.tm_dq, dq_stage + (uint32_t)bxi * 32u * rowb, bxi * inner,
+                                          jr * kBM + 32 * wq, (int)unit);
                     bulk_commit();
                 }
             }
+            return true;
+        };
+
+        bool ok = true;
+        for (int j = 0; j < P.nqt && ok; ++j) {
+            const uint32_t ph = (uint32_t)j & 1u;
+            const int q0 = j * kBM, st = j % P.qs;
+            const float* lse_s = reinterpret_cast<const float*>(gbase + L.lse + (uint32_t)st * 1024u);
+            const float* del_s = lse_s + 128;
+            ok = __all_sync(0xffffffffu, wait_bar(lse_full(st), (uint32_t)(j / P.qs) & 1u, abort_flag, P.status));
+            if (!ok) break;
+            for (int hh = 0; hh < 2 && ok; ++hh) {
+                ok = __all_sync(0xffffffffu, wait_bar(bias_full(hh), ph, abort_flag, P.status));
+                if (!ok) break;
+                ok = __all_sync(0xffffffffu, wait_bar(s_full(hh), ph, abort_flag, P.status));
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t tSh = tS + 64u * (uint32_t)hh, tDPh = tDP + 64u * (uint32_t)hh;
+                // Chunks of 16 queries: ql = the query row within the tile, col = the column in
+                // the half's buffers.  P^T and dS^T (16-bit pairs) go over the chunk's first 8
+                // columns, which this warp has read already.
+                constexpr int CW = 16;
+#pragma unroll 1
+                for (int c = 0; c < 2; ++c) {
+                    const int ql = 64 * hh + 32 * hq + CW * c;
+                    const uint32_t col = (uint32_t)(32 * hq + CW * c);
+                    uint32_t sr[CW], dr[CW];
+                    tmem_ld_x16(tSh + lane_off + col, sr);
+                    tmem_ld_x16(tDPh + lane_off + col, dr);
+                    // The chunk's lse and delta (shared-memory broadcasts, four at a time) and this
+                    // key's bias column: query row ql + i lives at bcb + 128 i + xo[i % 8].
+                    float ls[CW], dl[CW];
+#pragma unroll
+                    for (int i = 0; i < CW; i += 4) {
+                        const float4 l4 = *reinterpret_cast<const float4*>(lse_s + ql + i);
+                        const float4 d4 = *reinterpret_cast<const float4*>(del_s + ql + i);
+                        ls[i] = l4.x, ls[i + 1] = l4.y, ls[i + 2] = l4.z, ls[i + 3] = l4.w;
+                        dl[i] = d4.x, dl[i + 1] = d4.y, dl[i + 2] = d4.z, dl[i + 3] = d4.w;
+                    }
+                    const uint8_t* bcb = gbase + (bias_half(hh) - base) + bbox_off + (uint32_t)(ql - 64 * hh) * 128u;
+                    const int nq = P.Q - (q0 + ql);  // queries of the chunk that exist
+                    uint32_t pp[CW / 2], dd[CW / 2];
+                    if (__all_sync(0xffffffffu, valid) && nq >= CW) {
+                        // Every key of the warp valid and every query of the chunk present: each row
+                        // has a valid key, so its lse is a plain log-sum-exp and P = 2^(x log2e - lse log2e).
+                        const float2 sl2 = make_float2(P.scale * kLog2e, P.scale * kLog2e);
+                        const float2 l2e2 = make_float2(kLog2e, kLog2e);
+                        float* dbp = dbias_row ? dbias_row + (long long)(q0 + ql) * P.K : nullptr;
+#pragma unroll
+                        for (int i = 0; i < CW; i += 2) {
+                            float2 bv;
+                            if constexpr (BIAS_F32) {
+                                bv = make_float2(*reinterpret_cast<const float*>(bcb + i * 128 + xo[i & 7]),
+                                                 *reinterpret_cast<const float*>(bcb + (i + 1) * 128 + xo[(i + 1) & 7]));
+                            } else {
+                                const uint32_t b0 = *reinterpret_cast<const unsigned short*>(bcb + i * 128 + xo[i & 7]);
+                                const uint32_t b1 =
+                                    *reinterpret_cast<const unsigned short*>(bcb + (i + 1) * 128 + xo[(i + 1) & 7]);
+                                bv = unpack2<BF16>(b0 | (b1 << 16));
+                            }
+                            // y = s S log2e + b log2e - lse log2e
+                            const float2 nl = __fmul2_rn(make_float2(ls[i], ls[i + 1]), make_float2(-kLog2e, -kLog2e));
+                            const float2 y = __ffma2_rn(make_float2(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1])),
+                                                        sl2, __ffma2_rn(bv, l2e2, nl));
+                            const float2 pr = make_float2(ex2(y.x), ex2(y.y));
+                            const float2 ds = __fmul2_rn(
+                                pr, __fadd2_rn(make_float2(__uint_as_float(dr[i]), __uint_as_float(dr[i + 1])),
+                                               make_float2(-dl[i], -dl[i + 1])));
+                            pp[i / 2] = pack2<BF16>(pr.x, pr.y);
+                            dd[i / 2] = pack2<BF16>(ds.x, ds.y);
+                            if (dbp) {
+                                red_add_global(dbp + (long long)i * P.K, ds.x);
+                                red_add_global(dbp + (long long)(i + 1) * P.K, ds.y);
+                            }
+                        }
+                    } else {
+                        // Logits first (every read of the bias tile before any reduction into dBias).
+#pragma unroll
+                        for (int ii = 0; ii < CW; ++ii) {
+                            float x = kMasked;
+                            if (valid) {
+                                const uint8_t* ba = bcb + ii * 128 + xo[ii & 7];
+                                float bv;
+                                if constexpr (BIAS_F32) bv = *reinterpret_cast<const float*>(ba);
+                                else bv = unpack2<BF16>((uint32_t)*reinterpret_cast<const unsigned short*>(ba)).x;
+                                x = fmaf(P.scale, __uint_as_float(sr[ii]), bv);
+                            }
+                            sr[ii] = __float_as_uint(x);
+                        }
+                        // P and dS (dS kept in dr for the dBias reduction).
+#pragma unroll
+                        for (int i = 0; i < CW; i += 2) {
+                            float pv[2], sv[2];
+#pragma unroll
+                            for (int u = 0; u < 2; ++u) {
+                                const int ii = i + u;
+                                const bool live = exists && ii < nq;
+                                const float p = live ? bwd_weight(__uint_as_float(sr[ii]), ls[ii], inv_k) : 0.f;
+                                const float ds = (live && valid) ? p * (__uint_as_float(dr[ii]) - dl[ii]) : 0.f;
+                                pv[u] = p;
+                                sv[u] = ds;
+                                dr[ii] = __float_as_uint(ds);
+                            }
+                            pp[i / 2] = pack2<BF16>(pv[0], pv[1]);
+                            dd[i / 2] = pack2<BF16>(sv[0], sv[1]);
+                        }
+                        if (dbias_row) {
+#pragma unroll
+                            for (int ii = 0; ii < CW; ++ii)
+                                if (__uint_as_float(dr[ii]) != 0.f)
+                                    red_add_global(dbias_row + (long long)(q0 + ql + ii) * P.K, __uint_as_float(dr[ii]));
+                        }
+                    }
+                    tmem_st_x8(tSh + lane_off + col, pp);
+                    tmem_st_x8(tDPh + lane_off + col, dd);
+                    // dS as [key][query] in shared memory (box ql / 64, 16-byte chunks of 8 queries),
+                    // once dQ of the previous tile has read it.
+                    if (j > 0 && hh == 0 && c == 0) {
+                        ok = __all_sync(0xffffffffu, wait_bar(ds_free, (uint32_t)(j - 1) & 1u, abort_flag, P.status));
+                        if (!ok) break;
+                    }
+                    const uint32_t drow = base + L.ds + (uint32_t)(ql / 64) * kBox + (uint32_t)kr * 128u;
+#pragma unroll
+                    for (int g = 0; g < CW / 8; ++g) {
+                        const uint32_t ch = (uint32_t)((ql % 64) / 8 + g);
+                        st_shared_v4(drow + ((ch ^ rsw) << 4), dd[4 * g], dd[4 * g + 1], dd[4 * g + 2], dd[4 * g + 3]);
+                    }
+                }
+                if (!ok) break;
+                __syncwarp();  // every lane has read its bias values
+                if (lane == 0) mbar_arrive(bias_empty(hh));
+                tmem_st_wait();
+                fence_async_shared();  // dS in shared memory is read by the tensor core
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(p_full(hh));
+                // dQ of the previous tile, between this tile's halves (its MMAs ran meanwhile)
+                if (hh == 0 && j > 0) ok = readout(j - 1);
+            }
         }
+        if (ok && P.nqt > 0) ok = readout(P.nqt - 1);
         if (ok) ok = __all_sync(0xffffffffu, wait_bar(fin, 0, abort_flag, P.status));
         if (ok && hq == 0) {
             tc_fence_after();
@@ -560,7 +610,7 @@ cudaError_t launch_tc_bwd_main(const BwdParams& p, cudaStream_t stream) {
         encode_map_3d(&P.tm_k, dt, p.k, D, p.K, units, rs, rs * p.K, 64, kBN, 1, sw128) &&
         encode_map_3d(&P.tm_v, dt, p.v, D, p.K, units, rs, rs * p.K, 64, kBN, 1, sw128) &&
         encode_map_3d(&P.tm_bias, p.bias_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : dt, p.bias, p.K, p.Q,
-                      (uint64_t)p.B * p.H, p.K * eb, p.K * eb * p.Q, P.bias_box_cols, kBM, 1, sw128) &&
+                      (uint64_t)p.B * p.H, p.K * eb, p.K * eb * p.Q, P.bias_box_cols, kBM / 2, 1, sw128) &&
         encode_map_3d(&P.tm_dq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.dq_acc, D, p.Q, units, (uint64_t)D * 4,
                       (uint64_t)D * 4 * p.Q, inner, 32, 1, inner == 32 ? sw128 : CU_TENSOR_MAP_SWIZZLE_64B);
     if (!maps_ok) return cudaErrorInvalidValue;
@@ -583,7 +633,7 @@ cudaError_t launch_tc_bwd_main(const BwdParams& p, cudaStream_t stream) {
     P.nkt = (p.K + kBN - 1) / kBN;
     P.nqt = (p.Q + kBM - 1) / kBM;
     P.ksteps = D / 16;
-    P.idesc_s = bwd_idesc(bf16, 128, 128, false, false);
+    P.idesc_s = bwd_idesc(bf16, 128, 64, false, false);  // 64 queries (one half of the tile)
     P.idesc_g = bwd_idesc(bf16, 128, D, false, true);
     P.idesc_q = bwd_idesc(bf16, 128, D, true, true);
     const long long grid = (long long)units * P.nkt;
