@@ -240,6 +240,20 @@ def test_varlen_key_lengths_differ_with_lists():
     check_varlen(c)
 
 
+@pytest.mark.parametrize("D", [64, 128])
+def test_varlen_uneven_q_block_levels(D):
+    """Key-split kernel's deal over (q block level, sequence, head): 60 sequences of 0..900
+    tokens (levels that some sequences do not reach, empty sequences), an odd head count, and
+    more items than two rounds of the grid, so the cursor skips whole levels and ends in the
+    middle of (sequence, head) groups."""
+    g = torch.Generator().manual_seed(12)
+    lengths = torch.randint(0, 901, (60,), generator=g).tolist()
+    lengths[3] = 0
+    lengths[7] = 900
+    c = synth.make_varlen(f"vl_levels_{D}", len(lengths), 0, 0, 3, D, "bf16", seed=585 + D, lengths=lengths)
+    check_varlen(c)
+
+
 def test_varlen_many_short_sequences():
     """More sequences than the key-split kernel's schedule keeps in shared memory (1024): the
     two-tile kernel runs them; lengths 0..40, causal lists."""
