@@ -1134,8 +1134,12 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
             }
             if (o_tma) {
                 // Both warps of the lane quarter have staged their columns: one store of
-                // 32 rows x D (rows past Q are not written).
+                // 32 rows x D (rows past Q are not written).  The rendezvous is the lane
+                // quarter's hardware barrier; a warp enters it only while the CTA is not
+                // aborting, and a warp that leaves on an abort arrives on it once (below),
+                // so its partner is never left waiting.
                 fence_async_shared();
+                if (*abort_flag) return ok = false;
                 named_barrier(1 + wq, 64);
                 if (h == 0 && lane == 0 && pe.box_row < a.Q) {
                     tma_store_3d(&P.tm_o, base + L.ostage + (uint32_t)(wq * 32 * P.o_rowb), 0, pe.box_row,
@@ -1432,7 +1436,11 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
         }
         if (ok && pend) ok = epilogue(true);
         if (P.o_tma && h == 0 && lane == 0) bulk_wait_all();  // this lane quarter's O stores are done
-        if (!ok) *abort_flag = 1;
+        if (!ok) {
+            *abort_flag = 1;
+            // Release a partner that entered the staging barrier before the abort was raised.
+            if (kSplitO && P.o_tma) named_barrier_arrive(1 + wq, 64);
+        }
     }
 
     // ---------------------------------------------------------------- teardown
