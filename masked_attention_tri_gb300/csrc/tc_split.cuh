@@ -95,8 +95,8 @@ __host__ __device__ inline SplitLayout make_split_layout(const TcParams& P) {
     L.bars = L.ring + (P.a.varlen ? (uint32_t)(16 * kRing + kRing * sizeof(VEntry)) : 0u);
     // q_full, q_empty (QB each), k_full, k_empty, v_full, v_empty (S each),
     // bias_full, bias_empty (BS each), s_full[s_bufs], p_full[s_bufs],
-    // pv_done[2], xchg[4], drain, o_empty
-    L.nbars = 2 * P.q_bufs + 4 * P.kv_stages + 2 * P.bias_stages + 2 * P.s_bufs + 2 + 4 + 1 + 1;
+    // pv_done[2], drain, o_empty
+    L.nbars = 2 * P.q_bufs + 4 * P.kv_stages + 2 * P.bias_stages + 2 * P.s_bufs + 2 + 1 + 1;
     L.tmem_slot = L.bars + 8 * L.nbars;
     L.abort_flag = L.tmem_slot + 4;
     L.total = L.abort_flag + 4;
@@ -524,9 +524,8 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
     auto s_full = [&](int b) { return bar(bx0 + b); };
     auto p_full = [&](int b) { return bar(bx0 + SB + b); };
     auto pv_done = [&](uint32_t n) { return bar(bx0 + 2 * SB + (int)(n & 1u)); };  // PV n: phase n / 2 of barrier n % 2
-    auto xchg = [&](int q) { return bar(bx0 + 2 * SB + 2 + q); };
-    const uint32_t drain = bar(bx0 + 2 * SB + 6);
-    const uint32_t o_empty = bar(bx0 + 2 * SB + 7);  // one O accumulator: the softmax has read it
+    const uint32_t drain = bar(bx0 + 2 * SB + 2);
+    const uint32_t o_empty = bar(bx0 + 2 * SB + 3);  // one O accumulator: the softmax has read it
     const RingRef ring = {base + L.ring, abort_flag};
     auto ring_full = [&](int i) { return base + L.ring + 8u * (uint32_t)i; };
     auto ring_empty = [&](int i) { return base + L.ring + 8u * (uint32_t)(kRing + i); };
@@ -581,7 +580,6 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
         }
         mbar_init(pv_done(0), 1);
         mbar_init(pv_done(1), 1);
-        for (int q = 0; q < 4; ++q) mbar_init(xchg(q), 2);  // the two warps of a lane quarter
         mbar_init(drain, 1);
         mbar_init(o_empty, 8);  // one arrival per softmax warp
         if (VARLEN) {
@@ -927,13 +925,20 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
         // Swap a value with the partner warp of this lane quarter (bounded wait).
         // The fences order this warp's tensor-memory loads before the partner's
         // later stores (P of key half 1 lands in half 0's logit columns).
+        // Rendezvous of the two warps of this lane quarter on their hardware barrier.  A warp
+        // enters it only while the CTA is not aborting, and a warp that leaves on an abort
+        // arrives on it once (at the end of this role), so a partner that entered just before
+        // the abort is released: this wait without a time limit cannot hang.
+        auto pair_sync = [&]() -> bool {
+            if (__any_sync(0xffffffffu, *abort_flag != 0)) return false;
+            named_barrier(1 + wq, 64);
+            return true;
+        };
         auto swap = [&](float* buf, float v) -> float {
             buf[h * 128 + r] = v;
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(xchg(wq));
-            const bool w_ok = __all_sync(0xffffffffu, wait_bar(xchg(wq), x_it & 1, abort_flag, a.status));
-            ++x_it;
+            const bool w_ok = pair_sync();
             tc_fence_after();
             if (!w_ok) {
                 ok = false;
@@ -1021,10 +1026,8 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
                 // item's O store must have read them by then.
                 if (P.o_tma && h == 0 && lane == 0) bulk_wait_read_all();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(xchg(wq));
-                const bool w_ok = __all_sync(0xffffffffu, wait_bar(xchg(wq), x_it & 1, abort_flag, a.status));
+                if (!pair_sync()) return ok = false;
                 ++x_it;
-                if (!w_ok) return ok = false;
                 const int o3 = (1 - h) * 3;
                 const float m_oth = xe[(o3 + 0) * 128 + r], l_oth = xe[(o3 + 1) * 128 + r];
                 const float mt_oth = xe[(o3 + 2) * 128 + r];
@@ -1134,13 +1137,9 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
             }
             if (o_tma) {
                 // Both warps of the lane quarter have staged their columns: one store of
-                // 32 rows x D (rows past Q are not written).  The rendezvous is the lane
-                // quarter's hardware barrier; a warp enters it only while the CTA is not
-                // aborting, and a warp that leaves on an abort arrives on it once (below),
-                // so its partner is never left waiting.
+                // 32 rows x D (rows past Q are not written).
                 fence_async_shared();
-                if (*abort_flag) return ok = false;
-                named_barrier(1 + wq, 64);
+                if (!pair_sync()) return ok = false;
                 if (h == 0 && lane == 0 && pe.box_row < a.Q) {
                     tma_store_3d(&P.tm_o, base + L.ostage + (uint32_t)(wq * 32 * P.o_rowb), 0, pe.box_row,
                                  pe.box_unit);
@@ -1438,8 +1437,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1) tc_split_kernel(const __grid
         if (P.o_tma && h == 0 && lane == 0) bulk_wait_all();  // this lane quarter's O stores are done
         if (!ok) {
             *abort_flag = 1;
-            // Release a partner that entered the staging barrier before the abort was raised.
-            if (kSplitO && P.o_tma) named_barrier_arrive(1 + wq, 64);
+            named_barrier_arrive(1 + wq, 64);  // releases a partner inside pair_sync
         }
     }
 
