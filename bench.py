@@ -117,9 +117,17 @@ def triangle_work(c, slabs=None):
     return flops, byts
 
 
-def varlen_work(c):
+def varlen_work(c, window=0):
+    """(effective flops, algorithmic bytes) of a packed workload: causal, sliding window (q - window
+    < k <= q: sum over q of min(q + 1, window) pairs per sequence) or every pair."""
     L = c.lengths.to(torch.int64)
-    pairs = float((L * (L + 1) // 2).sum()) if c.mask_mod == "causal" else float((L * L).sum())
+    if c.mask_mod == "sliding_window":
+        W = int(window)
+        pairs = float(sum(min(n, W) * (min(n, W) + 1) // 2 + max(n - W, 0) * W for n in L.tolist()))
+    elif c.mask_mod == "causal":
+        pairs = float((L * (L + 1) // 2).sum())
+    else:
+        pairs = float((L * L).sum())
     e = ESIZE[c.dtype]
     total = float(L.sum())
     flops = 4.0 * c.H * c.D * pairs
@@ -303,7 +311,7 @@ def shard_case(c, world, rank):
                               sl(c.v), c.bias, sl(c.mask), sl(c.kv_lengths), c.scale)
 
 
-def time_varlen(ta, c, dev, steps, warmup, flush, qkv_packed=False):
+def time_varlen(ta, c, dev, steps, warmup, flush, qkv_packed=False, window=0):
     """Device time (ms) per launch of the packed-sequence forward, L2 flushed before each launch.
 
     qkv_packed: q, k, v read in place from one (total, 3, H, D) buffer
@@ -328,10 +336,11 @@ def time_varlen(ta, c, dev, steps, warmup, flush, qkv_packed=False):
     else:
         qq, kk, vv = q, k, v
         rs = H * D
-    mm = {"causal": abi.TA_MASK_CAUSAL, "none": abi.TA_MASK_NONE}[c.mask_mod]
+    mm = {"causal": abi.TA_MASK_CAUSAL, "none": abi.TA_MASK_NONE,
+          "sliding_window": abi.TA_MASK_SLIDING_WINDOW}[c.mask_mod]
     argv = (_ptr(qq), _ptr(kk), _ptr(vv), _DT[q.dtype], _ptr(cu), _ptr(cu), len(c.lengths), q.shape[0], k.shape[0],
             c.max_seqlen, c.max_seqlen, H, D, c.scale, _ptr(kn), _ptr(ki), _ptr(fn), _ptr(fi), kn.shape[1],
-            kn.shape[2], ki.shape[3], c.block, c.block, mm, 0, None, 0, None, abi.TA_F32, rs, rs, rs, _ptr(out),
+            kn.shape[2], ki.shape[3], c.block, c.block, mm, window, None, 0, None, abi.TA_F32, rs, rs, rs, _ptr(out),
             _ptr(lse), _ptr(mx),
             torch.cuda.current_stream(dev).cuda_stream)
 
@@ -548,8 +557,9 @@ def run_only(args):
     flush = make_l2_flusher(dev)
     c = synth.WORKLOADS[args.only]()
     if isinstance(c, synth.VarlenCase):
-        f, _ = varlen_work(c)
-        t = time_varlen(ta, c, dev, args.steps, args.warmup, flush)
+        window = 512 if c.mask_mod == "sliding_window" else 0  # the window workload's window
+        f, _ = varlen_work(c, window=window)
+        t = time_varlen(ta, c, dev, args.steps, args.warmup, flush, window=window)
     else:
         f, _ = triangle_work(c)
         t = time_triangle(ta, c, dev, args.steps, args.warmup, flush=flush)
@@ -675,6 +685,24 @@ def main():
             "pct_bf16_peak": 100 * f / (t * 1e-3) / (peaks["bf16_tflops"] * 1e12),
             "two_term_roofline_frac": max(f / (peaks["bf16_tflops"] * 1e12), b / (peaks["hbm_gbs"] * 1e9)) / (t * 1e-3),
             "layout": "one (total, 3, H, D) buffer read in place", "l2": "flushed before each launch"}
+        # The widened rows, measured like the others: a sliding-window BlockMask on the packed
+        # sequences (mask_mod sliding_window, window 512, its block lists) and D = 256.
+        wc = synth.bf16_varlen_window512()
+        f, b = varlen_work(wc, window=512)
+        t = time_varlen(ta, wc, dev, 50, 5, flush, window=512)
+        per_config["bf16_varlen_window512"] = {
+            "us": 1e3 * t, "tflops": f / (t * 1e-3) / 1e12,
+            "pct_bf16_peak": 100 * f / (t * 1e-3) / (peaks["bf16_tflops"] * 1e12),
+            "two_term_roofline_frac": max(f / (peaks["bf16_tflops"] * 1e12), b / (peaks["hbm_gbs"] * 1e9)) / (t * 1e-3),
+            "mask": "sliding window of 512 keys (valid pairs counted)", "l2": "flushed before each launch"}
+        dc = synth.bf16_d256()
+        f, b = triangle_work(dc)
+        t = time_triangle(ta, dc, dev, 20, 3, flush=flush)
+        per_config["bf16_d256"] = {"us": 1e3 * t, "tflops": f / (t * 1e-3) / 1e12,
+                                   "pct_bf16_peak": 100 * f / (t * 1e-3) / (peaks["bf16_tflops"] * 1e12),
+                                   "two_term_roofline_frac": max(f / (peaks["bf16_tflops"] * 1e12),
+                                                                 b / (peaks["hbm_gbs"] * 1e9)) / (t * 1e-3),
+                                   "path": "CUDA cores (fp32 arithmetic, D > 128)", "l2": "flushed before each launch"}
         per_config["bf16_long"] = {"us": 1e3 * ms, "tflops": flops / (ms * 1e-3) / 1e12,
                                    "pct_bf16_peak": 100 * flops / (ms * 1e-3) / (peaks["bf16_tflops"] * 1e12),
                                    "two_term_roofline_frac": roof["two_term_roofline_frac"],

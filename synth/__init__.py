@@ -205,6 +205,13 @@ def bf16_long() -> TriangleCase:
                          mask="kvlen", kv_range=(0, 768), forced_kv={0: 0, 1: 768})
 
 
+def bf16_d256() -> TriangleCase:
+    """The widest head dimension the forward takes: B=1,N=64,H=4,Q=K=384,D=256 bf16, bias bf16,
+    kv_lengths uniform in [0,384]."""
+    return make_triangle("bf16_d256", 1, 64, 4, 384, 384, 256, "bf16", "bf16", seed=1006,
+                         mask="kvlen", kv_range=(0, 384))
+
+
 TRIANGLE_WORKLOADS = {
     "tiny_fp32": tiny_fp32,
     "fp16_kvlen": fp16_kvlen,
@@ -212,6 +219,7 @@ TRIANGLE_WORKLOADS = {
     "fp16_page_example": fp16_page_example,
     "bf16_pairstack": bf16_pairstack,
     "bf16_long": bf16_long,
+    "bf16_d256": bf16_d256,
 }
 
 
@@ -265,8 +273,9 @@ def make_varlen(
 
     q and k share lengths unless lengths_k gives the key lengths (then
     block_lists must be "none": the causal lists assume equal lengths).
-    block_lists: "causal" (full + partial lists of a causal mask), "none"
-    (no lists: every block visited, mask_mod applied everywhere).
+    block_lists: "causal" (full + partial lists of a causal mask), "window<W>" (the
+    lists of a sliding window of W keys, `window_block_lists`), "none" (no lists:
+    every block visited, mask_mod applied everywhere).
     """
     g = torch.Generator("cpu").manual_seed(seed)
     if lengths is None:
@@ -289,6 +298,8 @@ def make_varlen(
     kv_num = kv_idx = full_num = full_idx = None
     if block_lists == "causal":
         kv_num, kv_idx, full_num, full_idx = causal_block_lists(lengths)
+    elif block_lists.startswith("window"):  # "window<W>": the lists of a sliding window of W keys
+        kv_num, kv_idx, full_num, full_idx = window_block_lists(lengths, int(block_lists[6:]))
     elif block_lists != "none":
         raise ValueError(block_lists)
     s = 1.0 / math.sqrt(D) if scale is None else scale
@@ -299,10 +310,51 @@ def make_varlen(
                       mask_mod, 128, s, max(lengths), lens_k, cu_k, max(lengths_k))
 
 
+def window_block_lists(lengths: list[int], window: int, block: int = 128, mask_heads: int = 1):
+    """Block lists of a causal sliding-window mask (keys q - window < k <= q) over equal-length
+    q/k sequences, in the layout of `causal_block_lists`: kv-block j of q-block i is full when
+    every (q, k) pair of the two blocks' extents is kept, partial when some pair is, unlisted
+    otherwise."""
+    if window < 1:
+        raise ValueError("window must be >= 1")
+    S = len(lengths)
+    nbs = [(L + block - 1) // block for L in lengths]
+    MQ = max(1, max(nbs))
+    MK = MQ
+    kv_num = torch.zeros(S, mask_heads, MQ, dtype=torch.int32)
+    kv_idx = torch.zeros(S, mask_heads, MQ, MK, dtype=torch.int32)
+    full_num = torch.zeros(S, mask_heads, MQ, dtype=torch.int32)
+    full_idx = torch.zeros(S, mask_heads, MQ, MK, dtype=torch.int32)
+    for s, nb in enumerate(nbs):
+        for i in range(nb):
+            a0, a1 = i * block, i * block + block - 1  # query rows of block i
+            part, full = [], []
+            for j in range(i + 1):
+                b0, b1 = j * block, j * block + block - 1  # keys of block j
+                if not (b0 <= a1 and b1 > a0 - window):
+                    continue
+                (full if (b1 <= a0 and b0 > a1 - window) else part).append(j)
+            kv_num[s, :, i] = len(part)
+            full_num[s, :, i] = len(full)
+            if part:
+                kv_idx[s, :, i, :len(part)] = torch.tensor(part, dtype=torch.int32)
+            if full:
+                full_idx[s, :, i, :len(full)] = torch.tensor(full, dtype=torch.int32)
+    return kv_num, kv_idx, full_num, full_idx
+
+
 def bf16_varlen() -> VarlenCase:
     """8 sequences, lengths uniform in [256,2048], H=8, D=128 bf16, no bias, causal BlockMask."""
     return make_varlen("bf16_varlen", 8, 256, 2048, 8, 128, "bf16", seed=1005)
 
 
+def bf16_varlen_window512() -> VarlenCase:
+    """The bf16_varlen sequences under a sliding window of 512 keys (mask_mod sliding_window,
+    the window's block lists)."""
+    return make_varlen("bf16_varlen_window512", 8, 256, 2048, 8, 128, "bf16", seed=1005,
+                       mask_mod="sliding_window", block_lists="window512")
+
+
 WORKLOADS = dict(TRIANGLE_WORKLOADS)
 WORKLOADS["bf16_varlen"] = bf16_varlen
+WORKLOADS["bf16_varlen_window512"] = bf16_varlen_window512

@@ -56,6 +56,17 @@ def test_bf16_varlen_full():
     check_varlen(synth.bf16_varlen())
 
 
+def test_bf16_varlen_window512_full():
+    """The benchmark's sliding-window workload (the bf16_varlen sequences, window 512 with its
+    block lists), every row."""
+    check_varlen(synth.bf16_varlen_window512(), window=512)
+
+
+def test_bf16_d256_full():
+    """The benchmark's D = 256 workload (CUDA-core kernel), every row."""
+    check_triangle(synth.bf16_d256())
+
+
 # ---------------------------------------------------------------------------
 # Edge cases: ragged tiles, head dimensions, kv_lengths extremes
 # ---------------------------------------------------------------------------

@@ -552,6 +552,35 @@ def test_varlen_sliding_window_with_block_lists():
     np.testing.assert_allclose(O, _varlen_sdpa_pairs(c, keep), atol=1e-12)
 
 
+@pytest.mark.parametrize("window", [1, 100, 128, 129, 300])
+def test_window_block_lists_give_banded_attention(window):
+    """The sliding-window block lists of the input generator (full where the whole block pair is
+    inside the band, partial where the band's edge or the diagonal crosses it) with mask_mod
+    sliding_window reproduce the banded attention q - W < k <= q exactly (fp64 SDPA with the
+    band built here), so skipping unlisted blocks loses nothing."""
+    lengths = [400, 129, 1, 260]
+    c = synth.make_varlen("t", 4, 0, 0, 2, 8, "f32", seed=38, lengths=lengths, mask_mod="sliding_window",
+                          block_lists=f"window{window}")
+    O, L, M = oracle.varlen_fwd(c.q, c.k, c.v, c.cu_seqlens, c.cu_seqlens, c.scale, c.kv_num_blocks, c.kv_indices,
+                                c.full_kv_num_blocks, c.full_kv_indices, mask_mod="sliding_window", window=window)
+
+    def keep(i, h, nq, nk):
+        qi = torch.arange(nq).view(-1, 1)
+        kj = torch.arange(nk).view(1, -1)
+        return (kj <= qi) & (qi - kj < window)
+
+    np.testing.assert_allclose(O, _varlen_sdpa_pairs(c, keep), atol=1e-12)
+    # the lists are minimal: every listed block pair holds a kept (q, k) pair of the band
+    for i, Lq in enumerate(lengths):
+        nb = (Lq + 127) // 128
+        for qb in range(nb):
+            listed = [int(x) for x in c.kv_indices[i, 0, qb, :int(c.kv_num_blocks[i, 0, qb])]]
+            listed += [int(x) for x in c.full_kv_indices[i, 0, qb, :int(c.full_kv_num_blocks[i, 0, qb])]]
+            assert len(listed) == len(set(listed))
+            for kb in listed:
+                assert kb * 128 <= qb * 128 + 127 and kb * 128 + 127 > qb * 128 - window
+
+
 @pytest.mark.parametrize("prefix", [0, 1, 50, 129, [10, 0, 400]])
 def test_varlen_prefix_lm_equals_prefix_plus_causal(prefix):
     """mask_mod prefix_lm(P): query q keeps keys k <= q or k < P (the prefix is seen by every
