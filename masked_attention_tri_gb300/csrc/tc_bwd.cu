@@ -15,16 +15,16 @@
 //     dQ_j = dS K      (per tile: A = dS from shared memory, M = queries, MN-major;
 //                       B = K read MN-major)                          TMEM [256 + 2D, 256 + 3D)
 // The two halves use separate S^T / dP^T columns, so the tensor core computes one
-// half's S^T / dP^T while the compute warps work on the other.  Warps 0-7 (one thread
-// per key row = TMEM lane; warps w and w + 4 take 32 queries each of every half) turn
-// S^T and dP^T into P^T and dS^T (16-bit pairs written over the columns just read; dS
-// also into shared memory as the A operand of dQ) and add dS to the fp32 dBias
-// accumulator (coalesced over keys); between the halves of tile j each reads its 32
-// columns of dQ_{j-1} (one thread per query row) and adds them to the fp32 dQ
-// accumulator with a TMA reduce-add; warps 0-3 write dK and dV at the end.
-// Warp 8 loads K and V once and, per query tile, Q, dO, the rows' lse / delta and
-// the two bias halves (each as soon as the previous tile's half is read); warp 9
-// issues the MMAs.  Every wait is bounded (TA_ERR_TIMEOUT).
+// half's S^T / dP^T while the compute warps work on the other.  Warps 0-15 (one thread
+// per key row = TMEM lane; the four warps w, w + 4, w + 8, w + 12 of a lane quarter take
+// 16 queries each of every half) turn S^T and dP^T into P^T and dS^T (16-bit pairs
+// written over the columns just read; dS also into shared memory as the A operand of
+// dQ) and add dS to the fp32 dBias accumulator (coalesced over keys); between the
+// halves of tile j each reads its 16 columns of dQ_{j-1} (one thread per query row)
+// and adds them to the fp32 dQ accumulator with a TMA reduce-add, and at the end
+// writes its 16 columns of dK and dV.  Warp 16 loads K and V once and, per query tile,
+// Q, dO, the rows' lse / delta and the two bias halves (each as soon as the previous
+// tile's half is read); warp 17 issues the MMAs.  Every wait is bounded (TA_ERR_TIMEOUT).
 
 #include "tc_kernel.cuh"
 
@@ -68,8 +68,8 @@ __host__ __device__ inline BwdLayout bwd_layout(const BwdTc& P) {
     L.q = L.v + kBox;
     L.ds = L.q + (uint32_t)P.qs * 2 * kBox;  // dS as [key][query]: two 64-query boxes
     L.bias = L.ds + 2 * kBox;
-    L.dqst = L.bias + P.bias_bytes;          // dQ staging: 4 lane quarters x 32 rows x D fp32
-    L.lse = L.dqst + 4u * 32u * (uint32_t)P.D * 4u;
+    L.dqst = L.bias + P.bias_bytes;          // dQ staging: 16 compute warps x 32 rows x 16 fp32
+    L.lse = L.dqst + 16u * 2048u;
     L.bars = L.lse + (uint32_t)P.qs * 1024u;
     L.tmem_slot = L.bars + 8 * kBwdBars;
     L.abort_flag = L.tmem_slot + 4;
@@ -98,7 +98,12 @@ __device__ __forceinline__ float bwd_weight(float x, float lse, float inv_k) {
     return lse <= kMasked + 64.f ? inv_k : __expf(x - lse);
 }
 
-constexpr int kBwdThreads = 10 * 32;
+// Warps 0-15 compute (four per TMEM lane quarter), warp 16 loads, warp 17 issues the MMAs.
+constexpr int kComputeWarps = 16;
+constexpr int kQuarterWarps = kComputeWarps / 4;  // compute warps per TMEM lane quarter
+constexpr int kWarpQ = 64 / kQuarterWarps;        // queries of every 64-query half per warp
+constexpr int kProducerWarp = kComputeWarps, kMmaWarp = kComputeWarps + 1;
+constexpr int kBwdThreads = (kComputeWarps + 2) * 32;
 
 template <bool BF16, bool BIAS_F32>
 __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_constant__ BwdTc P) {
@@ -159,19 +164,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
             mbar_init(q_empty(i), 1);
             mbar_init(lse_full(i), 1);    // the lse / delta rows written
             mbar_init(bias_full(i), 1);
-            mbar_init(bias_empty(i), 8);  // every compute warp has read the bias half
+            mbar_init(bias_empty(i), kComputeWarps);  // every compute warp has read the bias half
             mbar_init(s_full(i), 1);
-            mbar_init(p_full(i), 8);
+            mbar_init(p_full(i), kComputeWarps);
         }
         mbar_init(dq_full, 1);
-        mbar_init(dq_empty, P.D > 32 ? 8 : 4);  // the warps that read dQ_j
+        mbar_init(dq_empty, 4 * ((P.D + 15) / 16));  // the warps that read dQ_j (16 columns each)
         mbar_init(ds_free, 1);
         mbar_init(fin, 1);
         mbar_init(drain, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
-    if (warp == 9) {
+    if (warp == kMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(tmem_slot))
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
@@ -185,7 +190,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
     // place), then dV, dK and dQ_j.
     const uint32_t tS = tmem, tDP = tmem + 128, tDV = tmem + 256, tDK = tmem + 256 + D, tDQ = tmem + 256 + 2 * D;
 
-    if (warp == 8) {
+    if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer
         bool ok = true;
         if (lane == 0) {
@@ -239,7 +244,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
             ok = bias_load(1);
         }
         if (!ok) *abort_flag = 1;
-    } else if (warp == 9) {
+    } else if (warp == kMmaWarp) {
         // ----------------------------------------------------------------- MMA
         // Per query tile j and half hh (64 queries): S^T and dP^T of (j, hh) into buffer hh;
         // once P^T / dS^T of (j, hh) are written, dV and dK take them, then S^T / dP^T of
@@ -324,7 +329,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
     } else {
         // ------------------------------------------------------------- compute
         const int wq = warp & 3;          // TMEM lane quarter: keys (and later query rows) 32 wq ..
-        const int hq = warp >> 2;         // within each 64-query half: queries 32 hq .. 32 hq + 31
+        const int hq = warp >> 2;         // within each 64-query half: queries kWarpQ hq .. + kWarpQ - 1
         const int kr = wq * 32 + lane;    // key row of the tile
         const int key = k0 + kr;
         const bool exists = key < P.K;
@@ -349,46 +354,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
 #pragma unroll
         for (int r8 = 0; r8 < 8; ++r8) xo[r8] = ((((bcol_b >> 4) ^ (uint32_t)r8)) << 4) + (bcol_b & 15u);
         float* dbias_row = P.dbias_acc ? P.dbias_acc + ((long long)b * P.H + h) * P.Q * (long long)P.K + key : nullptr;
-        // dQ staging of this lane quarter: boxes of `inner` fp32 columns x 32 rows, swizzled by their row width
-        const int inner = P.D < 32 ? P.D : 32;
-        const uint32_t rowb = (uint32_t)inner * 4u;
-        const uint32_t dq_stage = base + L.dqst + (uint32_t)(wq * 32 * P.D * 4);
-        const uint32_t qsw = rowb == 128 ? (uint32_t)(lane & 7) : (uint32_t)((lane >> 1) & 3);
+        // dQ staging of this warp: 32 rows x 16 fp32 (64-byte rows, 64B-swizzled)
+        const uint32_t dq_stage = base + L.dqst + (uint32_t)warp * 2048u;
+        const uint32_t qsw = (uint32_t)((lane >> 1) & 3);
 
-        // dQ_j read out (thread = query row 128 j + 32 wq + lane; warp half hq takes columns
-        // [32 hq, 32 hq + 32), none for D <= 32 and hq = 1) and added into the accumulator.
+        // dQ_j read out (thread = query row 128 j + 32 wq + lane; warp hq takes columns
+        // [16 hq, 16 hq + 16), none past D) and added into the accumulator.
         auto readout = [&](int jr) -> bool {
-            const int dc0 = 32 * hq, dc1 = P.D < dc0 + 32 ? P.D : dc0 + 32;
+            const int dc0 = 16 * hq;
             if (dc0 >= P.D) return true;
             if (!__all_sync(0xffffffffu, wait_bar(dq_full, (uint32_t)jr & 1u, abort_flag, P.status))) return false;
             tc_fence_after();
-            if (lane == 0) bulk_wait_read_all();  // the previous reduce has read the staging rows
-            __syncwarp();
-#pragma unroll 1
-            for (int d0 = dc0; d0 < dc1; d0 += 16) {
-                uint32_t o[16];
-                tmem_ld_x16(tDQ + lane_off + (uint32_t)d0, o);
-                const int bxi = d0 / inner, cb = (d0 % inner) / 4;  // box, first 16-byte chunk in it
-                const uint32_t rowa = dq_stage + (uint32_t)bxi * 32u * rowb + (uint32_t)lane * rowb;
-#pragma unroll
-                for (int g = 0; g < 4; ++g)
-                    st_shared_v4(rowa + ((((uint32_t)(cb + g)) ^ qsw) << 4),
-                                 __float_as_uint(__uint_as_float(o[4 * g]) * P.scale),
-                                 __float_as_uint(__uint_as_float(o[4 * g + 1]) * P.scale),
-                                 __float_as_uint(__uint_as_float(o[4 * g + 2]) * P.scale),
-                                 __float_as_uint(__uint_as_float(o[4 * g + 3]) * P.scale));
-            }
+            uint32_t o[16];
+            tmem_ld_x16(tDQ + lane_off + (uint32_t)dc0, o);
             tc_fence_before();
-            fence_async_shared();
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(dq_empty);
-                if (jr * kBM + 32 * wq < P.Q) {
-                    for (int bxi = dc0 / inner; bxi * inner < dc1; ++bxi)
-                        tma_reduce_add_3d(&P.tm_dq, dq_stage + (uint32_t)bxi * 32u * rowb, bxi * inner,
-                                          jr * kBM + 32 * wq, (int)unit);
-                    bulk_commit();
-                }
+                mbar_arrive(dq_empty);    // the accumulator is read
+                bulk_wait_read_all();     // the previous reduce has read the staging rows
+            }
+            __syncwarp();
+            const uint32_t rowa = dq_stage + (uint32_t)lane * 64u;
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+                st_shared_v4(rowa + ((((uint32_t)g) ^ qsw) << 4), __float_as_uint(__uint_as_float(o[4 * g]) * P.scale),
+                             __float_as_uint(__uint_as_float(o[4 * g + 1]) * P.scale),
+                             __float_as_uint(__uint_as_float(o[4 * g + 2]) * P.scale),
+                             __float_as_uint(__uint_as_float(o[4 * g + 3]) * P.scale));
+            fence_async_shared();
+            __syncwarp();
+            if (lane == 0 && jr * kBM + 32 * wq < P.Q) {
+                tma_reduce_add_3d(&P.tm_dq, dq_stage, dc0, jr * kBM + 32 * wq, (int)unit);
+                bulk_commit();
             }
             return true;
         };
@@ -413,9 +410,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
                 // columns, which this warp has read already.
                 constexpr int CW = 16;
 #pragma unroll 1
-                for (int c = 0; c < 2; ++c) {
-                    const int ql = 64 * hh + 32 * hq + CW * c;
-                    const uint32_t col = (uint32_t)(32 * hq + CW * c);
+                for (int c = 0; c < kWarpQ / CW; ++c) {
+                    const int ql = 64 * hh + kWarpQ * hq + CW * c;
+                    const uint32_t col = (uint32_t)(kWarpQ * hq + CW * c);
                     uint32_t sr[CW], dr[CW];
                     tmem_ld_x16(tSh + lane_off + col, sr);
                     tmem_ld_x16(tDPh + lane_off + col, dr);
@@ -532,12 +529,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
         }
         if (ok && P.nqt > 0) ok = readout(P.nqt - 1);
         if (ok) ok = __all_sync(0xffffffffu, wait_bar(fin, 0, abort_flag, P.status));
-        if (ok && hq == 0) {
+        if (ok && 16 * hq < P.D) {  // dK and dV columns [16 hq, 16 hq + 16)
             tc_fence_after();
             uint16_t* dkp = static_cast<uint16_t*>(P.dk) + (unit * P.K + key) * (long long)P.D;
             uint16_t* dvp = static_cast<uint16_t*>(P.dv) + (unit * P.K + key) * (long long)P.D;
-#pragma unroll 1
-            for (int d0 = 0; d0 < P.D; d0 += 16) {
+            {
+                const int d0 = 16 * hq;
                 uint32_t ov[16], ok16[16];
                 tmem_ld_x16(tDV + lane_off + (uint32_t)d0, ov);
                 tmem_ld_x16(tDK + lane_off + (uint32_t)d0, ok16);
@@ -560,13 +557,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
     }
 
     // ---------------------------------------------------------------- teardown
-    if (warp == 8 && lane == 0 && *abort_flag) {
+    if (warp == kProducerWarp && lane == 0 && *abort_flag) {
 #pragma unroll 1
         for (int i = 0; i < 2000; ++i) __nanosleep(1000);  // TMA loads already issued land first
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
     }
@@ -603,7 +600,6 @@ cudaError_t launch_tc_bwd_main(const BwdParams& p, cudaStream_t stream) {
     P.bias_boxes = kBN / P.bias_box_cols;
     P.bias_bytes = (uint32_t)P.bias_boxes * kBox;
     const uint64_t eb = p.bias_f32 ? 4 : 2;
-    const int inner = D < 32 ? D : 32;  // fp32 dQ columns per reduce box (128 or 64 bytes)
     const bool maps_ok =
         encode_map_3d(&P.tm_q, dt, p.q, D, p.Q, units, rs, rs * p.Q, 64, kBM, 1, sw128) &&
         encode_map_3d(&P.tm_do, dt, p.d_out, D, p.Q, units, rs, rs * p.Q, 64, kBM, 1, sw128) &&
@@ -612,7 +608,7 @@ cudaError_t launch_tc_bwd_main(const BwdParams& p, cudaStream_t stream) {
         encode_map_3d(&P.tm_bias, p.bias_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : dt, p.bias, p.K, p.Q,
                       (uint64_t)p.B * p.H, p.K * eb, p.K * eb * p.Q, P.bias_box_cols, kBM / 2, 1, sw128) &&
         encode_map_3d(&P.tm_dq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.dq_acc, D, p.Q, units, (uint64_t)D * 4,
-                      (uint64_t)D * 4 * p.Q, inner, 32, 1, inner == 32 ? sw128 : CU_TENSOR_MAP_SWIZZLE_64B);
+                      (uint64_t)D * 4 * p.Q, 16, 32, 1, CU_TENSOR_MAP_SWIZZLE_64B);  // 16 fp32 x 32 rows
     if (!maps_ok) return cudaErrorInvalidValue;
     P.lse = p.lse;
     P.delta = p.delta;
