@@ -55,7 +55,7 @@ def kernel_source_hash() -> str:
     cs = os.path.join(ROOT, "masked_attention_tri_gb300", "csrc")
     files = sorted(glob.glob(os.path.join(cs, "tc_*.cu")) + glob.glob(os.path.join(cs, "tc_*.cuh")) +
                    [os.path.join(cs, "tmem_io.h"), os.path.join(cs, "internal.h")])
-    files = [f for f in files if os.path.basename(f) != "tc_bwd.cu"]
+    files = [f for f in files if os.path.basename(f) not in ("tc_bwd.cu", "tc_wide.cu")]
     h = hashlib.sha256()
     for f in files:
         h.update(os.path.relpath(f, ROOT).encode())
@@ -702,7 +702,7 @@ def main():
                                    "pct_bf16_peak": 100 * f / (t * 1e-3) / (peaks["bf16_tflops"] * 1e12),
                                    "two_term_roofline_frac": max(f / (peaks["bf16_tflops"] * 1e12),
                                                                  b / (peaks["hbm_gbs"] * 1e9)) / (t * 1e-3),
-                                   "path": "CUDA cores (fp32 arithmetic, D > 128)", "l2": "flushed before each launch"}
+                                   "path": "tensor cores, 64-key tiles (D in (128, 256])", "l2": "flushed before each launch"}
         per_config["bf16_long"] = {"us": 1e3 * ms, "tflops": flops / (ms * 1e-3) / 1e12,
                                    "pct_bf16_peak": 100 * flops / (ms * 1e-3) / (peaks["bf16_tflops"] * 1e12),
                                    "two_term_roofline_frac": roof["two_term_roofline_frac"],

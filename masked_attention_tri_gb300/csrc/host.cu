@@ -17,6 +17,10 @@
 
 namespace triattn {
 
+// The triangle form with 16-bit inputs and D in (128, 256] on tensor cores (tc_wide.cu);
+// cudaErrorNotSupported for a case it does not take.
+cudaError_t launch_tc_wide(const AttnParams& a, cudaStream_t stream);
+
 // One status word per device, written by kernels that give up.
 __device__ int g_status_word = 0;
 
@@ -54,11 +58,20 @@ bool supported_d(int dtype, int D) {
     return dtype == TA_F32 ? (D % 4 == 0) : (D % 8 == 0);
 }
 
-// fp32 inputs, and 16-bit inputs with D > 128, run on the CUDA-core kernel; the
-// rest on the tensor-core kernels.
+// fp32 inputs run on the CUDA-core kernel; 16-bit inputs on the tensor-core kernels:
+// D <= 128 on tc_fwd / tc_split, D in (128, 256] on tc_wide (the triangle form with
+// contiguous q / k / v; packed sequences and strided views with D > 128 take the
+// CUDA-core kernel).
 ta_status run(const AttnParams& p, cudaStream_t stream) {
-    cudaError_t e = (p.dtype == TA_F32 || p.D > 128) ? triattn::launch_simt_fwd(p, stream)
-                                                     : triattn::launch_tc_fwd(p, stream);
+    cudaError_t e;
+    if (p.dtype == TA_F32) {
+        e = triattn::launch_simt_fwd(p, stream);
+    } else if (p.D > 128) {
+        e = triattn::launch_tc_wide(p, stream);
+        if (e == cudaErrorNotSupported) e = triattn::launch_simt_fwd(p, stream);
+    } else {
+        e = triattn::launch_tc_fwd(p, stream);
+    }
     return e == cudaSuccess ? TA_OK : TA_ERR_CUDA;
 }
 

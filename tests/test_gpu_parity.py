@@ -122,8 +122,10 @@ def test_dense_mask_wide_heads(D, dtype, bias_dtype):
 
 # Strided q / k / v (the triangle form read in place): a (B,N,Q,H,D) buffer viewed as
 # (B,N,H,Q,D), and rows padded past D; on the key-split kernel (D <= 64), the two-tile
-# kernel (D > 64) and the fp32 CUDA-core kernel.  Same result as the contiguous copy.
-@pytest.mark.parametrize("D,dtype", [(64, "bf16"), (32, "f16"), (128, "bf16"), (16, "f32")])
+# kernel (D > 64), the fp32 CUDA-core kernel and, for 16-bit D > 128 (whose tensor-core
+# kernel takes contiguous tensors only), the CUDA-core kernel.  Same result as the
+# contiguous copy.
+@pytest.mark.parametrize("D,dtype", [(64, "bf16"), (32, "f16"), (128, "bf16"), (16, "f32"), (192, "bf16")])
 def test_triangle_strided_views(D, dtype):
     c = synth.make_triangle(f"strided_D{D}", 2, 3, 2, 150, 136, D, dtype, dtype, seed=720 + D, mask="kvlen",
                             kv_range=(0, 136))
@@ -143,13 +145,17 @@ def test_triangle_strided_views(D, dtype):
     torch.cuda.synchronize()
     assert ta.get_status() == 0
     assert o1.is_contiguous()
-    assert torch.equal(o1, o0) and torch.equal(l1, l0) and torch.equal(m1, m0)
     rO, rL, rM = oracle.tri_fwd(c.q, c.k, c.v, c.bias, kv_lengths=c.kv_lengths, scale=c.scale)
     compare(c.name, c.dtype, o1, l1, m1, rO, rL, rM)
+    if D > 128 and dtype != "f32":  # the views and the contiguous copy take different kernels here
+        compare(c.name + "_contiguous", c.dtype, o0, l0, m0, rO, rL, rM)
+    else:
+        assert torch.equal(o1, o0) and torch.equal(l1, l0) and torch.equal(m1, m0)
 
 
-# D in (128, 256] (the page's forward bound for half precision): the CUDA-core kernel,
-# exact fp32 arithmetic, for every input dtype; ragged tiles and kv_lengths extremes.
+# D in (128, 256] (the page's forward bound for half precision): 16-bit inputs on the
+# tensor-core kernel with 64-key tiles, fp32 on the CUDA-core kernel; ragged tiles and
+# kv_lengths extremes.
 @pytest.mark.parametrize("dtype,bias_dtype,D", [("bf16", "bf16", 136), ("bf16", "f32", 192), ("bf16", "bf16", 256),
                                                 ("f16", "f32", 256), ("f16", "f16", 200), ("f32", "f32", 256)])
 def test_wide_head_dims(dtype, bias_dtype, D):
@@ -162,6 +168,23 @@ def test_wide_head_dims(dtype, bias_dtype, D):
 def test_wide_head_dim_dense_mask():
     c = synth.make_triangle("wide_dense", 2, 2, 2, 33, 80, 256, "bf16", "f32", seed=480, mask="dense")
     c.mask[1, 1] = 0
+    check_triangle(c)
+
+
+# The tensor-core kernel for D in (128, 256] (64-key tiles): more work items than CTAs, several
+# query and key tiles per slab with ragged tails, kv_lengths extremes, and large logits (the
+# lazy O correction over all D columns).
+@pytest.mark.parametrize("dtype,bias_dtype,D", [("bf16", "bf16", 256), ("f16", "f32", 144), ("bf16", "f32", 200)])
+def test_wide_head_dims_many_tiles(dtype, bias_dtype, D):
+    c = synth.make_triangle(f"wide_tiles_{dtype}_{D}", 1, 40, 4, 300, 264, D, dtype, bias_dtype, seed=485 + D,
+                            mask="kvlen", kv_range=(0, 264))
+    c.kv_lengths.view(-1)[:5] = torch.tensor([0, 1, 64, 65, 264], dtype=torch.int32)
+    check_triangle(c)
+
+
+def test_wide_head_dims_large_logits():
+    c = synth.make_triangle("wide_large", 1, 3, 2, 200, 200, 256, "bf16", "bf16", seed=489, bias_std=8.0, scale=0.5,
+                            mask="kvlen", kv_range=(10, 200))
     check_triangle(c)
 
 
