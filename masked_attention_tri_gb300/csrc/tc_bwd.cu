@@ -45,6 +45,7 @@ struct BwdTc {
     float scale;
     int B, N, H, Q, K, D;
     int nkt, nqt, ksteps;
+    int nsub;           // 64-column boxes of D (1, or 2 for D in (64, 128])
     uint32_t idesc_s;   // M 128, N 64: K-major A and B
     uint32_t idesc_g;   // M 128, N D: A from TMEM, B MN-major
     uint32_t idesc_q;   // M 128, N D: A and B MN-major in shared memory
@@ -54,19 +55,22 @@ struct BwdTc {
 };
 
 // Shared memory (offsets from a 1024-byte aligned base).
-// Stage s of the query-tile ring: Q at q + s * 2 kBox, dO after it; lse / delta at lse + s * 1024.
+// Stage s of the query-tile ring: Q at q + s * 2 tile, dO after it; lse / delta at lse + s * 1024
+// (tile = nsub boxes of 128 rows x 128 bytes).
 struct BwdLayout {
     uint32_t k, v, q, ds, bias, dqst, lse, bars, tmem_slot, abort_flag, total;
 };
 // kv_full, q_full[2], q_empty[2], lse_full[2], bias_full[2], bias_empty[2], s_full[2], p_full[2],
 // dq_full, dq_empty, ds_free, fin, drain
 constexpr int kBwdBars = 20;
-__host__ __device__ inline BwdLayout bwd_layout(const BwdTc& P) {
+// nsub: the kernel passes its compile-time box count, so that the offsets fold into constants.
+__host__ __device__ inline BwdLayout bwd_layout(const BwdTc& P, int nsub) {
     BwdLayout L;
+    const uint32_t tile = (uint32_t)nsub * kBox;  // one 128-row tile of D columns
     L.k = 0;
-    L.v = L.k + kBox;
-    L.q = L.v + kBox;
-    L.ds = L.q + (uint32_t)P.qs * 2 * kBox;  // dS as [key][query]: two 64-query boxes
+    L.v = L.k + tile;
+    L.q = L.v + tile;
+    L.ds = L.q + (uint32_t)P.qs * 2 * tile;  // dS as [key][query]: two 64-query boxes
     L.bias = L.ds + 2 * kBox;
     L.dqst = L.bias + P.bias_bytes;          // dQ staging: 16 compute warps x 32 rows x 16 fp32
     L.lse = L.dqst + 16u * 2048u;
@@ -105,13 +109,17 @@ constexpr int kWarpQ = 64 / kQuarterWarps;        // queries of every 64-query h
 constexpr int kProducerWarp = kComputeWarps, kMmaWarp = kComputeWarps + 1;
 constexpr int kBwdThreads = (kComputeWarps + 2) * 32;
 
-template <bool BF16, bool BIAS_F32>
+// WIDE: D in (64, 128] (two 64-column boxes per tile, one S^T / dP^T buffer that the query
+// halves take in turn, 32 columns of dQ / dK / dV per compute warp); otherwise D <= 64.
+template <bool BF16, bool BIAS_F32, bool WIDE>
 __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_constant__ BwdTc P) {
+    constexpr int kNsub = WIDE ? 2 : 1;   // 64-column boxes per 128-row tile
+    constexpr int kCpw = WIDE ? 32 : 16;  // dQ / dK / dV columns per compute warp
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
-    const BwdLayout L = bwd_layout(P);
+    const BwdLayout L = bwd_layout(P, kNsub);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L.abort_flag);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L.tmem_slot);
@@ -125,8 +133,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
     auto s_full = [&](int hh) { return bar(11 + hh); };
     auto p_full = [&](int hh) { return bar(13 + hh); };
     const uint32_t dq_full = bar(15), dq_empty = bar(16), ds_free = bar(17), fin = bar(18), drain = bar(19);
-    auto q_smem = [&](int st) { return base + L.q + (uint32_t)st * 2u * kBox; };
-    auto do_smem = [&](int st) { return base + L.q + (uint32_t)st * 2u * kBox + kBox; };
+    constexpr uint32_t tileb = (uint32_t)kNsub * kBox;
+    auto q_smem = [&](int st) { return base + L.q + (uint32_t)st * 2u * tileb; };
+    auto do_smem = [&](int st) { return base + L.q + (uint32_t)st * 2u * tileb + tileb; };
     // bias rows [64 hh, 64 hh + 64) of the tile: boxes of bias_box_cols keys x 64 rows (8 KB each)
     auto bias_half = [&](int hh) { return base + L.bias + (uint32_t)hh * (P.bias_bytes / 2u); };
 
@@ -169,7 +178,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
             mbar_init(p_full(i), kComputeWarps);
         }
         mbar_init(dq_full, 1);
-        mbar_init(dq_empty, 4 * ((P.D + 15) / 16));  // the warps that read dQ_j (16 columns each)
+        mbar_init(dq_empty, 4 * ((P.D + kCpw - 1) / kCpw));  // the warps that read dQ_j (kCpw columns each)
         mbar_init(ds_free, 1);
         mbar_init(fin, 1);
         mbar_init(drain, 1);
@@ -188,15 +197,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
     const uint32_t D = (uint32_t)P.D;
     // S^T of query half hh at tS + 64 hh, dP^T at tDP + 64 hh (P^T and dS^T written over them in
     // place), then dV, dK and dQ_j.
-    const uint32_t tS = tmem, tDP = tmem + 128, tDV = tmem + 256, tDK = tmem + 256 + D, tDQ = tmem + 256 + 2 * D;
+    // D <= 64: S^T and dP^T of both halves (2 x 64 columns each), then dV, dK, dQ_j (D each).
+    // D > 64: one S^T / dP^T buffer (64 + 64 columns) that the halves take in turn, then dV,
+    // dK, dQ_j (128 columns each).  buf(hh): the S^T / dP^T buffer of half hh.
+    const uint32_t tS = tmem, tDP = tmem + (WIDE ? 64u : 128u);
+    const uint32_t tDV = tmem + (WIDE ? 128u : 256u), tDK = tDV + (WIDE ? 128u : D), tDQ = tDK + (WIDE ? 128u : D);
+    auto buf = [&](int hh) { return WIDE ? 0 : hh; };
+    // the phase of buffer buf(hh) that half hh of query tile j fills
+    auto sphase = [&](int j, int hh) { return WIDE ? (uint32_t)(2 * j + hh) & 1u : (uint32_t)j & 1u; };
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer
         bool ok = true;
         if (lane == 0) {
-            mbar_expect_tx(kv_full, 2 * kBox);
-            tma_load_3d(base + L.k, &P.tm_k, 0, k0, (int)unit, kv_full);
-            tma_load_3d(base + L.v, &P.tm_v, 0, k0, (int)unit, kv_full);
+            mbar_expect_tx(kv_full, 2u * tileb);
+            for (int bx = 0; bx < kNsub; ++bx) {
+                tma_load_3d(base + L.k + (uint32_t)bx * kBox, &P.tm_k, 64 * bx, k0, (int)unit, kv_full);
+                tma_load_3d(base + L.v + (uint32_t)bx * kBox, &P.tm_v, 64 * bx, k0, (int)unit, kv_full);
+            }
         }
         for (int j = 0; j < P.nqt && ok; ++j) {
             const int q0 = j * kBM, st = j % P.qs, use = j / P.qs;
@@ -219,9 +237,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
                 if (!ok) break;
             }
             if (lane == 0) {
-                mbar_expect_tx(q_full(st), 2 * kBox);
-                tma_load_3d(q_smem(st), &P.tm_q, 0, q0, (int)unit, q_full(st));
-                tma_load_3d(do_smem(st), &P.tm_do, 0, q0, (int)unit, q_full(st));
+                mbar_expect_tx(q_full(st), 2u * tileb);
+                for (int bx = 0; bx < kNsub; ++bx) {
+                    tma_load_3d(q_smem(st) + (uint32_t)bx * kBox, &P.tm_q, 64 * bx, q0, (int)unit, q_full(st));
+                    tma_load_3d(do_smem(st) + (uint32_t)bx * kBox, &P.tm_do, 64 * bx, q0, (int)unit, q_full(st));
+                }
             }
             ok = bias_load(0);
             if (!ok) break;
@@ -262,30 +282,46 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
                     return false;
                 tc_fence_after();
             }
-            // rows 64 hh .. 64 hh + 63 of the K-major Q / dO tiles: 8 KB on (a whole number of swizzle atoms)
+            // rows 64 hh .. 64 hh + 63 of the K-major Q / dO tiles: 8 KB on (a whole number of swizzle
+            // atoms); k step kk reads D elements [16 kk, 16 kk + 16): box kk / 4, 32 bytes per step.
             const uint64_t qK = sw128_desc(q_smem(st), 16, 1024) + 512u * (uint32_t)hh;
             const uint64_t doK = sw128_desc(do_smem(st), 16, 1024) + 512u * (uint32_t)hh;
+            const uint32_t b = (uint32_t)buf(hh);
             if (leader) {
+                if constexpr (WIDE) {
+#pragma unroll 1
+                    for (int kk = 0; kk < P.ksteps; ++kk) {  // S^T = K Q^T (D / 16 <= 8 k steps)
+                        const uint64_t ko = (uint64_t)((kk >> 2) * (kBox >> 4) + (kk & 3) * 2);
+                        mma_ss(tS + 64u * b, kK + ko, qK + ko, P.idesc_s, kk > 0 ? 1u : 0u);
+                    }
+#pragma unroll 1
+                    for (int kk = 0; kk < P.ksteps; ++kk) {  // dP^T = V dO^T
+                        const uint64_t ko = (uint64_t)((kk >> 2) * (kBox >> 4) + (kk & 3) * 2);
+                        mma_ss(tDP + 64u * b, vK + ko, doK + ko, P.idesc_s, kk > 0 ? 1u : 0u);
+                    }
+                } else {
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)  // S^T = K Q^T (D / 16 <= 4 k steps)
-                    if (kk < P.ksteps)
-                        mma_ss(tS + 64u * (uint32_t)hh, kK + 2u * (uint32_t)kk, qK + 2u * (uint32_t)kk, P.idesc_s,
-                               kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < 4; ++kk)  // S^T = K Q^T (D / 16 <= 4 k steps)
+                        if (kk < P.ksteps)
+                            mma_ss(tS + 64u * b, kK + 2u * (uint32_t)kk, qK + 2u * (uint32_t)kk, P.idesc_s,
+                                   kk > 0 ? 1u : 0u);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)  // dP^T = V dO^T
-                    if (kk < P.ksteps)
-                        mma_ss(tDP + 64u * (uint32_t)hh, vK + 2u * (uint32_t)kk, doK + 2u * (uint32_t)kk, P.idesc_s,
-                               kk > 0 ? 1u : 0u);
-                mma_commit(s_full(hh));
+                    for (int kk = 0; kk < 4; ++kk)  // dP^T = V dO^T
+                        if (kk < P.ksteps)
+                            mma_ss(tDP + 64u * b, vK + 2u * (uint32_t)kk, doK + 2u * (uint32_t)kk, P.idesc_s,
+                                   kk > 0 ? 1u : 0u);
+                }
+                mma_commit(s_full((int)b));
             }
             return true;
         };
-        if (ok && P.nqt > 0) ok = mma1(0, 0) && mma1(0, 1);
+        if (ok && P.nqt > 0) ok = WIDE ? mma1(0, 0) : (mma1(0, 0) && mma1(0, 1));
         for (int j = 0; j < P.nqt && ok; ++j) {
             const int st = j % P.qs;
             const uint64_t qM = sw128_desc(q_smem(st), kBox, 1024), doM = sw128_desc(do_smem(st), kBox, 1024);
             for (int hh = 0; hh < 2 && ok; ++hh) {
-                ok = __all_sync(0xffffffffu, wait_bar(p_full(hh), (uint32_t)j & 1u, abort_flag, P.status));
+                const uint32_t b = (uint32_t)buf(hh);
+                ok = __all_sync(0xffffffffu, wait_bar(p_full((int)b), sphase(j, hh), abort_flag, P.status));
                 if (!ok) break;
                 tc_fence_after();
                 if (leader) {
@@ -293,8 +329,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
                     for (int kk = 0; kk < 4; ++kk) {  // 16 queries per k step; P^T / dS^T at 16 kk
                         const uint32_t acc = (j > 0 || hh > 0 || kk > 0) ? 1u : 0u;
                         const uint32_t qs16 = (uint32_t)(4 * hh + kk);  // 16-query step within the tile
-                        mma_ts(tDV, tS + 64u * (uint32_t)hh + 16u * (uint32_t)kk, doM + 128u * qs16, P.idesc_g, acc);
-                        mma_ts(tDK, tDP + 64u * (uint32_t)hh + 16u * (uint32_t)kk, qM + 128u * qs16, P.idesc_g, acc);
+                        mma_ts(tDV, tS + 64u * b + 16u * (uint32_t)kk, doM + 128u * qs16, P.idesc_g, acc);
+                        mma_ts(tDK, tDP + 64u * b + 16u * (uint32_t)kk, qM + 128u * qs16, P.idesc_g, acc);
                     }
                 }
                 if (hh == 1) {
@@ -313,7 +349,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
                         mma_commit(q_empty(st));
                     }
                 }
-                if (j + 1 < P.nqt) {
+                if constexpr (WIDE) {  // the single buffer: the other half next (the tensor core runs them in order)
+                    if (hh == 0) ok = mma1(j, 1);
+                    else if (j + 1 < P.nqt) ok = mma1(j + 1, 0);
+                } else if (j + 1 < P.nqt) {
                     if (P.qs > 1) ok = mma1(j + 1, hh);
                     else if (hh == 1) ok = mma1(j + 1, 0) && mma1(j + 1, 1);
                 }
@@ -359,33 +398,64 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
         const uint32_t qsw = (uint32_t)((lane >> 1) & 3);
 
         // dQ_j read out (thread = query row 128 j + 32 wq + lane; warp hq takes columns
-        // [16 hq, 16 hq + 16), none past D) and added into the accumulator.
+        // [kCpw hq, kCpw hq + kCpw), none past D) and added into the accumulator.
         auto readout = [&](int jr) -> bool {
-            const int dc0 = 16 * hq;
+            const int dc0 = kCpw * hq;
             if (dc0 >= P.D) return true;
             if (!__all_sync(0xffffffffu, wait_bar(dq_full, (uint32_t)jr & 1u, abort_flag, P.status))) return false;
             tc_fence_after();
-            uint32_t o[16];
-            tmem_ld_x16(tDQ + lane_off + (uint32_t)dc0, o);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(dq_empty);    // the accumulator is read
-                bulk_wait_read_all();     // the previous reduce has read the staging rows
-            }
-            __syncwarp();
-            const uint32_t rowa = dq_stage + (uint32_t)lane * 64u;
+            if constexpr (!WIDE) {
+                uint32_t o[16];
+                tmem_ld_x16(tDQ + lane_off + (uint32_t)dc0, o);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(dq_empty);    // the accumulator is read
+                    bulk_wait_read_all();     // the previous reduce has read the staging rows
+                }
+                __syncwarp();
+                const uint32_t rowa = dq_stage + (uint32_t)lane * 64u;
 #pragma unroll
-            for (int g = 0; g < 4; ++g)
-                st_shared_v4(rowa + ((((uint32_t)g) ^ qsw) << 4), __float_as_uint(__uint_as_float(o[4 * g]) * P.scale),
-                             __float_as_uint(__uint_as_float(o[4 * g + 1]) * P.scale),
-                             __float_as_uint(__uint_as_float(o[4 * g + 2]) * P.scale),
-                             __float_as_uint(__uint_as_float(o[4 * g + 3]) * P.scale));
-            fence_async_shared();
-            __syncwarp();
-            if (lane == 0 && jr * kBM + 32 * wq < P.Q) {
-                tma_reduce_add_3d(&P.tm_dq, dq_stage, dc0, jr * kBM + 32 * wq, (int)unit);
-                bulk_commit();
+                for (int g = 0; g < 4; ++g)
+                    st_shared_v4(rowa + ((((uint32_t)g) ^ qsw) << 4), __float_as_uint(__uint_as_float(o[4 * g]) * P.scale),
+                                 __float_as_uint(__uint_as_float(o[4 * g + 1]) * P.scale),
+                                 __float_as_uint(__uint_as_float(o[4 * g + 2]) * P.scale),
+                                 __float_as_uint(__uint_as_float(o[4 * g + 3]) * P.scale));
+                fence_async_shared();
+                __syncwarp();
+                if (lane == 0 && jr * kBM + 32 * wq < P.Q) {
+                    tma_reduce_add_3d(&P.tm_dq, dq_stage, dc0, jr * kBM + 32 * wq, (int)unit);
+                    bulk_commit();
+                }
+            } else {
+                const bool rows = jr * kBM + 32 * wq < P.Q;
+#pragma unroll 1
+                for (int pc = 0; pc < kCpw / 16; ++pc) {  // 16 columns at a time through the staging rows
+                    const int d0 = dc0 + 16 * pc;
+                    if (d0 >= P.D) break;
+                    uint32_t o[16];
+                    tmem_ld_x16(tDQ + lane_off + (uint32_t)d0, o);
+                    if (pc + 1 == kCpw / 16 || d0 + 16 >= P.D) {  // the accumulator is read
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(dq_empty);
+                    }
+                    if (lane == 0) bulk_wait_read_all();  // the previous reduce has read the staging rows
+                    __syncwarp();
+                    const uint32_t rowa = dq_stage + (uint32_t)lane * 64u;
+#pragma unroll
+                    for (int g = 0; g < 4; ++g)
+                        st_shared_v4(rowa + ((((uint32_t)g) ^ qsw) << 4), __float_as_uint(__uint_as_float(o[4 * g]) * P.scale),
+                                     __float_as_uint(__uint_as_float(o[4 * g + 1]) * P.scale),
+                                     __float_as_uint(__uint_as_float(o[4 * g + 2]) * P.scale),
+                                     __float_as_uint(__uint_as_float(o[4 * g + 3]) * P.scale));
+                    fence_async_shared();
+                    __syncwarp();
+                    if (lane == 0 && rows) {
+                        tma_reduce_add_3d(&P.tm_dq, dq_stage, d0, jr * kBM + 32 * wq, (int)unit);
+                        bulk_commit();
+                    }
+                }
             }
             return true;
         };
@@ -401,10 +471,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
             for (int hh = 0; hh < 2 && ok; ++hh) {
                 ok = __all_sync(0xffffffffu, wait_bar(bias_full(hh), ph, abort_flag, P.status));
                 if (!ok) break;
-                ok = __all_sync(0xffffffffu, wait_bar(s_full(hh), ph, abort_flag, P.status));
+                ok = __all_sync(0xffffffffu, wait_bar(s_full(buf(hh)), sphase(j, hh), abort_flag, P.status));
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t tSh = tS + 64u * (uint32_t)hh, tDPh = tDP + 64u * (uint32_t)hh;
+                const uint32_t tSh = tS + 64u * (uint32_t)buf(hh), tDPh = tDP + 64u * (uint32_t)buf(hh);
                 // Chunks of 16 queries: ql = the query row within the tile, col = the column in
                 // the half's buffers.  P^T and dS^T (16-bit pairs) go over the chunk's first 8
                 // columns, which this warp has read already.
@@ -522,19 +592,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
                 fence_async_shared();  // dS in shared memory is read by the tensor core
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(p_full(hh));
+                if (lane == 0) mbar_arrive(p_full(buf(hh)));
                 // dQ of the previous tile, between this tile's halves (its MMAs ran meanwhile)
                 if (hh == 0 && j > 0) ok = readout(j - 1);
             }
         }
         if (ok && P.nqt > 0) ok = readout(P.nqt - 1);
         if (ok) ok = __all_sync(0xffffffffu, wait_bar(fin, 0, abort_flag, P.status));
-        if (ok && 16 * hq < P.D) {  // dK and dV columns [16 hq, 16 hq + 16)
+        if (ok && kCpw * hq < P.D) {  // dK and dV columns [kCpw hq, kCpw hq + kCpw)
             tc_fence_after();
             uint16_t* dkp = static_cast<uint16_t*>(P.dk) + (unit * P.K + key) * (long long)P.D;
             uint16_t* dvp = static_cast<uint16_t*>(P.dv) + (unit * P.K + key) * (long long)P.D;
-            {
-                const int d0 = 16 * hq;
+#pragma unroll 1
+            for (int pc = 0; pc < kCpw / 16; ++pc) {
+                const int d0 = kCpw * hq + 16 * pc;
+                if (WIDE && d0 >= P.D) break;
                 uint32_t ov[16], ok16[16];
                 tmem_ld_x16(tDV + lane_off + (uint32_t)d0, ov);
                 tmem_ld_x16(tDK + lane_off + (uint32_t)d0, ok16);
@@ -582,7 +654,17 @@ uint32_t bwd_idesc(bool bf16, int M, int N, bool a_mn, bool b_mn) {
 }  // namespace tc
 
 bool tc_bwd_supported(const BwdParams& p) {
-    return !p.varlen && p.dtype != TA_F32 && (p.D == 16 || p.D == 32 || p.D == 64) && p.K % 8 == 0;
+    if (p.varlen || p.dtype == TA_F32 || p.K % 8 != 0) return false;
+    if (p.D == 16 || p.D == 32 || p.D == 64) return true;
+    if (p.D % 16 != 0 || p.D <= 64 || p.D > 128) return false;
+    // D in (64, 128]: two-box tiles, one Q / dO stage; an fp32 bias tile does not fit beside them.
+    tc::BwdTc t;
+    memset(&t, 0, sizeof(t));
+    t.nsub = 2;
+    t.qs = 1;
+    t.D = p.D;
+    t.bias_bytes = (uint32_t)(tc::kBN / (p.bias_f32 ? 32 : 64)) * tc::kBox;
+    return tc::bwd_layout(t, t.nsub).total + 1024 <= 232448;
 }
 
 cudaError_t launch_tc_bwd_main(const BwdParams& p, cudaStream_t stream) {
@@ -629,6 +711,7 @@ cudaError_t launch_tc_bwd_main(const BwdParams& p, cudaStream_t stream) {
     P.nkt = (p.K + kBN - 1) / kBN;
     P.nqt = (p.Q + kBM - 1) / kBM;
     P.ksteps = D / 16;
+    P.nsub = (D + 63) / 64;
     P.idesc_s = bwd_idesc(bf16, 128, 64, false, false);  // 64 queries (one half of the tile)
     P.idesc_g = bwd_idesc(bf16, 128, D, false, true);
     P.idesc_q = bwd_idesc(bf16, 128, D, true, true);
@@ -636,10 +719,12 @@ cudaError_t launch_tc_bwd_main(const BwdParams& p, cudaStream_t stream) {
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     P.qs = 2;
-    if (bwd_layout(P).total + 1024 > 232448) P.qs = 1;  // the 227 KB per-block limit
-    const size_t smem = bwd_layout(P).total + 1024;
-    auto kern = bf16 ? (p.bias_f32 ? tc_bwd_kernel<true, true> : tc_bwd_kernel<true, false>)
-                     : (p.bias_f32 ? tc_bwd_kernel<false, true> : tc_bwd_kernel<false, false>);
+    if (bwd_layout(P, P.nsub).total + 1024 > 232448) P.qs = 1;  // the 227 KB per-block limit
+    const size_t smem = bwd_layout(P, P.nsub).total + 1024;
+    // D > 64 runs with a 16-bit bias only (tc_bwd_supported)
+    auto kern = D > 64 ? (bf16 ? tc_bwd_kernel<true, false, true> : tc_bwd_kernel<false, false, true>)
+                : bf16 ? (p.bias_f32 ? tc_bwd_kernel<true, true, false> : tc_bwd_kernel<true, false, false>)
+                       : (p.bias_f32 ? tc_bwd_kernel<false, true, false> : tc_bwd_kernel<false, false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     kern<<<(unsigned)grid, kBwdThreads, smem, stream>>>(P);

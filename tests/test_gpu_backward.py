@@ -2,8 +2,9 @@
 
 The oracle (oracle/backward.py) is the chain rule through the triangle_attention
 page's formula, pinned on the CPU by finite differences, torch autograd and
-closed forms.  The library recomputes P from the forward's own lse and works in
-fp32 on CUDA cores; dQ and dBias are summed with fp32 atomics.
+closed forms.  The library recomputes P from the forward's own lse; the per-key-tile
+gradients run on tensor cores (16-bit inputs, D up to 128) or in fp32 on CUDA cores; dQ and
+dBias are summed in fp32.
 
 Tolerance, per gradient g against the oracle r (element-wise):
     |g - r| <= atol * max|r| + rtol * |r|
@@ -71,12 +72,14 @@ def _check(case, seed, **kw):
 
 # dtypes x bias dtypes x masks; ragged Q and K (not multiples of the 32-row tiles), N > 1 for
 # the sum of dBias over n, kv_lengths extremes (0: every key masked, K, beyond K).  16-bit
-# inputs with D in {16, 32, 64} take the tensor-core gradients, the others the CUDA-core
-# kernel; with_out: sum_k P dP from the forward's O instead of the exact pass.
+# inputs with D in {16, 32, 64}, or a multiple of 16 in (64, 128] with a 16-bit bias, take the
+# tensor-core gradients, the others the CUDA-core kernel; with_out: sum_k P dP from the
+# forward's O instead of the exact pass.
 @pytest.mark.parametrize("with_out", [False, True])
 @pytest.mark.parametrize("dtype,bias_dtype,mask,D", [
     ("bf16", "bf16", "kvlen", 64), ("bf16", "f32", "dense", 32), ("f16", "f32", "none", 128),
     ("f16", "f16", "kvlen", 16), ("f32", "f32", "kvlen", 40), ("f32", "f32", "dense", 8),
+    ("bf16", "bf16", "kvlen", 128), ("f16", "f16", "dense", 96), ("bf16", "bf16", "none", 80),
 ])
 def test_backward_matches_oracle(dtype, bias_dtype, mask, D, with_out):
     K = 70 if dtype == "f32" else 72  # 16-bit inputs need K % 8 == 0 (the forward's rule)
@@ -103,22 +106,24 @@ def test_backward_without_dbias_and_large_logits(with_out):
     _check(c, 741, need_dbias=False, with_out=with_out)
 
 
-def test_backward_several_tiles():
-    """Several 128-key and 128-row tiles per slab (ragged), tensor-core gradients, both delta forms."""
-    c = synth.make_triangle("bwd_tiles", 1, 2, 2, 300, 264, 64, "bf16", "bf16", seed=745, mask="kvlen",
+@pytest.mark.parametrize("D", [64, 128])
+def test_backward_several_tiles(D):
+    """Several 128-key and 128-row tiles per slab (ragged), tensor-core gradients (D = 128: the
+    tiles' two column boxes, one S^T / dP^T buffer for both query halves), both delta forms."""
+    c = synth.make_triangle(f"bwd_tiles_{D}", 1, 2, 2, 300, 264, D, "bf16", "bf16", seed=745 + D, mask="kvlen",
                             kv_range=(100, 264))
-    _check(c, 746)
-    _check(c, 747, with_out=True)
+    _check(c, 746 + D)
+    _check(c, 747 + D, with_out=True)
 
 
-@pytest.mark.parametrize("dtype,D", [("bf16", 32), ("f16", 64)])
-def test_backward_padded_key_tiles(dtype, D):
+@pytest.mark.parametrize("dtype,D,bias_dtype", [("bf16", 32, "f32"), ("f16", 64, "f32"), ("bf16", 128, "bf16")])
+def test_backward_padded_key_tiles(dtype, D, bias_dtype):
     """kv_lengths that leave whole 128-key tiles past the valid prefix (their dK / dV are zero and
     they add nothing to dQ or dBias), next to 0 (every key weighted 1 / K), 1, tile edges, K and
     beyond K, and a negative value."""
     K = 264
     lens = [0, 1, 127, 128, 129, 256, 264, 300, -3]
-    c = synth.make_triangle(f"bwd_pad_{dtype}_{D}", 1, len(lens), 2, 140, K, D, dtype, "f32", seed=760 + D,
+    c = synth.make_triangle(f"bwd_pad_{dtype}_{D}", 1, len(lens), 2, 140, K, D, dtype, bias_dtype, seed=760 + D,
                             mask="kvlen", kv_range=(0, K))
     c.kv_lengths.view(-1)[:] = torch.tensor(lens, dtype=torch.int32)
     _check(c, 761 + D)
