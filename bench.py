@@ -296,7 +296,7 @@ def backward_entry(ta, c, dev, peaks, steps=5, warmup=2, with_dbias=True):
     return {"ms": t, "tflops": f / (t * 1e-3) / 1e12,
             "pct_bf16_peak": 100 * f / (t * 1e-3) / (peaks["bf16_tflops"] * 1e12),
             "outputs": "dQ, dK, dV, dBias (summed over N)" if with_dbias else "dQ, dK, dV",
-            "path": "per-row sums from the forward's O, per-key-tile gradients on tcgen05 (16-bit, D <= 64)"}
+            "path": "per-row sums from the forward's O, per-key-tile gradients on tcgen05 (16-bit, D <= 128)"}
 
 
 def shard_case(c, world, rank):
@@ -582,6 +582,8 @@ def main():
     ap.add_argument("--only-backward", action="store_true",
                     help="time only the backward of the bf16_long workload (one JSON line)")
     ap.add_argument("--backward-no-dbias", action="store_true", help="with --only-backward: skip dBias")
+    ap.add_argument("--backward-d", type=int, default=64, choices=(64, 128),
+                    help="with --only-backward: the head dimension (128: the same shape with D = 128)")
     ap.add_argument("--backward-n", type=int, default=None,
                     help="with --only-backward: the first N of the workload's 768 n rows only (a small case)")
     ap.add_argument("--only", default=None, choices=sorted(synth.WORKLOADS),
@@ -597,7 +599,8 @@ def main():
     if args.only_backward:
         import masked_attention_tri_gb300 as ta
         dev = torch.device("cuda", 0)
-        c = synth.bf16_long()
+        c = synth.bf16_long() if args.backward_d == 64 else synth.bf16_long_d128()
+        name = "bf16_long" if args.backward_d == 64 else "bf16_long_d128"
         if args.backward_n:
             n = args.backward_n
             c.q, c.k, c.v = (t[:, :n].contiguous() for t in (c.q, c.k, c.v))
@@ -605,7 +608,7 @@ def main():
             c.N = n
         line = backward_entry(ta, c, dev, load_peaks()[0], args.steps, args.warmup,
                               with_dbias=not args.backward_no_dbias)
-        line["workload"] = f"bf16_long backward, first {c.N} of 768 n rows" if args.backward_n else "bf16_long backward"
+        line["workload"] = f"{name} backward, first {c.N} of 768 n rows" if args.backward_n else f"{name} backward"
         print(json.dumps(line))
         return
     if args.only:
@@ -708,6 +711,9 @@ def main():
                                    "two_term_roofline_frac": roof["two_term_roofline_frac"],
                                    "l2": "inputs larger than L2"}
         per_config["bf16_long_backward"] = backward_entry(ta, c, dev, peaks)
+        c128 = synth.bf16_long_d128()
+        per_config["bf16_long_d128_backward"] = backward_entry(ta, c128, dev, peaks)
+        del c128
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -1,5 +1,6 @@
 // tc_bwd.cu -- the backward's per-key-tile gradients on tcgen05 tensor cores
-// (16-bit q/k/v with D % 16 == 0, D <= 64, K % 8 == 0; triangle form).
+// (16-bit q/k/v with D in {16, 32, 64}, or D % 16 == 0 in (64, 128] with a 16-bit bias;
+// K % 8 == 0; triangle form).
 //
 // The forward (cuEquivariance triangle_attention page) has its context saved for
 // backward.  With P recomputed from the saved lse and delta[q] = sum_k P dP (the
@@ -22,7 +23,11 @@
 // dQ) and add dS to the fp32 dBias accumulator (coalesced over keys); between the
 // halves of tile j each reads its 16 columns of dQ_{j-1} (one thread per query row)
 // and adds them to the fp32 dQ accumulator with a TMA reduce-add, and at the end
-// writes its 16 columns of dK and dV.  Warp 16 loads K and V once and, per query tile,
+// writes its 16 columns of dK and dV.
+// D in (64, 128] (WIDE): every 128-row tile is two 64-column boxes; dV, dK and dQ_j take
+// 128 columns each at TMEM [128, 512), leaving one S^T / dP^T buffer (columns [0, 64) and
+// [64, 128)) that the halves of a tile take in turn, and each compute warp reads out 32
+// columns of dQ / dK / dV (16 at a time through its staging rows).  Warp 16 loads K and V once and, per query tile,
 // Q, dO, the rows' lse / delta and the two bias halves (each as soon as the previous
 // tile's half is read); warp 17 issues the MMAs.  Every wait is bounded (TA_ERR_TIMEOUT).
 

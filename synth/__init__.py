@@ -205,6 +205,13 @@ def bf16_long() -> TriangleCase:
                          mask="kvlen", kv_range=(0, 768), forced_kv={0: 0, 1: 768})
 
 
+def bf16_long_d128() -> TriangleCase:
+    """bf16_long with a head dimension of 128: B=1,N=768,H=4,Q=K=768,D=128 bf16, bias bf16,
+    kv_lengths uniform in [0,768] (rows 0 and 1 pinned to 0 and 768)."""
+    return make_triangle("bf16_long_d128", 1, 768, 4, 768, 768, 128, "bf16", "bf16", seed=1005,
+                         mask="kvlen", kv_range=(0, 768), forced_kv={0: 0, 1: 768})
+
+
 def bf16_d256() -> TriangleCase:
     """The widest head dimension the forward takes: B=1,N=64,H=4,Q=K=384,D=256 bf16, bias bf16,
     kv_lengths uniform in [0,384]."""

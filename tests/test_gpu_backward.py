@@ -130,6 +130,34 @@ def test_backward_padded_key_tiles(dtype, D, bias_dtype):
     _check(c, 762 + D, with_out=True)
 
 
+@pytest.mark.parametrize("workload", ["bf16_long", "bf16_long_d128"])
+def test_backward_full_size_sampled_slabs(workload):
+    """The benchmark's backward launch at full size (B=1, N=768, H=4, Q=K=768, D = 64 or 128,
+    the forward's O given, dBias requested): dQ, dK and dV of sampled (b, n) slabs against the
+    oracle run on those slabs alone (each slab's dQ / dK / dV depends on that slab only; dBias,
+    a sum over all 768 slabs, is checked by the smaller cases).  The samples take kv_length 0
+    (every key masked), 768 (every key valid) and values in between."""
+    import masked_attention_tri_gb300 as ta
+    c = getattr(synth, workload)()
+    d_out = synth.grad_out(c, 790 + c.D)
+    q, k, v, bias, kl = (to_gpu(x) for x in (c.q, c.k, c.v, c.bias, c.kv_lengths))
+    o, lse, _ = ta.triangle_attention(q, k, v, bias, None, c.scale, True, kv_lengths=kl)
+    dq, dk, dv, db = ta.triangle_attention_backward(q, k, v, bias, lse, d_out.cuda(), None, c.scale, kv_lengths=kl,
+                                                    need_dbias=True, out=o)
+    torch.cuda.synchronize()
+    assert ta.get_status() == 0
+    assert db is not None and torch.isfinite(db.float()).all()
+    dq, dk, dv = dq.cpu(), dk.cpu(), dv.cpu()
+    del q, k, v, o, lse, db
+    for n in (0, 1, 2, 385, 767):
+        sl = slice(n, n + 1)
+        rq, rk, rv, _ = obwd.tri_bwd(c.q[:, sl], c.k[:, sl], c.v[:, sl], c.bias, d_out[:, sl],
+                                     kv_lengths=c.kv_lengths[:, sl], scale=c.scale)
+        _close(f"{workload}:dq[n={n}]", c.dtype, dq[:, sl], rq)
+        _close(f"{workload}:dk[n={n}]", c.dtype, dk[:, sl], rk)
+        _close(f"{workload}:dv[n={n}]", c.dtype, dv[:, sl], rv)
+
+
 def test_autograd_wrapper():
     """torch autograd through triangle_attention_autograd gives the same gradients (it passes the
     forward's O, so the per-row sums come from dO . O)."""
