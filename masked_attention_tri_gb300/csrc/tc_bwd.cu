@@ -237,28 +237,60 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
                 }
                 return true;
             };
-            if (j >= P.qs) {  // stage st held tile j - qs: its MMAs and its compute are done
-                ok = __all_sync(0xffffffffu, wait_bar(q_empty(st), (uint32_t)(use - 1) & 1u, abort_flag, P.status));
+            float lv[kBM / 32], dv[kBM / 32];  // the rows' lse / delta
+            if constexpr (WIDE) {
+                // One Q / dO stage taken as two half stages (q_full / q_empty (hh)): the rows of
+                // half hh are read only by that half's MMAs, so they are reloaded as soon as those
+                // are done.  The lse / delta loads go first (in flight during the waits); the
+                // rows are written after half 1 of tile j - 1 is done (its compute warps have
+                // read the previous rows by then).
+#pragma unroll
+                for (int t = 0; t < kBM / 32; ++t) {
+                    const int q = q0 + lane + 32 * t;
+                    lv[t] = q < P.Q ? P.lse[unit * P.Q + q] : 0.f;
+                    dv[t] = q < P.Q ? P.delta[unit * P.Q + q] : 0.f;
+                }
+                for (int hh = 0; hh < 2 && ok; ++hh) {
+                    if (j > 0) {
+                        ok = __all_sync(0xffffffffu,
+                                        wait_bar(q_empty(hh), (uint32_t)(j - 1) & 1u, abort_flag, P.status));
+                        if (!ok) break;
+                    }
+                    if (lane == 0) {
+                        mbar_expect_tx(q_full(hh), tileb);  // 64 rows x D of Q and of dO
+                        for (int bx = 0; bx < kNsub; ++bx) {
+                            const uint32_t o = (uint32_t)bx * kBox + (uint32_t)hh * (kBox / 2u);
+                            tma_load_3d(q_smem(0) + o, &P.tm_q, 64 * bx, q0 + 64 * hh, (int)unit, q_full(hh));
+                            tma_load_3d(do_smem(0) + o, &P.tm_do, 64 * bx, q0 + 64 * hh, (int)unit, q_full(hh));
+                        }
+                    }
+                    if (hh == 0) ok = bias_load(0);
+                }
                 if (!ok) break;
-            }
-            if (lane == 0) {
-                mbar_expect_tx(q_full(st), 2u * tileb);
-                for (int bx = 0; bx < kNsub; ++bx) {
-                    tma_load_3d(q_smem(st) + (uint32_t)bx * kBox, &P.tm_q, 64 * bx, q0, (int)unit, q_full(st));
-                    tma_load_3d(do_smem(st) + (uint32_t)bx * kBox, &P.tm_do, 64 * bx, q0, (int)unit, q_full(st));
+            } else {
+                if (j >= P.qs) {  // stage st held tile j - qs: its MMAs and its compute are done
+                    ok = __all_sync(0xffffffffu,
+                                    wait_bar(q_empty(st), (uint32_t)(use - 1) & 1u, abort_flag, P.status));
+                    if (!ok) break;
+                }
+                if (lane == 0) {
+                    mbar_expect_tx(q_full(st), 2u * tileb);
+                    for (int bx = 0; bx < kNsub; ++bx) {
+                        tma_load_3d(q_smem(st) + (uint32_t)bx * kBox, &P.tm_q, 64 * bx, q0, (int)unit, q_full(st));
+                        tma_load_3d(do_smem(st) + (uint32_t)bx * kBox, &P.tm_do, 64 * bx, q0, (int)unit, q_full(st));
+                    }
+                }
+                ok = bias_load(0);
+                if (!ok) break;
+#pragma unroll
+                for (int t = 0; t < kBM / 32; ++t) {  // every load in flight before the first store
+                    const int q = q0 + lane + 32 * t;
+                    lv[t] = q < P.Q ? P.lse[unit * P.Q + q] : 0.f;
+                    dv[t] = q < P.Q ? P.delta[unit * P.Q + q] : 0.f;
                 }
             }
-            ok = bias_load(0);
-            if (!ok) break;
             float* lse_s = reinterpret_cast<float*>(gbase + L.lse + (uint32_t)st * 1024u);
             float* del_s = lse_s + 128;
-            float lv[kBM / 32], dv[kBM / 32];  // every load in flight before the first store
-#pragma unroll
-            for (int t = 0; t < kBM / 32; ++t) {
-                const int q = q0 + lane + 32 * t;
-                lv[t] = q < P.Q ? P.lse[unit * P.Q + q] : 0.f;
-                dv[t] = q < P.Q ? P.delta[unit * P.Q + q] : 0.f;
-            }
 #pragma unroll
             for (int t = 0; t < kBM / 32; ++t) {
                 lse_s[lane + 32 * t] = lv[t];
@@ -275,15 +307,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
         // once P^T / dS^T of (j, hh) are written, dV and dK take them, then S^T / dP^T of
         // (j + 1, hh) go into the same buffer (the tensor core runs them in order), so the
         // compute warps find the next half ready.  After half 1, dQ_j = dS K.  With one Q / dO
-        // stage, tile j + 1's S^T / dP^T wait until tile j's MMAs are all issued.
+        // stage, tile j + 1's S^T / dP^T wait until tile j's MMAs are all issued.  WIDE: one
+        // S^T / dP^T buffer for (j, 0), (j, 1), (j + 1, 0), ... in turn; Q / dO rows per half.
         const bool leader = elect_one();
         bool ok = __all_sync(0xffffffffu, wait_bar(kv_full, 0, abort_flag, P.status));
         const uint64_t kK = sw128_desc(base + L.k, 16, 1024), vK = sw128_desc(base + L.v, 16, 1024);
         const uint64_t kM = sw128_desc(base + L.k, kBox, 1024), dsM = sw128_desc(base + L.ds, kBox, 1024);
         auto mma1 = [&](int j, int hh) -> bool {
             const int st = j % P.qs;
-            if (hh == 0) {
-                if (!__all_sync(0xffffffffu, wait_bar(q_full(st), (uint32_t)(j / P.qs) & 1u, abort_flag, P.status)))
+            if (WIDE || hh == 0) {  // WIDE: each half's rows have their own barrier
+                const uint32_t qb = WIDE ? q_full(hh) : q_full(st);
+                if (!__all_sync(0xffffffffu, wait_bar(qb, (uint32_t)(j / P.qs) & 1u, abort_flag, P.status)))
                     return false;
                 tc_fence_after();
             }
@@ -337,6 +371,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
                         mma_ts(tDV, tS + 64u * b + 16u * (uint32_t)kk, doM + 128u * qs16, P.idesc_g, acc);
                         mma_ts(tDK, tDP + 64u * b + 16u * (uint32_t)kk, qM + 128u * qs16, P.idesc_g, acc);
                     }
+                    if constexpr (WIDE) mma_commit(q_empty(hh));  // the rows of half hh are read
                 }
                 if (hh == 1) {
                     if (j > 0) {  // the compute warps have read dQ of the previous tile
@@ -351,7 +386,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
                                    kk > 0 ? 1u : 0u);
                         mma_commit(dq_full);
                         mma_commit(ds_free);
-                        mma_commit(q_empty(st));
+                        if constexpr (!WIDE) mma_commit(q_empty(st));
                     }
                 }
                 if constexpr (WIDE) {  // the single buffer: the other half next (the tensor core runs them in order)
@@ -687,9 +722,10 @@ cudaError_t launch_tc_bwd_main(const BwdParams& p, cudaStream_t stream) {
     P.bias_boxes = kBN / P.bias_box_cols;
     P.bias_bytes = (uint32_t)P.bias_boxes * kBox;
     const uint64_t eb = p.bias_f32 ? 4 : 2;
+    const int qbox = D > 64 ? kBM / 2 : kBM;  // D > 64: Q / dO rows loaded per query half
     const bool maps_ok =
-        encode_map_3d(&P.tm_q, dt, p.q, D, p.Q, units, rs, rs * p.Q, 64, kBM, 1, sw128) &&
-        encode_map_3d(&P.tm_do, dt, p.d_out, D, p.Q, units, rs, rs * p.Q, 64, kBM, 1, sw128) &&
+        encode_map_3d(&P.tm_q, dt, p.q, D, p.Q, units, rs, rs * p.Q, 64, qbox, 1, sw128) &&
+        encode_map_3d(&P.tm_do, dt, p.d_out, D, p.Q, units, rs, rs * p.Q, 64, qbox, 1, sw128) &&
         encode_map_3d(&P.tm_k, dt, p.k, D, p.K, units, rs, rs * p.K, 64, kBN, 1, sw128) &&
         encode_map_3d(&P.tm_v, dt, p.v, D, p.K, units, rs, rs * p.K, 64, kBN, 1, sw128) &&
         encode_map_3d(&P.tm_bias, p.bias_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : dt, p.bias, p.K, p.Q,
@@ -723,7 +759,7 @@ cudaError_t launch_tc_bwd_main(const BwdParams& p, cudaStream_t stream) {
     const long long grid = (long long)units * P.nkt;
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    P.qs = 2;
+    P.qs = D > 64 ? 1 : 2;  // D > 64: one stage, taken per query half
     if (bwd_layout(P, P.nsub).total + 1024 > 232448) P.qs = 1;  // the 227 KB per-block limit
     const size_t smem = bwd_layout(P, P.nsub).total + 1024;
     // D > 64 runs with a 16-bit bias only (tc_bwd_supported)
