@@ -299,6 +299,46 @@ def backward_entry(ta, c, dev, peaks, steps=5, warmup=2, with_dbias=True):
             "path": "per-row sums from the forward's O, per-key-tile gradients on tcgen05 (16-bit, D <= 128)"}
 
 
+def varlen_backward_entry(ta, c, dev, peaks, steps=5, warmup=2, repeats=3):
+    """The backward of the packed workload `c` through `varlen_attention_backward` (its
+    BlockMask, the forward's O and lse given): ms per call and effective TFLOP/s over the
+    five contractions (2.5x the forward's count)."""
+    bm = ta.BlockMask.from_kv_blocks(c.kv_num_blocks.to(dev), c.kv_indices.to(dev), c.full_kv_num_blocks.to(dev),
+                                     c.full_kv_indices.to(dev), BLOCK_SIZE=c.block, mask_mod=c.mask_mod)
+    q, k, v = c.q.to(dev), c.k.to(dev), c.v.to(dev)
+    cu = c.cu_seqlens.to(dev)
+    o, lse, _ = ta.varlen_attention(q, k, v, cu, cu, c.max_seqlen, c.max_seqlen, block_mask=bm, scale=c.scale,
+                                    return_aux=True)
+    g = torch.Generator("cpu").manual_seed(12)
+    d_out = torch.randn(tuple(c.q.shape), generator=g).to(q.dtype).to(dev)
+
+    def call():
+        ta.varlen_attention_backward(q, k, v, cu, cu, c.max_seqlen, c.max_seqlen, o, lse, d_out, block_mask=bm,
+                                     scale=c.scale)
+
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    stream = torch.cuda.current_stream(dev)
+    per = []
+    for _ in range(repeats):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            call()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        per.append(e0.elapsed_time(e1) / steps)
+    assert ta.get_status() == 0
+    t = statistics.median(per)
+    f = 2.5 * varlen_work(c)[0]
+    return {"ms": t, "tflops": f / (t * 1e-3) / 1e12,
+            "pct_bf16_peak": 100 * f / (t * 1e-3) / (peaks["bf16_tflops"] * 1e12),
+            "outputs": "dQ, dK, dV",
+            "path": "per-row sums from the forward's O, per-(sequence, head, key block) gradients on tcgen05",
+            "timing": "through varlen_attention_backward (argument checks and workspace included)"}
+
+
 def shard_case(c, world, rank):
     """This rank's contiguous range of (b, n) slabs of a B = 1 workload (the bias replicated)."""
     from masked_attention_tri_gb300.shard import slab_range
@@ -584,6 +624,8 @@ def main():
     ap.add_argument("--backward-no-dbias", action="store_true", help="with --only-backward: skip dBias")
     ap.add_argument("--backward-d", type=int, default=64, choices=(64, 128),
                     help="with --only-backward: the head dimension (128: the same shape with D = 128)")
+    ap.add_argument("--backward-varlen", action="store_true",
+                    help="with --only-backward: the backward of the bf16_varlen packed sequences instead")
     ap.add_argument("--backward-n", type=int, default=None,
                     help="with --only-backward: the first N of the workload's 768 n rows only (a small case)")
     ap.add_argument("--only", default=None, choices=sorted(synth.WORKLOADS),
@@ -599,6 +641,11 @@ def main():
     if args.only_backward:
         import masked_attention_tri_gb300 as ta
         dev = torch.device("cuda", 0)
+        if args.backward_varlen:
+            line = varlen_backward_entry(ta, synth.bf16_varlen(), dev, load_peaks()[0], args.steps, args.warmup)
+            line["workload"] = "bf16_varlen backward"
+            print(json.dumps(line))
+            return
         c = synth.bf16_long() if args.backward_d == 64 else synth.bf16_long_d128()
         name = "bf16_long" if args.backward_d == 64 else "bf16_long_d128"
         if args.backward_n:
@@ -688,6 +735,7 @@ def main():
             "pct_bf16_peak": 100 * f / (t * 1e-3) / (peaks["bf16_tflops"] * 1e12),
             "two_term_roofline_frac": max(f / (peaks["bf16_tflops"] * 1e12), b / (peaks["hbm_gbs"] * 1e9)) / (t * 1e-3),
             "layout": "one (total, 3, H, D) buffer read in place", "l2": "flushed before each launch"}
+        per_config["bf16_varlen_backward"] = varlen_backward_entry(ta, vc, dev, peaks)
         # The widened rows, measured like the others: a sliding-window BlockMask on the packed
         # sequences (mask_mod sliding_window, window 512, its block lists) and D = 256.
         wc = synth.bf16_varlen_window512()

@@ -352,9 +352,13 @@ ta_status tri_attn_varlen_fwd_masked(const void* q, const void* k, const void* v
  *   workspace     device scratch of tri_attn_varlen_bwd_workspace_size(...,
  *                 with_bias = dbias != NULL) bytes, 256-byte aligned, owned by
  *                 the caller.
- * Arithmetic: exact fp32 on CUDA cores for every dtype (one CTA per sequence,
- * head and 32 keys; dQ and dBias added with fp32 atomics, so their summation
- * order varies from run to run).  Errors as tri_attn_bwd; a sequence that
+ * Arithmetic: fp16 / bf16 inputs with D a multiple of 16 up to 128 and no bias
+ * run on tensor cores (one CTA per sequence, head and 128-key block, over the q
+ * blocks whose lists hold that block and those with a row that has no valid
+ * key; P and dS rounded to the input type as the MMAs' operands, fp32
+ * accumulation); every other case exact fp32 on CUDA cores (one CTA per
+ * sequence, head and 32 keys).  dQ and dBias are added in fp32 with atomic
+ * reductions, so their summation order varies from run to run.  Errors as tri_attn_bwd; a sequence that
  * breaks the max_seqlen / total contract is skipped and TA_ERR_DEVICE recorded.
  */
 ta_status tri_attn_varlen_bwd(const void* q, const void* k, const void* v, ta_dtype dtype,

@@ -1,6 +1,6 @@
 // tc_bwd.cu -- the backward's per-key-tile gradients on tcgen05 tensor cores
 // (16-bit q/k/v with D in {16, 32, 64}, or D % 16 == 0 in (64, 128] with a 16-bit bias;
-// K % 8 == 0; triangle form).
+// K % 8 == 0; triangle form; and packed sequences without a bias, D as above).
 //
 // The forward (cuEquivariance triangle_attention page) has its context saved for
 // backward.  With P recomputed from the saved lse and delta[q] = sum_k P dP (the
@@ -23,13 +23,21 @@
 // dQ) and add dS to the fp32 dBias accumulator (coalesced over keys); between the
 // halves of tile j each reads its 16 columns of dQ_{j-1} (one thread per query row)
 // and adds them to the fp32 dQ accumulator with a TMA reduce-add, and at the end
-// writes its 16 columns of dK and dV.
-// D in (64, 128] (WIDE): every 128-row tile is two 64-column boxes; dV, dK and dQ_j take
-// 128 columns each at TMEM [128, 512), leaving one S^T / dP^T buffer (columns [0, 64) and
-// [64, 128)) that the halves of a tile take in turn, and each compute warp reads out 32
-// columns of dQ / dK / dV (16 at a time through its staging rows).  Warp 16 loads K and V once and, per query tile,
+// writes its 16 columns of dK and dV.  Warp 16 loads K and V once and, per query tile,
 // Q, dO, the rows' lse / delta and the two bias halves (each as soon as the previous
 // tile's half is read); warp 17 issues the MMAs.  Every wait is bounded (TA_ERR_TIMEOUT).
+// D in (64, 128] (WIDE): every 128-row tile is two 64-column boxes; dV, dK and dQ_j take
+// 128 columns each at TMEM [128, 512), leaving one S^T / dP^T buffer (columns [0, 64) and
+// [64, 128)) that the halves of a tile take in turn; each compute warp reads out 32
+// columns of dQ / dK / dV (16 at a time through its staging rows); the one Q / dO stage
+// is filled per query half.
+// Packed sequences (VARLEN; tensorplay BlockMask page, Details 3-4: the backward walks the
+// q blocks of each kv block): one CTA per (sequence, head, 128-key block).  One warp first
+// lists, in shared memory, the q blocks whose full or partial lists hold the key block,
+// plus the q blocks with a row that has no valid key (the forward gave such a row the
+// mean of V, so it adds 1 / Lk dO to dV at every key); the tile walk above then runs over
+// that list, with mask_mod deciding each (query, key) of a partial block.  Rows of a tile
+// past the sequence (the next sequence's rows, read through the same maps) have P = 0.
 
 #include "tc_kernel.cuh"
 
@@ -57,13 +65,25 @@ struct BwdTc {
     uint32_t bias_bytes;
     int bias_boxes, bias_box_cols;
     int qs;             // stages of (Q, dO, lse, delta): 2 when shared memory allows, else 1
+    // Packed sequences (VARLEN): q / k / v / dO (total, H, D) and the fp32 dQ accumulator read
+    // through (D, total, H) maps, lse / delta (H, total_q), the BlockMask lists; no bias.
+    const int32_t* cu_q;
+    const int32_t* cu_k;
+    int total_q, total_k, max_q, max_k;
+    const int32_t* kv_num;
+    const int32_t* kv_idx;
+    const int32_t* full_num;
+    const int32_t* full_idx;
+    int mask_heads, MQ, MK, mask_mod, window, prefix_all;
+    const int32_t* prefix_len;
+    int qcap;           // entries of the q-block list in shared memory (0: triangle form)
 };
 
 // Shared memory (offsets from a 1024-byte aligned base).
 // Stage s of the query-tile ring: Q at q + s * 2 tile, dO after it; lse / delta at lse + s * 1024
 // (tile = nsub boxes of 128 rows x 128 bytes).
 struct BwdLayout {
-    uint32_t k, v, q, ds, bias, dqst, lse, bars, tmem_slot, abort_flag, total;
+    uint32_t k, v, q, ds, bias, dqst, lse, qlist, bars, tmem_slot, abort_flag, qn, total;
 };
 // kv_full, q_full[2], q_empty[2], lse_full[2], bias_full[2], bias_empty[2], s_full[2], p_full[2],
 // dq_full, dq_empty, ds_free, fin, drain
@@ -79,10 +99,12 @@ __host__ __device__ inline BwdLayout bwd_layout(const BwdTc& P, int nsub) {
     L.bias = L.ds + 2 * kBox;
     L.dqst = L.bias + P.bias_bytes;          // dQ staging: 16 compute warps x 32 rows x 16 fp32
     L.lse = L.dqst + 16u * 2048u;
-    L.bars = L.lse + (uint32_t)P.qs * 1024u;
+    L.qlist = L.lse + (uint32_t)P.qs * 1024u;  // packed form: the q blocks the key tile visits
+    L.bars = L.qlist + (((uint32_t)P.qcap * 4u + 15u) & ~15u);
     L.tmem_slot = L.bars + 8 * kBwdBars;
     L.abort_flag = L.tmem_slot + 4;
-    L.total = L.abort_flag + 4;
+    L.qn = L.abort_flag + 4;                   // packed form: entries of the q-block list
+    L.total = L.qn + 4;
     return L;
 }
 
@@ -114,9 +136,23 @@ constexpr int kWarpQ = 64 / kQuarterWarps;        // queries of every 64-query h
 constexpr int kProducerWarp = kComputeWarps, kMmaWarp = kComputeWarps + 1;
 constexpr int kBwdThreads = (kComputeWarps + 2) * 32;
 
+// mask_mod on a partial block (indices local to the sequence): causal k <= q; sliding window
+// q - window < k <= q; prefix LM k <= q or k < prefix (tensorplay BlockMask page, Details 2).
+__device__ __forceinline__ bool bwd_mod_keep(int mod, int q, int k, int window, int prefix) {
+    switch (mod) {
+    case TA_MASK_CAUSAL: return k <= q;
+    case TA_MASK_SLIDING_WINDOW: return k <= q && k > q - window;
+    case TA_MASK_PREFIX_LM: return k <= q || k < prefix;
+    default: return true;
+    }
+}
+
 // WIDE: D in (64, 128] (two 64-column boxes per tile, one S^T / dP^T buffer that the query
 // halves take in turn, 32 columns of dQ / dK / dV per compute warp); otherwise D <= 64.
-template <bool BF16, bool BIAS_F32, bool WIDE>
+// VARLEN: packed sequences, one CTA per (sequence, head, 128-key block), visiting the q blocks
+// whose lists hold the key block (full: every key valid; partial: mask_mod decides) and the
+// q blocks with a row that has no valid key (its weights are 1 / Lk at every key); no bias.
+template <bool BF16, bool BIAS_F32, bool WIDE, bool VARLEN>
 __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_constant__ BwdTc P) {
     constexpr int kNsub = WIDE ? 2 : 1;   // 64-column boxes per 128-row tile
     constexpr int kCpw = WIDE ? 32 : 16;  // dQ / dK / dV columns per compute warp
@@ -144,13 +180,42 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
     // bias rows [64 hh, 64 hh + 64) of the tile: boxes of bias_box_cols keys x 64 rows (8 KB each)
     auto bias_half = [&](int hh) { return base + L.bias + (uint32_t)hh * (P.bias_bytes / 2u); };
 
-    const long long unit = blockIdx.x / P.nkt;  // (b*N + n)*H + h
-    const int k0 = (int)(blockIdx.x - unit * P.nkt) * kBN;
-    const int h = (int)(unit % P.H);
-    const long long bn = unit / P.H;
-    const int b = (int)(bn / P.N);
+    // The key tile's unit.  Triangle form: slab unit = (b*N + n)*H + h, Qn x Kn = Q x K.
+    // Packed form: sequence seq and head h, Qn x Kn = its lengths.  Rows go through the maps
+    // at (x, qrow0 + q, tz) and (x, krow0 + k, tz); lse / delta at lrow0 + q.
+    long long unit = 0, bn = 0, lrow0;
+    int k0, h, b = 0, Qn, Kn, qrow0 = 0, krow0 = 0, tz, seq = 0, prefix = 0;
+    if constexpr (!VARLEN) {
+        unit = blockIdx.x / P.nkt;
+        k0 = (int)(blockIdx.x - unit * P.nkt) * kBN;
+        h = (int)(unit % P.H);
+        bn = unit / P.H;
+        b = (int)(bn / P.N);
+        Qn = P.Q;
+        Kn = P.K;
+        tz = (int)unit;
+        lrow0 = unit * P.Q;
+    } else {
+        seq = (int)(blockIdx.x / ((unsigned)P.H * (unsigned)P.nkt));
+        h = (int)((blockIdx.x / (unsigned)P.nkt) % (unsigned)P.H);
+        k0 = (int)(blockIdx.x % (unsigned)P.nkt) * kBN;
+        const int cq0 = P.cu_q[seq], cq1 = P.cu_q[seq + 1], ck0 = P.cu_k[seq], ck1 = P.cu_k[seq + 1];
+        Qn = cq1 - cq0;
+        Kn = ck1 - ck0;
+        if (Qn > P.max_q || Kn > P.max_k || Qn < 0 || Kn < 0 || cq0 < 0 || ck0 < 0 || cq1 > P.total_q ||
+            ck1 > P.total_k) {
+            if (threadIdx.x == 0 && k0 == 0 && h == 0) atomicCAS(P.status, 0, kStatusDevice);
+            return;
+        }
+        if (k0 >= Kn) return;
+        qrow0 = cq0;
+        krow0 = ck0;
+        tz = h;
+        lrow0 = (long long)h * P.total_q + cq0;
+        prefix = P.prefix_len ? P.prefix_len[seq] : P.prefix_all;
+    }
 
-    if (P.kv_len) {
+    if (!VARLEN && P.kv_len) {
         // A key tile wholly past a kv_length of at least 1: its keys have weight 0 in every
         // row (each row has a valid key), so dK = dV = 0 there and nothing reaches dQ or
         // dBias.  (With kv_length 0 every key has weight 1 / K and the tile is computed.)
@@ -169,6 +234,71 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
             return;
         }
     }
+
+    // Packed form: the q blocks this key tile visits, as (q block | status << 24) in shared
+    // memory (status 1 partial, 2 full, 3 every key masked), built by one warp.
+    int nqt = P.nqt;
+    const uint32_t* qlist = reinterpret_cast<const uint32_t*>(gbase + L.qlist);
+    if constexpr (VARLEN) {
+        if (warp == kProducerWarp) {
+            uint32_t* qw = reinterpret_cast<uint32_t*>(gbase + L.qlist);
+            const int kb = k0 / kBN, nqb = (Qn + kBM - 1) / kBM;
+            int cnt = 0;
+            for (int qb = 0; qb < nqb && qb < P.qcap; ++qb) {
+                int st = 1;  // no lists: every block partial
+                if (P.kv_num) {
+                    int f = 0;
+                    if (qb < P.MQ) {
+                        const int hm = P.mask_heads == 1 ? 0 : h;
+                        const long long row = ((long long)seq * P.mask_heads + hm) * P.MQ + qb;
+                        if (P.full_num) {
+                            const int n = min(max(P.full_num[row], 0), P.MK);
+                            for (int t = lane; t < n; t += 32)
+                                if (P.full_idx[row * P.MK + t] == kb) f = 2;
+                        }
+                        const int n = min(max(P.kv_num[row], 0), P.MK);
+                        for (int t = lane; t < n; t += 32)
+                            if (P.kv_idx[row * P.MK + t] == kb && f == 0) f = 1;
+                    }
+                    st = (int)__reduce_max_sync(0xffffffffu, (unsigned)f);  // full before partial
+                }
+                if (st == 0) {  // not listed: visited only for rows with no valid key
+                    bool fm = false;
+#pragma unroll
+                    for (int t = 0; t < kBM / 32; ++t) {
+                        const int q = qb * kBM + lane + 32 * t;
+                        if (q < Qn && P.lse[lrow0 + q] <= kMasked + 64.f) fm = true;
+                    }
+                    if (__any_sync(0xffffffffu, fm)) st = 3;
+                }
+                if (st != 0) {
+                    if (lane == 0) qw[cnt] = (uint32_t)qb | ((uint32_t)st << 24);
+                    ++cnt;
+                }
+            }
+            if (lane == 0) *reinterpret_cast<volatile int*>(gbase + L.qn) = cnt;
+        }
+        __syncthreads();
+        nqt = *reinterpret_cast<volatile int*>(gbase + L.qn);
+        if (nqt == 0) {  // no row reaches these keys: dK = dV = 0
+            const int rows = Kn - k0 < kBN ? Kn - k0 : kBN, per = P.D / 8;  // 16-byte pieces per row
+            for (int i = threadIdx.x; i < rows * per; i += blockDim.x) {
+                const long long off = (long long)(krow0 + k0 + i / per) * P.H * P.D + (long long)h * P.D + (i % per) * 8;
+                *reinterpret_cast<uint4*>(static_cast<uint16_t*>(P.dk) + off) = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(static_cast<uint16_t*>(P.dv) + off) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            return;
+        }
+    }
+    // the first query row (within the unit) and the status of entry j of the tile walk
+    auto tile_q0 = [&](int j) -> int {
+        if constexpr (VARLEN) return (int)(qlist[j] & 0xffffffu) * kBM;
+        else return j * kBM;
+    };
+    auto tile_st = [&](int j) -> int {
+        if constexpr (VARLEN) return (int)(qlist[j] >> 24);
+        else return 2;
+    };
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
@@ -217,15 +347,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
         if (lane == 0) {
             mbar_expect_tx(kv_full, 2u * tileb);
             for (int bx = 0; bx < kNsub; ++bx) {
-                tma_load_3d(base + L.k + (uint32_t)bx * kBox, &P.tm_k, 64 * bx, k0, (int)unit, kv_full);
-                tma_load_3d(base + L.v + (uint32_t)bx * kBox, &P.tm_v, 64 * bx, k0, (int)unit, kv_full);
+                tma_load_3d(base + L.k + (uint32_t)bx * kBox, &P.tm_k, 64 * bx, krow0 + k0, tz, kv_full);
+                tma_load_3d(base + L.v + (uint32_t)bx * kBox, &P.tm_v, 64 * bx, krow0 + k0, tz, kv_full);
             }
         }
-        for (int j = 0; j < P.nqt && ok; ++j) {
-            const int q0 = j * kBM, st = j % P.qs, use = j / P.qs;
+        for (int j = 0; j < nqt && ok; ++j) {
+            const int q0 = tile_q0(j), st = j % P.qs, use = j / P.qs;
             // This tile's Q / dO, bias half 0 (as soon as the compute warps have read half 0 of
             // tile j - 1), the rows' lse / delta, then bias half 1.
             auto bias_load = [&](int hh) -> bool {
+                if constexpr (VARLEN) return true;  // no bias
                 if (j > 0 &&
                     !__all_sync(0xffffffffu, wait_bar(bias_empty(hh), (uint32_t)(j - 1) & 1u, abort_flag, P.status)))
                     return false;
@@ -247,8 +378,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
 #pragma unroll
                 for (int t = 0; t < kBM / 32; ++t) {
                     const int q = q0 + lane + 32 * t;
-                    lv[t] = q < P.Q ? P.lse[unit * P.Q + q] : 0.f;
-                    dv[t] = q < P.Q ? P.delta[unit * P.Q + q] : 0.f;
+                    lv[t] = q < Qn ? P.lse[lrow0 + q] : 0.f;
+                    dv[t] = q < Qn ? P.delta[lrow0 + q] : 0.f;
                 }
                 for (int hh = 0; hh < 2 && ok; ++hh) {
                     if (j > 0) {
@@ -260,8 +391,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
                         mbar_expect_tx(q_full(hh), tileb);  // 64 rows x D of Q and of dO
                         for (int bx = 0; bx < kNsub; ++bx) {
                             const uint32_t o = (uint32_t)bx * kBox + (uint32_t)hh * (kBox / 2u);
-                            tma_load_3d(q_smem(0) + o, &P.tm_q, 64 * bx, q0 + 64 * hh, (int)unit, q_full(hh));
-                            tma_load_3d(do_smem(0) + o, &P.tm_do, 64 * bx, q0 + 64 * hh, (int)unit, q_full(hh));
+                            tma_load_3d(q_smem(0) + o, &P.tm_q, 64 * bx, qrow0 + q0 + 64 * hh, tz, q_full(hh));
+                            tma_load_3d(do_smem(0) + o, &P.tm_do, 64 * bx, qrow0 + q0 + 64 * hh, tz, q_full(hh));
                         }
                     }
                     if (hh == 0) ok = bias_load(0);
@@ -276,8 +407,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
                 if (lane == 0) {
                     mbar_expect_tx(q_full(st), 2u * tileb);
                     for (int bx = 0; bx < kNsub; ++bx) {
-                        tma_load_3d(q_smem(st) + (uint32_t)bx * kBox, &P.tm_q, 64 * bx, q0, (int)unit, q_full(st));
-                        tma_load_3d(do_smem(st) + (uint32_t)bx * kBox, &P.tm_do, 64 * bx, q0, (int)unit, q_full(st));
+                        tma_load_3d(q_smem(st) + (uint32_t)bx * kBox, &P.tm_q, 64 * bx, qrow0 + q0, tz, q_full(st));
+                        tma_load_3d(do_smem(st) + (uint32_t)bx * kBox, &P.tm_do, 64 * bx, qrow0 + q0, tz,
+                                    q_full(st));
                     }
                 }
                 ok = bias_load(0);
@@ -285,8 +417,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
 #pragma unroll
                 for (int t = 0; t < kBM / 32; ++t) {  // every load in flight before the first store
                     const int q = q0 + lane + 32 * t;
-                    lv[t] = q < P.Q ? P.lse[unit * P.Q + q] : 0.f;
-                    dv[t] = q < P.Q ? P.delta[unit * P.Q + q] : 0.f;
+                    lv[t] = q < Qn ? P.lse[lrow0 + q] : 0.f;
+                    dv[t] = q < Qn ? P.delta[lrow0 + q] : 0.f;
                 }
             }
             float* lse_s = reinterpret_cast<float*>(gbase + L.lse + (uint32_t)st * 1024u);
@@ -354,8 +486,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
             }
             return true;
         };
-        if (ok && P.nqt > 0) ok = WIDE ? mma1(0, 0) : (mma1(0, 0) && mma1(0, 1));
-        for (int j = 0; j < P.nqt && ok; ++j) {
+        if (ok && nqt > 0) ok = WIDE ? mma1(0, 0) : (mma1(0, 0) && mma1(0, 1));
+        for (int j = 0; j < nqt && ok; ++j) {
             const int st = j % P.qs;
             const uint64_t qM = sw128_desc(q_smem(st), kBox, 1024), doM = sw128_desc(do_smem(st), kBox, 1024);
             for (int hh = 0; hh < 2 && ok; ++hh) {
@@ -391,8 +523,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
                 }
                 if constexpr (WIDE) {  // the single buffer: the other half next (the tensor core runs them in order)
                     if (hh == 0) ok = mma1(j, 1);
-                    else if (j + 1 < P.nqt) ok = mma1(j + 1, 0);
-                } else if (j + 1 < P.nqt) {
+                    else if (j + 1 < nqt) ok = mma1(j + 1, 0);
+                } else if (j + 1 < nqt) {
                     if (P.qs > 1) ok = mma1(j + 1, hh);
                     else if (hh == 1) ok = mma1(j + 1, 0) && mma1(j + 1, 1);
                 }
@@ -411,9 +543,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
         const int hq = warp >> 2;         // within each 64-query half: queries kWarpQ hq .. + kWarpQ - 1
         const int kr = wq * 32 + lane;    // key row of the tile
         const int key = k0 + kr;
-        const bool exists = key < P.K;
+        const bool exists = key < Kn;
         bool valid = exists;
-        if (exists) {
+        if (!VARLEN && exists) {
             if (P.kv_len) {
                 int Lk = P.kv_len[bn];
                 Lk = Lk < 0 ? 0 : (Lk > P.K ? P.K : Lk);
@@ -423,7 +555,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
             }
         }
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-        const float inv_k = 1.f / (float)P.K;
+        const float inv_k = 1.f / (float)Kn;
         const uint32_t rsw = (uint32_t)(kr & 7);
         // this key's column in the bias halves: boxes of bias_box_cols keys x 64 rows, 128B-swizzled
         const uint32_t bbox_off = (uint32_t)(kr / P.bias_box_cols) * 8192u;
@@ -432,7 +564,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
         uint32_t xo[8];
 #pragma unroll
         for (int r8 = 0; r8 < 8; ++r8) xo[r8] = ((((bcol_b >> 4) ^ (uint32_t)r8)) << 4) + (bcol_b & 15u);
-        float* dbias_row = P.dbias_acc ? P.dbias_acc + ((long long)b * P.H + h) * P.Q * (long long)P.K + key : nullptr;
+        float* dbias_row = !VARLEN && P.dbias_acc
+                               ? P.dbias_acc + ((long long)b * P.H + h) * P.Q * (long long)P.K + key : nullptr;
         // dQ staging of this warp: 32 rows x 16 fp32 (64-byte rows, 64B-swizzled)
         const uint32_t dq_stage = base + L.dqst + (uint32_t)warp * 2048u;
         const uint32_t qsw = (uint32_t)((lane >> 1) & 3);
@@ -463,12 +596,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
                                  __float_as_uint(__uint_as_float(o[4 * g + 3]) * P.scale));
                 fence_async_shared();
                 __syncwarp();
-                if (lane == 0 && jr * kBM + 32 * wq < P.Q) {
-                    tma_reduce_add_3d(&P.tm_dq, dq_stage, dc0, jr * kBM + 32 * wq, (int)unit);
+                if (lane == 0 && tile_q0(jr) + 32 * wq < Qn) {
+                    tma_reduce_add_3d(&P.tm_dq, dq_stage, dc0, qrow0 + tile_q0(jr) + 32 * wq, tz);
                     bulk_commit();
                 }
             } else {
-                const bool rows = jr * kBM + 32 * wq < P.Q;
+                const bool rows = tile_q0(jr) + 32 * wq < Qn;
 #pragma unroll 1
                 for (int pc = 0; pc < kCpw / 16; ++pc) {  // 16 columns at a time through the staging rows
                     const int d0 = dc0 + 16 * pc;
@@ -492,7 +625,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
                     fence_async_shared();
                     __syncwarp();
                     if (lane == 0 && rows) {
-                        tma_reduce_add_3d(&P.tm_dq, dq_stage, d0, jr * kBM + 32 * wq, (int)unit);
+                        tma_reduce_add_3d(&P.tm_dq, dq_stage, d0, qrow0 + tile_q0(jr) + 32 * wq, tz);
                         bulk_commit();
                     }
                 }
@@ -501,16 +634,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
         };
 
         bool ok = true;
-        for (int j = 0; j < P.nqt && ok; ++j) {
+        for (int j = 0; j < nqt && ok; ++j) {
             const uint32_t ph = (uint32_t)j & 1u;
-            const int q0 = j * kBM, st = j % P.qs;
+            const int q0 = tile_q0(j), st = j % P.qs, tst = tile_st(j);
             const float* lse_s = reinterpret_cast<const float*>(gbase + L.lse + (uint32_t)st * 1024u);
             const float* del_s = lse_s + 128;
             ok = __all_sync(0xffffffffu, wait_bar(lse_full(st), (uint32_t)(j / P.qs) & 1u, abort_flag, P.status));
             if (!ok) break;
             for (int hh = 0; hh < 2 && ok; ++hh) {
-                ok = __all_sync(0xffffffffu, wait_bar(bias_full(hh), ph, abort_flag, P.status));
-                if (!ok) break;
+                if (!VARLEN) {
+                    ok = __all_sync(0xffffffffu, wait_bar(bias_full(hh), ph, abort_flag, P.status));
+                    if (!ok) break;
+                }
                 ok = __all_sync(0xffffffffu, wait_bar(s_full(buf(hh)), sphase(j, hh), abort_flag, P.status));
                 if (!ok) break;
                 tc_fence_after();
@@ -537,9 +672,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
                         dl[i] = d4.x, dl[i + 1] = d4.y, dl[i + 2] = d4.z, dl[i + 3] = d4.w;
                     }
                     const uint8_t* bcb = gbase + (bias_half(hh) - base) + bbox_off + (uint32_t)(ql - 64 * hh) * 128u;
-                    const int nq = P.Q - (q0 + ql);  // queries of the chunk that exist
+                    const int nq = Qn - (q0 + ql);  // queries of the chunk that exist
                     uint32_t pp[CW / 2], dd[CW / 2];
-                    if (__all_sync(0xffffffffu, valid) && nq >= CW) {
+                    if (__all_sync(0xffffffffu, valid) && nq >= CW && tst == 2) {
                         // Every key of the warp valid and every query of the chunk present: each row
                         // has a valid key, so its lse is a plain log-sum-exp and P = 2^(x log2e - lse log2e).
                         const float2 sl2 = make_float2(P.scale * kLog2e, P.scale * kLog2e);
@@ -548,7 +683,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
 #pragma unroll
                         for (int i = 0; i < CW; i += 2) {
                             float2 bv;
-                            if constexpr (BIAS_F32) {
+                            if constexpr (VARLEN) {
+                                bv = make_float2(0.f, 0.f);
+                            } else if constexpr (BIAS_F32) {
                                 bv = make_float2(*reinterpret_cast<const float*>(bcb + i * 128 + xo[i & 7]),
                                                  *reinterpret_cast<const float*>(bcb + (i + 1) * 128 + xo[(i + 1) & 7]));
                             } else {
@@ -574,10 +711,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
                         }
                     } else {
                         // Logits first (every read of the bias tile before any reduction into dBias).
+                        // Packed form: bit ii of vm = query ql + ii and this key valid (the block's
+                        // status; mask_mod on a partial block).
+                        uint32_t vm = 0;
 #pragma unroll
                         for (int ii = 0; ii < CW; ++ii) {
                             float x = kMasked;
-                            if (valid) {
+                            if constexpr (VARLEN) {
+                                const bool ve = valid && (tst == 2 || (tst == 1 && bwd_mod_keep(P.mask_mod, q0 + ql + ii,
+                                                                                              key, P.window, prefix)));
+                                if (ve) {
+                                    x = P.scale * __uint_as_float(sr[ii]);
+                                    vm |= 1u << ii;
+                                }
+                            } else if (valid) {
                                 const uint8_t* ba = bcb + ii * 128 + xo[ii & 7];
                                 float bv;
                                 if constexpr (BIAS_F32) bv = *reinterpret_cast<const float*>(ba);
@@ -594,8 +741,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
                             for (int u = 0; u < 2; ++u) {
                                 const int ii = i + u;
                                 const bool live = exists && ii < nq;
+                                const bool ve = VARLEN ? ((vm >> ii) & 1u) != 0u : valid;
                                 const float p = live ? bwd_weight(__uint_as_float(sr[ii]), ls[ii], inv_k) : 0.f;
-                                const float ds = (live && valid) ? p * (__uint_as_float(dr[ii]) - dl[ii]) : 0.f;
+                                const float ds = (live && ve) ? p * (__uint_as_float(dr[ii]) - dl[ii]) : 0.f;
                                 pv[u] = p;
                                 sv[u] = ds;
                                 dr[ii] = __float_as_uint(ds);
@@ -627,7 +775,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
                 }
                 if (!ok) break;
                 __syncwarp();  // every lane has read its bias values
-                if (lane == 0) mbar_arrive(bias_empty(hh));
+                if (!VARLEN && lane == 0) mbar_arrive(bias_empty(hh));
                 tmem_st_wait();
                 fence_async_shared();  // dS in shared memory is read by the tensor core
                 tc_fence_before();
@@ -637,12 +785,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
                 if (hh == 0 && j > 0) ok = readout(j - 1);
             }
         }
-        if (ok && P.nqt > 0) ok = readout(P.nqt - 1);
+        if (ok && nqt > 0) ok = readout(nqt - 1);
         if (ok) ok = __all_sync(0xffffffffu, wait_bar(fin, 0, abort_flag, P.status));
         if (ok && kCpw * hq < P.D) {  // dK and dV columns [kCpw hq, kCpw hq + kCpw)
             tc_fence_after();
-            uint16_t* dkp = static_cast<uint16_t*>(P.dk) + (unit * P.K + key) * (long long)P.D;
-            uint16_t* dvp = static_cast<uint16_t*>(P.dv) + (unit * P.K + key) * (long long)P.D;
+            // triangle form: row unit * K + key of (B, N, H, K, D); packed form: (krow0 + key, h) of (total_k, H, D)
+            const long long kofs = VARLEN ? ((long long)(krow0 + key) * P.H + h) * P.D : (unit * P.K + key) * (long long)P.D;
+            uint16_t* dkp = static_cast<uint16_t*>(P.dk) + kofs;
+            uint16_t* dvp = static_cast<uint16_t*>(P.dv) + kofs;
 #pragma unroll 1
             for (int pc = 0; pc < kCpw / 16; ++pc) {
                 const int d0 = kCpw * hq + 16 * pc;
@@ -694,15 +844,24 @@ uint32_t bwd_idesc(bool bf16, int M, int N, bool a_mn, bool b_mn) {
 }  // namespace tc
 
 bool tc_bwd_supported(const BwdParams& p) {
-    if (p.varlen || p.dtype == TA_F32 || p.K % 8 != 0) return false;
-    if (p.D == 16 || p.D == 32 || p.D == 64) return true;
-    if (p.D % 16 != 0 || p.D <= 64 || p.D > 128) return false;
-    // D in (64, 128]: two-box tiles, one Q / dO stage; an fp32 bias tile does not fit beside them.
+    if (p.dtype == TA_F32) return false;
+    const bool d_ok = p.D == 16 || p.D == 32 || p.D == 64 || (p.D % 16 == 0 && p.D > 64 && p.D <= 128);
+    if (!d_ok) return false;
     tc::BwdTc t;
     memset(&t, 0, sizeof(t));
-    t.nsub = 2;
+    t.nsub = (p.D + 63) / 64;
     t.qs = 1;
     t.D = p.D;
+    if (p.varlen) {
+        // Packed sequences without a bias; the q-block list of the longest sequence must fit
+        // beside the tiles.
+        if (p.bias) return false;
+        t.qcap = (p.max_q + tc::kBM - 1) / tc::kBM;
+        return tc::bwd_layout(t, t.nsub).total + 1024 <= 232448;
+    }
+    if (p.K % 8 != 0) return false;
+    if (p.D <= 64) return true;
+    // D in (64, 128]: two-box tiles, one Q / dO stage; an fp32 bias tile does not fit beside them.
     t.bias_bytes = (uint32_t)(tc::kBN / (p.bias_f32 ? 32 : 64)) * tc::kBox;
     return tc::bwd_layout(t, t.nsub).total + 1024 <= 232448;
 }
@@ -723,7 +882,17 @@ cudaError_t launch_tc_bwd_main(const BwdParams& p, cudaStream_t stream) {
     P.bias_bytes = (uint32_t)P.bias_boxes * kBox;
     const uint64_t eb = p.bias_f32 ? 4 : 2;
     const int qbox = D > 64 ? kBM / 2 : kBM;  // D > 64: Q / dO rows loaded per query half
-    const bool maps_ok =
+    const bool vl = p.varlen != 0;
+    if (vl && (p.total_q == 0 || p.total_k == 0 || p.num_seqs <= 0)) return cudaSuccess;  // no key rows
+    // Packed sequences: (D, total, H) maps over the (total, H, D) rows.
+    const uint64_t prs = (uint64_t)p.H * D * 2;
+    const bool maps_ok = vl ?
+        encode_map_3d(&P.tm_q, dt, p.q, D, p.total_q, p.H, prs, rs, 64, qbox, 1, sw128) &&
+        encode_map_3d(&P.tm_do, dt, p.d_out, D, p.total_q, p.H, prs, rs, 64, qbox, 1, sw128) &&
+        encode_map_3d(&P.tm_k, dt, p.k, D, p.total_k, p.H, prs, rs, 64, kBN, 1, sw128) &&
+        encode_map_3d(&P.tm_v, dt, p.v, D, p.total_k, p.H, prs, rs, 64, kBN, 1, sw128) &&
+        encode_map_3d(&P.tm_dq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.dq_acc, D, p.total_q, p.H, (uint64_t)p.H * D * 4,
+                      (uint64_t)D * 4, 16, 32, 1, CU_TENSOR_MAP_SWIZZLE_64B) :
         encode_map_3d(&P.tm_q, dt, p.q, D, p.Q, units, rs, rs * p.Q, 64, qbox, 1, sw128) &&
         encode_map_3d(&P.tm_do, dt, p.d_out, D, p.Q, units, rs, rs * p.Q, 64, qbox, 1, sw128) &&
         encode_map_3d(&P.tm_k, dt, p.k, D, p.K, units, rs, rs * p.K, 64, kBN, 1, sw128) &&
@@ -749,23 +918,47 @@ cudaError_t launch_tc_bwd_main(const BwdParams& p, cudaStream_t stream) {
     P.Q = p.Q;
     P.K = p.K;
     P.D = D;
-    P.nkt = (p.K + kBN - 1) / kBN;
-    P.nqt = (p.Q + kBM - 1) / kBM;
+    P.nkt = vl ? (p.max_k + kBN - 1) / kBN : (p.K + kBN - 1) / kBN;
+    P.nqt = vl ? 0 : (p.Q + kBM - 1) / kBM;  // packed form: per key tile, from its q-block list
+    if (vl) {
+        P.bias_bytes = 0;
+        P.dbias_acc = nullptr;
+        P.cu_q = p.cu_q;
+        P.cu_k = p.cu_k;
+        P.total_q = p.total_q;
+        P.total_k = p.total_k;
+        P.max_q = p.max_q;
+        P.max_k = p.max_k;
+        P.kv_num = p.kv_num;
+        P.kv_idx = p.kv_idx;
+        P.full_num = p.full_num;
+        P.full_idx = p.full_idx;
+        P.mask_heads = p.mask_heads;
+        P.MQ = p.MQ;
+        P.MK = p.MK;
+        P.mask_mod = p.mask_mod;
+        P.window = p.window;
+        P.prefix_len = p.prefix_len;
+        P.prefix_all = p.prefix_all;
+        P.qcap = (p.max_q + kBM - 1) / kBM;
+    }
     P.ksteps = D / 16;
     P.nsub = (D + 63) / 64;
     P.idesc_s = bwd_idesc(bf16, 128, 64, false, false);  // 64 queries (one half of the tile)
     P.idesc_g = bwd_idesc(bf16, 128, D, false, true);
     P.idesc_q = bwd_idesc(bf16, 128, D, true, true);
-    const long long grid = (long long)units * P.nkt;
+    const long long grid = vl ? (long long)p.num_seqs * p.H * P.nkt : (long long)units * P.nkt;
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     P.qs = D > 64 ? 1 : 2;  // D > 64: one stage, taken per query half
     if (bwd_layout(P, P.nsub).total + 1024 > 232448) P.qs = 1;  // the 227 KB per-block limit
     const size_t smem = bwd_layout(P, P.nsub).total + 1024;
-    // D > 64 runs with a 16-bit bias only (tc_bwd_supported)
-    auto kern = D > 64 ? (bf16 ? tc_bwd_kernel<true, false, true> : tc_bwd_kernel<false, false, true>)
-                : bf16 ? (p.bias_f32 ? tc_bwd_kernel<true, true, false> : tc_bwd_kernel<true, false, false>)
-                       : (p.bias_f32 ? tc_bwd_kernel<false, true, false> : tc_bwd_kernel<false, false, false>);
+    // D > 64 runs with a 16-bit bias only, packed sequences without a bias (tc_bwd_supported)
+    auto kern = vl ? (D > 64 ? (bf16 ? tc_bwd_kernel<true, false, true, true> : tc_bwd_kernel<false, false, true, true>)
+                             : (bf16 ? tc_bwd_kernel<true, false, false, true> : tc_bwd_kernel<false, false, false, true>))
+                : D > 64 ? (bf16 ? tc_bwd_kernel<true, false, true, false> : tc_bwd_kernel<false, false, true, false>)
+                : bf16 ? (p.bias_f32 ? tc_bwd_kernel<true, true, false, false> : tc_bwd_kernel<true, false, false, false>)
+                       : (p.bias_f32 ? tc_bwd_kernel<false, true, false, false> : tc_bwd_kernel<false, false, false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     kern<<<(unsigned)grid, kBwdThreads, smem, stream>>>(P);

@@ -256,3 +256,64 @@ def test_varlen_backward_prefix_lm_fp32_bias():
     g = torch.Generator().manual_seed(791)
     bias = torch.randn(1, 264, 264, generator=g)
     _check_varlen(c, 792, prefix=[20, 0, 300], bias=bias)
+
+
+# Packed sequences without a bias run on the tensor cores (16-bit, D <= 128): one CTA per
+# (sequence, head, 128-key block) over the q blocks whose lists hold the key block.
+
+def test_varlen_backward_lq_ne_lk_window_no_bias():
+    """Lq != Lk (top-left aligned), a sliding window on every block (no lists), keys past the
+    queries' reach and sequences shorter than one block."""
+    c = synth.make_varlen("vbwd_lqlk_nb", 3, 0, 0, 2, 64, "bf16", seed=783, lengths=[200, 70, 129],
+                          lengths_k=[90, 300, 129], block_lists="none", mask_mod="sliding_window")
+    c.max_seqlen, c.max_seqlen_k = 208, 304
+    _check_varlen(c, 784, window=40)
+
+
+def test_varlen_backward_prefix_lm_no_bias():
+    """Prefix-LM on every block, per-sequence prefixes 20, 0 and beyond the sequence."""
+    c = synth.make_varlen("vbwd_prefix_nb", 3, 0, 0, 2, 32, "f16", seed=793, lengths=[150, 40, 260],
+                          block_lists="none", mask_mod="prefix_lm")
+    c.max_seqlen = c.max_seqlen_k = 264
+    _check_varlen(c, 794, prefix=[20, 0, 300])
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_varlen_backward_many_blocks(D):
+    """Causal lists over several q and key blocks per sequence (full blocks below the diagonal,
+    partial ones on it), three heads, a one-token sequence."""
+    c = synth.make_varlen(f"vbwd_many_{D}", 3, 0, 0, 3, D, "bf16", seed=795 + D, lengths=[700, 300, 1],
+                          block_lists="causal", mask_mod="causal")
+    _check_varlen(c, 796 + D)
+
+
+def test_varlen_backward_full_size_sampled_sequences():
+    """The bf16_varlen packed sequences at full size (8 causal sequences of 256-2048 tokens, H=8,
+    D=128), as the benchmark runs them; dQ, dK and dV of the shortest and the longest sequence
+    against the oracle run on that sequence alone (without a bias a sequence's gradients depend
+    on its own rows only)."""
+    import masked_attention_tri_gb300 as ta
+    c = synth.bf16_varlen()
+    bm = ta.BlockMask.from_kv_blocks(to_gpu(c.kv_num_blocks), to_gpu(c.kv_indices), to_gpu(c.full_kv_num_blocks),
+                                     to_gpu(c.full_kv_indices), BLOCK_SIZE=c.block, mask_mod=c.mask_mod)
+    q, k, v, cu = c.q.cuda(), c.k.cuda(), c.v.cuda(), c.cu_seqlens.cuda()
+    o, lse, _ = ta.varlen_attention(q, k, v, cu, cu, c.max_seqlen, c.max_seqlen, block_mask=bm, scale=c.scale,
+                                    return_aux=True)
+    g = torch.Generator().manual_seed(799)
+    d_out = torch.randn(tuple(c.q.shape), generator=g).to(c.q.dtype)
+    dq, dk, dv, db = ta.varlen_attention_backward(q, k, v, cu, cu, c.max_seqlen, c.max_seqlen, o, lse, d_out.cuda(),
+                                                  block_mask=bm, scale=c.scale)
+    torch.cuda.synchronize()
+    assert ta.get_status() == 0 and db is None
+    dq, dk, dv = dq.cpu(), dk.cpu(), dv.cpu()
+    L = c.lengths.tolist()
+    for s in sorted({L.index(min(L)), L.index(max(L))}):
+        a, b = int(c.cu_seqlens[s]), int(c.cu_seqlens[s + 1])
+        cu1 = torch.tensor([0, b - a], dtype=torch.int32)
+        sl = slice(s, s + 1)
+        ref = obwd.varlen_bwd(c.q[a:b], c.k[a:b], c.v[a:b], cu1, cu1, d_out[a:b], scale=c.scale,
+                              kv_num_blocks=c.kv_num_blocks[sl], kv_indices=c.kv_indices[sl],
+                              full_kv_num_blocks=c.full_kv_num_blocks[sl], full_kv_indices=c.full_kv_indices[sl],
+                              block=c.block, mask_mod=c.mask_mod)
+        for nm, gr, r in zip(("dq", "dk", "dv"), (dq[a:b], dk[a:b], dv[a:b]), ref[:3]):
+            _close(f"bf16_varlen[seq {s}, {b - a} tokens]:{nm}", c.dtype, gr, r)
