@@ -352,7 +352,8 @@ ta_status tri_attn_varlen_fwd_masked(const void* q, const void* k, const void* v
  *   workspace     device scratch of tri_attn_varlen_bwd_workspace_size(...,
  *                 with_bias = dbias != NULL) bytes, 256-byte aligned, owned by
  *                 the caller.
- * Arithmetic: fp16 / bf16 inputs with D a multiple of 16 up to 128 and no bias
+ * Arithmetic: fp16 / bf16 inputs with D a multiple of 16 up to 128 (no bias, or
+ * a bias whose max_seqlen_k rows are 16-byte multiples; at D > 64 a 16-bit one)
  * run on tensor cores (one CTA per sequence, head and 128-key block, over the q
  * blocks whose lists hold that block and those with a row that has no valid
  * key; P and dS rounded to the input type as the MMAs' operands, fp32

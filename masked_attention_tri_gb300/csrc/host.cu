@@ -475,7 +475,7 @@ TA_EXPORT ta_status tri_attn_varlen_bwd(const void* q, const void* k, const void
     p.prefix_all = mask_mod == TA_MASK_PREFIX_LM ? prefix_length : 0;
     p.status = triattn::status_word();
     if (!p.status) return TA_ERR_CUDA;
-    p.tc_main = triattn::tc_bwd_supported(p) ? 1 : 0;  // 16-bit, no bias, D <= 128: tensor cores
+    p.tc_main = triattn::tc_bwd_supported(p) ? 1 : 0;  // 16-bit, D <= 128: tensor cores
     const cudaError_t e = triattn::launch_simt_bwd(p, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TA_OK : TA_ERR_CUDA;
 }

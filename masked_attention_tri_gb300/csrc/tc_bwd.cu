@@ -1,6 +1,6 @@
 // tc_bwd.cu -- the backward's per-key-tile gradients on tcgen05 tensor cores
 // (16-bit q/k/v with D in {16, 32, 64}, or D % 16 == 0 in (64, 128] with a 16-bit bias;
-// K % 8 == 0; triangle form; and packed sequences without a bias, D as above).
+// K % 8 == 0; triangle form; and packed sequences, D as above, with no bias or one as above).
 //
 // The forward (cuEquivariance triangle_attention page) has its context saved for
 // backward.  With P recomputed from the saved lse and delta[q] = sum_k P dP (the
@@ -66,10 +66,11 @@ struct BwdTc {
     int bias_boxes, bias_box_cols;
     int qs;             // stages of (Q, dO, lse, delta): 2 when shared memory allows, else 1
     // Packed sequences (VARLEN): q / k / v / dO (total, H, D) and the fp32 dQ accumulator read
-    // through (D, total, H) maps, lse / delta (H, total_q), the BlockMask lists; no bias.
+    // through (D, total, H) maps, lse / delta (H, total_q), the BlockMask lists, an optional
+    // bias (H, max_q, max_k) at local indices (dBias summed over the sequences).
     const int32_t* cu_q;
     const int32_t* cu_k;
-    int total_q, total_k, max_q, max_k;
+    int num_seqs, total_q, total_k, max_q, max_k;
     const int32_t* kv_num;
     const int32_t* kv_idx;
     const int32_t* full_num;
@@ -151,8 +152,9 @@ __device__ __forceinline__ bool bwd_mod_keep(int mod, int q, int k, int window, 
 // halves take in turn, 32 columns of dQ / dK / dV per compute warp); otherwise D <= 64.
 // VARLEN: packed sequences, one CTA per (sequence, head, 128-key block), visiting the q blocks
 // whose lists hold the key block (full: every key valid; partial: mask_mod decides) and the
-// q blocks with a row that has no valid key (its weights are 1 / Lk at every key); no bias.
-template <bool BF16, bool BIAS_F32, bool WIDE, bool VARLEN>
+// q blocks with a row that has no valid key (its weights are 1 / Lk at every key).
+// HASB: a bias (always in the triangle form; optional with packed sequences).
+template <bool BF16, bool BIAS_F32, bool WIDE, bool VARLEN, bool HASB>
 __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_constant__ BwdTc P) {
     constexpr int kNsub = WIDE ? 2 : 1;   // 64-column boxes per 128-row tile
     constexpr int kCpw = WIDE ? 32 : 16;  // dQ / dK / dV columns per compute warp
@@ -196,9 +198,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
         tz = (int)unit;
         lrow0 = unit * P.Q;
     } else {
-        seq = (int)(blockIdx.x / ((unsigned)P.H * (unsigned)P.nkt));
-        h = (int)((blockIdx.x / (unsigned)P.nkt) % (unsigned)P.H);
-        k0 = (int)(blockIdx.x % (unsigned)P.nkt) * kBN;
+        // key block slowest: under causal lists key block kb visits the q blocks kb.. of its
+        // sequence, so the CTAs with the most work are issued first
+        const unsigned sh = (unsigned)P.num_seqs * (unsigned)P.H;
+        k0 = (int)(blockIdx.x / sh) * kBN;
+        seq = (int)((blockIdx.x % sh) / (unsigned)P.H);
+        h = (int)(blockIdx.x % (unsigned)P.H);
         const int cq0 = P.cu_q[seq], cq1 = P.cu_q[seq + 1], ck0 = P.cu_k[seq], ck1 = P.cu_k[seq + 1];
         Qn = cq1 - cq0;
         Kn = ck1 - ck0;
@@ -214,6 +219,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
         lrow0 = (long long)h * P.total_q + cq0;
         prefix = P.prefix_len ? P.prefix_len[seq] : P.prefix_all;
     }
+
+    // The bias: triangle form (B, 1, H, Q, K), always present; packed form (H, max_q, max_k),
+    // optional.  Rows of dBias are bst floats apart.
+    constexpr bool hasb = HASB;
+    const int bz = VARLEN ? h : b * P.H + h;
+    const long long bst = VARLEN ? P.max_k : P.K;
 
     if (!VARLEN && P.kv_len) {
         // A key tile wholly past a kv_length of at least 1: its keys have weight 0 in every
@@ -356,7 +367,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
             // This tile's Q / dO, bias half 0 (as soon as the compute warps have read half 0 of
             // tile j - 1), the rows' lse / delta, then bias half 1.
             auto bias_load = [&](int hh) -> bool {
-                if constexpr (VARLEN) return true;  // no bias
+                if (!hasb) return true;
                 if (j > 0 &&
                     !__all_sync(0xffffffffu, wait_bar(bias_empty(hh), (uint32_t)(j - 1) & 1u, abort_flag, P.status)))
                     return false;
@@ -364,7 +375,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
                     mbar_expect_tx(bias_full(hh), P.bias_bytes / 2u);
                     for (int bx = 0; bx < P.bias_boxes; ++bx)
                         tma_load_3d(bias_half(hh) + (uint32_t)bx * 8192u, &P.tm_bias, k0 + bx * P.bias_box_cols,
-                                    q0 + 64 * hh, b * P.H + h, bias_full(hh));
+                                    q0 + 64 * hh, bz, bias_full(hh));
                 }
                 return true;
             };
@@ -564,8 +575,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
         uint32_t xo[8];
 #pragma unroll
         for (int r8 = 0; r8 < 8; ++r8) xo[r8] = ((((bcol_b >> 4) ^ (uint32_t)r8)) << 4) + (bcol_b & 15u);
-        float* dbias_row = !VARLEN && P.dbias_acc
-                               ? P.dbias_acc + ((long long)b * P.H + h) * P.Q * (long long)P.K + key : nullptr;
+        float* dbias_row = P.dbias_acc ? P.dbias_acc + (VARLEN ? (long long)h * P.max_q * P.max_k
+                                                               : ((long long)b * P.H + h) * P.Q * (long long)P.K) + key
+                                       : nullptr;
         // dQ staging of this warp: 32 rows x 16 fp32 (64-byte rows, 64B-swizzled)
         const uint32_t dq_stage = base + L.dqst + (uint32_t)warp * 2048u;
         const uint32_t qsw = (uint32_t)((lane >> 1) & 3);
@@ -642,7 +654,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
             ok = __all_sync(0xffffffffu, wait_bar(lse_full(st), (uint32_t)(j / P.qs) & 1u, abort_flag, P.status));
             if (!ok) break;
             for (int hh = 0; hh < 2 && ok; ++hh) {
-                if (!VARLEN) {
+                if (hasb) {
                     ok = __all_sync(0xffffffffu, wait_bar(bias_full(hh), ph, abort_flag, P.status));
                     if (!ok) break;
                 }
@@ -679,11 +691,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
                         // has a valid key, so its lse is a plain log-sum-exp and P = 2^(x log2e - lse log2e).
                         const float2 sl2 = make_float2(P.scale * kLog2e, P.scale * kLog2e);
                         const float2 l2e2 = make_float2(kLog2e, kLog2e);
-                        float* dbp = dbias_row ? dbias_row + (long long)(q0 + ql) * P.K : nullptr;
+                        float* dbp = dbias_row ? dbias_row + (long long)(q0 + ql) * bst : nullptr;
 #pragma unroll
                         for (int i = 0; i < CW; i += 2) {
                             float2 bv;
-                            if constexpr (VARLEN) {
+                            if (!hasb) {
                                 bv = make_float2(0.f, 0.f);
                             } else if constexpr (BIAS_F32) {
                                 bv = make_float2(*reinterpret_cast<const float*>(bcb + i * 128 + xo[i & 7]),
@@ -705,8 +717,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
                             pp[i / 2] = pack2<BF16>(pr.x, pr.y);
                             dd[i / 2] = pack2<BF16>(ds.x, ds.y);
                             if (dbp) {
-                                red_add_global(dbp + (long long)i * P.K, ds.x);
-                                red_add_global(dbp + (long long)(i + 1) * P.K, ds.y);
+                                red_add_global(dbp + (long long)i * bst, ds.x);
+                                red_add_global(dbp + (long long)(i + 1) * bst, ds.y);
                             }
                         }
                     } else {
@@ -721,7 +733,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
                                 const bool ve = valid && (tst == 2 || (tst == 1 && bwd_mod_keep(P.mask_mod, q0 + ql + ii,
                                                                                               key, P.window, prefix)));
                                 if (ve) {
-                                    x = P.scale * __uint_as_float(sr[ii]);
+                                    float bv = 0.f;
+                                    if (hasb) {
+                                        const uint8_t* ba = bcb + ii * 128 + xo[ii & 7];
+                                        if constexpr (BIAS_F32) bv = *reinterpret_cast<const float*>(ba);
+                                        else bv = unpack2<BF16>((uint32_t)*reinterpret_cast<const unsigned short*>(ba)).x;
+                                    }
+                                    x = fmaf(P.scale, __uint_as_float(sr[ii]), bv);
                                     vm |= 1u << ii;
                                 }
                             } else if (valid) {
@@ -755,7 +773,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
 #pragma unroll
                             for (int ii = 0; ii < CW; ++ii)
                                 if (__uint_as_float(dr[ii]) != 0.f)
-                                    red_add_global(dbias_row + (long long)(q0 + ql + ii) * P.K, __uint_as_float(dr[ii]));
+                                    red_add_global(dbias_row + (long long)(q0 + ql + ii) * bst, __uint_as_float(dr[ii]));
                         }
                     }
                     tmem_st_x8(tSh + lane_off + col, pp);
@@ -775,7 +793,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
                 }
                 if (!ok) break;
                 __syncwarp();  // every lane has read its bias values
-                if (!VARLEN && lane == 0) mbar_arrive(bias_empty(hh));
+                if (hasb && lane == 0) mbar_arrive(bias_empty(hh));
                 tmem_st_wait();
                 fence_async_shared();  // dS in shared memory is read by the tensor core
                 tc_fence_before();
@@ -853,10 +871,13 @@ bool tc_bwd_supported(const BwdParams& p) {
     t.qs = 1;
     t.D = p.D;
     if (p.varlen) {
-        // Packed sequences without a bias; the q-block list of the longest sequence must fit
-        // beside the tiles.
-        if (p.bias) return false;
+        // Packed sequences; the q-block list of the longest sequence must fit beside the tiles.
+        // A bias (H, max_q, max_k) is read through a tensor map: its rows must be 16-byte multiples.
         t.qcap = (p.max_q + tc::kBM - 1) / tc::kBM;
+        if (p.bias) {
+            if (p.max_q <= 0 || p.max_k <= 0 || ((long long)p.max_k * (p.bias_f32 ? 4 : 2)) % 16 != 0) return false;
+            t.bias_bytes = (uint32_t)(tc::kBN / (p.bias_f32 ? 32 : 64)) * tc::kBox;
+        }
         return tc::bwd_layout(t, t.nsub).total + 1024 <= 232448;
     }
     if (p.K % 8 != 0) return false;
@@ -892,7 +913,10 @@ cudaError_t launch_tc_bwd_main(const BwdParams& p, cudaStream_t stream) {
         encode_map_3d(&P.tm_k, dt, p.k, D, p.total_k, p.H, prs, rs, 64, kBN, 1, sw128) &&
         encode_map_3d(&P.tm_v, dt, p.v, D, p.total_k, p.H, prs, rs, 64, kBN, 1, sw128) &&
         encode_map_3d(&P.tm_dq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.dq_acc, D, p.total_q, p.H, (uint64_t)p.H * D * 4,
-                      (uint64_t)D * 4, 16, 32, 1, CU_TENSOR_MAP_SWIZZLE_64B) :
+                      (uint64_t)D * 4, 16, 32, 1, CU_TENSOR_MAP_SWIZZLE_64B) &&
+        (!p.bias || encode_map_3d(&P.tm_bias, p.bias_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : dt, p.bias, p.max_k,
+                                  p.max_q, p.H, p.max_k * eb, p.max_k * eb * p.max_q, P.bias_box_cols, kBM / 2, 1,
+                                  sw128)) :
         encode_map_3d(&P.tm_q, dt, p.q, D, p.Q, units, rs, rs * p.Q, 64, qbox, 1, sw128) &&
         encode_map_3d(&P.tm_do, dt, p.d_out, D, p.Q, units, rs, rs * p.Q, 64, qbox, 1, sw128) &&
         encode_map_3d(&P.tm_k, dt, p.k, D, p.K, units, rs, rs * p.K, 64, kBN, 1, sw128) &&
@@ -921,10 +945,11 @@ cudaError_t launch_tc_bwd_main(const BwdParams& p, cudaStream_t stream) {
     P.nkt = vl ? (p.max_k + kBN - 1) / kBN : (p.K + kBN - 1) / kBN;
     P.nqt = vl ? 0 : (p.Q + kBM - 1) / kBM;  // packed form: per key tile, from its q-block list
     if (vl) {
-        P.bias_bytes = 0;
-        P.dbias_acc = nullptr;
+        P.bias_bytes = p.bias ? (uint32_t)P.bias_boxes * kBox : 0;  // 0: no bias
+        P.dbias_acc = p.bias ? p.dbias_acc : nullptr;
         P.cu_q = p.cu_q;
         P.cu_k = p.cu_k;
+        P.num_seqs = p.num_seqs;
         P.total_q = p.total_q;
         P.total_k = p.total_k;
         P.max_q = p.max_q;
@@ -953,12 +978,20 @@ cudaError_t launch_tc_bwd_main(const BwdParams& p, cudaStream_t stream) {
     P.qs = D > 64 ? 1 : 2;  // D > 64: one stage, taken per query half
     if (bwd_layout(P, P.nsub).total + 1024 > 232448) P.qs = 1;  // the 227 KB per-block limit
     const size_t smem = bwd_layout(P, P.nsub).total + 1024;
-    // D > 64 runs with a 16-bit bias only, packed sequences without a bias (tc_bwd_supported)
-    auto kern = vl ? (D > 64 ? (bf16 ? tc_bwd_kernel<true, false, true, true> : tc_bwd_kernel<false, false, true, true>)
-                             : (bf16 ? tc_bwd_kernel<true, false, false, true> : tc_bwd_kernel<false, false, false, true>))
-                : D > 64 ? (bf16 ? tc_bwd_kernel<true, false, true, false> : tc_bwd_kernel<false, false, true, false>)
-                : bf16 ? (p.bias_f32 ? tc_bwd_kernel<true, true, false, false> : tc_bwd_kernel<true, false, false, false>)
-                       : (p.bias_f32 ? tc_bwd_kernel<false, true, false, false> : tc_bwd_kernel<false, false, false, false>);
+    // D > 64 runs with no bias or a 16-bit one (tc_bwd_supported); the triangle form always has one
+    const bool fb = p.bias_f32 != 0;
+    decltype(&tc_bwd_kernel<true, false, false, false, true>) kern;
+    if (!vl)
+        kern = D > 64 ? (bf16 ? tc_bwd_kernel<true, false, true, false, true> : tc_bwd_kernel<false, false, true, false, true>)
+             : bf16   ? (fb ? tc_bwd_kernel<true, true, false, false, true> : tc_bwd_kernel<true, false, false, false, true>)
+                      : (fb ? tc_bwd_kernel<false, true, false, false, true> : tc_bwd_kernel<false, false, false, false, true>);
+    else if (!p.bias)
+        kern = D > 64 ? (bf16 ? tc_bwd_kernel<true, false, true, true, false> : tc_bwd_kernel<false, false, true, true, false>)
+                      : (bf16 ? tc_bwd_kernel<true, false, false, true, false> : tc_bwd_kernel<false, false, false, true, false>);
+    else
+        kern = D > 64 ? (bf16 ? tc_bwd_kernel<true, false, true, true, true> : tc_bwd_kernel<false, false, true, true, true>)
+             : bf16   ? (fb ? tc_bwd_kernel<true, true, false, true, true> : tc_bwd_kernel<true, false, false, true, true>)
+                      : (fb ? tc_bwd_kernel<false, true, false, true, true> : tc_bwd_kernel<false, false, false, true, true>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     kern<<<(unsigned)grid, kBwdThreads, smem, stream>>>(P);

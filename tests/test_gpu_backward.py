@@ -258,7 +258,7 @@ def test_varlen_backward_prefix_lm_fp32_bias():
     _check_varlen(c, 792, prefix=[20, 0, 300], bias=bias)
 
 
-# Packed sequences without a bias run on the tensor cores (16-bit, D <= 128): one CTA per
+# Packed sequences run on the tensor cores (16-bit, D <= 128; a bias too, 16-bit at D > 64): one CTA per
 # (sequence, head, 128-key block) over the q blocks whose lists hold the key block.
 
 def test_varlen_backward_lq_ne_lk_window_no_bias():
@@ -317,3 +317,14 @@ def test_varlen_backward_full_size_sampled_sequences():
                               block=c.block, mask_mod=c.mask_mod)
         for nm, gr, r in zip(("dq", "dk", "dv"), (dq[a:b], dk[a:b], dv[a:b]), ref[:3]):
             _close(f"bf16_varlen[seq {s}, {b - a} tokens]:{nm}", c.dtype, gr, r)
+
+
+def test_varlen_backward_wide_bias_and_dbias():
+    """D = 128 with a bf16 post-scale bias (H, max_seqlen_q, max_seqlen_k) and its gradient summed
+    over the sequences, causal lists over several blocks."""
+    c = synth.make_varlen("vbwd_wide_bias", 2, 0, 0, 2, 128, "bf16", seed=801, lengths=[300, 129],
+                          block_lists="causal", mask_mod="causal")
+    c.max_seqlen = c.max_seqlen_k = 304
+    g = torch.Generator().manual_seed(802)
+    bias = torch.randn(2, 304, 304, generator=g).to(torch.bfloat16)
+    _check_varlen(c, 803, bias=bias)
