@@ -328,3 +328,15 @@ def test_varlen_backward_wide_bias_and_dbias():
     g = torch.Generator().manual_seed(802)
     bias = torch.randn(2, 304, 304, generator=g).to(torch.bfloat16)
     _check_varlen(c, 803, bias=bias)
+
+
+def test_varlen_backward_per_head_lists():
+    """Per-head lists (mask_heads = H): head 0 causal lists, head 1 only the diagonal blocks
+    (partial) and, for sequence 0, no block at all for q block 1 (its rows have no valid key and
+    weigh every key 1 / Lk); every key block derives its own q-block list per head."""
+    c = synth.make_varlen("vbwd_heads", 2, 0, 0, 2, 64, "bf16", seed=805, lengths=[384, 200])
+    kn, ki, fn, fi = synth.causal_block_lists([384, 200], mask_heads=2)
+    fn[:, 1] = 0
+    kn[0, 1, 1] = 0
+    c.kv_num_blocks, c.kv_indices, c.full_kv_num_blocks, c.full_kv_indices = kn, ki, fn, fi
+    _check_varlen(c, 806)
