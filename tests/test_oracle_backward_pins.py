@@ -205,3 +205,47 @@ def test_varlen_bwd_matches_torch_autograd(mod, lists):
     loss.backward()
     for a, t in zip(got, (qd, kd, vd, bd)):
         np.testing.assert_allclose(a, t.grad.numpy(), atol=1e-10, rtol=1e-9)
+
+
+def test_varlen_bwd_per_head_lists_match_torch_autograd():
+    """Per-head lists (mask_heads = H = 2, the lists' second axis): head 0 and head 1 list different
+    blocks (head 1 leaves one q block with no block at all, so its rows have no valid key), causal
+    mask_mod; fp64 autograd with each head's element mask from `_element_mask`."""
+    g = torch.Generator().manual_seed(61)
+    lq, H, D, block = [9, 7], 2, 4, 4
+    cu = torch.tensor([0, 9, 16])
+    q, k, v = (torch.randn(16, H, D, generator=g) for _ in range(3))
+    do = torch.randn(16, H, D, generator=g, dtype=torch.float64)
+    MQ = MK = 3
+    # [sequence][head]: q block -> partial / full kv blocks
+    P = [[{0: [0], 1: [1], 2: [2]}, {0: [0], 1: [], 2: [0, 2]}], [{0: [0], 1: [1]}, {0: [0], 1: [0, 1]}]]
+    F = [[{1: [0], 2: [0, 1]}, {2: [1]}], [{1: [0]}, {}]]
+    kn = torch.zeros(2, H, MQ, dtype=torch.int32); ki = torch.full((2, H, MQ, MK), 7, dtype=torch.int32)
+    fn = torch.zeros(2, H, MQ, dtype=torch.int32); fi = torch.full((2, H, MQ, MK), 7, dtype=torch.int32)
+    for s_ in range(2):
+        for h in range(H):
+            for qb, kbs in P[s_][h].items():
+                kn[s_, h, qb] = len(kbs)
+                if kbs:
+                    ki[s_, h, qb, :len(kbs)] = torch.tensor(kbs, dtype=torch.int32)
+            for qb, kbs in F[s_][h].items():
+                fn[s_, h, qb] = len(kbs)
+                fi[s_, h, qb, :len(kbs)] = torch.tensor(kbs, dtype=torch.int32)
+    scale = 0.375
+    got = varlen_bwd(q, k, v, cu, cu, do, scale=scale, kv_num_blocks=kn, kv_indices=ki, full_kv_num_blocks=fn,
+                     full_kv_indices=fi, block=block, mask_mod="causal")
+    qd, kd, vd = (t.double().clone().requires_grad_(True) for t in (q, k, v))
+    loss = 0.0
+    for s_ in range(2):
+        c0, L = int(cu[s_]), lq[s_]
+        for h in range(H):
+            m = _element_mask(L, L, block, {qb: set(x) for qb, x in P[s_][h].items()},
+                              {qb: set(x) for qb, x in F[s_][h].items()}, "causal", 0, 0)
+            x = scale * (qd[c0:c0 + L, h] @ kd[c0:c0 + L, h].T)
+            x = torch.where(m, x, torch.full_like(x, -1e9))
+            o = torch.softmax(x, dim=-1) @ vd[c0:c0 + L, h]
+            loss = loss + (o * do[c0:c0 + L, h]).sum()
+    loss.backward()
+    assert got[3] is None
+    for a, t in zip(got[:3], (qd, kd, vd)):
+        np.testing.assert_allclose(a, t.grad.numpy(), atol=1e-10, rtol=1e-9)
