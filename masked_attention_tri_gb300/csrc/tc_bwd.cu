@@ -64,6 +64,7 @@ struct BwdTc {
     uint32_t idesc_q;   // M 128, N D: A and B MN-major in shared memory
     uint32_t bias_bytes;
     int bias_boxes, bias_box_cols;
+    int bias_alias;     // 1: the two bias halves share one slot (an fp32 bias with D > 64)
     int qs;             // stages of (Q, dO, lse, delta): 2 when shared memory allows, else 1
     // Packed sequences (VARLEN): q / k / v / dO (total, H, D) and the fp32 dQ accumulator read
     // through (D, total, H) maps, lse / delta (H, total_q), the BlockMask lists, an optional
@@ -98,7 +99,7 @@ __host__ __device__ inline BwdLayout bwd_layout(const BwdTc& P, int nsub) {
     L.q = L.v + tile;
     L.ds = L.q + (uint32_t)P.qs * 2 * tile;  // dS as [key][query]: two 64-query boxes
     L.bias = L.ds + 2 * kBox;
-    L.dqst = L.bias + P.bias_bytes;          // dQ staging: 16 compute warps x 32 rows x 16 fp32
+    L.dqst = L.bias + (P.bias_alias ? P.bias_bytes / 2u : P.bias_bytes);  // dQ staging: 16 warps x 32 rows x 16 fp32
     L.lse = L.dqst + 16u * 2048u;
     L.qlist = L.lse + (uint32_t)P.qs * 1024u;  // packed form: the q blocks the key tile visits
     L.bars = L.qlist + (((uint32_t)P.qcap * 4u + 15u) & ~15u);
@@ -180,7 +181,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
     auto q_smem = [&](int st) { return base + L.q + (uint32_t)st * 2u * tileb; };
     auto do_smem = [&](int st) { return base + L.q + (uint32_t)st * 2u * tileb + tileb; };
     // bias rows [64 hh, 64 hh + 64) of the tile: boxes of bias_box_cols keys x 64 rows (8 KB each)
-    auto bias_half = [&](int hh) { return base + L.bias + (uint32_t)hh * (P.bias_bytes / 2u); };
+    // An fp32 bias with D > 64: both halves in one slot, used in the order (j, 0), (j, 1), (j + 1, 0).
+    constexpr bool kAlias = WIDE && BIAS_F32;
+    auto bias_half = [&](int hh) { return base + L.bias + (kAlias ? 0u : (uint32_t)hh * (P.bias_bytes / 2u)); };
 
     // The key tile's unit.  Triangle form: slab unit = (b*N + n)*H + h, Qn x Kn = Q x K.
     // Packed form: sequence seq and head h, Qn x Kn = its lengths.  Rows go through the maps
@@ -365,12 +368,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
         for (int j = 0; j < nqt && ok; ++j) {
             const int q0 = tile_q0(j), st = j % P.qs, use = j / P.qs;
             // This tile's Q / dO, bias half 0 (as soon as the compute warps have read half 0 of
-            // tile j - 1), the rows' lse / delta, then bias half 1.
+            // tile j - 1), the rows' lse / delta, then bias half 1.  One shared slot (kAlias):
+            // half 0 once half 1 of tile j - 1 is read, half 1 once half 0 of this tile is.
             auto bias_load = [&](int hh) -> bool {
                 if (!hasb) return true;
-                if (j > 0 &&
-                    !__all_sync(0xffffffffu, wait_bar(bias_empty(hh), (uint32_t)(j - 1) & 1u, abort_flag, P.status)))
+                if (kAlias) {
+                    if (hh == 0 && j > 0 &&
+                        !__all_sync(0xffffffffu, wait_bar(bias_empty(1), (uint32_t)(j - 1) & 1u, abort_flag, P.status)))
+                        return false;
+                    if (hh == 1 &&
+                        !__all_sync(0xffffffffu, wait_bar(bias_empty(0), (uint32_t)j & 1u, abort_flag, P.status)))
+                        return false;
+                } else if (j > 0 && !__all_sync(0xffffffffu, wait_bar(bias_empty(hh), (uint32_t)(j - 1) & 1u,
+                                                                      abort_flag, P.status))) {
                     return false;
+                }
                 if (lane == 0) {
                     mbar_expect_tx(bias_full(hh), P.bias_bytes / 2u);
                     for (int bx = 0; bx < P.bias_boxes; ++bx)
@@ -877,13 +889,16 @@ bool tc_bwd_supported(const BwdParams& p) {
         if (p.bias) {
             if (p.max_q <= 0 || p.max_k <= 0 || ((long long)p.max_k * (p.bias_f32 ? 4 : 2)) % 16 != 0) return false;
             t.bias_bytes = (uint32_t)(tc::kBN / (p.bias_f32 ? 32 : 64)) * tc::kBox;
+            t.bias_alias = p.D > 64 && p.bias_f32 ? 1 : 0;
         }
         return tc::bwd_layout(t, t.nsub).total + 1024 <= 232448;
     }
     if (p.K % 8 != 0) return false;
     if (p.D <= 64) return true;
-    // D in (64, 128]: two-box tiles, one Q / dO stage; an fp32 bias tile does not fit beside them.
+    // D in (64, 128]: two-box tiles, one Q / dO stage; an fp32 bias tile fits beside them as
+    // one half at a time.
     t.bias_bytes = (uint32_t)(tc::kBN / (p.bias_f32 ? 32 : 64)) * tc::kBox;
+    t.bias_alias = p.bias_f32 ? 1 : 0;
     return tc::bwd_layout(t, t.nsub).total + 1024 <= 232448;
 }
 
@@ -901,6 +916,7 @@ cudaError_t launch_tc_bwd_main(const BwdParams& p, cudaStream_t stream) {
     P.bias_box_cols = p.bias_f32 ? 32 : 64;
     P.bias_boxes = kBN / P.bias_box_cols;
     P.bias_bytes = (uint32_t)P.bias_boxes * kBox;
+    P.bias_alias = D > 64 && p.bias_f32 ? 1 : 0;
     const uint64_t eb = p.bias_f32 ? 4 : 2;
     const int qbox = D > 64 ? kBM / 2 : kBM;  // D > 64: Q / dO rows loaded per query half
     const bool vl = p.varlen != 0;
@@ -978,18 +994,20 @@ cudaError_t launch_tc_bwd_main(const BwdParams& p, cudaStream_t stream) {
     P.qs = D > 64 ? 1 : 2;  // D > 64: one stage, taken per query half
     if (bwd_layout(P, P.nsub).total + 1024 > 232448) P.qs = 1;  // the 227 KB per-block limit
     const size_t smem = bwd_layout(P, P.nsub).total + 1024;
-    // D > 64 runs with no bias or a 16-bit one (tc_bwd_supported); the triangle form always has one
+    // <BF16, BIAS_F32, WIDE, VARLEN, HASB>; the triangle form always has a bias
     const bool fb = p.bias_f32 != 0;
     decltype(&tc_bwd_kernel<true, false, false, false, true>) kern;
     if (!vl)
-        kern = D > 64 ? (bf16 ? tc_bwd_kernel<true, false, true, false, true> : tc_bwd_kernel<false, false, true, false, true>)
+        kern = D > 64 ? (bf16 ? (fb ? tc_bwd_kernel<true, true, true, false, true> : tc_bwd_kernel<true, false, true, false, true>)
+                              : (fb ? tc_bwd_kernel<false, true, true, false, true> : tc_bwd_kernel<false, false, true, false, true>))
              : bf16   ? (fb ? tc_bwd_kernel<true, true, false, false, true> : tc_bwd_kernel<true, false, false, false, true>)
                       : (fb ? tc_bwd_kernel<false, true, false, false, true> : tc_bwd_kernel<false, false, false, false, true>);
     else if (!p.bias)
         kern = D > 64 ? (bf16 ? tc_bwd_kernel<true, false, true, true, false> : tc_bwd_kernel<false, false, true, true, false>)
                       : (bf16 ? tc_bwd_kernel<true, false, false, true, false> : tc_bwd_kernel<false, false, false, true, false>);
     else
-        kern = D > 64 ? (bf16 ? tc_bwd_kernel<true, false, true, true, true> : tc_bwd_kernel<false, false, true, true, true>)
+        kern = D > 64 ? (bf16 ? (fb ? tc_bwd_kernel<true, true, true, true, true> : tc_bwd_kernel<true, false, true, true, true>)
+                              : (fb ? tc_bwd_kernel<false, true, true, true, true> : tc_bwd_kernel<false, false, true, true, true>))
              : bf16   ? (fb ? tc_bwd_kernel<true, true, false, true, true> : tc_bwd_kernel<true, false, false, true, true>)
                       : (fb ? tc_bwd_kernel<false, true, false, true, true> : tc_bwd_kernel<false, false, false, true, true>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -106,17 +106,19 @@ def test_backward_without_dbias_and_large_logits(with_out):
     _check(c, 741, need_dbias=False, with_out=with_out)
 
 
-@pytest.mark.parametrize("D", [64, 128])
-def test_backward_several_tiles(D):
+@pytest.mark.parametrize("D,bias_dtype", [(64, "bf16"), (128, "bf16"), (128, "f32")])
+def test_backward_several_tiles(D, bias_dtype):
     """Several 128-key and 128-row tiles per slab (ragged), tensor-core gradients (D = 128: the
-    tiles' two column boxes, one S^T / dP^T buffer for both query halves), both delta forms."""
-    c = synth.make_triangle(f"bwd_tiles_{D}", 1, 2, 2, 300, 264, D, "bf16", "bf16", seed=745 + D, mask="kvlen",
-                            kv_range=(100, 264))
+    tiles' two column boxes, one S^T / dP^T buffer for both query halves; with an fp32 bias its
+    two halves take turns in one shared-memory slot), both delta forms."""
+    c = synth.make_triangle(f"bwd_tiles_{D}_{bias_dtype}", 1, 2, 2, 300, 264, D, "bf16", bias_dtype, seed=745 + D,
+                            mask="kvlen", kv_range=(100, 264))
     _check(c, 746 + D)
     _check(c, 747 + D, with_out=True)
 
 
-@pytest.mark.parametrize("dtype,D,bias_dtype", [("bf16", 32, "f32"), ("f16", 64, "f32"), ("bf16", 128, "bf16")])
+@pytest.mark.parametrize("dtype,D,bias_dtype", [("bf16", 32, "f32"), ("f16", 64, "f32"), ("bf16", 128, "bf16"),
+                                                ("f16", 96, "f32")])
 def test_backward_padded_key_tiles(dtype, D, bias_dtype):
     """kv_lengths that leave whole 128-key tiles past the valid prefix (their dK / dV are zero and
     they add nothing to dQ or dBias), next to 0 (every key weighted 1 / K), 1, tile edges, K and
@@ -319,14 +321,16 @@ def test_varlen_backward_full_size_sampled_sequences():
             _close(f"bf16_varlen[seq {s}, {b - a} tokens]:{nm}", c.dtype, gr, r)
 
 
-def test_varlen_backward_wide_bias_and_dbias():
-    """D = 128 with a bf16 post-scale bias (H, max_seqlen_q, max_seqlen_k) and its gradient summed
-    over the sequences, causal lists over several blocks."""
+@pytest.mark.parametrize("bias_dtype", [torch.bfloat16, torch.float32])
+def test_varlen_backward_wide_bias_and_dbias(bias_dtype):
+    """D = 128 with a post-scale bias (H, max_seqlen_q, max_seqlen_k), bf16 or fp32 (its halves
+    sharing one slot), and its gradient summed over the sequences, causal lists over several
+    blocks."""
     c = synth.make_varlen("vbwd_wide_bias", 2, 0, 0, 2, 128, "bf16", seed=801, lengths=[300, 129],
                           block_lists="causal", mask_mod="causal")
     c.max_seqlen = c.max_seqlen_k = 304
     g = torch.Generator().manual_seed(802)
-    bias = torch.randn(2, 304, 304, generator=g).to(torch.bfloat16)
+    bias = torch.randn(2, 304, 304, generator=g).to(bias_dtype)
     _check_varlen(c, 803, bias=bias)
 
 
