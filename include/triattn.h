@@ -160,8 +160,9 @@ ta_status tri_attn_fwd_strided(const void* q, const void* k, const void* v, ta_d
  *               flight must not share a workspace.
  * Arithmetic (three kernels: the per-row sum of P dP, the per-key-tile
  * gradients with dQ and dBias added atomically in fp32, the conversion to the
- * output dtypes): fp16 / bf16 inputs with D in {16, 32, 64} and K % 8 == 0 take
- * the per-key-tile gradients on tcgen05 tensor cores (P^T and dS^T in 16 bits,
+ * output dtypes): fp16 / bf16 inputs with D in {16, 32, 64}, or a multiple of 16
+ * up to 128, and K % 8 == 0 take the per-key-tile gradients on tcgen05 tensor
+ * cores (P^T and dS^T in 16 bits,
  * fp32 accumulation); every other case runs exact fp32 on CUDA cores.  The
  * summation order of dQ and dBias varies from run to run within fp32 rounding.
  * Supported: as tri_attn_fwd (D <= 256).  Errors: NULL required pointer,
@@ -353,8 +354,7 @@ ta_status tri_attn_varlen_fwd_masked(const void* q, const void* k, const void* v
  *                 with_bias = dbias != NULL) bytes, 256-byte aligned, owned by
  *                 the caller.
  * Arithmetic: fp16 / bf16 inputs with D a multiple of 16 up to 128 (no bias, or
- * a bias whose max_seqlen_k rows are 16-byte multiples; at D > 64 a 16-bit one)
- * run on tensor cores (one CTA per sequence, head and 128-key block, over the q
+ * a bias whose max_seqlen_k rows are 16-byte multiples) run on tensor cores (one CTA per sequence, head and 128-key block, over the q
  * blocks whose lists hold that block and those with a row that has no valid
  * key; P and dS rounded to the input type as the MMAs' operands, fp32
  * accumulation); every other case exact fp32 on CUDA cores (one CTA per

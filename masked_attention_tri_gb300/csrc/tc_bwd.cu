@@ -1,5 +1,5 @@
 // tc_bwd.cu -- the backward's per-key-tile gradients on tcgen05 tensor cores
-// (16-bit q/k/v with D in {16, 32, 64}, or D % 16 == 0 in (64, 128] with a 16-bit bias;
+// (16-bit q/k/v with D in {16, 32, 64}, or D % 16 == 0 in (64, 128];
 // K % 8 == 0; triangle form; and packed sequences, D as above, with no bias or one as above).
 //
 // The forward (cuEquivariance triangle_attention page) has its context saved for

@@ -72,7 +72,7 @@ def _check(case, seed, **kw):
 
 # dtypes x bias dtypes x masks; ragged Q and K (not multiples of the 32-row tiles), N > 1 for
 # the sum of dBias over n, kv_lengths extremes (0: every key masked, K, beyond K).  16-bit
-# inputs with D in {16, 32, 64}, or a multiple of 16 in (64, 128] with a 16-bit bias, take the
+# inputs with D in {16, 32, 64}, or a multiple of 16 in (64, 128], take the
 # tensor-core gradients, the others the CUDA-core kernel; with_out: sum_k P dP from the
 # forward's O instead of the exact pass.
 @pytest.mark.parametrize("with_out", [False, True])
