@@ -698,7 +698,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1) tc_bwd_kernel(const __grid_con
                     const uint8_t* bcb = gbase + (bias_half(hh) - base) + bbox_off + (uint32_t)(ql - 64 * hh) * 128u;
                     const int nq = Qn - (q0 + ql);  // queries of the chunk that exist
                     uint32_t pp[CW / 2], dd[CW / 2];
-                    if (__all_sync(0xffffffffu, valid) && nq >= CW && tst == 2) {
+                    // Packed form, partial block: the chunk is wholly kept when mask_mod keeps every
+                    // (query, key) of it (warp-uniform: this warp's 32 keys x the chunk's 16 queries).
+                    bool whole = tst == 2;
+                    if (VARLEN && tst == 1) {
+                        const int kmin = k0 + 32 * wq, kmax = kmin + 31, qmin = q0 + ql, qmax = qmin + CW - 1;
+                        switch (P.mask_mod) {
+                        case TA_MASK_NONE: whole = true; break;
+                        case TA_MASK_CAUSAL: whole = kmax <= qmin; break;
+                        case TA_MASK_SLIDING_WINDOW: whole = kmax <= qmin && kmin > qmax - P.window; break;
+                        case TA_MASK_PREFIX_LM: whole = kmax <= qmin || kmax < prefix; break;
+                        default: whole = false;
+                        }
+                    }
+                    if (__all_sync(0xffffffffu, valid) && nq >= CW && whole) {
                         // Every key of the warp valid and every query of the chunk present: each row
                         // has a valid key, so its lse is a plain log-sum-exp and P = 2^(x log2e - lse log2e).
                         const float2 sl2 = make_float2(P.scale * kLog2e, P.scale * kLog2e);
